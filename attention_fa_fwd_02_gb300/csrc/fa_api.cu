@@ -1,0 +1,185 @@
+// fa_api.cu -- the extern "C" boundary of libfa.so (declared in include/fa.h):
+// argument validation, the library's stream-ordered scratch pool, TMA descriptor
+// encoding and the device status word. Kernels live in fa_fwd.cu / fa_bwd.cu.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <cudaTypedefs.h>
+#include "fa_common.cuh"
+
+namespace fa {
+namespace host {
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[MAX_DEVICES] = {};
+int g_sms[MAX_DEVICES] = {};
+}  // namespace
+
+bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
+                     uint64_t inner, uint64_t rows, uint64_t outer, uint64_t row_stride,
+                     uint32_t box_inner, uint32_t box_rows) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return false;
+  cuuint64_t dims[3] = {inner, rows, outer};
+  cuuint64_t strides[2] = {row_stride * esize, row_stride * esize * rows};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static cudaError_t pool_for_current_device(cudaMemPool_t* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  if (!g_pool[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool;
+    e = cudaMemPoolCreate(&pool, &props);
+    if (e != cudaSuccess) return e;
+    uint64_t keep = UINT64_MAX;  // keep freed blocks for reuse instead of returning them
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    g_pool[dev] = pool;
+  }
+  *out = g_pool[dev];
+  return cudaSuccess;
+}
+
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s) {
+  cudaMemPool_t pool;
+  cudaError_t e = pool_for_current_device(&pool);
+  if (e != cudaSuccess) return e;
+  return cudaMallocFromPoolAsync(p, bytes < 256 ? 256 : bytes, pool, s);
+}
+
+cudaError_t scratch_free(void* p, cudaStream_t s) {
+  return p ? cudaFreeAsync(p, s) : cudaSuccess;
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return 148;
+  if (!g_sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = n > 0 ? n : 148;
+  }
+  return g_sms[dev];
+}
+
+}  // namespace host
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by fa_fwd and fa_bwd (see the field comments in fa.h).
+fa_status validate(const fa_params* p) {
+  if (!p) return FA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || p->HKV < 1 || p->Sq < 0 || p->Sk < 0 || p->D < 1)
+    return FA_ERR_INVALID_ARG;
+  if (p->H % p->HKV != 0) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(p->scale) && p->scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if ((p->causal != 0 && p->causal != 1) || p->window < 0) return FA_ERR_INVALID_ARG;
+  if ((p->in_dtype != FA_F32 && p->in_dtype != FA_BF16) ||
+      (p->out_dtype != FA_F32 && p->out_dtype != FA_BF16))
+    return FA_ERR_INVALID_ARG;
+  // Index arithmetic inside the kernels uses 32-bit row / head / grid counters.
+  const long long bh = (long long)p->B * p->H;
+  if (bh > (1ll << 30) || p->Sq > (1 << 30) || p->Sk > (1 << 30)) return FA_ERR_INVALID_ARG;
+  if (bh * ((p->Sq + 255) / 256) > (1ll << 31) - 1) return FA_ERR_INVALID_ARG;
+  const bool ok_bf16 = p->in_dtype == FA_BF16 && (p->D == 64 || p->D == 128);
+  const bool ok_f32 = p->in_dtype == FA_F32 && p->D == 64;
+  if (!ok_bf16 && !ok_f32) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status check_ptrs(std::initializer_list<const void*> ptrs) {
+  for (const void* q : ptrs) {
+    if (!q) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q)) return FA_ERR_ALIGNMENT;
+  }
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                        const fa_params* p, fa_stream_t stream) {
+  fa_status st = validate(p);
+  if (st != FA_OK) return st;
+  if (p->Sq == 0) return FA_OK;  // nothing to compute
+  st = check_ptrs({O, LSE, Q});
+  if (st != FA_OK) return st;
+  if (p->Sk > 0) {
+    st = check_ptrs({K, V});
+    if (st != FA_OK) return st;
+  }
+  return launch_fwd(Q, K, V, O, LSE, *p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O,
+                        const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                        const fa_params* p, fa_stream_t stream) {
+  fa_status st = validate(p);
+  if (st != FA_OK) return st;
+  if (p->Sq > 0) {
+    st = check_ptrs({Q, O, dO, LSE, dQ});
+    if (st != FA_OK) return st;
+  }
+  if (p->Sk > 0) {
+    st = check_ptrs({K, V, dK, dV});
+    if (st != FA_OK) return st;
+  }
+  if (p->Sq == 0 && p->Sk == 0) return FA_OK;
+  return launch_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, *p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+FA_API fa_status fa_device_status(fa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  cudaError_t e1 = cudaSuccess, e2 = cudaSuccess;
+  const unsigned int v = read_and_clear_fwd_status(&e1) | read_and_clear_bwd_status(&e2);
+  if (e1 != cudaSuccess || e2 != cudaSuccess) return FA_ERR_CUDA;
+  return (v & DEV_TIMEOUT) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+FA_API const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "kernel barrier wait timed out";
+  }
+  return "unknown status";
+}
+
+FA_API const char* fa_version(void) { return "fa-sm103a 0.1"; }
+
+}  // extern "C"

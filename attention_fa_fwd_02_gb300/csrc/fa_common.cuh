@@ -1,0 +1,97 @@
+// fa_common.cuh -- tiling constants, tile-range arithmetic and host helpers shared
+// by the forward and backward translation units of libfa.so.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include "fa.h"
+
+namespace fa {
+
+constexpr int BLOCK_M = 128;  // query rows per tile (tcgen05 M = 128, one TMEM lane per row)
+constexpr int BLOCK_N = 128;  // key rows per tile
+constexpr uint32_t SW128_ROW = 128;          // bytes per swizzled smem row
+constexpr uint32_t SW128_ATOM = 1024;        // 8 rows x 128 bytes
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+// Rescale O only when the running max grows by more than this (log2 units): the
+// unnormalised probabilities then stay below 2^8, well inside fp16 range.
+constexpr float RESCALE_THRESHOLD = 8.0f;
+
+// Status bits a kernel may set in its device status word.
+enum : unsigned int { DEV_TIMEOUT = 1u };
+
+// Half-open range [lo, hi) of key tiles that query rows [r0, r1] may attend to:
+// key j is visible to row i iff j < Sk, (!causal || j <= i) and
+// (window == 0 || j >= i - window + 1). Blocks wholly outside the band are
+// skipped (forge flash_attn_fwd: kb limit for causal, tg_jmin for the window).
+__host__ __device__ inline void kv_tile_range(int r0, int r1, int Sk, int causal, int window,
+                                              int* lo, int* hi) {
+  int jmax = Sk - 1;
+  if (causal && r1 < jmax) jmax = r1;
+  int jmin = 0;
+  if (window > 0 && r0 - window + 1 > 0) jmin = r0 - window + 1;
+  if (jmax < jmin) { *lo = 0; *hi = 0; return; }
+  *lo = jmin / BLOCK_N;
+  *hi = jmax / BLOCK_N + 1;
+}
+
+// Half-open range [lo, hi) of query tiles whose rows may see key rows [c0, c1]
+// (the transpose of kv_tile_range; forge flash_attn_bwd_dv / _dk imin / imax).
+__host__ __device__ inline void q_tile_range(int c0, int c1, int Sq, int causal, int window,
+                                             int* lo, int* hi) {
+  int imin = 0;
+  if (causal) imin = c0;
+  int imax = Sq - 1;
+  if (window > 0) {
+    long long lim = (long long)c1 + window - 1;
+    if (lim < imax) imax = (int)lim;
+  }
+  if (imax < imin) { *lo = 0; *hi = 0; return; }
+  *lo = imin / BLOCK_M;
+  *hi = imax / BLOCK_M + 1;
+}
+
+// True if some (row, key) pair of the tile pair is invisible, i.e. the tile needs
+// the per-element mask; interior tiles skip it (forge flash_attn_fwd: only the
+// diagonal block pays the mask test).
+__host__ __device__ inline bool tile_needs_mask(int r0, int r1, int c0, int c1, int Sk,
+                                                int causal, int window) {
+  if (c1 >= Sk) return true;
+  if (causal && c1 > r0) return true;
+  if (window > 0 && (long long)c0 < (long long)r1 - window + 1) return true;
+  return false;
+}
+
+// ---------------------------------------------------------------- host side
+namespace host {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+// A [outer][rows][inner] tensor whose rows are `row_stride` elements apart and whose
+// outer slabs are rows * row_stride elements apart; 128-byte swizzle, box
+// {box_inner, box_rows, 1}, zero fill out of bounds.
+bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
+                     uint64_t inner, uint64_t rows, uint64_t outer, uint64_t row_stride,
+                     uint32_t box_inner, uint32_t box_rows);
+
+// Stream-ordered scratch from a library-owned pool on the current device.
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);
+cudaError_t scratch_free(void* p, cudaStream_t s);
+
+int sm_count();
+
+}  // namespace host
+
+// Launchers implemented by the kernel translation units.
+fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                     const fa_params& p, cudaStream_t stream);
+fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                     const float* LSE, void* dQ, void* dK, void* dV, const fa_params& p,
+                     cudaStream_t stream);
+unsigned int read_and_clear_fwd_status(cudaError_t* err);
+unsigned int read_and_clear_bwd_status(cudaError_t* err);
+
+// Default barrier-wait limit (ns) for the kernels.
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+}  // namespace fa

@@ -1,0 +1,602 @@
+// fa_fwd.cu -- forward attention on sm_103a: TMA-fed, warp-specialised, tcgen05/TMEM.
+//
+// One CTA owns NQ query tiles of 128 rows of one (batch, head) and walks the key
+// tiles they may see (forge "flash_attention.metal", flash_attn_fwd: threadgroup of
+// consecutive query rows, K/V staged once per group, blocks outside the causal /
+// window band skipped, online softmax with m starting at -FLT_MAX; rustytorch
+// "flash_attention_forward.metal": O = softmax(Q K^T * scale) V and the LSE row
+// output). Roles:
+//   warps [0, 4*NQ)   softmax: thread = one query row = one TMEM lane. Reads the
+//                     S row from TMEM, masks boundary tiles, keeps the running max
+//                     m (log2 units) and sum l, writes P back into TMEM (fp16 for
+//                     bf16 inputs; tf32 hi + lo for fp32 inputs), rescales its O
+//                     row in TMEM when m grows by more than RESCALE_THRESHOLD, and
+//                     in the epilogue writes O = acc / l and LSE = (m + log2 l) ln 2.
+//   warp 4*NQ         MMA issuer (one thread): S_q = Q_q K_j^T, O_q += P_q V_j.
+//   warp 4*NQ + 1     TMA producer (one thread): Q once, then K_j / V_j rings.
+// Every barrier wait is bounded; on expiry the kernel raises the device status
+// word, drains its in-flight copies and MMAs, frees TMEM and returns.
+#include <cfloat>
+#include <climits>
+#include <cstdio>
+#include "fa_common.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+using namespace ptx;
+
+static __device__ unsigned int g_fwd_status = 0;
+
+struct FwdArgs {
+  void* O;
+  float* LSE;
+  int H, HKV, Sq, Sk;
+  float scale_log2;  // softmax scale * log2(e)
+  int causal, window;
+  int out_bf16;
+  int n_qgroups;
+  int lpt;  // 1: launch the heaviest query groups first (causal)
+  int BH;
+  unsigned long long limit_ns;
+};
+
+template <int D_, bool F32_>
+struct FwdCfg {
+  static constexpr int D = D_;
+  static constexpr bool F32 = F32_;
+  static constexpr int NQ = F32 ? 1 : 2;                   // query tiles per CTA
+  static constexpr int ESZ = F32 ? 4 : 2;                  // operand bytes in smem
+  static constexpr int ROW_ELEMS = 128 / ESZ;              // elements per 128-byte row
+  static constexpr int NCB = D / ROW_ELEMS;                // 128-byte column blocks per row-tile
+  static constexpr uint32_t CB_BYTES = 128u * 128u;        // one column block of a 128-row tile
+  static constexpr uint32_t TILE_BYTES = NCB * CB_BYTES;   // a 128 x D operand tile
+  static constexpr uint32_t VT_CB_BYTES = D * 128u;        // fp32 V^T: 32 keys x D rows
+  static constexpr int NSPLIT = F32 ? 2 : 1;               // hi / lo copies
+  static constexpr int KST = F32 ? 1 : (D == 128 ? 2 : 3); // K ring depth
+  static constexpr int VST = KST;                          // V ring depth
+  static constexpr uint32_t Q_OFF = 0;
+  static constexpr uint32_t K_OFF = Q_OFF + NQ * NSPLIT * TILE_BYTES;
+  static constexpr uint32_t V_OFF = K_OFF + KST * NSPLIT * TILE_BYTES;
+  static constexpr uint32_t SMEM_BYTES = V_OFF + VST * NSPLIT * TILE_BYTES;
+  static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
+  static constexpr int SOFTMAX_WARPS = 4 * NQ;
+  static constexpr int MMA_WARP = SOFTMAX_WARPS;
+  static constexpr int TMA_WARP = SOFTMAX_WARPS + 1;
+  static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t PLO_COL = 128;                  // fp32 path: P_lo columns
+  __host__ __device__ static constexpr uint32_t s_col(int q) { return 128u * q; }
+  __host__ __device__ static constexpr uint32_t o_col(int q) { return 256u + (uint32_t)D * q; }
+  static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory budget");
+  static_assert(F32 ? (256 + D <= 512) : (256 + 2 * D <= 512), "TMEM budget");
+};
+
+template <class C>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sq_lo, uint32_t sk,
+                                         uint32_t sk_lo) {
+  if constexpr (!C::F32) {
+    constexpr uint32_t id = make_idesc(128, 128, FMT_BF16, FMT_BF16, false, false);
+#pragma unroll
+    for (int kk = 0; kk < C::D / 16; ++kk) {
+      const uint32_t off = (kk * 16 / 64) * C::CB_BYTES + (kk * 16 % 64) * 2;
+      mma_f16_ss(d_tmem, make_sdesc(sq + off, 16, SW128_ATOM), make_sdesc(sk + off, 16, SW128_ATOM),
+                 id, kk > 0);
+    }
+  } else {
+    constexpr uint32_t id = make_idesc(128, 128, FMT_TF32, FMT_TF32, false, false);
+#pragma unroll
+    for (int kk = 0; kk < C::D / 8; ++kk) {
+      const uint32_t off = (kk * 8 / 32) * C::CB_BYTES + (kk * 8 % 32) * 4;
+      const uint64_t qh = make_sdesc(sq + off, 16, SW128_ATOM);
+      const uint64_t ql = make_sdesc(sq_lo + off, 16, SW128_ATOM);
+      const uint64_t kh = make_sdesc(sk + off, 16, SW128_ATOM);
+      const uint64_t kl = make_sdesc(sk_lo + off, 16, SW128_ATOM);
+      mma_tf32_ss(d_tmem, qh, kh, id, kk > 0);
+      mma_tf32_ss(d_tmem, qh, kl, id, 1);
+      mma_tf32_ss(d_tmem, ql, kh, id, 1);
+    }
+  }
+}
+
+template <class C>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t plo_tmem,
+                                         uint32_t sv, uint32_t sv_lo, bool accumulate) {
+  if constexpr (!C::F32) {
+    // A = P (fp16, TMEM, 8 columns per 16 keys); B = V (fp16, MN-major in smem).
+    constexpr uint32_t id = make_idesc(128, C::D, FMT_F16, FMT_F16, false, true);
+#pragma unroll
+    for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+      mma_f16_ts(o_tmem, p_tmem + kk * 8, make_sdesc(sv + kk * 16 * 128, C::CB_BYTES, SW128_ATOM),
+                 id, (accumulate || kk > 0) ? 1u : 0u);
+  } else {
+    // A = P_hi / P_lo (fp32, TMEM, one column per key); B = V^T (K-major: rows = d).
+    constexpr uint32_t id = make_idesc(128, C::D, FMT_TF32, FMT_TF32, false, false);
+#pragma unroll
+    for (int kk = 0; kk < BLOCK_N / 8; ++kk) {
+      const uint32_t off = (kk / 4) * C::VT_CB_BYTES + (kk % 4) * 32;
+      const uint64_t vh = make_sdesc(sv + off, 16, SW128_ATOM);
+      const uint64_t vl = make_sdesc(sv_lo + off, 16, SW128_ATOM);
+      mma_tf32_ts(o_tmem, p_tmem + kk * 8, vh, id, (accumulate || kk > 0) ? 1u : 0u);
+      mma_tf32_ts(o_tmem, p_tmem + kk * 8, vl, id, 1);
+      mma_tf32_ts(o_tmem, plo_tmem + kk * 8, vh, id, 1);
+    }
+  }
+}
+
+template <int D, bool F32>
+__global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
+                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKlo,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmVlo,
+                  const FwdArgs a) {
+  using C = FwdCfg<D, F32>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bar_q, bar_kfull[C::KST], bar_kempty[C::KST],
+      bar_vfull[C::VST], bar_vempty[C::VST], bar_s[C::NQ], bar_p[C::NQ], bar_o[C::NQ], bar_drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  volatile int* abort_flag = &abort_sh;
+
+  // ---- work decode: heaviest causal query groups first, heads of one kv group adjacent.
+  const int qg_lin = blockIdx.x / a.BH;
+  const int bh = blockIdx.x % a.BH;
+  const int qg = a.lpt ? (a.n_qgroups - 1 - qg_lin) : qg_lin;
+  const int b = bh / a.H, h = bh % a.H;
+  const int g = h / (a.H / a.HKV);
+  const int bg = b * a.HKV + g;
+  const int row0 = qg * (BLOCK_M * C::NQ);
+  int t_lo, t_hi;
+  {
+    int r1 = row0 + BLOCK_M * C::NQ - 1;
+    if (r1 > a.Sq - 1) r1 = a.Sq - 1;
+    kv_tile_range(row0, r1, a.Sk, a.causal, a.window, &t_lo, &t_hi);
+  }
+  const int n = t_hi - t_lo;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < C::KST; ++s) { mbar_init(&bar_kfull[s], 1); mbar_init(&bar_kempty[s], 1); }
+    for (int s = 0; s < C::VST; ++s) { mbar_init(&bar_vfull[s], 1); mbar_init(&bar_vempty[s], 1); }
+    for (int q = 0; q < C::NQ; ++q) {
+      mbar_init(&bar_s[q], 1);
+      mbar_init(&bar_p[q], 128);
+      mbar_init(&bar_o[q], 1);
+    }
+    mbar_init(&bar_drain, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    __syncwarp();
+    tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t sbase = smem_u32(smem);
+  auto sQ = [&](int q, int sp) { return sbase + C::Q_OFF + (q * C::NSPLIT + sp) * C::TILE_BYTES; };
+  auto sK = [&](int st, int sp) { return sbase + C::K_OFF + (st * C::NSPLIT + sp) * C::TILE_BYTES; };
+  auto sV = [&](int st, int sp) { return sbase + C::V_OFF + (st * C::NSPLIT + sp) * C::TILE_BYTES; };
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    return mbar_wait(bar, parity, abort_flag, &g_fwd_status, DEV_TIMEOUT, a.limit_ns);
+  };
+
+  if (warp == C::TMA_WARP) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && n > 0) {
+      tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(&bar_q, C::NQ * C::NSPLIT * C::TILE_BYTES);
+      for (int q = 0; q < C::NQ; ++q)
+        for (int sp = 0; sp < C::NSPLIT; ++sp)
+          for (int cb = 0; cb < C::NCB; ++cb)
+            tma_load_3d(smem + (sQ(q, sp) - sbase) + cb * C::CB_BYTES, sp ? &tmQlo : &tmQ, &bar_q,
+                        cb * C::ROW_ELEMS, row0 + q * BLOCK_M, bh);
+      int last_k[C::KST], last_v[C::VST];
+      for (int s = 0; s < C::KST; ++s) last_k[s] = -1;
+      for (int s = 0; s < C::VST; ++s) last_v[s] = -1;
+      for (int it = 0; it < n; ++it) {
+        const int t = t_lo + it;
+        const int ks = it % C::KST;
+        if (!wait(&bar_kempty[ks], ((it / C::KST) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(&bar_kfull[ks], C::NSPLIT * C::TILE_BYTES);
+        for (int sp = 0; sp < C::NSPLIT; ++sp)
+          for (int cb = 0; cb < C::NCB; ++cb)
+            tma_load_3d(smem + (sK(ks, sp) - sbase) + cb * C::CB_BYTES, sp ? &tmKlo : &tmK,
+                        &bar_kfull[ks], cb * C::ROW_ELEMS, t * BLOCK_N, bg);
+        last_k[ks] = it / C::KST;
+        const int vs = it % C::VST;
+        if (!wait(&bar_vempty[vs], ((it / C::VST) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(&bar_vfull[vs], C::NSPLIT * C::TILE_BYTES);
+        for (int sp = 0; sp < C::NSPLIT; ++sp) {
+          if constexpr (!C::F32) {
+            for (int cb = 0; cb < C::NCB; ++cb)
+              tma_load_3d(smem + (sV(vs, sp) - sbase) + cb * C::CB_BYTES, &tmV, &bar_vfull[vs],
+                          cb * C::ROW_ELEMS, t * BLOCK_N, bg);
+          } else {  // V^T: 4 boxes of 32 keys x D rows
+            for (int cb = 0; cb < 4; ++cb)
+              tma_load_3d(smem + (sV(vs, sp) - sbase) + cb * C::VT_CB_BYTES, sp ? &tmVlo : &tmV,
+                          &bar_vfull[vs], t * BLOCK_N + cb * 32, 0, bg);
+          }
+        }
+        last_v[vs] = it / C::VST;
+      }
+      // Drain: every issued copy must land before the CTA may exit.
+      for (int s = 0; s < C::KST; ++s)
+        if (last_k[s] >= 0) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(&bar_kfull[s], last_k[s] & 1) && globaltimer() - t0 < a.limit_ns) {}
+        }
+      for (int s = 0; s < C::VST; ++s)
+        if (last_v[s] >= 0) {
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(&bar_vfull[s], last_v[s] & 1) && globaltimer() - t0 < a.limit_ns) {}
+        }
+      {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&bar_q, 0) && globaltimer() - t0 < a.limit_ns) {}
+      }
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      bool ok = wait(&bar_q, 0) && wait(&bar_kfull[0], 0);
+      tc_fence_after();
+      if (ok) {
+        for (int q = 0; q < C::NQ; ++q) {
+          issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(0, 0),
+                      sK(0, C::NSPLIT - 1));
+          tc_commit(&bar_s[q]);
+        }
+        tc_commit(&bar_kempty[0]);
+      }
+      for (int it = 0; ok && it < n; ++it) {
+        const int vs = it % C::VST;
+        if (!(ok = wait(&bar_vfull[vs], (it / C::VST) & 1))) break;
+        tc_fence_after();
+        for (int q = 0; q < C::NQ && ok; ++q) {
+          if (!(ok = wait(&bar_p[q], it & 1))) break;
+          tc_fence_after();
+          issue_pv<C>(tmem + C::o_col(q), tmem + C::s_col(q), tmem + C::PLO_COL, sV(vs, 0),
+                      sV(vs, C::NSPLIT - 1), it > 0);
+          if (it + 1 < n) {
+            const int ks = (it + 1) % C::KST;
+            if (q == 0) {
+              if (!(ok = wait(&bar_kfull[ks], ((it + 1) / C::KST) & 1))) break;
+              tc_fence_after();
+            }
+            issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(ks, 0),
+                        sK(ks, C::NSPLIT - 1));
+            tc_commit(&bar_s[q]);
+          }
+        }
+        if (!ok) break;
+        tc_commit(&bar_vempty[vs]);
+        if (it + 1 < n) tc_commit(&bar_kempty[(it + 1) % C::KST]);
+      }
+      if (ok)
+        for (int q = 0; q < C::NQ; ++q) tc_commit(&bar_o[q]);
+      // Drain: no MMA may still be running when TMEM is released.
+      tc_commit(&bar_drain);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&bar_drain, 0) && globaltimer() - t0 < a.limit_ns) {}
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int q = warp / 4;
+    const int wq = warp % 4;
+    const int r_in = wq * 32 + lane;
+    const int r0 = row0 + q * BLOCK_M;
+    const int i = r0 + r_in;  // this thread's query row
+    const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t s_addr = lane_addr + C::s_col(q);
+    const uint32_t o_addr = lane_addr + C::o_col(q);
+    const float sl2 = a.scale_log2;
+    // visible keys of row i: [lo_i, hi_i]
+    const int hi_i = a.causal ? min(i, a.Sk - 1) : a.Sk - 1;
+    const int lo_i = a.window > 0 ? i - a.window + 1 : INT_MIN / 2;
+    float m = -FLT_MAX;  // running max of scale*log2(e)*S, possibly stale by < threshold
+    float l = 0.f;
+    bool ok = true;
+    for (int it = 0; it < n; ++it) {
+      const int t = t_lo + it;
+      ok = __all_sync(0xffffffffu, wait(&bar_s[q], it & 1));
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(s_addr + c * 32, r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(r[k]);
+      }
+      const int c0 = t * BLOCK_N;
+      if (tile_needs_mask(r0, r0 + BLOCK_M - 1, c0, c0 + BLOCK_N - 1, a.Sk, a.causal, a.window)) {
+        const int rel_hi = hi_i - c0, rel_lo = lo_i - c0;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > rel_hi || c < rel_lo) s[c] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, s[c]); mx1 = fmaxf(mx1, s[c + 1]);
+        mx2 = fmaxf(mx2, s[c + 2]); mx3 = fmaxf(mx3, s[c + 3]);
+      }
+      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const bool need = mt > m + RESCALE_THRESHOLD;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = fmaxf(m, mt);
+        const float corr = ex2(m - m_new);
+        l *= corr;
+        if (it > 0) {
+#pragma unroll
+          for (int c = 0; c < C::D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(o_addr + c * 32, r);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * corr);
+            tmem_st32(o_addr + c * 32, r);
+          }
+        }
+        m = m_new;
+      }
+      const float nm = -m;
+      float l0 = 0.f, l1 = 0.f;
+      if constexpr (!C::F32) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float p0 = ex2(fmaf(s[c * 64 + 2 * k], sl2, nm));
+            const float p1 = ex2(fmaf(s[c * 64 + 2 * k + 1], sl2, nm));
+            l0 += p0;
+            l1 += p1;
+            pk[k] = pack_half2(p0, p1);
+          }
+          tmem_st32(s_addr + c * 32, pk);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ph[32], pl[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float p = ex2(fmaf(s[c * 32 + k], sl2, nm));
+            if (k & 1) l1 += p; else l0 += p;
+            const uint32_t hb = __float_as_uint(p) & 0xFFFFE000u;
+            ph[k] = hb;
+            pl[k] = __float_as_uint(p - __uint_as_float(hb));
+          }
+          tmem_st32(s_addr + c * 32, ph);
+          tmem_st32(lane_addr + C::PLO_COL + c * 32, pl);
+        }
+      }
+      l += l0 + l1;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_p[q]);
+    }
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, wait(&bar_o[q], 0));
+      tc_fence_after();
+    }
+    if (ok) {
+      const bool valid = i < a.Sq;
+      const float inv = (l > 0.f) ? (1.f / l) : 0.f;
+      const size_t row = (size_t)bh * a.Sq + (size_t)(valid ? i : 0);
+#pragma unroll
+      for (int c = 0; c < C::D / 32; ++c) {
+        uint32_t r[32];
+        if (n > 0) {
+          tmem_ld32(o_addr + c * 32, r);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) r[k] = 0u;
+        }
+        if (valid) {
+          if (!a.out_bf16) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.O) + row * D + c * 32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
+                                   __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.O) + row * D + c * 32);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[8 * k + 2 * e]) * inv,
+                                                          __uint_as_float(r[8 * k + 2 * e + 1]) * inv);
+                w[e] = *reinterpret_cast<uint32_t*>(&v2);
+              }
+              dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+      if (valid) a.LSE[row] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------ pre-pass kernels
+// bf16 -> fp16, exact for 2^-14 <= |x| <= 65504 (partner operand of the fp16 P).
+__global__ void cvt_bf16_to_f16_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+                                       size_t n8) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 v = in[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w[e] << 16);
+      const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
+      o[e] = pack_half2(lo, hi);
+    }
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// x = hi + lo with hi = x truncated to tf32 (low 13 mantissa bits cleared), lo exact.
+// Optionally writes the pair transposed per [rows x D] slab ([D x ld_t] layout).
+__global__ void split_tf32_kernel(const float* __restrict__ in, float* __restrict__ hi,
+                                  float* __restrict__ lo, float* __restrict__ hi_t,
+                                  float* __restrict__ lo_t, int rows, int D, int ld_t,
+                                  size_t n_slabs) {
+  const size_t total = n_slabs * (size_t)rows * D;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const float x = in[idx];
+    const float xh = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    const float xl = x - xh;
+    if (hi) { hi[idx] = xh; lo[idx] = xl; }
+    if (hi_t) {
+      const size_t slab = idx / ((size_t)rows * D);
+      const size_t rem = idx % ((size_t)rows * D);
+      const size_t r = rem / D, d = rem % D;
+      const size_t o = slab * (size_t)D * ld_t + d * ld_t + r;
+      hi_t[o] = xh;
+      lo_t[o] = xl;
+    }
+  }
+}
+
+// Rows that see no key at all (Sk == 0): O = 0, LSE = -inf.
+__global__ void fill_empty_kernel(void* O, float* LSE, size_t rows, int D, int out_bf16) {
+  for (size_t r = blockIdx.x * (size_t)blockDim.x + threadIdx.x; r < rows;
+       r += (size_t)gridDim.x * blockDim.x) {
+    LSE[r] = -INFINITY;
+    if (out_bf16) {
+      for (int d = 0; d < D; ++d) static_cast<__nv_bfloat16*>(O)[r * D + d] = __float2bfloat16(0.f);
+    } else {
+      for (int d = 0; d < D; ++d) static_cast<float*>(O)[r * D + d] = 0.f;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ launcher
+namespace {
+
+template <int D, bool F32>
+fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                  const fa_params& p, cudaStream_t stream) {
+  using C = FwdCfg<D, F32>;
+  const size_t nq = (size_t)p.B * p.H * p.Sq * D;
+  const size_t nk = (size_t)p.B * p.HKV * p.Sk * D;
+  const int grid_pp = 4 * host::sm_count();
+  void* ws = nullptr;
+  CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo;
+  const uint64_t BHq = (uint64_t)p.B * p.H, BHk = (uint64_t)p.B * p.HKV;
+  bool enc = true;
+  if constexpr (!F32) {
+    if (host::scratch_alloc(&ws, nk * 2, stream) != cudaSuccess) return FA_ERR_CUDA;
+    cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
+                                                       static_cast<uint4*>(ws), nk / 8);
+    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, D, p.Sq, BHq, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, D, p.Sk, BHk, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, D, p.Sk, BHk, D, 64, 128);
+    mQlo = mQ; mKlo = mK; mVlo = mV;
+  } else {
+    const int ldt = (p.Sk + 3) / 4 * 4;  // transposed V rows padded to 16 bytes
+    const size_t nvt = (size_t)p.B * p.HKV * D * ldt;
+    const size_t bytes = (2 * nq + 2 * nk + 2 * nvt) * 4;
+    if (host::scratch_alloc(&ws, bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
+    float* qh = static_cast<float*>(ws);
+    float* ql = qh + nq;
+    float* kh = ql + nq;
+    float* kl = kh + nk;
+    float* vth = kl + nk;
+    float* vtl = vth + nvt;
+    split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(Q), qh, ql, nullptr,
+                                                  nullptr, p.Sq, D, 0, BHq);
+    split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(K), kh, kl, nullptr,
+                                                  nullptr, p.Sk, D, 0, BHk);
+    split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(V), nullptr, nullptr,
+                                                  vth, vtl, p.Sk, D, ldt, BHk);
+    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, qh, D, p.Sq, BHq, D, 32, 128);
+    enc &= host::encode_tiled_3d(&mQlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ql, D, p.Sq, BHq, D, 32, 128);
+    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kh, D, p.Sk, BHk, D, 32, 128);
+    enc &= host::encode_tiled_3d(&mKlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kl, D, p.Sk, BHk, D, 32, 128);
+    // V^T: [BHk][D][ldt], inner extent Sk (row stride ldt), box 32 keys x D rows
+    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, vth, p.Sk, D, BHk, ldt, 32, D);
+    enc &= host::encode_tiled_3d(&mVlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, vtl, p.Sk, D, BHk, ldt, 32, D);
+  }
+  if (!enc) {
+    host::scratch_free(ws, stream);
+    return FA_ERR_CUDA;
+  }
+  FwdArgs a;
+  a.O = O;
+  a.LSE = LSE;
+  a.H = p.H;
+  a.HKV = p.HKV;
+  a.Sq = p.Sq;
+  a.Sk = p.Sk;
+  a.scale_log2 = p.scale * LOG2E;
+  a.causal = p.causal;
+  a.window = p.window;
+  a.out_bf16 = p.out_dtype == FA_BF16;
+  a.n_qgroups = (p.Sq + BLOCK_M * C::NQ - 1) / (BLOCK_M * C::NQ);
+  a.lpt = p.causal ? 1 : 0;
+  a.BH = (int)BHq;
+  a.limit_ns = WAIT_LIMIT_NS;
+  auto kern = fa_fwd_kernel<D, F32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)C::SMEM_ALLOC);
+  if (e == cudaSuccess) {
+    const unsigned grid = (unsigned)(BHq * a.n_qgroups);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, a);
+    e = cudaGetLastError();
+  }
+  cudaError_t e2 = host::scratch_free(ws, stream);
+  return (e == cudaSuccess && e2 == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                     const fa_params& p, cudaStream_t stream) {
+  if (p.Sk == 0) {
+    const size_t rows = (size_t)p.B * p.H * p.Sq;
+    fill_empty_kernel<<<4 * host::sm_count(), 256, 0, stream>>>(O, LSE, rows, p.D,
+                                                                p.out_dtype == FA_BF16);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+  if (p.in_dtype == FA_BF16) {
+    if (p.D == 128) return run_fwd<128, false>(Q, K, V, O, LSE, p, stream);
+    if (p.D == 64) return run_fwd<64, false>(Q, K, V, O, LSE, p, stream);
+  } else {
+    if (p.D == 64) return run_fwd<64, true>(Q, K, V, O, LSE, p, stream);
+  }
+  return FA_ERR_UNSUPPORTED;
+}
+
+unsigned int read_and_clear_fwd_status(cudaError_t* err) {
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_fwd_status, sizeof(v));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_fwd_status, &zero, sizeof(zero));
+  if (err) *err = e;
+  return v;
+}
+
+}  // namespace fa

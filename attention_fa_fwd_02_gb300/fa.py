@@ -1,0 +1,155 @@
+"""ctypes binding of libfa.so: same entry points as include/fa.h, argument
+marshalling only. Every step of the attention computation runs in the library's
+CUDA kernels; there is no Python or CPU fallback -- importing the binding fails
+loudly when the library is missing.
+
+The C calls take raw device pointers and a CUDA stream handle. The helpers
+``forward`` / ``backward`` allocate outputs with torch (device memory and
+streams are all torch is used for) and pass ``data_ptr()``s through.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa.so")
+
+FA_F32, FA_BF16 = 0, 1
+STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
+          4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string", "fa_version")
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({status_string(code)})")
+
+
+class fa_params(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("HKV", ctypes.c_int),
+                ("Sq", ctypes.c_int), ("Sk", ctypes.c_int), ("D", ctypes.c_int),
+                ("scale", ctypes.c_float), ("causal", ctypes.c_int), ("window", ctypes.c_int),
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int)]
+
+
+def _load(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libfa.so not built at {path}: run __graft_entry__.build() first "
+                          "(the attention path has no fallback)")
+    lib = ctypes.CDLL(path)
+    vp, st = ctypes.c_void_p, ctypes.c_int
+    P = ctypes.POINTER(fa_params)
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, P, vp]
+    lib.fa_fwd.restype = st
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, P, vp]
+    lib.fa_bwd.restype = st
+    lib.fa_device_status.argtypes = [vp]
+    lib.fa_device_status.restype = st
+    lib.fa_status_string.argtypes = [st]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().fa_status_string(int(code)).decode()
+
+
+def version() -> str:
+    return lib().fa_version().decode()
+
+
+# ------------------------------------------------------------ raw C entry points
+def fa_fwd(Q: int, K: int, V: int, O: int, LSE: int, params: fa_params, stream: int) -> int:
+    """Direct call of the C ``fa_fwd`` with integer device addresses; returns the status."""
+    return lib().fa_fwd(Q, K, V, O, LSE, ctypes.byref(params), stream)
+
+
+def fa_bwd(Q: int, K: int, V: int, O: int, dO: int, LSE: int, dQ: int, dK: int, dV: int,
+           params: fa_params, stream: int) -> int:
+    """Direct call of the C ``fa_bwd``; returns the status."""
+    return lib().fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, ctypes.byref(params), stream)
+
+
+def fa_device_status(stream: int) -> int:
+    return lib().fa_device_status(stream)
+
+
+# ------------------------------------------------------------ torch helpers
+def make_params(q, k, scale=None, causal=False, window=0, out_dtype=None) -> fa_params:
+    import torch
+    B, H, Sq, D = q.shape
+    HKV, Sk = k.shape[1], k.shape[2]
+    in_dt = {torch.float32: FA_F32, torch.bfloat16: FA_BF16}.get(q.dtype)
+    if in_dt is None:
+        raise TypeError(f"unsupported input dtype {q.dtype}")
+    out_dt = FA_F32 if out_dtype in (None, torch.float32) else FA_BF16
+    return fa_params(B, H, HKV, Sq, Sk, D, float(1.0 / math.sqrt(D) if scale is None else scale),
+                     int(bool(causal)), int(window), in_dt, out_dt)
+
+
+def _check(t, name):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def forward(q, k, v, scale=None, causal=False, window=0, out_dtype=None, stream=None):
+    """O, LSE = attention(q, k, v) on the GPU through ``fa_fwd``."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    p = make_params(q, k, scale, causal, window, out_dtype)
+    o = torch.empty(q.shape, dtype=torch.float32 if p.out_dtype == FA_F32 else torch.bfloat16,
+                    device=q.device)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), p,
+                _stream_handle(stream))
+    if rc:
+        raise FAError(rc, "fa_fwd")
+    return o, lse
+
+
+def backward(q, k, v, o, lse, do, scale=None, causal=False, window=0, out_dtype=None,
+             stream=None):
+    """dQ, dK, dV through ``fa_bwd`` (o / lse as returned by ``forward``)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (do, "do")):
+        _check(t, n)
+    p = make_params(q, k, scale, causal, window, out_dtype)
+    odt = torch.float32 if p.out_dtype == FA_F32 else torch.bfloat16
+    dq = torch.empty(q.shape, dtype=odt, device=q.device)
+    dk = torch.empty(k.shape, dtype=odt, device=q.device)
+    dv = torch.empty(v.shape, dtype=odt, device=q.device)
+    rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), p,
+                _stream_handle(stream))
+    if rc:
+        raise FAError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def check_device_status(stream=None) -> None:
+    """Synchronize and raise FAError if a kernel reported a barrier timeout."""
+    rc = fa_device_status(_stream_handle(stream))
+    if rc:
+        raise FAError(rc, "fa_device_status")

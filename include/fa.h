@@ -1,0 +1,134 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library, libfa.so.
+ *
+ * The operation is exact softmax attention with the online-softmax forward and
+ * the recompute-from-LSE backward described on the source pages:
+ *
+ *   O = softmax(scale * Q K^T + mask) V,   LSE_i = m_i + log(sum_j exp(S_ij - m_i))
+ *
+ *   - rustytorch "flash_attention_forward.metal": kernel header comment (the
+ *     formula), parameter block (batch, heads, seq_q, seq_kv, head_dim,
+ *     softmax_scale, causal) and the LSE output, one float per query row;
+ *   - forge "flash_attention.metal": FlashParams {B, T, H, HKV, scale, causal,
+ *     window}, GQA head mapping hkv = h / (H / HKV), the sliding window that
+ *     keeps keys j >= i - window + 1 (self included, 0 = full), and the backward
+ *     kernels flash_attn_bwd_dq / _dv / _dk that rebuild P from L and use
+ *     D_i = dO_i . O_i;
+ *   - boostr "flash.wgsl": FlashParams with separate seq_len_q / seq_len_k and
+ *     num_kv_heads, tensors laid out [B, heads, S, head_dim].
+ *
+ * Mask (top-left aligned when Sq != Sk): key j is visible to query i iff
+ *   (!causal || j <= i) && (window == 0 || j >= i - window + 1) && j < Sk.
+ * A query row that sees no key gets O_i = 0 and LSE_i = -inf, and contributes
+ * nothing to the gradients.
+ *
+ * Precision. in_dtype FA_BF16: QK^T and dO V^T run on bf16/fp16 tensor cores
+ * with fp32 accumulation; the probabilities P and dS enter the second GEMMs as
+ * fp16 (their partner operands are converted bf16 -> fp16, exact for
+ * 2^-14 <= |x| <= 65504; larger magnitudes are outside the supported range).
+ * in_dtype FA_F32: every GEMM uses three tf32 tensor-core products (the
+ * hi/lo split a = a_hi + a_lo; a_hi b_hi + a_hi b_lo + a_lo b_hi), giving close to
+ * fp32 accuracy. Outputs are written in out_dtype (FA_F32 recommended; FA_BF16
+ * rounds O / dQ / dK / dV to bf16 on store). LSE is always fp32, natural log.
+ *
+ * Supported in this build: D in {64, 128} for FA_BF16 inputs, D == 64 for
+ * FA_F32 inputs; other head dims return FA_ERR_UNSUPPORTED.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+/* ABI-compatible with cudaStream_t (a CUDA runtime / driver stream handle);
+ * NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum { FA_F32 = 0, FA_BF16 = 1 } fa_dtype;
+
+typedef struct {
+  int B;            /* batch size, >= 1 */
+  int H;            /* query heads, >= 1 */
+  int HKV;          /* key/value heads, >= 1, H % HKV == 0 (query head h reads kv head h / (H/HKV)) */
+  int Sq;           /* query rows per head, >= 0 */
+  int Sk;           /* key rows per head, >= 0 */
+  int D;            /* head dim */
+  float scale;      /* softmax scale applied to Q K^T (commonly 1/sqrt(D)); finite and > 0 */
+  int causal;       /* 0 or 1: key j visible only if j <= i (top-left aligned) */
+  int window;       /* >= 0; 0 = no window, else key j visible only if j >= i - window + 1 */
+  fa_dtype in_dtype;  /* dtype of Q, K, V, dO */
+  fa_dtype out_dtype; /* dtype of O, dQ, dK, dV */
+} fa_params;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* NULL pointer, bad shape, H % HKV != 0, bad enum */
+  FA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (head dim, dtype pair) */
+  FA_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
+  FA_ERR_CUDA = 4,        /* a CUDA runtime / driver call or a kernel launch failed */
+  FA_ERR_TIMEOUT = 5      /* a kernel gave up waiting on an internal barrier (device status) */
+} fa_status;
+
+/*
+ * Forward pass.
+ *   Q   [B, H,   Sq, D]  in_dtype, contiguous, device memory
+ *   K   [B, HKV, Sk, D]  in_dtype
+ *   V   [B, HKV, Sk, D]  in_dtype
+ *   O   [B, H,   Sq, D]  out_dtype, written (overwritten, never accumulated)
+ *   LSE [B, H,   Sq]     fp32, written: natural-log log-sum-exp of each row's
+ *                        scaled scores, -inf for rows with no visible key.
+ * All pointers are caller-owned device memory, 16-byte aligned; outputs must not
+ * alias inputs. The call validates its arguments synchronously, then enqueues
+ * work on `stream` and returns without waiting. Temporary buffers (an fp16 copy
+ * of V for bf16 inputs; hi/lo tf32 splits for fp32 inputs) are taken
+ * stream-ordered from a library-owned CUDA memory pool and released on the same
+ * stream. Errors: FA_ERR_INVALID_ARG / _UNSUPPORTED / _ALIGNMENT before any work
+ * is enqueued; FA_ERR_CUDA if a CUDA call or launch fails. Device-side barrier
+ * timeouts are reported later by fa_device_status().
+ */
+FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                 const fa_params* p, fa_stream_t stream);
+
+/*
+ * Backward pass for the loss L with upstream gradient dO = dL/dO.
+ *   Q, K, V  as in fa_fwd;  O [B,H,Sq,D] out_dtype and LSE [B,H,Sq] fp32 as
+ *   written by fa_fwd for the same inputs and params;  dO [B,H,Sq,D] in_dtype.
+ *   dQ [B,H,Sq,D], dK [B,HKV,Sk,D], dV [B,HKV,Sk,D]  out_dtype, overwritten.
+ * P is rebuilt tile by tile from LSE (never stored); D_i = rowsum(dO_i * O_i) is
+ * computed first by a preprocess kernel; dK/dV are accumulated per key tile over
+ * the grouped query heads without atomics (deterministic: two calls on the same
+ * inputs give bit-identical results). Workspace (D_i, fp16 / tf32-split operand
+ * copies) is stream-ordered from the library pool. Same ownership, alignment and
+ * error rules as fa_fwd.
+ */
+FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, const fa_params* p,
+                 fa_stream_t stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the library's device status word
+ * on the current device: FA_ERR_TIMEOUT if any kernel since the last call gave
+ * up on a barrier wait (its outputs are then undefined), FA_ERR_CUDA if the
+ * synchronization itself failed, else FA_OK.
+ */
+FA_API fa_status fa_device_status(fa_stream_t stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+FA_API const char* fa_status_string(fa_status s);
+
+/* Library version string, e.g. "fa-sm103a 0.1". */
+FA_API const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,122 @@
+"""Host-only checks of the C-ABI library: it loads, exports every symbol that
+include/fa.h declares, and rejects invalid calls with the documented status
+codes before touching the GPU (no call here reaches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    from attention_fa_fwd_02_gb300 import fa as fa_mod
+    return fa_mod
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    return set(re.findall(r"FA_API\s+[\w\s\*]*?\b(fa_\w+)\s*\(", text))
+
+
+def test_header_declares_the_abi():
+    assert _declared_symbols() == {"fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string",
+                                   "fa_version"}
+
+
+def test_library_exports_every_declared_symbol(fa):
+    lib = fa.lib()
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {fa.LIB_PATH}").read()
+    exported = set(re.findall(r"\bT (fa_\w+)", out))
+    assert _declared_symbols() <= exported
+    # hidden visibility: nothing but the ABI leaks out of the library
+    assert exported == _declared_symbols()
+
+
+def test_status_strings(fa):
+    assert fa.status_string(0) == "ok"
+    for code in range(1, 6):
+        assert fa.status_string(code) and fa.status_string(code) != "unknown status"
+    assert fa.status_string(99) == "unknown status"
+    assert fa.version().startswith("fa-sm103a")
+
+
+def _params(fa, **kw):
+    d = dict(B=1, H=4, HKV=2, Sq=128, Sk=128, D=128, scale=0.088, causal=1, window=0,
+             in_dtype=fa.FA_BF16, out_dtype=fa.FA_F32)
+    d.update(kw)
+    return fa.fa_params(**d)
+
+
+# Fake, never-dereferenced addresses: every call below must be rejected by
+# validation before any CUDA call is made.
+A = 0x10000
+MIS = 0x10008
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=3, HKV=2), 1),          # H % HKV != 0
+    (dict(B=0), 1),
+    (dict(HKV=0), 1),
+    (dict(Sq=-1), 1),
+    (dict(D=0), 1),
+    (dict(scale=0.0), 1),
+    (dict(scale=-0.1), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(scale=float("inf")), 1),
+    (dict(causal=2), 1),
+    (dict(window=-1), 1),
+    (dict(in_dtype=7), 1),
+    (dict(out_dtype=-1), 1),
+    (dict(D=96), 2),                # head dim not built
+    (dict(D=128, in_dtype=0), 2),   # fp32 inputs only at D=64
+    (dict(D=32), 2),
+])
+def test_invalid_params_rejected(fa, kw, code):
+    p = _params(fa, **kw)
+    assert fa.fa_fwd(A, A, A, A, A, p, 0) == code
+    assert fa.fa_bwd(A, A, A, A, A, A, A, A, A, p, 0) == code
+
+
+def test_null_params_rejected(fa):
+    lib = fa.lib()
+    assert lib.fa_fwd(A, A, A, A, A, None, None) == 1
+    assert lib.fa_bwd(A, A, A, A, A, A, A, A, A, None, None) == 1
+
+
+@pytest.mark.parametrize("which", range(5))
+def test_fwd_null_and_misaligned_pointers(fa, which):
+    p = _params(fa)
+    ptrs = [A] * 5
+    ptrs[which] = 0
+    assert fa.fa_fwd(*ptrs, p, 0) == 1
+    ptrs[which] = MIS
+    assert fa.fa_fwd(*ptrs, p, 0) == 3
+
+
+@pytest.mark.parametrize("which", range(9))
+def test_bwd_null_and_misaligned_pointers(fa, which):
+    p = _params(fa)
+    ptrs = [A] * 9
+    ptrs[which] = 0
+    assert fa.fa_bwd(*ptrs, p, 0) == 1
+    ptrs[which] = MIS
+    assert fa.fa_bwd(*ptrs, p, 0) == 3
+
+
+def test_empty_problems_are_no_ops(fa):
+    # Sq == 0: nothing to compute, no pointer is touched and no CUDA call is made.
+    assert fa.fa_fwd(0, 0, 0, 0, 0, _params(fa, Sq=0), 0) == 0
+    assert fa.fa_bwd(0, 0, 0, 0, 0, 0, 0, 0, 0, _params(fa, Sq=0, Sk=0), 0) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from attention_fa_fwd_02_gb300 import fa as fa_mod
+    with pytest.raises(ImportError):
+        fa_mod._load(str(tmp_path / "missing.so"))
