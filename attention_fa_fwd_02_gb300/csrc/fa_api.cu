@@ -22,7 +22,7 @@ int g_sms[MAX_DEVICES] = {};
 
 bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
                      uint64_t inner, uint64_t rows, uint64_t outer, uint64_t row_stride,
-                     uint32_t box_inner, uint32_t box_rows) {
+                     uint32_t box_inner, uint32_t box_rows, bool swizzle) {
   std::call_once(g_encode_once, [] {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -37,7 +37,8 @@ bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const 
   cuuint32_t box[3] = {box_inner, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -113,6 +114,14 @@ fa_status validate(const fa_params* p) {
   return FA_OK;
 }
 
+// A window of at least Sq keys excludes nothing (every key j >= 0 >= i - window + 1
+// for i < Sq); dropping it keeps all kernel index arithmetic within 31 bits.
+fa_params normalized(const fa_params& p) {
+  fa_params q = p;
+  if (q.window >= q.Sq) q.window = 0;
+  return q;
+}
+
 fa_status check_ptrs(std::initializer_list<const void*> ptrs) {
   for (const void* q : ptrs) {
     if (!q) return FA_ERR_INVALID_ARG;
@@ -139,7 +148,7 @@ FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, fl
     st = check_ptrs({K, V});
     if (st != FA_OK) return st;
   }
-  return launch_fwd(Q, K, V, O, LSE, *p, reinterpret_cast<cudaStream_t>(stream));
+  return launch_fwd(Q, K, V, O, LSE, normalized(*p), reinterpret_cast<cudaStream_t>(stream));
 }
 
 FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O,
@@ -156,7 +165,8 @@ FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void*
     if (st != FA_OK) return st;
   }
   if (p->Sq == 0 && p->Sk == 0) return FA_OK;
-  return launch_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, *p, reinterpret_cast<cudaStream_t>(stream));
+  return launch_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, normalized(*p),
+                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 FA_API fa_status fa_device_status(fa_stream_t stream) {

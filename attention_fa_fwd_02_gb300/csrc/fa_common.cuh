@@ -68,11 +68,11 @@ namespace host {
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 // A [outer][rows][inner] tensor whose rows are `row_stride` elements apart and whose
-// outer slabs are rows * row_stride elements apart; 128-byte swizzle, box
-// {box_inner, box_rows, 1}, zero fill out of bounds.
+// outer slabs are rows * row_stride elements apart; box {box_inner, box_rows, 1},
+// zero fill out of bounds; 128-byte swizzle unless `swizzle` is false.
 bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
                      uint64_t inner, uint64_t rows, uint64_t outer, uint64_t row_stride,
-                     uint32_t box_inner, uint32_t box_rows);
+                     uint32_t box_inner, uint32_t box_rows, bool swizzle = true);
 
 // Stream-ordered scratch from a library-owned pool on the current device.
 cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);

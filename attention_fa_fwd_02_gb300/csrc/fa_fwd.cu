@@ -21,6 +21,7 @@
 #include <cstdio>
 #include "fa_common.cuh"
 #include "ptx.cuh"
+#include "fa_prepass.cuh"
 
 namespace fa {
 using namespace ptx;
@@ -435,49 +436,6 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
-  }
-}
-
-// ------------------------------------------------------------ pre-pass kernels
-// bf16 -> fp16, exact for 2^-14 <= |x| <= 65504 (partner operand of the fp16 P).
-__global__ void cvt_bf16_to_f16_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
-                                       size_t n8) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const uint4 v = in[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float lo = __uint_as_float(w[e] << 16);
-      const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
-      o[e] = pack_half2(lo, hi);
-    }
-    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
-
-// x = hi + lo with hi = x truncated to tf32 (low 13 mantissa bits cleared), lo exact.
-// Optionally writes the pair transposed per [rows x D] slab ([D x ld_t] layout).
-__global__ void split_tf32_kernel(const float* __restrict__ in, float* __restrict__ hi,
-                                  float* __restrict__ lo, float* __restrict__ hi_t,
-                                  float* __restrict__ lo_t, int rows, int D, int ld_t,
-                                  size_t n_slabs) {
-  const size_t total = n_slabs * (size_t)rows * D;
-  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
-       idx += (size_t)gridDim.x * blockDim.x) {
-    const float x = in[idx];
-    const float xh = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-    const float xl = x - xh;
-    if (hi) { hi[idx] = xh; lo[idx] = xl; }
-    if (hi_t) {
-      const size_t slab = idx / ((size_t)rows * D);
-      const size_t rem = idx % ((size_t)rows * D);
-      const size_t r = rem / D, d = rem % D;
-      const size_t o = slab * (size_t)D * ld_t + d * ld_t + r;
-      hi_t[o] = xh;
-      lo_t[o] = xl;
-    }
   }
 }
 

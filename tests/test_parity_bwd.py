@@ -1,0 +1,115 @@
+"""GPU parity of the backward pass (fa_bwd through the C ABI) against the fp64 oracle.
+
+The GPU path takes O and LSE from its own forward pass, exactly as a caller
+would; the oracle derives dQ / dK / dV from Q, K, V, dO alone through the softmax
+Jacobian. Tolerances (max-abs error / RMS of the oracle tensor): 5e-3 for fp32
+inputs (3xTF32 path), 2e-2 for bf16 inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_fa_fwd_02_gb300.workloads import WORKLOADS, make_inputs
+from _parity import TOL, rms_err, to_np
+from test_parity_fwd import SMALL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU parity tests need a CUDA device"
+    from attention_fa_fwd_02_gb300 import fa as m
+    return m
+
+
+def _gpu_grads(fa, w, q, k, v, do, out_dtype=None):
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, w.scale, w.causal, w.window, out_dtype=out_dtype)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, w.scale, w.causal, w.window,
+                             out_dtype=out_dtype)
+    fa.check_device_status()
+    return dq, dk, dv
+
+
+def _check(w, got, ref, label):
+    tol = TOL[w.dtype]["grad"]
+    errs = {}
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        errs[name] = rms_err(to_np(g), r)
+    bad = {k: e for k, e in errs.items() if not e <= tol}
+    assert not bad, f"{label}: {errs} (tol {tol})"
+    return errs
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_backward_small(fa, name):
+    w = SMALL[name]
+    q, k, v, do = make_inputs(w)
+    got = _gpu_grads(fa, w, q, k, v, do)
+    ref = oracle.attention_bwd(q, k, v, do, w.scale, w.causal, w.window)
+    _check(w, got, ref, name)
+
+
+def test_backward_deterministic(fa):
+    # dK / dV are accumulated per key tile without atomics: bit-identical reruns.
+    w = SMALL["bf16-gqa-causal-ragged"]
+    q, k, v, do = make_inputs(w)
+    a = _gpu_grads(fa, w, q, k, v, do)
+    b = _gpu_grads(fa, w, q, k, v, do)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_backward_unseen_keys_get_zero_grad(fa):
+    # causal with Sq < Sk: keys j >= Sq are visible to no query -> dK = dV = 0 there
+    w = SMALL["bf16-causal-sq-lt-sk"]
+    q, k, v, do = make_inputs(w)
+    dq, dk, dv = _gpu_grads(fa, w, q, k, v, do)
+    assert torch.all(dk[:, :, w.Sq:] == 0) and torch.all(dv[:, :, w.Sq:] == 0)
+
+
+def test_backward_bf16_outputs(fa):
+    # bf16 outputs: each gradient element is rounded on store (2^-9 relative, the
+    # 2^-8 |r| term), and the forward's bf16-rounded O enters D_i = rowsum(dO * O),
+    # which perturbs dS = P (dP - D) by up to 2^-9 sum_d |dO_id O_id| per row -- an
+    # error of the same order as the fp16 dS rounding. The bound is therefore twice
+    # the fp32-output tolerance: |g - r| <= 2^-8 |r| + 4e-2 * RMS(r).
+    w = SMALL["bf16-gqa-causal-ragged"]
+    q, k, v, do = make_inputs(w)
+    got = _gpu_grads(fa, w, q, k, v, do, out_dtype=torch.bfloat16)
+    ref = oracle.attention_bwd(q, k, v, do, w.scale, w.causal, w.window)
+    for g, r in zip(got, ref):
+        assert g.dtype == torch.bfloat16
+        excess = np.abs(to_np(g) - r) - 2.0 ** -8 * np.abs(r)
+        assert excess.max() <= 4e-2 * np.sqrt(np.mean(r ** 2))
+
+
+@pytest.mark.parametrize("cfg", ["c1", "c2", "c5"])
+def test_backward_full_config_fp32(fa, cfg):
+    w = WORKLOADS[cfg]
+    q, k, v, do = make_inputs(w)
+    got = _gpu_grads(fa, w, q, k, v, do)
+    ref = oracle.attention_bwd(q, k, v, do, w.scale, w.causal, w.window)
+    _check(w, got, ref, cfg)
+
+
+@pytest.mark.parametrize("cfg,b,g", [("c3", 1, 5), ("c3", 0, 0), ("c4", 0, 3)])
+def test_backward_full_config_bf16_slice(fa, cfg, b, g):
+    # Full-size launch; whole (batch, kv-group) slices are independent, so the
+    # oracle checks one slice exactly (dK / dV of the group sum its query heads).
+    w = WORKLOADS[cfg]
+    q, k, v, do = make_inputs(w)
+    dq, dk, dv = _gpu_grads(fa, w, q, k, v, do)
+    rep = w.H // w.HKV
+    hs = slice(g * rep, (g + 1) * rep)
+    ref = oracle.attention_bwd(q[b:b + 1, hs], k[b:b + 1, g:g + 1], v[b:b + 1, g:g + 1],
+                               do[b:b + 1, hs], w.scale, w.causal, w.window)
+    _check(w, (dq[b:b + 1, hs], dk[b:b + 1, g:g + 1], dv[b:b + 1, g:g + 1]), ref,
+           f"{cfg} b{b} g{g}")
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()

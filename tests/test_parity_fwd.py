@@ -79,15 +79,17 @@ def test_forward_deterministic(fa):
 
 
 def test_forward_bf16_output(fa):
-    # bf16 outputs: the rounding of O itself dominates; checked against the
-    # bf16-rounded oracle output so the kernel's own error still has to be small.
+    # bf16 outputs: rounding O to bf16 moves each element by at most half an ulp,
+    # 2^-9 |O| (round to nearest, 8 significant bits). Allow that per element on top
+    # of the fp32-output tolerance: |o - ref| <= 2^-8 |ref| + 2e-2 * RMS(ref).
     w = SMALL["bf16-gqa-causal-ragged"]
     q, k, v, _ = make_inputs(w)
     o, lse = _run(fa, w, q, k, v, out_dtype=torch.bfloat16)
     assert o.dtype == torch.bfloat16
     ro, rl = oracle.attention_fwd(q, k, v, w.scale, w.causal, w.window)
-    ro_b = torch.tensor(ro).to(torch.bfloat16).double().numpy()
-    assert rms_err(to_np(o), ro_b) <= 2e-2
+    got = to_np(o)
+    excess = np.abs(got - ro) - 2.0 ** -8 * np.abs(ro)
+    assert excess.max() <= 2e-2 * np.sqrt(np.mean(ro ** 2))
     assert lse_err(to_np(lse), rl) <= 1e-2
 
 
