@@ -3,7 +3,9 @@
 // encoding and the device status word. Kernels live in fa_fwd.cu / fa_bwd.cu.
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
+#include <vector>
 #include <cudaTypedefs.h>
 #include "fa_common.cuh"
 
@@ -85,6 +87,44 @@ int sm_count() {
     g_sms[dev] = n > 0 ? n : 148;
   }
   return g_sms[dev];
+}
+
+namespace {
+struct Pending {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::mutex g_t_mu;
+bool g_t_on = false;
+std::vector<Pending> g_t_pending;
+std::vector<cudaEvent_t> g_t_free;
+
+cudaEvent_t take_event() {
+  if (!g_t_free.empty()) {
+    cudaEvent_t e = g_t_free.back();
+    g_t_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+}  // namespace
+
+KernelTimer::KernelTimer(const char* name, cudaStream_t s) : name_(name), stream_(s) {
+  std::lock_guard<std::mutex> lk(g_t_mu);
+  if (!g_t_on) return;
+  start_ = take_event();
+  if (start_) cudaEventRecord(start_, stream_);
+}
+
+KernelTimer::~KernelTimer() {
+  if (!start_) return;
+  std::lock_guard<std::mutex> lk(g_t_mu);
+  cudaEvent_t end = take_event();
+  if (!end) { g_t_free.push_back(start_); return; }
+  cudaEventRecord(end, stream_);
+  g_t_pending.push_back({name_, start_, end});
 }
 
 }  // namespace host
@@ -191,5 +231,42 @@ FA_API const char* fa_status_string(fa_status s) {
 }
 
 FA_API const char* fa_version(void) { return "fa-sm103a 0.1"; }
+
+FA_API fa_status fa_timing_enable(int on) {
+  using namespace fa::host;
+  std::lock_guard<std::mutex> lk(g_t_mu);
+  for (auto& p : g_t_pending) {
+    cudaEventSynchronize(p.b);
+    g_t_free.push_back(p.a);
+    g_t_free.push_back(p.b);
+  }
+  g_t_pending.clear();
+  g_t_on = on != 0;
+  return FA_OK;
+}
+
+FA_API int fa_timing_read(fa_kernel_time* out, int max_entries) {
+  using namespace fa::host;
+  std::lock_guard<std::mutex> lk(g_t_mu);
+  std::vector<fa_kernel_time> agg;
+  bool fail = false;
+  for (auto& p : g_t_pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess)
+      fail = true;
+    size_t k = 0;
+    while (k < agg.size() && std::strcmp(agg[k].name, p.name) != 0) ++k;
+    if (k == agg.size()) agg.push_back({p.name, 0, 0.0});
+    agg[k].launches += 1;
+    agg[k].total_ms += ms;
+    g_t_free.push_back(p.a);
+    g_t_free.push_back(p.b);
+  }
+  g_t_pending.clear();
+  if (fail) return -1;
+  for (size_t k = 0; k < agg.size() && (int)k < max_entries; ++k)
+    if (out) out[k] = agg[k];
+  return (int)agg.size();
+}
 
 }  // extern "C"

@@ -625,13 +625,19 @@ fa_status run_bwd_bf16(const void* Q, const void* K, const void* V, const void* 
   float* lse2 = reinterpret_cast<float*>(v16 + nk);
   float* delta = lse2 + nvec;
   const int grid_pp = 4 * host::sm_count();
-  bwd_preprocess_kernel<D><<<grid_pp, 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(dO), O, LSE, static_cast<const __nv_bfloat16*>(Q), do16, q16,
-      lse2, delta, p.Sq, ldq, nvec, p.out_dtype == FA_BF16);
-  cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(K),
-                                                     reinterpret_cast<uint4*>(k16), nk / 8);
-  cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
-                                                     reinterpret_cast<uint4*>(v16), nk / 8);
+  {
+    host::KernelTimer kt("bwd_preprocess", stream);
+    bwd_preprocess_kernel<D><<<grid_pp, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(dO), O, LSE, static_cast<const __nv_bfloat16*>(Q), do16,
+        q16, lse2, delta, p.Sq, ldq, nvec, p.out_dtype == FA_BF16);
+  }
+  {
+    host::KernelTimer kt("cvt_bf16_to_f16(K,V)", stream);
+    cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(K),
+                                                       reinterpret_cast<uint4*>(k16), nk / 8);
+    cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
+                                                       reinterpret_cast<uint4*>(v16), nk / 8);
+  }
   CUtensorMap mK, mV, mQc, mdOc, mL, mDl, mQ, mdO, mKc, mVc;
   const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const auto F32T = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -666,6 +672,8 @@ fa_status run_bwd_bf16(const void* Q, const void* K, const void* V, const void* 
     auto kern = fa_bwd_dkdv_kernel<D>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::KV_SMEM);
     if (e == cudaSuccess) {
+      host::KernelTimer kt(D == 128 ? "fa_bwd_dkdv_kernel<128,bf16>" : "fa_bwd_dkdv_kernel<64,bf16>",
+                           stream);
       kern<<<(unsigned)(BHk * ak.n_tiles), C::THREADS, C::KV_SMEM, stream>>>(mK, mV, mQc, mdOc, mL,
                                                                             mDl, ak);
       e = cudaGetLastError();
@@ -678,6 +686,8 @@ fa_status run_bwd_bf16(const void* Q, const void* K, const void* V, const void* 
     auto kern = fa_bwd_dq_kernel<D>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::Q_SMEM);
     if (e == cudaSuccess) {
+      host::KernelTimer kt(D == 128 ? "fa_bwd_dq_kernel<128,bf16>" : "fa_bwd_dq_kernel<64,bf16>",
+                           stream);
       kern<<<(unsigned)(BH * aq.n_tiles), C::THREADS, C::Q_SMEM, stream>>>(mQ, mdO, mKc, mVc, aq);
       e = cudaGetLastError();
     }

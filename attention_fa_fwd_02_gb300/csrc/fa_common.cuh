@@ -80,6 +80,21 @@ cudaError_t scratch_free(void* p, cudaStream_t s);
 
 int sm_count();
 
+// Records a CUDA event pair around the launches made during its lifetime when
+// kernel timing is enabled (fa_timing_enable); otherwise does nothing.
+class KernelTimer {
+ public:
+  KernelTimer(const char* name, cudaStream_t s);
+  ~KernelTimer();
+  KernelTimer(const KernelTimer&) = delete;
+  KernelTimer& operator=(const KernelTimer&) = delete;
+
+ private:
+  const char* name_;
+  cudaStream_t stream_;
+  cudaEvent_t start_ = nullptr;
+};
+
 }  // namespace host
 
 // Launchers implemented by the kernel translation units.

@@ -468,8 +468,11 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   bool enc = true;
   if constexpr (!F32) {
     if (host::scratch_alloc(&ws, nk * 2, stream) != cudaSuccess) return FA_ERR_CUDA;
-    cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
-                                                       static_cast<uint4*>(ws), nk / 8);
+    {
+      host::KernelTimer kt("cvt_bf16_to_f16(V)", stream);
+      cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
+                                                         static_cast<uint4*>(ws), nk / 8);
+    }
     enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, D, p.Sq, BHq, D, 64, 128);
     enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, D, p.Sk, BHk, D, 64, 128);
     enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, D, p.Sk, BHk, D, 64, 128);
@@ -485,6 +488,7 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
     float* kl = kh + nk;
     float* vth = kl + nk;
     float* vtl = vth + nvt;
+    host::KernelTimer kt("split_tf32(Q,K,V)", stream);
     split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(Q), qh, ql, nullptr,
                                                   nullptr, p.Sq, D, 0, BHq);
     split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(K), kh, kl, nullptr,
@@ -523,6 +527,9 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
                                        (int)C::SMEM_ALLOC);
   if (e == cudaSuccess) {
     const unsigned grid = (unsigned)(BHq * a.n_qgroups);
+    host::KernelTimer kt(F32 ? "fa_fwd_kernel<64,f32>"
+                             : (D == 128 ? "fa_fwd_kernel<128,bf16>" : "fa_fwd_kernel<64,bf16>"),
+                         stream);
     kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, a);
     e = cudaGetLastError();
   }

@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(PKG, "libfa.so")
 FA_F32, FA_BF16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
           4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string", "fa_version")
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string", "fa_version",
+           "fa_timing_enable", "fa_timing_read")
 
 
 class FAError(RuntimeError):
@@ -33,6 +34,10 @@ class fa_params(ctypes.Structure):
                 ("Sq", ctypes.c_int), ("Sk", ctypes.c_int), ("D", ctypes.c_int),
                 ("scale", ctypes.c_float), ("causal", ctypes.c_int), ("window", ctypes.c_int),
                 ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int)]
+
+
+class fa_kernel_time(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
 
 
 def _load(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -52,6 +57,10 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_version.argtypes = []
     lib.fa_version.restype = ctypes.c_char_p
+    lib.fa_timing_enable.argtypes = [st]
+    lib.fa_timing_enable.restype = st
+    lib.fa_timing_read.argtypes = [ctypes.POINTER(fa_kernel_time), st]
+    lib.fa_timing_read.restype = st
     return lib
 
 
@@ -87,6 +96,19 @@ def fa_bwd(Q: int, K: int, V: int, O: int, dO: int, LSE: int, dQ: int, dK: int, 
 
 def fa_device_status(stream: int) -> int:
     return lib().fa_device_status(stream)
+
+
+def fa_timing_enable(on: bool) -> int:
+    return lib().fa_timing_enable(int(bool(on)))
+
+
+def fa_timing_read() -> dict:
+    """{kernel name: (launches, total_ms)} for the launches recorded since the last read."""
+    buf = (fa_kernel_time * 64)()
+    n = lib().fa_timing_read(buf, 64)
+    if n < 0:
+        raise FAError(4, "fa_timing_read")
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(min(n, 64))}
 
 
 # ------------------------------------------------------------ torch helpers

@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention hot path (fa_fwd + fa_bwd through the C ABI).
+
+One step = one forward pass (fa_fwd) and one backward pass (fa_bwd) over one
+batch of synthetic inputs of the workload (default: causal GQA attention, bf16
+inputs, B=2 H=32 HKV=8 S=4096 D=128). Counted FLOPs follow the metric: forward
+4*B*H*vis*D, backward 2.5x that, with vis the number of visible (query, key)
+pairs per head. ``value`` is whole-job TFLOP/s with inputs resident in HBM;
+``e2e`` is the same metric with host->device copies of Q/K/V/dO and
+device->host copies of O/LSE/dQ/dK/dV inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c3]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+Under torchrun (N > 1) every rank runs its own independent problem (weak
+scaling; no collective on the data path) and rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s (H32/HKV8 S4096 D128 bf16 causal); % tensor peak"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# Algorithmic FLOPs per visible (query, key) pair per query head, per kernel:
+# forward 2 GEMMs (QK^T, PV); dK/dV kernel 4 (S^T, dP^T, dV, dK); dQ kernel 3 (S, dP, dQ).
+KERNEL_FLOPS_PER_PAIR_PER_D = {"fa_fwd_kernel": 4, "fa_bwd_dkdv_kernel": 8, "fa_bwd_dq_kernel": 6}
+# Source files whose change invalidates a committed DRAM-traffic figure.
+KERNEL_SOURCES = {"fa_fwd_kernel": ["fa_fwd.cu", "ptx.cuh", "fa_common.cuh"],
+                  "fa_bwd_dkdv_kernel": ["fa_bwd.cu", "ptx.cuh", "fa_common.cuh"],
+                  "fa_bwd_dq_kernel": ["fa_bwd.cu", "ptx.cuh", "fa_common.cuh"]}
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    except (OSError, ValueError, KeyError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(kernel_base):
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kernel_base, []):
+        with open(os.path.join(ROOT, "attention_fa_fwd_02_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_base, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            entries = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for e in entries:
+        if e.get("kernel") == kernel_base and e.get("workload") == workload:
+            if e.get("source_sha") == source_sha(kernel_base):
+                return e.get("bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def flops_for(w):
+    from attention_fa_fwd_02_gb300.workloads import visible_pairs
+    vis = visible_pairs(w)
+    fwd = 4.0 * w.B * w.H * vis * w.D
+    return fwd, 2.5 * fwd, vis
+
+
+_INPUT_CACHE = {}
+
+
+def oracle_sample(w, n_groups, batch=0):
+    """Time the oracle (fwd + bwd) on the first n_groups kv groups of one batch element."""
+    import oracle
+    from attention_fa_fwd_02_gb300.workloads import make_inputs
+    if w not in _INPUT_CACHE:
+        _INPUT_CACHE.clear()
+        _INPUT_CACHE[w] = make_inputs(w)
+    q, k, v, do = _INPUT_CACHE[w]
+    rep = w.H // w.HKV
+    hs = slice(0, n_groups * rep)
+    qs, ks, vs, dos = (q[batch:batch + 1, hs], k[batch:batch + 1, :n_groups],
+                       v[batch:batch + 1, :n_groups], do[batch:batch + 1, hs])
+    t0 = time.perf_counter()
+    oracle.attention_fwd(qs, ks, vs, w.scale, w.causal, w.window)
+    oracle.attention_bwd(qs, ks, vs, dos, w.scale, w.causal, w.window)
+    dt = time.perf_counter() - t0
+    fwd, bwd, _ = flops_for(w.with_(B=1, H=n_groups * rep, HKV=n_groups))
+    return (fwd + bwd) / dt / 1e12, dt, oracle.num_threads(), n_groups * rep
+
+
+def config_of(w, extra=None):
+    c = {"workload": w.name, "B": w.B, "H": w.H, "HKV": w.HKV, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
+         "causal": bool(w.causal), "window": w.window, "scale": w.scale, "in_dtype": w.dtype,
+         "out_dtype": "f32", "l2": "256 MiB memset between timed steps; inputs also exceed L2"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from attention_fa_fwd_02_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    # each step: one whole (batch, kv-group) slice of the workload through the oracle
+    for _ in range(args.warmup):
+        oracle_sample(w, 1)
+    vals, times = [], []
+    cores = 1
+    for _ in range(args.steps):
+        v, dt, cores, heads = oracle_sample(w, 1)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.mean(vals)
+    ms = statistics.mean(times) * 1e3
+    sample = (f"one (batch, kv-group) slice per step: {w.H // w.HKV} query heads of "
+              f"{w.B * w.H}, full sequence, fwd+bwd in fp64")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w),
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build_library()
+    from attention_fa_fwd_02_gb300 import fa
+    from attention_fa_fwd_02_gb300.workloads import WORKLOADS, make_inputs
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    wr = w.with_(seed=w.seed + 7919 * rank)  # independent problem per rank
+    q, k, v, do = make_inputs(wr)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    p = fa.make_params(qd, kd, w.scale, w.causal, w.window)
+    o = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    sh = int(stream.cuda_stream)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        rc = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(), p, sh)
+        if rc:
+            raise fa.FAError(rc, "fa_fwd")
+        rc = fa.fa_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), dod.data_ptr(),
+                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), p, sh)
+        if rc:
+            raise fa.FAError(rc, "fa_bwd")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    fa.check_device_status()
+
+    # ---- device-resident timed region
+    sampler = ClockSampler() if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    fa.fa_timing_enable(True)
+    for s, e in ev:
+        flush.zero_()
+        s.record(stream)
+        step()
+        e.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    kernels = fa.fa_timing_read()
+    fa.fa_timing_enable(False)
+    clocks = sampler.stop() if sampler else None
+    fa.check_device_status()
+    ms = statistics.mean(s.elapsed_time(e) for s, e in ev)
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    hdq = torch.empty(dq.shape, dtype=dq.dtype, pin_memory=True)
+    hdk = torch.empty(dk.shape, dtype=dk.dtype, pin_memory=True)
+    hdv = torch.empty(dv.shape, dtype=dv.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+
+    def e2e_step():
+        for dst, src in ((qd, hq), (kd, hk), (vd, hv), (dod, hdo)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in ((ho, o), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for s, e in ev2:
+        s.record(stream)
+        e2e_step()
+        e.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    fa.check_device_status()
+    ms_e2e = statistics.mean(s.elapsed_time(e) for s, e in ev2)
+    if dist is not None:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    fwd_fl, bwd_fl, vis = flops_for(w)
+    value = world * (fwd_fl + bwd_fl) / (ms_max * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops_sustained"] if w.dtype == "bf16" else peaks["bf16_tflops_sustained"] / 2
+    per_kernel = {}
+    fwd_ms = bwd_ms = 0.0
+    launches = 0
+    for name, (n, tot) in kernels.items():
+        launches += n
+        base = name.split("<")[0]
+        entry = {"launches": n, "ms_per_launch": tot / n}
+        if base in KERNEL_FLOPS_PER_PAIR_PER_D:
+            fl = KERNEL_FLOPS_PER_PAIR_PER_D[base] * w.B * w.H * vis * w.D
+            entry["tflops"] = fl / (tot / n * 1e-3) / 1e12
+        per_kernel[name] = entry
+        if base.startswith("fa_fwd") or "(V)" in name or "split" in name:
+            fwd_ms += tot / n
+        else:
+            bwd_ms += tot / n
+    dom = max((k_ for k_ in per_kernel if "tflops" in per_kernel[k_]),
+              key=lambda k_: per_kernel[k_]["launches"] * per_kernel[k_]["ms_per_launch"])
+    dom_base = dom.split("<")[0]
+    achieved = per_kernel[dom]["tflops"]
+    traffic = committed_traffic(dom_base, args.workload)
+    cpu = None
+    if not args.no_cpu_baseline:
+        groups = min(4, w.HKV) if args.workload in ("c3", "c4") else w.HKV
+        cv, cdt, cores, heads = oracle_sample(w, groups)
+        cpu = {"value": round(cv, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": (f"batch 0, kv groups 0..{groups - 1} ({heads} of {w.B * w.H} query "
+                          f"heads, full sequence), fwd+bwd in fp64, {cdt:.1f} s")}
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic", "config": config_of(w),
+        "fwd_tflops": round(fwd_fl / (fwd_ms * 1e-3) / 1e12, 3) if fwd_ms else None,
+        "bwd_tflops": round(bwd_fl / (bwd_ms * 1e-3) / 1e12, 3) if bwd_ms else None,
+        "pct_tensor_peak": round(100 * value / world / peak, 2),
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 sustained (MEASURED_PEAKS.json)"
+                     if peak_src == "measured" else "fallback 1.7 PFLOP/s sustained"},
+        "kernels": {k_: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
+                         for kk, vv in e.items()} for k_, e in per_kernel.items()},
+        "e2e": {"value": round(world * (fwd_fl + bwd_fl) / (ms_e2e * 1e-3) / 1e12, 3),
+                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c3", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = _env_int("RANK", 0)
+    world = _env_int("WORLD_SIZE", 1)
+    local_rank = _env_int("LOCAL_RANK", 0)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

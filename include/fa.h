@@ -127,6 +127,25 @@ FA_API const char* fa_status_string(fa_status s);
 /* Library version string, e.g. "fa-sm103a 0.1". */
 FA_API const char* fa_version(void);
 
+/*
+ * Kernel timing (a measurement aid; no counterpart on the source pages).
+ * fa_timing_enable(1) makes every later fa_fwd / fa_bwd call record a CUDA event
+ * pair around each kernel it launches, on the caller's stream; fa_timing_enable(0)
+ * stops recording and discards what was recorded. fa_timing_read() waits for the
+ * recorded events, aggregates them per kernel name into out[0..max_entries) and
+ * forgets them; it returns the number of distinct kernels (which may exceed
+ * max_entries), or -1 on a CUDA error. Names are static strings owned by the
+ * library. Not thread-safe with respect to concurrent fa_* calls on other threads.
+ */
+typedef struct {
+  const char* name;  /* kernel name, e.g. "fa_fwd_kernel<128,bf16>" */
+  int launches;      /* launches recorded since the last read */
+  double total_ms;   /* sum of their event-measured durations */
+} fa_kernel_time;
+
+FA_API fa_status fa_timing_enable(int on);
+FA_API int fa_timing_read(fa_kernel_time* out, int max_entries);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,7 @@ def _declared_symbols():
 
 def test_header_declares_the_abi():
     assert _declared_symbols() == {"fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string",
-                                   "fa_version"}
+                                   "fa_version", "fa_timing_enable", "fa_timing_read"}
 
 
 def test_library_exports_every_declared_symbol(fa):
@@ -37,6 +37,12 @@ def test_library_exports_every_declared_symbol(fa):
     assert _declared_symbols() <= exported
     # hidden visibility: nothing but the ABI leaks out of the library
     assert exported == _declared_symbols()
+
+
+def test_timing_read_empty(fa):
+    # nothing recorded: no CUDA call needed, zero kernels reported
+    assert fa.fa_timing_enable(False) == 0
+    assert fa.fa_timing_read() == {}
 
 
 def test_status_strings(fa):
