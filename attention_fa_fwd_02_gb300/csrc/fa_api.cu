@@ -191,6 +191,20 @@ FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, fl
   return launch_fwd(Q, K, V, O, LSE, normalized(*p), reinterpret_cast<cudaStream_t>(stream));
 }
 
+FA_API fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                const fa_params* p, fa_stream_t stream) {
+  fa_status st = validate(p);
+  if (st != FA_OK) return st;
+  if (p->Sq == 0) return FA_OK;
+  st = check_ptrs({O, LSE, Q});
+  if (st != FA_OK) return st;
+  if (p->Sk > 0) {
+    st = check_ptrs({K, V});
+    if (st != FA_OK) return st;
+  }
+  return launch_fwd_noalloc(Q, K, V, O, LSE, normalized(*p), reinterpret_cast<cudaStream_t>(stream));
+}
+
 FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O,
                         const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
                         const fa_params* p, fa_stream_t stream) {
@@ -226,6 +240,7 @@ FA_API const char* fa_status_string(fa_status s) {
     case FA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_TIMEOUT: return "kernel barrier wait timed out";
+    case FA_ERR_SCRATCH_LIMIT: return "problem needs more than the static scratch of fa_fwd_noalloc";
   }
   return "unknown status";
 }

@@ -103,6 +103,8 @@ fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float
 fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                      const float* LSE, void* dQ, void* dK, void* dV, const fa_params& p,
                      cudaStream_t stream);
+fa_status launch_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                             const fa_params& p, cudaStream_t stream);
 unsigned int read_and_clear_fwd_status(cudaError_t* err);
 unsigned int read_and_clear_bwd_status(cudaError_t* err);
 

@@ -19,6 +19,7 @@
 #include <cfloat>
 #include <climits>
 #include <cstdio>
+#include <mutex>
 #include "fa_common.cuh"
 #include "ptx.cuh"
 #include "fa_prepass.cuh"
@@ -552,6 +553,139 @@ fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float
     if (p.D == 64) return run_fwd<64, false>(Q, K, V, O, LSE, p, stream);
   } else {
     if (p.D == 64) return run_fwd<64, true>(Q, K, V, O, LSE, p, stream);
+  }
+  return FA_ERR_UNSUPPORTED;
+}
+
+// ------------------------------------------------- forward without allocation
+// fa_fwd_noalloc runs the same kernels as fa_fwd, but the temporary operand
+// copies live in this file-scope device array instead of the library's memory
+// pool, so the call itself never allocates device memory. Every GPU that loads
+// the library holds these bytes until the process exits.
+static __device__ __align__(256) uint8_t g_fwd_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[NOALLOC_MAX_DEVICES] = {};
+
+// Device address of the array on the current device. The symbol's host-side name
+// is only a stand-in; the address is looked up once per device, with that device
+// current, and cached.
+fa_status noalloc_scratch_addr(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES)
+    return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fwd_noalloc_scratch) != cudaSuccess || !ptr)
+      return FA_ERR_CUDA;
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = g_noalloc_addr[dev];
+  return FA_OK;
+}
+
+template <int D, bool F32>
+size_t noalloc_bytes(const fa_params& p) {
+  const size_t nq = (size_t)p.B * p.H * p.Sq * D;
+  const size_t nk = (size_t)p.B * p.HKV * p.Sk * D;
+  if constexpr (!F32) {
+    return nk * 2;
+  } else {
+    const size_t ldt = ((size_t)p.Sk + 3) / 4 * 4;
+    const size_t nvt = (size_t)p.B * p.HKV * D * ldt;
+    return (2 * nq + 2 * nk + 2 * nvt) * 4;
+  }
+}
+
+template <int D, bool F32>
+fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                          const fa_params& p, cudaStream_t stream) {
+  using C = FwdCfg<D, F32>;
+  if (noalloc_bytes<D, F32>(p) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+  void* ws = nullptr;
+  const fa_status st = noalloc_scratch_addr(&ws);
+  if (st != FA_OK) return st;
+  const size_t nq = (size_t)p.B * p.H * p.Sq * D;
+  const size_t nk = (size_t)p.B * p.HKV * p.Sk * D;
+  const int grid_pp = 4 * host::sm_count();
+  CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo;
+  const uint64_t BHq = (uint64_t)p.B * p.H, BHk = (uint64_t)p.B * p.HKV;
+  bool enc = true;
+  // The whole scratch region used below is rewritten by the pre-pass kernels on
+  // every call, so nothing left over from an earlier call is ever read.
+  if constexpr (!F32) {
+    cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
+                                                       static_cast<uint4*>(ws), nk / 8);
+    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, D, p.Sq, BHq, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, D, p.Sk, BHk, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, D, p.Sk, BHk, D, 64, 128);
+    mQlo = mQ; mKlo = mK; mVlo = mV;
+  } else {
+    const int ldt = (p.Sk + 3) / 4 * 4;
+    const size_t nvt = (size_t)p.B * p.HKV * D * ldt;
+    float* qh = static_cast<float*>(ws);
+    float* ql = qh + nq;
+    float* kh = ql + nq;
+    float* kl = kh + nk;
+    float* vth = kl + nk;
+    float* vtl = vth + nvt;
+    split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(Q), qh, ql, nullptr,
+                                                  nullptr, p.Sq, D, 0, BHq);
+    split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(K), kh, kl, nullptr,
+                                                  nullptr, p.Sk, D, 0, BHk);
+    split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(V), nullptr, nullptr,
+                                                  vth, vtl, p.Sk, D, ldt, BHk);
+    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, qh, D, p.Sq, BHq, D, 32, 128);
+    enc &= host::encode_tiled_3d(&mQlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ql, D, p.Sq, BHq, D, 32, 128);
+    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kh, D, p.Sk, BHk, D, 32, 128);
+    enc &= host::encode_tiled_3d(&mKlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kl, D, p.Sk, BHk, D, 32, 128);
+    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, vth, p.Sk, D, BHk, ldt, 32, D);
+    enc &= host::encode_tiled_3d(&mVlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, vtl, p.Sk, D, BHk, ldt, 32, D);
+  }
+  if (!enc || cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  FwdArgs a;
+  a.O = O;
+  a.LSE = LSE;
+  a.H = p.H;
+  a.HKV = p.HKV;
+  a.Sq = p.Sq;
+  a.Sk = p.Sk;
+  a.scale_log2 = p.scale * LOG2E;
+  a.causal = p.causal;
+  a.window = p.window;
+  a.out_bf16 = p.out_dtype == FA_BF16;
+  a.n_qgroups = (p.Sq + BLOCK_M * C::NQ - 1) / (BLOCK_M * C::NQ);
+  a.lpt = p.causal ? 1 : 0;
+  a.BH = (int)BHq;
+  a.limit_ns = WAIT_LIMIT_NS;
+  auto kern = fa_fwd_kernel<D, F32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)C::SMEM_ALLOC);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  kern<<<(unsigned)(BHq * a.n_qgroups), C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo,
+                                                                            mV, mVlo, a);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+fa_status launch_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                             const fa_params& p, cudaStream_t stream) {
+  if (p.Sk == 0) {  // no key at all: no scratch needed
+    const size_t rows = (size_t)p.B * p.H * p.Sq;
+    fill_empty_kernel<<<4 * host::sm_count(), 256, 0, stream>>>(O, LSE, rows, p.D,
+                                                                p.out_dtype == FA_BF16);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+  if (p.in_dtype == FA_BF16) {
+    if (p.D == 128) return run_fwd_noalloc<128, false>(Q, K, V, O, LSE, p, stream);
+    if (p.D == 64) return run_fwd_noalloc<64, false>(Q, K, V, O, LSE, p, stream);
+  } else {
+    if (p.D == 64) return run_fwd_noalloc<64, true>(Q, K, V, O, LSE, p, stream);
   }
   return FA_ERR_UNSUPPORTED;
 }

@@ -18,9 +18,11 @@ LIB_PATH = os.path.join(PKG, "libfa.so")
 
 FA_F32, FA_BF16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
-          4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
+          4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_SCRATCH_LIMIT"}
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string", "fa_version",
-           "fa_timing_enable", "fa_timing_read")
+           "fa_timing_enable", "fa_timing_read", "fa_fwd_noalloc")
+# Size of the static device scratch behind fa_fwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class FAError(RuntimeError):
@@ -49,6 +51,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     P = ctypes.POINTER(fa_params)
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, P, vp]
     lib.fa_fwd.restype = st
+    lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, P, vp]
+    lib.fa_fwd_noalloc.restype = st
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, P, vp]
     lib.fa_bwd.restype = st
     lib.fa_device_status.argtypes = [vp]
@@ -86,6 +90,13 @@ def version() -> str:
 def fa_fwd(Q: int, K: int, V: int, O: int, LSE: int, params: fa_params, stream: int) -> int:
     """Direct call of the C ``fa_fwd`` with integer device addresses; returns the status."""
     return lib().fa_fwd(Q, K, V, O, LSE, ctypes.byref(params), stream)
+
+
+def fa_fwd_noalloc(Q: int, K: int, V: int, O: int, LSE: int, params: fa_params,
+                   stream: int) -> int:
+    """Direct call of the C ``fa_fwd_noalloc`` (same contract as ``fa_fwd``, but its
+    scratch is the library's static device array, so it never allocates)."""
+    return lib().fa_fwd_noalloc(Q, K, V, O, LSE, ctypes.byref(params), stream)
 
 
 def fa_bwd(Q: int, K: int, V: int, O: int, dO: int, LSE: int, dQ: int, dK: int, dV: int,

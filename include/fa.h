@@ -74,7 +74,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (head dim, dtype pair) */
   FA_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
   FA_ERR_CUDA = 4,        /* a CUDA runtime / driver call or a kernel launch failed */
-  FA_ERR_TIMEOUT = 5      /* a kernel gave up waiting on an internal barrier (device status) */
+  FA_ERR_TIMEOUT = 5,     /* a kernel gave up waiting on an internal barrier (device status) */
+  FA_ERR_SCRATCH_LIMIT = 6 /* fa_fwd_noalloc: the problem needs more than FA_NOALLOC_SCRATCH_BYTES */
 } fa_status;
 
 /*
@@ -96,6 +97,37 @@ typedef enum {
  */
 FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                  const fa_params* p, fa_stream_t stream);
+
+/*
+ * Forward pass that never allocates device memory (no counterpart on the source
+ * pages; an addition for callers that cannot allocate).
+ *
+ * fa_fwd takes its temporary buffers from a memory pool that the library grows
+ * on demand. Some callers cannot let a library do that: runtimes that allocate
+ * everything up front and must keep a fixed device-memory footprint afterwards
+ * (real-time or safety-certified inference), hosts whose own allocator owns the
+ * whole device and would be starved or fragmented by a second pool, and code
+ * that runs where a cudaMalloc is not allowed or would block on a lock. For them
+ * this entry point computes exactly what fa_fwd computes, with the same
+ * arguments, rules and errors, but its scratch (the fp16 copy of V for bf16
+ * inputs; the tf32 hi/lo splits of Q, K, V for fp32 inputs) lives in a
+ * file-scope device array of FA_NOALLOC_SCRATCH_BYTES inside libfa.so. Every GPU
+ * on which the library is loaded holds that array until the process exits.
+ *   - A problem whose scratch would not fit returns FA_ERR_SCRATCH_LIMIT before
+ *     anything is enqueued: bf16 inputs need B*HKV*Sk*D*2 bytes; fp32 inputs
+ *     need 4*(2*B*H*Sq*D + 2*B*HKV*Sk*D + 2*B*HKV*D*round_up(Sk,4)) bytes.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture begins.
+ *   - All calls on a device share the one array. Each call rewrites the part it
+ *     uses before reading it, but two calls whose work overlaps on the GPU (on
+ *     different streams, without ordering between them) race on it and give
+ *     undefined results: order such calls on one stream or with events.
+ *   - It makes no cudaMalloc, cudaFree or other allocating call.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((unsigned long long)32 << 20)
+FA_API fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                const fa_params* p, fa_stream_t stream);
 
 /*
  * Backward pass for the loss L with upstream gradient dO = dL/dO.

@@ -25,7 +25,8 @@ def _declared_symbols():
 
 def test_header_declares_the_abi():
     assert _declared_symbols() == {"fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string",
-                                   "fa_version", "fa_timing_enable", "fa_timing_read"}
+                                   "fa_version", "fa_timing_enable", "fa_timing_read",
+                                   "fa_fwd_noalloc"}
 
 
 def test_library_exports_every_declared_symbol(fa):
@@ -47,7 +48,7 @@ def test_timing_read_empty(fa):
 
 def test_status_strings(fa):
     assert fa.status_string(0) == "ok"
-    for code in range(1, 6):
+    for code in range(1, 7):
         assert fa.status_string(code) and fa.status_string(code) != "unknown status"
     assert fa.status_string(99) == "unknown status"
     assert fa.version().startswith("fa-sm103a")
