@@ -8,16 +8,19 @@
 // group, without atomics (deterministic); dQ is accumulated per query row.
 //
 // Kernels:
-//   preprocess   one warp per query row: D_i, the log2-domain LSE (+inf for rows
-//                that saw no key, so their P is exactly 0), fp16 copies of Q, dO.
-//   dkdv         one CTA per (batch, kv head, 128-key tile). It walks 64-query
+//   preprocess   D_i, the log2-domain LSE (+inf for rows that saw no key, so their
+//                P is exactly 0) and the tensor-core operand copies: fp16 for bf16
+//                inputs; tf32 hi / lo splits (plus transposed copies of Q, K, dO,
+//                since tf32 operands must be K-major) for fp32 inputs.
+//   dkdv         one CTA per (batch, kv head, 128-key tile). It walks CH-query
 //                chunks of every grouped query head that can see the tile:
 //                S^T = K Q^T and dP^T = V dO^T into a double-buffered TMEM slot,
-//                softmax warps turn them into P^T and dS^T (fp16, back into TMEM),
+//                softmax warps turn them into P^T and dS^T (back into TMEM),
 //                then dV += P^T dO and dK += dS^T Q accumulate in TMEM.
-//   dq           one CTA per (batch, head, 128-query tile), 64-key chunks:
+//   dq           one CTA per (batch, head, 128-query tile), CH-key chunks:
 //                S = Q K^T, dP = dO V^T, dS = P (dP - D), dQ += dS K.
 // While the softmax warps work on chunk c, the tensor core computes chunk c+1.
+// For fp32 inputs every product is the 3xTF32 sum a_hi b_hi + a_hi b_lo + a_lo b_hi.
 #include <cfloat>
 #include <climits>
 #include "fa_common.cuh"
@@ -44,54 +47,107 @@ struct BwdArgs {
   unsigned long long limit_ns;
 };
 
-template <int D_>
+// Tensor maps of one kernel launch; index [split] selects the hi (0) / lo (1) copy.
+struct KVMaps {  // dkdv
+  CUtensorMap K[2], V[2], Qc[2], dOc[2], Qt[2], dOt[2], L, Dl;
+};
+struct QMaps {  // dq
+  CUtensorMap Q[2], dO[2], Kc[2], Vc[2], Kt[2];
+};
+
+template <int D_, bool F32_>
 struct BwdCfg {
   static constexpr int D = D_;
-  static constexpr int CH = 64;                        // rows per streamed chunk
-  static constexpr int NCB = D / 64;                   // 128-byte column blocks (fp16)
-  static constexpr uint32_t BIG_CB = 128u * 128u;      // column block of a 128-row tile
-  static constexpr uint32_t SMALL_CB = 64u * 128u;     // column block of a 64-row chunk
+  static constexpr bool F32 = F32_;
+  static constexpr int ESZ = F32 ? 4 : 2;
+  static constexpr int ROW = 128 / ESZ;                 // elements per 128-byte row
+  static constexpr int NCB = D / ROW;                   // 128-byte column blocks per row
+  static constexpr int CH = F32 ? 32 : 64;              // rows per streamed chunk
+  static constexpr int NSPLIT = F32 ? 2 : 1;
+  static constexpr uint32_t BIG_CB = 128u * 128u;       // column block of a 128-row tile
+  static constexpr uint32_t SMALL_CB = CH * 128u;       // column block of a CH-row chunk
   static constexpr uint32_t BIG_TILE = NCB * BIG_CB;
   static constexpr uint32_t SMALL_TILE = NCB * SMALL_CB;
-  static constexpr int NST = 4;                        // chunk ring depth
-  // dkdv smem: K | V | NST x (Q chunk, dO chunk) | NST x (lse2[64], delta[64])
-  static constexpr uint32_t KV_CH_OFF = 2 * BIG_TILE;
-  static constexpr uint32_t KV_VEC_OFF = KV_CH_OFF + NST * 2 * SMALL_TILE;
-  static constexpr uint32_t KV_SMEM = KV_VEC_OFF + NST * 512 + 1024;
-  // dq smem: Q | dO | NST x (K chunk, V chunk)
-  static constexpr uint32_t Q_CH_OFF = 2 * BIG_TILE;
-  static constexpr uint32_t Q_SMEM = Q_CH_OFF + NST * 2 * SMALL_TILE + 1024;
+  static constexpr uint32_t T_TILE = F32 ? D * 128u : 0u;  // transposed chunk: D rows x 32 fp32
+  static constexpr uint32_t VEC_STAGE = 2 * CH * 4;        // lse2 + delta of one chunk
+  // dkdv smem: K, V (hi[, lo]) | KV_NST x chunk (Q, dO [, Q^T, dO^T]) | KV_NST x vectors
+  static constexpr int KV_NST = F32 ? 1 : 4;
+  static constexpr uint32_t KV_RES = 2 * NSPLIT * BIG_TILE;
+  static constexpr uint32_t KV_STAGE = NSPLIT * (2 * SMALL_TILE + 2 * T_TILE);
+  static constexpr uint32_t KV_VEC_OFF = KV_RES + KV_NST * KV_STAGE;
+  static constexpr uint32_t KV_SMEM = KV_VEC_OFF + KV_NST * VEC_STAGE + 1024;
+  // dq smem: Q, dO (hi[, lo]) | Q_NST x chunk (K, V [, K^T])
+  static constexpr int Q_NST = F32 ? 2 : 4;
+  static constexpr uint32_t Q_RES = 2 * NSPLIT * BIG_TILE;
+  static constexpr uint32_t Q_STAGE = NSPLIT * (2 * SMALL_TILE + T_TILE);
+  static constexpr uint32_t Q_SMEM = Q_RES + Q_NST * Q_STAGE + 1024;
   static constexpr int THREADS = 192;  // 4 softmax warps, MMA warp, TMA warp
   static constexpr int MMA_WARP = 4, TMA_WARP = 5;
   static constexpr uint32_t TMEM_COLS = 512;
+  // TMEM slot b (b = 0, 1): S | dP | P_lo | dS_lo, CH columns each (fp32 P / dS hi
+  // overwrite S / dP; fp16 P / dS take the first CH/2 columns of S / dP).
   __host__ __device__ static constexpr uint32_t s_col(int b) { return 128u * b; }
-  __host__ __device__ static constexpr uint32_t dp_col(int b) { return 128u * b + 64u; }
-  static constexpr uint32_t ACC0 = 256;  // dV (dkdv) / dQ (dq)
+  __host__ __device__ static constexpr uint32_t dp_col(int b) { return 128u * b + CH; }
+  __host__ __device__ static constexpr uint32_t plo_col(int b) { return 128u * b + 2 * CH; }
+  __host__ __device__ static constexpr uint32_t dslo_col(int b) { return 128u * b + 3 * CH; }
+  static constexpr uint32_t ACC0 = 256;      // dV (dkdv) / dQ (dq)
   static constexpr uint32_t ACC1 = 256 + D;  // dK (dkdv)
   static_assert(KV_SMEM <= 227u * 1024u && Q_SMEM <= 227u * 1024u, "shared memory budget");
+  static_assert((F32 ? 4 * CH : 2 * CH) <= 128, "TMEM slot width");
+  static_assert(256 + 2 * D <= 512, "TMEM budget");
 };
 
-// S (+)= A[128 x D] * B[64 x D]^T, both K-major fp16 in 128B-swizzled smem.
+// S (+)= A[128 x D] * B[CH x D]^T, both K-major in 128B-swizzled smem.
 template <class C>
-__device__ __forceinline__ void issue_rowdot(uint32_t d_tmem, uint32_t sa, uint32_t sb) {
-  constexpr uint32_t id = make_idesc(128, 64, FMT_F16, FMT_F16, false, false);
+__device__ __forceinline__ void issue_rowdot(uint32_t d, uint32_t a, uint32_t a_lo, uint32_t b,
+                                             uint32_t b_lo) {
+  if constexpr (!C::F32) {
+    constexpr uint32_t id = make_idesc(128, C::CH, FMT_F16, FMT_F16, false, false);
 #pragma unroll
-  for (int kk = 0; kk < C::D / 16; ++kk) {
-    const uint32_t cb = kk * 16 / 64, in = (kk * 16 % 64) * 2;
-    mma_f16_ss(d_tmem, make_sdesc(sa + cb * C::BIG_CB + in, 16, SW128_ATOM),
-               make_sdesc(sb + cb * C::SMALL_CB + in, 16, SW128_ATOM), id, kk > 0);
+    for (int kk = 0; kk < C::D / 16; ++kk) {
+      const uint32_t cb = kk * 16 / 64, in = (kk * 16 % 64) * 2;
+      mma_f16_ss(d, make_sdesc(a + cb * C::BIG_CB + in, 16, SW128_ATOM),
+                 make_sdesc(b + cb * C::SMALL_CB + in, 16, SW128_ATOM), id, kk > 0);
+    }
+  } else {
+    constexpr uint32_t id = make_idesc(128, C::CH, FMT_TF32, FMT_TF32, false, false);
+#pragma unroll
+    for (int kk = 0; kk < C::D / 8; ++kk) {
+      const uint32_t cb = kk * 8 / 32, in = (kk * 8 % 32) * 4;
+      const uint64_t ah = make_sdesc(a + cb * C::BIG_CB + in, 16, SW128_ATOM);
+      const uint64_t al = make_sdesc(a_lo + cb * C::BIG_CB + in, 16, SW128_ATOM);
+      const uint64_t bh = make_sdesc(b + cb * C::SMALL_CB + in, 16, SW128_ATOM);
+      const uint64_t bl = make_sdesc(b_lo + cb * C::SMALL_CB + in, 16, SW128_ATOM);
+      mma_tf32_ss(d, ah, bh, id, kk > 0);
+      mma_tf32_ss(d, ah, bl, id, 1);
+      mma_tf32_ss(d, al, bh, id, 1);
+    }
   }
 }
 
-// ACC[128 x D] (+)= A(TMEM, fp16, 128 x 64) * B[64 x D] (smem, MN-major fp16 chunk).
+// ACC[128 x D] (+)= A(TMEM, 128 x CH) * B[CH x D]. fp16: B is the MN-major chunk
+// [CH rows][D]; tf32: B is the K-major transposed chunk [D rows][CH].
 template <class C>
-__device__ __forceinline__ void issue_acc(uint32_t acc_tmem, uint32_t a_tmem, uint32_t sb,
-                                          bool accumulate) {
-  constexpr uint32_t id = make_idesc(128, C::D, FMT_F16, FMT_F16, false, true);
+__device__ __forceinline__ void issue_acc(uint32_t acc, uint32_t a_tmem, uint32_t alo_tmem,
+                                          uint32_t b, uint32_t b_lo, bool accumulate) {
+  if constexpr (!C::F32) {
+    constexpr uint32_t id = make_idesc(128, C::D, FMT_F16, FMT_F16, false, true);
 #pragma unroll
-  for (int kk = 0; kk < C::CH / 16; ++kk)
-    mma_f16_ts(acc_tmem, a_tmem + kk * 8, make_sdesc(sb + kk * 16 * 128, C::SMALL_CB, SW128_ATOM),
-               id, (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < C::CH / 16; ++kk)
+      mma_f16_ts(acc, a_tmem + kk * 8, make_sdesc(b + kk * 16 * 128, C::SMALL_CB, SW128_ATOM), id,
+                 (accumulate || kk > 0) ? 1u : 0u);
+  } else {
+    constexpr uint32_t id = make_idesc(128, C::D, FMT_TF32, FMT_TF32, false, false);
+#pragma unroll
+    for (int kk = 0; kk < C::CH / 8; ++kk) {
+      const uint32_t in = (kk * 8 % 32) * 4;
+      const uint64_t bh = make_sdesc(b + in, 16, SW128_ATOM);
+      const uint64_t bl = make_sdesc(b_lo + in, 16, SW128_ATOM);
+      mma_tf32_ts(acc, a_tmem + kk * 8, bh, id, (accumulate || kk > 0) ? 1u : 0u);
+      mma_tf32_ts(acc, a_tmem + kk * 8, bl, id, 1);
+      mma_tf32_ts(acc, alo_tmem + kk * 8, bh, id, 1);
+    }
+  }
 }
 
 __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit) {
@@ -127,19 +183,59 @@ __device__ __forceinline__ void store_row32(void* base, size_t elem_off, const u
   }
 }
 
+// Load CH fp32 columns of this thread's TMEM lane.
+template <int CH>
+__device__ __forceinline__ void tmem_ld_row(uint32_t addr, float (&x)[CH]) {
+#pragma unroll
+  for (int c = 0; c < CH / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(addr + c * 32, r);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) x[c * 32 + k] = __uint_as_float(r[k]);
+  }
+}
+
+// Write probabilities / score gradients back into TMEM as the A operand of the
+// accumulating MMAs: fp16 pairs into the first CH/2 columns at `hi`, or tf32
+// hi (at `hi`) and lo (at `lo`) parts, one column each.
+template <class C>
+__device__ __forceinline__ void tmem_st_operand(uint32_t hi, uint32_t lo, const float (&x)[C::CH]) {
+  if constexpr (!C::F32) {
+#pragma unroll
+    for (int c = 0; c < C::CH / 64; ++c) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) pk[k] = pack_half2(x[c * 64 + 2 * k], x[c * 64 + 2 * k + 1]);
+      tmem_st32(hi + c * 32, pk);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < C::CH / 32; ++c) {
+      uint32_t ph[32], pl[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float v = x[c * 32 + k];
+        const uint32_t hb = __float_as_uint(v) & 0xFFFFE000u;
+        ph[k] = hb;
+        pl[k] = __float_as_uint(v - __uint_as_float(hb));
+      }
+      tmem_st32(hi + c * 32, ph);
+      tmem_st32(lo + c * 32, pl);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ dK / dV
-template <int D>
-__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
-    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmQc, const __grid_constant__ CUtensorMap tmdOc,
-                       const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmDl,
-                       const BwdArgs a) {
-  using C = BwdCfg<D>;
+template <int D, bool F32>
+__global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ KVMaps m, const BwdArgs a) {
+  using C = BwdCfg<D, F32>;
+  constexpr int CH = C::CH, NST = C::KV_NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_kv, bar_full[C::NST], bar_empty[C::NST], bar_sp[2],
-      bar_ds[2], bar_done, bar_drain;
+  __shared__ __align__(8) uint64_t bar_kv, bar_full[NST], bar_empty[NST], bar_sp[2], bar_ds[2],
+      bar_done, bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int warp = warp_id(), lane = lane_id();
@@ -160,14 +256,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (lim < imax) imax = (int)lim;
     }
     if (imax < imin) { qc_lo = 0; qc_hi = 0; }
-    else { qc_lo = imin / C::CH; qc_hi = imax / C::CH + 1; }
+    else { qc_lo = imin / CH; qc_hi = imax / CH + 1; }
   }
   const int ncq = qc_hi - qc_lo;
   const int nc = rep * ncq;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_kv, 1);
-    for (int s = 0; s < C::NST; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
+    for (int s = 0; s < NST; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&bar_sp[s], 1); mbar_init(&bar_ds[s], 128); }
     mbar_init(&bar_done, 1);
     mbar_init(&bar_drain, 1);
@@ -184,67 +280,103 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sK = sbase, sV = sbase + C::BIG_TILE;
-  auto sQc = [&](int st) { return sbase + C::KV_CH_OFF + st * 2 * C::SMALL_TILE; };
-  auto sdOc = [&](int st) { return sbase + C::KV_CH_OFF + st * 2 * C::SMALL_TILE + C::SMALL_TILE; };
-  float* vecs = reinterpret_cast<float*>(smem + C::KV_VEC_OFF);  // [NST][2][64]
+  auto sK = [&](int sp) { return sbase + sp * C::BIG_TILE; };
+  auto sV = [&](int sp) { return sbase + (C::NSPLIT + sp) * C::BIG_TILE; };
+  auto stage = [&](int st) { return sbase + C::KV_RES + st * C::KV_STAGE; };
+  auto sQc = [&](int st, int sp) { return stage(st) + sp * C::SMALL_TILE; };
+  auto sdOc = [&](int st, int sp) { return stage(st) + (C::NSPLIT + sp) * C::SMALL_TILE; };
+  auto sQt = [&](int st, int sp) { return stage(st) + 2 * C::NSPLIT * C::SMALL_TILE + sp * C::T_TILE; };
+  auto sdOt = [&](int st, int sp) {
+    return stage(st) + 2 * C::NSPLIT * C::SMALL_TILE + (C::NSPLIT + sp) * C::T_TILE;
+  };
+  float* vecs = reinterpret_cast<float*>(smem + C::KV_VEC_OFF);  // [NST][2][CH]
+  auto gen = [&](uint32_t s) { return smem + (s - sbase); };
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
   };
   auto chunk_rows = [&](int c, int* bh, int* i0) {
     const int r = c / ncq, qc = qc_lo + c % ncq;
     *bh = b * a.H + g * rep + r;
-    *i0 = qc * C::CH;
+    *i0 = qc * CH;
   };
 
   if (warp == C::TMA_WARP) {
     if (lane == 0 && nc > 0) {
-      tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmQc); tma_prefetch_desc(&tmdOc);
-      mbar_arrive_expect_tx(&bar_kv, 2 * C::BIG_TILE);
-      for (int cb = 0; cb < C::NCB; ++cb) {
-        tma_load_3d(smem + cb * C::BIG_CB, &tmK, &bar_kv, cb * 64, j0, bg);
-        tma_load_3d(smem + C::BIG_TILE + cb * C::BIG_CB, &tmV, &bar_kv, cb * 64, j0, bg);
-      }
-      int last[C::NST];
-      for (int s = 0; s < C::NST; ++s) last[s] = -1;
+      tma_prefetch_desc(&m.K[0]); tma_prefetch_desc(&m.Qc[0]); tma_prefetch_desc(&m.dOc[0]);
+      mbar_arrive_expect_tx(&bar_kv, 2 * C::NSPLIT * C::BIG_TILE);
+      for (int sp = 0; sp < C::NSPLIT; ++sp)
+        for (int cb = 0; cb < C::NCB; ++cb) {
+          tma_load_3d(gen(sK(sp)) + cb * C::BIG_CB, &m.K[sp], &bar_kv, cb * C::ROW, j0, bg);
+          tma_load_3d(gen(sV(sp)) + cb * C::BIG_CB, &m.V[sp], &bar_kv, cb * C::ROW, j0, bg);
+        }
+      int last[NST];
+      for (int s = 0; s < NST; ++s) last[s] = -1;
       for (int c = 0; c < nc; ++c) {
-        const int st = c % C::NST;
-        if (!wait(&bar_empty[st], ((c / C::NST) & 1) ^ 1)) break;
+        const int st = c % NST;
+        if (!wait(&bar_empty[st], ((c / NST) & 1) ^ 1)) break;
         int bh, i0;
         chunk_rows(c, &bh, &i0);
-        mbar_arrive_expect_tx(&bar_full[st], 2 * C::SMALL_TILE + 512);
-        for (int cb = 0; cb < C::NCB; ++cb) {
-          tma_load_3d(smem + (sQc(st) - sbase) + cb * C::SMALL_CB, &tmQc, &bar_full[st], cb * 64, i0, bh);
-          tma_load_3d(smem + (sdOc(st) - sbase) + cb * C::SMALL_CB, &tmdOc, &bar_full[st], cb * 64, i0, bh);
+        mbar_arrive_expect_tx(&bar_full[st], C::KV_STAGE + C::VEC_STAGE);
+        for (int sp = 0; sp < C::NSPLIT; ++sp) {
+          for (int cb = 0; cb < C::NCB; ++cb) {
+            tma_load_3d(gen(sQc(st, sp)) + cb * C::SMALL_CB, &m.Qc[sp], &bar_full[st], cb * C::ROW, i0, bh);
+            tma_load_3d(gen(sdOc(st, sp)) + cb * C::SMALL_CB, &m.dOc[sp], &bar_full[st], cb * C::ROW, i0, bh);
+          }
+          if constexpr (C::F32) {
+            tma_load_3d(gen(sQt(st, sp)), &m.Qt[sp], &bar_full[st], i0, 0, bh);
+            tma_load_3d(gen(sdOt(st, sp)), &m.dOt[sp], &bar_full[st], i0, 0, bh);
+          }
         }
-        tma_load_3d(vecs + st * 128, &tmL, &bar_full[st], i0, bh, 0);
-        tma_load_3d(vecs + st * 128 + 64, &tmDl, &bar_full[st], i0, bh, 0);
-        last[st] = c / C::NST;
+        tma_load_3d(vecs + st * 2 * CH, &m.L, &bar_full[st], i0, bh, 0);
+        tma_load_3d(vecs + st * 2 * CH + CH, &m.Dl, &bar_full[st], i0, bh, 0);
+        last[st] = c / NST;
       }
       drain_wait(&bar_kv, 0, a.limit_ns);
-      for (int s = 0; s < C::NST; ++s)
+      for (int s = 0; s < NST; ++s)
         if (last[s] >= 0) drain_wait(&bar_full[s], last[s] & 1, a.limit_ns);
     }
   } else if (warp == C::MMA_WARP) {
     if (lane == 0 && nc > 0) {
       bool ok = wait(&bar_kv, 0);
       tc_fence_after();
-      for (int c = 0; ok && c <= nc; ++c) {
-        if (c < nc) {
-          const int st = c % C::NST, bb = c & 1;
-          if (!(ok = wait(&bar_full[st], (c / C::NST) & 1))) break;
-          tc_fence_after();
-          issue_rowdot<C>(tmem + C::s_col(bb), sK, sQc(st));    // S^T  = K Q^T
-          issue_rowdot<C>(tmem + C::dp_col(bb), sV, sdOc(st));  // dP^T = V dO^T
-          tc_commit(&bar_sp[bb]);
+      // chunk c: S^T = K Q^T and dP^T = V dO^T into TMEM slot c & 1
+      auto scores = [&](int c) {
+        const int st = c % NST, bb = c & 1;
+        if (!wait(&bar_full[st], (c / NST) & 1)) return false;
+        tc_fence_after();
+        issue_rowdot<C>(tmem + C::s_col(bb), sK(0), sK(C::NSPLIT - 1), sQc(st, 0),
+                        sQc(st, C::NSPLIT - 1));
+        issue_rowdot<C>(tmem + C::dp_col(bb), sV(0), sV(C::NSPLIT - 1), sdOc(st, 0),
+                        sdOc(st, C::NSPLIT - 1));
+        tc_commit(&bar_sp[bb]);
+        return true;
+      };
+      // chunk pc: dV += P^T dO, dK += dS^T Q, then release its smem stage
+      auto accumulate = [&](int pc) {
+        const int pb = pc & 1, pst = pc % NST;
+        if (!wait(&bar_ds[pb], (pc >> 1) & 1)) return false;
+        tc_fence_after();
+        if constexpr (!C::F32) {
+          issue_acc<C>(tmem + C::ACC0, tmem + C::s_col(pb), 0, sdOc(pst, 0), 0, pc > 0);
+          issue_acc<C>(tmem + C::ACC1, tmem + C::dp_col(pb), 0, sQc(pst, 0), 0, pc > 0);
+        } else {
+          issue_acc<C>(tmem + C::ACC0, tmem + C::s_col(pb), tmem + C::plo_col(pb), sdOt(pst, 0),
+                       sdOt(pst, 1), pc > 0);
+          issue_acc<C>(tmem + C::ACC1, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sQt(pst, 0),
+                       sQt(pst, 1), pc > 0);
         }
-        if (c >= 1) {
-          const int pc = c - 1, pb = pc & 1, pst = pc % C::NST;
-          if (!(ok = wait(&bar_ds[pb], (pc >> 1) & 1))) break;
-          tc_fence_after();
-          issue_acc<C>(tmem + C::ACC0, tmem + C::s_col(pb), sdOc(pst), pc > 0);  // dV += P^T dO
-          issue_acc<C>(tmem + C::ACC1, tmem + C::dp_col(pb), sQc(pst), pc > 0); // dK += dS^T Q
-          tc_commit(&bar_empty[pst]);
+        tc_commit(&bar_empty[pst]);
+        return true;
+      };
+      for (int c = 0; ok && c <= nc; ++c) {
+        if constexpr (NST >= 2) {
+          // scores of chunk c overlap the softmax of chunk c - 1
+          if (c < nc && !(ok = scores(c))) break;
+          if (c >= 1 && !(ok = accumulate(c - 1))) break;
+        } else {
+          // one stage: chunk c can only be loaded once chunk c - 1 has been released
+          if (c >= 1 && !(ok = accumulate(c - 1))) break;
+          if (c < nc && !(ok = scores(c))) break;
         }
       }
       if (ok) tc_commit(&bar_done);
@@ -260,53 +392,36 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const float sl2 = a.scale_log2;
     bool ok = true;
     for (int c = 0; c < nc; ++c) {
-      const int bb = c & 1, st = c % C::NST;
+      const int bb = c & 1, st = c % NST;
       int bh, i0;
       chunk_rows(c, &bh, &i0);
-      ok = __all_sync(0xffffffffu, wait(&bar_sp[bb], (c >> 1) & 1) && wait(&bar_full[st], (c / C::NST) & 1));
+      ok = __all_sync(0xffffffffu, wait(&bar_sp[bb], (c >> 1) & 1) && wait(&bar_full[st], (c / NST) & 1));
       if (!ok) break;
       tc_fence_after();
-      float s[64], dp[64];
-      {
-        uint32_t r[32];
-        tmem_ld32(lane_addr + C::s_col(bb), r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] = __uint_as_float(r[k]);
-        tmem_ld32(lane_addr + C::s_col(bb) + 32, r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[32 + k] = __uint_as_float(r[k]);
-        tmem_ld32(lane_addr + C::dp_col(bb), r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) dp[k] = __uint_as_float(r[k]);
-        tmem_ld32(lane_addr + C::dp_col(bb) + 32, r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) dp[32 + k] = __uint_as_float(r[k]);
-      }
+      float s[CH], dp[CH];
+      tmem_ld_row<CH>(lane_addr + C::s_col(bb), s);
+      tmem_ld_row<CH>(lane_addr + C::dp_col(bb), dp);
       // queries i = i0 + k; key j visible iff (!causal || j <= i) && (!window || j >= i-w+1)
       // && j < Sk && i < Sq
-      if (tile_needs_mask(i0, i0 + C::CH - 1, j0, j0 + BLOCK_N - 1, a.Sk, a.causal, a.window) ||
-          i0 + C::CH > a.Sq) {
+      if (tile_needs_mask(i0, i0 + CH - 1, j0, j0 + BLOCK_N - 1, a.Sk, a.causal, a.window) ||
+          i0 + CH > a.Sq) {
         const int k_lo = a.causal ? j - i0 : INT_MIN / 2;                          // i >= j
         const int k_hi = min(a.window > 0 ? j + a.window - 1 - i0 : INT_MAX / 2,   // i <= j+w-1
                              a.Sq - 1 - i0);
         const bool row_dead = j >= a.Sk;
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
+        for (int k = 0; k < CH; ++k)
           if (row_dead || k < k_lo || k > k_hi) s[k] = -INFINITY;
       }
-      const float* lv = vecs + st * 128;
-      uint32_t pk[32], dk[32];
+      const float* lv = vecs + st * 2 * CH;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float p0 = ex2(fmaf(s[2 * k], sl2, -lv[2 * k]));
-        const float p1 = ex2(fmaf(s[2 * k + 1], sl2, -lv[2 * k + 1]));
-        const float d0 = p0 * (dp[2 * k] - lv[64 + 2 * k]);
-        const float d1 = p1 * (dp[2 * k + 1] - lv[64 + 2 * k + 1]);
-        pk[k] = pack_half2(p0, p1);
-        dk[k] = pack_half2(d0, d1);
+      for (int k = 0; k < CH; ++k) {
+        const float p = ex2(fmaf(s[k], sl2, -lv[k]));
+        dp[k] = p * (dp[k] - lv[CH + k]);
+        s[k] = p;
       }
-      tmem_st32(lane_addr + C::s_col(bb), pk);
-      tmem_st32(lane_addr + C::dp_col(bb), dk);
+      tmem_st_operand<C>(lane_addr + C::s_col(bb), lane_addr + C::plo_col(bb), s);
+      tmem_st_operand<C>(lane_addr + C::dp_col(bb), lane_addr + C::dslo_col(bb), dp);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar_ds[bb]);
@@ -346,16 +461,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 }
 
 // ----------------------------------------------------------------------- dQ
-template <int D>
-__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
-    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
-                     const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc,
-                     const BwdArgs a) {
-  using C = BwdCfg<D>;
+template <int D, bool F32>
+__global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ QMaps m, const BwdArgs a) {
+  using C = BwdCfg<D, F32>;
+  constexpr int CH = C::CH, NST = C::Q_NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_q, bar_full[C::NST], bar_empty[C::NST], bar_sp[2], bar_ds[2],
+  __shared__ __align__(8) uint64_t bar_q, bar_full[NST], bar_empty[NST], bar_sp[2], bar_ds[2],
       bar_done, bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -376,13 +490,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     int jmin = 0;
     if (a.window > 0 && i0 - a.window + 1 > 0) jmin = i0 - a.window + 1;
     if (jmax < jmin) { kc_lo = 0; kc_hi = 0; }
-    else { kc_lo = jmin / C::CH; kc_hi = jmax / C::CH + 1; }
+    else { kc_lo = jmin / CH; kc_hi = jmax / CH + 1; }
   }
   const int nc = kc_hi - kc_lo;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
-    for (int s = 0; s < C::NST; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
+    for (int s = 0; s < NST; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&bar_sp[s], 1); mbar_init(&bar_ds[s], 128); }
     mbar_init(&bar_done, 1);
     mbar_init(&bar_drain, 1);
@@ -399,36 +513,44 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase, sdO = sbase + C::BIG_TILE;
-  auto sKc = [&](int st) { return sbase + C::Q_CH_OFF + st * 2 * C::SMALL_TILE; };
-  auto sVc = [&](int st) { return sbase + C::Q_CH_OFF + st * 2 * C::SMALL_TILE + C::SMALL_TILE; };
+  auto sQ = [&](int sp) { return sbase + sp * C::BIG_TILE; };
+  auto sdO = [&](int sp) { return sbase + (C::NSPLIT + sp) * C::BIG_TILE; };
+  auto stage = [&](int st) { return sbase + C::Q_RES + st * C::Q_STAGE; };
+  auto sKc = [&](int st, int sp) { return stage(st) + sp * C::SMALL_TILE; };
+  auto sVc = [&](int st, int sp) { return stage(st) + (C::NSPLIT + sp) * C::SMALL_TILE; };
+  auto sKt = [&](int st, int sp) { return stage(st) + 2 * C::NSPLIT * C::SMALL_TILE + sp * C::T_TILE; };
+  auto gen = [&](uint32_t s) { return smem + (s - sbase); };
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
   };
 
   if (warp == C::TMA_WARP) {
     if (lane == 0 && nc > 0) {
-      tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmKc); tma_prefetch_desc(&tmVc);
-      mbar_arrive_expect_tx(&bar_q, 2 * C::BIG_TILE);
-      for (int cb = 0; cb < C::NCB; ++cb) {
-        tma_load_3d(smem + cb * C::BIG_CB, &tmQ, &bar_q, cb * 64, i0, bh);
-        tma_load_3d(smem + C::BIG_TILE + cb * C::BIG_CB, &tmdO, &bar_q, cb * 64, i0, bh);
-      }
-      int last[C::NST];
-      for (int s = 0; s < C::NST; ++s) last[s] = -1;
-      for (int c = 0; c < nc; ++c) {
-        const int st = c % C::NST;
-        if (!wait(&bar_empty[st], ((c / C::NST) & 1) ^ 1)) break;
-        const int k0 = (kc_lo + c) * C::CH;
-        mbar_arrive_expect_tx(&bar_full[st], 2 * C::SMALL_TILE);
+      tma_prefetch_desc(&m.Q[0]); tma_prefetch_desc(&m.Kc[0]); tma_prefetch_desc(&m.Vc[0]);
+      mbar_arrive_expect_tx(&bar_q, 2 * C::NSPLIT * C::BIG_TILE);
+      for (int sp = 0; sp < C::NSPLIT; ++sp)
         for (int cb = 0; cb < C::NCB; ++cb) {
-          tma_load_3d(smem + (sKc(st) - sbase) + cb * C::SMALL_CB, &tmKc, &bar_full[st], cb * 64, k0, bg);
-          tma_load_3d(smem + (sVc(st) - sbase) + cb * C::SMALL_CB, &tmVc, &bar_full[st], cb * 64, k0, bg);
+          tma_load_3d(gen(sQ(sp)) + cb * C::BIG_CB, &m.Q[sp], &bar_q, cb * C::ROW, i0, bh);
+          tma_load_3d(gen(sdO(sp)) + cb * C::BIG_CB, &m.dO[sp], &bar_q, cb * C::ROW, i0, bh);
         }
-        last[st] = c / C::NST;
+      int last[NST];
+      for (int s = 0; s < NST; ++s) last[s] = -1;
+      for (int c = 0; c < nc; ++c) {
+        const int st = c % NST;
+        if (!wait(&bar_empty[st], ((c / NST) & 1) ^ 1)) break;
+        const int k0 = (kc_lo + c) * CH;
+        mbar_arrive_expect_tx(&bar_full[st], C::Q_STAGE);
+        for (int sp = 0; sp < C::NSPLIT; ++sp) {
+          for (int cb = 0; cb < C::NCB; ++cb) {
+            tma_load_3d(gen(sKc(st, sp)) + cb * C::SMALL_CB, &m.Kc[sp], &bar_full[st], cb * C::ROW, k0, bg);
+            tma_load_3d(gen(sVc(st, sp)) + cb * C::SMALL_CB, &m.Vc[sp], &bar_full[st], cb * C::ROW, k0, bg);
+          }
+          if constexpr (C::F32) tma_load_3d(gen(sKt(st, sp)), &m.Kt[sp], &bar_full[st], k0, 0, bg);
+        }
+        last[st] = c / NST;
       }
       drain_wait(&bar_q, 0, a.limit_ns);
-      for (int s = 0; s < C::NST; ++s)
+      for (int s = 0; s < NST; ++s)
         if (last[s] >= 0) drain_wait(&bar_full[s], last[s] & 1, a.limit_ns);
     }
   } else if (warp == C::MMA_WARP) {
@@ -437,18 +559,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_after();
       for (int c = 0; ok && c <= nc; ++c) {
         if (c < nc) {
-          const int st = c % C::NST, bb = c & 1;
-          if (!(ok = wait(&bar_full[st], (c / C::NST) & 1))) break;
+          const int st = c % NST, bb = c & 1;
+          if (!(ok = wait(&bar_full[st], (c / NST) & 1))) break;
           tc_fence_after();
-          issue_rowdot<C>(tmem + C::s_col(bb), sQ, sKc(st));    // S  = Q K^T
-          issue_rowdot<C>(tmem + C::dp_col(bb), sdO, sVc(st));  // dP = dO V^T
+          issue_rowdot<C>(tmem + C::s_col(bb), sQ(0), sQ(C::NSPLIT - 1), sKc(st, 0),
+                          sKc(st, C::NSPLIT - 1));  // S = Q K^T
+          issue_rowdot<C>(tmem + C::dp_col(bb), sdO(0), sdO(C::NSPLIT - 1), sVc(st, 0),
+                          sVc(st, C::NSPLIT - 1));  // dP = dO V^T
           tc_commit(&bar_sp[bb]);
         }
         if (c >= 1) {
-          const int pc = c - 1, pb = pc & 1, pst = pc % C::NST;
+          const int pc = c - 1, pb = pc & 1, pst = pc % NST;
           if (!(ok = wait(&bar_ds[pb], (pc >> 1) & 1))) break;
           tc_fence_after();
-          issue_acc<C>(tmem + C::ACC0, tmem + C::dp_col(pb), sKc(pst), pc > 0);  // dQ += dS K
+          if constexpr (!C::F32)
+            issue_acc<C>(tmem + C::ACC0, tmem + C::dp_col(pb), 0, sKc(pst, 0), 0, pc > 0);
+          else
+            issue_acc<C>(tmem + C::ACC0, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sKt(pst, 0),
+                         sKt(pst, 1), pc > 0);
           tc_commit(&bar_empty[pst]);
         }
       }
@@ -471,41 +599,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bool ok = true;
     for (int c = 0; c < nc; ++c) {
       const int bb = c & 1;
-      const int k0 = (kc_lo + c) * C::CH;
+      const int k0 = (kc_lo + c) * CH;
       ok = __all_sync(0xffffffffu, wait(&bar_sp[bb], (c >> 1) & 1));
       if (!ok) break;
       tc_fence_after();
-      float s[64], dp[64];
-      {
-        uint32_t r[32];
-        tmem_ld32(lane_addr + C::s_col(bb), r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] = __uint_as_float(r[k]);
-        tmem_ld32(lane_addr + C::s_col(bb) + 32, r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[32 + k] = __uint_as_float(r[k]);
-        tmem_ld32(lane_addr + C::dp_col(bb), r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) dp[k] = __uint_as_float(r[k]);
-        tmem_ld32(lane_addr + C::dp_col(bb) + 32, r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) dp[32 + k] = __uint_as_float(r[k]);
-      }
-      if (tile_needs_mask(i0, i0 + BLOCK_M - 1, k0, k0 + C::CH - 1, a.Sk, a.causal, a.window)) {
+      float s[CH], dp[CH];
+      tmem_ld_row<CH>(lane_addr + C::s_col(bb), s);
+      tmem_ld_row<CH>(lane_addr + C::dp_col(bb), dp);
+      if (tile_needs_mask(i0, i0 + BLOCK_M - 1, k0, k0 + CH - 1, a.Sk, a.causal, a.window)) {
         const int rel_hi = hi_i - k0, rel_lo = lo_i - k0;
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
+        for (int k = 0; k < CH; ++k)
           if (k > rel_hi || k < rel_lo) s[k] = -INFINITY;
       }
       const float nl = -lse2;
-      uint32_t dk[32];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float p0 = ex2(fmaf(s[2 * k], sl2, nl));
-        const float p1 = ex2(fmaf(s[2 * k + 1], sl2, nl));
-        dk[k] = pack_half2(p0 * (dp[2 * k] - dl), p1 * (dp[2 * k + 1] - dl));
-      }
-      tmem_st32(lane_addr + C::dp_col(bb), dk);
+      for (int k = 0; k < CH; ++k) dp[k] = ex2(fmaf(s[k], sl2, nl)) * (dp[k] - dl);
+      tmem_st_operand<C>(lane_addr + C::dp_col(bb), lane_addr + C::dslo_col(bb), dp);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bar_ds[bb]);
@@ -539,15 +649,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 }
 
 // -------------------------------------------------------------- preprocess
+__device__ __forceinline__ void load4(const void* base, size_t off, int is_bf16, float (&v)[4]) {
+  if (is_bf16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + off);
+    v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  } else {
+    const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+  }
+}
+
 // One warp per padded query row (bh, i), i < ldq:
 //   delta[bh][i] = sum_d dO[i,d] * O[i,d];  lse2[bh][i] = LSE * log2(e) (+inf if -inf);
-//   fp16 copies of the dO and Q rows. Rows i >= Sq get lse2 = +inf, delta = 0.
+//   for bf16 inputs also the fp16 copies of the dO and Q rows (dO16 / Q16 non-null).
+// Rows i >= Sq get lse2 = +inf, delta = 0.
 template <int D>
-__global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ dO, const void* __restrict__ O,
-                                      const float* __restrict__ LSE, const __nv_bfloat16* __restrict__ Q,
+__global__ void bwd_preprocess_kernel(const void* __restrict__ dO, const void* __restrict__ O,
+                                      const float* __restrict__ LSE, const void* __restrict__ Q,
                                       __half* __restrict__ dO16, __half* __restrict__ Q16,
                                       float* __restrict__ lse2, float* __restrict__ delta, int Sq,
-                                      int ldq, size_t n_rows_padded, int o_bf16) {
+                                      int ldq, size_t n_rows_padded, int in_bf16, int o_bf16) {
   const size_t warps = (size_t)gridDim.x * (blockDim.x / 32);
   const int lane = threadIdx.x & 31;
   for (size_t w = blockIdx.x * (size_t)(blockDim.x / 32) + threadIdx.x / 32; w < n_rows_padded;
@@ -564,27 +686,21 @@ __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ dO, cons
     for (int d0 = 0; d0 < D; d0 += 128) {
       const int d = d0 + lane * 4;
       if (d >= D) break;  // D = 64: lanes 16..31 have no columns
-      const uint2 g = *reinterpret_cast<const uint2*>(dO + row * D + d);
-      const uint2 qv = *reinterpret_cast<const uint2*>(Q + row * D + d);
-      float gv[4] = {__uint_as_float(g.x << 16), __uint_as_float(g.x & 0xFFFF0000u),
-                     __uint_as_float(g.y << 16), __uint_as_float(g.y & 0xFFFF0000u)};
-      float ov[4];
-      if (o_bf16) {
-        const uint2 o = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(O) + row * D + d);
-        ov[0] = __uint_as_float(o.x << 16); ov[1] = __uint_as_float(o.x & 0xFFFF0000u);
-        ov[2] = __uint_as_float(o.y << 16); ov[3] = __uint_as_float(o.y & 0xFFFF0000u);
-      } else {
-        const float4 o = *reinterpret_cast<const float4*>(static_cast<const float*>(O) + row * D + d);
-        ov[0] = o.x; ov[1] = o.y; ov[2] = o.z; ov[3] = o.w;
-      }
+      float gv[4], ov[4];
+      load4(dO, row * D + d, in_bf16, gv);
+      load4(O, row * D + d, o_bf16, ov);
       acc += gv[0] * ov[0] + gv[1] * ov[1] + gv[2] * ov[2] + gv[3] * ov[3];
-      uint2 g16, q16;
-      g16.x = pack_half2(gv[0], gv[1]);
-      g16.y = pack_half2(gv[2], gv[3]);
-      q16.x = pack_half2(__uint_as_float(qv.x << 16), __uint_as_float(qv.x & 0xFFFF0000u));
-      q16.y = pack_half2(__uint_as_float(qv.y << 16), __uint_as_float(qv.y & 0xFFFF0000u));
-      *reinterpret_cast<uint2*>(dO16 + row * D + d) = g16;
-      *reinterpret_cast<uint2*>(Q16 + row * D + d) = q16;
+      if (dO16) {
+        float qv[4];
+        load4(Q, row * D + d, 1, qv);
+        uint2 g16, q16;
+        g16.x = pack_half2(gv[0], gv[1]);
+        g16.y = pack_half2(gv[2], gv[3]);
+        q16.x = pack_half2(qv[0], qv[1]);
+        q16.y = pack_half2(qv[2], qv[3]);
+        *reinterpret_cast<uint2*>(dO16 + row * D + d) = g16;
+        *reinterpret_cast<uint2*>(Q16 + row * D + d) = q16;
+      }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -606,52 +722,114 @@ __global__ void zero_kernel(uint4* p, size_t n16) {
 // ------------------------------------------------------------------ launcher
 namespace {
 
-template <int D>
-fa_status run_bwd_bf16(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                       const float* LSE, void* dQ, void* dK, void* dV, const fa_params& p,
-                       cudaStream_t stream) {
-  using C = BwdCfg<D>;
+template <int D, bool F32>
+fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                  const float* LSE, void* dQ, void* dK, void* dV, const fa_params& p,
+                  cudaStream_t stream) {
+  using C = BwdCfg<D, F32>;
   const size_t BH = (size_t)p.B * p.H, BHk = (size_t)p.B * p.HKV;
   const size_t nq = BH * p.Sq * D, nk = BHk * p.Sk * D;
   const int ldq = (p.Sq + 63) / 64 * 64;
   const size_t nvec = BH * ldq;
-  const size_t bytes = (2 * nq + 2 * nk) * 2 + 2 * nvec * 4;
+  const int ldqt = (p.Sq + 3) / 4 * 4, ldkt = (p.Sk + 3) / 4 * 4;  // transposed row pitch
+  const size_t nqt = BH * D * ldqt, nkt = BHk * D * ldkt;
+  size_t bytes = 2 * nvec * 4;
+  if constexpr (!F32) bytes += (2 * nq + 2 * nk) * 2;
+  else bytes += (4 * nq + 4 * nk + 4 * nqt + 2 * nkt) * 4;  // Q,dO,K,V hi/lo + Q^T,dO^T,K^T hi/lo
   void* ws = nullptr;
   if (host::scratch_alloc(&ws, bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
-  __half* q16 = static_cast<__half*>(ws);
-  __half* do16 = q16 + nq;
-  __half* k16 = do16 + nq;
-  __half* v16 = k16 + nk;
-  float* lse2 = reinterpret_cast<float*>(v16 + nk);
+  float* lse2 = static_cast<float*>(ws);
   float* delta = lse2 + nvec;
   const int grid_pp = 4 * host::sm_count();
-  {
-    host::KernelTimer kt("bwd_preprocess", stream);
-    bwd_preprocess_kernel<D><<<grid_pp, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(dO), O, LSE, static_cast<const __nv_bfloat16*>(Q), do16,
-        q16, lse2, delta, p.Sq, ldq, nvec, p.out_dtype == FA_BF16);
-  }
-  {
-    host::KernelTimer kt("cvt_bf16_to_f16(K,V)", stream);
-    cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(K),
-                                                       reinterpret_cast<uint4*>(k16), nk / 8);
-    cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
-                                                       reinterpret_cast<uint4*>(v16), nk / 8);
-  }
-  CUtensorMap mK, mV, mQc, mdOc, mL, mDl, mQ, mdO, mKc, mVc;
-  const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const auto F32T = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  KVMaps mk;
+  QMaps mq;
   bool enc = true;
-  enc &= host::encode_tiled_3d(&mK, F16, 2, k16, D, p.Sk, BHk, D, 64, 128);
-  enc &= host::encode_tiled_3d(&mV, F16, 2, v16, D, p.Sk, BHk, D, 64, 128);
-  enc &= host::encode_tiled_3d(&mKc, F16, 2, k16, D, p.Sk, BHk, D, 64, 64);
-  enc &= host::encode_tiled_3d(&mVc, F16, 2, v16, D, p.Sk, BHk, D, 64, 64);
-  enc &= host::encode_tiled_3d(&mQ, F16, 2, q16, D, p.Sq, BH, D, 64, 128);
-  enc &= host::encode_tiled_3d(&mdO, F16, 2, do16, D, p.Sq, BH, D, 64, 128);
-  enc &= host::encode_tiled_3d(&mQc, F16, 2, q16, D, p.Sq, BH, D, 64, 64);
-  enc &= host::encode_tiled_3d(&mdOc, F16, 2, do16, D, p.Sq, BH, D, 64, 64);
-  enc &= host::encode_tiled_3d(&mL, F32T, 4, lse2, ldq, BH, 1, ldq, 64, 1, false);
-  enc &= host::encode_tiled_3d(&mDl, F32T, 4, delta, ldq, BH, 1, ldq, 64, 1, false);
+  enc &= host::encode_tiled_3d(&mk.L, F32T, 4, lse2, ldq, BH, 1, ldq, C::CH, 1, false);
+  enc &= host::encode_tiled_3d(&mk.Dl, F32T, 4, delta, ldq, BH, 1, ldq, C::CH, 1, false);
+  if constexpr (!F32) {
+    __half* q16 = reinterpret_cast<__half*>(delta + nvec);
+    __half* do16 = q16 + nq;
+    __half* k16 = do16 + nq;
+    __half* v16 = k16 + nk;
+    {
+      host::KernelTimer kt("bwd_preprocess", stream);
+      bwd_preprocess_kernel<D><<<grid_pp, 256, 0, stream>>>(dO, O, LSE, Q, do16, q16, lse2, delta,
+                                                           p.Sq, ldq, nvec, 1, p.out_dtype == FA_BF16);
+    }
+    {
+      host::KernelTimer kt("cvt_bf16_to_f16(K,V)", stream);
+      cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(K),
+                                                         reinterpret_cast<uint4*>(k16), nk / 8);
+      cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
+                                                         reinterpret_cast<uint4*>(v16), nk / 8);
+    }
+    const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    enc &= host::encode_tiled_3d(&mk.K[0], F16, 2, k16, D, p.Sk, BHk, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mk.V[0], F16, 2, v16, D, p.Sk, BHk, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mk.Qc[0], F16, 2, q16, D, p.Sq, BH, D, 64, C::CH);
+    enc &= host::encode_tiled_3d(&mk.dOc[0], F16, 2, do16, D, p.Sq, BH, D, 64, C::CH);
+    enc &= host::encode_tiled_3d(&mq.Q[0], F16, 2, q16, D, p.Sq, BH, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mq.dO[0], F16, 2, do16, D, p.Sq, BH, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mq.Kc[0], F16, 2, k16, D, p.Sk, BHk, D, 64, C::CH);
+    enc &= host::encode_tiled_3d(&mq.Vc[0], F16, 2, v16, D, p.Sk, BHk, D, 64, C::CH);
+    mk.K[1] = mk.K[0]; mk.V[1] = mk.V[0]; mk.Qc[1] = mk.Qc[0]; mk.dOc[1] = mk.dOc[0];
+    mk.Qt[0] = mk.Qt[1] = mk.Qc[0]; mk.dOt[0] = mk.dOt[1] = mk.dOc[0];
+    mq.Q[1] = mq.Q[0]; mq.dO[1] = mq.dO[0]; mq.Kc[1] = mq.Kc[0]; mq.Vc[1] = mq.Vc[0];
+    mq.Kt[0] = mq.Kt[1] = mq.Kc[0];
+  } else {
+    float* qh = delta + nvec;
+    float* ql = qh + nq;
+    float* doh = ql + nq;
+    float* dol = doh + nq;
+    float* kh = dol + nq;
+    float* kl = kh + nk;
+    float* vh = kl + nk;
+    float* vl = vh + nk;
+    float* qth = vl + nk;
+    float* qtl = qth + nqt;
+    float* doth = qtl + nqt;
+    float* dotl = doth + nqt;
+    float* kth = dotl + nqt;
+    float* ktl = kth + nkt;
+    {
+      host::KernelTimer kt("bwd_preprocess", stream);
+      bwd_preprocess_kernel<D><<<grid_pp, 256, 0, stream>>>(dO, O, LSE, Q, nullptr, nullptr, lse2,
+                                                           delta, p.Sq, ldq, nvec, 0,
+                                                           p.out_dtype == FA_BF16);
+    }
+    {
+      host::KernelTimer kt("split_tf32(Q,dO,K,V)", stream);
+      split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(Q), qh, ql, qth, qtl,
+                                                    p.Sq, D, ldqt, BH);
+      split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(dO), doh, dol, doth,
+                                                    dotl, p.Sq, D, ldqt, BH);
+      split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(K), kh, kl, kth, ktl,
+                                                    p.Sk, D, ldkt, BHk);
+      split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(V), vh, vl, nullptr,
+                                                    nullptr, p.Sk, D, 0, BHk);
+    }
+    float* hl_q[2] = {qh, ql};
+    float* hl_do[2] = {doh, dol};
+    float* hl_k[2] = {kh, kl};
+    float* hl_v[2] = {vh, vl};
+    float* hl_qt[2] = {qth, qtl};
+    float* hl_dot[2] = {doth, dotl};
+    float* hl_kt[2] = {kth, ktl};
+    for (int sp = 0; sp < 2; ++sp) {
+      enc &= host::encode_tiled_3d(&mk.K[sp], F32T, 4, hl_k[sp], D, p.Sk, BHk, D, 32, 128);
+      enc &= host::encode_tiled_3d(&mk.V[sp], F32T, 4, hl_v[sp], D, p.Sk, BHk, D, 32, 128);
+      enc &= host::encode_tiled_3d(&mk.Qc[sp], F32T, 4, hl_q[sp], D, p.Sq, BH, D, 32, C::CH);
+      enc &= host::encode_tiled_3d(&mk.dOc[sp], F32T, 4, hl_do[sp], D, p.Sq, BH, D, 32, C::CH);
+      enc &= host::encode_tiled_3d(&mk.Qt[sp], F32T, 4, hl_qt[sp], p.Sq, D, BH, ldqt, 32, D);
+      enc &= host::encode_tiled_3d(&mk.dOt[sp], F32T, 4, hl_dot[sp], p.Sq, D, BH, ldqt, 32, D);
+      enc &= host::encode_tiled_3d(&mq.Q[sp], F32T, 4, hl_q[sp], D, p.Sq, BH, D, 32, 128);
+      enc &= host::encode_tiled_3d(&mq.dO[sp], F32T, 4, hl_do[sp], D, p.Sq, BH, D, 32, 128);
+      enc &= host::encode_tiled_3d(&mq.Kc[sp], F32T, 4, hl_k[sp], D, p.Sk, BHk, D, 32, C::CH);
+      enc &= host::encode_tiled_3d(&mq.Vc[sp], F32T, 4, hl_v[sp], D, p.Sk, BHk, D, 32, C::CH);
+      enc &= host::encode_tiled_3d(&mq.Kt[sp], F32T, 4, hl_kt[sp], p.Sk, D, BHk, ldkt, 32, D);
+    }
+  }
   if (!enc) {
     host::scratch_free(ws, stream);
     return FA_ERR_CUDA;
@@ -665,30 +843,33 @@ fa_status run_bwd_bf16(const void* Q, const void* K, const void* V, const void* 
   a.lpt = p.causal;
   a.limit_ns = WAIT_LIMIT_NS;
   cudaError_t e = cudaSuccess;
-  if (p.Sk > 0) {
+  {
     BwdArgs ak = a;
     ak.n_tiles = (p.Sk + BLOCK_N - 1) / BLOCK_N;
     ak.BHx = (int)BHk;
-    auto kern = fa_bwd_dkdv_kernel<D>;
+    auto kern = fa_bwd_dkdv_kernel<D, F32>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::KV_SMEM);
     if (e == cudaSuccess) {
-      host::KernelTimer kt(D == 128 ? "fa_bwd_dkdv_kernel<128,bf16>" : "fa_bwd_dkdv_kernel<64,bf16>",
+      host::KernelTimer kt(F32 ? "fa_bwd_dkdv_kernel<64,f32>"
+                               : (D == 128 ? "fa_bwd_dkdv_kernel<128,bf16>"
+                                           : "fa_bwd_dkdv_kernel<64,bf16>"),
                            stream);
-      kern<<<(unsigned)(BHk * ak.n_tiles), C::THREADS, C::KV_SMEM, stream>>>(mK, mV, mQc, mdOc, mL,
-                                                                            mDl, ak);
+      kern<<<(unsigned)(BHk * ak.n_tiles), C::THREADS, C::KV_SMEM, stream>>>(mk, ak);
       e = cudaGetLastError();
     }
   }
-  if (e == cudaSuccess && p.Sq > 0) {
+  if (e == cudaSuccess) {
     BwdArgs aq = a;
     aq.n_tiles = (p.Sq + BLOCK_M - 1) / BLOCK_M;
     aq.BHx = (int)BH;
-    auto kern = fa_bwd_dq_kernel<D>;
+    auto kern = fa_bwd_dq_kernel<D, F32>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::Q_SMEM);
     if (e == cudaSuccess) {
-      host::KernelTimer kt(D == 128 ? "fa_bwd_dq_kernel<128,bf16>" : "fa_bwd_dq_kernel<64,bf16>",
+      host::KernelTimer kt(F32 ? "fa_bwd_dq_kernel<64,f32>"
+                               : (D == 128 ? "fa_bwd_dq_kernel<128,bf16>"
+                                           : "fa_bwd_dq_kernel<64,bf16>"),
                            stream);
-      kern<<<(unsigned)(BH * aq.n_tiles), C::THREADS, C::Q_SMEM, stream>>>(mQ, mdO, mKc, mVc, aq);
+      kern<<<(unsigned)(BH * aq.n_tiles), C::THREADS, C::Q_SMEM, stream>>>(mq, aq);
       e = cudaGetLastError();
     }
   }
@@ -716,8 +897,10 @@ fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O,
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
   if (p.in_dtype == FA_BF16) {
-    if (p.D == 128) return run_bwd_bf16<128>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
-    if (p.D == 64) return run_bwd_bf16<64>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
+    if (p.D == 128) return run_bwd<128, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
+    if (p.D == 64) return run_bwd<64, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
+  } else {
+    if (p.D == 64) return run_bwd<64, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
   }
   return FA_ERR_UNSUPPORTED;
 }
