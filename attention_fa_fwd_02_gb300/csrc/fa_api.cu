@@ -247,6 +247,13 @@ FA_API const char* fa_status_string(fa_status s) {
 
 FA_API const char* fa_version(void) { return "fa-sm103a 0.1"; }
 
+FA_API fa_status fa_selftest_timeout(unsigned long long limit_ns, int* roles_done,
+                                     fa_stream_t stream) {
+  if (!roles_done || limit_ns == 0 || limit_ns > 10000000000ull) return FA_ERR_INVALID_ARG;
+  if (!aligned16(roles_done)) return FA_ERR_ALIGNMENT;
+  return launch_selftest_timeout(limit_ns, roles_done, reinterpret_cast<cudaStream_t>(stream));
+}
+
 FA_API fa_status fa_timing_enable(int on) {
   using namespace fa::host;
   std::lock_guard<std::mutex> lk(g_t_mu);

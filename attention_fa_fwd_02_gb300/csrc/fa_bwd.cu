@@ -183,15 +183,30 @@ __device__ __forceinline__ void store_row32(void* base, size_t elem_off, const u
   }
 }
 
-// Load CH fp32 columns of this thread's TMEM lane.
+// Load CH fp32 columns at `sa` and CH at `da` of this thread's TMEM lane, with a
+// single wait for all of them.
 template <int CH>
-__device__ __forceinline__ void tmem_ld_row(uint32_t addr, float (&x)[CH]) {
+__device__ __forceinline__ void tmem_ld_pair(uint32_t sa, uint32_t da, float (&x)[CH],
+                                             float (&y)[CH]) {
+  static_assert(CH == 32 || CH == 64, "chunk width");
+  if constexpr (CH == 64) {
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    tmem_ld32x4(sa, sa + 32, da, da + 32, r0, r1, r2, r3);
 #pragma unroll
-  for (int c = 0; c < CH / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld32(addr + c * 32, r);
+    for (int k = 0; k < 32; ++k) {
+      x[k] = __uint_as_float(r0[k]);
+      x[32 + k] = __uint_as_float(r1[k]);
+      y[k] = __uint_as_float(r2[k]);
+      y[32 + k] = __uint_as_float(r3[k]);
+    }
+  } else {
+    uint32_t r0[32], r1[32];
+    tmem_ld32x2(sa, da, r0, r1);
 #pragma unroll
-    for (int k = 0; k < 32; ++k) x[c * 32 + k] = __uint_as_float(r[k]);
+    for (int k = 0; k < 32; ++k) {
+      x[k] = __uint_as_float(r0[k]);
+      y[k] = __uint_as_float(r1[k]);
+    }
   }
 }
 
@@ -399,8 +414,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       float s[CH], dp[CH];
-      tmem_ld_row<CH>(lane_addr + C::s_col(bb), s);
-      tmem_ld_row<CH>(lane_addr + C::dp_col(bb), dp);
+      tmem_ld_pair<CH>(lane_addr + C::s_col(bb), lane_addr + C::dp_col(bb), s, dp);
       // queries i = i0 + k; key j visible iff (!causal || j <= i) && (!window || j >= i-w+1)
       // && j < Sk && i < Sq
       if (tile_needs_mask(i0, i0 + CH - 1, j0, j0 + BLOCK_N - 1, a.Sk, a.causal, a.window) ||
@@ -604,8 +618,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       float s[CH], dp[CH];
-      tmem_ld_row<CH>(lane_addr + C::s_col(bb), s);
-      tmem_ld_row<CH>(lane_addr + C::dp_col(bb), dp);
+      tmem_ld_pair<CH>(lane_addr + C::s_col(bb), lane_addr + C::dp_col(bb), s, dp);
       if (tile_needs_mask(i0, i0 + BLOCK_M - 1, k0, k0 + CH - 1, a.Sk, a.causal, a.window)) {
         const int rel_hi = hi_i - k0, rel_lo = lo_i - k0;
 #pragma unroll

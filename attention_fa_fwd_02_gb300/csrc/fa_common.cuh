@@ -105,6 +105,7 @@ fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O,
                      cudaStream_t stream);
 fa_status launch_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
                              const fa_params& p, cudaStream_t stream);
+fa_status launch_selftest_timeout(unsigned long long limit_ns, int* roles_done, cudaStream_t s);
 unsigned int read_and_clear_fwd_status(cudaError_t* err);
 unsigned int read_and_clear_bwd_status(cudaError_t* err);
 

@@ -55,16 +55,24 @@ struct FwdCfg {
   static constexpr uint32_t VT_CB_BYTES = D * 128u;        // fp32 V^T: 32 keys x D rows
   static constexpr int NSPLIT = F32 ? 2 : 1;               // hi / lo copies
   static constexpr int KST = F32 ? 1 : (D == 128 ? 2 : 3); // K ring depth
-  static constexpr int VST = KST;                          // V ring depth
+  static constexpr int VST = F32 ? 1 : 3;                  // V ring depth
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t K_OFF = Q_OFF + NQ * NSPLIT * TILE_BYTES;
   static constexpr uint32_t V_OFF = K_OFF + KST * NSPLIT * TILE_BYTES;
   static constexpr uint32_t SMEM_BYTES = V_OFF + VST * NSPLIT * TILE_BYTES;
   static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
   static constexpr int SOFTMAX_WARPS = 4 * NQ;
+  // Warps SOFTMAX_WARPS + q issue the MMAs of query tile q (the first one also owns
+  // TMEM); the TMA producer follows them. Whole warpgroups: the control warps share
+  // the last warpgroup with idle warps.
   static constexpr int MMA_WARP = SOFTMAX_WARPS;
-  static constexpr int TMA_WARP = SOFTMAX_WARPS + 1;
-  static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+  static constexpr int TMA_WARP = SOFTMAX_WARPS + NQ;
+  static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 4);
+  // Register split for NQ = 2 (launched at 168 per thread for 384 threads): the
+  // softmax warpgroups hold a whole 128-column S row in registers.
+  static constexpr uint32_t REGS_SOFTMAX = 216, REGS_CONTROL = 64;
+  static_assert(NQ == 1 || (2 * 128 * REGS_SOFTMAX + 128 * REGS_CONTROL) <= 384 * 168,
+                "register split exceeds the launch allocation");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t PLO_COL = 128;                  // fp32 path: P_lo columns
   __host__ __device__ static constexpr uint32_t s_col(int q) { return 128u * q; }
@@ -136,7 +144,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_q, bar_kfull[C::KST], bar_kempty[C::KST],
-      bar_vfull[C::VST], bar_vempty[C::VST], bar_s[C::NQ], bar_p[C::NQ], bar_o[C::NQ], bar_drain;
+      bar_vfull[C::VST], bar_vempty[C::VST], bar_s[C::NQ], bar_p[C::NQ], bar_o[C::NQ],
+      bar_drain[C::NQ];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -162,14 +171,15 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
-    for (int s = 0; s < C::KST; ++s) { mbar_init(&bar_kfull[s], 1); mbar_init(&bar_kempty[s], 1); }
-    for (int s = 0; s < C::VST; ++s) { mbar_init(&bar_vfull[s], 1); mbar_init(&bar_vempty[s], 1); }
+    // a K / V stage is free once every tile's issuer has consumed it
+    for (int s = 0; s < C::KST; ++s) { mbar_init(&bar_kfull[s], 1); mbar_init(&bar_kempty[s], C::NQ); }
+    for (int s = 0; s < C::VST; ++s) { mbar_init(&bar_vfull[s], 1); mbar_init(&bar_vempty[s], C::NQ); }
     for (int q = 0; q < C::NQ; ++q) {
       mbar_init(&bar_s[q], 1);
       mbar_init(&bar_p[q], 128);
       mbar_init(&bar_o[q], 1);
     }
-    mbar_init(&bar_drain, 1);
+    for (int q = 0; q < C::NQ; ++q) mbar_init(&bar_drain[q], 1);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -190,6 +200,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     return mbar_wait(bar, parity, abort_flag, &g_fwd_status, DEV_TIMEOUT, a.limit_ns);
   };
 
+  if (warp >= C::SOFTMAX_WARPS) {
+  if constexpr (C::NQ == 2) regs_decrease<C::REGS_CONTROL>();
   if (warp == C::TMA_WARP) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n > 0) {
@@ -245,52 +257,55 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         while (!mbar_try_wait(&bar_q, 0) && globaltimer() - t0 < a.limit_ns) {}
       }
     }
-  } else if (warp == C::MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp < C::MMA_WARP + C::NQ) {
+    // ------------------------------------------------------------ MMA issuer of tile q
+    // In order per tile: S_q(0); then per key tile j: O_q += P_q V_j (once the
+    // softmax wrote P_q), S_q(j+1) = Q_q K_{j+1}^T. P_q aliases S_q in TMEM; MMAs of
+    // one thread run in issue order, so S_q(j+1) after PV_q(j) is safe.
+    // Each tile has its own issuing warp: after a burst of MMAs a warp's next
+    // barrier operation waits for that burst, so a single issuer for both tiles
+    // lets the tensor core drain at every tile switch. Tile 1 starts once tile 0's
+    // first P is ready, which staggers the tiles; the in-order tensor pipe then
+    // keeps their bursts alternating, each tile's softmax overlapping the other
+    // tile's MMAs.
+    const int q = warp - C::MMA_WARP;
     if (lane == 0 && n > 0) {
       bool ok = wait(&bar_q, 0) && wait(&bar_kfull[0], 0);
+      if (ok && q > 0) ok = wait(&bar_p[0], 0);
       tc_fence_after();
       if (ok) {
-        for (int q = 0; q < C::NQ; ++q) {
-          issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(0, 0),
-                      sK(0, C::NSPLIT - 1));
-          tc_commit(&bar_s[q]);
-        }
+        issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(0, 0),
+                    sK(0, C::NSPLIT - 1));
+        tc_commit(&bar_s[q]);
         tc_commit(&bar_kempty[0]);
       }
       for (int it = 0; ok && it < n; ++it) {
         const int vs = it % C::VST;
-        if (!(ok = wait(&bar_vfull[vs], (it / C::VST) & 1))) break;
+        if (!(ok = wait(&bar_vfull[vs], (it / C::VST) & 1) && wait(&bar_p[q], it & 1))) break;
         tc_fence_after();
-        for (int q = 0; q < C::NQ && ok; ++q) {
-          if (!(ok = wait(&bar_p[q], it & 1))) break;
-          tc_fence_after();
-          issue_pv<C>(tmem + C::o_col(q), tmem + C::s_col(q), tmem + C::PLO_COL, sV(vs, 0),
-                      sV(vs, C::NSPLIT - 1), it > 0);
-          if (it + 1 < n) {
-            const int ks = (it + 1) % C::KST;
-            if (q == 0) {
-              if (!(ok = wait(&bar_kfull[ks], ((it + 1) / C::KST) & 1))) break;
-              tc_fence_after();
-            }
-            issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(ks, 0),
-                        sK(ks, C::NSPLIT - 1));
-            tc_commit(&bar_s[q]);
-          }
-        }
-        if (!ok) break;
+        issue_pv<C>(tmem + C::o_col(q), tmem + C::s_col(q), tmem + C::PLO_COL, sV(vs, 0),
+                    sV(vs, C::NSPLIT - 1), it > 0);
         tc_commit(&bar_vempty[vs]);
-        if (it + 1 < n) tc_commit(&bar_kempty[(it + 1) % C::KST]);
+        if (it + 1 < n) {
+          const int ks = (it + 1) % C::KST;
+          if (!(ok = wait(&bar_kfull[ks], ((it + 1) / C::KST) & 1))) break;
+          tc_fence_after();
+          issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(ks, 0),
+                      sK(ks, C::NSPLIT - 1));
+          tc_commit(&bar_s[q]);
+          tc_commit(&bar_kempty[ks]);
+        }
       }
-      if (ok)
-        for (int q = 0; q < C::NQ; ++q) tc_commit(&bar_o[q]);
+      if (ok) tc_commit(&bar_o[q]);
       // Drain: no MMA may still be running when TMEM is released.
-      tc_commit(&bar_drain);
+      tc_commit(&bar_drain[q]);
       const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(&bar_drain, 0) && globaltimer() - t0 < a.limit_ns) {}
+      while (!mbar_try_wait(&bar_drain[q], 0) && globaltimer() - t0 < a.limit_ns) {}
     }
+  }  // idle warps of the control warpgroup fall through
   } else {
     // ------------------------------------------------------------ softmax / epilogue
+    if constexpr (C::NQ == 2) regs_increase<C::REGS_SOFTMAX>();
     const int q = warp / 4;
     const int wq = warp % 4;
     const int r_in = wq * 32 + lane;
@@ -312,12 +327,16 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       float s[128];
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32x4(s_addr, s_addr + 32, s_addr + 64, s_addr + 96, r0, r1, r2, r3);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(s_addr + c * 32, r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(r[k]);
+        for (int k = 0; k < 32; ++k) {
+          s[k] = __uint_as_float(r0[k]);
+          s[32 + k] = __uint_as_float(r1[k]);
+          s[64 + k] = __uint_as_float(r2[k]);
+          s[96 + k] = __uint_as_float(r3[k]);
+        }
       }
       const int c0 = t * BLOCK_N;
       if (tile_needs_mask(r0, r0 + BLOCK_M - 1, c0, c0 + BLOCK_N - 1, a.Sk, a.causal, a.window)) {
@@ -555,6 +574,70 @@ fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float
     if (p.D == 64) return run_fwd<64, true>(Q, K, V, O, LSE, p, stream);
   }
   return FA_ERR_UNSUPPORTED;
+}
+
+// ------------------------------------------------------- barrier-timeout self test
+// A one-CTA kernel with the same control skeleton as the attention kernels
+// (TMEM allocation, a producer, a consumer waiting on a full barrier, bounded
+// waits, abort propagation, TMEM release), in which the producer deliberately
+// never issues its copy: the consumer's wait must expire after `limit_ns`, record
+// DEV_TIMEOUT in the device status word, make every other role leave, free TMEM
+// and let the kernel return normally.
+__global__ void __launch_bounds__(128, 1) selftest_timeout_kernel(unsigned long long limit_ns,
+                                                                  int* roles_done) {
+  __shared__ __align__(8) uint64_t bar_full, bar_empty;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  const int warp = warp_id(), lane = lane_id();
+  volatile int* abort_flag = &abort_sh;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_full, 1);
+    mbar_init(&bar_empty, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(&tmem_base_sh, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  if (warp == 1) {
+    // producer: the first slot is free at once; it "forgets" the copy, then waits
+    // for the consumer to release the slot, which never happens
+    if (lane == 0) {
+      mbar_wait(&bar_empty, 1, abort_flag, &g_fwd_status, DEV_TIMEOUT, limit_ns);
+      mbar_wait(&bar_empty, 0, abort_flag, &g_fwd_status, DEV_TIMEOUT, limit_ns);
+      atomicAdd(roles_done, 1);
+    }
+  } else if (warp == 2) {
+    // consumer: waits for data that never arrives
+    if (lane == 0) {
+      if (mbar_wait(&bar_full, 0, abort_flag, &g_fwd_status, DEV_TIMEOUT, limit_ns))
+        mbar_arrive(&bar_empty);
+      atomicAdd(roles_done, 1);
+    }
+  } else if (warp == 3) {
+    // a whole warp blocked behind the consumer; it must leave once the abort is raised
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_empty, 0, abort_flag, &g_fwd_status,
+                                                      DEV_TIMEOUT, limit_ns));
+    if (lane == 0 && !ok) atomicAdd(roles_done, 1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 32);
+  }
+}
+
+fa_status launch_selftest_timeout(unsigned long long limit_ns, int* roles_done, cudaStream_t s) {
+  selftest_timeout_kernel<<<1, 128, 0, s>>>(limit_ns, roles_done);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 // ------------------------------------------------- forward without allocation

@@ -205,6 +205,50 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 #undef FA_R8
+// Several 32-column loads issued back to back and completed by one wait (fewer
+// serial TMEM round trips than separate tmem_ld32 calls).
+#define FA_RR8(r, i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
+                     "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld32x2(uint32_t a0, uint32_t a1,
+                                              uint32_t (&r0)[32], uint32_t (&r1)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : FA_RR8(r0, 0), FA_RR8(r0, 8), FA_RR8(r0, 16), FA_RR8(r0, 24),
+        FA_RR8(r1, 0), FA_RR8(r1, 8), FA_RR8(r1, 16), FA_RR8(r1, 24)
+      : "r"(a0), "r"(a1)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t (&r0)[32], uint32_t (&r1)[32], uint32_t (&r2)[32], uint32_t (&r3)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%129];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95}, [%130];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%131];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : FA_RR8(r0, 0), FA_RR8(r0, 8), FA_RR8(r0, 16), FA_RR8(r0, 24),
+        FA_RR8(r1, 0), FA_RR8(r1, 8), FA_RR8(r1, 16), FA_RR8(r1, 24),
+        FA_RR8(r2, 0), FA_RR8(r2, 8), FA_RR8(r2, 16), FA_RR8(r2, 24),
+        FA_RR8(r3, 0), FA_RR8(r3, 8), FA_RR8(r3, 16), FA_RR8(r3, 24)
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+      : "memory");
+}
+#undef FA_RR8
+
+// Register reallocation between warpgroups (all four warps of a warpgroup execute
+// the same instruction). The per-thread counts of all warpgroups must sum to no
+// more than the registers the block was launched with, or an increase waits forever.
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 #define FA_W8(i) "r"(r[i + 0]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
                  "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {

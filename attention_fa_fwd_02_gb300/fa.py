@@ -20,7 +20,7 @@ FA_F32, FA_BF16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
           4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_SCRATCH_LIMIT"}
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string", "fa_version",
-           "fa_timing_enable", "fa_timing_read", "fa_fwd_noalloc")
+           "fa_timing_enable", "fa_timing_read", "fa_fwd_noalloc", "fa_selftest_timeout")
 # Size of the static device scratch behind fa_fwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -61,6 +61,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_version.argtypes = []
     lib.fa_version.restype = ctypes.c_char_p
+    lib.fa_selftest_timeout.argtypes = [ctypes.c_ulonglong, vp, vp]
+    lib.fa_selftest_timeout.restype = st
     lib.fa_timing_enable.argtypes = [st]
     lib.fa_timing_enable.restype = st
     lib.fa_timing_read.argtypes = [ctypes.POINTER(fa_kernel_time), st]
@@ -107,6 +109,11 @@ def fa_bwd(Q: int, K: int, V: int, O: int, dO: int, LSE: int, dQ: int, dK: int, 
 
 def fa_device_status(stream: int) -> int:
     return lib().fa_device_status(stream)
+
+
+def fa_selftest_timeout(limit_ns: int, roles_done: int, stream: int) -> int:
+    """Enqueue the barrier-timeout self test (see include/fa.h)."""
+    return lib().fa_selftest_timeout(int(limit_ns), roles_done, stream)
 
 
 def fa_timing_enable(on: bool) -> int:

@@ -204,6 +204,30 @@ def run_reference(args, rank, world):
     return 0
 
 
+# ------------------------------------------------------------------ ranks
+# Under torchrun every rank runs an independent problem of the same shape (the
+# path partitions by batch / kv group with no exchange), so the only cross-rank
+# operations are a barrier around the timed region and a max-reduce of the time.
+def rank_workload(w, rank):
+    """The workload a rank runs: same shape, its own seed."""
+    return w.with_(seed=w.seed + 7919 * rank)
+
+
+def max_over_ranks(value, dist, device=None):
+    """Max of a per-rank float over the process group (identity without one)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank, world, ms_max):
+    """Aggregate throughput: every rank's work over the slowest rank's time."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -219,7 +243,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     w = WORKLOADS[args.workload]
-    wr = w.with_(seed=w.seed + 7919 * rank)  # independent problem per rank
+    wr = rank_workload(w, rank)
     q, k, v, do = make_inputs(wr)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     p = fa.make_params(qd, kd, w.scale, w.causal, w.window)
@@ -272,11 +296,7 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop() if sampler else None
     fa.check_device_status()
     ms = statistics.mean(s.elapsed_time(e) for s, e in ev)
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist, dev)
 
     # ---- end to end through host buffers (pinned), copies inside the timed region
     hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
@@ -308,11 +328,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     fa.check_device_status()
-    ms_e2e = statistics.mean(s.elapsed_time(e) for s, e in ev2)
-    if dist is not None:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(statistics.mean(s.elapsed_time(e) for s, e in ev2), dist, dev)
 
     if rank != 0:
         if dist is not None:
@@ -320,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
         return 0
 
     fwd_fl, bwd_fl, vis = flops_for(w)
-    value = world * (fwd_fl + bwd_fl) / (ms_max * 1e-3) / 1e12
+    value = whole_job_tflops(fwd_fl + bwd_fl, world, ms_max)
     peaks, peak_src = load_peaks()
     peak = peaks["bf16_tflops_sustained"] if w.dtype == "bf16" else peaks["bf16_tflops_sustained"] / 2
     per_kernel = {}
@@ -365,7 +381,7 @@ def run_ours(args, rank, world, local_rank):
                      if peak_src == "measured" else "fallback 1.7 PFLOP/s sustained"},
         "kernels": {k_: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
                          for kk, vv in e.items()} for k_, e in per_kernel.items()},
-        "e2e": {"value": round(world * (fwd_fl + bwd_fl) / (ms_e2e * 1e-3) / 1e12, 3),
+        "e2e": {"value": round(whole_job_tflops(fwd_fl + bwd_fl, world, ms_e2e), 3),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clocks,

@@ -160,6 +160,20 @@ FA_API const char* fa_status_string(fa_status s);
 FA_API const char* fa_version(void);
 
 /*
+ * Failure-detection self test (a diagnostic; no counterpart on the source pages).
+ * Enqueues one small kernel built like the attention kernels -- TMEM allocation,
+ * a producer, a consumer and a third role synchronised by mbarriers -- in which
+ * the producer never issues its copy. Every wait in it gives up after `limit_ns`
+ * nanoseconds (0 < limit_ns <= 1e10); the expiry must be reported as
+ * FA_ERR_TIMEOUT by the next fa_device_status(), each of the three roles must
+ * leave (adding 1 to *roles_done, a caller-owned, 16-byte aligned device int
+ * that starts at 0), TMEM must be released, and the context stays usable.
+ * Returns FA_OK once enqueued.
+ */
+FA_API fa_status fa_selftest_timeout(unsigned long long limit_ns, int* roles_done,
+                                     fa_stream_t stream);
+
+/*
  * Kernel timing (a measurement aid; no counterpart on the source pages).
  * fa_timing_enable(1) makes every later fa_fwd / fa_bwd call record a CUDA event
  * pair around each kernel it launches, on the caller's stream; fa_timing_enable(0)

@@ -26,7 +26,7 @@ def _declared_symbols():
 def test_header_declares_the_abi():
     assert _declared_symbols() == {"fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string",
                                    "fa_version", "fa_timing_enable", "fa_timing_read",
-                                   "fa_fwd_noalloc"}
+                                   "fa_fwd_noalloc", "fa_selftest_timeout"}
 
 
 def test_library_exports_every_declared_symbol(fa):
@@ -44,6 +44,13 @@ def test_timing_read_empty(fa):
     # nothing recorded: no CUDA call needed, zero kernels reported
     assert fa.fa_timing_enable(False) == 0
     assert fa.fa_timing_read() == {}
+
+
+def test_selftest_timeout_rejects_bad_args(fa):
+    assert fa.fa_selftest_timeout(1000, 0, 0) == 1          # null counter
+    assert fa.fa_selftest_timeout(0, A, 0) == 1             # zero limit
+    assert fa.fa_selftest_timeout(20 * 10**9, A, 0) == 1    # limit above 10 s
+    assert fa.fa_selftest_timeout(1000, MIS, 0) == 3        # misaligned counter
 
 
 def test_status_strings(fa):
