@@ -81,8 +81,12 @@ struct BwdCfg {
   static constexpr uint32_t Q_RES = 2 * NSPLIT * BIG_TILE;
   static constexpr uint32_t Q_STAGE = NSPLIT * (2 * SMALL_TILE + T_TILE);
   static constexpr uint32_t Q_SMEM = Q_RES + Q_NST * Q_STAGE + 1024;
-  static constexpr int THREADS = 192;  // 4 softmax warps, MMA warp, TMA warp
-  static constexpr int MMA_WARP = 4, TMA_WARP = 5;
+  // 4 softmax warps; a score-MMA issuer (also owns TMEM), an accumulate-MMA issuer,
+  // the TMA producer and an idle warp. Separate issuers: after a burst of MMAs a
+  // warp's next barrier operation waits for that burst, so one issuer alternating
+  // score and accumulate bursts lets the tensor pipe drain at every switch.
+  static constexpr int THREADS = 256;
+  static constexpr int MMA_WARP = 4, ACC_WARP = 5, TMA_WARP = 6;
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM slot b (b = 0, 1): S | dP | P_lo | dS_lo, CH columns each (fp32 P / dS hi
   // overwrite S / dP; fp16 P / dS take the first CH/2 columns of S / dP).
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_kv, bar_full[NST], bar_empty[NST], bar_sp[2], bar_ds[2],
-      bar_done, bar_drain;
+      bar_accdone[2], bar_done, bar_drain[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int warp = warp_id(), lane = lane_id();
@@ -279,9 +283,13 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bar_kv, 1);
     for (int s = 0; s < NST; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(&bar_sp[s], 1); mbar_init(&bar_ds[s], 128); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_sp[s], 1);
+      mbar_init(&bar_ds[s], 128);
+      mbar_init(&bar_accdone[s], 1);
+      mbar_init(&bar_drain[s], 1);
+    }
     mbar_init(&bar_done, 1);
-    mbar_init(&bar_drain, 1);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -351,54 +359,50 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
         if (last[s] >= 0) drain_wait(&bar_full[s], last[s] & 1, a.limit_ns);
     }
   } else if (warp == C::MMA_WARP) {
+    // Score issuer: chunk c -> S^T = K Q^T and dP^T = V dO^T into TMEM slot c & 1,
+    // once the slot's previous chunk (c - 2) has been accumulated.
     if (lane == 0 && nc > 0) {
       bool ok = wait(&bar_kv, 0);
-      tc_fence_after();
-      // chunk c: S^T = K Q^T and dP^T = V dO^T into TMEM slot c & 1
-      auto scores = [&](int c) {
+      for (int c = 0; ok && c < nc; ++c) {
         const int st = c % NST, bb = c & 1;
-        if (!wait(&bar_full[st], (c / NST) & 1)) return false;
+        if (!(ok = wait(&bar_full[st], (c / NST) & 1))) break;
+        if (c >= 2 && !(ok = wait(&bar_accdone[bb], ((c - 2) >> 1) & 1))) break;
         tc_fence_after();
         issue_rowdot<C>(tmem + C::s_col(bb), sK(0), sK(C::NSPLIT - 1), sQc(st, 0),
                         sQc(st, C::NSPLIT - 1));
         issue_rowdot<C>(tmem + C::dp_col(bb), sV(0), sV(C::NSPLIT - 1), sdOc(st, 0),
                         sdOc(st, C::NSPLIT - 1));
         tc_commit(&bar_sp[bb]);
-        return true;
-      };
-      // chunk pc: dV += P^T dO, dK += dS^T Q, then release its smem stage
-      auto accumulate = [&](int pc) {
-        const int pb = pc & 1, pst = pc % NST;
-        if (!wait(&bar_ds[pb], (pc >> 1) & 1)) return false;
+      }
+      tc_commit(&bar_drain[0]);
+      drain_wait(&bar_drain[0], 0, a.limit_ns);
+    }
+  } else if (warp == C::ACC_WARP) {
+    // Accumulate issuer: chunk c -> dV += P^T dO, dK += dS^T Q once the softmax
+    // wrote P^T / dS^T; then the chunk's smem stage and TMEM slot are free.
+    if (lane == 0 && nc > 0) {
+      bool ok = true;
+      for (int c = 0; ok && c < nc; ++c) {
+        const int pb = c & 1, pst = c % NST;
+        if (!(ok = wait(&bar_ds[pb], (c >> 1) & 1))) break;
         tc_fence_after();
         if constexpr (!C::F32) {
-          issue_acc<C>(tmem + C::ACC0, tmem + C::s_col(pb), 0, sdOc(pst, 0), 0, pc > 0);
-          issue_acc<C>(tmem + C::ACC1, tmem + C::dp_col(pb), 0, sQc(pst, 0), 0, pc > 0);
+          issue_acc<C>(tmem + C::ACC0, tmem + C::s_col(pb), 0, sdOc(pst, 0), 0, c > 0);
+          issue_acc<C>(tmem + C::ACC1, tmem + C::dp_col(pb), 0, sQc(pst, 0), 0, c > 0);
         } else {
           issue_acc<C>(tmem + C::ACC0, tmem + C::s_col(pb), tmem + C::plo_col(pb), sdOt(pst, 0),
-                       sdOt(pst, 1), pc > 0);
+                       sdOt(pst, 1), c > 0);
           issue_acc<C>(tmem + C::ACC1, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sQt(pst, 0),
-                       sQt(pst, 1), pc > 0);
+                       sQt(pst, 1), c > 0);
         }
         tc_commit(&bar_empty[pst]);
-        return true;
-      };
-      for (int c = 0; ok && c <= nc; ++c) {
-        if constexpr (NST >= 2) {
-          // scores of chunk c overlap the softmax of chunk c - 1
-          if (c < nc && !(ok = scores(c))) break;
-          if (c >= 1 && !(ok = accumulate(c - 1))) break;
-        } else {
-          // one stage: chunk c can only be loaded once chunk c - 1 has been released
-          if (c >= 1 && !(ok = accumulate(c - 1))) break;
-          if (c < nc && !(ok = scores(c))) break;
-        }
+        tc_commit(&bar_accdone[pb]);
       }
       if (ok) tc_commit(&bar_done);
-      tc_commit(&bar_drain);
-      drain_wait(&bar_drain, 0, a.limit_ns);
+      tc_commit(&bar_drain[1]);
+      drain_wait(&bar_drain[1], 0, a.limit_ns);
     }
-  } else {
+  } else if (warp < C::MMA_WARP) {
     // softmax warps: thread = one key row j = one TMEM lane
     const int wq = warp;  // 0..3
     const int r_in = wq * 32 + lane;
@@ -484,7 +488,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_q, bar_full[NST], bar_empty[NST], bar_sp[2], bar_ds[2],
-      bar_done, bar_drain;
+      bar_accdone[2], bar_done, bar_drain[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int warp = warp_id(), lane = lane_id();
@@ -511,9 +515,13 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
     for (int s = 0; s < NST; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(&bar_sp[s], 1); mbar_init(&bar_ds[s], 128); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_sp[s], 1);
+      mbar_init(&bar_ds[s], 128);
+      mbar_init(&bar_accdone[s], 1);
+      mbar_init(&bar_drain[s], 1);
+    }
     mbar_init(&bar_done, 1);
-    mbar_init(&bar_drain, 1);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -568,37 +576,46 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
         if (last[s] >= 0) drain_wait(&bar_full[s], last[s] & 1, a.limit_ns);
     }
   } else if (warp == C::MMA_WARP) {
+    // Score issuer: chunk c -> S = Q K^T and dP = dO V^T into TMEM slot c & 1, once
+    // the slot's previous chunk (c - 2) has been accumulated.
     if (lane == 0 && nc > 0) {
       bool ok = wait(&bar_q, 0);
-      tc_fence_after();
-      for (int c = 0; ok && c <= nc; ++c) {
-        if (c < nc) {
-          const int st = c % NST, bb = c & 1;
-          if (!(ok = wait(&bar_full[st], (c / NST) & 1))) break;
-          tc_fence_after();
-          issue_rowdot<C>(tmem + C::s_col(bb), sQ(0), sQ(C::NSPLIT - 1), sKc(st, 0),
-                          sKc(st, C::NSPLIT - 1));  // S = Q K^T
-          issue_rowdot<C>(tmem + C::dp_col(bb), sdO(0), sdO(C::NSPLIT - 1), sVc(st, 0),
-                          sVc(st, C::NSPLIT - 1));  // dP = dO V^T
-          tc_commit(&bar_sp[bb]);
-        }
-        if (c >= 1) {
-          const int pc = c - 1, pb = pc & 1, pst = pc % NST;
-          if (!(ok = wait(&bar_ds[pb], (pc >> 1) & 1))) break;
-          tc_fence_after();
-          if constexpr (!C::F32)
-            issue_acc<C>(tmem + C::ACC0, tmem + C::dp_col(pb), 0, sKc(pst, 0), 0, pc > 0);
-          else
-            issue_acc<C>(tmem + C::ACC0, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sKt(pst, 0),
-                         sKt(pst, 1), pc > 0);
-          tc_commit(&bar_empty[pst]);
-        }
+      for (int c = 0; ok && c < nc; ++c) {
+        const int st = c % NST, bb = c & 1;
+        if (!(ok = wait(&bar_full[st], (c / NST) & 1))) break;
+        if (c >= 2 && !(ok = wait(&bar_accdone[bb], ((c - 2) >> 1) & 1))) break;
+        tc_fence_after();
+        issue_rowdot<C>(tmem + C::s_col(bb), sQ(0), sQ(C::NSPLIT - 1), sKc(st, 0),
+                        sKc(st, C::NSPLIT - 1));
+        issue_rowdot<C>(tmem + C::dp_col(bb), sdO(0), sdO(C::NSPLIT - 1), sVc(st, 0),
+                        sVc(st, C::NSPLIT - 1));
+        tc_commit(&bar_sp[bb]);
+      }
+      tc_commit(&bar_drain[0]);
+      drain_wait(&bar_drain[0], 0, a.limit_ns);
+    }
+  } else if (warp == C::ACC_WARP) {
+    // Accumulate issuer: chunk c -> dQ += dS K once the softmax wrote dS; then the
+    // chunk's smem stage and TMEM slot are free.
+    if (lane == 0 && nc > 0) {
+      bool ok = true;
+      for (int c = 0; ok && c < nc; ++c) {
+        const int pb = c & 1, pst = c % NST;
+        if (!(ok = wait(&bar_ds[pb], (c >> 1) & 1))) break;
+        tc_fence_after();
+        if constexpr (!C::F32)
+          issue_acc<C>(tmem + C::ACC0, tmem + C::dp_col(pb), 0, sKc(pst, 0), 0, c > 0);
+        else
+          issue_acc<C>(tmem + C::ACC0, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sKt(pst, 0),
+                       sKt(pst, 1), c > 0);
+        tc_commit(&bar_empty[pst]);
+        tc_commit(&bar_accdone[pb]);
       }
       if (ok) tc_commit(&bar_done);
-      tc_commit(&bar_drain);
-      drain_wait(&bar_drain, 0, a.limit_ns);
+      tc_commit(&bar_drain[1]);
+      drain_wait(&bar_drain[1], 0, a.limit_ns);
     }
-  } else {
+  } else if (warp < C::MMA_WARP) {
     const int wq = warp;
     const int r_in = wq * 32 + lane;
     const int i = i0 + r_in;
