@@ -55,24 +55,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread until the phase completes or `hint_ns`
+// passes, so a waiting warp does not spin and take issue slots from working warps.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // A wait that cannot hang: it gives up after `limit_ns` of wall time, or as soon as
 // another thread of the CTA has raised `*abort`. On giving up it raises `*abort`,
-// records `code` in the device status word and returns false.
+// records `code` in the device status word and returns false. Between checks the
+// thread sleeps in try_wait (at most 100 us at a time).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           unsigned int* status, uint32_t code,
                                           uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   if (*abort) return false;
   const uint64_t t0 = globaltimer();
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 63u) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > limit_ns) {
-        *abort = 1;
-        atomicOr(status, code);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      *abort = 1;
+      atomicOr(status, code);
+      return false;
     }
   }
 }
