@@ -79,6 +79,13 @@ struct FwdCfg {
   __host__ __device__ static constexpr uint32_t o_col(int q) { return 256u + (uint32_t)D * q; }
   static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory budget");
   static_assert(F32 ? (256 + D <= 512) : (256 + 2 * D <= 512), "TMEM budget");
+  // Epilogue: each softmax warp stages its 32 O rows in its quarter of the tile's Q
+  // buffer (free once the tile's last MMA has completed) as TMA boxes of 32 rows x
+  // 128 bytes with the 128-byte swizzle, several boxes per round.
+  static constexpr uint32_t O_BOX_BYTES = 32u * 128u;
+  static constexpr uint32_t STAGE_PER_WARP = NSPLIT * TILE_BYTES / 4;
+  static constexpr int BOXES_PER_ROUND = (int)(STAGE_PER_WARP / O_BOX_BYTES);
+  static_assert(BOXES_PER_ROUND >= 1 && STAGE_PER_WARP % 1024 == 0, "O staging layout");
 };
 
 template <class C>
@@ -133,12 +140,83 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
   }
 }
 
+// Epilogue of one softmax warp: O rows r_base .. r_base+31 of tile (bh), scaled by
+// inv = 1 / l, go through shared memory (box b of 32 rows x 128 bytes at
+// stage + (b % BOXES_PER_ROUND) * O_BOX_BYTES, 16-byte chunk c of row r at chunk
+// position c ^ (r % 8)) and leave by TMA stores, which drop rows past Sq. One row per
+// lane, as TMEM hands it out; the swizzle keeps the shared stores conflict-free.
+template <class C, bool OUT_BF16>
+__device__ __forceinline__ void store_o_rows(const CUtensorMap* tmO, uint32_t o_addr, bool have_o,
+                                             float inv, uint32_t stage, int r_base, bool any_row,
+                                             int bh) {
+  constexpr int COLS = OUT_BF16 ? 64 : 32;  // columns per 128-byte box row
+  constexpr int NBOX = C::D / COLS;
+  const uint32_t lane = lane_id();
+  const uint32_t sw = lane & 7u;
+#pragma unroll
+  for (int b = 0; b < NBOX; ++b) {
+    const int slot = b % C::BOXES_PER_ROUND;
+    if (slot == 0 && b > 0) {  // reuse of the staging area: the earlier stores must have read it
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+    }
+    const uint32_t row = stage + slot * C::O_BOX_BYTES + lane * 128u;
+    if constexpr (!OUT_BF16) {
+      uint32_t r[32];
+      if (have_o) {
+        tmem_ld32(o_addr + b * 32, r);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = 0u;
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(row + ((c ^ sw) << 4), __float_as_uint(__uint_as_float(r[4 * c]) * inv),
+                     __float_as_uint(__uint_as_float(r[4 * c + 1]) * inv),
+                     __float_as_uint(__uint_as_float(r[4 * c + 2]) * inv),
+                     __float_as_uint(__uint_as_float(r[4 * c + 3]) * inv));
+    } else {
+      uint32_t r0[32], r1[32];
+      if (have_o) {
+        tmem_ld32x2(o_addr + b * 64, o_addr + b * 64 + 32, r0, r1);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r0[k] = r1[k] = 0u;
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = (c % 4) * 8 + 2 * e;
+          const float x0 = __uint_as_float(c < 4 ? r0[k] : r1[k]) * inv;
+          const float x1 = __uint_as_float(c < 4 ? r0[k + 1] : r1[k + 1]) * inv;
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(x0, x1);
+          w[e] = *reinterpret_cast<uint32_t*>(&v2);
+        }
+        st_shared_v4(row + ((c ^ sw) << 4), w[0], w[1], w[2], w[3]);
+      }
+    }
+    if (slot == C::BOXES_PER_ROUND - 1 || b == NBOX - 1) {
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0 && any_row) {
+        for (int j = b - slot; j <= b; ++j)
+          tma_store_3d(tmO, stage + (j % C::BOXES_PER_ROUND) * C::O_BOX_BYTES, j * COLS, r_base, bh);
+        bulk_commit_group();
+      }
+    }
+  }
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
+}
+
 template <int D, bool F32>
 __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKlo,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmVlo,
-                  const FwdArgs a) {
+                  const __grid_constant__ CUtensorMap tmO, const FwdArgs a) {
   using C = FwdCfg<D, F32>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -411,42 +489,15 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
       tc_fence_after();
     }
     if (ok) {
-      const bool valid = i < a.Sq;
       const float inv = (l > 0.f) ? (1.f / l) : 0.f;
-      const size_t row = (size_t)bh * a.Sq + (size_t)(valid ? i : 0);
-#pragma unroll
-      for (int c = 0; c < C::D / 32; ++c) {
-        uint32_t r[32];
-        if (n > 0) {
-          tmem_ld32(o_addr + c * 32, r);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) r[k] = 0u;
-        }
-        if (valid) {
-          if (!a.out_bf16) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.O) + row * D + c * 32);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
-                                   __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.O) + row * D + c * 32);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint32_t w[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[8 * k + 2 * e]) * inv,
-                                                          __uint_as_float(r[8 * k + 2 * e + 1]) * inv);
-                w[e] = *reinterpret_cast<uint32_t*>(&v2);
-              }
-              dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
-        }
-      }
-      if (valid) a.LSE[row] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
+      if (i < a.Sq) a.LSE[(size_t)bh * a.Sq + i] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
+      // The tile's last MMA has completed (bar_o), so nothing reads Q_q any more.
+      const uint32_t stage = sQ(q, 0) + wq * C::STAGE_PER_WARP;
+      const int r_base = r0 + wq * 32;
+      if (a.out_bf16)
+        store_o_rows<C, true>(&tmO, o_addr, n > 0, inv, stage, r_base, r_base < a.Sq, bh);
+      else
+        store_o_rows<C, false>(&tmO, o_addr, n > 0, inv, stage, r_base, r_base < a.Sq, bh);
     }
   }
 
@@ -475,6 +526,14 @@ __global__ void fill_empty_kernel(void* O, float* LSE, size_t rows, int D, int o
 // ------------------------------------------------------------------ launcher
 namespace {
 
+// O as [B*H][Sq][D] in the output type; boxes of 32 rows x 128 bytes, 128-byte swizzle.
+template <int D>
+bool encode_o_map(CUtensorMap* m, void* O, const fa_params& p) {
+  const bool bf = p.out_dtype == FA_BF16;
+  return host::encode_tiled_3d(m, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                               bf ? 2 : 4, O, D, p.Sq, (uint64_t)p.B * p.H, D, bf ? 64 : 32, 32);
+}
+
 template <int D, bool F32>
 fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                   const fa_params& p, cudaStream_t stream) {
@@ -483,9 +542,9 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   const size_t nk = (size_t)p.B * p.HKV * p.Sk * D;
   const int grid_pp = 4 * host::sm_count();
   void* ws = nullptr;
-  CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo;
+  CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo, mO;
   const uint64_t BHq = (uint64_t)p.B * p.H, BHk = (uint64_t)p.B * p.HKV;
-  bool enc = true;
+  bool enc = encode_o_map<D>(&mO, O, p);
   if constexpr (!F32) {
     if (host::scratch_alloc(&ws, nk * 2, stream) != cudaSuccess) return FA_ERR_CUDA;
     {
@@ -550,7 +609,7 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
     host::KernelTimer kt(F32 ? "fa_fwd_kernel<64,f32>"
                              : (D == 128 ? "fa_fwd_kernel<128,bf16>" : "fa_fwd_kernel<64,bf16>"),
                          stream);
-    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, a);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, mO, a);
     e = cudaGetLastError();
   }
   cudaError_t e2 = host::scratch_free(ws, stream);
@@ -695,9 +754,9 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
   const size_t nq = (size_t)p.B * p.H * p.Sq * D;
   const size_t nk = (size_t)p.B * p.HKV * p.Sk * D;
   const int grid_pp = 4 * host::sm_count();
-  CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo;
+  CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo, mO;
   const uint64_t BHq = (uint64_t)p.B * p.H, BHk = (uint64_t)p.B * p.HKV;
-  bool enc = true;
+  bool enc = encode_o_map<D>(&mO, O, p);
   // The whole scratch region used below is rewritten by the pre-pass kernels on
   // every call, so nothing left over from an earlier call is ever read.
   if constexpr (!F32) {
@@ -750,7 +809,7 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
                                        (int)C::SMEM_ALLOC);
   if (e != cudaSuccess) return FA_ERR_CUDA;
   kern<<<(unsigned)(BHq * a.n_qgroups), C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo,
-                                                                            mV, mVlo, a);
+                                                                            mV, mVlo, mO, a);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
