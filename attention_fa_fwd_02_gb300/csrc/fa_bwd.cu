@@ -26,6 +26,7 @@
 #include "fa_common.cuh"
 #include "ptx.cuh"
 #include "fa_prepass.cuh"
+#include "fa_epilogue.cuh"
 
 namespace fa {
 using namespace ptx;
@@ -48,11 +49,12 @@ struct BwdArgs {
 };
 
 // Tensor maps of one kernel launch; index [split] selects the hi (0) / lo (1) copy.
+// dK / dV / dQ: the outputs, stored by TMA in boxes of 32 rows x 128 bytes.
 struct KVMaps {  // dkdv
-  CUtensorMap K[2], V[2], Qc[2], dOc[2], Qt[2], dOt[2], L, Dl;
+  CUtensorMap K[2], V[2], Qc[2], dOc[2], Qt[2], dOt[2], L, Dl, dK, dV;
 };
 struct QMaps {  // dq
-  CUtensorMap Q[2], dO[2], Kc[2], Vc[2], Kt[2];
+  CUtensorMap Q[2], dO[2], Kc[2], Vc[2], Kt[2], dQ;
 };
 
 template <int D_, bool F32_>
@@ -99,6 +101,11 @@ struct BwdCfg {
   static_assert(KV_SMEM <= 227u * 1024u && Q_SMEM <= 227u * 1024u, "shared memory budget");
   static_assert((F32 ? 4 * CH : 2 * CH) <= 128, "TMEM slot width");
   static_assert(256 + 2 * D <= 512, "TMEM budget");
+  // Epilogues stage each warp's rows from the start of shared memory (every operand
+  // buffer is spent by then): dV and dK side by side (dkdv), dQ (dq).
+  static constexpr uint32_t EPI_WARP = epi_warp_bytes<D, false>();
+  static_assert(4 * 2 * EPI_WARP <= KV_VEC_OFF && 4 * EPI_WARP <= Q_RES + Q_NST * Q_STAGE,
+                "epilogue staging");
 };
 
 // S (+)= A[128 x D] * B[CH x D]^T, both K-major in 128B-swizzled smem.
@@ -160,31 +167,6 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity, uint6
     if (globaltimer() - t0 > limit) return false;
   }
   return true;
-}
-
-// Store 32 consecutive fp32 values of one row (fp32 or bf16 destination).
-__device__ __forceinline__ void store_row32(void* base, size_t elem_off, const uint32_t (&r)[32],
-                                            float mul, int out_bf16) {
-  if (!out_bf16) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + elem_off);
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      dst[k] = make_float4(__uint_as_float(r[4 * k]) * mul, __uint_as_float(r[4 * k + 1]) * mul,
-                           __uint_as_float(r[4 * k + 2]) * mul, __uint_as_float(r[4 * k + 3]) * mul);
-  } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + elem_off);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[8 * k + 2 * e]) * mul,
-                                                  __uint_as_float(r[8 * k + 2 * e + 1]) * mul);
-        w[e] = *reinterpret_cast<uint32_t*>(&v2);
-      }
-      dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
 }
 
 // Load CH fp32 columns at `sa` and CH at `da` of this thread's TMEM lane, with a
@@ -449,24 +431,23 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       tc_fence_after();
     }
     if (ok) {
-      const bool valid = j < a.Sk;
-      const size_t row = (size_t)bg * a.Sk + (size_t)(valid ? j : 0);
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        void* dst = which == 0 ? a.dV : a.dK;
-        const float mul = which == 0 ? 1.f : a.scale;
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t r[32];
-          if (nc > 0) {
-            tmem_ld32(lane_addr + (which == 0 ? C::ACC0 : C::ACC1) + cc * 32, r);
-          } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) r[k] = 0u;
-          }
-          if (valid) store_row32(dst, row * D + cc * 32, r, mul, a.out_bf16);
-        }
+      // bar_done: every MMA has completed, so all operand buffers are free.
+      const uint32_t st_v = sbase + wq * 2 * C::EPI_WARP, st_k = st_v + C::EPI_WARP;
+      const int r_base = j0 + wq * 32;
+      const bool any = r_base < a.Sk;
+      if (a.out_bf16) {
+        store_rows_tma<D, true, D / 64, false>(&m.dV, lane_addr + C::ACC0, nc > 0, 1.f, st_v,
+                                               r_base, any, bg);
+        store_rows_tma<D, true, D / 64, false>(&m.dK, lane_addr + C::ACC1, nc > 0, a.scale, st_k,
+                                               r_base, any, bg);
+      } else {
+        store_rows_tma<D, false, D / 32, false>(&m.dV, lane_addr + C::ACC0, nc > 0, 1.f, st_v,
+                                                r_base, any, bg);
+        store_rows_tma<D, false, D / 32, false>(&m.dK, lane_addr + C::ACC1, nc > 0, a.scale, st_k,
+                                                r_base, any, bg);
       }
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
   }
   tc_fence_before();
@@ -655,18 +636,15 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       tc_fence_after();
     }
     if (ok) {
-      const size_t row = (size_t)bh * a.Sq + (size_t)(row_valid ? i : 0);
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        if (nc > 0) {
-          tmem_ld32(lane_addr + C::ACC0 + cc * 32, r);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) r[k] = 0u;
-        }
-        if (row_valid) store_row32(a.dQ, row * D + cc * 32, r, a.scale, a.out_bf16);
-      }
+      // bar_done: every MMA has completed, so all operand buffers are free.
+      const uint32_t st_q = sbase + wq * C::EPI_WARP;
+      const int r_base = i0 + wq * 32;
+      if (a.out_bf16)
+        store_rows_tma<D, true, D / 64>(&m.dQ, lane_addr + C::ACC0, nc > 0, a.scale, st_q, r_base,
+                                        r_base < a.Sq, bh);
+      else
+        store_rows_tma<D, false, D / 32>(&m.dQ, lane_addr + C::ACC0, nc > 0, a.scale, st_q,
+                                         r_base, r_base < a.Sq, bh);
     }
   }
   tc_fence_before();
@@ -776,6 +754,14 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   QMaps mq;
   bool enc = true;
   enc &= host::encode_tiled_3d(&mk.L, F32T, 4, lse2, ldq, BH, 1, ldq, C::CH, 1, false);
+  {
+    const bool bf = p.out_dtype == FA_BF16;
+    const auto odt = bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : F32T;
+    const int oes = bf ? 2 : 4;
+    enc &= host::encode_tiled_3d(&mk.dK, odt, oes, dK, D, p.Sk, BHk, D, 128 / oes, 32);
+    enc &= host::encode_tiled_3d(&mk.dV, odt, oes, dV, D, p.Sk, BHk, D, 128 / oes, 32);
+    enc &= host::encode_tiled_3d(&mq.dQ, odt, oes, dQ, D, p.Sq, BH, D, 128 / oes, 32);
+  }
   enc &= host::encode_tiled_3d(&mk.Dl, F32T, 4, delta, ldq, BH, 1, ldq, C::CH, 1, false);
   if constexpr (!F32) {
     __half* q16 = reinterpret_cast<__half*>(delta + nvec);

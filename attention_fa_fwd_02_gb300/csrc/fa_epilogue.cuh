@@ -1,0 +1,105 @@
+// fa_epilogue.cuh -- writing a 128-row accumulator from TMEM to global memory.
+//
+// Each of the four epilogue warps owns 32 TMEM lanes = 32 output rows. A thread
+// holds one whole row (tcgen05.ld 32x32b), so storing straight from registers
+// would make every warp store touch 32 rows / 32 cache lines. Instead each warp
+// stages its rows in shared memory as TMA boxes of 32 rows x 128 bytes in the
+// 128-byte swizzled layout (16-byte chunk c of row r at chunk position c ^ (r % 8),
+// which keeps the shared stores free of bank conflicts) and writes them out with
+// tensor stores, which also drop rows past the tensor's end.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr uint32_t EPI_BOX_BYTES = 32u * 128u;  // one box: 32 rows x 128 bytes
+
+// Shared-memory bytes one warp needs to stage all its boxes at once.
+template <int D, bool OUT_BF16>
+constexpr uint32_t epi_warp_bytes() {
+  return (uint32_t)(D * (OUT_BF16 ? 2 : 4) / 128) * EPI_BOX_BYTES;
+}
+
+// Rows r_base .. r_base + 31 of slab z: columns [0, D) of the fp32 accumulator at
+// TMEM address t_addr (this warp's lane base), times mul, in the output type of
+// the tensor map `tm` (fp32, or bf16 when OUT_BF16). `stage` (1024-byte aligned)
+// holds BOXES boxes; with fewer boxes than the row needs, the warp waits for the
+// previous stores to have read the staging area before refilling it. have == false
+// writes zeros (no accumulator). any_row == false skips the stores (all rows are
+// past the tensor's end). With WAIT, every store has completed on return; without,
+// the caller issues bulk_wait_all() (lane 0) before the staging area is reused or
+// the CTA exits.
+template <int D, bool OUT_BF16, int BOXES, bool WAIT = true>
+__device__ __forceinline__ void store_rows_tma(const CUtensorMap* tm, uint32_t t_addr, bool have,
+                                               float mul, uint32_t stage, int r_base, bool any_row,
+                                               int z) {
+  using namespace ptx;
+  constexpr int COLS = OUT_BF16 ? 64 : 32;  // output columns per 128-byte box row
+  constexpr int NBOX = D / COLS;
+  static_assert(BOXES >= 1 && D % COLS == 0, "epilogue staging");
+  const uint32_t lane = lane_id();
+  const uint32_t sw = lane & 7u;
+#pragma unroll
+  for (int b = 0; b < NBOX; ++b) {
+    const int slot = b % BOXES;
+    if (slot == 0 && b > 0) {
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+    }
+    const uint32_t row = stage + slot * EPI_BOX_BYTES + lane * 128u;
+    if constexpr (!OUT_BF16) {
+      uint32_t r[32];
+      if (have) {
+        tmem_ld32(t_addr + b * 32, r);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = 0u;
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(row + ((c ^ sw) << 4), __float_as_uint(__uint_as_float(r[4 * c]) * mul),
+                     __float_as_uint(__uint_as_float(r[4 * c + 1]) * mul),
+                     __float_as_uint(__uint_as_float(r[4 * c + 2]) * mul),
+                     __float_as_uint(__uint_as_float(r[4 * c + 3]) * mul));
+    } else {
+      uint32_t r0[32], r1[32];
+      if (have) {
+        tmem_ld32x2(t_addr + b * 64, t_addr + b * 64 + 32, r0, r1);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r0[k] = r1[k] = 0u;
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = (c % 4) * 8 + 2 * e;
+          const float x0 = __uint_as_float(c < 4 ? r0[k] : r1[k]) * mul;
+          const float x1 = __uint_as_float(c < 4 ? r0[k + 1] : r1[k + 1]) * mul;
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(x0, x1);
+          w[e] = *reinterpret_cast<uint32_t*>(&v2);
+        }
+        st_shared_v4(row + ((c ^ sw) << 4), w[0], w[1], w[2], w[3]);
+      }
+    }
+    if (slot == BOXES - 1 || b == NBOX - 1) {
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0 && any_row) {
+        for (int j = b - slot; j <= b; ++j)
+          tma_store_3d(tm, stage + (j % BOXES) * EPI_BOX_BYTES, j * COLS, r_base, z);
+        bulk_commit_group();
+      }
+    }
+  }
+  if constexpr (WAIT) {
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+}
+
+}  // namespace fa

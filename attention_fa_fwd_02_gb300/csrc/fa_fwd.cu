@@ -11,9 +11,10 @@
 //                     m (log2 units) and sum l, writes P back into TMEM (fp16 for
 //                     bf16 inputs; tf32 hi + lo for fp32 inputs), rescales its O
 //                     row in TMEM when m grows by more than RESCALE_THRESHOLD, and
-//                     in the epilogue writes O = acc / l and LSE = (m + log2 l) ln 2.
-//   warp 4*NQ         MMA issuer (one thread): S_q = Q_q K_j^T, O_q += P_q V_j.
-//   warp 4*NQ + 1     TMA producer (one thread): Q once, then K_j / V_j rings.
+//                     in the epilogue writes LSE = (m + log2 l) ln 2 and O = acc / l
+//                     (staged in the tile's spent Q buffer, written by TMA stores).
+//   warp 4*NQ + q     MMA issuer of tile q (one thread): S_q = Q_q K_j^T, O_q += P_q V_j.
+//   warp 5*NQ         TMA producer (one thread): Q once, then K_j / V_j rings.
 // Every barrier wait is bounded; on expiry the kernel raises the device status
 // word, drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cfloat>
@@ -23,6 +24,7 @@
 #include "fa_common.cuh"
 #include "ptx.cuh"
 #include "fa_prepass.cuh"
+#include "fa_epilogue.cuh"
 
 namespace fa {
 using namespace ptx;
@@ -80,12 +82,10 @@ struct FwdCfg {
   static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory budget");
   static_assert(F32 ? (256 + D <= 512) : (256 + 2 * D <= 512), "TMEM budget");
   // Epilogue: each softmax warp stages its 32 O rows in its quarter of the tile's Q
-  // buffer (free once the tile's last MMA has completed) as TMA boxes of 32 rows x
-  // 128 bytes with the 128-byte swizzle, several boxes per round.
-  static constexpr uint32_t O_BOX_BYTES = 32u * 128u;
+  // buffer, free once the tile's last MMA has completed.
   static constexpr uint32_t STAGE_PER_WARP = NSPLIT * TILE_BYTES / 4;
-  static constexpr int BOXES_PER_ROUND = (int)(STAGE_PER_WARP / O_BOX_BYTES);
-  static_assert(BOXES_PER_ROUND >= 1 && STAGE_PER_WARP % 1024 == 0, "O staging layout");
+  static constexpr int STAGE_BOXES = (int)(STAGE_PER_WARP / EPI_BOX_BYTES);
+  static_assert(STAGE_BOXES >= 1 && STAGE_PER_WARP % 1024 == 0, "O staging layout");
 };
 
 template <class C>
@@ -138,77 +138,6 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
       mma_tf32_ts(o_tmem, plo_tmem + kk * 8, vh, id, 1);
     }
   }
-}
-
-// Epilogue of one softmax warp: O rows r_base .. r_base+31 of tile (bh), scaled by
-// inv = 1 / l, go through shared memory (box b of 32 rows x 128 bytes at
-// stage + (b % BOXES_PER_ROUND) * O_BOX_BYTES, 16-byte chunk c of row r at chunk
-// position c ^ (r % 8)) and leave by TMA stores, which drop rows past Sq. One row per
-// lane, as TMEM hands it out; the swizzle keeps the shared stores conflict-free.
-template <class C, bool OUT_BF16>
-__device__ __forceinline__ void store_o_rows(const CUtensorMap* tmO, uint32_t o_addr, bool have_o,
-                                             float inv, uint32_t stage, int r_base, bool any_row,
-                                             int bh) {
-  constexpr int COLS = OUT_BF16 ? 64 : 32;  // columns per 128-byte box row
-  constexpr int NBOX = C::D / COLS;
-  const uint32_t lane = lane_id();
-  const uint32_t sw = lane & 7u;
-#pragma unroll
-  for (int b = 0; b < NBOX; ++b) {
-    const int slot = b % C::BOXES_PER_ROUND;
-    if (slot == 0 && b > 0) {  // reuse of the staging area: the earlier stores must have read it
-      if (lane == 0) bulk_wait_read_all();
-      __syncwarp();
-    }
-    const uint32_t row = stage + slot * C::O_BOX_BYTES + lane * 128u;
-    if constexpr (!OUT_BF16) {
-      uint32_t r[32];
-      if (have_o) {
-        tmem_ld32(o_addr + b * 32, r);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) r[k] = 0u;
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_shared_v4(row + ((c ^ sw) << 4), __float_as_uint(__uint_as_float(r[4 * c]) * inv),
-                     __float_as_uint(__uint_as_float(r[4 * c + 1]) * inv),
-                     __float_as_uint(__uint_as_float(r[4 * c + 2]) * inv),
-                     __float_as_uint(__uint_as_float(r[4 * c + 3]) * inv));
-    } else {
-      uint32_t r0[32], r1[32];
-      if (have_o) {
-        tmem_ld32x2(o_addr + b * 64, o_addr + b * 64 + 32, r0, r1);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) r0[k] = r1[k] = 0u;
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k = (c % 4) * 8 + 2 * e;
-          const float x0 = __uint_as_float(c < 4 ? r0[k] : r1[k]) * inv;
-          const float x1 = __uint_as_float(c < 4 ? r0[k + 1] : r1[k + 1]) * inv;
-          __nv_bfloat162 v2 = __floats2bfloat162_rn(x0, x1);
-          w[e] = *reinterpret_cast<uint32_t*>(&v2);
-        }
-        st_shared_v4(row + ((c ^ sw) << 4), w[0], w[1], w[2], w[3]);
-      }
-    }
-    if (slot == C::BOXES_PER_ROUND - 1 || b == NBOX - 1) {
-      fence_async_shared();
-      __syncwarp();
-      if (lane == 0 && any_row) {
-        for (int j = b - slot; j <= b; ++j)
-          tma_store_3d(tmO, stage + (j % C::BOXES_PER_ROUND) * C::O_BOX_BYTES, j * COLS, r_base, bh);
-        bulk_commit_group();
-      }
-    }
-  }
-  if (lane == 0) bulk_wait_all();
-  __syncwarp();
 }
 
 template <int D, bool F32>
@@ -495,9 +424,11 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
       const uint32_t stage = sQ(q, 0) + wq * C::STAGE_PER_WARP;
       const int r_base = r0 + wq * 32;
       if (a.out_bf16)
-        store_o_rows<C, true>(&tmO, o_addr, n > 0, inv, stage, r_base, r_base < a.Sq, bh);
+        store_rows_tma<D, true, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
+                                                 r_base < a.Sq, bh);
       else
-        store_o_rows<C, false>(&tmO, o_addr, n > 0, inv, stage, r_base, r_base < a.Sq, bh);
+        store_rows_tma<D, false, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
+                                                  r_base < a.Sq, bh);
     }
   }
 
