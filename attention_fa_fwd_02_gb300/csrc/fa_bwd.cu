@@ -90,17 +90,21 @@ struct BwdCfg {
   static constexpr int THREADS = 256;
   static constexpr int MMA_WARP = 4, ACC_WARP = 5, TMA_WARP = 6;
   static constexpr uint32_t TMEM_COLS = 512;
-  // TMEM slot b (b = 0, 1): S | dP | P_lo | dS_lo, CH columns each (fp32 P / dS hi
-  // overwrite S / dP; fp16 P / dS take the first CH/2 columns of S / dP).
+  // TMEM slots: S | dP | P_lo | dS_lo, CH columns each (fp32 P / dS hi overwrite
+  // S / dP; fp16 P / dS take the first CH/2 columns of S / dP). A ring of slots
+  // lets the tensor core score chunk c+1.. while the softmax works on chunk c:
+  // dkdv has room for two slots next to its dV and dK accumulators, dq for three.
+  static constexpr int KV_NSLOT = 2, Q_NSLOT = 3;
   __host__ __device__ static constexpr uint32_t s_col(int b) { return 128u * b; }
   __host__ __device__ static constexpr uint32_t dp_col(int b) { return 128u * b + CH; }
   __host__ __device__ static constexpr uint32_t plo_col(int b) { return 128u * b + 2 * CH; }
   __host__ __device__ static constexpr uint32_t dslo_col(int b) { return 128u * b + 3 * CH; }
-  static constexpr uint32_t ACC0 = 256;      // dV (dkdv) / dQ (dq)
-  static constexpr uint32_t ACC1 = 256 + D;  // dK (dkdv)
+  static constexpr uint32_t KV_ACC0 = 128 * KV_NSLOT;      // dV (dkdv)
+  static constexpr uint32_t KV_ACC1 = 128 * KV_NSLOT + D;  // dK (dkdv)
+  static constexpr uint32_t Q_ACC = 128 * Q_NSLOT;         // dQ (dq)
   static_assert(KV_SMEM <= 227u * 1024u && Q_SMEM <= 227u * 1024u, "shared memory budget");
   static_assert((F32 ? 4 * CH : 2 * CH) <= 128, "TMEM slot width");
-  static_assert(256 + 2 * D <= 512, "TMEM budget");
+  static_assert(KV_ACC1 + D <= TMEM_COLS && Q_ACC + D <= TMEM_COLS, "TMEM budget");
   // Epilogues stage each warp's rows from the start of shared memory (every operand
   // buffer is spent by then): dV and dK side by side (dkdv), dQ (dq).
   static constexpr uint32_t EPI_WARP = epi_warp_bytes<D, false>();
@@ -369,12 +373,12 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
         if (!(ok = wait(&bar_ds[pb], (c >> 1) & 1))) break;
         tc_fence_after();
         if constexpr (!C::F32) {
-          issue_acc<C>(tmem + C::ACC0, tmem + C::s_col(pb), 0, sdOc(pst, 0), 0, c > 0);
-          issue_acc<C>(tmem + C::ACC1, tmem + C::dp_col(pb), 0, sQc(pst, 0), 0, c > 0);
+          issue_acc<C>(tmem + C::KV_ACC0, tmem + C::s_col(pb), 0, sdOc(pst, 0), 0, c > 0);
+          issue_acc<C>(tmem + C::KV_ACC1, tmem + C::dp_col(pb), 0, sQc(pst, 0), 0, c > 0);
         } else {
-          issue_acc<C>(tmem + C::ACC0, tmem + C::s_col(pb), tmem + C::plo_col(pb), sdOt(pst, 0),
+          issue_acc<C>(tmem + C::KV_ACC0, tmem + C::s_col(pb), tmem + C::plo_col(pb), sdOt(pst, 0),
                        sdOt(pst, 1), c > 0);
-          issue_acc<C>(tmem + C::ACC1, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sQt(pst, 0),
+          issue_acc<C>(tmem + C::KV_ACC1, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sQt(pst, 0),
                        sQt(pst, 1), c > 0);
         }
         tc_commit(&bar_empty[pst]);
@@ -436,14 +440,14 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       const int r_base = j0 + wq * 32;
       const bool any = r_base < a.Sk;
       if (a.out_bf16) {
-        store_rows_tma<D, true, D / 64, false>(&m.dV, lane_addr + C::ACC0, nc > 0, 1.f, st_v,
+        store_rows_tma<D, true, D / 64, false>(&m.dV, lane_addr + C::KV_ACC0, nc > 0, 1.f, st_v,
                                                r_base, any, bg);
-        store_rows_tma<D, true, D / 64, false>(&m.dK, lane_addr + C::ACC1, nc > 0, a.scale, st_k,
+        store_rows_tma<D, true, D / 64, false>(&m.dK, lane_addr + C::KV_ACC1, nc > 0, a.scale, st_k,
                                                r_base, any, bg);
       } else {
-        store_rows_tma<D, false, D / 32, false>(&m.dV, lane_addr + C::ACC0, nc > 0, 1.f, st_v,
+        store_rows_tma<D, false, D / 32, false>(&m.dV, lane_addr + C::KV_ACC0, nc > 0, 1.f, st_v,
                                                 r_base, any, bg);
-        store_rows_tma<D, false, D / 32, false>(&m.dK, lane_addr + C::ACC1, nc > 0, a.scale, st_k,
+        store_rows_tma<D, false, D / 32, false>(&m.dK, lane_addr + C::KV_ACC1, nc > 0, a.scale, st_k,
                                                 r_base, any, bg);
       }
       if (lane == 0) bulk_wait_all();
@@ -468,8 +472,9 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_q, bar_full[NST], bar_empty[NST], bar_sp[2], bar_ds[2],
-      bar_accdone[2], bar_done, bar_drain[2];
+  constexpr int NSL = C::Q_NSLOT;
+  __shared__ __align__(8) uint64_t bar_q, bar_full[NST], bar_empty[NST], bar_sp[NSL], bar_ds[NSL],
+      bar_accdone[NSL], bar_done, bar_drain[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int warp = warp_id(), lane = lane_id();
@@ -496,12 +501,12 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
     for (int s = 0; s < NST; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NSL; ++s) {
       mbar_init(&bar_sp[s], 1);
       mbar_init(&bar_ds[s], 128);
       mbar_init(&bar_accdone[s], 1);
-      mbar_init(&bar_drain[s], 1);
     }
+    for (int s = 0; s < 2; ++s) mbar_init(&bar_drain[s], 1);
     mbar_init(&bar_done, 1);
     abort_sh = 0;
     fence_mbar_init();
@@ -557,14 +562,14 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
         if (last[s] >= 0) drain_wait(&bar_full[s], last[s] & 1, a.limit_ns);
     }
   } else if (warp == C::MMA_WARP) {
-    // Score issuer: chunk c -> S = Q K^T and dP = dO V^T into TMEM slot c & 1, once
-    // the slot's previous chunk (c - 2) has been accumulated.
+    // Score issuer: chunk c -> S = Q K^T and dP = dO V^T into TMEM slot c % NSL,
+    // once the slot's previous chunk (c - NSL) has been accumulated.
     if (lane == 0 && nc > 0) {
       bool ok = wait(&bar_q, 0);
       for (int c = 0; ok && c < nc; ++c) {
-        const int st = c % NST, bb = c & 1;
+        const int st = c % NST, bb = c % NSL;
         if (!(ok = wait(&bar_full[st], (c / NST) & 1))) break;
-        if (c >= 2 && !(ok = wait(&bar_accdone[bb], ((c - 2) >> 1) & 1))) break;
+        if (c >= NSL && !(ok = wait(&bar_accdone[bb], ((c / NSL) - 1) & 1))) break;
         tc_fence_after();
         issue_rowdot<C>(tmem + C::s_col(bb), sQ(0), sQ(C::NSPLIT - 1), sKc(st, 0),
                         sKc(st, C::NSPLIT - 1));
@@ -581,13 +586,13 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
     if (lane == 0 && nc > 0) {
       bool ok = true;
       for (int c = 0; ok && c < nc; ++c) {
-        const int pb = c & 1, pst = c % NST;
-        if (!(ok = wait(&bar_ds[pb], (c >> 1) & 1))) break;
+        const int pb = c % NSL, pst = c % NST;
+        if (!(ok = wait(&bar_ds[pb], (c / NSL) & 1))) break;
         tc_fence_after();
         if constexpr (!C::F32)
-          issue_acc<C>(tmem + C::ACC0, tmem + C::dp_col(pb), 0, sKc(pst, 0), 0, c > 0);
+          issue_acc<C>(tmem + C::Q_ACC, tmem + C::dp_col(pb), 0, sKc(pst, 0), 0, c > 0);
         else
-          issue_acc<C>(tmem + C::ACC0, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sKt(pst, 0),
+          issue_acc<C>(tmem + C::Q_ACC, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sKt(pst, 0),
                        sKt(pst, 1), c > 0);
         tc_commit(&bar_empty[pst]);
         tc_commit(&bar_accdone[pb]);
@@ -610,9 +615,9 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
     const int lo_i = a.window > 0 ? i - a.window + 1 : INT_MIN / 2;
     bool ok = true;
     for (int c = 0; c < nc; ++c) {
-      const int bb = c & 1;
+      const int bb = c % NSL;
       const int k0 = (kc_lo + c) * CH;
-      ok = __all_sync(0xffffffffu, wait(&bar_sp[bb], (c >> 1) & 1));
+      ok = __all_sync(0xffffffffu, wait(&bar_sp[bb], (c / NSL) & 1));
       if (!ok) break;
       tc_fence_after();
       float s[CH], dp[CH];
@@ -640,11 +645,286 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       const uint32_t st_q = sbase + wq * C::EPI_WARP;
       const int r_base = i0 + wq * 32;
       if (a.out_bf16)
-        store_rows_tma<D, true, D / 64>(&m.dQ, lane_addr + C::ACC0, nc > 0, a.scale, st_q, r_base,
+        store_rows_tma<D, true, D / 64>(&m.dQ, lane_addr + C::Q_ACC, nc > 0, a.scale, st_q, r_base,
                                         r_base < a.Sq, bh);
       else
-        store_rows_tma<D, false, D / 32>(&m.dQ, lane_addr + C::ACC0, nc > 0, a.scale, st_q,
+        store_rows_tma<D, false, D / 32>(&m.dQ, lane_addr + C::Q_ACC, nc > 0, a.scale, st_q,
                                          r_base, r_base < a.Sq, bh);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// --------------------------------------------------------- dQ, fp16 operands
+// bf16 inputs: one CTA per (batch, head, 128-query tile), 128-key chunks, so the
+// score MMAs are 128 x 128 (a 128 x 64 MMA reads 3/4 of the shared-memory bytes of a
+// 128 x 128 one for half the work, and the dq kernel is bound by those reads).
+// TMEM: S slot [0, 128), dP slot [128, 256), two fp16 dS operand slots of 64
+// columns at 256 / 320, dQ at 384. The S and dP slots are single: the softmax
+// releases each as soon as it has loaded it, so chunk c+1's S = Q K^T runs while
+// the softmax finishes chunk c. Eight softmax warps: warps w and w+4 share TMEM
+// lanes 32*(w%4).., w < 4 taking keys [0, 64) of the chunk, w >= 4 keys [64, 128).
+template <int D>
+struct Dq16Cfg {
+  static constexpr int NCB = D / 64;                     // 128-byte column blocks per row
+  static constexpr uint32_t CB = 128u * 128u;            // column block of a 128-row tile
+  static constexpr uint32_t TILE = NCB * CB;
+  static constexpr int KST = 3, VST = 2;                 // K is held until dQ += dS K
+  static constexpr uint32_t Q_OFF = 0, DO_OFF = TILE, K_OFF = 2 * TILE;
+  static constexpr uint32_t V_OFF = K_OFF + KST * TILE;
+  static constexpr uint32_t SMEM = V_OFF + VST * TILE + 1024;
+  static constexpr int SOFTMAX_WARPS = 8;
+  static constexpr int MMA_WARP = 8, ACC_WARP = 9, TMA_WARP = 10;
+  static constexpr int THREADS = 384;
+  static constexpr uint32_t REGS_SOFTMAX = 200, REGS_CONTROL = 96;
+  static_assert(256 * REGS_SOFTMAX + 128 * REGS_CONTROL <= 384 * 168, "register split");
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t S_COL = 0, DP_COL = 128, DS_COL = 256, ACC = 384;
+  static constexpr uint32_t EPI_WARP = epi_warp_bytes<D, false>();
+  static_assert(SMEM <= 227u * 1024u, "shared memory budget");
+  static_assert(4 * EPI_WARP <= 2 * TILE + KST * TILE, "epilogue staging");
+};
+
+template <int D>
+__device__ __forceinline__ void issue_rowdot128(uint32_t d, uint32_t a, uint32_t b) {
+  constexpr uint32_t id = make_idesc(128, 128, FMT_F16, FMT_F16, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk * 16 / 64) * Dq16Cfg<D>::CB + (kk * 16 % 64) * 2;
+    mma_f16_ss(d, make_sdesc(a + off, 16, SW128_ATOM), make_sdesc(b + off, 16, SW128_ATOM), id,
+               kk > 0);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
+    fa_bwd_dq16_kernel(const __grid_constant__ QMaps m, const BwdArgs a) {
+  using C = Dq16Cfg<D>;
+  constexpr int KST = C::KST, VST = C::VST;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bar_qd, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST],
+      bar_vempty[VST], bar_s, bar_dp, bar_sfree, bar_dpfree, bar_ds[2], bar_accdone[2], bar_done,
+      bar_drain[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  const int warp = warp_id(), lane = lane_id();
+  volatile int* abort_flag = &abort_sh;
+
+  const int qt_lin = blockIdx.x / a.BHx;
+  const int bh = blockIdx.x % a.BHx;
+  const int qt = a.lpt ? (a.n_tiles - 1 - qt_lin) : qt_lin;
+  const int b = bh / a.H, h = bh % a.H;
+  const int bg = b * a.HKV + h / (a.H / a.HKV);
+  const int i0 = qt * BLOCK_M;
+  int kt_lo, kt_hi;
+  kv_tile_range(i0, min(i0 + BLOCK_M - 1, a.Sq - 1), a.Sk, a.causal, a.window, &kt_lo, &kt_hi);
+  const int nc = kt_hi - kt_lo;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_qd, 1);
+    for (int s = 0; s < KST; ++s) { mbar_init(&bar_kfull[s], 1); mbar_init(&bar_kempty[s], 1); }
+    for (int s = 0; s < VST; ++s) { mbar_init(&bar_vfull[s], 1); mbar_init(&bar_vempty[s], 1); }
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_dp, 1);
+    mbar_init(&bar_sfree, 256);
+    mbar_init(&bar_dpfree, 256);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_ds[s], 256);
+      mbar_init(&bar_accdone[s], 1);
+      mbar_init(&bar_drain[s], 1);
+    }
+    mbar_init(&bar_done, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    __syncwarp();
+    tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t sbase = smem_u32(smem);
+  auto sK = [&](int st) { return sbase + C::K_OFF + st * C::TILE; };
+  auto sV = [&](int st) { return sbase + C::V_OFF + st * C::TILE; };
+  auto gen = [&](uint32_t s) { return smem + (s - sbase); };
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    return mbar_wait(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
+  };
+
+  if (warp >= C::SOFTMAX_WARPS) {
+  regs_decrease<C::REGS_CONTROL>();
+  if (warp == C::TMA_WARP) {
+    if (lane == 0 && nc > 0) {
+      tma_prefetch_desc(&m.Q[0]); tma_prefetch_desc(&m.Kc[0]); tma_prefetch_desc(&m.Vc[0]);
+      mbar_arrive_expect_tx(&bar_qd, 2 * C::TILE);
+      for (int cb = 0; cb < C::NCB; ++cb) {
+        tma_load_3d(gen(sbase + C::Q_OFF) + cb * C::CB, &m.Q[0], &bar_qd, cb * 64, i0, bh);
+        tma_load_3d(gen(sbase + C::DO_OFF) + cb * C::CB, &m.dO[0], &bar_qd, cb * 64, i0, bh);
+      }
+      int last_k[KST], last_v[VST];
+      for (int s = 0; s < KST; ++s) last_k[s] = -1;
+      for (int s = 0; s < VST; ++s) last_v[s] = -1;
+      for (int c = 0; c < nc; ++c) {
+        const int k0 = (kt_lo + c) * BLOCK_N;
+        const int ks = c % KST, vs = c % VST;
+        if (!wait(&bar_kempty[ks], ((c / KST) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(&bar_kfull[ks], C::TILE);
+        for (int cb = 0; cb < C::NCB; ++cb)
+          tma_load_3d(gen(sK(ks)) + cb * C::CB, &m.Kc[0], &bar_kfull[ks], cb * 64, k0, bg);
+        last_k[ks] = c / KST;
+        if (!wait(&bar_vempty[vs], ((c / VST) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(&bar_vfull[vs], C::TILE);
+        for (int cb = 0; cb < C::NCB; ++cb)
+          tma_load_3d(gen(sV(vs)) + cb * C::CB, &m.Vc[0], &bar_vfull[vs], cb * 64, k0, bg);
+        last_v[vs] = c / VST;
+      }
+      drain_wait(&bar_qd, 0, a.limit_ns);
+      for (int s = 0; s < KST; ++s)
+        if (last_k[s] >= 0) drain_wait(&bar_kfull[s], last_k[s] & 1, a.limit_ns);
+      for (int s = 0; s < VST; ++s)
+        if (last_v[s] >= 0) drain_wait(&bar_vfull[s], last_v[s] & 1, a.limit_ns);
+    }
+  } else if (warp == C::MMA_WARP) {
+    // Score issuer: S(c) = Q K_c^T once the softmax has loaded S(c-1); dP(c) = dO V_c^T
+    // once it has loaded dP(c-1).
+    if (lane == 0 && nc > 0) {
+      bool ok = wait(&bar_qd, 0);
+      for (int c = 0; ok && c < nc; ++c) {
+        const int ks = c % KST, vs = c % VST;
+        if (!(ok = wait(&bar_kfull[ks], (c / KST) & 1))) break;
+        if (c > 0 && !(ok = wait(&bar_sfree, (c - 1) & 1))) break;
+        tc_fence_after();
+        issue_rowdot128<D>(tmem + C::S_COL, sbase + C::Q_OFF, sK(ks));
+        tc_commit(&bar_s);
+        if (!(ok = wait(&bar_vfull[vs], (c / VST) & 1))) break;
+        if (c > 0 && !(ok = wait(&bar_dpfree, (c - 1) & 1))) break;
+        tc_fence_after();
+        issue_rowdot128<D>(tmem + C::DP_COL, sbase + C::DO_OFF, sV(vs));
+        tc_commit(&bar_dp);
+        tc_commit(&bar_vempty[vs]);
+      }
+      tc_commit(&bar_drain[0]);
+      drain_wait(&bar_drain[0], 0, a.limit_ns);
+    }
+  } else if (warp == C::ACC_WARP) {
+    // Accumulate issuer: dQ += dS(c) K_c (dS fp16 in TMEM, K_c MN-major); then K_c's
+    // stage and the dS slot are free.
+    if (lane == 0 && nc > 0) {
+      constexpr uint32_t id = make_idesc(128, D, FMT_F16, FMT_F16, false, true);
+      bool ok = true;
+      for (int c = 0; ok && c < nc; ++c) {
+        const int pb = c & 1, ks = c % KST;
+        if (!(ok = wait(&bar_ds[pb], (c >> 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+          mma_f16_ts(tmem + C::ACC, tmem + C::DS_COL + 64 * pb + kk * 8,
+                     make_sdesc(sK(ks) + kk * 16 * 128, C::CB, SW128_ATOM), id,
+                     (c > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&bar_kempty[ks]);
+        tc_commit(&bar_accdone[pb]);
+      }
+      if (ok) tc_commit(&bar_done);
+      tc_commit(&bar_drain[1]);
+      drain_wait(&bar_drain[1], 0, a.limit_ns);
+    }
+  }  // the idle warp falls through
+  } else {
+    regs_increase<C::REGS_SOFTMAX>();
+    const int wq = warp % 4, half = warp / 4;
+    const int i = i0 + wq * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    const float sl2 = a.scale_log2;
+    const bool row_valid = i < a.Sq;
+    const size_t vrow = (size_t)bh * a.ldq + (size_t)(row_valid ? i : 0);
+    const float nl = row_valid ? -a.lse2[vrow] : -INFINITY;
+    const float dl = row_valid ? a.delta[vrow] : 0.f;
+    const int hi_i = a.causal ? min(i, a.Sk - 1) : a.Sk - 1;
+    const int lo_i = a.window > 0 ? i - a.window + 1 : INT_MIN / 2;
+    bool ok = true;
+    for (int c = 0; c < nc; ++c) {
+      const int pb = c & 1;
+      const int kc0 = (kt_lo + c) * BLOCK_N;
+      const int k0 = kc0 + half * 64;
+      float s[64], dp[64];
+      ok = __all_sync(0xffffffffu, wait(&bar_s, c & 1));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32x2(lane_addr + C::S_COL + half * 64, lane_addr + C::S_COL + half * 64 + 32, r0, r1);
+        tc_fence_before();
+        mbar_arrive(&bar_sfree);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          s[k] = __uint_as_float(r0[k]);
+          s[32 + k] = __uint_as_float(r1[k]);
+        }
+      }
+      if (tile_needs_mask(i0, i0 + BLOCK_M - 1, kc0, kc0 + BLOCK_N - 1, a.Sk, a.causal, a.window)) {
+        const int rel_hi = hi_i - k0, rel_lo = lo_i - k0;
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          if (k > rel_hi || k < rel_lo) s[k] = -INFINITY;
+      }
+#pragma unroll
+      for (int k = 0; k < 64; ++k) s[k] = ex2(fmaf(s[k], sl2, nl));
+      ok = __all_sync(0xffffffffu, wait(&bar_dp, c & 1));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32x2(lane_addr + C::DP_COL + half * 64, lane_addr + C::DP_COL + half * 64 + 32, r0, r1);
+        tc_fence_before();
+        mbar_arrive(&bar_dpfree);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          dp[k] = __uint_as_float(r0[k]);
+          dp[32 + k] = __uint_as_float(r1[k]);
+        }
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        pk[k] = pack_half2(s[2 * k] * (dp[2 * k] - dl), s[2 * k + 1] * (dp[2 * k + 1] - dl));
+      // the dS slot is free once dQ += dS(c-2) K has completed
+      if (c >= 2) {
+        ok = __all_sync(0xffffffffu, wait(&bar_accdone[pb], ((c >> 1) - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      tmem_st32(lane_addr + C::DS_COL + 64 * pb + half * 32, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_ds[pb]);
+    }
+    if (half == 0) {
+      if (ok && nc > 0) {
+        ok = __all_sync(0xffffffffu, wait(&bar_done, 0));
+        tc_fence_after();
+      }
+      if (ok) {
+        // bar_done: every MMA has completed, so all operand buffers are free.
+        const uint32_t st_q = sbase + wq * C::EPI_WARP;
+        const int r_base = i0 + wq * 32;
+        if (a.out_bf16)
+          store_rows_tma<D, true, D / 64>(&m.dQ, lane_addr + C::ACC, nc > 0, a.scale, st_q,
+                                          r_base, r_base < a.Sq, bh);
+        else
+          store_rows_tma<D, false, D / 32>(&m.dQ, lane_addr + C::ACC, nc > 0, a.scale, st_q,
+                                           r_base, r_base < a.Sq, bh);
+      }
     }
   }
   tc_fence_before();
@@ -787,8 +1067,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     enc &= host::encode_tiled_3d(&mk.dOc[0], F16, 2, do16, D, p.Sq, BH, D, 64, C::CH);
     enc &= host::encode_tiled_3d(&mq.Q[0], F16, 2, q16, D, p.Sq, BH, D, 64, 128);
     enc &= host::encode_tiled_3d(&mq.dO[0], F16, 2, do16, D, p.Sq, BH, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mq.Kc[0], F16, 2, k16, D, p.Sk, BHk, D, 64, C::CH);
-    enc &= host::encode_tiled_3d(&mq.Vc[0], F16, 2, v16, D, p.Sk, BHk, D, 64, C::CH);
+    enc &= host::encode_tiled_3d(&mq.Kc[0], F16, 2, k16, D, p.Sk, BHk, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mq.Vc[0], F16, 2, v16, D, p.Sk, BHk, D, 64, 128);
     mk.K[1] = mk.K[0]; mk.V[1] = mk.V[0]; mk.Qc[1] = mk.Qc[0]; mk.dOc[1] = mk.dOc[0];
     mk.Qt[0] = mk.Qt[1] = mk.Qc[0]; mk.dOt[0] = mk.dOt[1] = mk.dOc[0];
     mq.Q[1] = mq.Q[0]; mq.dO[1] = mq.dO[0]; mq.Kc[1] = mq.Kc[0]; mq.Vc[1] = mq.Vc[0];
@@ -878,15 +1158,24 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     BwdArgs aq = a;
     aq.n_tiles = (p.Sq + BLOCK_M - 1) / BLOCK_M;
     aq.BHx = (int)BH;
-    auto kern = fa_bwd_dq_kernel<D, F32>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::Q_SMEM);
-    if (e == cudaSuccess) {
-      host::KernelTimer kt(F32 ? "fa_bwd_dq_kernel<64,f32>"
-                               : (D == 128 ? "fa_bwd_dq_kernel<128,bf16>"
-                                           : "fa_bwd_dq_kernel<64,bf16>"),
-                           stream);
-      kern<<<(unsigned)(BH * aq.n_tiles), C::THREADS, C::Q_SMEM, stream>>>(mq, aq);
-      e = cudaGetLastError();
+    if constexpr (F32) {
+      auto kern = fa_bwd_dq_kernel<D, F32>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::Q_SMEM);
+      if (e == cudaSuccess) {
+        host::KernelTimer kt("fa_bwd_dq_kernel<64,f32>", stream);
+        kern<<<(unsigned)(BH * aq.n_tiles), C::THREADS, C::Q_SMEM, stream>>>(mq, aq);
+        e = cudaGetLastError();
+      }
+    } else {
+      using C16 = Dq16Cfg<D>;
+      auto kern = fa_bwd_dq16_kernel<D>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C16::SMEM);
+      if (e == cudaSuccess) {
+        host::KernelTimer kt(D == 128 ? "fa_bwd_dq_kernel<128,bf16>" : "fa_bwd_dq_kernel<64,bf16>",
+                             stream);
+        kern<<<(unsigned)(BH * aq.n_tiles), C16::THREADS, C16::SMEM, stream>>>(mq, aq);
+        e = cudaGetLastError();
+      }
     }
   }
   const cudaError_t e2 = host::scratch_free(ws, stream);
