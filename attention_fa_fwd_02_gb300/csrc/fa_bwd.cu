@@ -936,6 +936,284 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
   }
 }
 
+// ------------------------------------------------------ dK / dV, fp16 operands
+// bf16 inputs: one CTA per (batch, kv head, 128-key tile), 128-query chunks of every
+// grouped query head that can see the tile, so the score MMAs are 128 x 128.
+// TMEM: S^T slot [0, 128), dP^T slot [128, 256), dV, dK accumulators after them.
+// The softmax writes P^T / dS^T (fp16) back into the first half of each 64-column
+// half of its own slot. Two issuers, each owning one slot and one accumulator:
+//   issuer A: S^T(c) = K Q_c^T, then (once P^T(c) is written) dV += P^T(c) dO_c;
+//   issuer B: dP^T(c) = V dO_c^T, then (once dS^T(c) is written) dK += dS^T(c) Q_c.
+// A thread's MMAs run in issue order, so S^T(c+1) may overwrite the slot right
+// after dV(c) has been issued (likewise dP^T(c+1) after dK(c)), and each issuer's
+// bursts fill the tensor pipe while the other waits for the softmax.
+template <int D>
+struct Dkv16Cfg {
+  static constexpr int NCB = D / 64;
+  static constexpr uint32_t CB = 128u * 128u;
+  static constexpr uint32_t TILE = NCB * CB;            // 128 rows x D fp16
+  static constexpr int NST = D == 128 ? 2 : 3;          // (Q, dO) chunk stages
+  static constexpr uint32_t K_OFF = 0, V_OFF = TILE, ST_OFF = 2 * TILE;
+  static constexpr uint32_t STAGE = 2 * TILE;
+  static constexpr uint32_t VEC = 2 * 128 * 4;          // lse2 | delta of a chunk
+  static constexpr uint32_t VEC_OFF = ST_OFF + NST * STAGE;
+  static constexpr uint32_t SMEM = VEC_OFF + NST * VEC + 1024;
+  static constexpr int SOFTMAX_WARPS = 8;
+  static constexpr int A_WARP = 8, B_WARP = 9, TMA_WARP = 10;
+  static constexpr int THREADS = 384;
+  static constexpr uint32_t REGS_SOFTMAX = 200, REGS_CONTROL = 96;
+  static_assert(256 * REGS_SOFTMAX + 128 * REGS_CONTROL <= 384 * 168, "register split");
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t S_COL = 0, DP_COL = 128, DV = 256, DK = 256 + D;
+  static constexpr uint32_t EPI_WARP = epi_warp_bytes<D, false>();
+  static_assert(SMEM <= 227u * 1024u, "shared memory budget");
+  static_assert(DK + D <= TMEM_COLS, "TMEM budget");
+  static_assert(8 * EPI_WARP <= VEC_OFF, "epilogue staging");
+  // fp16 operand column of k-step kk (16 queries): halves of 64 queries sit at
+  // columns 0 and 64 of the slot, 8 columns per k-step.
+  __host__ __device__ static constexpr uint32_t op_col(int kk) { return (kk / 4) * 64 + (kk % 4) * 8; }
+};
+
+// ACC[128 x D] (+)= A(TMEM fp16, 128 x 128, halves at columns 0 / 64) * B[128 x D]
+// (MN-major fp16 tile in smem).
+template <int D>
+__device__ __forceinline__ void issue_acc128(uint32_t acc, uint32_t a_tmem, uint32_t b,
+                                             bool accumulate) {
+  constexpr uint32_t id = make_idesc(128, D, FMT_F16, FMT_F16, false, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_f16_ts(acc, a_tmem + Dkv16Cfg<D>::op_col(kk),
+               make_sdesc(b + kk * 16 * 128, Dkv16Cfg<D>::CB, SW128_ATOM), id,
+               (accumulate || kk > 0) ? 1u : 0u);
+}
+
+template <int D>
+__global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
+    fa_bwd_dkdv16_kernel(const __grid_constant__ KVMaps m, const BwdArgs a) {
+  using C = Dkv16Cfg<D>;
+  constexpr int NST = C::NST;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bar_kv, bar_full[NST], bar_empty[NST], bar_s, bar_dp, bar_p,
+      bar_ds, bar_done, bar_drain[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  const int warp = warp_id(), lane = lane_id();
+  volatile int* abort_flag = &abort_sh;
+
+  const int jt = blockIdx.x / a.BHx;
+  const int bg = blockIdx.x % a.BHx;
+  const int b = bg / a.HKV, g = bg % a.HKV;
+  const int rep = a.H / a.HKV;
+  const int j0 = jt * BLOCK_N;
+  int qt_lo, qt_hi;
+  q_tile_range(j0, min(j0 + BLOCK_N - 1, a.Sk - 1), a.Sq, a.causal, a.window, &qt_lo, &qt_hi);
+  const int ncq = qt_hi - qt_lo;
+  const int nc = rep * ncq;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_kv, 1);
+    for (int s = 0; s < NST; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 2); }
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_dp, 1);
+    mbar_init(&bar_p, 256);
+    mbar_init(&bar_ds, 256);
+    mbar_init(&bar_done, 2);
+    for (int s = 0; s < 2; ++s) mbar_init(&bar_drain[s], 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::A_WARP) {
+    __syncwarp();
+    tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t sbase = smem_u32(smem);
+  auto sQc = [&](int st) { return sbase + C::ST_OFF + st * C::STAGE; };
+  auto sdOc = [&](int st) { return sbase + C::ST_OFF + st * C::STAGE + C::TILE; };
+  float* vecs = reinterpret_cast<float*>(smem + C::VEC_OFF);  // [NST][2][128]
+  auto gen = [&](uint32_t s) { return smem + (s - sbase); };
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    return mbar_wait(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
+  };
+  auto chunk_rows = [&](int c, int* bh, int* i0) {
+    const int r = c / ncq, qt = qt_lo + c % ncq;
+    *bh = b * a.H + g * rep + r;
+    *i0 = qt * BLOCK_M;
+  };
+
+  if (warp >= C::SOFTMAX_WARPS) {
+  regs_decrease<C::REGS_CONTROL>();
+  if (warp == C::TMA_WARP) {
+    if (lane == 0 && nc > 0) {
+      tma_prefetch_desc(&m.K[0]); tma_prefetch_desc(&m.Qc[0]); tma_prefetch_desc(&m.dOc[0]);
+      mbar_arrive_expect_tx(&bar_kv, 2 * C::TILE);
+      for (int cb = 0; cb < C::NCB; ++cb) {
+        tma_load_3d(gen(sbase + C::K_OFF) + cb * C::CB, &m.K[0], &bar_kv, cb * 64, j0, bg);
+        tma_load_3d(gen(sbase + C::V_OFF) + cb * C::CB, &m.V[0], &bar_kv, cb * 64, j0, bg);
+      }
+      int last[NST];
+      for (int s = 0; s < NST; ++s) last[s] = -1;
+      for (int c = 0; c < nc; ++c) {
+        const int st = c % NST;
+        if (!wait(&bar_empty[st], ((c / NST) & 1) ^ 1)) break;
+        int bh, i0;
+        chunk_rows(c, &bh, &i0);
+        mbar_arrive_expect_tx(&bar_full[st], C::STAGE + C::VEC);
+        for (int cb = 0; cb < C::NCB; ++cb) {
+          tma_load_3d(gen(sQc(st)) + cb * C::CB, &m.Qc[0], &bar_full[st], cb * 64, i0, bh);
+          tma_load_3d(gen(sdOc(st)) + cb * C::CB, &m.dOc[0], &bar_full[st], cb * 64, i0, bh);
+        }
+        tma_load_3d(vecs + st * 256, &m.L, &bar_full[st], i0, bh, 0);
+        tma_load_3d(vecs + st * 256 + 128, &m.Dl, &bar_full[st], i0, bh, 0);
+        last[st] = c / NST;
+      }
+      drain_wait(&bar_kv, 0, a.limit_ns);
+      for (int s = 0; s < NST; ++s)
+        if (last[s] >= 0) drain_wait(&bar_full[s], last[s] & 1, a.limit_ns);
+    }
+  } else if (warp == C::A_WARP || warp == C::B_WARP) {
+    const bool is_a = warp == C::A_WARP;
+    if (lane == 0 && nc > 0) {
+      const uint32_t slot = tmem + (is_a ? C::S_COL : C::DP_COL);
+      const uint32_t acc = tmem + (is_a ? C::DV : C::DK);
+      const uint32_t lhs = sbase + (is_a ? C::K_OFF : C::V_OFF);
+      uint64_t* scored = is_a ? &bar_s : &bar_dp;
+      uint64_t* ready = is_a ? &bar_p : &bar_ds;
+      bool ok = wait(&bar_kv, 0);
+      for (int c = 0; ok && c < nc; ++c) {
+        const int st = c % NST;
+        // A: S^T = K Q^T, dV += P^T dO.  B: dP^T = V dO^T, dK += dS^T Q.
+        const uint32_t rhs = is_a ? sQc(st) : sdOc(st);
+        const uint32_t other = is_a ? sdOc(st) : sQc(st);
+        if (!(ok = wait(&bar_full[st], (c / NST) & 1))) break;
+        tc_fence_after();
+        issue_rowdot128<D>(slot, lhs, rhs);
+        tc_commit(scored);
+        if (!(ok = wait(ready, c & 1))) break;
+        tc_fence_after();
+        issue_acc128<D>(acc, slot, other, c > 0);
+        tc_commit(&bar_empty[st]);
+      }
+      if (ok) tc_commit(&bar_done);
+      tc_commit(&bar_drain[is_a ? 0 : 1]);
+      drain_wait(&bar_drain[is_a ? 0 : 1], 0, a.limit_ns);
+    }
+  }  // the idle warp falls through
+  } else {
+    regs_increase<C::REGS_SOFTMAX>();
+    // thread = key row j = TMEM lane; warps w and w + 4 take queries [0, 64) / [64, 128)
+    const int wq = warp % 4, half = warp / 4;
+    const int j = j0 + wq * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    const float sl2 = a.scale_log2;
+    const bool row_dead = j >= a.Sk;
+    bool ok = true;
+    for (int c = 0; c < nc; ++c) {
+      const int st = c % NST;
+      int bh, i0;
+      chunk_rows(c, &bh, &i0);
+      const int q0 = i0 + half * 64;  // first query of this thread's half
+      float s[64];
+      ok = __all_sync(0xffffffffu, wait(&bar_s, c & 1) && wait(&bar_full[st], (c / NST) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32x2(lane_addr + C::S_COL + half * 64, lane_addr + C::S_COL + half * 64 + 32, r0, r1);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          s[k] = __uint_as_float(r0[k]);
+          s[32 + k] = __uint_as_float(r1[k]);
+        }
+      }
+      // query i = q0 + k sees key j iff (!causal || j <= i) && (!window || j >= i-w+1)
+      // && i < Sq && j < Sk
+      if (tile_needs_mask(i0, i0 + BLOCK_M - 1, j0, j0 + BLOCK_N - 1, a.Sk, a.causal, a.window) ||
+          i0 + BLOCK_M > a.Sq) {
+        const int k_lo = a.causal ? j - q0 : INT_MIN / 2;
+        const int k_hi = min(a.window > 0 ? j + a.window - 1 - q0 : INT_MAX / 2, a.Sq - 1 - q0);
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          if (row_dead || k < k_lo || k > k_hi) s[k] = -INFINITY;
+      }
+      const float4* lv = reinterpret_cast<const float4*>(vecs + st * 256 + half * 64);
+#pragma unroll
+      for (int k4 = 0; k4 < 16; ++k4) {
+        const float4 l4 = lv[k4];
+        s[4 * k4] = ex2(fmaf(s[4 * k4], sl2, -l4.x));
+        s[4 * k4 + 1] = ex2(fmaf(s[4 * k4 + 1], sl2, -l4.y));
+        s[4 * k4 + 2] = ex2(fmaf(s[4 * k4 + 2], sl2, -l4.z));
+        s[4 * k4 + 3] = ex2(fmaf(s[4 * k4 + 3], sl2, -l4.w));
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) pk[k] = pack_half2(s[2 * k], s[2 * k + 1]);
+        tmem_st32(lane_addr + C::S_COL + half * 64, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_p);
+      ok = __all_sync(0xffffffffu, wait(&bar_dp, c & 1));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32x2(lane_addr + C::DP_COL + half * 64, lane_addr + C::DP_COL + half * 64 + 32, r0,
+                    r1);
+        const float4* dv = reinterpret_cast<const float4*>(vecs + st * 256 + 128 + half * 64);
+        uint32_t pk[32];
+#pragma unroll
+        for (int k4 = 0; k4 < 16; ++k4) {
+          const float4 d4 = dv[k4];
+          const int k = 4 * k4;
+          const float g0 = __uint_as_float(k < 32 ? r0[k] : r1[k - 32]);
+          const float g1 = __uint_as_float(k < 32 ? r0[k + 1] : r1[k - 31]);
+          const float g2 = __uint_as_float(k < 32 ? r0[k + 2] : r1[k - 30]);
+          const float g3 = __uint_as_float(k < 32 ? r0[k + 3] : r1[k - 29]);
+          pk[2 * k4] = pack_half2(s[k] * (g0 - d4.x), s[k + 1] * (g1 - d4.y));
+          pk[2 * k4 + 1] = pack_half2(s[k + 2] * (g2 - d4.z), s[k + 3] * (g3 - d4.w));
+        }
+        tmem_st32(lane_addr + C::DP_COL + half * 64, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar_ds);
+    }
+    if (ok && nc > 0) {
+      ok = __all_sync(0xffffffffu, wait(&bar_done, 0));
+      tc_fence_after();
+    }
+    if (ok) {
+      // bar_done: every MMA has completed, so all operand buffers are free. Warps
+      // w < 4 write dV, warps w >= 4 dK, rows j0 + 32 (w % 4) ...
+      const uint32_t stage = sbase + warp * C::EPI_WARP;
+      const int r_base = j0 + wq * 32;
+      const bool any = r_base < a.Sk;
+      const uint32_t acc = lane_addr + (half ? C::DK : C::DV);
+      const CUtensorMap* tm = half ? &m.dK : &m.dV;
+      const float mul = half ? a.scale : 1.f;
+      if (a.out_bf16)
+        store_rows_tma<D, true, D / 64>(tm, acc, nc > 0, mul, stage, r_base, any, bg);
+      else
+        store_rows_tma<D, false, D / 32>(tm, acc, nc > 0, mul, stage, r_base, any, bg);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::A_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 // -------------------------------------------------------------- preprocess
 __device__ __forceinline__ void load4(const void* base, size_t off, int is_bf16, float (&v)[4]) {
   if (is_bf16) {
@@ -1017,7 +1295,7 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   using C = BwdCfg<D, F32>;
   const size_t BH = (size_t)p.B * p.H, BHk = (size_t)p.B * p.HKV;
   const size_t nq = BH * p.Sq * D, nk = BHk * p.Sk * D;
-  const int ldq = (p.Sq + 63) / 64 * 64;
+  const int ldq = (p.Sq + 127) / 128 * 128;  // lse2 / delta row pitch: whole 128-query chunks
   const size_t nvec = BH * ldq;
   const int ldqt = (p.Sq + 3) / 4 * 4, ldkt = (p.Sk + 3) / 4 * 4;  // transposed row pitch
   const size_t nqt = BH * D * ldqt, nkt = BHk * D * ldkt;
@@ -1033,7 +1311,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   KVMaps mk;
   QMaps mq;
   bool enc = true;
-  enc &= host::encode_tiled_3d(&mk.L, F32T, 4, lse2, ldq, BH, 1, ldq, C::CH, 1, false);
+  const uint32_t qchunk = F32 ? C::CH : 128;  // query rows per dkdv chunk
+  enc &= host::encode_tiled_3d(&mk.L, F32T, 4, lse2, ldq, BH, 1, ldq, qchunk, 1, false);
   {
     const bool bf = p.out_dtype == FA_BF16;
     const auto odt = bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : F32T;
@@ -1042,7 +1321,7 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     enc &= host::encode_tiled_3d(&mk.dV, odt, oes, dV, D, p.Sk, BHk, D, 128 / oes, 32);
     enc &= host::encode_tiled_3d(&mq.dQ, odt, oes, dQ, D, p.Sq, BH, D, 128 / oes, 32);
   }
-  enc &= host::encode_tiled_3d(&mk.Dl, F32T, 4, delta, ldq, BH, 1, ldq, C::CH, 1, false);
+  enc &= host::encode_tiled_3d(&mk.Dl, F32T, 4, delta, ldq, BH, 1, ldq, qchunk, 1, false);
   if constexpr (!F32) {
     __half* q16 = reinterpret_cast<__half*>(delta + nvec);
     __half* do16 = q16 + nq;
@@ -1063,8 +1342,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     enc &= host::encode_tiled_3d(&mk.K[0], F16, 2, k16, D, p.Sk, BHk, D, 64, 128);
     enc &= host::encode_tiled_3d(&mk.V[0], F16, 2, v16, D, p.Sk, BHk, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mk.Qc[0], F16, 2, q16, D, p.Sq, BH, D, 64, C::CH);
-    enc &= host::encode_tiled_3d(&mk.dOc[0], F16, 2, do16, D, p.Sq, BH, D, 64, C::CH);
+    enc &= host::encode_tiled_3d(&mk.Qc[0], F16, 2, q16, D, p.Sq, BH, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mk.dOc[0], F16, 2, do16, D, p.Sq, BH, D, 64, 128);
     enc &= host::encode_tiled_3d(&mq.Q[0], F16, 2, q16, D, p.Sq, BH, D, 64, 128);
     enc &= host::encode_tiled_3d(&mq.dO[0], F16, 2, do16, D, p.Sq, BH, D, 64, 128);
     enc &= host::encode_tiled_3d(&mq.Kc[0], F16, 2, k16, D, p.Sk, BHk, D, 64, 128);
@@ -1143,15 +1422,24 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     BwdArgs ak = a;
     ak.n_tiles = (p.Sk + BLOCK_N - 1) / BLOCK_N;
     ak.BHx = (int)BHk;
-    auto kern = fa_bwd_dkdv_kernel<D, F32>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::KV_SMEM);
-    if (e == cudaSuccess) {
-      host::KernelTimer kt(F32 ? "fa_bwd_dkdv_kernel<64,f32>"
-                               : (D == 128 ? "fa_bwd_dkdv_kernel<128,bf16>"
-                                           : "fa_bwd_dkdv_kernel<64,bf16>"),
-                           stream);
-      kern<<<(unsigned)(BHk * ak.n_tiles), C::THREADS, C::KV_SMEM, stream>>>(mk, ak);
-      e = cudaGetLastError();
+    if constexpr (F32) {
+      auto kern = fa_bwd_dkdv_kernel<D, F32>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::KV_SMEM);
+      if (e == cudaSuccess) {
+        host::KernelTimer kt("fa_bwd_dkdv_kernel<64,f32>", stream);
+        kern<<<(unsigned)(BHk * ak.n_tiles), C::THREADS, C::KV_SMEM, stream>>>(mk, ak);
+        e = cudaGetLastError();
+      }
+    } else {
+      using C16 = Dkv16Cfg<D>;
+      auto kern = fa_bwd_dkdv16_kernel<D>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C16::SMEM);
+      if (e == cudaSuccess) {
+        host::KernelTimer kt(D == 128 ? "fa_bwd_dkdv_kernel<128,bf16>" : "fa_bwd_dkdv_kernel<64,bf16>",
+                             stream);
+        kern<<<(unsigned)(BHk * ak.n_tiles), C16::THREADS, C16::SMEM, stream>>>(mk, ak);
+        e = cudaGetLastError();
+      }
     }
   }
   if (e == cudaSuccess) {
