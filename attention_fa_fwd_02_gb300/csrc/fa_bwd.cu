@@ -1142,10 +1142,11 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         for (int k = 0; k < 64; ++k)
           if (row_dead || k < k_lo || k > k_hi) s[k] = -INFINITY;
       }
-      const float4* lv = reinterpret_cast<const float4*>(vecs + st * 256 + half * 64);
+      // lse2 / delta of the chunk's queries, read with explicit shared-space loads
+      const uint32_t lv = sbase + C::VEC_OFF + (st * 256 + half * 64) * 4;
 #pragma unroll
       for (int k4 = 0; k4 < 16; ++k4) {
-        const float4 l4 = lv[k4];
+        const float4 l4 = ld_shared_v4(lv + 16 * k4);
         s[4 * k4] = ex2(fmaf(s[4 * k4], sl2, -l4.x));
         s[4 * k4 + 1] = ex2(fmaf(s[4 * k4 + 1], sl2, -l4.y));
         s[4 * k4 + 2] = ex2(fmaf(s[4 * k4 + 2], sl2, -l4.z));
@@ -1167,11 +1168,11 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         uint32_t r0[32], r1[32];
         tmem_ld32x2(lane_addr + C::DP_COL + half * 64, lane_addr + C::DP_COL + half * 64 + 32, r0,
                     r1);
-        const float4* dv = reinterpret_cast<const float4*>(vecs + st * 256 + 128 + half * 64);
+        const uint32_t dv = sbase + C::VEC_OFF + (st * 256 + 128 + half * 64) * 4;
         uint32_t pk[32];
 #pragma unroll
         for (int k4 = 0; k4 < 16; ++k4) {
-          const float4 d4 = dv[k4];
+          const float4 d4 = ld_shared_v4(dv + 16 * k4);
           const int k = 4 * k4;
           const float g0 = __uint_as_float(k < 32 ? r0[k] : r1[k - 32]);
           const float g1 = __uint_as_float(k < 32 ? r0[k + 1] : r1[k - 31]);
