@@ -89,6 +89,17 @@ int sm_count() {
   return g_sms[dev];
 }
 
+cudaError_t max_dynamic_smem(const void* kernel, int* bytes) {
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa_attr;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa_attr, kernel);
+  if (e != cudaSuccess) return e;
+  *bytes = optin - (int)fa_attr.sharedSizeBytes;
+  return *bytes > 0 ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 namespace {
 struct Pending {
   const char* name;
@@ -229,6 +240,7 @@ FA_API fa_status fa_device_status(fa_stream_t stream) {
   cudaError_t e1 = cudaSuccess, e2 = cudaSuccess;
   const unsigned int v = read_and_clear_fwd_status(&e1) | read_and_clear_bwd_status(&e2);
   if (e1 != cudaSuccess || e2 != cudaSuccess) return FA_ERR_CUDA;
+  if (v & DEV_LAYOUT) return FA_ERR_LAYOUT;
   return (v & DEV_TIMEOUT) ? FA_ERR_TIMEOUT : FA_OK;
 }
 
@@ -241,6 +253,7 @@ FA_API const char* fa_status_string(fa_status s) {
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_TIMEOUT: return "kernel barrier wait timed out";
     case FA_ERR_SCRATCH_LIMIT: return "problem needs more than the static scratch of fa_fwd_noalloc";
+    case FA_ERR_LAYOUT: return "kernel shared-memory layout did not fit its allocation";
   }
   return "unknown status";
 }

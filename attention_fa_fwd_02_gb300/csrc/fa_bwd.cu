@@ -940,36 +940,40 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
 // bf16 inputs: one CTA per (batch, kv head, 128-key tile), 128-query chunks of every
 // grouped query head that can see the tile, so the score MMAs are 128 x 128.
 // TMEM: S^T slot [0, 128), dP^T slot [128, 256), dV, dK accumulators after them.
-// The softmax writes P^T / dS^T (fp16) back into the first half of each 64-column
-// half of its own slot. Two issuers, each owning one slot and one accumulator:
-//   issuer A: S^T(c) = K Q_c^T, then (once P^T(c) is written) dV += P^T(c) dO_c;
-//   issuer B: dP^T(c) = V dO_c^T, then (once dS^T(c) is written) dK += dS^T(c) Q_c.
-// A thread's MMAs run in issue order, so S^T(c+1) may overwrite the slot right
-// after dV(c) has been issued (likewise dP^T(c+1) after dK(c)), and each issuer's
-// bursts fill the tensor pipe while the other waits for the softmax.
+// Three issuers (a thread's MMAs run in issue order; an issuer stalls while the
+// tensor pipe is full, so independent streams get their own thread):
+//   S issuer:  S^T(c) = K Q_c^T as soon as the softmax has loaded S^T(c-1);
+//   dV issuer: dV += P^T(c) dO_c, P^T (fp16) written by the softmax to shared memory;
+//   B issuer:  dP^T(c) = V dO_c^T, then dK += dS^T(c) Q_c with dS^T (fp16) written
+//              by the softmax into the first half of each 64-column half of its
+//              slot, so dP^T(c+1) may overwrite the slot right after dK(c) is issued.
+// P^T lives in shared memory so that the next score tile can enter the tensor pipe
+// while the softmax is still exponentiating.
 template <int D>
 struct Dkv16Cfg {
   static constexpr int NCB = D / 64;
   static constexpr uint32_t CB = 128u * 128u;
   static constexpr uint32_t TILE = NCB * CB;            // 128 rows x D fp16
-  static constexpr int NST = D == 128 ? 2 : 3;          // (Q, dO) chunk stages
-  static constexpr uint32_t K_OFF = 0, V_OFF = TILE, ST_OFF = 2 * TILE;
-  static constexpr uint32_t STAGE = 2 * TILE;
-  static constexpr uint32_t VEC = 2 * 128 * 4;          // lse2 | delta of a chunk
-  static constexpr uint32_t VEC_OFF = ST_OFF + NST * STAGE;
-  static constexpr uint32_t SMEM = VEC_OFF + NST * VEC + 1024;
+  static constexpr int NS = D == 128 ? 2 : 3;           // Q and dO ring depth
+  static constexpr uint32_t K_OFF = 0, V_OFF = TILE, Q_OFF = 2 * TILE;
+  static constexpr uint32_t DO_OFF = Q_OFF + NS * TILE;
+  static constexpr uint32_t PT_OFF = DO_OFF + NS * TILE;  // P^T: 128 keys x 128 queries fp16
+  static constexpr uint32_t VEC = 2 * 128 * 4;            // lse2 | delta of a chunk
+  static constexpr uint32_t VEC_OFF = PT_OFF + 2 * CB;
+  static constexpr uint32_t LAYOUT = VEC_OFF + NS * VEC;  // bytes from the 1 KB-aligned base
   static constexpr int SOFTMAX_WARPS = 8;
-  static constexpr int A_WARP = 8, B_WARP = 9, TMA_WARP = 10;
+  static constexpr int A_WARP = 8, B_WARP = 9, TMA_WARP = 10, DV_WARP = 11;
   static constexpr int THREADS = 384;
   static constexpr uint32_t REGS_SOFTMAX = 200, REGS_CONTROL = 96;
   static_assert(256 * REGS_SOFTMAX + 128 * REGS_CONTROL <= 384 * 168, "register split");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DV = 256, DK = 256 + D;
   static constexpr uint32_t EPI_WARP = epi_warp_bytes<D, false>();
-  static_assert(SMEM <= 227u * 1024u, "shared memory budget");
+  // 227 KB per block minus the alignment of the base to 1 KB leaves 226 KB.
+  static_assert(LAYOUT <= 226u * 1024u, "shared memory budget");
   static_assert(DK + D <= TMEM_COLS, "TMEM budget");
   static_assert(8 * EPI_WARP <= VEC_OFF, "epilogue staging");
-  // fp16 operand column of k-step kk (16 queries): halves of 64 queries sit at
+  // fp16 dS^T column of k-step kk (16 queries): halves of 64 queries sit at
   // columns 0 and 64 of the slot, 8 columns per k-step.
   __host__ __device__ static constexpr uint32_t op_col(int kk) { return (kk / 4) * 64 + (kk % 4) * 8; }
 };
@@ -987,18 +991,42 @@ __device__ __forceinline__ void issue_acc128(uint32_t acc, uint32_t a_tmem, uint
                (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// ACC[128 x D] (+)= A[128 x 128] (K-major fp16 tile in smem) * B[128 x D] (MN-major).
+template <int D>
+__device__ __forceinline__ void issue_acc128_ss(uint32_t acc, uint32_t a, uint32_t b,
+                                                bool accumulate) {
+  constexpr uint32_t id = make_idesc(128, D, FMT_F16, FMT_F16, false, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t off = (kk * 16 / 64) * Dkv16Cfg<D>::CB + (kk * 16 % 64) * 2;
+    mma_f16_ss(acc, make_sdesc(a + off, 16, SW128_ATOM),
+               make_sdesc(b + kk * 16 * 128, Dkv16Cfg<D>::CB, SW128_ATOM), id,
+               (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     fa_bwd_dkdv16_kernel(const __grid_constant__ KVMaps m, const BwdArgs a) {
   using C = Dkv16Cfg<D>;
-  constexpr int NST = C::NST;
+  constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_kv, bar_full[NST], bar_empty[NST], bar_s, bar_dp, bar_p,
-      bar_ds, bar_done, bar_drain[2];
+  __shared__ __align__(8) uint64_t bar_kv, bar_qfull[NS], bar_qempty[NS], bar_dofull[NS],
+      bar_doempty[NS], bar_s, bar_sfree, bar_p, bar_dvdone, bar_dp, bar_ds, bar_done, bar_drain[3];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  {
+    // The layout needs LAYOUT bytes above the 1 KB-aligned base; the launch asks
+    // for as much dynamic shared memory as the block may have.
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (smem_u32(smem) + C::LAYOUT > smem_u32(smem_raw) + dyn) {
+      if (threadIdx.x == 0) atomicOr(&g_bwd_status, DEV_LAYOUT);
+      return;
+    }
+  }
   const int warp = warp_id(), lane = lane_id();
   volatile int* abort_flag = &abort_sh;
 
@@ -1014,13 +1042,20 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_kv, 1);
-    for (int s = 0; s < NST; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 2); }
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bar_qfull[s], 1);
+      mbar_init(&bar_qempty[s], 2);   // S^T(c) (A) and dK(c) (B) have read Q_c
+      mbar_init(&bar_dofull[s], 1);
+      mbar_init(&bar_doempty[s], 2);  // dP^T(c) (B) and dV(c) (A) have read dO_c
+    }
     mbar_init(&bar_s, 1);
-    mbar_init(&bar_dp, 1);
+    mbar_init(&bar_sfree, 256);
     mbar_init(&bar_p, 256);
+    mbar_init(&bar_dvdone, 1);
+    mbar_init(&bar_dp, 1);
     mbar_init(&bar_ds, 256);
-    mbar_init(&bar_done, 2);
-    for (int s = 0; s < 2; ++s) mbar_init(&bar_drain[s], 1);
+    mbar_init(&bar_done, 2);  // dV issuer and B issuer
+    for (int s = 0; s < 3; ++s) mbar_init(&bar_drain[s], 1);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -1034,9 +1069,8 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t sbase = smem_u32(smem);
-  auto sQc = [&](int st) { return sbase + C::ST_OFF + st * C::STAGE; };
-  auto sdOc = [&](int st) { return sbase + C::ST_OFF + st * C::STAGE + C::TILE; };
-  float* vecs = reinterpret_cast<float*>(smem + C::VEC_OFF);  // [NST][2][128]
+  auto sQ = [&](int st) { return sbase + C::Q_OFF + st * C::TILE; };
+  auto sdO = [&](int st) { return sbase + C::DO_OFF + st * C::TILE; };
   auto gen = [&](uint32_t s) { return smem + (s - sbase); };
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
@@ -1057,75 +1091,112 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         tma_load_3d(gen(sbase + C::K_OFF) + cb * C::CB, &m.K[0], &bar_kv, cb * 64, j0, bg);
         tma_load_3d(gen(sbase + C::V_OFF) + cb * C::CB, &m.V[0], &bar_kv, cb * 64, j0, bg);
       }
-      int last[NST];
-      for (int s = 0; s < NST; ++s) last[s] = -1;
+      int last_q[NS], last_do[NS];
+      for (int s = 0; s < NS; ++s) last_q[s] = last_do[s] = -1;
       for (int c = 0; c < nc; ++c) {
-        const int st = c % NST;
-        if (!wait(&bar_empty[st], ((c / NST) & 1) ^ 1)) break;
+        const int st = c % NS;
         int bh, i0;
         chunk_rows(c, &bh, &i0);
-        mbar_arrive_expect_tx(&bar_full[st], C::STAGE + C::VEC);
-        for (int cb = 0; cb < C::NCB; ++cb) {
-          tma_load_3d(gen(sQc(st)) + cb * C::CB, &m.Qc[0], &bar_full[st], cb * 64, i0, bh);
-          tma_load_3d(gen(sdOc(st)) + cb * C::CB, &m.dOc[0], &bar_full[st], cb * 64, i0, bh);
-        }
-        tma_load_3d(vecs + st * 256, &m.L, &bar_full[st], i0, bh, 0);
-        tma_load_3d(vecs + st * 256 + 128, &m.Dl, &bar_full[st], i0, bh, 0);
-        last[st] = c / NST;
+        if (!wait(&bar_doempty[st], ((c / NS) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(&bar_dofull[st], C::TILE);
+        for (int cb = 0; cb < C::NCB; ++cb)
+          tma_load_3d(gen(sdO(st)) + cb * C::CB, &m.dOc[0], &bar_dofull[st], cb * 64, i0, bh);
+        last_do[st] = c / NS;
+        if (!wait(&bar_qempty[st], ((c / NS) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(&bar_qfull[st], C::TILE + C::VEC);
+        for (int cb = 0; cb < C::NCB; ++cb)
+          tma_load_3d(gen(sQ(st)) + cb * C::CB, &m.Qc[0], &bar_qfull[st], cb * 64, i0, bh);
+        float* vec = reinterpret_cast<float*>(smem + C::VEC_OFF + st * C::VEC);
+        tma_load_3d(vec, &m.L, &bar_qfull[st], i0, bh, 0);
+        tma_load_3d(vec + 128, &m.Dl, &bar_qfull[st], i0, bh, 0);
+        last_q[st] = c / NS;
       }
       drain_wait(&bar_kv, 0, a.limit_ns);
-      for (int s = 0; s < NST; ++s)
-        if (last[s] >= 0) drain_wait(&bar_full[s], last[s] & 1, a.limit_ns);
+      for (int s = 0; s < NS; ++s) {
+        if (last_q[s] >= 0) drain_wait(&bar_qfull[s], last_q[s] & 1, a.limit_ns);
+        if (last_do[s] >= 0) drain_wait(&bar_dofull[s], last_do[s] & 1, a.limit_ns);
+      }
     }
-  } else if (warp == C::A_WARP || warp == C::B_WARP) {
-    const bool is_a = warp == C::A_WARP;
+  } else if (warp == C::A_WARP) {
+    // S issuer: S^T(c) once Q_c is in and the softmax has loaded S^T(c-1).
     if (lane == 0 && nc > 0) {
-      const uint32_t slot = tmem + (is_a ? C::S_COL : C::DP_COL);
-      const uint32_t acc = tmem + (is_a ? C::DV : C::DK);
-      const uint32_t lhs = sbase + (is_a ? C::K_OFF : C::V_OFF);
-      uint64_t* scored = is_a ? &bar_s : &bar_dp;
-      uint64_t* ready = is_a ? &bar_p : &bar_ds;
       bool ok = wait(&bar_kv, 0);
       for (int c = 0; ok && c < nc; ++c) {
-        const int st = c % NST;
-        // A: S^T = K Q^T, dV += P^T dO.  B: dP^T = V dO^T, dK += dS^T Q.
-        const uint32_t rhs = is_a ? sQc(st) : sdOc(st);
-        const uint32_t other = is_a ? sdOc(st) : sQc(st);
-        if (!(ok = wait(&bar_full[st], (c / NST) & 1))) break;
+        const int st = c % NS;
+        if (!(ok = wait(&bar_qfull[st], (c / NS) & 1))) break;
+        if (c > 0 && !(ok = wait(&bar_sfree, (c - 1) & 1))) break;
         tc_fence_after();
-        issue_rowdot128<D>(slot, lhs, rhs);
-        tc_commit(scored);
-        if (!(ok = wait(ready, c & 1))) break;
+        issue_rowdot128<D>(tmem + C::S_COL, sbase + C::K_OFF, sQ(st));
+        tc_commit(&bar_s);
+        tc_commit(&bar_qempty[st]);
+      }
+      tc_commit(&bar_drain[0]);
+      drain_wait(&bar_drain[0], 0, a.limit_ns);
+    }
+  } else if (warp == C::DV_WARP) {
+    // dV issuer: dV += P^T(c) dO_c once the softmax has written P^T(c).
+    if (lane == 0 && nc > 0) {
+      bool ok = true;
+      for (int c = 0; ok && c < nc; ++c) {
+        const int st = c % NS;
+        if (!(ok = wait(&bar_p, c & 1))) break;
         tc_fence_after();
-        issue_acc128<D>(acc, slot, other, c > 0);
-        tc_commit(&bar_empty[st]);
+        issue_acc128_ss<D>(tmem + C::DV, sbase + C::PT_OFF, sdO(st), c > 0);
+        tc_commit(&bar_doempty[st]);
+        tc_commit(&bar_dvdone);
       }
       if (ok) tc_commit(&bar_done);
-      tc_commit(&bar_drain[is_a ? 0 : 1]);
-      drain_wait(&bar_drain[is_a ? 0 : 1], 0, a.limit_ns);
+      tc_commit(&bar_drain[2]);
+      drain_wait(&bar_drain[2], 0, a.limit_ns);
     }
-  }  // the idle warp falls through
+  } else if (warp == C::B_WARP) {
+    // Chunk c: dP^T(c) = V dO^T, then dK += dS^T(c) Q once the softmax wrote dS^T(c).
+    if (lane == 0 && nc > 0) {
+      bool ok = wait(&bar_kv, 0);
+      for (int c = 0; ok && c < nc; ++c) {
+        const int st = c % NS;
+        if (!(ok = wait(&bar_dofull[st], (c / NS) & 1))) break;
+        tc_fence_after();
+        issue_rowdot128<D>(tmem + C::DP_COL, sbase + C::V_OFF, sdO(st));
+        tc_commit(&bar_dp);
+        tc_commit(&bar_doempty[st]);
+        if (!(ok = wait(&bar_ds, c & 1))) break;
+        tc_fence_after();
+        issue_acc128<D>(tmem + C::DK, tmem + C::DP_COL, sQ(st), c > 0);
+        tc_commit(&bar_qempty[st]);
+      }
+      if (ok) tc_commit(&bar_done);
+      tc_commit(&bar_drain[1]);
+      drain_wait(&bar_drain[1], 0, a.limit_ns);
+    }
+  }
   } else {
     regs_increase<C::REGS_SOFTMAX>();
     // thread = key row j = TMEM lane; warps w and w + 4 take queries [0, 64) / [64, 128)
     const int wq = warp % 4, half = warp / 4;
-    const int j = j0 + wq * 32 + lane;
+    const int r_in = wq * 32 + lane;
+    const int j = j0 + r_in;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    // this thread's 128-byte row of P^T (queries half*64 ..) in the swizzled tile
+    const uint32_t pt_row = sbase + C::PT_OFF + half * C::CB + r_in * 128;
+    const uint32_t sw = (uint32_t)(r_in & 7);
     const float sl2 = a.scale_log2;
     const bool row_dead = j >= a.Sk;
     bool ok = true;
     for (int c = 0; c < nc; ++c) {
-      const int st = c % NST;
+      const int st = c % NS;
       int bh, i0;
       chunk_rows(c, &bh, &i0);
       const int q0 = i0 + half * 64;  // first query of this thread's half
       float s[64];
-      ok = __all_sync(0xffffffffu, wait(&bar_s, c & 1) && wait(&bar_full[st], (c / NST) & 1));
+      ok = __all_sync(0xffffffffu, wait(&bar_s, c & 1) && wait(&bar_qfull[st], (c / NS) & 1));
       if (!ok) break;
       tc_fence_after();
       {
         uint32_t r0[32], r1[32];
         tmem_ld32x2(lane_addr + C::S_COL + half * 64, lane_addr + C::S_COL + half * 64 + 32, r0, r1);
+        tc_fence_before();
+        mbar_arrive(&bar_sfree);  // the S^T slot may take the next chunk
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           s[k] = __uint_as_float(r0[k]);
@@ -1143,7 +1214,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
           if (row_dead || k < k_lo || k > k_hi) s[k] = -INFINITY;
       }
       // lse2 / delta of the chunk's queries, read with explicit shared-space loads
-      const uint32_t lv = sbase + C::VEC_OFF + (st * 256 + half * 64) * 4;
+      const uint32_t lv = sbase + C::VEC_OFF + st * C::VEC + half * 64 * 4;
 #pragma unroll
       for (int k4 = 0; k4 < 16; ++k4) {
         const float4 l4 = ld_shared_v4(lv + 16 * k4);
@@ -1152,14 +1223,17 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         s[4 * k4 + 2] = ex2(fmaf(s[4 * k4 + 2], sl2, -l4.z));
         s[4 * k4 + 3] = ex2(fmaf(s[4 * k4 + 3], sl2, -l4.w));
       }
-      {
-        uint32_t pk[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) pk[k] = pack_half2(s[2 * k], s[2 * k + 1]);
-        tmem_st32(lane_addr + C::S_COL + half * 64, pk);
+      // P^T into shared memory once dV has consumed the previous chunk's
+      if (c > 0) {
+        ok = __all_sync(0xffffffffu, wait(&bar_dvdone, (c - 1) & 1));
+        if (!ok) break;
       }
-      tmem_st_wait();
-      tc_fence_before();
+#pragma unroll
+      for (int k8 = 0; k8 < 8; ++k8)
+        st_shared_v4(pt_row + (((uint32_t)k8 ^ sw) << 4), pack_half2(s[8 * k8], s[8 * k8 + 1]),
+                     pack_half2(s[8 * k8 + 2], s[8 * k8 + 3]), pack_half2(s[8 * k8 + 4], s[8 * k8 + 5]),
+                     pack_half2(s[8 * k8 + 6], s[8 * k8 + 7]));
+      fence_async_shared();
       mbar_arrive(&bar_p);
       ok = __all_sync(0xffffffffu, wait(&bar_dp, c & 1));
       if (!ok) break;
@@ -1168,7 +1242,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         uint32_t r0[32], r1[32];
         tmem_ld32x2(lane_addr + C::DP_COL + half * 64, lane_addr + C::DP_COL + half * 64 + 32, r0,
                     r1);
-        const uint32_t dv = sbase + C::VEC_OFF + (st * 256 + 128 + half * 64) * 4;
+        const uint32_t dv = lv + 128 * 4;
         uint32_t pk[32];
 #pragma unroll
         for (int k4 = 0; k4 < 16; ++k4) {
@@ -1434,11 +1508,16 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     } else {
       using C16 = Dkv16Cfg<D>;
       auto kern = fa_bwd_dkdv16_kernel<D>;
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C16::SMEM);
+      // all the dynamic shared memory a block may have: the layout fills it after
+      // aligning its base to 1 KB (the kernel checks the fit)
+      int dyn = 0;
+      e = host::max_dynamic_smem(reinterpret_cast<const void*>(kern), &dyn);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
       if (e == cudaSuccess) {
         host::KernelTimer kt(D == 128 ? "fa_bwd_dkdv_kernel<128,bf16>" : "fa_bwd_dkdv_kernel<64,bf16>",
                              stream);
-        kern<<<(unsigned)(BHk * ak.n_tiles), C16::THREADS, C16::SMEM, stream>>>(mk, ak);
+        kern<<<(unsigned)(BHk * ak.n_tiles), C16::THREADS, dyn, stream>>>(mk, ak);
         e = cudaGetLastError();
       }
     }

@@ -19,7 +19,10 @@ constexpr float LN2 = 0.6931471805599453f;
 constexpr float RESCALE_THRESHOLD = 8.0f;
 
 // Status bits a kernel may set in its device status word.
-enum : unsigned int { DEV_TIMEOUT = 1u };
+enum : unsigned int {
+  DEV_TIMEOUT = 1u,  // a barrier wait gave up
+  DEV_LAYOUT = 2u,   // a kernel's shared-memory layout did not fit its allocation
+};
 
 // Half-open range [lo, hi) of key tiles that query rows [r0, r1] may attend to:
 // key j is visible to row i iff j < Sk, (!causal || j <= i) and
@@ -82,6 +85,10 @@ int sm_count();
 
 // Records a CUDA event pair around the launches made during its lifetime when
 // kernel timing is enabled (fa_timing_enable); otherwise does nothing.
+// Largest dynamic shared-memory size a block of `kernel` may request on the current
+// device (the per-block opt-in limit minus the kernel's static shared memory).
+cudaError_t max_dynamic_smem(const void* kernel, int* bytes);
+
 class KernelTimer {
  public:
   KernelTimer(const char* name, cudaStream_t s);

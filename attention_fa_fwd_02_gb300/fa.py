@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(PKG, "libfa.so")
 
 FA_F32, FA_BF16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
-          4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_SCRATCH_LIMIT"}
+          4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_SCRATCH_LIMIT", 7: "FA_ERR_LAYOUT"}
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string", "fa_version",
            "fa_timing_enable", "fa_timing_read", "fa_fwd_noalloc", "fa_selftest_timeout")
 # Size of the static device scratch behind fa_fwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).

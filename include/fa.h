@@ -75,7 +75,9 @@ typedef enum {
   FA_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
   FA_ERR_CUDA = 4,        /* a CUDA runtime / driver call or a kernel launch failed */
   FA_ERR_TIMEOUT = 5,     /* a kernel gave up waiting on an internal barrier (device status) */
-  FA_ERR_SCRATCH_LIMIT = 6 /* fa_fwd_noalloc: the problem needs more than FA_NOALLOC_SCRATCH_BYTES */
+  FA_ERR_SCRATCH_LIMIT = 6, /* fa_fwd_noalloc: the problem needs more than FA_NOALLOC_SCRATCH_BYTES */
+  FA_ERR_LAYOUT = 7         /* a kernel found less shared memory than its layout needs (device
+                               status; the kernel skipped its work, outputs undefined) */
 } fa_status;
 
 /*
@@ -147,8 +149,9 @@ FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void*
 
 /*
  * Synchronizes `stream`, then reads and clears the library's device status word
- * on the current device: FA_ERR_TIMEOUT if any kernel since the last call gave
- * up on a barrier wait (its outputs are then undefined), FA_ERR_CUDA if the
+ * on the current device: FA_ERR_LAYOUT if a kernel since the last call found less
+ * shared memory than its layout needs, FA_ERR_TIMEOUT if one gave up on a barrier
+ * wait (outputs are then undefined in both cases), FA_ERR_CUDA if the
  * synchronization itself failed, else FA_OK.
  */
 FA_API fa_status fa_device_status(fa_stream_t stream);
