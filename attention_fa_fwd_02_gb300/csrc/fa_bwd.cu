@@ -668,7 +668,8 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
 // TMEM: S slot [0, 128), dP slot [128, 256), two fp16 dS operand slots of 64
 // columns at 256 / 320, dQ at 384. The S and dP slots are single: the softmax
 // releases each as soon as it has loaded it, so chunk c+1's S = Q K^T runs while
-// the softmax finishes chunk c. Eight softmax warps: warps w and w+4 share TMEM
+// the softmax finishes chunk c. S, dP and dQ MMAs come from three issuing threads:
+// an issuer stalls while the tensor pipe is full, so each stream gets its own. Eight softmax warps: warps w and w+4 share TMEM
 // lanes 32*(w%4).., w < 4 taking keys [0, 64) of the chunk, w >= 4 keys [64, 128).
 template <int D>
 struct Dq16Cfg {
@@ -680,7 +681,7 @@ struct Dq16Cfg {
   static constexpr uint32_t V_OFF = K_OFF + KST * TILE;
   static constexpr uint32_t SMEM = V_OFF + VST * TILE + 1024;
   static constexpr int SOFTMAX_WARPS = 8;
-  static constexpr int MMA_WARP = 8, ACC_WARP = 9, TMA_WARP = 10;
+  static constexpr int MMA_WARP = 8, ACC_WARP = 9, TMA_WARP = 10, DP_WARP = 11;
   static constexpr int THREADS = 384;
   static constexpr uint32_t REGS_SOFTMAX = 200, REGS_CONTROL = 96;
   static_assert(256 * REGS_SOFTMAX + 128 * REGS_CONTROL <= 384 * 168, "register split");
@@ -712,7 +713,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_qd, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST],
       bar_vempty[VST], bar_s, bar_dp, bar_sfree, bar_dpfree, bar_ds[2], bar_accdone[2], bar_done,
-      bar_drain[2];
+      bar_drain[3];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int warp = warp_id(), lane = lane_id();
@@ -739,8 +740,8 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_ds[s], 256);
       mbar_init(&bar_accdone[s], 1);
-      mbar_init(&bar_drain[s], 1);
     }
+    for (int s = 0; s < 3; ++s) mbar_init(&bar_drain[s], 1);
     mbar_init(&bar_done, 1);
     abort_sh = 0;
     fence_mbar_init();
@@ -795,27 +796,33 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
       for (int s = 0; s < VST; ++s)
         if (last_v[s] >= 0) drain_wait(&bar_vfull[s], last_v[s] & 1, a.limit_ns);
     }
-  } else if (warp == C::MMA_WARP) {
-    // Score issuer: S(c) = Q K_c^T once the softmax has loaded S(c-1); dP(c) = dO V_c^T
-    // once it has loaded dP(c-1).
+  } else if (warp == C::MMA_WARP || warp == C::DP_WARP) {
+    // Score issuers (one thread each, so neither waits behind the other's barrier):
+    // S(c) = Q K_c^T once the softmax has loaded S(c-1); dP(c) = dO V_c^T once it
+    // has loaded dP(c-1).
+    const bool is_s = warp == C::MMA_WARP;
     if (lane == 0 && nc > 0) {
       bool ok = wait(&bar_qd, 0);
       for (int c = 0; ok && c < nc; ++c) {
-        const int ks = c % KST, vs = c % VST;
-        if (!(ok = wait(&bar_kfull[ks], (c / KST) & 1))) break;
-        if (c > 0 && !(ok = wait(&bar_sfree, (c - 1) & 1))) break;
-        tc_fence_after();
-        issue_rowdot128<D>(tmem + C::S_COL, sbase + C::Q_OFF, sK(ks));
-        tc_commit(&bar_s);
-        if (!(ok = wait(&bar_vfull[vs], (c / VST) & 1))) break;
-        if (c > 0 && !(ok = wait(&bar_dpfree, (c - 1) & 1))) break;
-        tc_fence_after();
-        issue_rowdot128<D>(tmem + C::DP_COL, sbase + C::DO_OFF, sV(vs));
-        tc_commit(&bar_dp);
-        tc_commit(&bar_vempty[vs]);
+        if (is_s) {
+          const int ks = c % KST;
+          if (!(ok = wait(&bar_kfull[ks], (c / KST) & 1))) break;
+          if (c > 0 && !(ok = wait(&bar_sfree, (c - 1) & 1))) break;
+          tc_fence_after();
+          issue_rowdot128<D>(tmem + C::S_COL, sbase + C::Q_OFF, sK(ks));
+          tc_commit(&bar_s);
+        } else {
+          const int vs = c % VST;
+          if (!(ok = wait(&bar_vfull[vs], (c / VST) & 1))) break;
+          if (c > 0 && !(ok = wait(&bar_dpfree, (c - 1) & 1))) break;
+          tc_fence_after();
+          issue_rowdot128<D>(tmem + C::DP_COL, sbase + C::DO_OFF, sV(vs));
+          tc_commit(&bar_dp);
+          tc_commit(&bar_vempty[vs]);
+        }
       }
-      tc_commit(&bar_drain[0]);
-      drain_wait(&bar_drain[0], 0, a.limit_ns);
+      tc_commit(&bar_drain[is_s ? 0 : 2]);
+      drain_wait(&bar_drain[is_s ? 0 : 2], 0, a.limit_ns);
     }
   } else if (warp == C::ACC_WARP) {
     // Accumulate issuer: dQ += dS(c) K_c (dS fp16 in TMEM, K_c MN-major); then K_c's
@@ -839,7 +846,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
       tc_commit(&bar_drain[1]);
       drain_wait(&bar_drain[1], 0, a.limit_ns);
     }
-  }  // the idle warp falls through
+  }
   } else {
     regs_increase<C::REGS_SOFTMAX>();
     const int wq = warp % 4, half = warp / 4;
