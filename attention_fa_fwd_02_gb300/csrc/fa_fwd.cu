@@ -352,13 +352,18 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         for (int c = 0; c < 128; ++c)
           if (c > rel_hi || c < rel_lo) s[c] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      // row max: eight chains of three-input maxima
+      float mx[8];
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, s[c]); mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]); mx3 = fmaxf(mx3, s[c + 3]);
-      }
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      for (int k = 0; k < 8; ++k) mx[k] = max3(s[k], s[8 + k], s[16 + k]);
+#pragma unroll
+      for (int c = 24; c < 120; c += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = max3(mx[k], s[c + k], s[c + 8 + k]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], s[120 + k]);
+      const float mt =
+          max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
       const bool need = mt > m + RESCALE_THRESHOLD;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = fmaxf(m, mt);
@@ -379,19 +384,23 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
       const float nm = -m;
       float l0 = 0.f, l1 = 0.f;
       if constexpr (!C::F32) {
+        // exponent arguments and the row sum on packed pairs
+        const float2 sl2x2 = make_float2(sl2, sl2), nmx2 = make_float2(nm, nm);
+        float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t pk[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            const float p0 = ex2(fmaf(s[c * 64 + 2 * k], sl2, nm));
-            const float p1 = ex2(fmaf(s[c * 64 + 2 * k + 1], sl2, nm));
-            l0 += p0;
-            l1 += p1;
-            pk[k] = pack_half2(p0, p1);
+            const float2 x = fma2(make_float2(s[c * 64 + 2 * k], s[c * 64 + 2 * k + 1]), sl2x2, nmx2);
+            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+            ls[k & 1] = add2(ls[k & 1], pp);
+            pk[k] = pack_half2(pp.x, pp.y);
           }
           tmem_st32(s_addr + c * 32, pk);
         }
+        l0 = ls[0].x + ls[1].x;
+        l1 = ls[0].y + ls[1].y;
       } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
