@@ -1360,6 +1360,86 @@ __global__ void bwd_preprocess_kernel(const void* __restrict__ dO, const void* _
   }
 }
 
+// bf16 inputs, one launch for every pre-pass of the backward:
+//   rows (bh, i < ldq) of Q / dO / O:  delta[bh][i] = sum_d dO[i,d] * O[i,d],
+//       lse2[bh][i] = LSE * log2(e) (+inf for LSE = -inf; rows i >= Sq get +inf / 0),
+//       fp16 copies of the Q and dO rows;
+//   rows of K / V (B*HKV*Sk of them): fp16 copies.
+// D/8 threads per row, 8 elements (16 bytes of bf16) each, so a warp moves whole
+// 256-byte rows with 16-byte accesses.
+template <int D>
+__global__ void bwd_prepass16_kernel(const __nv_bfloat16* __restrict__ dO, const void* __restrict__ O,
+                                     const float* __restrict__ LSE, const __nv_bfloat16* __restrict__ Q,
+                                     const __nv_bfloat16* __restrict__ K,
+                                     const __nv_bfloat16* __restrict__ V, __half* __restrict__ dO16,
+                                     __half* __restrict__ Q16, __half* __restrict__ K16,
+                                     __half* __restrict__ V16, float* __restrict__ lse2,
+                                     float* __restrict__ delta, int Sq, int ldq, size_t q_rows,
+                                     size_t kv_rows, int o_bf16) {
+  constexpr int TPR = D / 8;  // threads per row
+  const int t = threadIdx.x % TPR;
+  const size_t rows_per_grid = (size_t)gridDim.x * (blockDim.x / TPR);
+  auto cvt8 = [](uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      o[e] = pack_half2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  for (size_t r = blockIdx.x * (size_t)(blockDim.x / TPR) + threadIdx.x / TPR; r < q_rows + kv_rows;
+       r += rows_per_grid) {
+    if (r < q_rows) {
+      const size_t bh = r / ldq;
+      const int i = (int)(r % ldq);
+      float acc = 0.f;
+      if (i < Sq) {
+        const size_t off = (bh * Sq + i) * D + t * 8;
+        const uint4 g = *reinterpret_cast<const uint4*>(dO + off);
+        const uint4 q = *reinterpret_cast<const uint4*>(Q + off);
+        float ov[8];
+        if (o_bf16) {
+          const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(O) + off);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            ov[2 * e] = __uint_as_float(w[e] << 16);
+            ov[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+          }
+        } else {
+          const float4 a4 = *reinterpret_cast<const float4*>(static_cast<const float*>(O) + off);
+          const float4 b4 = *reinterpret_cast<const float4*>(static_cast<const float*>(O) + off + 4);
+          ov[0] = a4.x; ov[1] = a4.y; ov[2] = a4.z; ov[3] = a4.w;
+          ov[4] = b4.x; ov[5] = b4.y; ov[6] = b4.z; ov[7] = b4.w;
+        }
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          acc += __uint_as_float(gw[e] << 16) * ov[2 * e] +
+                 __uint_as_float(gw[e] & 0xFFFF0000u) * ov[2 * e + 1];
+        *reinterpret_cast<uint4*>(dO16 + off) = cvt8(g);
+        *reinterpret_cast<uint4*>(Q16 + off) = cvt8(q);
+      }
+#pragma unroll
+      for (int w = TPR / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+      if (t == 0) {
+        if (i < Sq) {
+          const float L = LSE[bh * Sq + i];
+          lse2[r] = (L == -INFINITY) ? INFINITY : L * LOG2E;
+          delta[r] = acc;
+        } else {
+          lse2[r] = INFINITY;
+          delta[r] = 0.f;
+        }
+      }
+    } else {
+      const size_t off = (r - q_rows) * D + t * 8;
+      *reinterpret_cast<uint4*>(K16 + off) = cvt8(*reinterpret_cast<const uint4*>(K + off));
+      *reinterpret_cast<uint4*>(V16 + off) = cvt8(*reinterpret_cast<const uint4*>(V + off));
+    }
+  }
+}
+
 // Zero-fill outputs of an empty side (Sq == 0 or Sk == 0).
 __global__ void zero_kernel(uint4* p, size_t n16) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16;
@@ -1410,16 +1490,11 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     __half* k16 = do16 + nq;
     __half* v16 = k16 + nk;
     {
-      host::KernelTimer kt("bwd_preprocess", stream);
-      bwd_preprocess_kernel<D><<<grid_pp, 256, 0, stream>>>(dO, O, LSE, Q, do16, q16, lse2, delta,
-                                                           p.Sq, ldq, nvec, 1, p.out_dtype == FA_BF16);
-    }
-    {
-      host::KernelTimer kt("cvt_bf16_to_f16(K,V)", stream);
-      cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(K),
-                                                         reinterpret_cast<uint4*>(k16), nk / 8);
-      cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
-                                                         reinterpret_cast<uint4*>(v16), nk / 8);
+      host::KernelTimer kt("bwd_prepass", stream);
+      bwd_prepass16_kernel<D><<<8 * host::sm_count(), 256, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(dO), O, LSE, static_cast<const __nv_bfloat16*>(Q),
+          static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(V), do16, q16, k16,
+          v16, lse2, delta, p.Sq, ldq, nvec, BHk * p.Sk, p.out_dtype == FA_BF16);
     }
     const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     enc &= host::encode_tiled_3d(&mk.K[0], F16, 2, k16, D, p.Sk, BHk, D, 64, 128);
