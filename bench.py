@@ -38,9 +38,11 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # forward 2 GEMMs (QK^T, PV); dK/dV kernel 4 (S^T, dP^T, dV, dK); dQ kernel 3 (S, dP, dQ).
 KERNEL_FLOPS_PER_PAIR_PER_D = {"fa_fwd_kernel": 4, "fa_bwd_dkdv_kernel": 8, "fa_bwd_dq_kernel": 6}
 # Source files whose change invalidates a committed DRAM-traffic figure.
-KERNEL_SOURCES = {"fa_fwd_kernel": ["fa_fwd.cu", "ptx.cuh", "fa_common.cuh"],
-                  "fa_bwd_dkdv_kernel": ["fa_bwd.cu", "ptx.cuh", "fa_common.cuh"],
-                  "fa_bwd_dq_kernel": ["fa_bwd.cu", "ptx.cuh", "fa_common.cuh"]}
+_COMMON_SOURCES = ["ptx.cuh", "fa_common.cuh", "fa_epilogue.cuh", "fa_prepass.cuh"]
+KERNEL_SOURCES = {"fa_fwd_kernel": ["fa_fwd.cu"] + _COMMON_SOURCES,
+                  "fa_bwd_dkdv_kernel": ["fa_bwd.cu"] + _COMMON_SOURCES,
+                  "fa_bwd_dq_kernel": ["fa_bwd.cu"] + _COMMON_SOURCES,
+                  "bwd_prepass": ["fa_bwd.cu"] + _COMMON_SOURCES}
 
 
 def _env_int(name, default):
