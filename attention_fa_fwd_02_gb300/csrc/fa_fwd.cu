@@ -13,7 +13,8 @@
 //                     row in TMEM when m grows by more than RESCALE_THRESHOLD, and
 //                     in the epilogue writes LSE = (m + log2 l) ln 2 and O = acc / l
 //                     (staged in the tile's spent Q buffer, written by TMA stores).
-//   warp 4*NQ + q     MMA issuer of tile q (one thread): S_q = Q_q K_j^T, O_q += P_q V_j.
+//   warp 4*NQ         MMA issuer (one thread): S_q = Q_q K_j^T, O_q += P_q V_j,
+//                     bursts in a fixed tile order so the tiles alternate.
 //   warp 5*NQ         TMA producer (one thread): Q once, then K_j / V_j rings.
 // Every barrier wait is bounded; on expiry the kernel raises the device status
 // word, drains its in-flight copies and MMAs, frees TMEM and returns.
@@ -64,9 +65,9 @@ struct FwdCfg {
   static constexpr uint32_t SMEM_BYTES = V_OFF + VST * NSPLIT * TILE_BYTES;
   static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
   static constexpr int SOFTMAX_WARPS = 4 * NQ;
-  // Warps SOFTMAX_WARPS + q issue the MMAs of query tile q (the first one also owns
-  // TMEM); the TMA producer follows them. Whole warpgroups: the control warps share
-  // the last warpgroup with idle warps.
+  // Warp SOFTMAX_WARPS issues every MMA and owns TMEM; the TMA producer follows the
+  // issuer slots. Whole warpgroups: the control warps share the last warpgroup with
+  // idle warps.
   static constexpr int MMA_WARP = SOFTMAX_WARPS;
   static constexpr int TMA_WARP = SOFTMAX_WARPS + NQ;
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 4);
@@ -178,9 +179,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
-    // a K / V stage is free once every tile's issuer has consumed it
-    for (int s = 0; s < C::KST; ++s) { mbar_init(&bar_kfull[s], 1); mbar_init(&bar_kempty[s], C::NQ); }
-    for (int s = 0; s < C::VST; ++s) { mbar_init(&bar_vfull[s], 1); mbar_init(&bar_vempty[s], C::NQ); }
+    // a K / V stage is free once the MMAs of every tile that read it have completed
+    for (int s = 0; s < C::KST; ++s) { mbar_init(&bar_kfull[s], 1); mbar_init(&bar_kempty[s], 1); }
+    for (int s = 0; s < C::VST; ++s) { mbar_init(&bar_vfull[s], 1); mbar_init(&bar_vempty[s], 1); }
     for (int q = 0; q < C::NQ; ++q) {
       mbar_init(&bar_s[q], 1);
       mbar_init(&bar_p[q], 128);
@@ -264,50 +265,70 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         while (!mbar_try_wait(&bar_q, 0) && globaltimer() - t0 < a.limit_ns) {}
       }
     }
-  } else if (warp < C::MMA_WARP + C::NQ) {
-    // ------------------------------------------------------------ MMA issuer of tile q
-    // In order per tile: S_q(0); then per key tile j: O_q += P_q V_j (once the
-    // softmax wrote P_q), S_q(j+1) = Q_q K_{j+1}^T. P_q aliases S_q in TMEM; MMAs of
-    // one thread run in issue order, so S_q(j+1) after PV_q(j) is safe.
-    // Each tile has its own issuing warp: after a burst of MMAs a warp's next
-    // barrier operation waits for that burst, so a single issuer for both tiles
-    // lets the tensor core drain at every tile switch. Tile 1 starts once tile 0's
-    // first P is ready, which staggers the tiles; the in-order tensor pipe then
-    // keeps their bursts alternating, each tile's softmax overlapping the other
-    // tile's MMAs.
-    const int q = warp - C::MMA_WARP;
-    if (lane == 0 && n > 0) {
-      bool ok = wait(&bar_q, 0) && wait(&bar_kfull[0], 0);
-      if (ok && q > 0) ok = wait(&bar_p[0], 0);
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    // One warp issues every MMA (lane 0), in a fixed order per key tile j:
+    //   O_0 += P_0 V_j, S_0 = Q_0 K_{j+1}^T, O_1 += P_1 V_j, S_1 = Q_1 K_{j+1}^T.
+    // The tensor pipe runs them in that order, so S_0(j+1) completes one burst
+    // before S_1(j+1): tile 0's softmax runs while tile 1's MMAs execute and vice
+    // versa. (With one issuer per tile the two streams interleave in the pipe, both
+    // S tiles complete together and both softmaxes compete for the exponential
+    // units.) "P_q written" comes through named barrier 1 + q rather than an
+    // mbarrier: an mbarrier wait right after a burst of MMAs only returns once the
+    // burst has drained, which would idle the pipe between bursts. P_q aliases S_q
+    // in TMEM; a thread's MMAs run in issue order, so S_q(j+1) after O_q += P_q V_j
+    // is safe.
+    if (n > 0) {
+      const bool leader = lane == 0;
+      bool ok = __all_sync(0xffffffffu, wait(&bar_q, 0) && wait(&bar_kfull[0], 0));
       tc_fence_after();
-      if (ok) {
-        issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(0, 0),
-                    sK(0, C::NSPLIT - 1));
-        tc_commit(&bar_s[q]);
+      if (ok && leader) {
+        for (int q = 0; q < C::NQ; ++q) {
+          issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(0, 0),
+                      sK(0, C::NSPLIT - 1));
+          tc_commit(&bar_s[q]);
+        }
         tc_commit(&bar_kempty[0]);
       }
+      __syncwarp();
       for (int it = 0; ok && it < n; ++it) {
-        const int vs = it % C::VST;
-        if (!(ok = wait(&bar_vfull[vs], (it / C::VST) & 1) && wait(&bar_p[q], it & 1))) break;
-        tc_fence_after();
-        issue_pv<C>(tmem + C::o_col(q), tmem + C::s_col(q), tmem + C::PLO_COL, sV(vs, 0),
-                    sV(vs, C::NSPLIT - 1), it > 0);
-        tc_commit(&bar_vempty[vs]);
-        if (it + 1 < n) {
-          const int ks = (it + 1) % C::KST;
-          if (!(ok = wait(&bar_kfull[ks], ((it + 1) / C::KST) & 1))) break;
+        const int vs = it % C::VST, ks = (it + 1) % C::KST;
+        const bool more = it + 1 < n;
+        for (int q = 0; ok && q < C::NQ; ++q) {
+          if (!(ok = __all_sync(0xffffffffu, wait(&bar_vfull[vs], (it / C::VST) & 1)))) break;
+          named_bar_sync(1 + q, 128 + 32);  // P_q(it) is in TMEM
+          if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }  // warp-uniform
           tc_fence_after();
-          issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(ks, 0),
-                      sK(ks, C::NSPLIT - 1));
-          tc_commit(&bar_s[q]);
-          tc_commit(&bar_kempty[ks]);
+          if (leader)
+            issue_pv<C>(tmem + C::o_col(q), tmem + C::s_col(q), tmem + C::PLO_COL, sV(vs, 0),
+                        sV(vs, C::NSPLIT - 1), it > 0);
+          if (more) {
+            if (!(ok = __all_sync(0xffffffffu, wait(&bar_kfull[ks], ((it + 1) / C::KST) & 1)))) break;
+            tc_fence_after();
+            if (leader) {
+              issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(ks, 0),
+                          sK(ks, C::NSPLIT - 1));
+              tc_commit(&bar_s[q]);
+            }
+          }
+          __syncwarp();
         }
+        if (!ok) break;
+        if (leader) {
+          tc_commit(&bar_vempty[vs]);
+          if (more) tc_commit(&bar_kempty[ks]);
+        }
+        __syncwarp();
       }
-      if (ok) tc_commit(&bar_o[q]);
-      // Drain: no MMA may still be running when TMEM is released.
-      tc_commit(&bar_drain[q]);
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(&bar_drain[q], 0) && globaltimer() - t0 < a.limit_ns) {}
+      if (leader) {
+        if (ok)
+          for (int q = 0; q < C::NQ; ++q) tc_commit(&bar_o[q]);
+        // Drain: no MMA may still be running when TMEM is released.
+        tc_commit(&bar_drain[0]);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&bar_drain[0], 0) && globaltimer() - t0 < a.limit_ns) {}
+      }
+      __syncwarp();
     }
   }  // idle warps of the control warpgroup fall through
   } else {
@@ -331,7 +352,12 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     for (int it = 0; it < n; ++it) {
       const int t = t_lo + it;
       ok = __all_sync(0xffffffffu, wait(&bar_s[q], it & 1));
-      if (!ok) break;
+      if (!ok) {
+        // The issuer waits on named barrier 1 + q once per key tile: give it the
+        // remaining arrivals so that it cannot wait forever (it sees the abort flag).
+        for (int r = it; r < n; ++r) named_bar_arrive(1 + q, 128 + 32);
+        break;
+      }
       tc_fence_after();
       float s[128];
       {
@@ -420,7 +446,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
       l += l0 + l1;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar_p[q]);
+      named_bar_arrive(1 + q, 128 + 32);
     }
     if (ok && n > 0) {
       ok = __all_sync(0xffffffffu, wait(&bar_o[q], 0));
