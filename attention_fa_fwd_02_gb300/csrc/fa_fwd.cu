@@ -70,6 +70,8 @@ struct FwdCfg {
   // idle warps.
   static constexpr int MMA_WARP = SOFTMAX_WARPS;
   static constexpr int TMA_WARP = SOFTMAX_WARPS + NQ;
+  static constexpr int RELAY_WARP = TMA_WARP + 1;  // relays load completions to the issuer
+  static constexpr uint32_t RELAY_BAR = 3;         // named barriers 1, 2: P of tile 0, 1
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 4);
   // Register split for NQ = 2 (launched at 168 per thread for 384 threads): the
   // softmax warpgroups hold a whole 128-column S row in registers.
@@ -273,14 +275,15 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     // before S_1(j+1): tile 0's softmax runs while tile 1's MMAs execute and vice
     // versa. (With one issuer per tile the two streams interleave in the pipe, both
     // S tiles complete together and both softmaxes compete for the exponential
-    // units.) "P_q written" comes through named barrier 1 + q rather than an
-    // mbarrier: an mbarrier wait right after a burst of MMAs only returns once the
-    // burst has drained, which would idle the pipe between bursts. P_q aliases S_q
-    // in TMEM; a thread's MMAs run in issue order, so S_q(j+1) after O_q += P_q V_j
-    // is safe.
+    // units.) Inside the loop the issuer waits only on named barriers -- "P_q
+    // written" (1 + q, from the softmax) and "V_j, K_{j+1} loaded" (RELAY_BAR, from
+    // the relay warp): an mbarrier wait right after a burst of MMAs returns only once
+    // the burst has drained, which would idle the pipe between bursts. P_q aliases
+    // S_q in TMEM; a thread's MMAs run in issue order, so S_q(j+1) after
+    // O_q += P_q V_j is safe.
     if (n > 0) {
       const bool leader = lane == 0;
-      bool ok = __all_sync(0xffffffffu, wait(&bar_q, 0) && wait(&bar_kfull[0], 0));
+      const bool ok = __all_sync(0xffffffffu, wait(&bar_q, 0) && wait(&bar_kfull[0], 0));
       tc_fence_after();
       if (ok && leader) {
         for (int q = 0; q < C::NQ; ++q) {
@@ -291,21 +294,25 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         tc_commit(&bar_kempty[0]);
       }
       __syncwarp();
-      for (int it = 0; ok && it < n; ++it) {
+      // Every role takes part in every round of the named barriers, in order, whatever
+      // happens: the issuer runs all n rounds (issuing nothing once a wait failed),
+      // the relay syncs each round, and a softmax warpgroup that gave up syncs (not
+      // merely arrives) for its remaining rounds. A named barrier counts arrivals, so
+      // a role that arrived for two rounds before its partner synced once would
+      // complete a round without that partner and leave it waiting forever; in the
+      // normal flow the softmax cannot run a round ahead (P_q(j+1) needs S_q(j+1),
+      // issued only after the issuer passed round j).
+      for (int it = 0; it < n; ++it) {
         const int vs = it % C::VST, ks = (it + 1) % C::KST;
         const bool more = it + 1 < n;
-        for (int q = 0; ok && q < C::NQ; ++q) {
-          if (!(ok = __all_sync(0xffffffffu, wait(&bar_vfull[vs], (it / C::VST) & 1)))) break;
+        named_bar_sync(C::RELAY_BAR, 64);  // V_it (and K_{it+1}) are in smem
+        for (int q = 0; q < C::NQ; ++q) {
           named_bar_sync(1 + q, 128 + 32);  // P_q(it) is in TMEM
-          if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }  // warp-uniform
           tc_fence_after();
-          if (leader)
+          if (ok && leader) {
             issue_pv<C>(tmem + C::o_col(q), tmem + C::s_col(q), tmem + C::PLO_COL, sV(vs, 0),
                         sV(vs, C::NSPLIT - 1), it > 0);
-          if (more) {
-            if (!(ok = __all_sync(0xffffffffu, wait(&bar_kfull[ks], ((it + 1) / C::KST) & 1)))) break;
-            tc_fence_after();
-            if (leader) {
+            if (more) {
               issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(ks, 0),
                           sK(ks, C::NSPLIT - 1));
               tc_commit(&bar_s[q]);
@@ -313,8 +320,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
           }
           __syncwarp();
         }
-        if (!ok) break;
-        if (leader) {
+        if (ok && leader) {
           tc_commit(&bar_vempty[vs]);
           if (more) tc_commit(&bar_kempty[ks]);
         }
@@ -329,6 +335,21 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         while (!mbar_try_wait(&bar_drain[0], 0) && globaltimer() - t0 < a.limit_ns) {}
       }
       __syncwarp();
+    }
+  } else if (warp == C::RELAY_WARP) {
+    // ------------------------------------------------------------ load relay
+    // Waits (on mbarriers, which this warp can do without stalling any MMA) until V_j
+    // and K_{j+1} have landed and passes that on to the issuer through RELAY_BAR, one
+    // sync per round (never a bare arrive: see the issuer), also after an abort.
+    if (n > 0) {
+      bool ok = __all_sync(0xffffffffu, wait(&bar_q, 0));
+      for (int it = 0; it < n; ++it) {
+        if (ok)
+          ok = __all_sync(0xffffffffu,
+                          wait(&bar_vfull[it % C::VST], (it / C::VST) & 1) &&
+                              (it + 1 >= n || wait(&bar_kfull[(it + 1) % C::KST], ((it + 1) / C::KST) & 1)));
+        named_bar_sync(C::RELAY_BAR, 64);
+      }
     }
   }  // idle warps of the control warpgroup fall through
   } else {
@@ -353,9 +374,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
       const int t = t_lo + it;
       ok = __all_sync(0xffffffffu, wait(&bar_s[q], it & 1));
       if (!ok) {
-        // The issuer waits on named barrier 1 + q once per key tile: give it the
-        // remaining arrivals so that it cannot wait forever (it sees the abort flag).
-        for (int r = it; r < n; ++r) named_bar_arrive(1 + q, 128 + 32);
+        // The issuer takes one round of named barrier 1 + q per key tile: join the
+        // remaining rounds one by one (sync, not arrive) so that it can run out.
+        for (int r = it; r < n; ++r) named_bar_sync(1 + q, 128 + 32);
         break;
       }
       tc_fence_after();
