@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
         store_rows_tma<D, false, D / 32, false>(&m.dK, lane_addr + C::KV_ACC1, nc > 0, a.scale, st_k,
                                                 r_base, any, bg);
       }
-      if (lane == 0) bulk_wait_all();
+      if (lane == 0) bulk_wait_read_all();
       __syncwarp();
     }
   }
@@ -745,6 +745,20 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     mbar_init(&bar_done, 1);
     abort_sh = 0;
     fence_mbar_init();
+    if (nc > 0) {
+      // The resident Q / dO tiles and the first K / V chunk are issued here, before
+      // the TMEM allocation and the CTA-wide sync, so their latency overlaps the setup.
+      const int k0 = kt_lo * BLOCK_N;
+      mbar_arrive_expect_tx(&bar_qd, 2 * C::TILE);
+      mbar_arrive_expect_tx(&bar_kfull[0], C::TILE);
+      mbar_arrive_expect_tx(&bar_vfull[0], C::TILE);
+      for (int cb = 0; cb < C::NCB; ++cb) {
+        tma_load_3d(smem + C::Q_OFF + cb * C::CB, &m.Q[0], &bar_qd, cb * 64, i0, bh);
+        tma_load_3d(smem + C::DO_OFF + cb * C::CB, &m.dO[0], &bar_qd, cb * 64, i0, bh);
+        tma_load_3d(smem + C::K_OFF + cb * C::CB, &m.Kc[0], &bar_kfull[0], cb * 64, k0, bg);
+        tma_load_3d(smem + C::V_OFF + cb * C::CB, &m.Vc[0], &bar_vfull[0], cb * 64, k0, bg);
+      }
+    }
   }
   if (warp == C::MMA_WARP) {
     __syncwarp();
@@ -767,16 +781,10 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
   regs_decrease<C::REGS_CONTROL>();
   if (warp == C::TMA_WARP) {
     if (lane == 0 && nc > 0) {
-      tma_prefetch_desc(&m.Q[0]); tma_prefetch_desc(&m.Kc[0]); tma_prefetch_desc(&m.Vc[0]);
-      mbar_arrive_expect_tx(&bar_qd, 2 * C::TILE);
-      for (int cb = 0; cb < C::NCB; ++cb) {
-        tma_load_3d(gen(sbase + C::Q_OFF) + cb * C::CB, &m.Q[0], &bar_qd, cb * 64, i0, bh);
-        tma_load_3d(gen(sbase + C::DO_OFF) + cb * C::CB, &m.dO[0], &bar_qd, cb * 64, i0, bh);
-      }
-      int last_k[KST], last_v[VST];
-      for (int s = 0; s < KST; ++s) last_k[s] = -1;
-      for (int s = 0; s < VST; ++s) last_v[s] = -1;
-      for (int c = 0; c < nc; ++c) {
+      int last_k[KST], last_v[VST];  // chunk 0 was issued with the resident tiles
+      for (int s = 0; s < KST; ++s) last_k[s] = s == 0 ? 0 : -1;
+      for (int s = 0; s < VST; ++s) last_v[s] = s == 0 ? 0 : -1;
+      for (int c = 1; c < nc; ++c) {
         const int k0 = (kt_lo + c) * BLOCK_N;
         const int ks = c % KST, vs = c % VST;
         if (!wait(&bar_kempty[ks], ((c / KST) & 1) ^ 1)) break;
@@ -1065,6 +1073,23 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     for (int s = 0; s < 3; ++s) mbar_init(&bar_drain[s], 1);
     abort_sh = 0;
     fence_mbar_init();
+    if (nc > 0) {
+      // The resident K / V tiles and the first (Q, dO) chunk are issued here, before
+      // the TMEM allocation and the CTA-wide sync, so their latency overlaps the setup.
+      const int bh0 = b * a.H + g * rep, i00 = qt_lo * BLOCK_M;  // chunk 0
+      mbar_arrive_expect_tx(&bar_kv, 2 * C::TILE);
+      mbar_arrive_expect_tx(&bar_dofull[0], C::TILE);
+      mbar_arrive_expect_tx(&bar_qfull[0], C::TILE + C::VEC);
+      for (int cb = 0; cb < C::NCB; ++cb) {
+        tma_load_3d(smem + C::K_OFF + cb * C::CB, &m.K[0], &bar_kv, cb * 64, j0, bg);
+        tma_load_3d(smem + C::V_OFF + cb * C::CB, &m.V[0], &bar_kv, cb * 64, j0, bg);
+        tma_load_3d(smem + C::DO_OFF + cb * C::CB, &m.dOc[0], &bar_dofull[0], cb * 64, i00, bh0);
+        tma_load_3d(smem + C::Q_OFF + cb * C::CB, &m.Qc[0], &bar_qfull[0], cb * 64, i00, bh0);
+      }
+      float* vec = reinterpret_cast<float*>(smem + C::VEC_OFF);
+      tma_load_3d(vec, &m.L, &bar_qfull[0], i00, bh0, 0);
+      tma_load_3d(vec + 128, &m.Dl, &bar_qfull[0], i00, bh0, 0);
+    }
   }
   if (warp == C::A_WARP) {
     __syncwarp();
@@ -1092,15 +1117,9 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
   regs_decrease<C::REGS_CONTROL>();
   if (warp == C::TMA_WARP) {
     if (lane == 0 && nc > 0) {
-      tma_prefetch_desc(&m.K[0]); tma_prefetch_desc(&m.Qc[0]); tma_prefetch_desc(&m.dOc[0]);
-      mbar_arrive_expect_tx(&bar_kv, 2 * C::TILE);
-      for (int cb = 0; cb < C::NCB; ++cb) {
-        tma_load_3d(gen(sbase + C::K_OFF) + cb * C::CB, &m.K[0], &bar_kv, cb * 64, j0, bg);
-        tma_load_3d(gen(sbase + C::V_OFF) + cb * C::CB, &m.V[0], &bar_kv, cb * 64, j0, bg);
-      }
-      int last_q[NS], last_do[NS];
-      for (int s = 0; s < NS; ++s) last_q[s] = last_do[s] = -1;
-      for (int c = 0; c < nc; ++c) {
+      int last_q[NS], last_do[NS];  // chunk 0 was issued with the resident tiles
+      for (int s = 0; s < NS; ++s) last_q[s] = last_do[s] = s == 0 ? 0 : -1;
+      for (int c = 1; c < nc; ++c) {
         const int st = c % NS;
         int bh, i0;
         chunk_rows(c, &bh, &i0);

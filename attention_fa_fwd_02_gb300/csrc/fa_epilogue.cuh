@@ -29,9 +29,10 @@ constexpr uint32_t epi_warp_bytes() {
 // holds BOXES boxes; with fewer boxes than the row needs, the warp waits for the
 // previous stores to have read the staging area before refilling it. have == false
 // writes zeros (no accumulator). any_row == false skips the stores (all rows are
-// past the tensor's end). With WAIT, every store has completed on return; without,
-// the caller issues bulk_wait_all() (lane 0) before the staging area is reused or
-// the CTA exits.
+// past the tensor's end). With WAIT, the stores have read their shared-memory
+// sources on return (the global writes complete on their own, before the kernel
+// does); without, the caller issues bulk_wait_read_all() (lane 0) before the staging
+// area is reused or the CTA exits.
 template <int D, bool OUT_BF16, int BOXES, bool WAIT = true>
 __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tm, uint32_t t_addr, bool have,
                                                float mul, uint32_t stage, int r_base, bool any_row,
@@ -97,7 +98,7 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tm, uint32_t t
     }
   }
   if constexpr (WAIT) {
-    if (lane == 0) bulk_wait_all();
+    if (lane == 0) bulk_wait_read_all();
     __syncwarp();
   }
 }

@@ -143,6 +143,37 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
   }
 }
 
+// TMA loads of key tile t into ring slot it % KST (K) / it % VST (V).
+template <class C>
+__device__ __forceinline__ void issue_k_load(uint8_t* smem, int it, int t, int bg,
+                                             const CUtensorMap* tmK, const CUtensorMap* tmKlo,
+                                             uint64_t* bar_kfull) {
+  const int ks = it % C::KST;
+  mbar_arrive_expect_tx(&bar_kfull[ks], C::NSPLIT * C::TILE_BYTES);
+  for (int sp = 0; sp < C::NSPLIT; ++sp)
+    for (int cb = 0; cb < C::NCB; ++cb)
+      tma_load_3d(smem + C::K_OFF + (ks * C::NSPLIT + sp) * C::TILE_BYTES + cb * C::CB_BYTES,
+                  sp ? tmKlo : tmK, &bar_kfull[ks], cb * C::ROW_ELEMS, t * BLOCK_N, bg);
+}
+template <class C>
+__device__ __forceinline__ void issue_v_load(uint8_t* smem, int it, int t, int bg,
+                                             const CUtensorMap* tmV, const CUtensorMap* tmVlo,
+                                             uint64_t* bar_vfull) {
+  const int vs = it % C::VST;
+  mbar_arrive_expect_tx(&bar_vfull[vs], C::NSPLIT * C::TILE_BYTES);
+  for (int sp = 0; sp < C::NSPLIT; ++sp) {
+    uint8_t* dst = smem + C::V_OFF + (vs * C::NSPLIT + sp) * C::TILE_BYTES;
+    if constexpr (!C::F32) {
+      for (int cb = 0; cb < C::NCB; ++cb)
+        tma_load_3d(dst + cb * C::CB_BYTES, tmV, &bar_vfull[vs], cb * C::ROW_ELEMS, t * BLOCK_N, bg);
+    } else {  // V^T: 4 boxes of 32 keys x D rows
+      for (int cb = 0; cb < 4; ++cb)
+        tma_load_3d(dst + cb * C::VT_CB_BYTES, sp ? tmVlo : tmV, &bar_vfull[vs], t * BLOCK_N + cb * 32,
+                    0, bg);
+    }
+  }
+}
+
 template <int D, bool F32>
 __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
@@ -192,6 +223,18 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     for (int q = 0; q < C::NQ; ++q) mbar_init(&bar_drain[q], 1);
     abort_sh = 0;
     fence_mbar_init();
+    if (n > 0) {
+      // The Q tiles and the first K / V tiles are issued here, before the TMEM
+      // allocation and the CTA-wide sync, so their latency overlaps the setup.
+      mbar_arrive_expect_tx(&bar_q, C::NQ * C::NSPLIT * C::TILE_BYTES);
+      for (int q = 0; q < C::NQ; ++q)
+        for (int sp = 0; sp < C::NSPLIT; ++sp)
+          for (int cb = 0; cb < C::NCB; ++cb)
+            tma_load_3d(smem + C::Q_OFF + (q * C::NSPLIT + sp) * C::TILE_BYTES + cb * C::CB_BYTES,
+                        sp ? &tmQlo : &tmQ, &bar_q, cb * C::ROW_ELEMS, row0 + q * BLOCK_M, bh);
+      issue_k_load<C>(smem, 0, t_lo, bg, &tmK, &tmKlo, bar_kfull);
+      issue_v_load<C>(smem, 0, t_lo, bg, &tmV, &tmVlo, bar_vfull);
+    }
   }
   if (warp == C::MMA_WARP) {
     __syncwarp();
@@ -215,40 +258,16 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
   if (warp == C::TMA_WARP) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n > 0) {
-      tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(&bar_q, C::NQ * C::NSPLIT * C::TILE_BYTES);
-      for (int q = 0; q < C::NQ; ++q)
-        for (int sp = 0; sp < C::NSPLIT; ++sp)
-          for (int cb = 0; cb < C::NCB; ++cb)
-            tma_load_3d(smem + (sQ(q, sp) - sbase) + cb * C::CB_BYTES, sp ? &tmQlo : &tmQ, &bar_q,
-                        cb * C::ROW_ELEMS, row0 + q * BLOCK_M, bh);
-      int last_k[C::KST], last_v[C::VST];
-      for (int s = 0; s < C::KST; ++s) last_k[s] = -1;
-      for (int s = 0; s < C::VST; ++s) last_v[s] = -1;
-      for (int it = 0; it < n; ++it) {
-        const int t = t_lo + it;
-        const int ks = it % C::KST;
+      int last_k[C::KST], last_v[C::VST];  // key tile 0 was issued with the Q tiles
+      for (int s = 0; s < C::KST; ++s) last_k[s] = s == 0 ? 0 : -1;
+      for (int s = 0; s < C::VST; ++s) last_v[s] = s == 0 ? 0 : -1;
+      for (int it = 1; it < n; ++it) {
+        const int ks = it % C::KST, vs = it % C::VST;
         if (!wait(&bar_kempty[ks], ((it / C::KST) & 1) ^ 1)) break;
-        mbar_arrive_expect_tx(&bar_kfull[ks], C::NSPLIT * C::TILE_BYTES);
-        for (int sp = 0; sp < C::NSPLIT; ++sp)
-          for (int cb = 0; cb < C::NCB; ++cb)
-            tma_load_3d(smem + (sK(ks, sp) - sbase) + cb * C::CB_BYTES, sp ? &tmKlo : &tmK,
-                        &bar_kfull[ks], cb * C::ROW_ELEMS, t * BLOCK_N, bg);
+        issue_k_load<C>(smem, it, t_lo + it, bg, &tmK, &tmKlo, bar_kfull);
         last_k[ks] = it / C::KST;
-        const int vs = it % C::VST;
         if (!wait(&bar_vempty[vs], ((it / C::VST) & 1) ^ 1)) break;
-        mbar_arrive_expect_tx(&bar_vfull[vs], C::NSPLIT * C::TILE_BYTES);
-        for (int sp = 0; sp < C::NSPLIT; ++sp) {
-          if constexpr (!C::F32) {
-            for (int cb = 0; cb < C::NCB; ++cb)
-              tma_load_3d(smem + (sV(vs, sp) - sbase) + cb * C::CB_BYTES, &tmV, &bar_vfull[vs],
-                          cb * C::ROW_ELEMS, t * BLOCK_N, bg);
-          } else {  // V^T: 4 boxes of 32 keys x D rows
-            for (int cb = 0; cb < 4; ++cb)
-              tma_load_3d(smem + (sV(vs, sp) - sbase) + cb * C::VT_CB_BYTES, sp ? &tmVlo : &tmV,
-                          &bar_vfull[vs], t * BLOCK_N + cb * 32, 0, bg);
-          }
-        }
+        issue_v_load<C>(smem, it, t_lo + it, bg, &tmV, &tmVlo, bar_vfull);
         last_v[vs] = it / C::VST;
       }
       // Drain: every issued copy must land before the CTA may exit.
