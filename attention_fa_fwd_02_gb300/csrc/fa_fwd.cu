@@ -89,6 +89,10 @@ struct FwdCfg {
   static constexpr uint32_t STAGE_PER_WARP = NSPLIT * TILE_BYTES / 4;
   static constexpr int STAGE_BOXES = (int)(STAGE_PER_WARP / EPI_BOX_BYTES);
   static_assert(STAGE_BOXES >= 1 && STAGE_PER_WARP % 1024 == 0, "O staging layout");
+  // The last tile stages in the K ring instead (free once every MMA has completed).
+  static constexpr uint32_t LAST_STAGE_PER_WARP = KST * NSPLIT * TILE_BYTES / 4;
+  static constexpr int LAST_STAGE_BOXES = (int)(LAST_STAGE_PER_WARP / EPI_BOX_BYTES);
+  static_assert(LAST_STAGE_BOXES >= 1 && LAST_STAGE_PER_WARP % 1024 == 0, "O staging layout");
 };
 
 template <class C>
@@ -335,6 +339,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
               issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(ks, 0),
                           sK(ks, C::NSPLIT - 1));
               tc_commit(&bar_s[q]);
+            } else {
+              tc_commit(&bar_o[q]);  // tile q's last MMA: its epilogue may start
             }
           }
           __syncwarp();
@@ -346,8 +352,6 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         __syncwarp();
       }
       if (leader) {
-        if (ok)
-          for (int q = 0; q < C::NQ; ++q) tc_commit(&bar_o[q]);
         // Drain: no MMA may still be running when TMEM is released.
         tc_commit(&bar_drain[0]);
         const uint64_t t0 = globaltimer();
@@ -495,15 +499,27 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     if (ok) {
       const float inv = (l > 0.f) ? (1.f / l) : 0.f;
       if (i < a.Sq) a.LSE[(size_t)bh * a.Sq + i] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
-      // The tile's last MMA has completed (bar_o), so nothing reads Q_q any more.
-      const uint32_t stage = sQ(q, 0) + wq * C::STAGE_PER_WARP;
+      // The tile's last MMA has completed (bar_o), so nothing reads Q_q any more. The
+      // last tile's bar_o follows every MMA of the CTA, so it may also stage in the
+      // (spent) K ring and write all its boxes in one round.
       const int r_base = r0 + wq * 32;
-      if (a.out_bf16)
-        store_rows_tma<D, true, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                 r_base < a.Sq, bh);
-      else
-        store_rows_tma<D, false, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                  r_base < a.Sq, bh);
+      if (q == C::NQ - 1 && C::NQ > 1) {
+        const uint32_t stage = sbase + C::K_OFF + wq * C::LAST_STAGE_PER_WARP;
+        if (a.out_bf16)
+          store_rows_tma<D, true, C::LAST_STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
+                                                        r_base < a.Sq, bh);
+        else
+          store_rows_tma<D, false, C::LAST_STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
+                                                         r_base < a.Sq, bh);
+      } else {
+        const uint32_t stage = sQ(q, 0) + wq * C::STAGE_PER_WARP;
+        if (a.out_bf16)
+          store_rows_tma<D, true, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
+                                                   r_base < a.Sq, bh);
+        else
+          store_rows_tma<D, false, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
+                                                    r_base < a.Sq, bh);
+      }
     }
   }
 
