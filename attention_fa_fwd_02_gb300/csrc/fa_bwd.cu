@@ -711,7 +711,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_qd, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST],
+  __shared__ __align__(8) uint64_t bar_q, bar_do, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST],
       bar_vempty[VST], bar_s, bar_dp, bar_sfree, bar_dpfree, bar_ds[2], bar_accdone[2], bar_done,
       bar_drain[3];
   __shared__ uint32_t tmem_base_sh;
@@ -730,7 +730,8 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
   const int nc = kt_hi - kt_lo;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar_qd, 1);
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_do, 1);
     for (int s = 0; s < KST; ++s) { mbar_init(&bar_kfull[s], 1); mbar_init(&bar_kempty[s], 1); }
     for (int s = 0; s < VST; ++s) { mbar_init(&bar_vfull[s], 1); mbar_init(&bar_vempty[s], 1); }
     mbar_init(&bar_s, 1);
@@ -749,12 +750,13 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
       // The resident Q / dO tiles and the first K / V chunk are issued here, before
       // the TMEM allocation and the CTA-wide sync, so their latency overlaps the setup.
       const int k0 = kt_lo * BLOCK_N;
-      mbar_arrive_expect_tx(&bar_qd, 2 * C::TILE);
+      mbar_arrive_expect_tx(&bar_q, C::TILE);
+      mbar_arrive_expect_tx(&bar_do, C::TILE);
       mbar_arrive_expect_tx(&bar_kfull[0], C::TILE);
       mbar_arrive_expect_tx(&bar_vfull[0], C::TILE);
       for (int cb = 0; cb < C::NCB; ++cb) {
-        tma_load_3d(smem + C::Q_OFF + cb * C::CB, &m.Q[0], &bar_qd, cb * 64, i0, bh);
-        tma_load_3d(smem + C::DO_OFF + cb * C::CB, &m.dO[0], &bar_qd, cb * 64, i0, bh);
+        tma_load_3d(smem + C::Q_OFF + cb * C::CB, &m.Q[0], &bar_q, cb * 64, i0, bh);
+        tma_load_3d(smem + C::DO_OFF + cb * C::CB, &m.dO[0], &bar_do, cb * 64, i0, bh);
         tma_load_3d(smem + C::K_OFF + cb * C::CB, &m.Kc[0], &bar_kfull[0], cb * 64, k0, bg);
         tma_load_3d(smem + C::V_OFF + cb * C::CB, &m.Vc[0], &bar_vfull[0], cb * 64, k0, bg);
       }
@@ -798,7 +800,8 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
           tma_load_3d(gen(sV(vs)) + cb * C::CB, &m.Vc[0], &bar_vfull[vs], cb * 64, k0, bg);
         last_v[vs] = c / VST;
       }
-      drain_wait(&bar_qd, 0, a.limit_ns);
+      drain_wait(&bar_q, 0, a.limit_ns);
+      drain_wait(&bar_do, 0, a.limit_ns);
       for (int s = 0; s < KST; ++s)
         if (last_k[s] >= 0) drain_wait(&bar_kfull[s], last_k[s] & 1, a.limit_ns);
       for (int s = 0; s < VST; ++s)
@@ -810,7 +813,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     // has loaded dP(c-1).
     const bool is_s = warp == C::MMA_WARP;
     if (lane == 0 && nc > 0) {
-      bool ok = wait(&bar_qd, 0);
+      bool ok = wait(is_s ? &bar_q : &bar_do, 0);  // S needs Q, dP needs dO
       for (int c = 0; ok && c < nc; ++c) {
         if (is_s) {
           const int ks = c % KST;

@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_q, bar_kfull[C::KST], bar_kempty[C::KST],
+  __shared__ __align__(8) uint64_t bar_q[C::NQ], bar_kfull[C::KST], bar_kempty[C::KST],
       bar_vfull[C::VST], bar_vempty[C::VST], bar_s[C::NQ], bar_p[C::NQ], bar_o[C::NQ],
       bar_drain[C::NQ];
   __shared__ uint32_t tmem_base_sh;
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
   const int n = t_hi - t_lo;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar_q, 1);
+    for (int q = 0; q < C::NQ; ++q) mbar_init(&bar_q[q], 1);  // one per tile: S_0 need not wait for Q_1
     // a K / V stage is free once the MMAs of every tile that read it have completed
     for (int s = 0; s < C::KST; ++s) { mbar_init(&bar_kfull[s], 1); mbar_init(&bar_kempty[s], 1); }
     for (int s = 0; s < C::VST; ++s) { mbar_init(&bar_vfull[s], 1); mbar_init(&bar_vempty[s], 1); }
@@ -230,12 +230,13 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     if (n > 0) {
       // The Q tiles and the first K / V tiles are issued here, before the TMEM
       // allocation and the CTA-wide sync, so their latency overlaps the setup.
-      mbar_arrive_expect_tx(&bar_q, C::NQ * C::NSPLIT * C::TILE_BYTES);
-      for (int q = 0; q < C::NQ; ++q)
+      for (int q = 0; q < C::NQ; ++q) {
+        mbar_arrive_expect_tx(&bar_q[q], C::NSPLIT * C::TILE_BYTES);
         for (int sp = 0; sp < C::NSPLIT; ++sp)
           for (int cb = 0; cb < C::NCB; ++cb)
             tma_load_3d(smem + C::Q_OFF + (q * C::NSPLIT + sp) * C::TILE_BYTES + cb * C::CB_BYTES,
-                        sp ? &tmQlo : &tmQ, &bar_q, cb * C::ROW_ELEMS, row0 + q * BLOCK_M, bh);
+                        sp ? &tmQlo : &tmQ, &bar_q[q], cb * C::ROW_ELEMS, row0 + q * BLOCK_M, bh);
+      }
       issue_k_load<C>(smem, 0, t_lo, bg, &tmK, &tmKlo, bar_kfull);
       issue_v_load<C>(smem, 0, t_lo, bg, &tmV, &tmVlo, bar_vfull);
     }
@@ -285,9 +286,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
           const uint64_t t0 = globaltimer();
           while (!mbar_try_wait(&bar_vfull[s], last_v[s] & 1) && globaltimer() - t0 < a.limit_ns) {}
         }
-      {
+      for (int q = 0; q < C::NQ; ++q) {
         const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(&bar_q, 0) && globaltimer() - t0 < a.limit_ns) {}
+        while (!mbar_try_wait(&bar_q[q], 0) && globaltimer() - t0 < a.limit_ns) {}
       }
     }
   } else if (warp == C::MMA_WARP) {
@@ -306,16 +307,18 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     // O_q += P_q V_j is safe.
     if (n > 0) {
       const bool leader = lane == 0;
-      const bool ok = __all_sync(0xffffffffu, wait(&bar_q, 0) && wait(&bar_kfull[0], 0));
-      tc_fence_after();
-      if (ok && leader) {
-        for (int q = 0; q < C::NQ; ++q) {
+      bool ok = __all_sync(0xffffffffu, wait(&bar_kfull[0], 0));
+      for (int q = 0; q < C::NQ; ++q) {
+        ok = ok && __all_sync(0xffffffffu, wait(&bar_q[q], 0));
+        tc_fence_after();
+        if (ok && leader) {
           issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(0, 0),
                       sK(0, C::NSPLIT - 1));
           tc_commit(&bar_s[q]);
         }
-        tc_commit(&bar_kempty[0]);
+        __syncwarp();
       }
+      if (ok && leader) tc_commit(&bar_kempty[0]);
       __syncwarp();
       // Every role takes part in every round of the named barriers, in order, whatever
       // happens: the issuer runs all n rounds (issuing nothing once a wait failed),
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     // and K_{j+1} have landed and passes that on to the issuer through RELAY_BAR, one
     // sync per round (never a bare arrive: see the issuer), also after an abort.
     if (n > 0) {
-      bool ok = __all_sync(0xffffffffu, wait(&bar_q, 0));
+      bool ok = true;
       for (int it = 0; it < n; ++it) {
         if (ok)
           ok = __all_sync(0xffffffffu,
