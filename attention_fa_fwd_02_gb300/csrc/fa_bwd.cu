@@ -23,6 +23,8 @@
 // For fp32 inputs every product is the 3xTF32 sum a_hi b_hi + a_hi b_lo + a_lo b_hi.
 #include <cfloat>
 #include <climits>
+#include <algorithm>
+#include <type_traits>
 #include "fa_common.cuh"
 #include "ptx.cuh"
 #include "fa_prepass.cuh"
@@ -689,7 +691,7 @@ struct Dq16Cfg {
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DS_COL = 256, ACC = 384;
   static constexpr uint32_t EPI_WARP = epi_warp_bytes<D, false>();
   static_assert(SMEM <= 227u * 1024u, "shared memory budget");
-  static_assert(4 * EPI_WARP <= 2 * TILE + KST * TILE, "epilogue staging");
+  static_assert(4 * EPI_WARP <= VST * TILE, "epilogue staging (the V ring)");
 };
 
 template <int D>
@@ -703,6 +705,63 @@ __device__ __forceinline__ void issue_rowdot128(uint32_t d, uint32_t a, uint32_t
   }
 }
 
+// Epilogue piece of the persistent dQ kernel: NCOL accumulator columns of this
+// warp's 32 rows, already in registers, times mul, go out through the 1024-byte
+// aligned staging area `stage` (NCOL * 4 or * 2 bytes per row, as 128-byte boxes)
+// with TMA stores to tensor columns x0 ..; lane 0 commits them as one bulk group.
+template <int NCOL, bool OUT_BF16>
+__device__ __forceinline__ void stage_store_rows(const uint32_t (&r)[NCOL], float mul,
+                                                 uint32_t stage, const CUtensorMap* tm, int x0,
+                                                 int r_base, bool any_row, int z) {
+  constexpr int COLS = OUT_BF16 ? 64 : 32;  // columns per 128-byte box row
+  constexpr int NBOX = NCOL / COLS;
+  static_assert(NCOL % COLS == 0, "whole boxes");
+  const uint32_t lane = lane_id(), sw = lane & 7u;
+#pragma unroll
+  for (int bx = 0; bx < NBOX; ++bx) {
+    const uint32_t row = stage + bx * EPI_BOX_BYTES + lane * 128u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint32_t w[4];
+      if constexpr (!OUT_BF16) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = __float_as_uint(__uint_as_float(r[bx * 32 + 4 * c + e]) * mul);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = bx * 64 + 8 * c + 2 * e;
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[k]) * mul,
+                                                    __uint_as_float(r[k + 1]) * mul);
+          w[e] = *reinterpret_cast<uint32_t*>(&v2);
+        }
+      }
+      st_shared_v4(row + ((c ^ sw) << 4), w[0], w[1], w[2], w[3]);
+    }
+  }
+  fence_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    if (any_row)
+      for (int bx = 0; bx < NBOX; ++bx)
+        tma_store_3d(tm, stage + bx * EPI_BOX_BYTES, x0 + bx * COLS, r_base, z);
+    bulk_commit_group();
+  }
+}
+
+// Persistent: one CTA per SM walks the (batch, head, query tile) work items
+// blockIdx.x, blockIdx.x + gridDim.x, ... (heaviest causal tiles first, so the round
+// robin stays balanced). Every ring and hand-off barrier counts chunks across items
+// (g), so the K / V ring streams the next item's first chunks while the current
+// item's epilogue runs. Per item with keys (counted by j): Q_{j+1} (dO_{j+1}) is
+// loaded as soon as the last S (dP) MMA of item j has completed (q_rel / do_rel),
+// the epilogue stages dQ in the V ring, so item j+1's first V chunk waits until the
+// epilogue has read that staging area (v_free), and the first dQ MMA of item j+1
+// waits until the epilogue has read dQ out of TMEM (dq_free). Each of these
+// per-item phases can only complete after every role has observed the one before
+// (e.g. q_rel(j+1) follows S MMAs of item j+1, which need Q_{j+1}, loaded only after
+// q_rel(j) was seen), so a parity wait never misses a phase. An item whose rows see
+// no key touches none of these barriers: its softmax warps write the zero rows
+// directly.
 template <int D>
 __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     fa_bwd_dq16_kernel(const __grid_constant__ QMaps m, const BwdArgs a) {
@@ -713,21 +772,27 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_q, bar_do, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST],
       bar_vempty[VST], bar_s, bar_dp, bar_sfree, bar_dpfree, bar_ds[2], bar_accdone[2], bar_done,
-      bar_drain[3];
+      bar_dqfree, bar_qrel, bar_dorel, bar_vfree, bar_drain[3];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int warp = warp_id(), lane = lane_id();
   volatile int* abort_flag = &abort_sh;
 
-  const int qt_lin = blockIdx.x / a.BHx;
-  const int bh = blockIdx.x % a.BHx;
-  const int qt = a.lpt ? (a.n_tiles - 1 - qt_lin) : qt_lin;
-  const int b = bh / a.H, h = bh % a.H;
-  const int bg = b * a.HKV + h / (a.H / a.HKV);
-  const int i0 = qt * BLOCK_M;
-  int kt_lo, kt_hi;
-  kv_tile_range(i0, min(i0 + BLOCK_M - 1, a.Sq - 1), a.Sk, a.causal, a.window, &kt_lo, &kt_hi);
-  const int nc = kt_hi - kt_lo;
+  const int n_items = a.n_tiles * a.BHx;
+  struct Item { int bh, bg, i0, kt_lo, nc; };
+  auto item = [&](int w) {
+    Item it;
+    const int qt_lin = w / a.BHx;
+    it.bh = w % a.BHx;
+    const int qt = a.lpt ? (a.n_tiles - 1 - qt_lin) : qt_lin;
+    const int b = it.bh / a.H, h = it.bh % a.H;
+    it.bg = b * a.HKV + h / (a.H / a.HKV);
+    it.i0 = qt * BLOCK_M;
+    int hi;
+    kv_tile_range(it.i0, min(it.i0 + BLOCK_M - 1, a.Sq - 1), a.Sk, a.causal, a.window, &it.kt_lo, &hi);
+    it.nc = hi - it.kt_lo;
+    return it;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
@@ -742,23 +807,28 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
       mbar_init(&bar_ds[s], 256);
       mbar_init(&bar_accdone[s], 1);
     }
-    for (int s = 0; s < 3; ++s) mbar_init(&bar_drain[s], 1);
     mbar_init(&bar_done, 1);
+    mbar_init(&bar_dqfree, 256);
+    mbar_init(&bar_qrel, 1);
+    mbar_init(&bar_dorel, 1);
+    mbar_init(&bar_vfree, 256);
+    for (int s = 0; s < 3; ++s) mbar_init(&bar_drain[s], 1);
     abort_sh = 0;
     fence_mbar_init();
-    if (nc > 0) {
-      // The resident Q / dO tiles and the first K / V chunk are issued here, before
+    if ((int)blockIdx.x < n_items && item(blockIdx.x).nc > 0) {
+      // The first item's Q / dO tiles and first K / V chunk are issued here, before
       // the TMEM allocation and the CTA-wide sync, so their latency overlaps the setup.
-      const int k0 = kt_lo * BLOCK_N;
+      const Item it = item(blockIdx.x);
+      const int k0 = it.kt_lo * BLOCK_N;
       mbar_arrive_expect_tx(&bar_q, C::TILE);
       mbar_arrive_expect_tx(&bar_do, C::TILE);
       mbar_arrive_expect_tx(&bar_kfull[0], C::TILE);
       mbar_arrive_expect_tx(&bar_vfull[0], C::TILE);
       for (int cb = 0; cb < C::NCB; ++cb) {
-        tma_load_3d(smem + C::Q_OFF + cb * C::CB, &m.Q[0], &bar_q, cb * 64, i0, bh);
-        tma_load_3d(smem + C::DO_OFF + cb * C::CB, &m.dO[0], &bar_do, cb * 64, i0, bh);
-        tma_load_3d(smem + C::K_OFF + cb * C::CB, &m.Kc[0], &bar_kfull[0], cb * 64, k0, bg);
-        tma_load_3d(smem + C::V_OFF + cb * C::CB, &m.Vc[0], &bar_vfull[0], cb * 64, k0, bg);
+        tma_load_3d(smem + C::Q_OFF + cb * C::CB, &m.Q[0], &bar_q, cb * 64, it.i0, it.bh);
+        tma_load_3d(smem + C::DO_OFF + cb * C::CB, &m.dO[0], &bar_do, cb * 64, it.i0, it.bh);
+        tma_load_3d(smem + C::K_OFF + cb * C::CB, &m.Kc[0], &bar_kfull[0], cb * 64, k0, it.bg);
+        tma_load_3d(smem + C::V_OFF + cb * C::CB, &m.Vc[0], &bar_vfull[0], cb * 64, k0, it.bg);
       }
     }
   }
@@ -782,167 +852,258 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
   if (warp >= C::SOFTMAX_WARPS) {
   regs_decrease<C::REGS_CONTROL>();
   if (warp == C::TMA_WARP) {
-    if (lane == 0 && nc > 0) {
-      int last_k[KST], last_v[VST];  // chunk 0 was issued with the resident tiles
-      for (int s = 0; s < KST; ++s) last_k[s] = s == 0 ? 0 : -1;
-      for (int s = 0; s < VST; ++s) last_v[s] = s == 0 ? 0 : -1;
-      for (int c = 1; c < nc; ++c) {
-        const int k0 = (kt_lo + c) * BLOCK_N;
-        const int ks = c % KST, vs = c % VST;
-        if (!wait(&bar_kempty[ks], ((c / KST) & 1) ^ 1)) break;
+    if (lane == 0) {
+      const bool setup_issued = (int)blockIdx.x < n_items && item(blockIdx.x).nc > 0;
+      int g = 0, j = 0;  // chunks, items with keys, issued so far
+      int last_k[KST], last_v[VST], last_qd = setup_issued ? 0 : -1;
+      for (int s = 0; s < KST; ++s) last_k[s] = -1;
+      for (int s = 0; s < VST; ++s) last_v[s] = -1;
+      auto load_k = [&](int g_, int k0, int bg) {
+        const int ks = g_ % KST;
+        if (!wait(&bar_kempty[ks], ((g_ / KST) & 1) ^ 1)) return false;
         mbar_arrive_expect_tx(&bar_kfull[ks], C::TILE);
         for (int cb = 0; cb < C::NCB; ++cb)
           tma_load_3d(gen(sK(ks)) + cb * C::CB, &m.Kc[0], &bar_kfull[ks], cb * 64, k0, bg);
-        last_k[ks] = c / KST;
-        if (!wait(&bar_vempty[vs], ((c / VST) & 1) ^ 1)) break;
+        last_k[ks] = g_ / KST;
+        return true;
+      };
+      auto load_v = [&](int g_, int k0, int bg) {
+        const int vs = g_ % VST;
+        if (!wait(&bar_vempty[vs], ((g_ / VST) & 1) ^ 1)) return false;
         mbar_arrive_expect_tx(&bar_vfull[vs], C::TILE);
         for (int cb = 0; cb < C::NCB; ++cb)
           tma_load_3d(gen(sV(vs)) + cb * C::CB, &m.Vc[0], &bar_vfull[vs], cb * 64, k0, bg);
-        last_v[vs] = c / VST;
+        last_v[vs] = g_ / VST;
+        return true;
+      };
+      // Q (dO) of item j once the last S (dP) MMA of item j-1 has read the buffer
+      auto load_res = [&](const Item& it, bool is_q) {
+        uint64_t* full = is_q ? &bar_q : &bar_do;
+        if (j > 0 && !wait(is_q ? &bar_qrel : &bar_dorel, (j - 1) & 1)) return false;
+        mbar_arrive_expect_tx(full, C::TILE);
+        for (int cb = 0; cb < C::NCB; ++cb)
+          tma_load_3d(gen(sbase + (is_q ? C::Q_OFF : C::DO_OFF)) + cb * C::CB, is_q ? &m.Q[0] : &m.dO[0],
+                      full, cb * 64, it.i0, it.bh);
+        last_qd = j;
+        return true;
+      };
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+        const Item it = item(w);
+        if (it.nc == 0) continue;
+        const bool pre = j == 0 && setup_issued;  // Q / dO and chunk 0 came with the setup
+        for (int c = 0; c < it.nc; ++c, ++g) {
+          const int k0 = (it.kt_lo + c) * BLOCK_N;
+          if (c == 0) {
+            if (pre) { last_k[0] = last_v[0] = 0; continue; }
+            // Q, K_0, dO first; V_0 goes where the previous epilogue staged its dQ
+            if (!(ok = load_res(it, true) && load_k(g, k0, it.bg) && load_res(it, false))) break;
+            if (j > 0 && !(ok = wait(&bar_vfree, (j - 1) & 1))) break;
+            if (!(ok = load_v(g, k0, it.bg))) break;
+          } else if (!(ok = load_k(g, k0, it.bg) && load_v(g, k0, it.bg))) {
+            break;
+          }
+        }
+        ++j;
       }
-      drain_wait(&bar_q, 0, a.limit_ns);
-      drain_wait(&bar_do, 0, a.limit_ns);
+      // Drain: every issued copy must land before the CTA may exit.
       for (int s = 0; s < KST; ++s)
         if (last_k[s] >= 0) drain_wait(&bar_kfull[s], last_k[s] & 1, a.limit_ns);
       for (int s = 0; s < VST; ++s)
         if (last_v[s] >= 0) drain_wait(&bar_vfull[s], last_v[s] & 1, a.limit_ns);
+      if (last_qd >= 0) {
+        drain_wait(&bar_q, last_qd & 1, a.limit_ns);
+        drain_wait(&bar_do, last_qd & 1, a.limit_ns);
+      }
     }
   } else if (warp == C::MMA_WARP || warp == C::DP_WARP) {
-    // Score issuers (one thread each, so neither waits behind the other's barrier):
-    // S(c) = Q K_c^T once the softmax has loaded S(c-1); dP(c) = dO V_c^T once it
-    // has loaded dP(c-1).
+    // Score issuers (one thread each): S(g) = Q K_g^T once the softmax has loaded
+    // S(g-1); dP(g) = dO V_g^T once it has loaded dP(g-1).
     const bool is_s = warp == C::MMA_WARP;
-    if (lane == 0 && nc > 0) {
-      bool ok = wait(is_s ? &bar_q : &bar_do, 0);  // S needs Q, dP needs dO
-      for (int c = 0; ok && c < nc; ++c) {
-        if (is_s) {
-          const int ks = c % KST;
-          if (!(ok = wait(&bar_kfull[ks], (c / KST) & 1))) break;
-          if (c > 0 && !(ok = wait(&bar_sfree, (c - 1) & 1))) break;
-          tc_fence_after();
-          issue_rowdot128<D>(tmem + C::S_COL, sbase + C::Q_OFF, sK(ks));
-          tc_commit(&bar_s);
-        } else {
-          const int vs = c % VST;
-          if (!(ok = wait(&bar_vfull[vs], (c / VST) & 1))) break;
-          if (c > 0 && !(ok = wait(&bar_dpfree, (c - 1) & 1))) break;
-          tc_fence_after();
-          issue_rowdot128<D>(tmem + C::DP_COL, sbase + C::DO_OFF, sV(vs));
-          tc_commit(&bar_dp);
-          tc_commit(&bar_vempty[vs]);
+    if (lane == 0) {
+      bool ok = true;
+      int g = 0, j = 0;  // chunks and items with keys so far
+      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+        const Item it = item(w);
+        if (it.nc == 0) continue;
+        if (!(ok = wait(is_s ? &bar_q : &bar_do, j & 1))) break;  // S needs Q, dP needs dO
+        ++j;
+        for (int c = 0; c < it.nc; ++c, ++g) {
+          if (is_s) {
+            const int ks = g % KST;
+            if (!(ok = wait(&bar_kfull[ks], (g / KST) & 1))) break;
+            if (g > 0 && !(ok = wait(&bar_sfree, (g - 1) & 1))) break;
+            tc_fence_after();
+            issue_rowdot128<D>(tmem + C::S_COL, sbase + C::Q_OFF, sK(ks));
+            tc_commit(&bar_s);
+          } else {
+            const int vs = g % VST;
+            if (!(ok = wait(&bar_vfull[vs], (g / VST) & 1))) break;
+            if (g > 0 && !(ok = wait(&bar_dpfree, (g - 1) & 1))) break;
+            tc_fence_after();
+            issue_rowdot128<D>(tmem + C::DP_COL, sbase + C::DO_OFF, sV(vs));
+            tc_commit(&bar_dp);
+            tc_commit(&bar_vempty[vs]);
+          }
         }
+        // the item's Q (dO) buffer is free once its last S (dP) MMA has completed
+        if (ok) tc_commit(is_s ? &bar_qrel : &bar_dorel);
       }
       tc_commit(&bar_drain[is_s ? 0 : 2]);
       drain_wait(&bar_drain[is_s ? 0 : 2], 0, a.limit_ns);
     }
   } else if (warp == C::ACC_WARP) {
-    // Accumulate issuer: dQ += dS(c) K_c (dS fp16 in TMEM, K_c MN-major); then K_c's
-    // stage and the dS slot are free.
-    if (lane == 0 && nc > 0) {
+    // Accumulate issuer: dQ += dS(g) K_g once the softmax has written dS(g); the
+    // first chunk of an item also waits until the previous dQ left TMEM.
+    if (lane == 0) {
       constexpr uint32_t id = make_idesc(128, D, FMT_F16, FMT_F16, false, true);
       bool ok = true;
-      for (int c = 0; ok && c < nc; ++c) {
-        const int pb = c & 1, ks = c % KST;
-        if (!(ok = wait(&bar_ds[pb], (c >> 1) & 1))) break;
-        tc_fence_after();
+      int g = 0, j = 0;  // chunks and items with keys so far
+      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+        const Item it = item(w);
+        if (it.nc == 0) continue;
+        for (int c = 0; c < it.nc; ++c, ++g) {
+          const int pb = g & 1, ks = g % KST;
+          if (!(ok = wait(&bar_ds[pb], (g >> 1) & 1))) break;
+          if (c == 0 && j > 0 && !(ok = wait(&bar_dqfree, (j - 1) & 1))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-          mma_f16_ts(tmem + C::ACC, tmem + C::DS_COL + 64 * pb + kk * 8,
-                     make_sdesc(sK(ks) + kk * 16 * 128, C::CB, SW128_ATOM), id,
-                     (c > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&bar_kempty[ks]);
-        tc_commit(&bar_accdone[pb]);
+          for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+            mma_f16_ts(tmem + C::ACC, tmem + C::DS_COL + 64 * pb + kk * 8,
+                       make_sdesc(sK(ks) + kk * 16 * 128, C::CB, SW128_ATOM), id,
+                       (c > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&bar_kempty[ks]);
+          tc_commit(&bar_accdone[pb]);
+        }
+        if (ok) tc_commit(&bar_done);  // the item's dQ is complete (one phase per item)
+        ++j;
       }
-      if (ok) tc_commit(&bar_done);
       tc_commit(&bar_drain[1]);
       drain_wait(&bar_drain[1], 0, a.limit_ns);
     }
-  }
+  }  // the idle warp falls through
   } else {
     regs_increase<C::REGS_SOFTMAX>();
     const int wq = warp % 4, half = warp / 4;
-    const int i = i0 + wq * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = a.scale_log2;
-    const bool row_valid = i < a.Sq;
-    const size_t vrow = (size_t)bh * a.ldq + (size_t)(row_valid ? i : 0);
-    const float nl = row_valid ? -a.lse2[vrow] : -INFINITY;
-    const float dl = row_valid ? a.delta[vrow] : 0.f;
-    const int hi_i = a.causal ? min(i, a.Sk - 1) : a.Sk - 1;
-    const int lo_i = a.window > 0 ? i - a.window + 1 : INT_MIN / 2;
     bool ok = true;
-    for (int c = 0; c < nc; ++c) {
-      const int pb = c & 1;
-      const int kc0 = (kt_lo + c) * BLOCK_N;
-      const int k0 = kc0 + half * 64;
-      float s[64], dp[64];
-      ok = __all_sync(0xffffffffu, wait(&bar_s, c & 1));
-      if (!ok) break;
-      tc_fence_after();
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld32x2(lane_addr + C::S_COL + half * 64, lane_addr + C::S_COL + half * 64 + 32, r0, r1);
-        tc_fence_before();
-        mbar_arrive(&bar_sfree);
+    int g = 0, j = 0;  // chunks and items with keys so far
+    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      const Item it = item(w);
+      const int i = it.i0 + wq * 32 + lane;
+      if (it.nc == 0) {
+        // no key for any row of the tile: dQ = 0, written directly (no barrier involved)
+        if (i < a.Sq) {
+          const size_t off = ((size_t)it.bh * a.Sq + i) * D + half * (D / 2);
+          if (a.out_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dQ) + off);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          s[k] = __uint_as_float(r0[k]);
-          s[32 + k] = __uint_as_float(r1[k]);
+            for (int e = 0; e < D / 16; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.dQ) + off);
+#pragma unroll
+            for (int e = 0; e < D / 8; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
+        continue;
       }
-      if (tile_needs_mask(i0, i0 + BLOCK_M - 1, kc0, kc0 + BLOCK_N - 1, a.Sk, a.causal, a.window)) {
-        const int rel_hi = hi_i - k0, rel_lo = lo_i - k0;
-#pragma unroll
-        for (int k = 0; k < 64; ++k)
-          if (k > rel_hi || k < rel_lo) s[k] = -INFINITY;
-      }
-#pragma unroll
-      for (int k = 0; k < 64; ++k) s[k] = ex2(fmaf(s[k], sl2, nl));
-      ok = __all_sync(0xffffffffu, wait(&bar_dp, c & 1));
-      if (!ok) break;
-      tc_fence_after();
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld32x2(lane_addr + C::DP_COL + half * 64, lane_addr + C::DP_COL + half * 64 + 32, r0, r1);
-        tc_fence_before();
-        mbar_arrive(&bar_dpfree);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          dp[k] = __uint_as_float(r0[k]);
-          dp[32 + k] = __uint_as_float(r1[k]);
-        }
-      }
-      uint32_t pk[32];
-#pragma unroll
-      for (int k = 0; k < 32; ++k)
-        pk[k] = pack_half2(s[2 * k] * (dp[2 * k] - dl), s[2 * k + 1] * (dp[2 * k + 1] - dl));
-      // the dS slot is free once dQ += dS(c-2) K has completed
-      if (c >= 2) {
-        ok = __all_sync(0xffffffffu, wait(&bar_accdone[pb], ((c >> 1) - 1) & 1));
+      const bool row_valid = i < a.Sq;
+      const size_t vrow = (size_t)it.bh * a.ldq + (size_t)(row_valid ? i : 0);
+      const float nl = row_valid ? -a.lse2[vrow] : -INFINITY;
+      const float dl = row_valid ? a.delta[vrow] : 0.f;
+      const int hi_i = a.causal ? min(i, a.Sk - 1) : a.Sk - 1;
+      const int lo_i = a.window > 0 ? i - a.window + 1 : INT_MIN / 2;
+      for (int c = 0; c < it.nc; ++c, ++g) {
+        const int pb = g & 1;
+        const int kc0 = (it.kt_lo + c) * BLOCK_N;
+        const int k0 = kc0 + half * 64;
+        float s[64], dp[64];
+        ok = __all_sync(0xffffffffu, wait(&bar_s, g & 1));
         if (!ok) break;
         tc_fence_after();
-      }
-      tmem_st32(lane_addr + C::DS_COL + 64 * pb + half * 32, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar_ds[pb]);
-    }
-    if (half == 0) {
-      if (ok && nc > 0) {
-        ok = __all_sync(0xffffffffu, wait(&bar_done, 0));
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld32x2(lane_addr + C::S_COL + half * 64, lane_addr + C::S_COL + half * 64 + 32, r0, r1);
+          tc_fence_before();
+          mbar_arrive(&bar_sfree);
+#pragma unroll
+          for (int kk = 0; kk < 32; ++kk) {
+            s[kk] = __uint_as_float(r0[kk]);
+            s[32 + kk] = __uint_as_float(r1[kk]);
+          }
+        }
+        if (tile_needs_mask(it.i0, it.i0 + BLOCK_M - 1, kc0, kc0 + BLOCK_N - 1, a.Sk, a.causal,
+                            a.window)) {
+          const int rel_hi = hi_i - k0, rel_lo = lo_i - k0;
+#pragma unroll
+          for (int kk = 0; kk < 64; ++kk)
+            if (kk > rel_hi || kk < rel_lo) s[kk] = -INFINITY;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 64; ++kk) s[kk] = ex2(fmaf(s[kk], sl2, nl));
+        ok = __all_sync(0xffffffffu, wait(&bar_dp, g & 1));
+        if (!ok) break;
         tc_fence_after();
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld32x2(lane_addr + C::DP_COL + half * 64, lane_addr + C::DP_COL + half * 64 + 32, r0, r1);
+          tc_fence_before();
+          mbar_arrive(&bar_dpfree);
+#pragma unroll
+          for (int kk = 0; kk < 32; ++kk) {
+            dp[kk] = __uint_as_float(r0[kk]);
+            dp[32 + kk] = __uint_as_float(r1[kk]);
+          }
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int kk = 0; kk < 32; ++kk)
+          pk[kk] = pack_half2(s[2 * kk] * (dp[2 * kk] - dl), s[2 * kk + 1] * (dp[2 * kk + 1] - dl));
+        // the dS slot is free once dQ += dS(g-2) K has completed
+        if (g >= 2) {
+          ok = __all_sync(0xffffffffu, wait(&bar_accdone[pb], ((g >> 1) - 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        tmem_st32(lane_addr + C::DS_COL + 64 * pb + half * 32, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar_ds[pb]);
       }
-      if (ok) {
-        // bar_done: every MMA has completed, so all operand buffers are free.
-        const uint32_t st_q = sbase + wq * C::EPI_WARP;
-        const int r_base = i0 + wq * 32;
-        if (a.out_bf16)
-          store_rows_tma<D, true, D / 64>(&m.dQ, lane_addr + C::ACC, nc > 0, a.scale, st_q,
-                                          r_base, r_base < a.Sq, bh);
-        else
-          store_rows_tma<D, false, D / 32>(&m.dQ, lane_addr + C::ACC, nc > 0, a.scale, st_q,
-                                           r_base, r_base < a.Sq, bh);
-      }
+      if (!ok) break;
+      // ---- epilogue of the item: dQ * scale, rows i0 + 32 (w % 4) .., warps w < 4 and
+      // w >= 4 taking halves of the columns (bf16 at D = 64: warps w < 4 all of them).
+      ok = __all_sync(0xffffffffu, wait(&bar_done, j & 1));
+      if (!ok) break;
+      tc_fence_after();
+      ++j;
+      const int r_base = it.i0 + wq * 32;
+      const bool any = r_base < a.Sq;
+      auto epilogue = [&](auto out_bf16_tag) {
+        constexpr bool BF = decltype(out_bf16_tag)::value;
+        constexpr bool ONE_HALF = BF && D == 64;  // a bf16 box is a whole 64-column row
+        constexpr int NCOL = ONE_HALF ? D : D / 2;
+        const bool mine = !ONE_HALF || half == 0;
+        const int x0 = ONE_HALF ? 0 : half * (D / 2);
+        uint32_t r[NCOL];
+        if (mine) {
+          if constexpr (NCOL == 64) tmem_ld32x2(lane_addr + C::ACC + x0, lane_addr + C::ACC + x0 + 32,
+                                                *reinterpret_cast<uint32_t(*)[32]>(&r[0]),
+                                                *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+          else tmem_ld32(lane_addr + C::ACC + x0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        }
+        tc_fence_before();
+        mbar_arrive(&bar_dqfree);  // dQ has left TMEM: the next item may accumulate
+        if (mine)
+          stage_store_rows<NCOL, BF>(r, a.scale, sbase + C::V_OFF + warp * (C::EPI_WARP / 2),
+                                     &m.dQ, x0, r_base, any, it.bh);
+      };
+      if (a.out_bf16) epilogue(std::true_type{});
+      else epilogue(std::false_type{});
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+      mbar_arrive(&bar_vfree);  // the staging area (the V ring) may be refilled
     }
   }
   tc_fence_before();
@@ -1645,7 +1806,10 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       if (e == cudaSuccess) {
         host::KernelTimer kt(D == 128 ? "fa_bwd_dq_kernel<128,bf16>" : "fa_bwd_dq_kernel<64,bf16>",
                              stream);
-        kern<<<(unsigned)(BH * aq.n_tiles), C16::THREADS, C16::SMEM, stream>>>(mq, aq);
+        // persistent: one CTA per SM, each walking work items with the grid's stride
+        const size_t n_items = BH * (size_t)aq.n_tiles;
+        const unsigned grid = (unsigned)std::min<size_t>(n_items, (size_t)host::sm_count());
+        kern<<<grid, C16::THREADS, C16::SMEM, stream>>>(mq, aq);
         e = cudaGetLastError();
       }
     }
