@@ -1040,8 +1040,15 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
           for (int kk = 0; kk < 64; ++kk)
             if (kk > rel_hi || kk < rel_lo) s[kk] = -INFINITY;
         }
+        {
+          const float2 sl2x2 = make_float2(sl2, sl2), nlx2 = make_float2(nl, nl);
 #pragma unroll
-        for (int kk = 0; kk < 64; ++kk) s[kk] = ex2(fmaf(s[kk], sl2, nl));
+          for (int kk = 0; kk < 32; ++kk) {  // exponent arguments on packed pairs
+            const float2 x = fma2(make_float2(s[2 * kk], s[2 * kk + 1]), sl2x2, nlx2);
+            s[2 * kk] = ex2(x.x);
+            s[2 * kk + 1] = ex2(x.y);
+          }
+        }
         ok = __all_sync(0xffffffffu, wait(&bar_dp, g & 1));
         if (!ok) break;
         tc_fence_after();
@@ -1057,9 +1064,13 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
           }
         }
         uint32_t pk[32];
+        const float2 ndl = make_float2(-dl, -dl);
 #pragma unroll
-        for (int kk = 0; kk < 32; ++kk)
-          pk[kk] = pack_half2(s[2 * kk] * (dp[2 * kk] - dl), s[2 * kk + 1] * (dp[2 * kk + 1] - dl));
+        for (int kk = 0; kk < 32; ++kk) {  // dS = P (dP - delta) on packed pairs
+          const float2 u = mul2(make_float2(s[2 * kk], s[2 * kk + 1]),
+                                add2(make_float2(dp[2 * kk], dp[2 * kk + 1]), ndl));
+          pk[kk] = pack_half2(u.x, u.y);
+        }
         // the dS slot is free once dQ += dS(g-2) K has completed
         if (g >= 2) {
           ok = __all_sync(0xffffffffu, wait(&bar_accdone[pb], ((g >> 1) - 1) & 1));
@@ -1140,21 +1151,34 @@ struct Dkv16Cfg {
   static constexpr uint32_t VEC = 2 * 128 * 4;            // lse2 | delta of a chunk
   static constexpr uint32_t VEC_OFF = PT_OFF + 2 * CB;
   static constexpr uint32_t LAYOUT = VEC_OFF + NS * VEC;  // bytes from the 1 KB-aligned base
-  static constexpr int SOFTMAX_WARPS = 8;
-  static constexpr int A_WARP = 8, B_WARP = 9, TMA_WARP = 10, DV_WARP = 11;
-  static constexpr int THREADS = 384;
-  static constexpr uint32_t REGS_SOFTMAX = 200, REGS_CONTROL = 96;
-  static_assert(256 * REGS_SOFTMAX + 128 * REGS_CONTROL <= 384 * 168, "register split");
+  // NPART softmax warps share each TMEM lane quarter, each taking QC = 128 / NPART
+  // of the chunk's queries: more warps per SM sub-partition hide more latency.
+  static constexpr int NPART = 2, QC = 128 / NPART;
+  static constexpr int SOFTMAX_WARPS = 4 * NPART;
+  static constexpr int A_WARP = SOFTMAX_WARPS, B_WARP = A_WARP + 1, TMA_WARP = A_WARP + 2,
+                       DV_WARP = A_WARP + 3;
+  static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 4);
+  static constexpr int SM_THREADS = 32 * SOFTMAX_WARPS;
+  // The softmax barriers take one arrival per warp (lane 0, after every lane's fence
+  // and a warp sync): 32x fewer shared-memory atomics than one per thread.
+  static constexpr int SM_ARRIVALS = SOFTMAX_WARPS;
+  static constexpr uint32_t REGS_LAUNCH = (65536 / THREADS) / 8 * 8;
+  static constexpr uint32_t REGS_SOFTMAX = NPART == 4 ? 104 : 200;
+  static constexpr uint32_t REGS_CONTROL = NPART == 4 ? 64 : 96;
+  static_assert(SM_THREADS * REGS_SOFTMAX + 128 * REGS_CONTROL <= THREADS * REGS_LAUNCH,
+                "register split");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DV = 256, DK = 256 + D;
   static constexpr uint32_t EPI_WARP = epi_warp_bytes<D, false>();
   // 227 KB per block minus the alignment of the base to 1 KB leaves 226 KB.
   static_assert(LAYOUT <= 226u * 1024u, "shared memory budget");
   static_assert(DK + D <= TMEM_COLS, "TMEM budget");
-  static_assert(8 * EPI_WARP <= VEC_OFF, "epilogue staging");
-  // fp16 dS^T column of k-step kk (16 queries): halves of 64 queries sit at
-  // columns 0 and 64 of the slot, 8 columns per k-step.
-  __host__ __device__ static constexpr uint32_t op_col(int kk) { return (kk / 4) * 64 + (kk % 4) * 8; }
+  static_assert(SOFTMAX_WARPS * (EPI_WARP * 2 / NPART) <= VEC_OFF, "epilogue staging");
+  // fp16 dS^T column of k-step kk (16 queries): each part writes its QC / 2 packed
+  // columns at the start of its own QC-column range of the dP^T slot.
+  __host__ __device__ static constexpr uint32_t op_col(int kk) {
+    return (kk / (QC / 16)) * QC + (kk % (QC / 16)) * 8;
+  }
 };
 
 // ACC[128 x D] (+)= A(TMEM fp16, 128 x 128, halves at columns 0 / 64) * B[128 x D]
@@ -1228,11 +1252,11 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
       mbar_init(&bar_doempty[s], 2);  // dP^T(c) (B) and dV(c) (A) have read dO_c
     }
     mbar_init(&bar_s, 1);
-    mbar_init(&bar_sfree, 256);
-    mbar_init(&bar_p, 256);
+    mbar_init(&bar_sfree, C::SM_ARRIVALS);
+    mbar_init(&bar_p, C::SM_ARRIVALS);
     mbar_init(&bar_dvdone, 1);
     mbar_init(&bar_dp, 1);
-    mbar_init(&bar_ds, 256);
+    mbar_init(&bar_ds, C::SM_ARRIVALS);
     mbar_init(&bar_done, 2);  // dV issuer and B issuer
     for (int s = 0; s < 3; ++s) mbar_init(&bar_drain[s], 1);
     abort_sh = 0;
@@ -1362,37 +1386,46 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
   }
   } else {
     regs_increase<C::REGS_SOFTMAX>();
-    // thread = key row j = TMEM lane; warps w and w + 4 take queries [0, 64) / [64, 128)
-    const int wq = warp % 4, half = warp / 4;
+    // thread = key row j = TMEM lane; warp w takes queries [QC p, QC p + QC), p = w / 4
+    constexpr int QC = C::QC;
+    const int wq = warp % 4, part = warp / 4;
     const int r_in = wq * 32 + lane;
     const int j = j0 + r_in;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-    // this thread's 128-byte row of P^T (queries half*64 ..) in the swizzled tile
-    const uint32_t pt_row = sbase + C::PT_OFF + half * C::CB + r_in * 128;
+    // this thread's QC queries of row r_in of the swizzled P^T tile: column block
+    // (QC p) / 64, 16-byte chunks from (QC p % 64) / 8
+    const uint32_t pt_row = sbase + C::PT_OFF + (QC * part / 64) * C::CB + r_in * 128;
+    const uint32_t chunk0 = (uint32_t)((QC * part % 64) / 8);
     const uint32_t sw = (uint32_t)(r_in & 7);
     const float sl2 = a.scale_log2;
     const bool row_dead = j >= a.Sk;
+    auto ld_cols = [&](uint32_t addr, float (&x)[QC]) {
+      if constexpr (QC == 64) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32x2(addr, addr + 32, r0, r1);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) { x[k] = __uint_as_float(r0[k]); x[32 + k] = __uint_as_float(r1[k]); }
+      } else {
+        uint32_t r0[32];
+        tmem_ld32(addr, r0);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(r0[k]);
+      }
+    };
     bool ok = true;
     for (int c = 0; c < nc; ++c) {
       const int st = c % NS;
       int bh, i0;
       chunk_rows(c, &bh, &i0);
-      const int q0 = i0 + half * 64;  // first query of this thread's half
-      float s[64];
+      const int q0 = i0 + part * QC;  // first query of this thread's part
+      float s[QC];
       ok = __all_sync(0xffffffffu, wait(&bar_s, c & 1) && wait(&bar_qfull[st], (c / NS) & 1));
       if (!ok) break;
       tc_fence_after();
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld32x2(lane_addr + C::S_COL + half * 64, lane_addr + C::S_COL + half * 64 + 32, r0, r1);
-        tc_fence_before();
-        mbar_arrive(&bar_sfree);  // the S^T slot may take the next chunk
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          s[k] = __uint_as_float(r0[k]);
-          s[32 + k] = __uint_as_float(r1[k]);
-        }
-      }
+      ld_cols(lane_addr + C::S_COL + part * QC, s);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_sfree);  // the S^T slot may take the next chunk
       // query i = q0 + k sees key j iff (!causal || j <= i) && (!window || j >= i-w+1)
       // && i < Sq && j < Sk
       if (tile_needs_mask(i0, i0 + BLOCK_M - 1, j0, j0 + BLOCK_N - 1, a.Sk, a.causal, a.window) ||
@@ -1400,18 +1433,21 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         const int k_lo = a.causal ? j - q0 : INT_MIN / 2;
         const int k_hi = min(a.window > 0 ? j + a.window - 1 - q0 : INT_MAX / 2, a.Sq - 1 - q0);
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
+        for (int k = 0; k < QC; ++k)
           if (row_dead || k < k_lo || k > k_hi) s[k] = -INFINITY;
       }
       // lse2 / delta of the chunk's queries, read with explicit shared-space loads
-      const uint32_t lv = sbase + C::VEC_OFF + st * C::VEC + half * 64 * 4;
+      const uint32_t lv = sbase + C::VEC_OFF + st * C::VEC + part * QC * 4;
+      const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
-      for (int k4 = 0; k4 < 16; ++k4) {
+      for (int k4 = 0; k4 < QC / 4; ++k4) {  // exponent arguments on packed pairs
         const float4 l4 = ld_shared_v4(lv + 16 * k4);
-        s[4 * k4] = ex2(fmaf(s[4 * k4], sl2, -l4.x));
-        s[4 * k4 + 1] = ex2(fmaf(s[4 * k4 + 1], sl2, -l4.y));
-        s[4 * k4 + 2] = ex2(fmaf(s[4 * k4 + 2], sl2, -l4.z));
-        s[4 * k4 + 3] = ex2(fmaf(s[4 * k4 + 3], sl2, -l4.w));
+        const float2 xa = fma2(make_float2(s[4 * k4], s[4 * k4 + 1]), sl2x2, make_float2(-l4.x, -l4.y));
+        const float2 xb = fma2(make_float2(s[4 * k4 + 2], s[4 * k4 + 3]), sl2x2, make_float2(-l4.z, -l4.w));
+        s[4 * k4] = ex2(xa.x);
+        s[4 * k4 + 1] = ex2(xa.y);
+        s[4 * k4 + 2] = ex2(xb.x);
+        s[4 * k4 + 3] = ex2(xb.y);
       }
       // P^T into shared memory once dV has consumed the previous chunk's
       if (c > 0) {
@@ -1419,55 +1455,68 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         if (!ok) break;
       }
 #pragma unroll
-      for (int k8 = 0; k8 < 8; ++k8)
-        st_shared_v4(pt_row + (((uint32_t)k8 ^ sw) << 4), pack_half2(s[8 * k8], s[8 * k8 + 1]),
+      for (int k8 = 0; k8 < QC / 8; ++k8)
+        st_shared_v4(pt_row + (((chunk0 + (uint32_t)k8) ^ sw) << 4), pack_half2(s[8 * k8], s[8 * k8 + 1]),
                      pack_half2(s[8 * k8 + 2], s[8 * k8 + 3]), pack_half2(s[8 * k8 + 4], s[8 * k8 + 5]),
                      pack_half2(s[8 * k8 + 6], s[8 * k8 + 7]));
       fence_async_shared();
-      mbar_arrive(&bar_p);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p);
       ok = __all_sync(0xffffffffu, wait(&bar_dp, c & 1));
       if (!ok) break;
       tc_fence_after();
       {
-        uint32_t r0[32], r1[32];
-        tmem_ld32x2(lane_addr + C::DP_COL + half * 64, lane_addr + C::DP_COL + half * 64 + 32, r0,
-                    r1);
+        float g[QC];
+        ld_cols(lane_addr + C::DP_COL + part * QC, g);
         const uint32_t dv = lv + 128 * 4;
-        uint32_t pk[32];
+        uint32_t pk[QC / 2];
 #pragma unroll
-        for (int k4 = 0; k4 < 16; ++k4) {
+        for (int k4 = 0; k4 < QC / 4; ++k4) {
           const float4 d4 = ld_shared_v4(dv + 16 * k4);
           const int k = 4 * k4;
-          const float g0 = __uint_as_float(k < 32 ? r0[k] : r1[k - 32]);
-          const float g1 = __uint_as_float(k < 32 ? r0[k + 1] : r1[k - 31]);
-          const float g2 = __uint_as_float(k < 32 ? r0[k + 2] : r1[k - 30]);
-          const float g3 = __uint_as_float(k < 32 ? r0[k + 3] : r1[k - 29]);
-          pk[2 * k4] = pack_half2(s[k] * (g0 - d4.x), s[k + 1] * (g1 - d4.y));
-          pk[2 * k4 + 1] = pack_half2(s[k + 2] * (g2 - d4.z), s[k + 3] * (g3 - d4.w));
+          // dS = P (dP - delta) on packed pairs
+          const float2 ua = mul2(make_float2(s[k], s[k + 1]),
+                                 add2(make_float2(g[k], g[k + 1]), make_float2(-d4.x, -d4.y)));
+          const float2 ub = mul2(make_float2(s[k + 2], s[k + 3]),
+                                 add2(make_float2(g[k + 2], g[k + 3]), make_float2(-d4.z, -d4.w)));
+          pk[2 * k4] = pack_half2(ua.x, ua.y);
+          pk[2 * k4 + 1] = pack_half2(ub.x, ub.y);
         }
-        tmem_st32(lane_addr + C::DP_COL + half * 64, pk);
+        // dS^T (fp16) into the first QC / 2 columns of this part's own dP^T range
+        if constexpr (QC == 64) tmem_st32(lane_addr + C::DP_COL + part * QC, pk);
+        else tmem_st16(lane_addr + C::DP_COL + part * QC, pk);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar_ds);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_ds);
     }
     if (ok && nc > 0) {
       ok = __all_sync(0xffffffffu, wait(&bar_done, 0));
       tc_fence_after();
     }
     if (ok) {
-      // bar_done: every MMA has completed, so all operand buffers are free. Warps
-      // w < 4 write dV, warps w >= 4 dK, rows j0 + 32 (w % 4) ...
-      const uint32_t stage = sbase + warp * C::EPI_WARP;
+      // bar_done: every MMA has completed, so all operand buffers are free. Parts
+      // 0 .. NPART/2-1 write dV, the others dK; each part D / (NPART / 2) columns of
+      // rows j0 + 32 (w % 4) ...
+      constexpr int HP = C::NPART / 2;     // parts per output
+      constexpr int DW = D / HP;           // columns per warp
+      const int which = part / HP, cpart = part % HP;
       const int r_base = j0 + wq * 32;
       const bool any = r_base < a.Sk;
-      const uint32_t acc = lane_addr + (half ? C::DK : C::DV);
-      const CUtensorMap* tm = half ? &m.dK : &m.dV;
-      const float mul = half ? a.scale : 1.f;
-      if (a.out_bf16)
-        store_rows_tma<D, true, D / 64>(tm, acc, nc > 0, mul, stage, r_base, any, bg);
-      else
-        store_rows_tma<D, false, D / 32>(tm, acc, nc > 0, mul, stage, r_base, any, bg);
+      const uint32_t acc = lane_addr + (which ? C::DK : C::DV) + cpart * DW;
+      const CUtensorMap* tm = which ? &m.dK : &m.dV;
+      const float mul = which ? a.scale : 1.f;
+      const uint32_t stage = sbase + warp * (C::EPI_WARP / HP);
+      if (a.out_bf16) {
+        if constexpr (DW % 64 == 0)
+          store_rows_tma<DW, true, DW / 64>(tm, acc, nc > 0, mul, stage, r_base, any, bg, cpart * DW);
+        else if (cpart == 0)  // a bf16 box is a 64-column row: one warp per output does it
+          store_rows_tma<D, true, D / 64>(tm, lane_addr + (which ? C::DK : C::DV), nc > 0, mul,
+                                          sbase + warp * C::EPI_WARP, r_base, any, bg);
+      } else {
+        store_rows_tma<DW, false, DW / 32>(tm, acc, nc > 0, mul, stage, r_base, any, bg, cpart * DW);
+      }
     }
   }
   tc_fence_before();
