@@ -574,7 +574,7 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
     if (host::scratch_alloc(&ws, nk * 2, stream) != cudaSuccess) return FA_ERR_CUDA;
     {
       host::KernelTimer kt("cvt_bf16_to_f16(V)", stream);
-      cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
+      cvt_bf16_to_f16_kernel<<<2 * grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
                                                          static_cast<uint4*>(ws), nk / 8);
     }
     enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, D, p.Sq, BHq, D, 64, 128);
@@ -785,7 +785,7 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
   // The whole scratch region used below is rewritten by the pre-pass kernels on
   // every call, so nothing left over from an earlier call is ever read.
   if constexpr (!F32) {
-    cvt_bf16_to_f16_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
+    cvt_bf16_to_f16_kernel<<<2 * grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
                                                        static_cast<uint4*>(ws), nk / 8);
     enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, D, p.Sq, BHq, D, 64, 128);
     enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, D, p.Sk, BHk, D, 64, 128);

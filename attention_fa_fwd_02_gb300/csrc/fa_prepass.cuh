@@ -12,9 +12,8 @@ namespace {
 // bf16 -> fp16, exact for 2^-14 <= |x| <= 65504. 8 elements per 16-byte vector.
 __global__ void cvt_bf16_to_f16_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
                                        size_t n8) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const uint4 v = in[i];
+  // four independent 16-byte loads in flight per thread, then the grid-stride tail
+  auto cvt = [](uint4 v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
 #pragma unroll
@@ -23,8 +22,18 @@ __global__ void cvt_bf16_to_f16_kernel(const uint4* __restrict__ in, uint4* __re
       const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
       o[e] = ptx::pack_half2(lo, hi);
     }
-    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = in[i + u * stride];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) out[i + u * stride] = cvt(v[u]);
   }
+  for (; i < n8; i += stride) out[i] = cvt(in[i]);
 }
 
 // x = hi + lo with hi = x with its low 13 mantissa bits cleared (a tf32 value)
