@@ -748,11 +748,10 @@ __device__ __forceinline__ void stage_store_rows(const uint32_t (&r)[NCOL], floa
   }
 }
 
-// Persistent: one CTA per SM walks the (batch, head, query tile) work items
-// blockIdx.x, blockIdx.x + gridDim.x, ... (heaviest causal tiles first, so the round
-// robin stays balanced). Every ring and hand-off barrier counts chunks across items
-// (g), so the K / V ring streams the next item's first chunks while the current
-// item's epilogue runs. Per item with keys (counted by j): Q_{j+1} (dO_{j+1}) is
+// Persistent: one CTA per SM walks the (batch, head, query tile) work items, heaviest
+// causal tiles first, in rounds of gridDim.x items taken in alternating directions.
+// Every ring and hand-off barrier counts chunks across items (g), so the K / V ring
+// streams the next item's first chunks while the current item's epilogue runs. Per item with keys (counted by j): Q_{j+1} (dO_{j+1}) is
 // loaded as soon as the last S (dP) MMA of item j has completed (q_rel / do_rel),
 // the epilogue stages dQ in the V ring, so item j+1's first V chunk waits until the
 // epilogue has read that staging area (v_free), and the first dQ MMA of item j+1
@@ -792,6 +791,14 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     kv_tile_range(it.i0, min(it.i0 + BLOCK_M - 1, a.Sq - 1), a.Sk, a.causal, a.window, &it.kt_lo, &hi);
     it.nc = hi - it.kt_lo;
     return it;
+  };
+  // The k-th item of this CTA: rounds of gridDim.x items, walked in alternating
+  // directions (CTA c takes item c of even rounds and item G-1-c of odd ones), so
+  // with the heaviest items first every CTA's total stays close to the mean. A round
+  // that has no item for this CTA is the last round.
+  auto item_w = [&](int k) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return k * G + ((k & 1) ? G - 1 - c : c);
   };
 
   if (threadIdx.x == 0) {
@@ -888,7 +895,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         return true;
       };
       bool ok = true;
-      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
         const Item it = item(w);
         if (it.nc == 0) continue;
         const bool pre = j == 0 && setup_issued;  // Q / dO and chunk 0 came with the setup
@@ -923,7 +930,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     if (lane == 0) {
       bool ok = true;
       int g = 0, j = 0;  // chunks and items with keys so far
-      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
         const Item it = item(w);
         if (it.nc == 0) continue;
         if (!(ok = wait(is_s ? &bar_q : &bar_do, j & 1))) break;  // S needs Q, dP needs dO
@@ -959,7 +966,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
       constexpr uint32_t id = make_idesc(128, D, FMT_F16, FMT_F16, false, true);
       bool ok = true;
       int g = 0, j = 0;  // chunks and items with keys so far
-      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
         const Item it = item(w);
         if (it.nc == 0) continue;
         for (int c = 0; c < it.nc; ++c, ++g) {
@@ -989,7 +996,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     const float sl2 = a.scale_log2;
     bool ok = true;
     int g = 0, j = 0;  // chunks and items with keys so far
-    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+    for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
       const Item it = item(w);
       const int i = it.i0 + wq * 32 + lane;
       if (it.nc == 0) {

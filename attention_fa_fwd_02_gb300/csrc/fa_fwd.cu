@@ -1,23 +1,26 @@
 // fa_fwd.cu -- forward attention on sm_103a: TMA-fed, warp-specialised, tcgen05/TMEM.
 //
-// One CTA owns NQ query tiles of 128 rows of one (batch, head) and walks the key
+// A work item is NQ query tiles of 128 rows of one (batch, head); it walks the key
 // tiles they may see (forge "flash_attention.metal", flash_attn_fwd: threadgroup of
 // consecutive query rows, K/V staged once per group, blocks outside the causal /
 // window band skipped, online softmax with m starting at -FLT_MAX; rustytorch
 // "flash_attention_forward.metal": O = softmax(Q K^T * scale) V and the LSE row
-// output). Roles:
+// output). One persistent CTA per SM runs a sequence of items. Roles:
 //   warps [0, 4*NQ)   softmax: thread = one query row = one TMEM lane. Reads the
 //                     S row from TMEM, masks boundary tiles, keeps the running max
 //                     m (log2 units) and sum l, writes P back into TMEM (fp16 for
 //                     bf16 inputs; tf32 hi + lo for fp32 inputs), rescales its O
 //                     row in TMEM when m grows by more than RESCALE_THRESHOLD, and
 //                     in the epilogue writes LSE = (m + log2 l) ln 2 and O = acc / l
-//                     (staged in the tile's spent Q buffer, written by TMA stores).
+//                     (staged in a V ring stage, written by TMA stores).
 //   warp 4*NQ         MMA issuer (one thread): S_q = Q_q K_j^T, O_q += P_q V_j,
 //                     bursts in a fixed tile order so the tiles alternate.
-//   warp 5*NQ         TMA producer (one thread): Q once, then K_j / V_j rings.
+//   warp 4*NQ + 1     TMA producer (one thread): Q per item, K_j ring.
+//   warp 4*NQ + 2     TMA producer (one thread): V_j ring and the epilogue stages.
+//   warp 4*NQ + 3     load relay: mbarrier waits passed on to the issuer.
 // Every barrier wait is bounded; on expiry the kernel raises the device status
 // word, drains its in-flight copies and MMAs, frees TMEM and returns.
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 #include <cstdio>
@@ -40,7 +43,8 @@ struct FwdArgs {
   int causal, window;
   int out_bf16;
   int n_qgroups;
-  int lpt;  // 1: launch the heaviest query groups first (causal)
+  int n_items;  // BH * n_qgroups
+  int lpt;  // 1: the heaviest query groups first (causal)
   int BH;
   unsigned long long limit_ns;
 };
@@ -65,13 +69,16 @@ struct FwdCfg {
   static constexpr uint32_t SMEM_BYTES = V_OFF + VST * NSPLIT * TILE_BYTES;
   static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
   static constexpr int SOFTMAX_WARPS = 4 * NQ;
-  // Warp SOFTMAX_WARPS issues every MMA and owns TMEM; the TMA producer follows the
-  // issuer slots. Whole warpgroups: the control warps share the last warpgroup with
-  // idle warps.
+  // The last warpgroup holds the control warps: the MMA issuer (which also owns
+  // TMEM), the Q / K producer, the V producer and the load relay.
   static constexpr int MMA_WARP = SOFTMAX_WARPS;
-  static constexpr int TMA_WARP = SOFTMAX_WARPS + NQ;
-  static constexpr int RELAY_WARP = TMA_WARP + 1;  // relays load completions to the issuer
-  static constexpr uint32_t RELAY_BAR = 3;         // named barriers 1, 2: P of tile 0, 1
+  static constexpr int KQ_WARP = SOFTMAX_WARPS + 1;
+  static constexpr int V_WARP = SOFTMAX_WARPS + 2;
+  static constexpr int RELAY_WARP = SOFTMAX_WARPS + 3;  // relays load completions to the issuer
+  // named barriers: 1 + q = P_q written (softmax -> issuer), RELAY_BAR = operands
+  // loaded (relay -> issuer), EPI_BAR0 + q = the four warps of tile q (epilogue)
+  static constexpr uint32_t RELAY_BAR = 3;
+  static constexpr uint32_t EPI_BAR0 = 4;
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 4);
   // Register split for NQ = 2 (launched at 168 per thread for 384 threads): the
   // softmax warpgroups hold a whole 128-column S row in registers.
@@ -84,15 +91,10 @@ struct FwdCfg {
   __host__ __device__ static constexpr uint32_t o_col(int q) { return 256u + (uint32_t)D * q; }
   static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory budget");
   static_assert(F32 ? (256 + D <= 512) : (256 + 2 * D <= 512), "TMEM budget");
-  // Epilogue: each softmax warp stages its 32 O rows in its quarter of the tile's Q
-  // buffer, free once the tile's last MMA has completed.
+  // Epilogue: each softmax warp stages its 32 O rows in its quarter of a V ring stage.
   static constexpr uint32_t STAGE_PER_WARP = NSPLIT * TILE_BYTES / 4;
   static constexpr int STAGE_BOXES = (int)(STAGE_PER_WARP / EPI_BOX_BYTES);
   static_assert(STAGE_BOXES >= 1 && STAGE_PER_WARP % 1024 == 0, "O staging layout");
-  // The last tile stages in the K ring instead (free once every MMA has completed).
-  static constexpr uint32_t LAST_STAGE_PER_WARP = KST * NSPLIT * TILE_BYTES / 4;
-  static constexpr int LAST_STAGE_BOXES = (int)(LAST_STAGE_PER_WARP / EPI_BOX_BYTES);
-  static_assert(LAST_STAGE_BOXES >= 1 && LAST_STAGE_PER_WARP % 1024 == 0, "O staging layout");
 };
 
 template <class C>
@@ -178,6 +180,18 @@ __device__ __forceinline__ void issue_v_load(uint8_t* smem, int it, int t, int b
   }
 }
 
+// Persistent: min(#work items, #SMs) CTAs; CTA c walks the work items (pairs of query
+// tiles of one (batch, head), heaviest causal groups first) in rounds of gridDim.x,
+// taking item c of even rounds and item G-1-c of odd ones so that every CTA's total
+// stays close to the mean. Every ring and hand-off barrier counts across items: key
+// tiles by g (K ring, S barriers), items with keys by j (Q tiles, O completion), and
+// the V ring by position, where each item also takes NQ positions for its epilogue's
+// staging. So the next item's Q tiles and first K tile load while the current item
+// finishes, its first S MMAs are issued right after the current item's last PV, and
+// the epilogue (O through the V ring to TMA stores) overlaps the other tile's MMAs.
+// A phase of a per-item barrier can only complete after every role has observed the
+// previous one (Q_q of item j+1 loads only after the last S MMA of item j completed,
+// which needs Q_q of item j), so a parity wait never misses a phase.
 template <int D, bool F32>
 __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
@@ -185,12 +199,12 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmVlo,
                   const __grid_constant__ CUtensorMap tmO, const FwdArgs a) {
   using C = FwdCfg<D, F32>;
+  constexpr int NQ = C::NQ, KST = C::KST, VST = C::VST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_q[C::NQ], bar_kfull[C::KST], bar_kempty[C::KST],
-      bar_vfull[C::VST], bar_vempty[C::VST], bar_s[C::NQ], bar_p[C::NQ], bar_o[C::NQ],
-      bar_drain[C::NQ];
+  __shared__ __align__(8) uint64_t bar_q[NQ], bar_qfree[NQ], bar_kfull[KST], bar_kempty[KST],
+      bar_vfull[VST], bar_vempty[VST], bar_grant[NQ], bar_s[NQ], bar_o[NQ], bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -198,47 +212,59 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
   const int lane = lane_id();
   volatile int* abort_flag = &abort_sh;
 
-  // ---- work decode: heaviest causal query groups first, heads of one kv group adjacent.
-  const int qg_lin = blockIdx.x / a.BH;
-  const int bh = blockIdx.x % a.BH;
-  const int qg = a.lpt ? (a.n_qgroups - 1 - qg_lin) : qg_lin;
-  const int b = bh / a.H, h = bh % a.H;
-  const int g = h / (a.H / a.HKV);
-  const int bg = b * a.HKV + g;
-  const int row0 = qg * (BLOCK_M * C::NQ);
-  int t_lo, t_hi;
-  {
-    int r1 = row0 + BLOCK_M * C::NQ - 1;
+  // ---- work items: query group qg (NQ tiles of 128 rows) of head bh, linear index
+  // w = qg_lin * BH + bh (the heads of one kv group adjacent).
+  struct Item { int bh, bg, row0, t_lo, n; };
+  auto item = [&](int w) {
+    Item it;
+    const int qg_lin = w / a.BH;
+    it.bh = w % a.BH;
+    const int qg = a.lpt ? (a.n_qgroups - 1 - qg_lin) : qg_lin;
+    const int b = it.bh / a.H, h = it.bh % a.H;
+    it.bg = b * a.HKV + h / (a.H / a.HKV);
+    it.row0 = qg * (BLOCK_M * NQ);
+    int r1 = it.row0 + BLOCK_M * NQ - 1;
     if (r1 > a.Sq - 1) r1 = a.Sq - 1;
-    kv_tile_range(row0, r1, a.Sk, a.causal, a.window, &t_lo, &t_hi);
-  }
-  const int n = t_hi - t_lo;
+    int hi;
+    kv_tile_range(it.row0, r1, a.Sk, a.causal, a.window, &it.t_lo, &hi);
+    it.n = hi - it.t_lo;
+    return it;
+  };
+  auto item_w = [&](int k) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return k * G + ((k & 1) ? G - 1 - c : c);
+  };
+  const Item first = item(item_w(0));  // gridDim.x <= n_items: every CTA has round 0
+  const bool setup_issued = first.n > 0;
 
   if (threadIdx.x == 0) {
-    for (int q = 0; q < C::NQ; ++q) mbar_init(&bar_q[q], 1);  // one per tile: S_0 need not wait for Q_1
-    // a K / V stage is free once the MMAs of every tile that read it have completed
-    for (int s = 0; s < C::KST; ++s) { mbar_init(&bar_kfull[s], 1); mbar_init(&bar_kempty[s], 1); }
-    for (int s = 0; s < C::VST; ++s) { mbar_init(&bar_vfull[s], 1); mbar_init(&bar_vempty[s], 1); }
-    for (int q = 0; q < C::NQ; ++q) {
+    for (int q = 0; q < NQ; ++q) {
+      mbar_init(&bar_q[q], 1);  // one per tile: S_0 need not wait for Q_1
+      mbar_init(&bar_qfree[q], 1);
       mbar_init(&bar_s[q], 1);
-      mbar_init(&bar_p[q], 128);
       mbar_init(&bar_o[q], 1);
+      mbar_init(&bar_grant[q], 1);
     }
-    for (int q = 0; q < C::NQ; ++q) mbar_init(&bar_drain[q], 1);
+    // a K / V stage is free once the MMAs of every tile that read it have completed
+    // (or, for a V stage lent to an epilogue, once its TMA stores have read it)
+    for (int s = 0; s < KST; ++s) { mbar_init(&bar_kfull[s], 1); mbar_init(&bar_kempty[s], 1); }
+    for (int s = 0; s < VST; ++s) { mbar_init(&bar_vfull[s], 1); mbar_init(&bar_vempty[s], 1); }
+    mbar_init(&bar_drain, 1);
     abort_sh = 0;
     fence_mbar_init();
-    if (n > 0) {
-      // The Q tiles and the first K / V tiles are issued here, before the TMEM
-      // allocation and the CTA-wide sync, so their latency overlaps the setup.
-      for (int q = 0; q < C::NQ; ++q) {
+    if (setup_issued) {
+      // The first item's Q tiles and first K / V tiles are issued here, before the
+      // TMEM allocation and the CTA-wide sync, so their latency overlaps the setup.
+      for (int q = 0; q < NQ; ++q) {
         mbar_arrive_expect_tx(&bar_q[q], C::NSPLIT * C::TILE_BYTES);
         for (int sp = 0; sp < C::NSPLIT; ++sp)
           for (int cb = 0; cb < C::NCB; ++cb)
             tma_load_3d(smem + C::Q_OFF + (q * C::NSPLIT + sp) * C::TILE_BYTES + cb * C::CB_BYTES,
-                        sp ? &tmQlo : &tmQ, &bar_q[q], cb * C::ROW_ELEMS, row0 + q * BLOCK_M, bh);
+                        sp ? &tmQlo : &tmQ, &bar_q[q], cb * C::ROW_ELEMS, first.row0 + q * BLOCK_M,
+                        first.bh);
       }
-      issue_k_load<C>(smem, 0, t_lo, bg, &tmK, &tmKlo, bar_kfull);
-      issue_v_load<C>(smem, 0, t_lo, bg, &tmV, &tmVlo, bar_vfull);
+      issue_k_load<C>(smem, 0, first.t_lo, first.bg, &tmK, &tmKlo, bar_kfull);
+      issue_v_load<C>(smem, 0, first.t_lo, first.bg, &tmV, &tmVlo, bar_vfull);
     }
   }
   if (warp == C::MMA_WARP) {
@@ -257,273 +283,396 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait(bar, parity, abort_flag, &g_fwd_status, DEV_TIMEOUT, a.limit_ns);
   };
+  auto drain = [&](uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity) && globaltimer() - t0 < a.limit_ns) {}
+  };
 
   if (warp >= C::SOFTMAX_WARPS) {
-  if constexpr (C::NQ == 2) regs_decrease<C::REGS_CONTROL>();
-  if (warp == C::TMA_WARP) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n > 0) {
-      int last_k[C::KST], last_v[C::VST];  // key tile 0 was issued with the Q tiles
-      for (int s = 0; s < C::KST; ++s) last_k[s] = s == 0 ? 0 : -1;
-      for (int s = 0; s < C::VST; ++s) last_v[s] = s == 0 ? 0 : -1;
-      for (int it = 1; it < n; ++it) {
-        const int ks = it % C::KST, vs = it % C::VST;
-        if (!wait(&bar_kempty[ks], ((it / C::KST) & 1) ^ 1)) break;
-        issue_k_load<C>(smem, it, t_lo + it, bg, &tmK, &tmKlo, bar_kfull);
-        last_k[ks] = it / C::KST;
-        if (!wait(&bar_vempty[vs], ((it / C::VST) & 1) ^ 1)) break;
-        issue_v_load<C>(smem, it, t_lo + it, bg, &tmV, &tmVlo, bar_vfull);
-        last_v[vs] = it / C::VST;
+  if constexpr (NQ == 2) regs_decrease<C::REGS_CONTROL>();
+  if (warp == C::KQ_WARP) {
+    // ------------------------------------------------------------ Q / K producer
+    if (lane == 0) {
+      int g = 0, j = 0;  // key tiles, items with keys
+      int last_k[KST], last_q = setup_issued ? 0 : -1;
+      for (int s = 0; s < KST; ++s) last_k[s] = (setup_issued && s == 0) ? 0 : -1;
+      bool ok = true;
+      for (int k = 0, w = item_w(0); ok && w < a.n_items; w = item_w(++k)) {
+        const Item it = item(w);
+        if (it.n == 0) continue;
+        for (int t = 0; t < it.n; ++t, ++g) {
+          if (k == 0 && t == 0) continue;  // issued with the setup
+          const int ks = g % KST;
+          if (!(ok = wait(&bar_kempty[ks], ((g / KST) & 1) ^ 1))) break;
+          issue_k_load<C>(smem, g, it.t_lo + t, it.bg, &tmK, &tmKlo, bar_kfull);
+          last_k[ks] = g / KST;
+          if (t == 0) {
+            // the item's Q tiles, each once the previous item's last S MMA on it completed
+            for (int q = 0; ok && q < NQ; ++q) {
+              if (j > 0 && !(ok = wait(&bar_qfree[q], (j - 1) & 1))) break;
+              mbar_arrive_expect_tx(&bar_q[q], C::NSPLIT * C::TILE_BYTES);
+              for (int sp = 0; sp < C::NSPLIT; ++sp)
+                for (int cb = 0; cb < C::NCB; ++cb)
+                  tma_load_3d(smem + C::Q_OFF + (q * C::NSPLIT + sp) * C::TILE_BYTES + cb * C::CB_BYTES,
+                              sp ? &tmQlo : &tmQ, &bar_q[q], cb * C::ROW_ELEMS, it.row0 + q * BLOCK_M,
+                              it.bh);
+            }
+            if (!ok) break;
+            last_q = j;
+          }
+        }
+        ++j;
       }
       // Drain: every issued copy must land before the CTA may exit.
-      for (int s = 0; s < C::KST; ++s)
-        if (last_k[s] >= 0) {
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(&bar_kfull[s], last_k[s] & 1) && globaltimer() - t0 < a.limit_ns) {}
+      for (int s = 0; s < KST; ++s)
+        if (last_k[s] >= 0) drain(&bar_kfull[s], last_k[s] & 1);
+      if (last_q >= 0)
+        for (int q = 0; q < NQ; ++q) drain(&bar_q[q], last_q & 1);
+    }
+  } else if (warp == C::V_WARP) {
+    // ------------------------------------------------------------ V producer
+    // Every use of a V stage -- a key tile, or the staging area of an item's
+    // epilogue -- has a ring position (per item: its key tiles, then one for the
+    // epilogue) and is released once (by the MMAs' commit, or by the last query
+    // tile's epilogue once its TMA stores have read the stage). This thread starts
+    // every use in position order and is the only waiter on the empty barriers, so
+    // it sees every release of a stage in order (seen[] counts them) and no parity
+    // wait can skip a phase. Key tiles complete on the full barriers (only loads
+    // count there); the epilogue stage goes to query tile 0 on its grant barrier (one
+    // phase per item, only after the previous epilogue stage was released), and tile
+    // q hands it to tile q + 1 on the next grant barrier once its stores have read it.
+    if (lane == 0) {
+      uint32_t pos = 0;
+      int seen[VST], loads[VST];  // releases seen, copies issued, per stage
+      for (int s = 0; s < VST; ++s) { seen[s] = 0; loads[s] = (setup_issued && s == 0) ? 1 : 0; }
+      int prev_stage = -1;
+      bool ok = true;
+      // wait until the use at position p has been released
+      auto wait_release = [&](uint32_t p) {
+        const int s = p % VST, u = p / VST;
+        if (seen[s] > u) return true;
+        if (!wait(&bar_vempty[s], u & 1)) return false;
+        seen[s] = u + 1;
+        return true;
+      };
+      for (int k = 0, w = item_w(0); ok && w < a.n_items; w = item_w(++k)) {
+        const Item it = item(w);
+        for (int t = 0; t < it.n; ++t, ++pos) {
+          if (k == 0 && t == 0) continue;  // issued with the setup
+          if (pos >= (uint32_t)VST && !(ok = wait_release(pos - VST))) break;
+          issue_v_load<C>(smem, (int)pos, it.t_lo + t, it.bg, &tmV, &tmVlo, bar_vfull);
+          ++loads[pos % VST];
         }
-      for (int s = 0; s < C::VST; ++s)
-        if (last_v[s] >= 0) {
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(&bar_vfull[s], last_v[s] & 1) && globaltimer() - t0 < a.limit_ns) {}
-        }
-      for (int q = 0; q < C::NQ; ++q) {
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(&bar_q[q], 0) && globaltimer() - t0 < a.limit_ns) {}
+        if (!ok) break;
+        if (pos >= (uint32_t)VST && !(ok = wait_release(pos - VST))) break;
+        if (prev_stage >= 0 && !(ok = wait_release((uint32_t)prev_stage))) break;
+        mbar_arrive(&bar_grant[0]);
+        prev_stage = (int)pos;
+        ++pos;
       }
+      // Drain: every issued copy must land before the CTA may exit.
+      for (int s = 0; s < VST; ++s)
+        if (loads[s] > 0) drain(&bar_vfull[s], (loads[s] - 1) & 1);
     }
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    // One warp issues every MMA (lane 0), in a fixed order per key tile j:
-    //   O_0 += P_0 V_j, S_0 = Q_0 K_{j+1}^T, O_1 += P_1 V_j, S_1 = Q_1 K_{j+1}^T.
-    // The tensor pipe runs them in that order, so S_0(j+1) completes one burst
-    // before S_1(j+1): tile 0's softmax runs while tile 1's MMAs execute and vice
-    // versa. (With one issuer per tile the two streams interleave in the pipe, both
-    // S tiles complete together and both softmaxes compete for the exponential
-    // units.) Inside the loop the issuer waits only on named barriers -- "P_q
-    // written" (1 + q, from the softmax) and "V_j, K_{j+1} loaded" (RELAY_BAR, from
-    // the relay warp): an mbarrier wait right after a burst of MMAs returns only once
-    // the burst has drained, which would idle the pipe between bursts. P_q aliases
-    // S_q in TMEM; a thread's MMAs run in issue order, so S_q(j+1) after
-    // O_q += P_q V_j is safe.
-    if (n > 0) {
-      const bool leader = lane == 0;
-      bool ok = __all_sync(0xffffffffu, wait(&bar_kfull[0], 0));
-      for (int q = 0; q < C::NQ; ++q) {
-        ok = ok && __all_sync(0xffffffffu, wait(&bar_q[q], 0));
+    // One warp issues every MMA (lane 0): per item S_0 = Q_0 K_0^T, S_1 = Q_1 K_0^T,
+    // then in a fixed order per key tile g:
+    //   O_0 += P_0 V_g, S_0 = Q_0 K_{g+1}^T, O_1 += P_1 V_g, S_1 = Q_1 K_{g+1}^T
+    // (no S after the item's last tile; the next item's first S tiles follow its last
+    // PVs in the pipe). The
+    // tensor pipe runs them in that order, so S_0(g+1) completes one burst before
+    // S_1(g+1): tile 0's softmax runs while tile 1's MMAs execute and vice versa.
+    // (With one issuer per tile the two streams interleave in the pipe, both S tiles
+    // complete together and both softmaxes compete for the exponential units.)
+    // Inside the loop the issuer waits only on named barriers -- "P_q written"
+    // (1 + q, from the softmax) and "operands loaded" (RELAY_BAR, from the relay
+    // warp): an mbarrier wait right after a burst of MMAs returns only once the
+    // burst has drained, which would idle the pipe between bursts. P_q aliases S_q
+    // in TMEM; a thread's MMAs run in issue order, so S_q(g+1) after O_q += P_q V_g
+    // is safe, and the next item's first O_q = P_q V (no accumulate) is issued only
+    // after its softmax has read the previous O_q out of TMEM.
+    const bool leader = lane == 0;
+    int g = 0, j = 0;
+    uint32_t pos = 0;
+    for (int k = 0, w = item_w(0); w < a.n_items; w = item_w(++k)) {
+      const int n = item(w).n;
+      if (n == 0) { pos += 1; continue; }
+      // item start: S_q(0) on the item's Q tiles and first K tile, once the relay has
+      // seen them land (after the previous item's last PVs in the pipe)
+      const int k0 = g % KST;
+      for (int q = 0; q < NQ; ++q) {
+        named_bar_sync(C::RELAY_BAR, 64);
         tc_fence_after();
-        if (ok && leader) {
-          issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(0, 0),
-                      sK(0, C::NSPLIT - 1));
+        if (leader) {
+          issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(k0, 0), sK(k0, C::NSPLIT - 1));
           tc_commit(&bar_s[q]);
+          if (n == 1) tc_commit(&bar_qfree[q]);
         }
         __syncwarp();
       }
-      if (ok && leader) tc_commit(&bar_kempty[0]);
+      if (leader) tc_commit(&bar_kempty[k0]);
       __syncwarp();
       // Every role takes part in every round of the named barriers, in order, whatever
-      // happens: the issuer runs all n rounds (issuing nothing once a wait failed),
-      // the relay syncs each round, and a softmax warpgroup that gave up syncs (not
-      // merely arrives) for its remaining rounds. A named barrier counts arrivals, so
-      // a role that arrived for two rounds before its partner synced once would
-      // complete a round without that partner and leave it waiting forever; in the
-      // normal flow the softmax cannot run a round ahead (P_q(j+1) needs S_q(j+1),
-      // issued only after the issuer passed round j).
-      for (int it = 0; it < n; ++it) {
-        const int vs = it % C::VST, ks = (it + 1) % C::KST;
-        const bool more = it + 1 < n;
-        named_bar_sync(C::RELAY_BAR, 64);  // V_it (and K_{it+1}) are in smem
-        for (int q = 0; q < C::NQ; ++q) {
-          named_bar_sync(1 + q, 128 + 32);  // P_q(it) is in TMEM
+      // happens: the issuer runs all rounds (it has no wait of its own that could
+      // fail; after an abort its MMAs compute garbage that nobody stores), the relay
+      // syncs each round, and a softmax warpgroup that gave up syncs (not merely
+      // arrives) for its remaining rounds. A named barrier counts arrivals, so a role
+      // that arrived for two rounds before its partner synced once would complete a
+      // round without that partner and leave it waiting forever; in the normal flow
+      // the softmax cannot run a round ahead (P_q(g+1) needs S_q(g+1), issued only
+      // after the issuer passed round g).
+      for (int t = 0; t < n; ++t, ++g, ++pos) {
+        const int vs = pos % VST, ks = (g + 1) % KST;
+        const bool more = t + 1 < n;
+        named_bar_sync(C::RELAY_BAR, 64);  // V_g (and K_{g+1}) are in smem
+        for (int q = 0; q < NQ; ++q) {
+          named_bar_sync(1 + q, 128 + 32);  // P_q(g) is in TMEM
           tc_fence_after();
-          if (ok && leader) {
+          if (leader) {
             issue_pv<C>(tmem + C::o_col(q), tmem + C::s_col(q), tmem + C::PLO_COL, sV(vs, 0),
-                        sV(vs, C::NSPLIT - 1), it > 0);
+                        sV(vs, C::NSPLIT - 1), t > 0);
             if (more) {
               issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(ks, 0),
                           sK(ks, C::NSPLIT - 1));
               tc_commit(&bar_s[q]);
+              if (t + 2 == n) tc_commit(&bar_qfree[q]);  // that was the item's last S_q
             } else {
               tc_commit(&bar_o[q]);  // tile q's last MMA: its epilogue may start
             }
           }
           __syncwarp();
         }
-        if (ok && leader) {
+        if (leader) {
           tc_commit(&bar_vempty[vs]);
           if (more) tc_commit(&bar_kempty[ks]);
         }
         __syncwarp();
       }
-      if (leader) {
-        // Drain: no MMA may still be running when TMEM is released.
-        tc_commit(&bar_drain[0]);
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(&bar_drain[0], 0) && globaltimer() - t0 < a.limit_ns) {}
-      }
-      __syncwarp();
+      pos += 1;  // the epilogue's staging position
+      ++j;
     }
+    if (j > 0 && leader) {
+      // Drain: no MMA may still be running when TMEM is released.
+      tc_commit(&bar_drain);
+      drain(&bar_drain, 0);
+    }
+    __syncwarp();
   } else if (warp == C::RELAY_WARP) {
     // ------------------------------------------------------------ load relay
-    // Waits (on mbarriers, which this warp can do without stalling any MMA) until V_j
-    // and K_{j+1} have landed and passes that on to the issuer through RELAY_BAR, one
-    // sync per round (never a bare arrive: see the issuer), also after an abort.
-    if (n > 0) {
-      bool ok = true;
-      for (int it = 0; it < n; ++it) {
+    // Waits (on mbarriers, which this warp can do without stalling any MMA) until the
+    // operands of the issuer's next bursts have landed and passes that on through
+    // RELAY_BAR, the same number of syncs as the issuer (never a bare arrive: see the
+    // issuer), also after an abort. It observes every phase of the full barriers in
+    // order: per item Q_q and the first K tile, then K_{g+1} and V_g per key tile (the
+    // V barriers count loads only, vc[] per stage); the issuer releases a K stage only
+    // after its relay round, so no K phase can pass unobserved.
+    bool ok = true;
+    int g = 0, j = 0;
+    uint32_t pos = 0;
+    int vc[VST];
+    for (int s = 0; s < VST; ++s) vc[s] = 0;
+    for (int k = 0, w = item_w(0); w < a.n_items; w = item_w(++k)) {
+      const int n = item(w).n;
+      if (n == 0) { pos += 1; continue; }
+      for (int q = 0; q < NQ; ++q) {  // item start: Q_q (and the first K tile)
         if (ok)
-          ok = __all_sync(0xffffffffu,
-                          wait(&bar_vfull[it % C::VST], (it / C::VST) & 1) &&
-                              (it + 1 >= n || wait(&bar_kfull[(it + 1) % C::KST], ((it + 1) / C::KST) & 1)));
+          ok = __all_sync(0xffffffffu, wait(&bar_q[q], j & 1) &&
+                                           (q > 0 || wait(&bar_kfull[g % KST], (g / KST) & 1)));
         named_bar_sync(C::RELAY_BAR, 64);
       }
+      for (int t = 0; t < n; ++t, ++g, ++pos) {
+        const bool more = t + 1 < n;
+        const int vs = pos % VST;
+        if (ok)
+          ok = __all_sync(0xffffffffu,
+                          wait(&bar_vfull[vs], vc[vs] & 1) &&
+                              (!more || wait(&bar_kfull[(g + 1) % KST], ((g + 1) / KST) & 1)));
+        ++vc[vs];
+        named_bar_sync(C::RELAY_BAR, 64);
+      }
+      pos += 1;
+      ++j;
     }
   }  // idle warps of the control warpgroup fall through
   } else {
     // ------------------------------------------------------------ softmax / epilogue
-    if constexpr (C::NQ == 2) regs_increase<C::REGS_SOFTMAX>();
+    if constexpr (NQ == 2) regs_increase<C::REGS_SOFTMAX>();
     const int q = warp / 4;
     const int wq = warp % 4;
     const int r_in = wq * 32 + lane;
-    const int r0 = row0 + q * BLOCK_M;
-    const int i = r0 + r_in;  // this thread's query row
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const uint32_t s_addr = lane_addr + C::s_col(q);
     const uint32_t o_addr = lane_addr + C::o_col(q);
     const float sl2 = a.scale_log2;
-    // visible keys of row i: [lo_i, hi_i]
-    const int hi_i = a.causal ? min(i, a.Sk - 1) : a.Sk - 1;
-    const int lo_i = a.window > 0 ? i - a.window + 1 : INT_MIN / 2;
-    float m = -FLT_MAX;  // running max of scale*log2(e)*S, possibly stale by < threshold
-    float l = 0.f;
     bool ok = true;
-    for (int it = 0; it < n; ++it) {
-      const int t = t_lo + it;
-      ok = __all_sync(0xffffffffu, wait(&bar_s[q], it & 1));
-      if (!ok) {
-        // The issuer takes one round of named barrier 1 + q per key tile: join the
-        // remaining rounds one by one (sync, not arrive) so that it can run out.
-        for (int r = it; r < n; ++r) named_bar_sync(1 + q, 128 + 32);
-        break;
-      }
-      tc_fence_after();
-      float s[128];
-      {
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32x4(s_addr, s_addr + 32, s_addr + 64, s_addr + 96, r0, r1, r2, r3);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          s[k] = __uint_as_float(r0[k]);
-          s[32 + k] = __uint_as_float(r1[k]);
-          s[64 + k] = __uint_as_float(r2[k]);
-          s[96 + k] = __uint_as_float(r3[k]);
+    int g = 0, j = 0;
+    uint32_t pos = 0;
+    // The last tile's epilogue gives the stage back to the V ring once its TMA stores
+    // have read it: checked after this warpgroup's next hand-off, so the wait for the
+    // stores does not delay the next P.
+    bool pending = false;
+    int pend_slot = 0;
+    auto release = [&]() {
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+      named_bar_sync(C::EPI_BAR0 + q, 128);
+      if (wq == 0 && lane == 0) mbar_arrive(&bar_vempty[pend_slot]);
+      pending = false;
+    };
+    for (int k = 0, w = item_w(0); w < a.n_items; w = item_w(++k)) {
+      const Item itm = item(w);
+      const int n = itm.n;
+      const int r0 = itm.row0 + q * BLOCK_M;
+      const int i = r0 + r_in;  // this thread's query row
+      // visible keys of row i: [lo_i, hi_i]
+      const int hi_i = a.causal ? min(i, a.Sk - 1) : a.Sk - 1;
+      const int lo_i = a.window > 0 ? i - a.window + 1 : INT_MIN / 2;
+      float m = -FLT_MAX;  // running max of scale*log2(e)*S, possibly stale by < threshold
+      float l = 0.f;
+      for (int t = 0; t < n; ++t, ++g) {
+        if (ok) ok = __all_sync(0xffffffffu, wait(&bar_s[q], g & 1));
+        if (!ok) {
+          // The issuer takes one round of named barrier 1 + q per key tile: join the
+          // remaining rounds one by one (sync, not arrive) so that it can run out.
+          named_bar_sync(1 + q, 128 + 32);
+          if (pending) release();
+          continue;
         }
-      }
-      const int c0 = t * BLOCK_N;
-      if (tile_needs_mask(r0, r0 + BLOCK_M - 1, c0, c0 + BLOCK_N - 1, a.Sk, a.causal, a.window)) {
-        const int rel_hi = hi_i - c0, rel_lo = lo_i - c0;
+        tc_fence_after();
+        float s[128];
+        {
+          uint32_t v0[32], v1[32], v2[32], v3[32];
+          tmem_ld32x4(s_addr, s_addr + 32, s_addr + 64, s_addr + 96, v0, v1, v2, v3);
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > rel_hi || c < rel_lo) s[c] = -INFINITY;
-      }
-      // row max: eight chains of three-input maxima
-      float mx[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = max3(s[k], s[8 + k], s[16 + k]);
-#pragma unroll
-      for (int c = 24; c < 120; c += 16)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = max3(mx[k], s[c + k], s[c + 8 + k]);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], s[120 + k]);
-      const float mt =
-          max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
-      const bool need = mt > m + RESCALE_THRESHOLD;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = fmaxf(m, mt);
-        const float corr = ex2(m - m_new);
-        l *= corr;
-        if (it > 0) {
-#pragma unroll
-          for (int c = 0; c < C::D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(o_addr + c * 32, r);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * corr);
-            tmem_st32(o_addr + c * 32, r);
+          for (int kk = 0; kk < 32; ++kk) {
+            s[kk] = __uint_as_float(v0[kk]);
+            s[32 + kk] = __uint_as_float(v1[kk]);
+            s[64 + kk] = __uint_as_float(v2[kk]);
+            s[96 + kk] = __uint_as_float(v3[kk]);
           }
         }
-        m = m_new;
-      }
-      const float nm = -m;
-      float l0 = 0.f, l1 = 0.f;
-      if constexpr (!C::F32) {
-        // exponent arguments and the row sum on packed pairs
-        const float2 sl2x2 = make_float2(sl2, sl2), nmx2 = make_float2(nm, nm);
-        float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const int c0 = (itm.t_lo + t) * BLOCK_N;
+        if (tile_needs_mask(r0, r0 + BLOCK_M - 1, c0, c0 + BLOCK_N - 1, a.Sk, a.causal, a.window)) {
+          const int rel_hi = hi_i - c0, rel_lo = lo_i - c0;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float2 x = fma2(make_float2(s[c * 64 + 2 * k], s[c * 64 + 2 * k + 1]), sl2x2, nmx2);
-            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-            ls[k & 1] = add2(ls[k & 1], pp);
-            pk[k] = pack_half2(pp.x, pp.y);
-          }
-          tmem_st32(s_addr + c * 32, pk);
+          for (int c = 0; c < 128; ++c)
+            if (c > rel_hi || c < rel_lo) s[c] = -INFINITY;
         }
-        l0 = ls[0].x + ls[1].x;
-        l1 = ls[0].y + ls[1].y;
-      } else {
+        // row max: eight chains of three-input maxima
+        float mx[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t ph[32], pl[32];
+        for (int kk = 0; kk < 8; ++kk) mx[kk] = max3(s[kk], s[8 + kk], s[16 + kk]);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float p = ex2(fmaf(s[c * 32 + k], sl2, nm));
-            if (k & 1) l1 += p; else l0 += p;
-            const uint32_t hb = __float_as_uint(p) & 0xFFFFE000u;
-            ph[k] = hb;
-            pl[k] = __float_as_uint(p - __uint_as_float(hb));
+        for (int c = 24; c < 120; c += 16)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mx[kk] = max3(mx[kk], s[c + kk], s[c + 8 + kk]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mx[kk] = fmaxf(mx[kk], s[120 + kk]);
+        const float mt =
+            max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
+        const bool need = mt > m + RESCALE_THRESHOLD;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = fmaxf(m, mt);
+          const float corr = ex2(m - m_new);
+          l *= corr;
+          if (t > 0) {
+#pragma unroll
+            for (int c = 0; c < C::D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(o_addr + c * 32, r);
+#pragma unroll
+              for (int kk = 0; kk < 32; ++kk) r[kk] = __float_as_uint(__uint_as_float(r[kk]) * corr);
+              tmem_st32(o_addr + c * 32, r);
+            }
           }
-          tmem_st32(s_addr + c * 32, ph);
-          tmem_st32(lane_addr + C::PLO_COL + c * 32, pl);
+          m = m_new;
         }
+        const float nm = -m;
+        float l0 = 0.f, l1 = 0.f;
+        if constexpr (!C::F32) {
+          // exponent arguments and the row sum on packed pairs
+          const float2 sl2x2 = make_float2(sl2, sl2), nmx2 = make_float2(nm, nm);
+          float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int kk = 0; kk < 32; ++kk) {
+              const float2 x = fma2(make_float2(s[c * 64 + 2 * kk], s[c * 64 + 2 * kk + 1]), sl2x2, nmx2);
+              const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+              ls[kk & 1] = add2(ls[kk & 1], pp);
+              pk[kk] = pack_half2(pp.x, pp.y);
+            }
+            tmem_st32(s_addr + c * 32, pk);
+          }
+          l0 = ls[0].x + ls[1].x;
+          l1 = ls[0].y + ls[1].y;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ph[32], pl[32];
+#pragma unroll
+            for (int kk = 0; kk < 32; ++kk) {
+              const float p = ex2(fmaf(s[c * 32 + kk], sl2, nm));
+              if (kk & 1) l1 += p; else l0 += p;
+              const uint32_t hb = __float_as_uint(p) & 0xFFFFE000u;
+              ph[kk] = hb;
+              pl[kk] = __float_as_uint(p - __uint_as_float(hb));
+            }
+            tmem_st32(s_addr + c * 32, ph);
+            tmem_st32(lane_addr + C::PLO_COL + c * 32, pl);
+          }
+        }
+        l += l0 + l1;
+        tmem_st_wait();
+        tc_fence_before();
+        named_bar_arrive(1 + q, 128 + 32);
+        if (pending) release();
       }
-      l += l0 + l1;
-      tmem_st_wait();
-      tc_fence_before();
-      named_bar_arrive(1 + q, 128 + 32);
-    }
-    if (ok && n > 0) {
-      ok = __all_sync(0xffffffffu, wait(&bar_o[q], 0));
-      tc_fence_after();
-    }
-    if (ok) {
+      pos += n;
+      if (n > 0) {
+        if (ok) ok = __all_sync(0xffffffffu, wait(&bar_o[q], j & 1));
+        tc_fence_after();
+        ++j;
+      }
+      if (pending) release();
+      // ---- epilogue: LSE, and O = acc / l staged in the item's V ring stage (tile 0
+      // gets it from the V producer, tile q + 1 from tile q once q's stores have read
+      // it), TMA stores.
+      const int slot = pos % VST;
+      if (ok) ok = __all_sync(0xffffffffu, wait(&bar_grant[q], k & 1));
       const float inv = (l > 0.f) ? (1.f / l) : 0.f;
-      if (i < a.Sq) a.LSE[(size_t)bh * a.Sq + i] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
-      // The tile's last MMA has completed (bar_o), so nothing reads Q_q any more. The
-      // last tile's bar_o follows every MMA of the CTA, so it may also stage in the
-      // (spent) K ring and write all its boxes in one round.
+      if (ok && i < a.Sq)
+        a.LSE[(size_t)itm.bh * a.Sq + i] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
       const int r_base = r0 + wq * 32;
-      if (q == C::NQ - 1 && C::NQ > 1) {
-        const uint32_t stage = sbase + C::K_OFF + wq * C::LAST_STAGE_PER_WARP;
-        if (a.out_bf16)
-          store_rows_tma<D, true, C::LAST_STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                        r_base < a.Sq, bh);
-        else
-          store_rows_tma<D, false, C::LAST_STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                         r_base < a.Sq, bh);
+      const uint32_t stage = sV(slot, 0) + wq * C::STAGE_PER_WARP;
+      if (q < NQ - 1) {
+        if (ok) {
+          if (a.out_bf16)
+            store_rows_tma<D, true, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
+                                                     r_base < a.Sq, itm.bh);
+          else
+            store_rows_tma<D, false, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
+                                                      r_base < a.Sq, itm.bh);
+        }
+        named_bar_sync(C::EPI_BAR0 + q, 128);
+        if (wq == 0 && lane == 0) mbar_arrive(&bar_grant[q + 1]);
       } else {
-        const uint32_t stage = sQ(q, 0) + wq * C::STAGE_PER_WARP;
-        if (a.out_bf16)
-          store_rows_tma<D, true, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                   r_base < a.Sq, bh);
-        else
-          store_rows_tma<D, false, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                    r_base < a.Sq, bh);
+        if (ok) {
+          if (a.out_bf16)
+            store_rows_tma<D, true, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage, r_base,
+                                                            r_base < a.Sq, itm.bh);
+          else
+            store_rows_tma<D, false, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage,
+                                                             r_base, r_base < a.Sq, itm.bh);
+        }
+        pending = true;
+        pend_slot = slot;
       }
+      pos += 1;
     }
+    if (pending) release();
   }
 
   tc_fence_before();
@@ -623,14 +772,15 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   a.window = p.window;
   a.out_bf16 = p.out_dtype == FA_BF16;
   a.n_qgroups = (p.Sq + BLOCK_M * C::NQ - 1) / (BLOCK_M * C::NQ);
+  a.n_items = (int)BHq * a.n_qgroups;
   a.lpt = p.causal ? 1 : 0;
   a.BH = (int)BHq;
   a.limit_ns = WAIT_LIMIT_NS;
+  const unsigned grid = (unsigned)std::min(a.n_items, host::sm_count());
   auto kern = fa_fwd_kernel<D, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_ALLOC);
   if (e == cudaSuccess) {
-    const unsigned grid = (unsigned)(BHq * a.n_qgroups);
     host::KernelTimer kt(F32 ? "fa_fwd_kernel<64,f32>"
                              : (D == 128 ? "fa_fwd_kernel<128,bf16>" : "fa_fwd_kernel<64,bf16>"),
                          stream);
@@ -826,15 +976,16 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
   a.window = p.window;
   a.out_bf16 = p.out_dtype == FA_BF16;
   a.n_qgroups = (p.Sq + BLOCK_M * C::NQ - 1) / (BLOCK_M * C::NQ);
+  a.n_items = (int)BHq * a.n_qgroups;
   a.lpt = p.causal ? 1 : 0;
   a.BH = (int)BHq;
   a.limit_ns = WAIT_LIMIT_NS;
+  const unsigned grid = (unsigned)std::min(a.n_items, host::sm_count());
   auto kern = fa_fwd_kernel<D, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_ALLOC);
   if (e != cudaSuccess) return FA_ERR_CUDA;
-  kern<<<(unsigned)(BHq * a.n_qgroups), C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo,
-                                                                            mV, mVlo, mO, a);
+  kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, mO, a);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -32,6 +32,12 @@ SMALL = {
     "f32-noncausal": C5.with_(Sq=700, Sk=700, seed=19),
     "f32-gqa-window": C2.with_(B=1, H=4, HKV=2, Sq=450, Sk=450, window=100, seed=20),
     "f32-empty-rows": C2.with_(B=1, H=2, HKV=2, Sq=400, Sk=150, window=40, seed=23),
+    # more work items than SMs: every persistent CTA runs several items, of mixed
+    # lengths, some with one key tile and some with none
+    "bf16-many-items-causal": C3.with_(B=1, H=96, HKV=24, Sq=700, Sk=700, seed=24),
+    "bf16-many-items-empty": C3.with_(B=1, H=160, HKV=40, Sq=800, Sk=200, window=64, seed=25),
+    "f32-many-items-causal": C2.with_(B=1, H=64, HKV=16, Sq=500, Sk=500, seed=26),
+    "f32-many-items-empty": C2.with_(B=1, H=64, HKV=16, Sq=600, Sk=150, window=40, seed=27),
 }
 
 
