@@ -47,6 +47,7 @@ struct BwdArgs {
   int n_tiles;  // key tiles (dkdv) / query tiles (dq) per head
   int BHx;      // B*HKV (dkdv) / B*H (dq)
   int lpt;
+  int* sched;  // dq (bf16 inputs): work-item counter, zero at launch
   unsigned long long limit_ns;
 };
 
@@ -685,6 +686,9 @@ struct Dq16Cfg {
   static constexpr int SOFTMAX_WARPS = 8;
   static constexpr int MMA_WARP = 8, ACC_WARP = 9, TMA_WARP = 10, DP_WARP = 11;
   static constexpr int THREADS = 384;
+  // work-item hand-out ring: the producer writes, the three issuers and the eight
+  // softmax warps read every entry
+  static constexpr int IRING = 4, ITEM_READERS = 3 + SOFTMAX_WARPS;
   static constexpr uint32_t REGS_SOFTMAX = 200, REGS_CONTROL = 96;
   static_assert(256 * REGS_SOFTMAX + 128 * REGS_CONTROL <= 384 * 168, "register split");
   static constexpr uint32_t TMEM_COLS = 512;
@@ -748,10 +752,13 @@ __device__ __forceinline__ void stage_store_rows(const uint32_t (&r)[NCOL], floa
   }
 }
 
-// Persistent: one CTA per SM walks the (batch, head, query tile) work items, heaviest
-// causal tiles first, in rounds of gridDim.x items taken in alternating directions.
-// Every ring and hand-off barrier counts chunks across items (g), so the K / V ring
-// streams the next item's first chunks while the current item's epilogue runs. Per item with keys (counted by j): Q_{j+1} (dO_{j+1}) is
+// Persistent: one CTA per SM walks (batch, head, query tile) work items, heaviest
+// causal tiles first: its first item is blockIdx.x, the next ones come from a global
+// counter (a CTA that starts late, e.g. while another kernel still holds SMs, takes
+// fewer items). The TMA producer fetches them, one item ahead, and hands them to the
+// other roles through a small shared ring. Every ring and hand-off barrier counts
+// chunks across items (g), so the K / V ring streams the next item's first chunks
+// while the current item's epilogue runs. Per item with keys (counted by j): Q_{j+1} (dO_{j+1}) is
 // loaded as soon as the last S (dP) MMA of item j has completed (q_rel / do_rel),
 // the epilogue stages dQ in the V ring, so item j+1's first V chunk waits until the
 // epilogue has read that staging area (v_free), and the first dQ MMA of item j+1
@@ -771,7 +778,9 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_q, bar_do, bar_kfull[KST], bar_kempty[KST], bar_vfull[VST],
       bar_vempty[VST], bar_s, bar_dp, bar_sfree, bar_dpfree, bar_ds[2], bar_accdone[2], bar_done,
-      bar_dqfree, bar_qrel, bar_dorel, bar_vfree, bar_drain[3];
+      bar_dqfree, bar_qrel, bar_dorel, bar_vfree, bar_drain[3], bar_ifull[C::IRING],
+      bar_iempty[C::IRING];
+  __shared__ int ring_w_sh[C::IRING];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int warp = warp_id(), lane = lane_id();
@@ -792,14 +801,9 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     it.nc = hi - it.kt_lo;
     return it;
   };
-  // The k-th item of this CTA: rounds of gridDim.x items, walked in alternating
-  // directions (CTA c takes item c of even rounds and item G-1-c of odd ones), so
-  // with the heaviest items first every CTA's total stays close to the mean. A round
-  // that has no item for this CTA is the last round.
-  auto item_w = [&](int k) {
-    const int G = gridDim.x, c = blockIdx.x;
-    return k * G + ((k & 1) ? G - 1 - c : c);
-  };
+  // work-item hand-out (see above): entry k of the ring holds this CTA's k-th item
+  // (n_items or more: no further item)
+  volatile int* ring_w = ring_w_sh;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
@@ -820,6 +824,10 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     mbar_init(&bar_dorel, 1);
     mbar_init(&bar_vfree, 256);
     for (int s = 0; s < 3; ++s) mbar_init(&bar_drain[s], 1);
+    for (int s = 0; s < C::IRING; ++s) {
+      mbar_init(&bar_ifull[s], 1);
+      mbar_init(&bar_iempty[s], C::ITEM_READERS);
+    }
     abort_sh = 0;
     fence_mbar_init();
     if ((int)blockIdx.x < n_items && item(blockIdx.x).nc > 0) {
@@ -854,6 +862,23 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
   auto gen = [&](uint32_t s) { return smem + (s - sbase); };
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
+  };
+  // Reader side of the item ring: entry k, then release the entry (one arrival per
+  // reading thread / warp). A failed wait reads as "no further item".
+  auto take_thread = [&](int k) {
+    const int s = k % C::IRING;
+    if (!wait(&bar_ifull[s], (k / C::IRING) & 1)) return INT_MAX;
+    const int w = ring_w[s];
+    mbar_arrive(&bar_iempty[s]);
+    return w;
+  };
+  auto take_warp = [&](int k) {
+    const int s = k % C::IRING;
+    if (!__all_sync(0xffffffffu, wait(&bar_ifull[s], (k / C::IRING) & 1))) return INT_MAX;
+    const int w = ring_w[s];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar_iempty[s]);
+    return w;
   };
 
   if (warp >= C::SOFTMAX_WARPS) {
@@ -894,9 +919,23 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         last_qd = j;
         return true;
       };
+      // Writer side of the item ring: entry k once every reader released entry k - IRING.
+      auto publish = [&](int k, int w) {
+        const int s = k % C::IRING;
+        if (!wait(&bar_iempty[s], ((k / C::IRING) & 1) ^ 1)) return false;
+        ring_w[s] = w;
+        mbar_arrive(&bar_ifull[s]);
+        return true;
+      };
+      const int G = (int)gridDim.x;
+      int w = blockIdx.x;  // the first item is fixed; the next is fetched one item early
+      int w_next = n_items > G ? G + atomicAdd(a.sched, 1) : n_items;
       bool ok = true;
-      for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
+      for (int k = 0; ok; ++k) {
+        if (!(ok = publish(k, w)) || w >= n_items) break;
         const Item it = item(w);
+        w = w_next;
+        if (w_next < n_items) w_next = G + atomicAdd(a.sched, 1);
         if (it.nc == 0) continue;
         const bool pre = j == 0 && setup_issued;  // Q / dO and chunk 0 came with the setup
         for (int c = 0; c < it.nc; ++c, ++g) {
@@ -930,7 +969,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     if (lane == 0) {
       bool ok = true;
       int g = 0, j = 0;  // chunks and items with keys so far
-      for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
+      for (int k = 0, w = take_thread(0); ok && w < n_items; w = take_thread(++k)) {
         const Item it = item(w);
         if (it.nc == 0) continue;
         if (!(ok = wait(is_s ? &bar_q : &bar_do, j & 1))) break;  // S needs Q, dP needs dO
@@ -966,7 +1005,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
       constexpr uint32_t id = make_idesc(128, D, FMT_F16, FMT_F16, false, true);
       bool ok = true;
       int g = 0, j = 0;  // chunks and items with keys so far
-      for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
+      for (int k = 0, w = take_thread(0); ok && w < n_items; w = take_thread(++k)) {
         const Item it = item(w);
         if (it.nc == 0) continue;
         for (int c = 0; c < it.nc; ++c, ++g) {
@@ -996,7 +1035,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     const float sl2 = a.scale_log2;
     bool ok = true;
     int g = 0, j = 0;  // chunks and items with keys so far
-    for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
+    for (int k = 0, w = take_warp(0); ok && w < n_items; w = take_warp(++k)) {
       const Item it = item(w);
       const int i = it.i0 + wq * 32 + lane;
       if (it.nc == 0) {
@@ -1131,6 +1170,9 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // Launched as a programmatic dependent of the dK / dV grid: this grid completes
+  // only after that one has (nothing above reads its results).
+  grid_dependency_wait();
 }
 
 // ------------------------------------------------------ dK / dV, fp16 operands
@@ -1220,6 +1262,9 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     fa_bwd_dkdv16_kernel(const __grid_constant__ KVMaps m, const BwdArgs a) {
   using C = Dkv16Cfg<D>;
   constexpr int NS = C::NS;
+  // The dQ grid launched after this one reads nothing this grid writes: it may start
+  // as soon as every block of this grid has started (see the launcher).
+  grid_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -1614,8 +1659,9 @@ __global__ void bwd_prepass16_kernel(const __nv_bfloat16* __restrict__ dO, const
                                      __half* __restrict__ Q16, __half* __restrict__ K16,
                                      __half* __restrict__ V16, float* __restrict__ lse2,
                                      float* __restrict__ delta, int Sq, int ldq, size_t q_rows,
-                                     size_t kv_rows, int o_bf16) {
+                                     size_t kv_rows, int o_bf16, int* __restrict__ sched) {
   constexpr int TPR = D / 8;  // threads per row
+  if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;  // the dQ kernel's work-item counter
   const int t = threadIdx.x % TPR;
   const size_t rows_per_grid = (size_t)gridDim.x * (blockDim.x / TPR);
   auto cvt8 = [](uint4 v) {
@@ -1703,10 +1749,13 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   size_t bytes = 2 * nvec * 4;
   if constexpr (!F32) bytes += (2 * nq + 2 * nk) * 2;
   else bytes += (4 * nq + 4 * nk + 4 * nqt + 2 * nkt) * 4;  // Q,dO,K,V hi/lo + Q^T,dO^T,K^T hi/lo
+  const size_t sched_off = (bytes + 15) / 16 * 16;  // the dQ kernel's work-item counter
+  bytes = sched_off + 16;
   void* ws = nullptr;
   if (host::scratch_alloc(&ws, bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
   float* lse2 = static_cast<float*>(ws);
   float* delta = lse2 + nvec;
+  int* sched = reinterpret_cast<int*>(static_cast<char*>(ws) + sched_off);
   const int grid_pp = 4 * host::sm_count();
   const auto F32T = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   KVMaps mk;
@@ -1733,7 +1782,7 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       bwd_prepass16_kernel<D><<<8 * host::sm_count(), 256, 0, stream>>>(
           static_cast<const __nv_bfloat16*>(dO), O, LSE, static_cast<const __nv_bfloat16*>(Q),
           static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(V), do16, q16, k16,
-          v16, lse2, delta, p.Sq, ldq, nvec, BHk * p.Sk, p.out_dtype == FA_BF16);
+          v16, lse2, delta, p.Sq, ldq, nvec, BHk * p.Sk, p.out_dtype == FA_BF16, sched);
     }
     const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     enc &= host::encode_tiled_3d(&mk.K[0], F16, 2, k16, D, p.Sk, BHk, D, 64, 128);
@@ -1812,6 +1861,7 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   a.scale = p.scale; a.scale_log2 = p.scale * LOG2E;
   a.causal = p.causal; a.window = p.window; a.out_bf16 = p.out_dtype == FA_BF16;
   a.lpt = p.causal;
+  a.sched = sched;
   a.limit_ns = WAIT_LIMIT_NS;
   cudaError_t e = cudaSuccess;
   {
@@ -1862,11 +1912,26 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       if (e == cudaSuccess) {
         host::KernelTimer kt(D == 128 ? "fa_bwd_dq_kernel<128,bf16>" : "fa_bwd_dq_kernel<64,bf16>",
                              stream);
-        // persistent: one CTA per SM, each walking work items with the grid's stride
+        // Persistent: one CTA per SM (at most), work items handed out dynamically.
+        // Launched as a programmatic dependent of the dK / dV kernel (which does not
+        // write anything dQ reads): its blocks may start as soon as every dK / dV block
+        // has started, on the SMs that dK / dV's last wave leaves idle, and each waits
+        // for the dK / dV grid to complete before it exits, so the dQ grid's completion
+        // (which the rest of the stream waits for) implies dK / dV's.
         const size_t n_items = BH * (size_t)aq.n_tiles;
         const unsigned grid = (unsigned)std::min<size_t>(n_items, (size_t)host::sm_count());
-        kern<<<grid, C16::THREADS, C16::SMEM, stream>>>(mq, aq);
-        e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(C16::THREADS);
+        cfg.dynamicSmemBytes = C16::SMEM;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, mq, aq);
+        if (e == cudaSuccess) e = cudaGetLastError();
       }
     }
   }

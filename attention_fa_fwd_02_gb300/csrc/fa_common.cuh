@@ -83,12 +83,12 @@ cudaError_t scratch_free(void* p, cudaStream_t s);
 
 int sm_count();
 
-// Records a CUDA event pair around the launches made during its lifetime when
-// kernel timing is enabled (fa_timing_enable); otherwise does nothing.
 // Largest dynamic shared-memory size a block of `kernel` may request on the current
 // device (the per-block opt-in limit minus the kernel's static shared memory).
 cudaError_t max_dynamic_smem(const void* kernel, int* bytes);
 
+// Records a CUDA event pair around the launches made during its lifetime when
+// kernel timing is enabled (fa_timing_enable); otherwise does nothing.
 class KernelTimer {
  public:
   KernelTimer(const char* name, cudaStream_t s);

@@ -91,6 +91,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Programmatic dependent launch (sm_90 and later). launch_dependents: the grid
+// launched next on the stream with programmatic serialization may start once every
+// block of this grid has executed it (or exited). dependency_wait: block until the
+// grid this one depends on programmatically has completed and its memory writes are
+// visible (returns at once for a grid launched without that dependency).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Named CTA barrier `id` (1..15; 0 is __syncthreads) over `count` threads (a multiple
 // of 32): sync waits for the barrier, arrive only contributes to it.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {

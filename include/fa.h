@@ -141,7 +141,10 @@ FA_API fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, voi
  * the grouped query heads without atomics (deterministic: two calls on the same
  * inputs give bit-identical results). Workspace (D_i, fp16 / tf32-split operand
  * copies) is stream-ordered from the library pool. Same ownership, alignment and
- * error rules as fa_fwd.
+ * error rules as fa_fwd. For bf16 inputs the dQ kernel is launched on `stream` as
+ * a programmatic dependent of the dK/dV kernel: it starts on the SMs that dK/dV's
+ * last wave leaves idle and completes only after dK/dV has, so work enqueued on
+ * `stream` afterwards sees all three gradients.
  */
 FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                  const float* LSE, void* dQ, void* dK, void* dV, const fa_params* p,
