@@ -159,8 +159,11 @@ fa_status validate(const fa_params* p) {
   const long long bh = (long long)p->B * p->H;
   if (bh > (1ll << 30) || p->Sq > (1 << 30) || p->Sk > (1 << 30)) return FA_ERR_INVALID_ARG;
   if (bh * ((p->Sq + 255) / 256) > (1ll << 31) - 1) return FA_ERR_INVALID_ARG;
-  const bool ok_bf16 = p->in_dtype == FA_BF16 && (p->D == 64 || p->D == 128);
-  const bool ok_f32 = p->in_dtype == FA_F32 && p->D == 64;
+  // Head dims: multiples of 16 up to 128 (bf16) / 64 (fp32); each runs in the kernel
+  // built for the next of 64 / 128, with the missing columns read as zeros.
+  const bool d16 = p->D % 16 == 0 && p->D >= 16;
+  const bool ok_bf16 = p->in_dtype == FA_BF16 && d16 && p->D <= 128;
+  const bool ok_f32 = p->in_dtype == FA_F32 && d16 && p->D <= 64;
   if (!ok_bf16 && !ok_f32) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }

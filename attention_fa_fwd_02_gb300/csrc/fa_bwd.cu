@@ -47,6 +47,7 @@ struct BwdArgs {
   int n_tiles;  // key tiles (dkdv) / query tiles (dq) per head
   int BHx;      // B*HKV (dkdv) / B*H (dq)
   int lpt;
+  int Dv;      // head dim of the tensors (<= the kernel's D; missing columns read as 0)
   int* sched;  // dq (bf16 inputs): work-item counter, zero at launch
   unsigned long long limit_ns;
 };
@@ -444,14 +445,14 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       const bool any = r_base < a.Sk;
       if (a.out_bf16) {
         store_rows_tma<D, true, D / 64, false>(&m.dV, lane_addr + C::KV_ACC0, nc > 0, 1.f, st_v,
-                                               r_base, any, bg);
+                                               r_base, any, bg, 0, a.Dv);
         store_rows_tma<D, true, D / 64, false>(&m.dK, lane_addr + C::KV_ACC1, nc > 0, a.scale, st_k,
-                                               r_base, any, bg);
+                                               r_base, any, bg, 0, a.Dv);
       } else {
         store_rows_tma<D, false, D / 32, false>(&m.dV, lane_addr + C::KV_ACC0, nc > 0, 1.f, st_v,
-                                                r_base, any, bg);
+                                                r_base, any, bg, 0, a.Dv);
         store_rows_tma<D, false, D / 32, false>(&m.dK, lane_addr + C::KV_ACC1, nc > 0, a.scale, st_k,
-                                                r_base, any, bg);
+                                                r_base, any, bg, 0, a.Dv);
       }
       if (lane == 0) bulk_wait_read_all();
       __syncwarp();
@@ -649,10 +650,10 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       const int r_base = i0 + wq * 32;
       if (a.out_bf16)
         store_rows_tma<D, true, D / 64>(&m.dQ, lane_addr + C::Q_ACC, nc > 0, a.scale, st_q, r_base,
-                                        r_base < a.Sq, bh);
+                                        r_base < a.Sq, bh, 0, a.Dv);
       else
         store_rows_tma<D, false, D / 32>(&m.dQ, lane_addr + C::Q_ACC, nc > 0, a.scale, st_q,
-                                         r_base, r_base < a.Sq, bh);
+                                         r_base, r_base < a.Sq, bh, 0, a.Dv);
     }
   }
   tc_fence_before();
@@ -716,7 +717,7 @@ __device__ __forceinline__ void issue_rowdot128(uint32_t d, uint32_t a, uint32_t
 template <int NCOL, bool OUT_BF16>
 __device__ __forceinline__ void stage_store_rows(const uint32_t (&r)[NCOL], float mul,
                                                  uint32_t stage, const CUtensorMap* tm, int x0,
-                                                 int r_base, bool any_row, int z) {
+                                                 int r_base, bool any_row, int z, int x_end) {
   constexpr int COLS = OUT_BF16 ? 64 : 32;  // columns per 128-byte box row
   constexpr int NBOX = NCOL / COLS;
   static_assert(NCOL % COLS == 0, "whole boxes");
@@ -747,7 +748,8 @@ __device__ __forceinline__ void stage_store_rows(const uint32_t (&r)[NCOL], floa
   if (lane == 0) {
     if (any_row)
       for (int bx = 0; bx < NBOX; ++bx)
-        tma_store_3d(tm, stage + bx * EPI_BOX_BYTES, x0 + bx * COLS, r_base, z);
+        if (x0 + bx * COLS < x_end)  // (boxes past the tensor's width are not stored)
+          tma_store_3d(tm, stage + bx * EPI_BOX_BYTES, x0 + bx * COLS, r_base, z);
     bulk_commit_group();
   }
 }
@@ -766,8 +768,8 @@ __device__ __forceinline__ void stage_store_rows(const uint32_t (&r)[NCOL], floa
 // per-item phases can only complete after every role has observed the one before
 // (e.g. q_rel(j+1) follows S MMAs of item j+1, which need Q_{j+1}, loaded only after
 // q_rel(j) was seen), so a parity wait never misses a phase. An item whose rows see
-// no key touches none of these barriers: its softmax warps write the zero rows
-// directly.
+// no key touches none of these barriers and writes nothing: the launcher zeroes those
+// dQ rows beforehand.
 template <int D>
 __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     fa_bwd_dq16_kernel(const __grid_constant__ QMaps m, const BwdArgs a) {
@@ -1038,22 +1040,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     for (int k = 0, w = take_warp(0); ok && w < n_items; w = take_warp(++k)) {
       const Item it = item(w);
       const int i = it.i0 + wq * 32 + lane;
-      if (it.nc == 0) {
-        // no key for any row of the tile: dQ = 0, written directly (no barrier involved)
-        if (i < a.Sq) {
-          const size_t off = ((size_t)it.bh * a.Sq + i) * D + half * (D / 2);
-          if (a.out_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dQ) + off);
-#pragma unroll
-            for (int e = 0; e < D / 16; ++e) dst[e] = make_uint4(0, 0, 0, 0);
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.dQ) + off);
-#pragma unroll
-            for (int e = 0; e < D / 8; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-        continue;
-      }
+      if (it.nc == 0) continue;  // no key for any row of the tile: zeroed by the launcher
       const bool row_valid = i < a.Sq;
       const size_t vrow = (size_t)it.bh * a.ldq + (size_t)(row_valid ? i : 0);
       const float nl = row_valid ? -a.lse2[vrow] : -INFINITY;
@@ -1154,7 +1141,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         mbar_arrive(&bar_dqfree);  // dQ has left TMEM: the next item may accumulate
         if (mine)
           stage_store_rows<NCOL, BF>(r, a.scale, sbase + C::V_OFF + warp * (C::EPI_WARP / 2),
-                                     &m.dQ, x0, r_base, any, it.bh);
+                                     &m.dQ, x0, r_base, any, it.bh, a.Dv);
       };
       if (a.out_bf16) epilogue(std::true_type{});
       else epilogue(std::false_type{});
@@ -1562,12 +1549,14 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
       const uint32_t stage = sbase + warp * (C::EPI_WARP / HP);
       if (a.out_bf16) {
         if constexpr (DW % 64 == 0)
-          store_rows_tma<DW, true, DW / 64>(tm, acc, nc > 0, mul, stage, r_base, any, bg, cpart * DW);
+          store_rows_tma<DW, true, DW / 64>(tm, acc, nc > 0, mul, stage, r_base, any, bg, cpart * DW,
+                                            a.Dv);
         else if (cpart == 0)  // a bf16 box is a 64-column row: one warp per output does it
           store_rows_tma<D, true, D / 64>(tm, lane_addr + (which ? C::DK : C::DV), nc > 0, mul,
-                                          sbase + warp * C::EPI_WARP, r_base, any, bg);
+                                          sbase + warp * C::EPI_WARP, r_base, any, bg, 0, a.Dv);
       } else {
-        store_rows_tma<DW, false, DW / 32>(tm, acc, nc > 0, mul, stage, r_base, any, bg, cpart * DW);
+        store_rows_tma<DW, false, DW / 32>(tm, acc, nc > 0, mul, stage, r_base, any, bg, cpart * DW,
+                                           a.Dv);
       }
     }
   }
@@ -1601,7 +1590,8 @@ __global__ void bwd_preprocess_kernel(const void* __restrict__ dO, const void* _
                                       const float* __restrict__ LSE, const void* __restrict__ Q,
                                       __half* __restrict__ dO16, __half* __restrict__ Q16,
                                       float* __restrict__ lse2, float* __restrict__ delta, int Sq,
-                                      int ldq, size_t n_rows_padded, int in_bf16, int o_bf16) {
+                                      int ldq, size_t n_rows_padded, int in_bf16, int o_bf16,
+                                      int Dv) {
   const size_t warps = (size_t)gridDim.x * (blockDim.x / 32);
   const int lane = threadIdx.x & 31;
   for (size_t w = blockIdx.x * (size_t)(blockDim.x / 32) + threadIdx.x / 32; w < n_rows_padded;
@@ -1617,21 +1607,21 @@ __global__ void bwd_preprocess_kernel(const void* __restrict__ dO, const void* _
 #pragma unroll
     for (int d0 = 0; d0 < D; d0 += 128) {
       const int d = d0 + lane * 4;
-      if (d >= D) break;  // D = 64: lanes 16..31 have no columns
+      if (d >= Dv) break;  // rows of Dv <= D columns: the lanes past them have none
       float gv[4], ov[4];
-      load4(dO, row * D + d, in_bf16, gv);
-      load4(O, row * D + d, o_bf16, ov);
+      load4(dO, row * Dv + d, in_bf16, gv);
+      load4(O, row * Dv + d, o_bf16, ov);
       acc += gv[0] * ov[0] + gv[1] * ov[1] + gv[2] * ov[2] + gv[3] * ov[3];
       if (dO16) {
         float qv[4];
-        load4(Q, row * D + d, 1, qv);
+        load4(Q, row * Dv + d, 1, qv);
         uint2 g16, q16;
         g16.x = pack_half2(gv[0], gv[1]);
         g16.y = pack_half2(gv[2], gv[3]);
         q16.x = pack_half2(qv[0], qv[1]);
         q16.y = pack_half2(qv[2], qv[3]);
-        *reinterpret_cast<uint2*>(dO16 + row * D + d) = g16;
-        *reinterpret_cast<uint2*>(Q16 + row * D + d) = q16;
+        *reinterpret_cast<uint2*>(dO16 + row * Dv + d) = g16;
+        *reinterpret_cast<uint2*>(Q16 + row * Dv + d) = q16;
       }
     }
 #pragma unroll
@@ -1659,10 +1649,11 @@ __global__ void bwd_prepass16_kernel(const __nv_bfloat16* __restrict__ dO, const
                                      __half* __restrict__ Q16, __half* __restrict__ K16,
                                      __half* __restrict__ V16, float* __restrict__ lse2,
                                      float* __restrict__ delta, int Sq, int ldq, size_t q_rows,
-                                     size_t kv_rows, int o_bf16, int* __restrict__ sched) {
-  constexpr int TPR = D / 8;  // threads per row
+                                     size_t kv_rows, int o_bf16, int* __restrict__ sched, int Dv) {
+  constexpr int TPR = D / 8;  // threads per row (rows have Dv <= D columns: the rest idle)
   if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;  // the dQ kernel's work-item counter
   const int t = threadIdx.x % TPR;
+  const bool cols = t * 8 < Dv;  // this thread's 8 columns exist
   const size_t rows_per_grid = (size_t)gridDim.x * (blockDim.x / TPR);
   auto cvt8 = [](uint4 v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -1678,8 +1669,8 @@ __global__ void bwd_prepass16_kernel(const __nv_bfloat16* __restrict__ dO, const
       const size_t bh = r / ldq;
       const int i = (int)(r % ldq);
       float acc = 0.f;
-      if (i < Sq) {
-        const size_t off = (bh * Sq + i) * D + t * 8;
+      if (i < Sq && cols) {
+        const size_t off = (bh * Sq + i) * Dv + t * 8;
         const uint4 g = *reinterpret_cast<const uint4*>(dO + off);
         const uint4 q = *reinterpret_cast<const uint4*>(Q + off);
         float ov[8];
@@ -1717,8 +1708,8 @@ __global__ void bwd_prepass16_kernel(const __nv_bfloat16* __restrict__ dO, const
           delta[r] = 0.f;
         }
       }
-    } else {
-      const size_t off = (r - q_rows) * D + t * 8;
+    } else if (cols) {
+      const size_t off = (r - q_rows) * Dv + t * 8;
       *reinterpret_cast<uint4*>(K16 + off) = cvt8(*reinterpret_cast<const uint4*>(K + off));
       *reinterpret_cast<uint4*>(V16 + off) = cvt8(*reinterpret_cast<const uint4*>(V + off));
     }
@@ -1740,12 +1731,15 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
                   const float* LSE, void* dQ, void* dK, void* dV, const fa_params& p,
                   cudaStream_t stream) {
   using C = BwdCfg<D, F32>;
+  // Tensors have Dv = p.D <= D columns: loads past Dv read zeros, stores past it are
+  // dropped, and the pre-passes work on Dv-element rows.
+  const int Dv = p.D;
   const size_t BH = (size_t)p.B * p.H, BHk = (size_t)p.B * p.HKV;
-  const size_t nq = BH * p.Sq * D, nk = BHk * p.Sk * D;
+  const size_t nq = BH * p.Sq * Dv, nk = BHk * p.Sk * Dv;
   const int ldq = (p.Sq + 127) / 128 * 128;  // lse2 / delta row pitch: whole 128-query chunks
   const size_t nvec = BH * ldq;
   const int ldqt = (p.Sq + 3) / 4 * 4, ldkt = (p.Sk + 3) / 4 * 4;  // transposed row pitch
-  const size_t nqt = BH * D * ldqt, nkt = BHk * D * ldkt;
+  const size_t nqt = BH * Dv * ldqt, nkt = BHk * Dv * ldkt;
   size_t bytes = 2 * nvec * 4;
   if constexpr (!F32) bytes += (2 * nq + 2 * nk) * 2;
   else bytes += (4 * nq + 4 * nk + 4 * nqt + 2 * nkt) * 4;  // Q,dO,K,V hi/lo + Q^T,dO^T,K^T hi/lo
@@ -1767,9 +1761,9 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     const bool bf = p.out_dtype == FA_BF16;
     const auto odt = bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : F32T;
     const int oes = bf ? 2 : 4;
-    enc &= host::encode_tiled_3d(&mk.dK, odt, oes, dK, D, p.Sk, BHk, D, 128 / oes, 32);
-    enc &= host::encode_tiled_3d(&mk.dV, odt, oes, dV, D, p.Sk, BHk, D, 128 / oes, 32);
-    enc &= host::encode_tiled_3d(&mq.dQ, odt, oes, dQ, D, p.Sq, BH, D, 128 / oes, 32);
+    enc &= host::encode_tiled_3d(&mk.dK, odt, oes, dK, Dv, p.Sk, BHk, Dv, 128 / oes, 32);
+    enc &= host::encode_tiled_3d(&mk.dV, odt, oes, dV, Dv, p.Sk, BHk, Dv, 128 / oes, 32);
+    enc &= host::encode_tiled_3d(&mq.dQ, odt, oes, dQ, Dv, p.Sq, BH, Dv, 128 / oes, 32);
   }
   enc &= host::encode_tiled_3d(&mk.Dl, F32T, 4, delta, ldq, BH, 1, ldq, qchunk, 1, false);
   if constexpr (!F32) {
@@ -1782,17 +1776,40 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       bwd_prepass16_kernel<D><<<8 * host::sm_count(), 256, 0, stream>>>(
           static_cast<const __nv_bfloat16*>(dO), O, LSE, static_cast<const __nv_bfloat16*>(Q),
           static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(V), do16, q16, k16,
-          v16, lse2, delta, p.Sq, ldq, nvec, BHk * p.Sk, p.out_dtype == FA_BF16, sched);
+          v16, lse2, delta, p.Sq, ldq, nvec, BHk * p.Sk, p.out_dtype == FA_BF16, sched, Dv);
+    }
+    // Query tiles whose rows see no key (a window ending before the keys do: a suffix
+    // of tiles) are skipped by the dQ kernel; their rows are zeroed here, before the
+    // dK/dV launch (nothing may come between it and its dependent dQ launch).
+    {
+      const int n_qt = (p.Sq + BLOCK_M - 1) / BLOCK_M;
+      int t0 = n_qt;
+      while (t0 > 0) {
+        int lo, hi;
+        kv_tile_range((t0 - 1) * BLOCK_M, std::min(t0 * BLOCK_M, p.Sq) - 1, p.Sk, p.causal,
+                      p.window, &lo, &hi);
+        if (hi > lo) break;
+        --t0;
+      }
+      if (t0 < n_qt) {
+        const size_t esz = p.out_dtype == FA_BF16 ? 2 : 4;
+        const size_t row = (size_t)Dv * esz;
+        if (cudaMemset2DAsync(static_cast<char*>(dQ) + (size_t)t0 * BLOCK_M * row, p.Sq * row, 0,
+                              (size_t)(p.Sq - t0 * BLOCK_M) * row, BH, stream) != cudaSuccess) {
+          host::scratch_free(ws, stream);
+          return FA_ERR_CUDA;
+        }
+      }
     }
     const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    enc &= host::encode_tiled_3d(&mk.K[0], F16, 2, k16, D, p.Sk, BHk, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mk.V[0], F16, 2, v16, D, p.Sk, BHk, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mk.Qc[0], F16, 2, q16, D, p.Sq, BH, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mk.dOc[0], F16, 2, do16, D, p.Sq, BH, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mq.Q[0], F16, 2, q16, D, p.Sq, BH, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mq.dO[0], F16, 2, do16, D, p.Sq, BH, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mq.Kc[0], F16, 2, k16, D, p.Sk, BHk, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mq.Vc[0], F16, 2, v16, D, p.Sk, BHk, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mk.K[0], F16, 2, k16, Dv, p.Sk, BHk, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mk.V[0], F16, 2, v16, Dv, p.Sk, BHk, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mk.Qc[0], F16, 2, q16, Dv, p.Sq, BH, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mk.dOc[0], F16, 2, do16, Dv, p.Sq, BH, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mq.Q[0], F16, 2, q16, Dv, p.Sq, BH, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mq.dO[0], F16, 2, do16, Dv, p.Sq, BH, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mq.Kc[0], F16, 2, k16, Dv, p.Sk, BHk, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mq.Vc[0], F16, 2, v16, Dv, p.Sk, BHk, Dv, 64, 128);
     mk.K[1] = mk.K[0]; mk.V[1] = mk.V[0]; mk.Qc[1] = mk.Qc[0]; mk.dOc[1] = mk.dOc[0];
     mk.Qt[0] = mk.Qt[1] = mk.Qc[0]; mk.dOt[0] = mk.dOt[1] = mk.dOc[0];
     mq.Q[1] = mq.Q[0]; mq.dO[1] = mq.dO[0]; mq.Kc[1] = mq.Kc[0]; mq.Vc[1] = mq.Vc[0];
@@ -1816,18 +1833,18 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       host::KernelTimer kt("bwd_preprocess", stream);
       bwd_preprocess_kernel<D><<<grid_pp, 256, 0, stream>>>(dO, O, LSE, Q, nullptr, nullptr, lse2,
                                                            delta, p.Sq, ldq, nvec, 0,
-                                                           p.out_dtype == FA_BF16);
+                                                           p.out_dtype == FA_BF16, Dv);
     }
     {
       host::KernelTimer kt("split_tf32(Q,dO,K,V)", stream);
       split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(Q), qh, ql, qth, qtl,
-                                                    p.Sq, D, ldqt, BH);
+                                                    p.Sq, Dv, ldqt, BH);
       split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(dO), doh, dol, doth,
-                                                    dotl, p.Sq, D, ldqt, BH);
+                                                    dotl, p.Sq, Dv, ldqt, BH);
       split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(K), kh, kl, kth, ktl,
-                                                    p.Sk, D, ldkt, BHk);
+                                                    p.Sk, Dv, ldkt, BHk);
       split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(V), vh, vl, nullptr,
-                                                    nullptr, p.Sk, D, 0, BHk);
+                                                    nullptr, p.Sk, Dv, 0, BHk);
     }
     float* hl_q[2] = {qh, ql};
     float* hl_do[2] = {doh, dol};
@@ -1837,17 +1854,17 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     float* hl_dot[2] = {doth, dotl};
     float* hl_kt[2] = {kth, ktl};
     for (int sp = 0; sp < 2; ++sp) {
-      enc &= host::encode_tiled_3d(&mk.K[sp], F32T, 4, hl_k[sp], D, p.Sk, BHk, D, 32, 128);
-      enc &= host::encode_tiled_3d(&mk.V[sp], F32T, 4, hl_v[sp], D, p.Sk, BHk, D, 32, 128);
-      enc &= host::encode_tiled_3d(&mk.Qc[sp], F32T, 4, hl_q[sp], D, p.Sq, BH, D, 32, C::CH);
-      enc &= host::encode_tiled_3d(&mk.dOc[sp], F32T, 4, hl_do[sp], D, p.Sq, BH, D, 32, C::CH);
-      enc &= host::encode_tiled_3d(&mk.Qt[sp], F32T, 4, hl_qt[sp], p.Sq, D, BH, ldqt, 32, D);
-      enc &= host::encode_tiled_3d(&mk.dOt[sp], F32T, 4, hl_dot[sp], p.Sq, D, BH, ldqt, 32, D);
-      enc &= host::encode_tiled_3d(&mq.Q[sp], F32T, 4, hl_q[sp], D, p.Sq, BH, D, 32, 128);
-      enc &= host::encode_tiled_3d(&mq.dO[sp], F32T, 4, hl_do[sp], D, p.Sq, BH, D, 32, 128);
-      enc &= host::encode_tiled_3d(&mq.Kc[sp], F32T, 4, hl_k[sp], D, p.Sk, BHk, D, 32, C::CH);
-      enc &= host::encode_tiled_3d(&mq.Vc[sp], F32T, 4, hl_v[sp], D, p.Sk, BHk, D, 32, C::CH);
-      enc &= host::encode_tiled_3d(&mq.Kt[sp], F32T, 4, hl_kt[sp], p.Sk, D, BHk, ldkt, 32, D);
+      enc &= host::encode_tiled_3d(&mk.K[sp], F32T, 4, hl_k[sp], Dv, p.Sk, BHk, Dv, 32, 128);
+      enc &= host::encode_tiled_3d(&mk.V[sp], F32T, 4, hl_v[sp], Dv, p.Sk, BHk, Dv, 32, 128);
+      enc &= host::encode_tiled_3d(&mk.Qc[sp], F32T, 4, hl_q[sp], Dv, p.Sq, BH, Dv, 32, C::CH);
+      enc &= host::encode_tiled_3d(&mk.dOc[sp], F32T, 4, hl_do[sp], Dv, p.Sq, BH, Dv, 32, C::CH);
+      enc &= host::encode_tiled_3d(&mk.Qt[sp], F32T, 4, hl_qt[sp], p.Sq, Dv, BH, ldqt, 32, D);
+      enc &= host::encode_tiled_3d(&mk.dOt[sp], F32T, 4, hl_dot[sp], p.Sq, Dv, BH, ldqt, 32, D);
+      enc &= host::encode_tiled_3d(&mq.Q[sp], F32T, 4, hl_q[sp], Dv, p.Sq, BH, Dv, 32, 128);
+      enc &= host::encode_tiled_3d(&mq.dO[sp], F32T, 4, hl_do[sp], Dv, p.Sq, BH, Dv, 32, 128);
+      enc &= host::encode_tiled_3d(&mq.Kc[sp], F32T, 4, hl_k[sp], Dv, p.Sk, BHk, Dv, 32, C::CH);
+      enc &= host::encode_tiled_3d(&mq.Vc[sp], F32T, 4, hl_v[sp], Dv, p.Sk, BHk, Dv, 32, C::CH);
+      enc &= host::encode_tiled_3d(&mq.Kt[sp], F32T, 4, hl_kt[sp], p.Sk, Dv, BHk, ldkt, 32, D);
     }
   }
   if (!enc) {
@@ -1861,6 +1878,7 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   a.scale = p.scale; a.scale_log2 = p.scale * LOG2E;
   a.causal = p.causal; a.window = p.window; a.out_bf16 = p.out_dtype == FA_BF16;
   a.lpt = p.causal;
+  a.Dv = Dv;
   a.sched = sched;
   a.limit_ns = WAIT_LIMIT_NS;
   cudaError_t e = cudaSuccess;
@@ -1958,11 +1976,12 @@ fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O,
     }
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
+  // head dims below a kernel's D run in it with the missing columns read as zeros
   if (p.in_dtype == FA_BF16) {
-    if (p.D == 128) return run_bwd<128, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
-    if (p.D == 64) return run_bwd<64, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
+    if (p.D <= 64) return run_bwd<64, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
+    if (p.D <= 128) return run_bwd<128, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
   } else {
-    if (p.D == 64) return run_bwd<64, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
+    if (p.D <= 64) return run_bwd<64, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
   }
   return FA_ERR_UNSUPPORTED;
 }

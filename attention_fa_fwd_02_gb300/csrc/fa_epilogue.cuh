@@ -34,11 +34,13 @@ constexpr uint32_t epi_warp_bytes() {
 // does); without, the caller issues bulk_wait_read_all() (lane 0) before the staging
 // area is reused or the CTA exits.
 // D is the number of columns this call stores: TMEM columns t_addr .. t_addr + D of
-// the warp's lanes go to tensor columns x0 .. x0 + D.
+// the warp's lanes go to tensor columns x0 .. x0 + D. Boxes that would start at or
+// beyond column x_end (the tensor's width, for head dims below the kernel's D) are not
+// stored; the TMA store clips a box that crosses it.
 template <int D, bool OUT_BF16, int BOXES, bool WAIT = true>
 __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tm, uint32_t t_addr, bool have,
                                                float mul, uint32_t stage, int r_base, bool any_row,
-                                               int z, int x0 = 0) {
+                                               int z, int x0 = 0, int x_end = 1 << 30) {
   using namespace ptx;
   constexpr int COLS = OUT_BF16 ? 64 : 32;  // output columns per 128-byte box row
   constexpr int NBOX = D / COLS;
@@ -94,7 +96,8 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tm, uint32_t t
       __syncwarp();
       if (lane == 0 && any_row) {
         for (int j = b - slot; j <= b; ++j)
-          tma_store_3d(tm, stage + (j % BOXES) * EPI_BOX_BYTES, x0 + j * COLS, r_base, z);
+          if (x0 + j * COLS < x_end)
+            tma_store_3d(tm, stage + (j % BOXES) * EPI_BOX_BYTES, x0 + j * COLS, r_base, z);
         bulk_commit_group();
       }
     }

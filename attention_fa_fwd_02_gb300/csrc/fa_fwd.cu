@@ -44,6 +44,7 @@ struct FwdArgs {
   int out_bf16;
   int n_qgroups;
   int n_items;  // BH * n_qgroups
+  int Dv;       // head dim of the tensors (<= the kernel's D; missing columns read as 0)
   int lpt;  // 1: the heaviest query groups first (causal)
   int BH;
   unsigned long long limit_ns;
@@ -651,10 +652,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         if (ok) {
           if (a.out_bf16)
             store_rows_tma<D, true, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                     r_base < a.Sq, itm.bh);
+                                                     r_base < a.Sq, itm.bh, 0, a.Dv);
           else
             store_rows_tma<D, false, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                      r_base < a.Sq, itm.bh);
+                                                      r_base < a.Sq, itm.bh, 0, a.Dv);
         }
         named_bar_sync(C::EPI_BAR0 + q, 128);
         if (wq == 0 && lane == 0) mbar_arrive(&bar_grant[q + 1]);
@@ -662,10 +663,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         if (ok) {
           if (a.out_bf16)
             store_rows_tma<D, true, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                            r_base < a.Sq, itm.bh);
+                                                            r_base < a.Sq, itm.bh, 0, a.Dv);
           else
             store_rows_tma<D, false, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage,
-                                                             r_base, r_base < a.Sq, itm.bh);
+                                                             r_base, r_base < a.Sq, itm.bh, 0, a.Dv);
         }
         pending = true;
         pend_slot = slot;
@@ -701,24 +702,26 @@ __global__ void fill_empty_kernel(void* O, float* LSE, size_t rows, int D, int o
 namespace {
 
 // O as [B*H][Sq][D] in the output type; boxes of 32 rows x 128 bytes, 128-byte swizzle.
-template <int D>
+// Tensors have p.D columns (the kernel's D or fewer: loads past p.D read zeros, stores
+// past it are dropped).
 bool encode_o_map(CUtensorMap* m, void* O, const fa_params& p) {
   const bool bf = p.out_dtype == FA_BF16;
   return host::encode_tiled_3d(m, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                               bf ? 2 : 4, O, D, p.Sq, (uint64_t)p.B * p.H, D, bf ? 64 : 32, 32);
+                               bf ? 2 : 4, O, p.D, p.Sq, (uint64_t)p.B * p.H, p.D, bf ? 64 : 32, 32);
 }
 
 template <int D, bool F32>
 fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                   const fa_params& p, cudaStream_t stream) {
   using C = FwdCfg<D, F32>;
-  const size_t nq = (size_t)p.B * p.H * p.Sq * D;
-  const size_t nk = (size_t)p.B * p.HKV * p.Sk * D;
+  const int Dv = p.D;
+  const size_t nq = (size_t)p.B * p.H * p.Sq * Dv;
+  const size_t nk = (size_t)p.B * p.HKV * p.Sk * Dv;
   const int grid_pp = 4 * host::sm_count();
   void* ws = nullptr;
   CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo, mO;
   const uint64_t BHq = (uint64_t)p.B * p.H, BHk = (uint64_t)p.B * p.HKV;
-  bool enc = encode_o_map<D>(&mO, O, p);
+  bool enc = encode_o_map(&mO, O, p);
   if constexpr (!F32) {
     if (host::scratch_alloc(&ws, nk * 2, stream) != cudaSuccess) return FA_ERR_CUDA;
     {
@@ -726,13 +729,13 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
       cvt_bf16_to_f16_kernel<<<2 * grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
                                                          static_cast<uint4*>(ws), nk / 8);
     }
-    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, D, p.Sq, BHq, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, D, p.Sk, BHk, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, D, p.Sk, BHk, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, Dv, p.Sq, BHq, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, Dv, p.Sk, BHk, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, Dv, p.Sk, BHk, Dv, 64, 128);
     mQlo = mQ; mKlo = mK; mVlo = mV;
   } else {
     const int ldt = (p.Sk + 3) / 4 * 4;  // transposed V rows padded to 16 bytes
-    const size_t nvt = (size_t)p.B * p.HKV * D * ldt;
+    const size_t nvt = (size_t)p.B * p.HKV * Dv * ldt;
     const size_t bytes = (2 * nq + 2 * nk + 2 * nvt) * 4;
     if (host::scratch_alloc(&ws, bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
     float* qh = static_cast<float*>(ws);
@@ -743,18 +746,18 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
     float* vtl = vth + nvt;
     host::KernelTimer kt("split_tf32(Q,K,V)", stream);
     split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(Q), qh, ql, nullptr,
-                                                  nullptr, p.Sq, D, 0, BHq);
+                                                  nullptr, p.Sq, Dv, 0, BHq);
     split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(K), kh, kl, nullptr,
-                                                  nullptr, p.Sk, D, 0, BHk);
+                                                  nullptr, p.Sk, Dv, 0, BHk);
     split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(V), nullptr, nullptr,
-                                                  vth, vtl, p.Sk, D, ldt, BHk);
-    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, qh, D, p.Sq, BHq, D, 32, 128);
-    enc &= host::encode_tiled_3d(&mQlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ql, D, p.Sq, BHq, D, 32, 128);
-    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kh, D, p.Sk, BHk, D, 32, 128);
-    enc &= host::encode_tiled_3d(&mKlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kl, D, p.Sk, BHk, D, 32, 128);
+                                                  vth, vtl, p.Sk, Dv, ldt, BHk);
+    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, qh, Dv, p.Sq, BHq, Dv, 32, 128);
+    enc &= host::encode_tiled_3d(&mQlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ql, Dv, p.Sq, BHq, Dv, 32, 128);
+    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kh, Dv, p.Sk, BHk, Dv, 32, 128);
+    enc &= host::encode_tiled_3d(&mKlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kl, Dv, p.Sk, BHk, Dv, 32, 128);
     // V^T: [BHk][D][ldt], inner extent Sk (row stride ldt), box 32 keys x D rows
-    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, vth, p.Sk, D, BHk, ldt, 32, D);
-    enc &= host::encode_tiled_3d(&mVlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, vtl, p.Sk, D, BHk, ldt, 32, D);
+    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, vth, p.Sk, Dv, BHk, ldt, 32, D);
+    enc &= host::encode_tiled_3d(&mVlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, vtl, p.Sk, Dv, BHk, ldt, 32, D);
   }
   if (!enc) {
     host::scratch_free(ws, stream);
@@ -773,6 +776,7 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   a.out_bf16 = p.out_dtype == FA_BF16;
   a.n_qgroups = (p.Sq + BLOCK_M * C::NQ - 1) / (BLOCK_M * C::NQ);
   a.n_items = (int)BHq * a.n_qgroups;
+  a.Dv = Dv;
   a.lpt = p.causal ? 1 : 0;
   a.BH = (int)BHq;
   a.limit_ns = WAIT_LIMIT_NS;
@@ -801,11 +805,12 @@ fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float
                                                                 p.out_dtype == FA_BF16);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
+  // head dims below a kernel's D run in it with the missing columns read as zeros
   if (p.in_dtype == FA_BF16) {
-    if (p.D == 128) return run_fwd<128, false>(Q, K, V, O, LSE, p, stream);
-    if (p.D == 64) return run_fwd<64, false>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 64) return run_fwd<64, false>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 128) return run_fwd<128, false>(Q, K, V, O, LSE, p, stream);
   } else {
-    if (p.D == 64) return run_fwd<64, true>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 64) return run_fwd<64, true>(Q, K, V, O, LSE, p, stream);
   }
   return FA_ERR_UNSUPPORTED;
 }
@@ -905,15 +910,15 @@ fa_status noalloc_scratch_addr(void** out) {
   return FA_OK;
 }
 
-template <int D, bool F32>
+template <bool F32>
 size_t noalloc_bytes(const fa_params& p) {
-  const size_t nq = (size_t)p.B * p.H * p.Sq * D;
-  const size_t nk = (size_t)p.B * p.HKV * p.Sk * D;
+  const size_t nq = (size_t)p.B * p.H * p.Sq * p.D;
+  const size_t nk = (size_t)p.B * p.HKV * p.Sk * p.D;
   if constexpr (!F32) {
     return nk * 2;
   } else {
     const size_t ldt = ((size_t)p.Sk + 3) / 4 * 4;
-    const size_t nvt = (size_t)p.B * p.HKV * D * ldt;
+    const size_t nvt = (size_t)p.B * p.HKV * p.D * ldt;
     return (2 * nq + 2 * nk + 2 * nvt) * 4;
   }
 }
@@ -922,28 +927,29 @@ template <int D, bool F32>
 fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
                           const fa_params& p, cudaStream_t stream) {
   using C = FwdCfg<D, F32>;
-  if (noalloc_bytes<D, F32>(p) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+  if (noalloc_bytes<F32>(p) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;
   const fa_status st = noalloc_scratch_addr(&ws);
   if (st != FA_OK) return st;
-  const size_t nq = (size_t)p.B * p.H * p.Sq * D;
-  const size_t nk = (size_t)p.B * p.HKV * p.Sk * D;
+  const int Dv = p.D;
+  const size_t nq = (size_t)p.B * p.H * p.Sq * Dv;
+  const size_t nk = (size_t)p.B * p.HKV * p.Sk * Dv;
   const int grid_pp = 4 * host::sm_count();
   CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo, mO;
   const uint64_t BHq = (uint64_t)p.B * p.H, BHk = (uint64_t)p.B * p.HKV;
-  bool enc = encode_o_map<D>(&mO, O, p);
+  bool enc = encode_o_map(&mO, O, p);
   // The whole scratch region used below is rewritten by the pre-pass kernels on
   // every call, so nothing left over from an earlier call is ever read.
   if constexpr (!F32) {
     cvt_bf16_to_f16_kernel<<<2 * grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
                                                        static_cast<uint4*>(ws), nk / 8);
-    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, D, p.Sq, BHq, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, D, p.Sk, BHk, D, 64, 128);
-    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, D, p.Sk, BHk, D, 64, 128);
+    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, Dv, p.Sq, BHq, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, Dv, p.Sk, BHk, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, Dv, p.Sk, BHk, Dv, 64, 128);
     mQlo = mQ; mKlo = mK; mVlo = mV;
   } else {
     const int ldt = (p.Sk + 3) / 4 * 4;
-    const size_t nvt = (size_t)p.B * p.HKV * D * ldt;
+    const size_t nvt = (size_t)p.B * p.HKV * Dv * ldt;
     float* qh = static_cast<float*>(ws);
     float* ql = qh + nq;
     float* kh = ql + nq;
@@ -951,17 +957,17 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
     float* vth = kl + nk;
     float* vtl = vth + nvt;
     split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(Q), qh, ql, nullptr,
-                                                  nullptr, p.Sq, D, 0, BHq);
+                                                  nullptr, p.Sq, Dv, 0, BHq);
     split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(K), kh, kl, nullptr,
-                                                  nullptr, p.Sk, D, 0, BHk);
+                                                  nullptr, p.Sk, Dv, 0, BHk);
     split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(V), nullptr, nullptr,
-                                                  vth, vtl, p.Sk, D, ldt, BHk);
-    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, qh, D, p.Sq, BHq, D, 32, 128);
-    enc &= host::encode_tiled_3d(&mQlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ql, D, p.Sq, BHq, D, 32, 128);
-    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kh, D, p.Sk, BHk, D, 32, 128);
-    enc &= host::encode_tiled_3d(&mKlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kl, D, p.Sk, BHk, D, 32, 128);
-    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, vth, p.Sk, D, BHk, ldt, 32, D);
-    enc &= host::encode_tiled_3d(&mVlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, vtl, p.Sk, D, BHk, ldt, 32, D);
+                                                  vth, vtl, p.Sk, Dv, ldt, BHk);
+    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, qh, Dv, p.Sq, BHq, Dv, 32, 128);
+    enc &= host::encode_tiled_3d(&mQlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ql, Dv, p.Sq, BHq, Dv, 32, 128);
+    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kh, Dv, p.Sk, BHk, Dv, 32, 128);
+    enc &= host::encode_tiled_3d(&mKlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kl, Dv, p.Sk, BHk, Dv, 32, 128);
+    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, vth, p.Sk, Dv, BHk, ldt, 32, D);
+    enc &= host::encode_tiled_3d(&mVlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, vtl, p.Sk, Dv, BHk, ldt, 32, D);
   }
   if (!enc || cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   FwdArgs a;
@@ -977,6 +983,7 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
   a.out_bf16 = p.out_dtype == FA_BF16;
   a.n_qgroups = (p.Sq + BLOCK_M * C::NQ - 1) / (BLOCK_M * C::NQ);
   a.n_items = (int)BHq * a.n_qgroups;
+  a.Dv = Dv;
   a.lpt = p.causal ? 1 : 0;
   a.BH = (int)BHq;
   a.limit_ns = WAIT_LIMIT_NS;
@@ -1000,10 +1007,10 @@ fa_status launch_fwd_noalloc(const void* Q, const void* K, const void* V, void* 
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
   if (p.in_dtype == FA_BF16) {
-    if (p.D == 128) return run_fwd_noalloc<128, false>(Q, K, V, O, LSE, p, stream);
-    if (p.D == 64) return run_fwd_noalloc<64, false>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 64) return run_fwd_noalloc<64, false>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 128) return run_fwd_noalloc<128, false>(Q, K, V, O, LSE, p, stream);
   } else {
-    if (p.D == 64) return run_fwd_noalloc<64, true>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 64) return run_fwd_noalloc<64, true>(Q, K, V, O, LSE, p, stream);
   }
   return FA_ERR_UNSUPPORTED;
 }

@@ -39,6 +39,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 KERNEL_FLOPS_PER_PAIR_PER_D = {"fa_fwd_kernel": 4, "fa_bwd_dkdv_kernel": 8, "fa_bwd_dq_kernel": 6}
 # Source files whose change invalidates a committed DRAM-traffic figure.
 _COMMON_SOURCES = ["ptx.cuh", "fa_common.cuh", "fa_epilogue.cuh", "fa_prepass.cuh"]
+# head dim of each named workload (traffic figures in profiles/ are for these)
+WORKLOADS_D = {"c1": 64, "c2": 64, "c3": 128, "c4": 128, "c5": 64}
 KERNEL_SOURCES = {"fa_fwd_kernel": ["fa_fwd.cu"] + _COMMON_SOURCES,
                   "fa_bwd_dkdv_kernel": ["fa_bwd.cu"] + _COMMON_SOURCES,
                   "fa_bwd_dq_kernel": ["fa_bwd.cu"] + _COMMON_SOURCES,
@@ -175,12 +177,21 @@ def config_of(w, extra=None):
     return c
 
 
+def workload_of(args):
+    """The named workload, with another head dim (scale 1/sqrt(D)) if --head-dim is given."""
+    from attention_fa_fwd_02_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.head_dim and args.head_dim != w.D:
+        w = w.with_(D=args.head_dim, scale=args.head_dim ** -0.5,
+                    name=w.name.replace(f"-d{w.D}-", f"-d{args.head_dim}-"))
+    return w
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
-    from attention_fa_fwd_02_gb300.workloads import WORKLOADS
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     # each step: one whole (batch, kv-group) slice of the workload through the oracle
     for _ in range(args.warmup):
         oracle_sample(w, 1)
@@ -236,7 +247,7 @@ def run_ours(args, rank, world, local_rank):
     import __graft_entry__
     __graft_entry__.build_library()
     from attention_fa_fwd_02_gb300 import fa
-    from attention_fa_fwd_02_gb300.workloads import WORKLOADS, make_inputs
+    from attention_fa_fwd_02_gb300.workloads import make_inputs
 
     dist = None
     if world > 1:
@@ -244,7 +255,7 @@ def run_ours(args, rank, world, local_rank):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     wr = rank_workload(w, rank)
     q, k, v, do = make_inputs(wr)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
@@ -423,7 +434,7 @@ def run_ours(args, rank, world, local_rank):
               key=lambda k_: per_kernel[k_]["launches"] * per_kernel[k_]["ms_per_launch"])
     dom_base = dom.split("<")[0]
     achieved = per_kernel[dom]["tflops"]
-    traffic = committed_traffic(dom_base, args.workload)
+    traffic = committed_traffic(dom_base, args.workload) if w.D == WORKLOADS_D[args.workload] else None
     cpu = None
     if not args.no_cpu_baseline:
         # every kv group of batch element 0: ~10 s of oracle work on the 16 host cores at C3
@@ -470,6 +481,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c3", choices=["c1", "c2", "c3", "c4", "c5"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--head-dim", type=int, default=None,
+                    help="run the workload with another head dim (measurement lines; the "
+                         "headline is the workload's own)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

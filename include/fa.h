@@ -31,8 +31,11 @@
  * fp32 accuracy. Outputs are written in out_dtype (FA_F32 recommended; FA_BF16
  * rounds O / dQ / dK / dV to bf16 on store). LSE is always fp32, natural log.
  *
- * Supported in this build: D in {64, 128} for FA_BF16 inputs, D == 64 for
- * FA_F32 inputs; other head dims return FA_ERR_UNSUPPORTED.
+ * Supported in this build: head dims D that are multiples of 16, 16 <= D <= 128
+ * for FA_BF16 inputs and 16 <= D <= 64 for FA_F32 inputs (the pages' set 16, 32, 48,
+ * 64, 80, 96, 128 among them); other head dims return FA_ERR_UNSUPPORTED. A D below
+ * 64 / 128 runs in the kernels built for 64 / 128, whose tensor-core work then
+ * includes the zero columns up to that width.
  */
 #ifndef FA_H_
 #define FA_H_

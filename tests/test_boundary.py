@@ -88,9 +88,11 @@ MIS = 0x10008
     (dict(window=-1), 1),
     (dict(in_dtype=7), 1),
     (dict(out_dtype=-1), 1),
-    (dict(D=96), 2),                # head dim not built
-    (dict(D=128, in_dtype=0), 2),   # fp32 inputs only at D=64
-    (dict(D=32), 2),
+    (dict(D=24), 2),                # head dim not a multiple of 16
+    (dict(D=144), 2),               # above 128
+    (dict(D=8), 2),
+    (dict(D=128, in_dtype=0), 2),   # fp32 inputs up to D=64
+    (dict(D=80, in_dtype=0), 2),
 ])
 def test_invalid_params_rejected(fa, kw, code):
     p = _params(fa, **kw)

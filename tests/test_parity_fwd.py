@@ -38,6 +38,19 @@ SMALL = {
     "bf16-many-items-empty": C3.with_(B=1, H=160, HKV=40, Sq=800, Sk=200, window=64, seed=25),
     "f32-many-items-causal": C2.with_(B=1, H=64, HKV=16, Sq=500, Sk=500, seed=26),
     "f32-many-items-empty": C2.with_(B=1, H=64, HKV=16, Sq=600, Sk=150, window=40, seed=27),
+    # head dims below the kernels' 64 / 128 (the missing columns read as zeros)
+    "bf16-d96-causal-gqa": C3.with_(B=1, H=4, HKV=2, Sq=333, Sk=333, D=96, scale=96 ** -0.5, seed=41),
+    "bf16-d80-window": C4.with_(B=1, H=2, HKV=1, Sq=400, Sk=400, D=80, window=100, scale=80 ** -0.5,
+                                seed=42),
+    "bf16-d48-noncausal-sq-ne-sk": C3.with_(B=1, H=2, HKV=2, Sq=200, Sk=300, D=48, causal=False,
+                                            scale=48 ** -0.5, seed=43),
+    "bf16-d32-empty-rows": C3.with_(B=1, H=2, HKV=1, Sq=500, Sk=200, D=32, window=64,
+                                    scale=32 ** -0.5, seed=44),
+    "bf16-d16-causal": C3.with_(B=2, H=2, HKV=1, Sq=150, Sk=150, D=16, scale=0.25, seed=45),
+    "f32-d48-window": C2.with_(B=1, H=2, HKV=1, Sq=260, Sk=260, D=48, window=60, scale=48 ** -0.5,
+                               seed=46),
+    "f32-d32-causal": C2.with_(B=1, H=2, HKV=2, Sq=200, Sk=200, D=32, scale=32 ** -0.5, seed=47),
+    "f32-d16-noncausal": C5.with_(Sq=190, Sk=250, D=16, scale=0.25, seed=48),
 }
 
 
