@@ -43,7 +43,9 @@ struct FwdArgs {
   int causal, window;
   int out_bf16;
   int n_qgroups;
-  int n_items;  // BH * n_qgroups
+  int n_splits;  // key ranges per (query group, head): > 1 writes partial O / LSE per range
+  int tps;       // key tiles per range
+  int n_items;  // BH * n_qgroups * n_splits
   int Dv;       // head dim of the tensors (<= the kernel's D; missing columns read as 0)
   int lpt;  // 1: the heaviest query groups first (causal)
   int BH;
@@ -213,22 +215,31 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
   const int lane = lane_id();
   volatile int* abort_flag = &abort_sh;
 
-  // ---- work items: query group qg (NQ tiles of 128 rows) of head bh, linear index
-  // w = qg_lin * BH + bh (the heads of one kv group adjacent).
-  struct Item { int bh, bg, row0, t_lo, n; };
+  // ---- work items: query group qg (NQ tiles of 128 rows) of head bh, and key range sp
+  // (tiles [sp * tps, (sp + 1) * tps) when the keys are split), linear index
+  // w = (qg_lin * BH + bh) * n_splits + sp (the heads of one kv group adjacent). The
+  // outputs go to slab zo = sp * BH + bh (partial outputs when split).
+  struct Item { int bh, bg, zo, row0, t_lo, n; };
   auto item = [&](int w) {
     Item it;
-    const int qg_lin = w / a.BH;
-    it.bh = w % a.BH;
+    const int sp = w % a.n_splits, wq = w / a.n_splits;
+    const int qg_lin = wq / a.BH;
+    it.bh = wq % a.BH;
+    it.zo = sp * a.BH + it.bh;
     const int qg = a.lpt ? (a.n_qgroups - 1 - qg_lin) : qg_lin;
     const int b = it.bh / a.H, h = it.bh % a.H;
     it.bg = b * a.HKV + h / (a.H / a.HKV);
     it.row0 = qg * (BLOCK_M * NQ);
     int r1 = it.row0 + BLOCK_M * NQ - 1;
     if (r1 > a.Sq - 1) r1 = a.Sq - 1;
-    int hi;
-    kv_tile_range(it.row0, r1, a.Sk, a.causal, a.window, &it.t_lo, &hi);
-    it.n = hi - it.t_lo;
+    int lo, hi;
+    kv_tile_range(it.row0, r1, a.Sk, a.causal, a.window, &lo, &hi);
+    if (a.n_splits > 1) {
+      lo = max(lo, sp * a.tps);
+      hi = min(hi, (sp + 1) * a.tps);
+    }
+    it.t_lo = lo;
+    it.n = hi > lo ? hi - lo : 0;
     return it;
   };
   auto item_w = [&](int k) {
@@ -645,17 +656,17 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
       if (ok) ok = __all_sync(0xffffffffu, wait(&bar_grant[q], k & 1));
       const float inv = (l > 0.f) ? (1.f / l) : 0.f;
       if (ok && i < a.Sq)
-        a.LSE[(size_t)itm.bh * a.Sq + i] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
+        a.LSE[(size_t)itm.zo * a.Sq + i] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
       const int r_base = r0 + wq * 32;
       const uint32_t stage = sV(slot, 0) + wq * C::STAGE_PER_WARP;
       if (q < NQ - 1) {
         if (ok) {
           if (a.out_bf16)
             store_rows_tma<D, true, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                     r_base < a.Sq, itm.bh, 0, a.Dv);
+                                                     r_base < a.Sq, itm.zo, 0, a.Dv);
           else
             store_rows_tma<D, false, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                      r_base < a.Sq, itm.bh, 0, a.Dv);
+                                                      r_base < a.Sq, itm.zo, 0, a.Dv);
         }
         named_bar_sync(C::EPI_BAR0 + q, 128);
         if (wq == 0 && lane == 0) mbar_arrive(&bar_grant[q + 1]);
@@ -663,10 +674,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         if (ok) {
           if (a.out_bf16)
             store_rows_tma<D, true, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                            r_base < a.Sq, itm.bh, 0, a.Dv);
+                                                            r_base < a.Sq, itm.zo, 0, a.Dv);
           else
             store_rows_tma<D, false, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage,
-                                                             r_base, r_base < a.Sq, itm.bh, 0, a.Dv);
+                                                             r_base, r_base < a.Sq, itm.zo, 0, a.Dv);
         }
         pending = true;
         pend_slot = slot;
@@ -694,6 +705,45 @@ __global__ void fill_empty_kernel(void* O, float* LSE, size_t rows, int D, int o
       for (int d = 0; d < D; ++d) static_cast<__nv_bfloat16*>(O)[r * D + d] = __float2bfloat16(0.f);
     } else {
       for (int d = 0; d < D; ++d) static_cast<float*>(O)[r * D + d] = 0.f;
+    }
+  }
+}
+
+// Key ranges of one (query group, head) computed separately: partial outputs O_s
+// (each normalised by its own row sum) and natural-log LSE_s per range, slab
+// s * rows + r. The row's result is the softmax over all its keys:
+//   LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
+// (ranges with no visible key have LSE_s = -inf and weigh 0; a row with none at all
+// gets O = 0, LSE = -inf). One warp per row, ranges summed in order (deterministic).
+__global__ void combine_splits_kernel(const float* __restrict__ Op, const float* __restrict__ Lp,
+                                      void* __restrict__ O, float* __restrict__ LSE, int n_splits,
+                                      size_t rows, int Dv, int out_bf16) {
+  const int lane = threadIdx.x & 31;
+  const size_t warps = (size_t)gridDim.x * (blockDim.x / 32);
+  for (size_t r = blockIdx.x * (size_t)(blockDim.x / 32) + threadIdx.x / 32; r < rows; r += warps) {
+    float mx = -INFINITY;
+    for (int sp = 0; sp < n_splits; ++sp) mx = fmaxf(mx, Lp[sp * rows + r]);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // columns lane + 32 c, Dv <= 128
+    float sum = 0.f;
+    if (mx > -INFINITY) {
+      for (int sp = 0; sp < n_splits; ++sp) {
+        const float ls = Lp[sp * rows + r];
+        const float wgt = ls == -INFINITY ? 0.f : expf(ls - mx);
+        sum += wgt;
+        const float* src = Op + (sp * rows + r) * Dv;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (lane + 32 * c < Dv) acc[c] += wgt * src[lane + 32 * c];
+      }
+    }
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    if (lane == 0) LSE[r] = sum > 0.f ? mx + logf(sum) : -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int d = lane + 32 * c;
+      if (d >= Dv) break;
+      if (out_bf16) static_cast<__nv_bfloat16*>(O)[r * Dv + d] = __float2bfloat16(acc[c] * inv);
+      else static_cast<float*>(O)[r * Dv + d] = acc[c] * inv;
     }
   }
 }
@@ -775,12 +825,45 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   a.window = p.window;
   a.out_bf16 = p.out_dtype == FA_BF16;
   a.n_qgroups = (p.Sq + BLOCK_M * C::NQ - 1) / (BLOCK_M * C::NQ);
-  a.n_items = (int)BHq * a.n_qgroups;
+  // Fewer (query group, head) items than SMs -- short query sequences: split each
+  // item's keys into ranges of tps tiles (each range a work item writing a partial O
+  // and LSE, combined afterwards), enough for about two items per SM.
+  const int sms = host::sm_count();
+  const int n_kt = (p.Sk + BLOCK_N - 1) / BLOCK_N;
+  const int base_items = (int)BHq * a.n_qgroups;
+  a.n_splits = 1;
+  a.tps = n_kt;
+  if (base_items < sms && n_kt >= 8) {
+    const int want = std::min({16, (2 * sms + base_items - 1) / base_items, n_kt / 4});
+    if (want > 1) {
+      a.tps = (n_kt + want - 1) / want;
+      a.n_splits = (n_kt + a.tps - 1) / a.tps;
+    }
+  }
+  a.n_items = base_items * a.n_splits;
   a.Dv = Dv;
   a.lpt = p.causal ? 1 : 0;
   a.BH = (int)BHq;
   a.limit_ns = WAIT_LIMIT_NS;
-  const unsigned grid = (unsigned)std::min(a.n_items, host::sm_count());
+  void* pws = nullptr;  // partial O [splits][BH][Sq][Dv] and LSE [splits][BH][Sq], fp32
+  const size_t rows = (size_t)BHq * p.Sq;
+  if (a.n_splits > 1) {
+    const size_t o_floats = (size_t)a.n_splits * rows * Dv;
+    if (host::scratch_alloc(&pws, (o_floats + (size_t)a.n_splits * rows) * 4, stream) != cudaSuccess) {
+      host::scratch_free(ws, stream);
+      return FA_ERR_CUDA;
+    }
+    a.O = pws;
+    a.LSE = static_cast<float*>(pws) + o_floats;
+    a.out_bf16 = 0;
+    if (!host::encode_tiled_3d(&mO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pws, Dv, p.Sq,
+                               (uint64_t)a.n_splits * BHq, Dv, 32, 32)) {
+      host::scratch_free(pws, stream);
+      host::scratch_free(ws, stream);
+      return FA_ERR_CUDA;
+    }
+  }
+  const unsigned grid = (unsigned)std::min(a.n_items, sms);
   auto kern = fa_fwd_kernel<D, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_ALLOC);
@@ -791,8 +874,17 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
     kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, mO, a);
     e = cudaGetLastError();
   }
+  if (e == cudaSuccess && a.n_splits > 1) {
+    host::KernelTimer kt("combine_splits", stream);
+    const float* op = static_cast<const float*>(pws);
+    combine_splits_kernel<<<4 * sms, 256, 0, stream>>>(op, op + (size_t)a.n_splits * rows * Dv, O,
+                                                       LSE, a.n_splits, rows, Dv,
+                                                       p.out_dtype == FA_BF16);
+    e = cudaGetLastError();
+  }
   cudaError_t e2 = host::scratch_free(ws, stream);
-  return (e == cudaSuccess && e2 == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
+  const cudaError_t e3 = host::scratch_free(pws, stream);
+  return (e == cudaSuccess && e2 == cudaSuccess && e3 == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace
@@ -982,6 +1074,8 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
   a.window = p.window;
   a.out_bf16 = p.out_dtype == FA_BF16;
   a.n_qgroups = (p.Sq + BLOCK_M * C::NQ - 1) / (BLOCK_M * C::NQ);
+  a.n_splits = 1;  // (split keys need scratch for the partial outputs)
+  a.tps = (p.Sk + BLOCK_N - 1) / BLOCK_N;
   a.n_items = (int)BHq * a.n_qgroups;
   a.Dv = Dv;
   a.lpt = p.causal ? 1 : 0;

@@ -168,10 +168,11 @@ def oracle_sample(w, n_groups, batch=0):
     return (fwd + bwd) / dt / 1e12, dt, oracle.num_threads(), n_groups * rep
 
 
-def config_of(w, extra=None):
+def config_of(w, out_dtype="f32", extra=None):
     c = {"workload": w.name, "B": w.B, "H": w.H, "HKV": w.HKV, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
          "causal": bool(w.causal), "window": w.window, "scale": w.scale, "in_dtype": w.dtype,
-         "out_dtype": "f32", "l2": "256 MiB memset between timed steps; inputs also exceed L2"}
+         "out_dtype": out_dtype,
+         "l2": "256 MiB memset between timed steps; inputs also exceed L2"}
     if extra:
         c.update(extra)
     return c
@@ -184,6 +185,10 @@ def workload_of(args):
     if args.head_dim and args.head_dim != w.D:
         w = w.with_(D=args.head_dim, scale=args.head_dim ** -0.5,
                     name=w.name.replace(f"-d{w.D}-", f"-d{args.head_dim}-"))
+    if args.sq and args.sq != w.Sq:  # short query sequence against the same keys
+        w = w.with_(Sq=args.sq, name=f"{w.name}-sq{args.sq}")
+    if args.non_causal and w.causal:
+        w = w.with_(causal=False, window=0, name=f"{w.name}-noncausal")
     return w
 
 
@@ -208,7 +213,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_of(w),
+            "data": "synthetic", "config": config_of(w, args.out_dtype),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -259,12 +264,13 @@ def run_ours(args, rank, world, local_rank):
     wr = rank_workload(w, rank)
     q, k, v, do = make_inputs(wr)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
-    p = fa.make_params(qd, kd, w.scale, w.causal, w.window)
-    o = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    odt = torch.bfloat16 if args.out_dtype == "bf16" else torch.float32
+    p = fa.make_params(qd, kd, w.scale, w.causal, w.window, out_dtype=odt)
+    o = torch.empty(q.shape, dtype=odt, device=dev)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
-    dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
-    dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+    dq = torch.empty(q.shape, dtype=odt, device=dev)
+    dk = torch.empty(k.shape, dtype=odt, device=dev)
+    dv = torch.empty(v.shape, dtype=odt, device=dev)
     stream = torch.cuda.current_stream()
     sh = int(stream.cuda_stream)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -434,7 +440,9 @@ def run_ours(args, rank, world, local_rank):
               key=lambda k_: per_kernel[k_]["launches"] * per_kernel[k_]["ms_per_launch"])
     dom_base = dom.split("<")[0]
     achieved = per_kernel[dom]["tflops"]
-    traffic = committed_traffic(dom_base, args.workload) if w.D == WORKLOADS_D[args.workload] else None
+    traffic = (committed_traffic(dom_base, args.workload)
+               if w.D == WORKLOADS_D[args.workload] and args.out_dtype == "f32" and not args.sq
+               and not args.non_causal else None)
     cpu = None
     if not args.no_cpu_baseline:
         # every kv group of batch element 0: ~10 s of oracle work on the 16 host cores at C3
@@ -447,7 +455,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-        "data": "synthetic", "config": config_of(w),
+        "data": "synthetic", "config": config_of(w, args.out_dtype),
         "fwd_tflops": round(fwd_fl / (fwd_ms * 1e-3) / 1e12, 3) if fwd_ms else None,
         # the backward's share of the step: step time minus the forward kernels' time
         # (its dK / dV and dQ kernels overlap inside the step)
@@ -481,6 +489,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c3", choices=["c1", "c2", "c3", "c4", "c5"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sq", type=int, default=None,
+                    help="query rows per head (measurement lines, e.g. decode-shaped)")
+    ap.add_argument("--non-causal", action="store_true",
+                    help="full attention over the keys (measurement lines)")
+    ap.add_argument("--out-dtype", choices=["f32", "bf16"], default="f32",
+                    help="dtype of O, dQ, dK, dV (measurement lines; the headline is f32)")
     ap.add_argument("--head-dim", type=int, default=None,
                     help="run the workload with another head dim (measurement lines; the "
                          "headline is the workload's own)")

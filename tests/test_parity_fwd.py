@@ -51,6 +51,13 @@ SMALL = {
                                seed=46),
     "f32-d32-causal": C2.with_(B=1, H=2, HKV=2, Sq=200, Sk=200, D=32, scale=32 ** -0.5, seed=47),
     "f32-d16-noncausal": C5.with_(Sq=190, Sk=250, D=16, scale=0.25, seed=48),
+    # short query sequences against long key sequences: fewer work items than SMs, so
+    # each item's keys are split into ranges whose partial results are combined
+    "bf16-decode-gqa": C3.with_(B=2, H=8, HKV=2, Sq=64, Sk=3000, causal=False, seed=51),
+    "bf16-decode-causal-sq-lt-sk": C3.with_(B=1, H=4, HKV=2, Sq=130, Sk=2000, seed=52),
+    "bf16-decode-d96": C3.with_(B=1, H=4, HKV=1, Sq=32, Sk=4000, D=96, causal=False,
+                                scale=96 ** -0.5, seed=53),
+    "f32-decode": C5.with_(Sq=100, Sk=4000, seed=54),
 }
 
 
