@@ -49,6 +49,8 @@ struct BwdArgs {
   int lpt;
   int Dv;      // head dim of the tensors (<= the kernel's D; missing columns read as 0)
   int* sched;  // dq (bf16 inputs): work-item counter, zero at launch
+  int n_splits;  // dq (bf16 inputs): key ranges per query tile; > 1 writes partial dQ per range
+  int tps;       // key tiles per range
   unsigned long long limit_ns;
 };
 
@@ -768,9 +770,11 @@ __device__ __forceinline__ void stage_store_rows(const uint32_t (&r)[NCOL], floa
 // per-item phases can only complete after every role has observed the one before
 // (e.g. q_rel(j+1) follows S MMAs of item j+1, which need Q_{j+1}, loaded only after
 // q_rel(j) was seen), so a parity wait never misses a phase. An item whose rows see
-// no key touches none of these barriers and writes nothing: the launcher zeroes those
-// dQ rows beforehand.
-template <int D>
+// no key (in its key range) touches none of these barriers and writes nothing: the
+// launcher zeroes those dQ rows beforehand, or, with the keys split into ranges, the
+// sum over the ranges leaves that range out. SPLIT: the keys are split into ranges (a
+// separate instantiation, so the unsplit kernel's code is not touched by it).
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     fa_bwd_dq16_kernel(const __grid_constant__ QMaps m, const BwdArgs a) {
   using C = Dq16Cfg<D>;
@@ -788,18 +792,28 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
   const int warp = warp_id(), lane = lane_id();
   volatile int* abort_flag = &abort_sh;
 
-  const int n_items = a.n_tiles * a.BHx;
+  // Work item w = (qt_lin * BH + bh) * n_splits + sp: query tile, head and (SPLIT) key
+  // range sp, key tiles [sp * tps, (sp + 1) * tps); dQ goes to slab zo = sp * BH + bh
+  // (the partial sum over one key range when split, else dQ itself).
+  const int n_items = a.n_tiles * a.BHx * (SPLIT ? a.n_splits : 1);
   struct Item { int bh, bg, i0, kt_lo, nc; };
   auto item = [&](int w) {
     Item it;
-    const int qt_lin = w / a.BHx;
-    it.bh = w % a.BHx;
+    const int wq = SPLIT ? w / a.n_splits : w;
+    const int qt_lin = wq / a.BHx;
+    it.bh = wq % a.BHx;
     const int qt = a.lpt ? (a.n_tiles - 1 - qt_lin) : qt_lin;
     const int b = it.bh / a.H, h = it.bh % a.H;
     it.bg = b * a.HKV + h / (a.H / a.HKV);
     it.i0 = qt * BLOCK_M;
     int hi;
     kv_tile_range(it.i0, min(it.i0 + BLOCK_M - 1, a.Sq - 1), a.Sk, a.causal, a.window, &it.kt_lo, &hi);
+    if constexpr (SPLIT) {
+      const int sp = w % a.n_splits;
+      it.kt_lo = max(it.kt_lo, sp * a.tps);
+      hi = min(hi, (sp + 1) * a.tps);
+      if (hi < it.kt_lo) hi = it.kt_lo;
+    }
     it.nc = hi - it.kt_lo;
     return it;
   };
@@ -1141,7 +1155,8 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         mbar_arrive(&bar_dqfree);  // dQ has left TMEM: the next item may accumulate
         if (mine)
           stage_store_rows<NCOL, BF>(r, a.scale, sbase + C::V_OFF + warp * (C::EPI_WARP / 2),
-                                     &m.dQ, x0, r_base, any, it.bh, a.Dv);
+                                     &m.dQ, x0, r_base, any,
+                                     SPLIT ? (w % a.n_splits) * a.BHx + it.bh : it.bh, a.Dv);
       };
       if (a.out_bf16) epilogue(std::true_type{});
       else epilogue(std::false_type{});
@@ -1716,6 +1731,53 @@ __global__ void bwd_prepass16_kernel(const __nv_bfloat16* __restrict__ dO, const
   }
 }
 
+// Key ranges of a query tile computed as separate dQ work items (few query tiles per
+// SM): dQ = sum_s dQ_s over the ranges s that hold a key tile the query tile can see
+// (exactly the ranges whose work items wrote their slab), summed in range order, so
+// the result is deterministic; rows of a tile that sees no key get 0. One thread per
+// 4 columns of a row; partial slab s holds rows (bh, i) of range s.
+__global__ void dq_range_sum_kernel(const float* __restrict__ part, void* __restrict__ dQ,
+                                    int tps, int BH, int Sq, int Sk, int causal, int window, int Dv,
+                                    int out_bf16) {
+  const int q4 = Dv / 4;
+  const size_t rows = (size_t)BH * Sq, n = rows * q4, slab = rows * Dv;
+  for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n;
+       t += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = t / q4;
+    const int c = (int)(t % q4) * 4;
+    const int i0 = (int)(r % Sq) / BLOCK_M * BLOCK_M;
+    int lo, hi;
+    kv_tile_range(i0, min(i0 + BLOCK_M - 1, Sq - 1), Sk, causal, window, &lo, &hi);
+    // range s covers key tiles [s * tps, (s + 1) * tps): it meets [lo, hi) for s in
+    // [lo / tps, (hi - 1) / tps]
+    const int s_lo = lo / tps, n_s = hi > lo ? (hi - 1) / tps + 1 - s_lo : 0;
+    const float* src = part + (size_t)s_lo * slab + r * Dv + c;
+    float4 v[MAX_KEY_RANGES];  // every range's load issued before any is used
+#pragma unroll
+    for (int k = 0; k < MAX_KEY_RANGES; ++k)
+      if (k < n_s) v[k] = *reinterpret_cast<const float4*>(src + k * slab);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < MAX_KEY_RANGES; ++k) {
+      if (k < n_s) {
+        acc.x += v[k].x;
+        acc.y += v[k].y;
+        acc.z += v[k].z;
+        acc.w += v[k].w;
+      }
+    }
+    if (out_bf16) {
+      __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y), hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo2);
+      u.y = *reinterpret_cast<uint32_t*>(&hi2);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dQ) + r * Dv + c) = u;
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(dQ) + r * Dv + c) = acc;
+    }
+  }
+}
+
 // Zero-fill outputs of an empty side (Sq == 0 or Sk == 0).
 __global__ void zero_kernel(uint4* p, size_t n16) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16;
@@ -1745,12 +1807,29 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   else bytes += (4 * nq + 4 * nk + 4 * nqt + 2 * nkt) * 4;  // Q,dO,K,V hi/lo + Q^T,dO^T,K^T hi/lo
   const size_t sched_off = (bytes + 15) / 16 * 16;  // the dQ kernel's work-item counter
   bytes = sched_off + 16;
+  // Fewer query tiles than SMs (short query sequences, bf16 inputs): the dQ work items
+  // also split the keys into ranges of tps tiles -- about two items per SM -- each
+  // range writing a partial dQ (fp32) that a sum kernel adds up afterwards.
+  const int sms = host::sm_count();
+  const int n_qt = (p.Sq + BLOCK_M - 1) / BLOCK_M, n_kt = (p.Sk + BLOCK_N - 1) / BLOCK_N;
+  int dq_splits = 1, dq_tps = n_kt;
+  if (!F32 && BH * n_qt < (size_t)sms && n_kt >= 8) {
+    const int base = (int)BH * n_qt;
+    const int want = std::min({MAX_KEY_RANGES, (2 * sms + base - 1) / base, n_kt / 4});
+    if (want > 1) {
+      dq_tps = (n_kt + want - 1) / want;
+      dq_splits = (n_kt + dq_tps - 1) / dq_tps;
+    }
+  }
+  const size_t part_off = (bytes + 255) / 256 * 256;  // partial dQ [splits][BH][Sq][Dv]
+  if (dq_splits > 1) bytes = part_off + (size_t)dq_splits * nq * 4;
   void* ws = nullptr;
   if (host::scratch_alloc(&ws, bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
   float* lse2 = static_cast<float*>(ws);
   float* delta = lse2 + nvec;
   int* sched = reinterpret_cast<int*>(static_cast<char*>(ws) + sched_off);
-  const int grid_pp = 4 * host::sm_count();
+  float* dq_part = dq_splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(ws) + part_off) : nullptr;
+  const int grid_pp = 4 * sms;
   const auto F32T = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   KVMaps mk;
   QMaps mq;
@@ -1763,7 +1842,11 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     const int oes = bf ? 2 : 4;
     enc &= host::encode_tiled_3d(&mk.dK, odt, oes, dK, Dv, p.Sk, BHk, Dv, 128 / oes, 32);
     enc &= host::encode_tiled_3d(&mk.dV, odt, oes, dV, Dv, p.Sk, BHk, Dv, 128 / oes, 32);
-    enc &= host::encode_tiled_3d(&mq.dQ, odt, oes, dQ, Dv, p.Sq, BH, Dv, 128 / oes, 32);
+    if (dq_splits > 1)
+      enc &= host::encode_tiled_3d(&mq.dQ, F32T, 4, dq_part, Dv, p.Sq, (uint64_t)dq_splits * BH, Dv,
+                                   32, 32);
+    else
+      enc &= host::encode_tiled_3d(&mq.dQ, odt, oes, dQ, Dv, p.Sq, BH, Dv, 128 / oes, 32);
   }
   enc &= host::encode_tiled_3d(&mk.Dl, F32T, 4, delta, ldq, BH, 1, ldq, qchunk, 1, false);
   if constexpr (!F32) {
@@ -1780,9 +1863,9 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     }
     // Query tiles whose rows see no key (a window ending before the keys do: a suffix
     // of tiles) are skipped by the dQ kernel; their rows are zeroed here, before the
-    // dK/dV launch (nothing may come between it and its dependent dQ launch).
-    {
-      const int n_qt = (p.Sq + BLOCK_M - 1) / BLOCK_M;
+    // dK/dV launch (nothing may come between it and its dependent dQ launch). With
+    // the keys split into ranges, the sum over the ranges writes them instead.
+    if (dq_splits == 1) {
       int t0 = n_qt;
       while (t0 > 0) {
         int lo, hi;
@@ -1880,6 +1963,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   a.lpt = p.causal;
   a.Dv = Dv;
   a.sched = sched;
+  a.n_splits = 1;
+  a.tps = n_kt;
   a.limit_ns = WAIT_LIMIT_NS;
   cudaError_t e = cudaSuccess;
   {
@@ -1913,8 +1998,11 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   }
   if (e == cudaSuccess) {
     BwdArgs aq = a;
-    aq.n_tiles = (p.Sq + BLOCK_M - 1) / BLOCK_M;
+    aq.n_tiles = n_qt;
     aq.BHx = (int)BH;
+    aq.n_splits = dq_splits;
+    aq.tps = dq_tps;
+    if (dq_splits > 1) aq.out_bf16 = 0;  // the partial sums are fp32
     if constexpr (F32) {
       auto kern = fa_bwd_dq_kernel<D, F32>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::Q_SMEM);
@@ -1925,7 +2013,7 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       }
     } else {
       using C16 = Dq16Cfg<D>;
-      auto kern = fa_bwd_dq16_kernel<D>;
+      auto kern = dq_splits > 1 ? fa_bwd_dq16_kernel<D, true> : fa_bwd_dq16_kernel<D, false>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C16::SMEM);
       if (e == cudaSuccess) {
         host::KernelTimer kt(D == 128 ? "fa_bwd_dq_kernel<128,bf16>" : "fa_bwd_dq_kernel<64,bf16>",
@@ -1936,8 +2024,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
         // has started, on the SMs that dK / dV's last wave leaves idle, and each waits
         // for the dK / dV grid to complete before it exits, so the dQ grid's completion
         // (which the rest of the stream waits for) implies dK / dV's.
-        const size_t n_items = BH * (size_t)aq.n_tiles;
-        const unsigned grid = (unsigned)std::min<size_t>(n_items, (size_t)host::sm_count());
+        const size_t n_items = BH * (size_t)aq.n_tiles * dq_splits;
+        const unsigned grid = (unsigned)std::min<size_t>(n_items, (size_t)sms);
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
         cfg.blockDim = dim3(C16::THREADS);
@@ -1950,6 +2038,13 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, kern, mq, aq);
         if (e == cudaSuccess) e = cudaGetLastError();
+      }
+      if (e == cudaSuccess && dq_splits > 1) {
+        host::KernelTimer kt("dq_range_sum", stream);
+        dq_range_sum_kernel<<<grid_pp, 256, 0, stream>>>(dq_part, dQ, dq_tps, (int)BH, p.Sq, p.Sk,
+                                                         p.causal, p.window, Dv,
+                                                         p.out_dtype == FA_BF16);
+        e = cudaGetLastError();
       }
     }
   }

@@ -17,6 +17,9 @@ constexpr float LN2 = 0.6931471805599453f;
 // Rescale O only when the running max grows by more than this (log2 units): the
 // unnormalised probabilities then stay below 2^8, well inside fp16 range.
 constexpr float RESCALE_THRESHOLD = 8.0f;
+// Short query sequences split each work item's keys into at most this many ranges
+// (forward and dQ), whose partial results a combine kernel adds up.
+constexpr int MAX_KEY_RANGES = 16;
 
 // Status bits a kernel may set in its device status word.
 enum : unsigned int {

@@ -714,36 +714,58 @@ __global__ void fill_empty_kernel(void* O, float* LSE, size_t rows, int D, int o
 // s * rows + r. The row's result is the softmax over all its keys:
 //   LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
 // (ranges with no visible key have LSE_s = -inf and weigh 0; a row with none at all
-// gets O = 0, LSE = -inf). One warp per row, ranges summed in order (deterministic).
+// gets O = 0, LSE = -inf). Ranges are summed in order (deterministic). One thread per
+// 4 columns of a row; it issues the loads of all (at most 16) ranges before using
+// any, so a row costs one round trip to L2, where the partials still are.
 __global__ void combine_splits_kernel(const float* __restrict__ Op, const float* __restrict__ Lp,
                                       void* __restrict__ O, float* __restrict__ LSE, int n_splits,
                                       size_t rows, int Dv, int out_bf16) {
-  const int lane = threadIdx.x & 31;
-  const size_t warps = (size_t)gridDim.x * (blockDim.x / 32);
-  for (size_t r = blockIdx.x * (size_t)(blockDim.x / 32) + threadIdx.x / 32; r < rows; r += warps) {
-    float mx = -INFINITY;
-    for (int sp = 0; sp < n_splits; ++sp) mx = fmaxf(mx, Lp[sp * rows + r]);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // columns lane + 32 c, Dv <= 128
-    float sum = 0.f;
-    if (mx > -INFINITY) {
-      for (int sp = 0; sp < n_splits; ++sp) {
-        const float ls = Lp[sp * rows + r];
-        const float wgt = ls == -INFINITY ? 0.f : expf(ls - mx);
-        sum += wgt;
-        const float* src = Op + (sp * rows + r) * Dv;
+  const int q4 = Dv / 4;
+  const size_t n = rows * q4;
+  for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n;
+       t += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = t / q4;
+    const int c = (int)(t % q4) * 4;
+    float ls[MAX_KEY_RANGES];
+    float4 ov[MAX_KEY_RANGES];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (lane + 32 * c < Dv) acc[c] += wgt * src[lane + 32 * c];
+    for (int sp = 0; sp < MAX_KEY_RANGES; ++sp) {
+      if (sp < n_splits) {
+        ls[sp] = Lp[sp * rows + r];
+        ov[sp] = *reinterpret_cast<const float4*>(Op + (sp * rows + r) * Dv + c);
+      }
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int sp = 0; sp < MAX_KEY_RANGES; ++sp)
+      if (sp < n_splits) mx = fmaxf(mx, ls[sp]);
+    // (no branch on mx, so that the partial-O loads need not wait for the LSE ones:
+    // a range with no visible key has LSE_s = -inf, weight 0 and O_s = 0 written)
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float sum = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < MAX_KEY_RANGES; ++sp) {
+      if (sp < n_splits) {
+        const float wgt = ls[sp] == -INFINITY ? 0.f : expf(ls[sp] - mx);
+        sum += wgt;
+        acc.x += wgt * ov[sp].x;
+        acc.y += wgt * ov[sp].y;
+        acc.z += wgt * ov[sp].z;
+        acc.w += wgt * ov[sp].w;
       }
     }
     const float inv = sum > 0.f ? 1.f / sum : 0.f;
-    if (lane == 0) LSE[r] = sum > 0.f ? mx + logf(sum) : -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int d = lane + 32 * c;
-      if (d >= Dv) break;
-      if (out_bf16) static_cast<__nv_bfloat16*>(O)[r * Dv + d] = __float2bfloat16(acc[c] * inv);
-      else static_cast<float*>(O)[r * Dv + d] = acc[c] * inv;
+    if (c == 0) LSE[r] = sum > 0.f ? mx + logf(sum) : -INFINITY;
+    if (out_bf16) {
+      __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo2);
+      u.y = *reinterpret_cast<uint32_t*>(&hi2);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(O) + r * Dv + c) = u;
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(O) + r * Dv + c) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
   }
 }
@@ -834,7 +856,7 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   a.n_splits = 1;
   a.tps = n_kt;
   if (base_items < sms && n_kt >= 8) {
-    const int want = std::min({16, (2 * sms + base_items - 1) / base_items, n_kt / 4});
+    const int want = std::min({MAX_KEY_RANGES, (2 * sms + base_items - 1) / base_items, n_kt / 4});
     if (want > 1) {
       a.tps = (n_kt + want - 1) / want;
       a.n_splits = (n_kt + a.tps - 1) / a.tps;

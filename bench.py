@@ -40,6 +40,8 @@ KERNEL_FLOPS_PER_PAIR_PER_D = {"fa_fwd_kernel": 4, "fa_bwd_dkdv_kernel": 8, "fa_
 # Source files whose change invalidates a committed DRAM-traffic figure.
 _COMMON_SOURCES = ["ptx.cuh", "fa_common.cuh", "fa_epilogue.cuh", "fa_prepass.cuh"]
 # head dim of each named workload (traffic figures in profiles/ are for these)
+# fa_fwd's launches besides its kernel (operand conversion, the key-range combine)
+FWD_AUX_KERNELS = ("cvt_bf16_to_f16(V)", "split_tf32(Q,K,V)", "combine_splits")
 WORKLOADS_D = {"c1": 64, "c2": 64, "c3": 128, "c4": 128, "c5": 64}
 KERNEL_SOURCES = {"fa_fwd_kernel": ["fa_fwd.cu"] + _COMMON_SOURCES,
                   "fa_bwd_dkdv_kernel": ["fa_bwd.cu"] + _COMMON_SOURCES,
@@ -434,7 +436,7 @@ def run_ours(args, rank, world, local_rank):
             fl = KERNEL_FLOPS_PER_PAIR_PER_D[base] * w.B * w.H * vis * w.D
             entry["tflops"] = fl / (tot / n * 1e-3) / 1e12
         per_kernel[name] = entry
-        if base.startswith("fa_fwd") or "(V)" in name or "split" in name:
+        if base.startswith("fa_fwd") or name in FWD_AUX_KERNELS:
             fwd_ms += tot / n
     dom = max((k_ for k_ in per_kernel if "tflops" in per_kernel[k_]),
               key=lambda k_: per_kernel[k_]["launches"] * per_kernel[k_]["ms_per_launch"])
@@ -465,8 +467,9 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16 sustained (MEASURED_PEAKS.json)"
-                     if peak_src == "measured" else "fallback 1.7 PFLOP/s sustained"},
+                     "peak_source": (f"{peak_src} bf16 sustained (MEASURED_PEAKS.json)"
+                                     if peak_src == "measured" else "fallback 1.7 PFLOP/s sustained")
+                     + ("" if w.dtype == "bf16" else " x 1/2, the nominal tf32 / bf16 rate ratio")},
         "kernels": {k_: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
                          for kk, vv in e.items()} for k_, e in per_kernel.items()},
         "e2e": {"value": round(whole_job_tflops(fwd_fl + bwd_fl, world, ms_e2e), 3),

@@ -18,6 +18,9 @@ CASES = {
     "bf16-causal-gqa": WORKLOADS["c3"].with_(B=1, H=8, HKV=2, Sq=700, Sk=700, seed=31),
     "bf16-window": WORKLOADS["c4"].with_(B=1, H=4, HKV=1, Sq=900, Sk=900, window=200, seed=33),
     "f32-causal": WORKLOADS["c2"].with_(B=1, H=4, HKV=2, Sq=300, Sk=300, seed=32),
+    # short queries: forward and dQ split the keys into ranges (scratch for the partial
+    # results allocated and freed inside the graph)
+    "bf16-decode": WORKLOADS["c3"].with_(B=1, H=4, HKV=2, Sq=100, Sk=2500, causal=False, seed=34),
 }
 
 

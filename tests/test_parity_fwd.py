@@ -58,6 +58,12 @@ SMALL = {
     "bf16-decode-d96": C3.with_(B=1, H=4, HKV=1, Sq=32, Sk=4000, D=96, causal=False,
                                 scale=96 ** -0.5, seed=53),
     "f32-decode": C5.with_(Sq=100, Sk=4000, seed=54),
+    # window ending before the keys do, with the dQ keys split into ranges: tile 10
+    # sees only the last range, tile 11 no key at all (its dQ rows must come out 0)
+    "bf16-decode-window-empty-tail": C4.with_(B=1, H=4, HKV=1, Sq=1500, Sk=1200, window=100,
+                                              seed=55),
+    # the decode-shaped measurement line's launch: 128 queries against 16384 keys
+    "bf16-decode-sq128-sk16384": C4.with_(Sq=128, causal=False, window=0, seed=56),
 }
 
 
