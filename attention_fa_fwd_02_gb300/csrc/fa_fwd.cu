@@ -49,6 +49,7 @@ struct FwdArgs {
   int Dv;       // head dim of the tensors (<= the kernel's D; missing columns read as 0)
   int lpt;  // 1: the heaviest query groups first (causal)
   int BH;
+  int BHi;  // work units per query group: heads (BH), or head pairs (BH / 2)
   unsigned long long limit_ns;
 };
 
@@ -195,7 +196,13 @@ __device__ __forceinline__ void issue_v_load(uint8_t* smem, int it, int t, int b
 // A phase of a per-item barrier can only complete after every role has observed the
 // previous one (Q_q of item j+1 loads only after the last S MMA of item j completed,
 // which needs Q_q of item j), so a parity wait never misses a phase.
-template <int D, bool F32>
+//
+// HP (head pairs, NQ = 2 only): the two query tiles of an item are the same 128 rows
+// of two query heads of one kv head, which read the same K / V tiles, instead of two
+// consecutive row tiles of one head. Both tiles then need exactly the item's key
+// tiles (two row tiles of a causal or windowed item need different ones, so one of
+// them computes a tile that is masked for it), and at Sq <= 128 no tile is padding.
+template <int D, bool F32, bool HP>
 __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKlo,
@@ -215,22 +222,26 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
   const int lane = lane_id();
   volatile int* abort_flag = &abort_sh;
 
-  // ---- work items: query group qg (NQ tiles of 128 rows) of head bh, and key range sp
-  // (tiles [sp * tps, (sp + 1) * tps) when the keys are split), linear index
-  // w = (qg_lin * BH + bh) * n_splits + sp (the heads of one kv group adjacent). The
-  // outputs go to slab zo = sp * BH + bh (partial outputs when split).
+  // ---- work items: query group qg (NQ tiles of 128 rows of head bh, or with HP 128
+  // rows of heads bh, bh + 1) and key range sp (tiles [sp * tps, (sp + 1) * tps) when
+  // the keys are split), linear index w = (qg_lin * BHi + u) * n_splits + sp, u the
+  // head (pair), so the heads of one kv group are adjacent. Tile q's outputs go to
+  // slab zo (+ q with HP), zo = sp * BH + bh (partial outputs when split).
+  constexpr int ITEM_ROWS = HP ? BLOCK_M : BLOCK_M * NQ;
+  static_assert(!HP || NQ == 2, "head pairs need two query tiles per item");
   struct Item { int bh, bg, zo, row0, t_lo, n; };
   auto item = [&](int w) {
     Item it;
     const int sp = w % a.n_splits, wq = w / a.n_splits;
-    const int qg_lin = wq / a.BH;
-    it.bh = wq % a.BH;
+    const int qg_lin = wq / a.BHi;
+    const int u = wq % a.BHi;
+    it.bh = HP ? 2 * u : u;
     it.zo = sp * a.BH + it.bh;
     const int qg = a.lpt ? (a.n_qgroups - 1 - qg_lin) : qg_lin;
     const int b = it.bh / a.H, h = it.bh % a.H;
     it.bg = b * a.HKV + h / (a.H / a.HKV);
-    it.row0 = qg * (BLOCK_M * NQ);
-    int r1 = it.row0 + BLOCK_M * NQ - 1;
+    it.row0 = qg * ITEM_ROWS;
+    int r1 = it.row0 + ITEM_ROWS - 1;
     if (r1 > a.Sq - 1) r1 = a.Sq - 1;
     int lo, hi;
     kv_tile_range(it.row0, r1, a.Sk, a.causal, a.window, &lo, &hi);
@@ -272,8 +283,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         for (int sp = 0; sp < C::NSPLIT; ++sp)
           for (int cb = 0; cb < C::NCB; ++cb)
             tma_load_3d(smem + C::Q_OFF + (q * C::NSPLIT + sp) * C::TILE_BYTES + cb * C::CB_BYTES,
-                        sp ? &tmQlo : &tmQ, &bar_q[q], cb * C::ROW_ELEMS, first.row0 + q * BLOCK_M,
-                        first.bh);
+                        sp ? &tmQlo : &tmQ, &bar_q[q], cb * C::ROW_ELEMS,
+                        first.row0 + (HP ? 0 : q * BLOCK_M), first.bh + (HP ? q : 0));
       }
       issue_k_load<C>(smem, 0, first.t_lo, first.bg, &tmK, &tmKlo, bar_kfull);
       issue_v_load<C>(smem, 0, first.t_lo, first.bg, &tmV, &tmVlo, bar_vfull);
@@ -326,8 +337,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
               for (int sp = 0; sp < C::NSPLIT; ++sp)
                 for (int cb = 0; cb < C::NCB; ++cb)
                   tma_load_3d(smem + C::Q_OFF + (q * C::NSPLIT + sp) * C::TILE_BYTES + cb * C::CB_BYTES,
-                              sp ? &tmQlo : &tmQ, &bar_q[q], cb * C::ROW_ELEMS, it.row0 + q * BLOCK_M,
-                              it.bh);
+                              sp ? &tmQlo : &tmQ, &bar_q[q], cb * C::ROW_ELEMS,
+                              it.row0 + (HP ? 0 : q * BLOCK_M), it.bh + (HP ? q : 0));
             }
             if (!ok) break;
             last_q = j;
@@ -535,7 +546,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     for (int k = 0, w = item_w(0); w < a.n_items; w = item_w(++k)) {
       const Item itm = item(w);
       const int n = itm.n;
-      const int r0 = itm.row0 + q * BLOCK_M;
+      const int r0 = itm.row0 + (HP ? 0 : q * BLOCK_M);
+      const int zo = itm.zo + (HP ? q : 0);  // this tile's output slab
       const int i = r0 + r_in;  // this thread's query row
       // visible keys of row i: [lo_i, hi_i]
       const int hi_i = a.causal ? min(i, a.Sk - 1) : a.Sk - 1;
@@ -656,17 +668,17 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
       if (ok) ok = __all_sync(0xffffffffu, wait(&bar_grant[q], k & 1));
       const float inv = (l > 0.f) ? (1.f / l) : 0.f;
       if (ok && i < a.Sq)
-        a.LSE[(size_t)itm.zo * a.Sq + i] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
+        a.LSE[(size_t)zo * a.Sq + i] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
       const int r_base = r0 + wq * 32;
       const uint32_t stage = sV(slot, 0) + wq * C::STAGE_PER_WARP;
       if (q < NQ - 1) {
         if (ok) {
           if (a.out_bf16)
             store_rows_tma<D, true, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                     r_base < a.Sq, itm.zo, 0, a.Dv);
+                                                     r_base < a.Sq, zo, 0, a.Dv);
           else
             store_rows_tma<D, false, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                      r_base < a.Sq, itm.zo, 0, a.Dv);
+                                                      r_base < a.Sq, zo, 0, a.Dv);
         }
         named_bar_sync(C::EPI_BAR0 + q, 128);
         if (wq == 0 && lane == 0) mbar_arrive(&bar_grant[q + 1]);
@@ -674,10 +686,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         if (ok) {
           if (a.out_bf16)
             store_rows_tma<D, true, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                            r_base < a.Sq, itm.zo, 0, a.Dv);
+                                                            r_base < a.Sq, zo, 0, a.Dv);
           else
             store_rows_tma<D, false, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage,
-                                                             r_base, r_base < a.Sq, itm.zo, 0, a.Dv);
+                                                             r_base, r_base < a.Sq, zo, 0, a.Dv);
         }
         pending = true;
         pend_slot = slot;
@@ -782,6 +794,15 @@ bool encode_o_map(CUtensorMap* m, void* O, const fa_params& p) {
                                bf ? 2 : 4, O, p.D, p.Sq, (uint64_t)p.B * p.H, p.D, bf ? 64 : 32, 32);
 }
 
+// The forward kernel instantiation: head-pair items (two-tile kernels only) or not.
+template <int D, bool F32>
+auto fwd_kernel_for(bool hp) {
+  auto kern = fa_fwd_kernel<D, F32, false>;
+  if constexpr (FwdCfg<D, F32>::NQ == 2)
+    if (hp) kern = fa_fwd_kernel<D, F32, true>;
+  return kern;
+}
+
 template <int D, bool F32>
 fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                   const fa_params& p, cudaStream_t stream) {
@@ -846,13 +867,18 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   a.causal = p.causal;
   a.window = p.window;
   a.out_bf16 = p.out_dtype == FA_BF16;
-  a.n_qgroups = (p.Sq + BLOCK_M * C::NQ - 1) / (BLOCK_M * C::NQ);
+  // Two query tiles per item: two heads of one kv head when the group size is even,
+  // else two row tiles of one head.
+  const bool hp = C::NQ == 2 && (p.H / p.HKV) % 2 == 0;
+  const int item_rows = hp ? BLOCK_M : BLOCK_M * C::NQ;
+  a.n_qgroups = (p.Sq + item_rows - 1) / item_rows;
+  a.BHi = hp ? (int)BHq / 2 : (int)BHq;
   // Fewer (query group, head) items than SMs -- short query sequences: split each
   // item's keys into ranges of tps tiles (each range a work item writing a partial O
   // and LSE, combined afterwards), enough for about two items per SM.
   const int sms = host::sm_count();
   const int n_kt = (p.Sk + BLOCK_N - 1) / BLOCK_N;
-  const int base_items = (int)BHq * a.n_qgroups;
+  const int base_items = a.BHi * a.n_qgroups;
   a.n_splits = 1;
   a.tps = n_kt;
   if (base_items < sms && n_kt >= 8) {
@@ -886,7 +912,7 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
     }
   }
   const unsigned grid = (unsigned)std::min(a.n_items, sms);
-  auto kern = fa_fwd_kernel<D, F32>;
+  auto kern = fwd_kernel_for<D, F32>(hp);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_ALLOC);
   if (e == cudaSuccess) {
@@ -1095,16 +1121,19 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
   a.causal = p.causal;
   a.window = p.window;
   a.out_bf16 = p.out_dtype == FA_BF16;
-  a.n_qgroups = (p.Sq + BLOCK_M * C::NQ - 1) / (BLOCK_M * C::NQ);
+  const bool hp = C::NQ == 2 && (p.H / p.HKV) % 2 == 0;  // head pairs (see run_fwd)
+  const int item_rows = hp ? BLOCK_M : BLOCK_M * C::NQ;
+  a.n_qgroups = (p.Sq + item_rows - 1) / item_rows;
+  a.BHi = hp ? (int)BHq / 2 : (int)BHq;
   a.n_splits = 1;  // (split keys need scratch for the partial outputs)
   a.tps = (p.Sk + BLOCK_N - 1) / BLOCK_N;
-  a.n_items = (int)BHq * a.n_qgroups;
+  a.n_items = a.BHi * a.n_qgroups;
   a.Dv = Dv;
   a.lpt = p.causal ? 1 : 0;
   a.BH = (int)BHq;
   a.limit_ns = WAIT_LIMIT_NS;
   const unsigned grid = (unsigned)std::min(a.n_items, host::sm_count());
-  auto kern = fa_fwd_kernel<D, F32>;
+  auto kern = fwd_kernel_for<D, F32>(hp);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_ALLOC);
   if (e != cudaSuccess) return FA_ERR_CUDA;
