@@ -64,6 +64,12 @@ SMALL = {
                                               seed=55),
     # the decode-shaped measurement line's launch: 128 queries against 16384 keys
     "bf16-decode-sq128-sk16384": C4.with_(Sq=128, causal=False, window=0, seed=56),
+    # forward items pair two query heads of a kv head when the group size is even
+    # (three pairs per kv head here), else two row tiles of one head (group of 3)
+    "bf16-gqa6-causal-ragged": C3.with_(B=1, H=12, HKV=2, Sq=300, Sk=300, seed=57),
+    "bf16-gqa3-window-ragged": C4.with_(B=1, H=6, HKV=2, Sq=420, Sk=420, window=150, seed=58),
+    "bf16-decode-gqa6": C3.with_(B=1, H=6, HKV=1, Sq=90, Sk=2600, causal=False, seed=59),
+    "bf16-decode-gqa3": C3.with_(B=1, H=3, HKV=1, Sq=90, Sk=2600, causal=False, seed=60),
 }
 
 
