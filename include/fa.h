@@ -94,9 +94,11 @@ typedef enum {
  * All pointers are caller-owned device memory, 16-byte aligned; outputs must not
  * alias inputs. The call validates its arguments synchronously, then enqueues
  * work on `stream` and returns without waiting. Temporary buffers (an fp16 copy
- * of V for bf16 inputs; hi/lo tf32 splits for fp32 inputs) are taken
- * stream-ordered from a library-owned CUDA memory pool and released on the same
- * stream. Errors: FA_ERR_INVALID_ARG / _UNSUPPORTED / _ALIGNMENT before any work
+ * of V for bf16 inputs; hi/lo tf32 splits for fp32 inputs; for short query
+ * sequences, whose work items are fewer than the SMs, fp32 partial O and LSE of up
+ * to 16 key ranges, combined in range order, so results stay deterministic) are
+ * taken stream-ordered from a library-owned CUDA memory pool and released on the
+ * same stream. Errors: FA_ERR_INVALID_ARG / _UNSUPPORTED / _ALIGNMENT before any work
  * is enqueued; FA_ERR_CUDA if a CUDA call or launch fails. Device-side barrier
  * timeouts are reported later by fa_device_status().
  */
@@ -143,7 +145,8 @@ FA_API fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, voi
  * computed first by a preprocess kernel; dK/dV are accumulated per key tile over
  * the grouped query heads without atomics (deterministic: two calls on the same
  * inputs give bit-identical results). Workspace (D_i, fp16 / tf32-split operand
- * copies) is stream-ordered from the library pool. Same ownership, alignment and
+ * copies; for short query sequences with bf16 inputs, fp32 partial dQ of up to 16
+ * key ranges, summed in range order) is stream-ordered from the library pool. Same ownership, alignment and
  * error rules as fa_fwd. For bf16 inputs the dQ kernel is launched on `stream` as
  * a programmatic dependent of the dK/dV kernel: it starts on the SMs that dK/dV's
  * last wave leaves idle and completes only after dK/dV has, so work enqueued on
