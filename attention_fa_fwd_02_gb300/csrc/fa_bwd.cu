@@ -1734,23 +1734,24 @@ __global__ void bwd_prepass16_kernel(const __nv_bfloat16* __restrict__ dO, const
 // Key ranges of a query tile computed as separate dQ work items (few query tiles per
 // SM): dQ = sum_s dQ_s over the ranges s that hold a key tile the query tile can see
 // (exactly the ranges whose work items wrote their slab), summed in range order, so
-// the result is deterministic; rows of a tile that sees no key get 0. One thread per
-// 4 columns of a row; partial slab s holds rows (bh, i) of range s.
+// the result is deterministic; rows of a tile that sees no key get 0. Thread (x, y)
+// of a block takes columns 4x.. of row blockIdx.x * blockDim.y + y of head blockIdx.y
+// (+ multiples of gridDim.y); partial slab s holds rows (bh, i) of range s.
 __global__ void dq_range_sum_kernel(const float* __restrict__ part, void* __restrict__ dQ,
                                     int tps, int BH, int Sq, int Sk, int causal, int window, int Dv,
                                     int out_bf16) {
-  const int q4 = Dv / 4;
-  const size_t rows = (size_t)BH * Sq, n = rows * q4, slab = rows * Dv;
-  for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n;
-       t += (size_t)gridDim.x * blockDim.x) {
-    const size_t r = t / q4;
-    const int c = (int)(t % q4) * 4;
-    const int i0 = (int)(r % Sq) / BLOCK_M * BLOCK_M;
-    int lo, hi;
-    kv_tile_range(i0, min(i0 + BLOCK_M - 1, Sq - 1), Sk, causal, window, &lo, &hi);
-    // range s covers key tiles [s * tps, (s + 1) * tps): it meets [lo, hi) for s in
-    // [lo / tps, (hi - 1) / tps]
-    const int s_lo = lo / tps, n_s = hi > lo ? (hi - 1) / tps + 1 - s_lo : 0;
+  const int i = blockIdx.x * blockDim.y + threadIdx.y;
+  const int c = threadIdx.x * 4;
+  if (i >= Sq || c >= Dv) return;
+  const size_t slab = (size_t)BH * Sq * Dv;
+  const int i0 = i / BLOCK_M * BLOCK_M;
+  int lo, hi;
+  kv_tile_range(i0, min(i0 + BLOCK_M - 1, Sq - 1), Sk, causal, window, &lo, &hi);
+  // range s covers key tiles [s * tps, (s + 1) * tps): it meets [lo, hi) for s in
+  // [lo / tps, (hi - 1) / tps]
+  const int s_lo = lo / tps, n_s = hi > lo ? (hi - 1) / tps + 1 - s_lo : 0;
+  for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+    const size_t r = (size_t)bh * Sq + i;
     const float* src = part + (size_t)s_lo * slab + r * Dv + c;
     float4 v[MAX_KEY_RANGES];  // every range's load issued before any is used
 #pragma unroll
@@ -2041,9 +2042,10 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       }
       if (e == cudaSuccess && dq_splits > 1) {
         host::KernelTimer kt("dq_range_sum", stream);
-        dq_range_sum_kernel<<<grid_pp, 256, 0, stream>>>(dq_part, dQ, dq_tps, (int)BH, p.Sq, p.Sk,
-                                                         p.causal, p.window, Dv,
-                                                         p.out_dtype == FA_BF16);
+        dim3 cg, cb;
+        combine_launch_shape((int)BH, p.Sq, Dv, &cg, &cb);
+        dq_range_sum_kernel<<<cg, cb, 0, stream>>>(dq_part, dQ, dq_tps, (int)BH, p.Sq, p.Sk,
+                                                   p.causal, p.window, Dv, p.out_dtype == FA_BF16);
         e = cudaGetLastError();
       }
     }

@@ -21,6 +21,15 @@ constexpr float RESCALE_THRESHOLD = 8.0f;
 // (forward and dQ), whose partial results a combine kernel adds up.
 constexpr int MAX_KEY_RANGES = 16;
 
+// Launch shape of the key-range combine kernels (one thread per 4 of a row's Dv
+// columns): blockDim (Dv / 4, rows per block), about 64 threads; grid (row blocks,
+// heads, at most 65535: the kernels loop over the rest).
+inline void combine_launch_shape(int BH, int Sq, int Dv, dim3* grid, dim3* block) {
+  const int q4 = Dv / 4, rpb = 64 / q4 > 1 ? 64 / q4 : 1;
+  *block = dim3(q4, rpb);
+  *grid = dim3((Sq + rpb - 1) / rpb, BH < 65535 ? BH : 65535);
+}
+
 // Status bits a kernel may set in its device status word.
 enum : unsigned int {
   DEV_TIMEOUT = 1u,  // a barrier wait gave up

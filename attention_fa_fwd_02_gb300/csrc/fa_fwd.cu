@@ -726,18 +726,19 @@ __global__ void fill_empty_kernel(void* O, float* LSE, size_t rows, int D, int o
 // s * rows + r. The row's result is the softmax over all its keys:
 //   LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
 // (ranges with no visible key have LSE_s = -inf and weigh 0; a row with none at all
-// gets O = 0, LSE = -inf). Ranges are summed in order (deterministic). One thread per
-// 4 columns of a row; it issues the loads of all (at most 16) ranges before using
-// any, so a row costs one round trip to L2, where the partials still are.
+// gets O = 0, LSE = -inf). Ranges are summed in order (deterministic). Thread
+// (x, y) of a block takes columns 4x.. of row blockIdx.x * blockDim.y + y of head
+// blockIdx.y (+ multiples of gridDim.y), so no index needs a division; it issues the
+// loads of all (at most 16) ranges before using any.
 __global__ void combine_splits_kernel(const float* __restrict__ Op, const float* __restrict__ Lp,
                                       void* __restrict__ O, float* __restrict__ LSE, int n_splits,
-                                      size_t rows, int Dv, int out_bf16) {
-  const int q4 = Dv / 4;
-  const size_t n = rows * q4;
-  for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n;
-       t += (size_t)gridDim.x * blockDim.x) {
-    const size_t r = t / q4;
-    const int c = (int)(t % q4) * 4;
+                                      int BH, int Sq, int Dv, int out_bf16) {
+  const int i = blockIdx.x * blockDim.y + threadIdx.y;
+  const int c = threadIdx.x * 4;
+  if (i >= Sq || c >= Dv) return;
+  const size_t rows = (size_t)BH * Sq;
+  for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+    const size_t r = (size_t)bh * Sq + i;
     float ls[MAX_KEY_RANGES];
     float4 ov[MAX_KEY_RANGES];
 #pragma unroll
@@ -925,9 +926,11 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   if (e == cudaSuccess && a.n_splits > 1) {
     host::KernelTimer kt("combine_splits", stream);
     const float* op = static_cast<const float*>(pws);
-    combine_splits_kernel<<<4 * sms, 256, 0, stream>>>(op, op + (size_t)a.n_splits * rows * Dv, O,
-                                                       LSE, a.n_splits, rows, Dv,
-                                                       p.out_dtype == FA_BF16);
+    dim3 cg, cb;
+    combine_launch_shape((int)BHq, p.Sq, Dv, &cg, &cb);
+    combine_splits_kernel<<<cg, cb, 0, stream>>>(op, op + (size_t)a.n_splits * rows * Dv, O, LSE,
+                                                 a.n_splits, (int)BHq, p.Sq, Dv,
+                                                 p.out_dtype == FA_BF16);
     e = cudaGetLastError();
   }
   cudaError_t e2 = host::scratch_free(ws, stream);
