@@ -1750,21 +1750,24 @@ __global__ void dq_range_sum_kernel(const float* __restrict__ part, void* __rest
   // range s covers key tiles [s * tps, (s + 1) * tps): it meets [lo, hi) for s in
   // [lo / tps, (hi - 1) / tps]
   const int s_lo = lo / tps, n_s = hi > lo ? (hi - 1) / tps + 1 - s_lo : 0;
+  constexpr int G = KEY_RANGE_GROUP;
   for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
     const size_t r = (size_t)bh * Sq + i;
     const float* src = part + (size_t)s_lo * slab + r * Dv + c;
-    float4 v[MAX_KEY_RANGES];  // every range's load issued before any is used
-#pragma unroll
-    for (int k = 0; k < MAX_KEY_RANGES; ++k)
-      if (k < n_s) v[k] = *reinterpret_cast<const float4*>(src + k * slab);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g0 = 0; g0 < n_s; g0 += G) {
+      float4 v[G];  // a group's loads issued before any is used
 #pragma unroll
-    for (int k = 0; k < MAX_KEY_RANGES; ++k) {
-      if (k < n_s) {
-        acc.x += v[k].x;
-        acc.y += v[k].y;
-        acc.z += v[k].z;
-        acc.w += v[k].w;
+      for (int k = 0; k < G; ++k)
+        if (g0 + k < n_s) v[k] = *reinterpret_cast<const float4*>(src + (g0 + k) * slab);
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        if (g0 + k < n_s) {
+          acc.x += v[k].x;
+          acc.y += v[k].y;
+          acc.z += v[k].z;
+          acc.w += v[k].w;
+        }
       }
     }
     if (out_bf16) {
@@ -1809,19 +1812,13 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   const size_t sched_off = (bytes + 15) / 16 * 16;  // the dQ kernel's work-item counter
   bytes = sched_off + 16;
   // Fewer query tiles than SMs (short query sequences, bf16 inputs): the dQ work items
-  // also split the keys into ranges of tps tiles -- about two items per SM -- each
+  // also split the keys into ranges of tps tiles (key_range_tiles picks tps), each
   // range writing a partial dQ (fp32) that a sum kernel adds up afterwards.
   const int sms = host::sm_count();
   const int n_qt = (p.Sq + BLOCK_M - 1) / BLOCK_M, n_kt = (p.Sk + BLOCK_N - 1) / BLOCK_N;
-  int dq_splits = 1, dq_tps = n_kt;
-  if (!F32 && BH * n_qt < (size_t)sms && n_kt >= 8) {
-    const int base = (int)BH * n_qt;
-    const int want = std::min({MAX_KEY_RANGES, (2 * sms + base - 1) / base, n_kt / 4});
-    if (want > 1) {
-      dq_tps = (n_kt + want - 1) / want;
-      dq_splits = (n_kt + dq_tps - 1) / dq_tps;
-    }
-  }
+  int dq_tps = n_kt;
+  if (!F32 && BH * n_qt < (size_t)sms) dq_tps = key_range_tiles((int)BH * n_qt, n_kt, sms);
+  const int dq_splits = (n_kt + dq_tps - 1) / dq_tps;
   const size_t part_off = (bytes + 255) / 256 * 256;  // partial dQ [splits][BH][Sq][Dv]
   if (dq_splits > 1) bytes = part_off + (size_t)dq_splits * nq * 4;
   void* ws = nullptr;

@@ -18,8 +18,27 @@ constexpr float LN2 = 0.6931471805599453f;
 // unnormalised probabilities then stay below 2^8, well inside fp16 range.
 constexpr float RESCALE_THRESHOLD = 8.0f;
 // Short query sequences split each work item's keys into at most this many ranges
-// (forward and dQ), whose partial results a combine kernel adds up.
-constexpr int MAX_KEY_RANGES = 16;
+// (forward and dQ), whose partial results a combine kernel adds up, KEY_RANGE_GROUP
+// ranges' loads in flight at a time.
+constexpr int MAX_KEY_RANGES = 32;
+constexpr int KEY_RANGE_GROUP = 16;
+
+// Key tiles per range for a pass whose `base` work items (one persistent CTA per SM,
+// `sms` of them) are fewer than the SMs: the split count s (ranges of at least 4 of
+// the n_kt key tiles, at most MAX_KEY_RANGES) that minimises the estimated finish
+// time ceil(base * s / sms) * (ceil(n_kt / s) + 2), i.e. rounds of equal items, each
+// costing its key tiles plus about two tiles' worth of item overhead. n_kt: no split.
+inline int key_range_tiles(int base, int n_kt, int sms) {
+  if (base >= sms || n_kt < 8) return n_kt;
+  int best_t = n_kt;
+  long long best = -1;
+  for (int s = 1; s <= MAX_KEY_RANGES && s <= n_kt / 4; ++s) {
+    const int t = (n_kt + s - 1) / s, ns = (n_kt + t - 1) / t;
+    const long long cost = ((long long)base * ns + sms - 1) / sms * (t + 2);
+    if (best < 0 || cost < best) { best = cost; best_t = t; }
+  }
+  return best_t;
+}
 
 // Launch shape of the key-range combine kernels (one thread per 4 of a row's Dv
 // columns): blockDim (Dv / 4, rows per block), about 64 threads; grid (row blocks,

@@ -42,10 +42,10 @@ struct FwdArgs {
   float scale_log2;  // softmax scale * log2(e)
   int causal, window;
   int out_bf16;
-  int n_qgroups;
-  int n_splits;  // key ranges per (query group, head): > 1 writes partial O / LSE per range
+  int n_qgroups;  // row groups per head: 128 rows (head pairs) or 256 rows
+  int n_splits;  // key ranges per (query group, head (pair)): > 1 writes partial O / LSE per range
   int tps;       // key tiles per range
-  int n_items;  // BH * n_qgroups * n_splits
+  int n_items;  // BHi * n_qgroups * n_splits
   int Dv;       // head dim of the tensors (<= the kernel's D; missing columns read as 0)
   int lpt;  // 1: the heaviest query groups first (causal)
   int BH;
@@ -721,54 +721,62 @@ __global__ void fill_empty_kernel(void* O, float* LSE, size_t rows, int D, int o
   }
 }
 
-// Key ranges of one (query group, head) computed separately: partial outputs O_s
+// Key ranges of one query row computed separately: partial outputs O_s
 // (each normalised by its own row sum) and natural-log LSE_s per range, slab
 // s * rows + r. The row's result is the softmax over all its keys:
 //   LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
 // (ranges with no visible key have LSE_s = -inf and weigh 0; a row with none at all
-// gets O = 0, LSE = -inf). Ranges are summed in order (deterministic). Thread
+// gets O = 0, LSE = -inf). One pass over the ranges in order (deterministic), with a
+// running maximum m: the sums are rescaled by exp(m_old - m_new) when a larger LSE_s
+// arrives, so the LSE and partial-O loads of KEY_RANGE_GROUP ranges go out together
+// (a separate pass for the maximum would cost another round trip to memory). Thread
 // (x, y) of a block takes columns 4x.. of row blockIdx.x * blockDim.y + y of head
-// blockIdx.y (+ multiples of gridDim.y), so no index needs a division; it issues the
-// loads of all (at most 16) ranges before using any.
+// blockIdx.y (+ multiples of gridDim.y).
 __global__ void combine_splits_kernel(const float* __restrict__ Op, const float* __restrict__ Lp,
                                       void* __restrict__ O, float* __restrict__ LSE, int n_splits,
                                       int BH, int Sq, int Dv, int out_bf16) {
+  constexpr int G = KEY_RANGE_GROUP;
   const int i = blockIdx.x * blockDim.y + threadIdx.y;
   const int c = threadIdx.x * 4;
   if (i >= Sq || c >= Dv) return;
   const size_t rows = (size_t)BH * Sq;
   for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
     const size_t r = (size_t)bh * Sq + i;
-    float ls[MAX_KEY_RANGES];
-    float4 ov[MAX_KEY_RANGES];
-#pragma unroll
-    for (int sp = 0; sp < MAX_KEY_RANGES; ++sp) {
-      if (sp < n_splits) {
-        ls[sp] = Lp[sp * rows + r];
-        ov[sp] = *reinterpret_cast<const float4*>(Op + (sp * rows + r) * Dv + c);
-      }
-    }
-    float mx = -INFINITY;
-#pragma unroll
-    for (int sp = 0; sp < MAX_KEY_RANGES; ++sp)
-      if (sp < n_splits) mx = fmaxf(mx, ls[sp]);
-    // (no branch on mx, so that the partial-O loads need not wait for the LSE ones:
-    // a range with no visible key has LSE_s = -inf, weight 0 and O_s = 0 written)
+    float m = -INFINITY, sum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float sum = 0.f;
+    for (int g0 = 0; g0 < n_splits; g0 += G) {
+      float ls[G];
+      float4 ov[G];
 #pragma unroll
-    for (int sp = 0; sp < MAX_KEY_RANGES; ++sp) {
-      if (sp < n_splits) {
-        const float wgt = ls[sp] == -INFINITY ? 0.f : expf(ls[sp] - mx);
-        sum += wgt;
-        acc.x += wgt * ov[sp].x;
-        acc.y += wgt * ov[sp].y;
-        acc.z += wgt * ov[sp].z;
-        acc.w += wgt * ov[sp].w;
+      for (int k = 0; k < G; ++k) {
+        if (g0 + k < n_splits) {
+          ls[k] = Lp[(g0 + k) * rows + r];
+          ov[k] = *reinterpret_cast<const float4*>(Op + ((g0 + k) * rows + r) * Dv + c);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        if (g0 + k < n_splits && ls[k] != -INFINITY) {
+          if (ls[k] > m) {  // new maximum: rescale what was summed (exp(-inf) = 0 at first)
+            const float sc = expf(m - ls[k]);
+            sum *= sc;
+            acc.x *= sc;
+            acc.y *= sc;
+            acc.z *= sc;
+            acc.w *= sc;
+            m = ls[k];
+          }
+          const float wgt = expf(ls[k] - m);
+          sum += wgt;
+          acc.x += wgt * ov[k].x;
+          acc.y += wgt * ov[k].y;
+          acc.z += wgt * ov[k].z;
+          acc.w += wgt * ov[k].w;
+        }
       }
     }
     const float inv = sum > 0.f ? 1.f / sum : 0.f;
-    if (c == 0) LSE[r] = sum > 0.f ? mx + logf(sum) : -INFINITY;
+    if (c == 0) LSE[r] = sum > 0.f ? m + logf(sum) : -INFINITY;
     if (out_bf16) {
       __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
       __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
@@ -874,21 +882,14 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   const int item_rows = hp ? BLOCK_M : BLOCK_M * C::NQ;
   a.n_qgroups = (p.Sq + item_rows - 1) / item_rows;
   a.BHi = hp ? (int)BHq / 2 : (int)BHq;
-  // Fewer (query group, head) items than SMs -- short query sequences: split each
-  // item's keys into ranges of tps tiles (each range a work item writing a partial O
-  // and LSE, combined afterwards), enough for about two items per SM.
+  // Fewer (query group, head (pair)) items than SMs -- short query sequences: split each
+  // item's keys into ranges of tps tiles, each range a work item writing a partial O
+  // and LSE, combined afterwards (key_range_tiles picks tps).
   const int sms = host::sm_count();
   const int n_kt = (p.Sk + BLOCK_N - 1) / BLOCK_N;
   const int base_items = a.BHi * a.n_qgroups;
-  a.n_splits = 1;
-  a.tps = n_kt;
-  if (base_items < sms && n_kt >= 8) {
-    const int want = std::min({MAX_KEY_RANGES, (2 * sms + base_items - 1) / base_items, n_kt / 4});
-    if (want > 1) {
-      a.tps = (n_kt + want - 1) / want;
-      a.n_splits = (n_kt + a.tps - 1) / a.tps;
-    }
-  }
+  a.tps = key_range_tiles(base_items, n_kt, sms);
+  a.n_splits = (n_kt + a.tps - 1) / a.tps;
   a.n_items = base_items * a.n_splits;
   a.Dv = Dv;
   a.lpt = p.causal ? 1 : 0;
