@@ -108,19 +108,24 @@ def test_forward_small(fa, name):
     _check(w, o, lse, ro, rl, name)
 
 
-def test_forward_deterministic(fa):
-    w = SMALL["bf16-gqa-causal-ragged"]
+@pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa",
+                                  "bf16-decode-sq128-sk16384"])
+def test_forward_deterministic(fa, name):
+    # the decode cases split the keys into ranges (6 and 19) combined in range order
+    w = SMALL[name]
     q, k, v, _ = make_inputs(w)
     o1, l1 = _run(fa, w, q, k, v)
     o2, l2 = _run(fa, w, q, k, v)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_forward_bf16_output(fa):
+@pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa"])
+def test_forward_bf16_output(fa, name):
     # bf16 outputs: rounding O to bf16 moves each element by at most half an ulp,
     # 2^-9 |O| (round to nearest, 8 significant bits). Allow that per element on top
-    # of the fp32-output tolerance: |o - ref| <= 2^-8 |ref| + 2e-2 * RMS(ref).
-    w = SMALL["bf16-gqa-causal-ragged"]
+    # of the fp32-output tolerance: |o - ref| <= 2^-8 |ref| + 2e-2 * RMS(ref). (The
+    # decode case combines fp32 partial outputs of 6 key ranges and rounds once.)
+    w = SMALL[name]
     q, k, v, _ = make_inputs(w)
     o, lse = _run(fa, w, q, k, v, out_dtype=torch.bfloat16)
     assert o.dtype == torch.bfloat16
