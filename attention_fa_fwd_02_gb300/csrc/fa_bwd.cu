@@ -1918,14 +1918,11 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     }
     {
       host::KernelTimer kt("split_tf32(Q,dO,K,V)", stream);
-      split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(Q), qh, ql, qth, qtl,
-                                                    p.Sq, Dv, ldqt, BH);
-      split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(dO), doh, dol, doth,
-                                                    dotl, p.Sq, Dv, ldqt, BH);
-      split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(K), kh, kl, kth, ktl,
-                                                    p.Sk, Dv, ldkt, BHk);
-      split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(V), vh, vl, nullptr,
-                                                    nullptr, p.Sk, Dv, 0, BHk);
+      launch_split_tf32({{static_cast<const float*>(Q), qh, ql, qth, qtl, p.Sq, ldqt, (int)BH},
+                         {static_cast<const float*>(dO), doh, dol, doth, dotl, p.Sq, ldqt, (int)BH},
+                         {static_cast<const float*>(K), kh, kl, kth, ktl, p.Sk, ldkt, (int)BHk},
+                         {static_cast<const float*>(V), vh, vl, nullptr, nullptr, p.Sk, 0, (int)BHk}},
+                        Dv, grid_pp, stream);
     }
     float* hl_q[2] = {qh, ql};
     float* hl_do[2] = {doh, dol};

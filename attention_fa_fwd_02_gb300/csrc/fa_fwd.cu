@@ -847,12 +847,10 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
     float* vth = kl + nk;
     float* vtl = vth + nvt;
     host::KernelTimer kt("split_tf32(Q,K,V)", stream);
-    split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(Q), qh, ql, nullptr,
-                                                  nullptr, p.Sq, Dv, 0, BHq);
-    split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(K), kh, kl, nullptr,
-                                                  nullptr, p.Sk, Dv, 0, BHk);
-    split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(V), nullptr, nullptr,
-                                                  vth, vtl, p.Sk, Dv, ldt, BHk);
+    launch_split_tf32({{static_cast<const float*>(Q), qh, ql, nullptr, nullptr, p.Sq, 0, (int)BHq},
+                       {static_cast<const float*>(K), kh, kl, nullptr, nullptr, p.Sk, 0, (int)BHk},
+                       {static_cast<const float*>(V), nullptr, nullptr, vth, vtl, p.Sk, ldt, (int)BHk}},
+                      Dv, grid_pp, stream);
     enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, qh, Dv, p.Sq, BHq, Dv, 32, 128);
     enc &= host::encode_tiled_3d(&mQlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ql, Dv, p.Sq, BHq, Dv, 32, 128);
     enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kh, Dv, p.Sk, BHk, Dv, 32, 128);
@@ -1100,12 +1098,10 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
     float* kl = kh + nk;
     float* vth = kl + nk;
     float* vtl = vth + nvt;
-    split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(Q), qh, ql, nullptr,
-                                                  nullptr, p.Sq, Dv, 0, BHq);
-    split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(K), kh, kl, nullptr,
-                                                  nullptr, p.Sk, Dv, 0, BHk);
-    split_tf32_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<const float*>(V), nullptr, nullptr,
-                                                  vth, vtl, p.Sk, Dv, ldt, BHk);
+    launch_split_tf32({{static_cast<const float*>(Q), qh, ql, nullptr, nullptr, p.Sq, 0, (int)BHq},
+                       {static_cast<const float*>(K), kh, kl, nullptr, nullptr, p.Sk, 0, (int)BHk},
+                       {static_cast<const float*>(V), nullptr, nullptr, vth, vtl, p.Sk, ldt, (int)BHk}},
+                      Dv, grid_pp, stream);
     enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, qh, Dv, p.Sq, BHq, Dv, 32, 128);
     enc &= host::encode_tiled_3d(&mQlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ql, Dv, p.Sq, BHq, Dv, 32, 128);
     enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kh, Dv, p.Sk, BHk, Dv, 32, 128);
