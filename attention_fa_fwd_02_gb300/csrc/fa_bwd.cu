@@ -242,11 +242,19 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ KVMaps m, const BwdArgs a) {
   using C = BwdCfg<D, F32>;
   constexpr int CH = C::CH, NST = C::KV_NST;
+  // (fp32 inputs only: bf16 inputs use fa_bwd_dkdv16_kernel, whose accumulating MMAs
+  // would read the score half of a stage, which this kernel releases early)
+  static_assert(F32, "the 3xTF32 dK / dV kernel");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_kv, bar_full[NST], bar_empty[NST], bar_sp[2], bar_ds[2],
-      bar_accdone[2], bar_done, bar_drain[2];
+  // A stage has two halves with their own full / empty barriers: the score half (Q and
+  // dO chunks, read by S^T and dP^T) is free once those MMAs completed, so the next
+  // chunk's copy lands while the softmax and the accumulating MMAs of this one run;
+  // the accumulate half (Q^T, dO^T chunks and the lse2 / delta vectors, read by dV, dK
+  // and the softmax) once dV and dK completed.
+  __shared__ __align__(8) uint64_t bar_kv, bar_sfull[NST], bar_sempty[NST], bar_afull[NST],
+      bar_aempty[NST], bar_sp[2], bar_ds[2], bar_accdone[2], bar_done, bar_drain[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int warp = warp_id(), lane = lane_id();
@@ -274,7 +282,12 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_kv, 1);
-    for (int s = 0; s < NST; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&bar_sfull[s], 1);
+      mbar_init(&bar_sempty[s], 1);
+      mbar_init(&bar_afull[s], 1);
+      mbar_init(&bar_aempty[s], 1);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_sp[s], 1);
       mbar_init(&bar_ds[s], 128);
@@ -324,31 +337,36 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
           tma_load_3d(gen(sK(sp)) + cb * C::BIG_CB, &m.K[sp], &bar_kv, cb * C::ROW, j0, bg);
           tma_load_3d(gen(sV(sp)) + cb * C::BIG_CB, &m.V[sp], &bar_kv, cb * C::ROW, j0, bg);
         }
-      int last[NST];
-      for (int s = 0; s < NST; ++s) last[s] = -1;
+      int last_s[NST], last_a[NST];
+      for (int s = 0; s < NST; ++s) last_s[s] = last_a[s] = -1;
       for (int c = 0; c < nc; ++c) {
         const int st = c % NST;
-        if (!wait(&bar_empty[st], ((c / NST) & 1) ^ 1)) break;
         int bh, i0;
         chunk_rows(c, &bh, &i0);
-        mbar_arrive_expect_tx(&bar_full[st], C::KV_STAGE + C::VEC_STAGE);
+        if (!wait(&bar_sempty[st], ((c / NST) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(&bar_sfull[st], 2 * C::NSPLIT * C::SMALL_TILE);
         for (int sp = 0; sp < C::NSPLIT; ++sp) {
           for (int cb = 0; cb < C::NCB; ++cb) {
-            tma_load_3d(gen(sQc(st, sp)) + cb * C::SMALL_CB, &m.Qc[sp], &bar_full[st], cb * C::ROW, i0, bh);
-            tma_load_3d(gen(sdOc(st, sp)) + cb * C::SMALL_CB, &m.dOc[sp], &bar_full[st], cb * C::ROW, i0, bh);
-          }
-          if constexpr (C::F32) {
-            tma_load_3d(gen(sQt(st, sp)), &m.Qt[sp], &bar_full[st], i0, 0, bh);
-            tma_load_3d(gen(sdOt(st, sp)), &m.dOt[sp], &bar_full[st], i0, 0, bh);
+            tma_load_3d(gen(sQc(st, sp)) + cb * C::SMALL_CB, &m.Qc[sp], &bar_sfull[st], cb * C::ROW, i0, bh);
+            tma_load_3d(gen(sdOc(st, sp)) + cb * C::SMALL_CB, &m.dOc[sp], &bar_sfull[st], cb * C::ROW, i0, bh);
           }
         }
-        tma_load_3d(vecs + st * 2 * CH, &m.L, &bar_full[st], i0, bh, 0);
-        tma_load_3d(vecs + st * 2 * CH + CH, &m.Dl, &bar_full[st], i0, bh, 0);
-        last[st] = c / NST;
+        last_s[st] = c / NST;
+        if (!wait(&bar_aempty[st], ((c / NST) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(&bar_afull[st], 2 * C::NSPLIT * C::T_TILE + C::VEC_STAGE);
+        for (int sp = 0; sp < C::NSPLIT; ++sp) {
+          tma_load_3d(gen(sQt(st, sp)), &m.Qt[sp], &bar_afull[st], i0, 0, bh);
+          tma_load_3d(gen(sdOt(st, sp)), &m.dOt[sp], &bar_afull[st], i0, 0, bh);
+        }
+        tma_load_3d(vecs + st * 2 * CH, &m.L, &bar_afull[st], i0, bh, 0);
+        tma_load_3d(vecs + st * 2 * CH + CH, &m.Dl, &bar_afull[st], i0, bh, 0);
+        last_a[st] = c / NST;
       }
       drain_wait(&bar_kv, 0, a.limit_ns);
-      for (int s = 0; s < NST; ++s)
-        if (last[s] >= 0) drain_wait(&bar_full[s], last[s] & 1, a.limit_ns);
+      for (int s = 0; s < NST; ++s) {
+        if (last_s[s] >= 0) drain_wait(&bar_sfull[s], last_s[s] & 1, a.limit_ns);
+        if (last_a[s] >= 0) drain_wait(&bar_afull[s], last_a[s] & 1, a.limit_ns);
+      }
     }
   } else if (warp == C::MMA_WARP) {
     // Score issuer: chunk c -> S^T = K Q^T and dP^T = V dO^T into TMEM slot c & 1,
@@ -357,7 +375,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       bool ok = wait(&bar_kv, 0);
       for (int c = 0; ok && c < nc; ++c) {
         const int st = c % NST, bb = c & 1;
-        if (!(ok = wait(&bar_full[st], (c / NST) & 1))) break;
+        if (!(ok = wait(&bar_sfull[st], (c / NST) & 1))) break;
         if (c >= 2 && !(ok = wait(&bar_accdone[bb], ((c - 2) >> 1) & 1))) break;
         tc_fence_after();
         issue_rowdot<C>(tmem + C::s_col(bb), sK(0), sK(C::NSPLIT - 1), sQc(st, 0),
@@ -365,6 +383,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
         issue_rowdot<C>(tmem + C::dp_col(bb), sV(0), sV(C::NSPLIT - 1), sdOc(st, 0),
                         sdOc(st, C::NSPLIT - 1));
         tc_commit(&bar_sp[bb]);
+        tc_commit(&bar_sempty[st]);  // the score half of the stage may take the next chunk
       }
       tc_commit(&bar_drain[0]);
       drain_wait(&bar_drain[0], 0, a.limit_ns);
@@ -377,17 +396,14 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       for (int c = 0; ok && c < nc; ++c) {
         const int pb = c & 1, pst = c % NST;
         if (!(ok = wait(&bar_ds[pb], (c >> 1) & 1))) break;
+        // the accumulate half (its phase of chunk c cannot be passed before aempty(c))
+        if (!(ok = wait(&bar_afull[pst], (c / NST) & 1))) break;
         tc_fence_after();
-        if constexpr (!C::F32) {
-          issue_acc<C>(tmem + C::KV_ACC0, tmem + C::s_col(pb), 0, sdOc(pst, 0), 0, c > 0);
-          issue_acc<C>(tmem + C::KV_ACC1, tmem + C::dp_col(pb), 0, sQc(pst, 0), 0, c > 0);
-        } else {
-          issue_acc<C>(tmem + C::KV_ACC0, tmem + C::s_col(pb), tmem + C::plo_col(pb), sdOt(pst, 0),
-                       sdOt(pst, 1), c > 0);
-          issue_acc<C>(tmem + C::KV_ACC1, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sQt(pst, 0),
-                       sQt(pst, 1), c > 0);
-        }
-        tc_commit(&bar_empty[pst]);
+        issue_acc<C>(tmem + C::KV_ACC0, tmem + C::s_col(pb), tmem + C::plo_col(pb), sdOt(pst, 0),
+                     sdOt(pst, 1), c > 0);
+        issue_acc<C>(tmem + C::KV_ACC1, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sQt(pst, 0),
+                     sQt(pst, 1), c > 0);
+        tc_commit(&bar_aempty[pst]);
         tc_commit(&bar_accdone[pb]);
       }
       if (ok) tc_commit(&bar_done);
@@ -406,7 +422,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       const int bb = c & 1, st = c % NST;
       int bh, i0;
       chunk_rows(c, &bh, &i0);
-      ok = __all_sync(0xffffffffu, wait(&bar_sp[bb], (c >> 1) & 1) && wait(&bar_full[st], (c / NST) & 1));
+      ok = __all_sync(0xffffffffu, wait(&bar_sp[bb], (c >> 1) & 1) && wait(&bar_afull[st], (c / NST) & 1));
       if (!ok) break;
       tc_fence_after();
       float s[CH], dp[CH];
