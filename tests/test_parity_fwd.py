@@ -70,6 +70,10 @@ SMALL = {
     "bf16-gqa3-window-ragged": C4.with_(B=1, H=6, HKV=2, Sq=420, Sk=420, window=150, seed=58),
     "bf16-decode-gqa6": C3.with_(B=1, H=6, HKV=1, Sq=90, Sk=2600, causal=False, seed=59),
     "bf16-decode-gqa3": C3.with_(B=1, H=3, HKV=1, Sq=90, Sk=2600, causal=False, seed=60),
+    # a single query row: many key ranges; causal (top-left) sees key 0 only, so every
+    # range but the first is empty
+    "bf16-decode-sq1": C3.with_(B=1, H=8, HKV=2, Sq=1, Sk=5000, causal=False, seed=61),
+    "bf16-decode-sq1-causal": C3.with_(B=1, H=8, HKV=2, Sq=1, Sk=5000, seed=62),
 }
 
 
