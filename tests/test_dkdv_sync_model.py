@@ -1,0 +1,229 @@
+"""A CPU model of the bf16 dK/dV kernel's synchronisation protocol.
+
+fa_bwd_dkdv16_kernel (fa_bwd.cu) walks the 128-query chunks of one key tile:
+
+  * the TMA producer keeps K, V resident and streams Q and dO chunks through two-slot
+    rings; a Q slot is free once S^T = K Q^T and dK += dS^T Q of its chunk have read
+    it (two commits), a dO slot once dP^T = V dO^T and dV += P^T dO have (two commits);
+  * the S issuer runs S^T(c) into the S^T slot once the softmax loaded S^T(c - 1);
+  * the B issuer runs dP^T(c) into the dP^T slot, then, once the softmax wrote
+    dS^T(c) over the first half of that slot, dK += dS^T Q; dP^T(c + 1) follows dK(c)
+    from the same thread, so the tensor pipe reads dS^T(c) before overwriting it;
+  * the dV issuer runs dV += P^T(c) dO once the softmax wrote P^T(c) into the shared
+    P^T tile, which the softmax refills only after that MMA completed (dv_done);
+  * the softmax warps wait for S^T(c), chunk c's vectors (with Q_c) and dO_c, load S^T
+    (freeing the slot), exponentiate, write P^T, wait for dP^T, write dS^T. The dO_c
+    wait is what orders the dV MMA after the dO copy (P^T would otherwise be written
+    as soon as S^T, i.e. Q_c, is in); dropping it is one of the planted faults.
+
+This test replays the roles in the kernel's order under random interleavings (copies
+land in any order, the tensor pipe runs in issue order) and checks every read of Q,
+dO, the TMEM slots and the P^T tile, and the accumulation order of dV and dK. Planted
+faults must be caught.
+"""
+import random
+
+import pytest
+
+from test_fwd_sync_model import MBarrier, ProtocolError
+
+NS = 2  # Q / dO ring depth at D = 128
+
+
+def run_protocol(nc, seed, q_release_count=2, wait_dv_done=True, wait_sfree=True,
+                 softmax_waits_do=True):
+    """Play the chunks of one key tile; raises ProtocolError on a violation."""
+    rnd = random.Random(seed)
+    mb = {}
+
+    def M(name, count=1):
+        if name not in mb:
+            mb[name] = MBarrier(name, count)
+        return mb[name]
+
+    for s in range(NS):
+        M(("qempty", s), q_release_count)
+        M(("doempty", s), 2)
+    smem_q, smem_do = [None] * NS, [None] * NS
+    reads = {"Q": {}, "dO": {}}  # chunk -> MMAs still to read that slot
+    pt = {"tile": None, "read": True}  # P^T smem tile: chunk and whether dV read it
+    tmem = {"S": None, "dP": None}
+    acc = {"dV": 0, "dK": 0}
+    copies, pipe = [], []
+
+    def commit(bar):
+        pipe.append(bar.arrive)
+
+    def load(kind, c):
+        st = c % NS
+        bar = M((kind + "full", st))
+        buf = smem_q if kind == "q" else smem_do
+        name = "Q" if kind == "q" else "dO"
+        bar.arrive_expect_tx(1)
+        reads[name][c] = 2  # the two MMAs that read this chunk's tile
+
+        def land():
+            old = buf[st]
+            if old is not None and reads[name].get(old[1], 0) > 0:
+                raise ProtocolError(f"{name} chunk {c} landed on chunk {old[1]} still read by an MMA")
+            buf[st] = (name, c)
+            bar.complete_tx(1)
+        copies.append(land)
+
+    def read(name, buf, c):
+        st = c % NS
+        if buf[st] != (name, c):
+            raise ProtocolError(f"an MMA of chunk {c} read {buf[st]}")
+        reads[name][c] -= 1
+
+    def tma():
+        for c in range(nc):
+            st = c % NS
+            yield (lambda st=st, c=c: M(("doempty", st)).passed(((c // NS) & 1) ^ 1))
+            load("do", c)
+            yield (lambda st=st, c=c: M(("qempty", st)).passed(((c // NS) & 1) ^ 1))
+            load("q", c)
+
+    def s_issuer():
+        for c in range(nc):
+            st = c % NS
+            yield (lambda st=st, c=c: M(("qfull", st)).passed((c // NS) & 1))
+            if c > 0 and wait_sfree:
+                yield (lambda c=c: M("sfree").passed((c - 1) & 1))
+
+            def mma(c=c):
+                read("Q", smem_q, c)
+                if tmem["S"] is not None and not tmem["S"][2]:
+                    raise ProtocolError(f"S^T({c}) overwrote S^T({tmem['S'][1]}) before the softmax read it")
+                tmem["S"] = ("S", c, False)
+            pipe.append(mma)
+            commit(M("s"))
+            commit(M(("qempty", st)))
+
+    def dv_issuer():
+        for c in range(nc):
+            st = c % NS
+            yield (lambda c=c: M("p").passed(c & 1))
+
+            def mma(c=c):
+                if pt["tile"] != c:
+                    raise ProtocolError(f"dV({c}) read the P^T tile of chunk {pt['tile']}")
+                read("dO", smem_do, c)
+                if acc["dV"] != c:
+                    raise ProtocolError(f"dV accumulated chunk {c} after {acc['dV']} chunks")
+                acc["dV"] += 1
+                pt["read"] = True
+            pipe.append(mma)
+            commit(M(("doempty", st)))
+            commit(M("dvdone"))
+        commit(M("done", 2))
+
+    def b_issuer():
+        for c in range(nc):
+            st = c % NS
+            yield (lambda st=st, c=c: M(("dofull", st)).passed((c // NS) & 1))
+
+            def dp(c=c):
+                read("dO", smem_do, c)
+                if tmem["dP"] is not None and tmem["dP"][0] != "USED":
+                    raise ProtocolError(f"dP^T({c}) overwrote {tmem['dP']}")
+                tmem["dP"] = ("dP", c)
+            pipe.append(dp)
+            commit(M("dp"))
+            commit(M(("doempty", st)))
+            yield (lambda c=c: M("ds").passed(c & 1))
+
+            def dk(c=c):
+                if tmem["dP"] != ("dS", c):
+                    raise ProtocolError(f"dK({c}) read {tmem['dP']}")
+                read("Q", smem_q, c)
+                if acc["dK"] != c:
+                    raise ProtocolError(f"dK accumulated chunk {c} after {acc['dK']} chunks")
+                acc["dK"] += 1
+                tmem["dP"] = ("USED", c)
+            pipe.append(dk)
+            commit(M(("qempty", st)))
+        commit(M("done", 2))
+
+    def softmax():
+        for c in range(nc):
+            st = c % NS
+            yield (lambda st=st, c=c: M("s").passed(c & 1) and M(("qfull", st)).passed((c // NS) & 1)
+                   and (not softmax_waits_do or M(("dofull", st)).passed((c // NS) & 1)))
+            if tmem["S"] != ("S", c, False):
+                raise ProtocolError(f"softmax read S^T {tmem['S']}, wanted chunk {c}")
+            tmem["S"] = ("S", c, True)
+            M("sfree").arrive()
+            yield None  # exponentials (lse2 of the chunk from the ring's vector slot)
+            if c > 0 and wait_dv_done:
+                yield (lambda c=c: M("dvdone").passed((c - 1) & 1))
+            if not pt["read"]:
+                raise ProtocolError(f"P^T({c}) written over P^T({pt['tile']}) before dV read it")
+            pt["tile"], pt["read"] = c, False
+            M("p").arrive()
+            yield (lambda c=c: M("dp").passed(c & 1))
+            if tmem["dP"] != ("dP", c):
+                raise ProtocolError(f"softmax read dP^T {tmem['dP']}, wanted chunk {c}")
+            yield None
+            tmem["dP"] = ("dS", c)
+            M("ds").arrive()
+        yield (lambda: M("done", 2).passed(0))
+        if acc["dV"] != nc or acc["dK"] != nc:
+            raise ProtocolError("epilogue before every chunk was accumulated")
+
+    roles = {"tma": tma(), "S": s_issuer(), "dV": dv_issuer(), "B": b_issuer(), "softmax": softmax()}
+    waiting = {r: None for r in roles}
+    done = set()
+    for _ in range(1_000_000):
+        runnable = [r for r in roles if r not in done and (waiting[r] is None or waiting[r]())]
+        choices = len(runnable) + (1 if copies else 0) + (1 if pipe else 0)
+        if choices == 0:
+            if len(done) == len(roles):
+                return
+            raise ProtocolError(f"deadlock: {sorted(set(roles) - done)} wait forever")
+        k = rnd.randrange(choices)
+        if k < len(runnable):
+            r = runnable[k]
+            try:
+                waiting[r] = next(roles[r])
+            except StopIteration:
+                done.add(r)
+                waiting[r] = None
+        elif copies and k == len(runnable):
+            copies.pop(rnd.randrange(len(copies)))()
+        else:
+            pipe.pop(0)()
+    raise ProtocolError("no progress")
+
+
+def test_protocol_holds_under_random_interleavings():
+    rnd = random.Random(20261206)
+    for _ in range(2000):
+        run_protocol(rnd.randint(1, 10), seed=rnd.randrange(10 ** 9))
+
+
+def _caught(trials, **fault):
+    rnd = random.Random(19)
+    for _ in range(trials):
+        try:
+            run_protocol(rnd.randint(2, 10), seed=rnd.randrange(10 ** 9), **fault)
+        except ProtocolError:
+            return True
+    return False
+
+
+def test_planted_fault_q_slot_freed_by_one_reader_is_caught():
+    # a Q slot released after S^T alone (dK of the chunk still has to read it)
+    assert _caught(3000, q_release_count=1)
+
+
+def test_planted_fault_pt_refilled_before_dv_read_it_is_caught():
+    assert _caught(3000, wait_dv_done=False)
+
+
+def test_planted_fault_st_slot_refilled_before_the_softmax_read_it_is_caught():
+    assert _caught(3000, wait_sfree=False)
+
+
+def test_planted_fault_dv_not_ordered_after_the_do_copy_is_caught():
+    assert _caught(3000, softmax_waits_do=False)
