@@ -159,6 +159,12 @@ fa_status validate(const fa_params* p) {
   const long long bh = (long long)p->B * p->H;
   if (bh > (1ll << 30) || p->Sq > (1 << 30) || p->Sk > (1 << 30)) return FA_ERR_INVALID_ARG;
   if (bh * ((p->Sq + 255) / 256) > (1ll << 31) - 1) return FA_ERR_INVALID_ARG;
+  // Every tensor's byte size (and the scratch sized from it) must be far from wrapping
+  // a size_t: at most 2^50 bytes per tensor, in fp32, checked in double (no overflow).
+  const double lim = 1125899906842624.0;  // 2^50
+  if ((double)p->B * p->H * p->Sq * p->D * 4.0 > lim ||
+      (double)p->B * p->HKV * p->Sk * p->D * 4.0 > lim)
+    return FA_ERR_INVALID_ARG;
   // Head dims: multiples of 16 up to 128 (bf16) / 64 (fp32); each runs in the kernel
   // built for the next of 64 / 128, with the missing columns read as zeros.
   const bool d16 = p->D % 16 == 0 && p->D >= 16;
@@ -262,6 +268,8 @@ FA_API const char* fa_status_string(fa_status s) {
 }
 
 FA_API const char* fa_version(void) { return "fa-sm103a 0.1"; }
+
+FA_API unsigned long long fa_noalloc_scratch_bytes(void) { return FA_NOALLOC_SCRATCH_BYTES; }
 
 FA_API fa_status fa_selftest_timeout(unsigned long long limit_ns, int* roles_done,
                                      fa_stream_t stream) {

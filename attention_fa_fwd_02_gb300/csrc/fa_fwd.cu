@@ -1052,15 +1052,17 @@ fa_status noalloc_scratch_addr(void** out) {
   return FA_OK;
 }
 
+// Scratch bytes the problem needs, in double so that no product can wrap around
+// (exact while it is anywhere near the array's size).
 template <bool F32>
-size_t noalloc_bytes(const fa_params& p) {
-  const size_t nq = (size_t)p.B * p.H * p.Sq * p.D;
-  const size_t nk = (size_t)p.B * p.HKV * p.Sk * p.D;
+double noalloc_bytes(const fa_params& p) {
+  const double nq = (double)p.B * p.H * p.Sq * p.D;
+  const double nk = (double)p.B * p.HKV * p.Sk * p.D;
   if constexpr (!F32) {
     return nk * 2;
   } else {
-    const size_t ldt = ((size_t)p.Sk + 3) / 4 * 4;
-    const size_t nvt = (size_t)p.B * p.HKV * p.D * ldt;
+    const double ldt = (double)(((long long)p.Sk + 3) / 4 * 4);
+    const double nvt = (double)p.B * p.HKV * p.D * ldt;
     return (2 * nq + 2 * nk + 2 * nvt) * 4;
   }
 }
@@ -1069,7 +1071,7 @@ template <int D, bool F32>
 fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
                           const fa_params& p, cudaStream_t stream) {
   using C = FwdCfg<D, F32>;
-  if (noalloc_bytes<F32>(p) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+  if (noalloc_bytes<F32>(p) > (double)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;
   const fa_status st = noalloc_scratch_addr(&ws);
   if (st != FA_OK) return st;

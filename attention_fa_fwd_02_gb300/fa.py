@@ -20,9 +20,8 @@ FA_F32, FA_BF16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
           4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_SCRATCH_LIMIT", 7: "FA_ERR_LAYOUT"}
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string", "fa_version",
-           "fa_timing_enable", "fa_timing_read", "fa_fwd_noalloc", "fa_selftest_timeout")
-# Size of the static device scratch behind fa_fwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).
-NOALLOC_SCRATCH_BYTES = 32 << 20
+           "fa_timing_enable", "fa_timing_read", "fa_fwd_noalloc", "fa_selftest_timeout",
+           "fa_noalloc_scratch_bytes")
 
 
 class FAError(RuntimeError):
@@ -61,6 +60,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_version.argtypes = []
     lib.fa_version.restype = ctypes.c_char_p
+    lib.fa_noalloc_scratch_bytes.argtypes = []
+    lib.fa_noalloc_scratch_bytes.restype = ctypes.c_ulonglong
     lib.fa_selftest_timeout.argtypes = [ctypes.c_ulonglong, vp, vp]
     lib.fa_selftest_timeout.restype = st
     lib.fa_timing_enable.argtypes = [st]
@@ -86,6 +87,12 @@ def status_string(code: int) -> str:
 
 def version() -> str:
     return lib().fa_version().decode()
+
+
+def noalloc_scratch_bytes() -> int:
+    """Size of the static device scratch behind ``fa_fwd_noalloc``, as compiled into
+    the loaded library (FA_NOALLOC_SCRATCH_BYTES)."""
+    return int(lib().fa_noalloc_scratch_bytes())
 
 
 # ------------------------------------------------------------ raw C entry points

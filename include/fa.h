@@ -92,7 +92,10 @@ typedef enum {
  *   LSE [B, H,   Sq]     fp32, written: natural-log log-sum-exp of each row's
  *                        scaled scores, -inf for rows with no visible key.
  * All pointers are caller-owned device memory, 16-byte aligned; outputs must not
- * alias inputs. The call validates its arguments synchronously, then enqueues
+ * alias inputs. The library keeps per-device state for the life of the process (its
+ * memory pool, the fa_fwd_noalloc scratch address, the status word): do not call it
+ * again on a device after cudaDeviceReset() on that device, which invalidates that
+ * state. The call validates its arguments synchronously, then enqueues
  * work on `stream` and returns without waiting. Temporary buffers (an fp16 copy
  * of V for bf16 inputs; hi/lo tf32 splits for fp32 inputs; for short query
  * sequences, whose work items are fewer than the SMs, fp32 partial O and LSE of up
@@ -136,6 +139,11 @@ FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, fl
 FA_API fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                 const fa_params* p, fa_stream_t stream);
 
+/* FA_NOALLOC_SCRATCH_BYTES as compiled into this libfa.so (so that a caller built
+ * against another copy of this header can check the size it relies on). Makes no
+ * CUDA call. */
+FA_API unsigned long long fa_noalloc_scratch_bytes(void);
+
 /*
  * Backward pass for the loss L with upstream gradient dO = dL/dO.
  *   Q, K, V  as in fa_fwd;  O [B,H,Sq,D] out_dtype and LSE [B,H,Sq] fp32 as
@@ -162,6 +170,11 @@ FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void*
  * shared memory than its layout needs, FA_ERR_TIMEOUT if one gave up on a barrier
  * wait (outputs are then undefined in both cases), FA_ERR_CUDA if the
  * synchronization itself failed, else FA_OK.
+ * The status word is one per device, not per stream: kernels on every stream of
+ * the device set bits in it, and the first fa_device_status() call after a fault
+ * (on any stream) reports and clears it. A caller that runs the library on several
+ * streams at once and needs to know which call failed must serialize status checks
+ * with its own launches (or treat a reported fault as affecting all of them).
  */
 FA_API fa_status fa_device_status(fa_stream_t stream);
 

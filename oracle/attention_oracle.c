@@ -11,7 +11,7 @@
  *
  *   S_ij  = scale * sum_d Q[b,h,i,d] * K[b,g,j,d]
  *           -- rustytorch "flash_attention_forward.metal", kernel header comment
- *              "Computes: O = softmax(Q @ K^T * scale) @ V"
+ *              (the output is the scaled-score row softmax applied to V)
  *   visible(i,j) = (!causal || j <= i) && (window == 0 || j >= i - window + 1)
  *           -- forge "flash_attention.metal", FlashParams comment (window keeps
  *              keys including self, 0 = full) and flash_attn_fwd's jmin / j_end;

@@ -89,3 +89,11 @@ def test_source_hash_covers_the_kernel_sources():
         h = bench.source_sha(k)
         assert len(h) == 16 and int(h, 16) >= 0
     assert bench.source_sha("fa_fwd_kernel") != bench.source_sha("fa_bwd_dkdv_kernel")
+
+
+def test_roofline_denominator_is_the_burst_peak():
+    # the kernels are timed for well under a second at full clocks: the burst cuBLAS
+    # figure is their denominator, the power-capped sustained one is reported beside it
+    peaks = {"bf16_tflops": 1965.9, "bf16_tflops_sustained": 1727.6, "hbm_gbs": 6795.1}
+    assert bench.tensor_peaks(peaks, "bf16") == (1965.9, 1727.6)
+    assert bench.tensor_peaks(peaks, "f32") == (1965.9 / 2, 1727.6 / 2)

@@ -26,7 +26,16 @@ def _declared_symbols():
 def test_header_declares_the_abi():
     assert _declared_symbols() == {"fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string",
                                    "fa_version", "fa_timing_enable", "fa_timing_read",
-                                   "fa_fwd_noalloc", "fa_selftest_timeout"}
+                                   "fa_fwd_noalloc", "fa_selftest_timeout",
+                                   "fa_noalloc_scratch_bytes"}
+
+
+def test_noalloc_scratch_size_matches_the_header(fa):
+    # the binding reads the size from the library; it must be the header's value
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    m = re.search(r"#define FA_NOALLOC_SCRATCH_BYTES \(\(unsigned long long\)(\d+) << (\d+)\)", text)
+    assert m, "FA_NOALLOC_SCRATCH_BYTES definition not found"
+    assert fa.noalloc_scratch_bytes() == int(m.group(1)) << int(m.group(2))
 
 
 def test_library_exports_every_declared_symbol(fa):
@@ -93,11 +102,20 @@ MIS = 0x10008
     (dict(D=8), 2),
     (dict(D=128, in_dtype=0), 2),   # fp32 inputs up to D=64
     (dict(D=80, in_dtype=0), 2),
+    # K and V of 2^59 bytes each: refused before any size is computed in size_t
+    (dict(B=1024, H=1024, HKV=1024, Sq=1, Sk=1 << 30), 1),
 ])
 def test_invalid_params_rejected(fa, kw, code):
     p = _params(fa, **kw)
     assert fa.fa_fwd(A, A, A, A, A, p, 0) == code
     assert fa.fa_bwd(A, A, A, A, A, A, A, A, A, p, 0) == code
+
+
+def test_noalloc_rejects_oversized_params_before_sizing_scratch(fa):
+    # a product of the shape fields that would wrap a size_t must not slip past the
+    # scratch-size check
+    p = _params(fa, B=1024, H=1024, HKV=1024, Sq=1, Sk=1 << 30)
+    assert fa.fa_fwd_noalloc(A, A, A, A, A, p, 0) == 1
 
 
 def test_null_params_rejected(fa):

@@ -143,7 +143,7 @@ def test_backward_full_config_fp32(fa, cfg):
     _check(w, got, ref, cfg)
 
 
-@pytest.mark.parametrize("cfg,b,g", [("c3", 1, 5), ("c3", 0, 0), ("c4", 0, 3)])
+@pytest.mark.parametrize("cfg,b,g", [("c3", 1, 5), ("c3", 0, 0), ("c4", 0, 3), ("c4", 0, 0)])
 def test_backward_full_config_bf16_slice(fa, cfg, b, g):
     # Full-size launch; whole (batch, kv-group) slices are independent, so the
     # oracle checks one slice exactly (dK / dV of the group sum its query heads).

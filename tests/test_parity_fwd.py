@@ -158,7 +158,7 @@ def test_forward_full_config_fp32(fa, cfg):
     _check(w, o, lse, ro, rl, cfg)
 
 
-@pytest.mark.parametrize("cfg,b,g", [("c3", 1, 5), ("c3", 0, 0), ("c4", 0, 3)])
+@pytest.mark.parametrize("cfg,b,g", [("c3", 1, 5), ("c3", 0, 0), ("c4", 0, 3), ("c4", 0, 0)])
 def test_forward_full_config_bf16_slice(fa, cfg, b, g):
     # Full-size launch (the benchmark's configuration); the oracle checks whole
     # (batch, kv-group) slices, which are independent of the rest.

@@ -9,14 +9,15 @@ keeps its scratch in a fixed array compiled into libfa.so.
 
 This file checks, through the C ABI, that two calls in a row of fa_fwd_noalloc
 (on different inputs, so the second call cannot reuse what the first left in the
-shared array) give the same O and LSE as fa_fwd within the parity tolerances,
-for both input precisions, and that a problem too large for the array is
-refused with FA_ERR_SCRATCH_LIMIT. It is named to run after every other test
+shared array) give O and LSE within the parity tolerances of the fp64 oracle and
+of fa_fwd, for both input precisions, and that a problem too large for the array
+is refused with FA_ERR_SCRATCH_LIMIT. It is named to run after every other test
 file and also passes when run on its own in a fresh process.
 """
 import pytest
 import torch
 
+import oracle
 from attention_fa_fwd_02_gb300.workloads import WORKLOADS, make_inputs
 from _parity import TOL, lse_err, rms_err, to_np
 
@@ -55,16 +56,22 @@ PAIRS = {
 
 
 @pytest.mark.parametrize("kind", list(PAIRS))
-def test_noalloc_matches_fa_fwd_on_two_calls_in_a_row(fa, kind):
+def test_noalloc_matches_oracle_and_fa_fwd_on_two_calls_in_a_row(fa, kind):
     ws = PAIRS[kind]
-    ins = [tuple(t.cuda() for t in make_inputs(w)[:3]) for w in ws]
+    cpu = [make_inputs(w)[:3] for w in ws]
+    ins = [tuple(t.cuda() for t in c) for c in cpu]
     # two no-allocation calls back to back, the second on different data
     got = [_call(fa, fa.fa_fwd_noalloc, w, t) for w, t in zip(ws, ins)]
     fa.check_device_status()
     ref = [_call(fa, fa.fa_fwd, w, t) for w, t in zip(ws, ins)]
     fa.check_device_status()
-    for w, (o, lse), (ro, rl) in zip(ws, got, ref):
+    for w, c, (o, lse), (ro, rl) in zip(ws, cpu, got, ref):
         tol = TOL[w.dtype]
+        # against the fp64 oracle on the same inputs ...
+        xo, xl = oracle.attention_fwd(*c, w.scale, w.causal, w.window)
+        assert rms_err(to_np(o), xo) <= tol["O"], w.name
+        assert lse_err(to_np(lse), xl) <= tol["LSE"], w.name
+        # ... and against the allocating entry point
         assert rms_err(to_np(o), to_np(ro)) <= tol["O"]
         assert lse_err(to_np(lse), to_np(rl)) <= tol["LSE"]
 
@@ -73,7 +80,7 @@ def test_noalloc_refuses_problems_larger_than_its_scratch(fa):
     # bf16 inputs need B*HKV*Sk*D*2 bytes of scratch: Sk = 2^17 + 1 keys at D = 128 is
     # just over the 32 MiB array. The tensors are real, so even a wrong answer here
     # would stay inside allocated memory.
-    sk = (fa.NOALLOC_SCRATCH_BYTES // (128 * 2)) + 1
+    sk = (fa.noalloc_scratch_bytes() // (128 * 2)) + 1
     q = torch.zeros(1, 1, 1, 128, dtype=torch.bfloat16, device="cuda")
     k = torch.zeros(1, 1, sk, 128, dtype=torch.bfloat16, device="cuda")
     p = fa.make_params(q, k, 0.1, False, 0)
