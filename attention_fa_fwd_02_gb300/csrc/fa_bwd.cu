@@ -52,6 +52,9 @@ struct BwdArgs {
   int n_splits;  // dq (bf16 inputs): key ranges per query tile; > 1 writes partial dQ per range
   int tps;       // key tiles per range
   unsigned long long limit_ns;
+  // bf16 inputs: multipliers that undo the power-of-two scaling of the fp16 operand
+  // copies (written by bwd_scales_kernel before these kernels start)
+  const OperandScales* sc;
 };
 
 // Tensor maps of one kernel launch; index [split] selects the hi (0) / lo (1) copy.
@@ -1064,7 +1067,9 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
     regs_increase<C::REGS_SOFTMAX>();
     const int wq = warp % 4, half = warp / 4;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-    const float sl2 = a.scale_log2;
+    // scores and dP come from the scaled fp16 copies: sl2 and dp_mul bring them back
+    // (dP into the stored delta's units, which makes dS = 2^eD dS), dq_mul undoes 2^eD 2^eK
+    const float sl2 = a.sc->sl2, dp_mul = a.sc->dp_mul, dq_mul = a.sc->dq_mul;
     bool ok = true;
     int g = 0, j = 0;  // chunks and items with keys so far
     for (int k = 0, w = take_warp(0); ok && w < n_items; w = take_warp(++k)) {
@@ -1127,11 +1132,11 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
           }
         }
         uint32_t pk[32];
-        const float2 ndl = make_float2(-dl, -dl);
+        const float2 ndl = make_float2(-dl, -dl), dpm = make_float2(dp_mul, dp_mul);
 #pragma unroll
         for (int kk = 0; kk < 32; ++kk) {  // dS = P (dP - delta) on packed pairs
           const float2 u = mul2(make_float2(s[2 * kk], s[2 * kk + 1]),
-                                add2(make_float2(dp[2 * kk], dp[2 * kk + 1]), ndl));
+                                fma2(make_float2(dp[2 * kk], dp[2 * kk + 1]), dpm, ndl));
           pk[kk] = pack_half2(u.x, u.y);
         }
         // the dS slot is free once dQ += dS(g-2) K has completed
@@ -1170,7 +1175,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(&bar_dqfree);  // dQ has left TMEM: the next item may accumulate
         if (mine)
-          stage_store_rows<NCOL, BF>(r, a.scale, sbase + C::V_OFF + warp * (C::EPI_WARP / 2),
+          stage_store_rows<NCOL, BF>(r, dq_mul, sbase + C::V_OFF + warp * (C::EPI_WARP / 2),
                                      &m.dQ, x0, r_base, any,
                                      SPLIT ? (w % a.n_splits) * a.BHx + it.bh : it.bh, a.Dv);
       };
@@ -1469,7 +1474,8 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     const uint32_t pt_row = sbase + C::PT_OFF + (QC * part / 64) * C::CB + r_in * 128;
     const uint32_t chunk0 = (uint32_t)((QC * part % 64) / 8);
     const uint32_t sw = (uint32_t)(r_in & 7);
-    const float sl2 = a.scale_log2;
+    // scores and dP^T come from the scaled fp16 copies (see the dQ kernel)
+    const float sl2 = a.sc->sl2, dp_mul = a.sc->dp_mul;
     const bool row_dead = j >= a.Sk;
     auto ld_cols = [&](uint32_t addr, float (&x)[QC]) {
       if constexpr (QC == 64) {
@@ -1544,6 +1550,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         float g[QC];
         ld_cols(lane_addr + C::DP_COL + part * QC, g);
         const uint32_t dv = lv + 128 * 4;
+        const float2 dpm = make_float2(dp_mul, dp_mul);
         uint32_t pk[QC / 2];
 #pragma unroll
         for (int k4 = 0; k4 < QC / 4; ++k4) {
@@ -1551,9 +1558,9 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
           const int k = 4 * k4;
           // dS = P (dP - delta) on packed pairs
           const float2 ua = mul2(make_float2(s[k], s[k + 1]),
-                                 add2(make_float2(g[k], g[k + 1]), make_float2(-d4.x, -d4.y)));
+                                 fma2(make_float2(g[k], g[k + 1]), dpm, make_float2(-d4.x, -d4.y)));
           const float2 ub = mul2(make_float2(s[k + 2], s[k + 3]),
-                                 add2(make_float2(g[k + 2], g[k + 3]), make_float2(-d4.z, -d4.w)));
+                                 fma2(make_float2(g[k + 2], g[k + 3]), dpm, make_float2(-d4.z, -d4.w)));
           pk[2 * k4] = pack_half2(ua.x, ua.y);
           pk[2 * k4 + 1] = pack_half2(ub.x, ub.y);
         }
@@ -1581,7 +1588,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
       const bool any = r_base < a.Sk;
       const uint32_t acc = lane_addr + (which ? C::DK : C::DV) + cpart * DW;
       const CUtensorMap* tm = which ? &m.dK : &m.dV;
-      const float mul = which ? a.scale : 1.f;
+      const float mul = which ? a.sc->dk_mul : a.sc->dv_mul;  // scale 2^-(eD+eQ) / 2^-eO
       const uint32_t stage = sbase + warp * (C::EPI_WARP / HP);
       if (a.out_bf16) {
         if constexpr (DW % 64 == 0)
@@ -1675,18 +1682,25 @@ __global__ void bwd_preprocess_kernel(const void* __restrict__ dO, const void* _
 //       lse2[bh][i] = LSE * log2(e) (+inf for LSE = -inf; rows i >= Sq get +inf / 0),
 //       fp16 copies of the Q and dO rows;
 //   rows of K / V (B*HKV*Sk of them): fp16 copies.
-// D/8 threads per row, 8 elements (16 bytes of bf16) each, so a warp moves whole
-// 256-byte rows with 16-byte accesses.
-template <int D>
-__global__ void bwd_prepass16_kernel(const __nv_bfloat16* __restrict__ dO, const void* __restrict__ O,
+// The copies are made with exponent 0; block b writes part[5 b ..] = the largest |Q|,
+// |K|, |V|, |dO| and |delta| it saw (fp32 bits), from which bwd_scales_kernel picks
+// the exponents. D/8 threads per row, 8 elements (16 bytes of bf16) each, so a warp
+// moves whole 256-byte rows with 16-byte accesses.
+// (Launched as 8 blocks of 256 threads per SM, one wave: the bounds keep it at 32
+// registers so that all 8 fit.) O_BF16: O is bf16 (else fp32).
+template <int D, bool O_BF16>
+__global__ void __launch_bounds__(256, 8)
+    bwd_prepass16_kernel(const __nv_bfloat16* __restrict__ dO, const void* __restrict__ O,
                                      const float* __restrict__ LSE, const __nv_bfloat16* __restrict__ Q,
                                      const __nv_bfloat16* __restrict__ K,
                                      const __nv_bfloat16* __restrict__ V, __half* __restrict__ dO16,
                                      __half* __restrict__ Q16, __half* __restrict__ K16,
                                      __half* __restrict__ V16, float* __restrict__ lse2,
                                      float* __restrict__ delta, int Sq, int ldq, size_t q_rows,
-                                     size_t kv_rows, int o_bf16, int* __restrict__ sched, int Dv) {
+                                     size_t kv_rows, int* __restrict__ sched, int Dv,
+                                     uint32_t* __restrict__ part) {
   constexpr int TPR = D / 8;  // threads per row (rows have Dv <= D columns: the rest idle)
+  grid_launch_dependents();  // bwd_scales_kernel waits for this grid before reading part[]
   if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;  // the dQ kernel's work-item counter
   const int t = threadIdx.x % TPR;
   const bool cols = t * 8 < Dv;  // this thread's 8 columns exist
@@ -1699,18 +1713,36 @@ __global__ void bwd_prepass16_kernel(const __nv_bfloat16* __restrict__ dO, const
       o[e] = pack_half2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
     return make_uint4(o[0], o[1], o[2], o[3]);
   };
-  for (size_t r = blockIdx.x * (size_t)(blockDim.x / TPR) + threadIdx.x / TPR; r < q_rows + kv_rows;
-       r += rows_per_grid) {
+  // Largest |Q|, |K|, |V|, |dO|, |delta| of the block (fp32 bits), folded in once per
+  // warp and row group: nothing is carried across iterations in registers, which keeps
+  // the kernel at 8 resident blocks per SM.
+  __shared__ uint32_t amax_sh[5];
+  if (threadIdx.x < 5) amax_sh[threadIdx.x] = 0;
+  __syncthreads();
+  auto fold = [&](int k, uint32_t v) {  // warp-uniform call sites only
+    v = __reduce_max_sync(0xffffffffu, v);
+    if ((threadIdx.x & 31) == 0 && v != 0) atomicMax(&amax_sh[k], v);
+  };
+  // The loop runs the same iterations in every thread of the block (rows past the end
+  // do nothing), so the warp-wide reductions always see the whole warp; the Q-row /
+  // KV-row branch is warp-uniform too (a warp's rows are consecutive and the Q rows
+  // are a multiple of 128).
+  const size_t rows = q_rows + kv_rows;
+  for (size_t rb = blockIdx.x * (size_t)(blockDim.x / TPR); rb < rows; rb += rows_per_grid) {
+    const size_t r = rb + threadIdx.x / TPR;
     if (r < q_rows) {
       const size_t bh = r / ldq;
       const int i = (int)(r % ldq);
       float acc = 0.f;
+      uint32_t aq = 0, ag = 0;
       if (i < Sq && cols) {
         const size_t off = (bh * Sq + i) * Dv + t * 8;
         const uint4 g = *reinterpret_cast<const uint4*>(dO + off);
         const uint4 q = *reinterpret_cast<const uint4*>(Q + off);
+        ag = amax_bits(amax_acc(0u, g));
+        aq = amax_bits(amax_acc(0u, q));
         float ov[8];
-        if (o_bf16) {
+        if constexpr (O_BF16) {
           const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(O) + off);
           const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -1734,6 +1766,9 @@ __global__ void bwd_prepass16_kernel(const __nv_bfloat16* __restrict__ dO, const
       }
 #pragma unroll
       for (int w = TPR / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+      fold(0, aq);
+      fold(3, ag);
+      fold(4, i < Sq ? __float_as_uint(fabsf(acc)) : 0u);
       if (t == 0) {
         if (i < Sq) {
           const float L = LSE[bh * Sq + i];
@@ -1744,11 +1779,72 @@ __global__ void bwd_prepass16_kernel(const __nv_bfloat16* __restrict__ dO, const
           delta[r] = 0.f;
         }
       }
-    } else if (cols) {
-      const size_t off = (r - q_rows) * Dv + t * 8;
-      *reinterpret_cast<uint4*>(K16 + off) = cvt8(*reinterpret_cast<const uint4*>(K + off));
-      *reinterpret_cast<uint4*>(V16 + off) = cvt8(*reinterpret_cast<const uint4*>(V + off));
+    } else {
+      uint32_t ak = 0, av = 0;
+      if (cols && r < rows) {
+        const size_t off = (r - q_rows) * Dv + t * 8;
+        const uint4 kx = *reinterpret_cast<const uint4*>(K + off);
+        const uint4 vx = *reinterpret_cast<const uint4*>(V + off);
+        *reinterpret_cast<uint4*>(K16 + off) = cvt8(kx);
+        *reinterpret_cast<uint4*>(V16 + off) = cvt8(vx);
+        ak = amax_bits(amax_acc(0u, kx));
+        av = amax_bits(amax_acc(0u, vx));
+      }
+      fold(1, ak);
+      fold(2, av);
     }
+  }
+  __syncthreads();
+  if (threadIdx.x < 5) part[(size_t)blockIdx.x * 5 + threadIdx.x] = amax_sh[threadIdx.x];
+}
+
+// Exponents of the fp16 operand copies of one backward call (fa_scale.cuh): every block
+// reduces the pre-pass blocks' partial maxima of |Q|, |K|, |V|, |dO| and |delta| and
+// derives eQ, eK, eV, eO and eD; block 0 publishes the multipliers; then the grid
+// rewrites every copy whose exponent is not 0 as fp16(x * 2^e), and delta as
+// delta * 2^eD if eD is not 0. With all exponents 0 (inputs of ordinary magnitude)
+// the blocks only reduce and return.
+struct BwdScaleArgs {
+  const uint32_t* part;
+  int n_part;
+  int dlog;  // ceil(log2 Dv)
+  const __nv_bfloat16* src[4];  // Q, K, V, dO
+  __half* dst[4];               // their fp16 copies
+  size_t n8[4];                 // groups of 8 elements
+  float* delta;
+  size_t n_delta;
+  float scale, scale_log2;
+  OperandScales* out;
+};
+
+__global__ void __launch_bounds__(1024) bwd_scales_kernel(const __grid_constant__ BwdScaleArgs a) {
+  // launched as a programmatic dependent of the pre-pass: wait until that grid has
+  // completed and its writes (copies, delta, part[]) are visible
+  grid_dependency_wait();
+  uint32_t m[5];
+  reduce_partials<5>(a.part, a.n_part, m);
+  int e[5];
+  for (int k = 0; k < 4; ++k) e[k] = copy_exponent(m[k]);
+  e[SC_DS] = ds_exponent(m[3], m[2], m[4], a.dlog);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    OperandScales sc;
+    sc.sl2 = ldexpf(a.scale_log2, -(e[SC_Q] + e[SC_K]));
+    sc.dp_mul = ldexpf(1.f, e[SC_DS] - e[SC_DO] - e[SC_V]);
+    sc.dq_mul = ldexpf(a.scale, -(e[SC_DS] + e[SC_K]));
+    sc.dk_mul = ldexpf(a.scale, -(e[SC_DS] + e[SC_Q]));
+    sc.dv_mul = ldexpf(1.f, -e[SC_DO]);
+    sc.o_mul = 1.f;
+    for (int k = 0; k < 5; ++k) sc.e[k] = e[k];
+    sc.pad = 0;
+    *a.out = sc;
+  }
+  for (int k = 0; k < 4; ++k)
+    if (e[k] != 0) rescale_copy(a.src[k], a.dst[k], a.n8[k], e[k]);
+  if (e[SC_DS] != 0) {
+    const float f = pow2i(e[SC_DS]);
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < a.n_delta; i += stride)
+      a.delta[i] *= f;
   }
 }
 
@@ -1832,6 +1928,10 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   else bytes += (4 * nq + 4 * nk + 4 * nqt + 2 * nkt) * 4;  // Q,dO,K,V hi/lo + Q^T,dO^T,K^T hi/lo
   const size_t sched_off = (bytes + 15) / 16 * 16;  // the dQ kernel's work-item counter
   bytes = sched_off + 16;
+  // bf16 inputs: the call's OperandScales and the pre-pass blocks' partial maxima
+  const int n_pre = 8 * host::sm_count();  // pre-pass blocks
+  const size_t sc_off = (bytes + 255) / 256 * 256;
+  if constexpr (!F32) bytes = sc_off + 256 + (size_t)n_pre * 5 * 4;
   // Fewer query tiles than SMs (short query sequences, bf16 inputs): the dQ work items
   // also split the keys into ranges of tps tiles (key_range_tiles picks tps), each
   // range writing a partial dQ (fp32) that a sum kernel adds up afterwards.
@@ -1847,6 +1947,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   float* lse2 = static_cast<float*>(ws);
   float* delta = lse2 + nvec;
   int* sched = reinterpret_cast<int*>(static_cast<char*>(ws) + sched_off);
+  OperandScales* sc = F32 ? nullptr : reinterpret_cast<OperandScales*>(static_cast<char*>(ws) + sc_off);
+  uint32_t* part = F32 ? nullptr : reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + sc_off + 256);
   float* dq_part = dq_splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(ws) + part_off) : nullptr;
   const int grid_pp = 4 * sms;
   const auto F32T = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -1875,10 +1977,37 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     __half* v16 = k16 + nk;
     {
       host::KernelTimer kt("bwd_prepass", stream);
-      bwd_prepass16_kernel<D><<<8 * host::sm_count(), 256, 0, stream>>>(
+      auto pre = p.out_dtype == FA_BF16 ? bwd_prepass16_kernel<D, true> : bwd_prepass16_kernel<D, false>;
+      pre<<<n_pre, 256, 0, stream>>>(
           static_cast<const __nv_bfloat16*>(dO), O, LSE, static_cast<const __nv_bfloat16*>(Q),
           static_cast<const __nv_bfloat16*>(K), static_cast<const __nv_bfloat16*>(V), do16, q16, k16,
-          v16, lse2, delta, p.Sq, ldq, nvec, BHk * p.Sk, p.out_dtype == FA_BF16, sched, Dv);
+          v16, lse2, delta, p.Sq, ldq, nvec, BHk * p.Sk, sched, Dv, part);
+    }
+    {
+      // exponents of the copies; rewrites the copies / delta whose exponent is not 0
+      host::KernelTimer kt("bwd_scales", stream);
+      BwdScaleArgs sa;
+      sa.part = part;
+      sa.n_part = n_pre;
+      int dlog = 0;
+      while ((1 << dlog) < Dv) ++dlog;
+      sa.dlog = dlog;
+      const __nv_bfloat16* srcs[4] = {static_cast<const __nv_bfloat16*>(Q),
+                                      static_cast<const __nv_bfloat16*>(K),
+                                      static_cast<const __nv_bfloat16*>(V),
+                                      static_cast<const __nv_bfloat16*>(dO)};
+      __half* dsts[4] = {q16, k16, v16, do16};
+      const size_t n8s[4] = {nq / 8, nk / 8, nk / 8, nq / 8};
+      for (int k = 0; k < 4; ++k) { sa.src[k] = srcs[k]; sa.dst[k] = dsts[k]; sa.n8[k] = n8s[k]; }
+      sa.delta = delta;
+      sa.n_delta = nvec;
+      sa.scale = p.scale;
+      sa.scale_log2 = p.scale * LOG2E;
+      sa.out = sc;
+      if (launch_programmatic(bwd_scales_kernel, dim3(sms), dim3(1024), stream, sa) != cudaSuccess) {
+        host::scratch_free(ws, stream);
+        return FA_ERR_CUDA;
+      }
     }
     // Query tiles whose rows see no key (a window ending before the keys do: a suffix
     // of tiles) are skipped by the dQ kernel; their rows are zeroed here, before the
@@ -1982,6 +2111,7 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   a.n_splits = 1;
   a.tps = n_kt;
   a.limit_ns = WAIT_LIMIT_NS;
+  a.sc = sc;
   cudaError_t e = cudaSuccess;
   {
     BwdArgs ak = a;

@@ -147,6 +147,26 @@ fa_status launch_selftest_timeout(unsigned long long limit_ns, int* roles_done, 
 unsigned int read_and_clear_fwd_status(cudaError_t* err);
 unsigned int read_and_clear_bwd_status(cudaError_t* err);
 
+// Launches `kernel` on `stream` as a programmatic dependent of the grid launched before
+// it there: its blocks may be scheduled once every block of that grid has signalled
+// (griddepcontrol.launch_dependents) or exited, and the kernel must execute
+// griddepcontrol.wait before it reads anything that grid writes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                      cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Default barrier-wait limit (ns) for the kernels.
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 

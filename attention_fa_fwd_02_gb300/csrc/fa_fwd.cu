@@ -21,6 +21,7 @@
 // Every barrier wait is bounded; on expiry the kernel raises the device status
 // word, drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <algorithm>
+#include <cmath>
 #include <cfloat>
 #include <climits>
 #include <cstdio>
@@ -51,6 +52,7 @@ struct FwdArgs {
   int BH;
   int BHi;  // work units per query group: heads (BH), or head pairs (BH / 2)
   unsigned long long limit_ns;
+  const OperandScales* sc;  // bf16 inputs: o_mul = 2^-eV undoes the scaled fp16 copy of V
 };
 
 template <int D_, bool F32_>
@@ -528,6 +530,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     const uint32_t s_addr = lane_addr + C::s_col(q);
     const uint32_t o_addr = lane_addr + C::o_col(q);
     const float sl2 = a.scale_log2;
+    const float o_mul = a.sc ? a.sc->o_mul : 1.f;  // O from the scaled V copy, back to V's units
     bool ok = true;
     int g = 0, j = 0;
     uint32_t pos = 0;
@@ -666,7 +669,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
       // it), TMA stores.
       const int slot = pos % VST;
       if (ok) ok = __all_sync(0xffffffffu, wait(&bar_grant[q], k & 1));
-      const float inv = (l > 0.f) ? (1.f / l) : 0.f;
+      const float inv = (l > 0.f) ? (o_mul / l) : 0.f;
       if (ok && i < a.Sq)
         a.LSE[(size_t)zo * a.Sq + i] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
       const int r_base = r0 + wq * 32;
@@ -719,6 +722,30 @@ __global__ void fill_empty_kernel(void* O, float* LSE, size_t rows, int D, int o
       for (int d = 0; d < D; ++d) static_cast<float*>(O)[r * D + d] = 0.f;
     }
   }
+}
+
+// The exponent of V's fp16 copy (the copy was made with exponent 0 by the conversion
+// kernel, whose blocks left their largest |V| in part[]): every block reduces the
+// partial maxima; block 0 publishes the multipliers, and if the exponent is not 0 the
+// grid rewrites the copy as fp16(V * 2^eV).
+__global__ void __launch_bounds__(1024) fwd_scales_kernel(const uint32_t* __restrict__ part,
+                                                          int n_part, const __nv_bfloat16* V,
+                                                          __half* V16, size_t n8,
+                                                          OperandScales* out) {
+  // launched as a programmatic dependent of the conversion: wait until that grid has
+  // completed and its writes (the copy, part[]) are visible
+  grid_dependency_wait();
+  uint32_t m[1];
+  reduce_partials<1>(part, n_part, m);
+  const int ev = copy_exponent(m[0]);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    OperandScales sc = {};
+    sc.sl2 = sc.dp_mul = sc.dq_mul = sc.dk_mul = sc.dv_mul = 1.f;
+    sc.o_mul = pow2i(-ev);
+    sc.e[SC_V] = ev;
+    *out = sc;
+  }
+  if (ev != 0) rescale_copy(V, V16, n8, ev);
 }
 
 // Key ranges of one query row computed separately: partial outputs O_s
@@ -824,12 +851,28 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo, mO;
   const uint64_t BHq = (uint64_t)p.B * p.H, BHk = (uint64_t)p.B * p.HKV;
   bool enc = encode_o_map(&mO, O, p);
+  OperandScales* sc = nullptr;
   if constexpr (!F32) {
-    if (host::scratch_alloc(&ws, nk * 2, stream) != cudaSuccess) return FA_ERR_CUDA;
+    // fp16 copy of V | the call's OperandScales | the conversion blocks' partial maxima
+    const int n_cvt = 2 * grid_pp;
+    const size_t sc_off = (nk * 2 + 255) / 256 * 256;
+    if (host::scratch_alloc(&ws, sc_off + 256 + (size_t)n_cvt * 4, stream) != cudaSuccess)
+      return FA_ERR_CUDA;
+    sc = reinterpret_cast<OperandScales*>(static_cast<char*>(ws) + sc_off);
+    uint32_t* part = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + sc_off + 256);
     {
       host::KernelTimer kt("cvt_bf16_to_f16(V)", stream);
-      cvt_bf16_to_f16_kernel<<<2 * grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
-                                                         static_cast<uint4*>(ws), nk / 8);
+      cvt_bf16_to_f16_kernel<<<n_cvt, 256, 0, stream>>>(static_cast<const uint4*>(V),
+                                                        static_cast<uint4*>(ws), nk / 8, part);
+    }
+    {
+      host::KernelTimer kt("fwd_scales", stream);
+      if (launch_programmatic(fwd_scales_kernel, dim3(host::sm_count()), dim3(1024), stream,
+                              (const uint32_t*)part, n_cvt, static_cast<const __nv_bfloat16*>(V),
+                              static_cast<__half*>(ws), nk / 8, sc) != cudaSuccess) {
+        host::scratch_free(ws, stream);
+        return FA_ERR_CUDA;
+      }
     }
     enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, Dv, p.Sq, BHq, Dv, 64, 128);
     enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, Dv, p.Sk, BHk, Dv, 64, 128);
@@ -893,6 +936,7 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   a.lpt = p.causal ? 1 : 0;
   a.BH = (int)BHq;
   a.limit_ns = WAIT_LIMIT_NS;
+  a.sc = sc;
   void* pws = nullptr;  // partial O [splits][BH][Sq][Dv] and LSE [splits][BH][Sq], fp32
   const size_t rows = (size_t)BHq * p.Sq;
   if (a.n_splits > 1) {
@@ -1053,13 +1097,14 @@ fa_status noalloc_scratch_addr(void** out) {
 }
 
 // Scratch bytes the problem needs, in double so that no product can wrap around
-// (exact while it is anywhere near the array's size).
+// (exact while it is anywhere near the array's size). bf16: the fp16 copy of V, padded
+// to 256 bytes, then the OperandScales and one partial maximum per conversion block.
 template <bool F32>
-double noalloc_bytes(const fa_params& p) {
+double noalloc_bytes(const fa_params& p, int n_cvt) {
   const double nq = (double)p.B * p.H * p.Sq * p.D;
   const double nk = (double)p.B * p.HKV * p.Sk * p.D;
   if constexpr (!F32) {
-    return nk * 2;
+    return std::ceil(nk * 2 / 256) * 256 + 256 + 4.0 * n_cvt;
   } else {
     const double ldt = (double)(((long long)p.Sk + 3) / 4 * 4);
     const double nvt = (double)p.B * p.HKV * p.D * ldt;
@@ -1071,7 +1116,8 @@ template <int D, bool F32>
 fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
                           const fa_params& p, cudaStream_t stream) {
   using C = FwdCfg<D, F32>;
-  if (noalloc_bytes<F32>(p) > (double)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+  const int n_cvt = 8 * host::sm_count();  // conversion blocks (bf16 inputs)
+  if (noalloc_bytes<F32>(p, n_cvt) > (double)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;
   const fa_status st = noalloc_scratch_addr(&ws);
   if (st != FA_OK) return st;
@@ -1083,10 +1129,19 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
   const uint64_t BHq = (uint64_t)p.B * p.H, BHk = (uint64_t)p.B * p.HKV;
   bool enc = encode_o_map(&mO, O, p);
   // The whole scratch region used below is rewritten by the pre-pass kernels on
-  // every call, so nothing left over from an earlier call is ever read.
+  // every call (the V copy, every conversion block's partial maximum, the scales),
+  // so nothing left over from an earlier call is ever read.
+  OperandScales* sc = nullptr;
   if constexpr (!F32) {
-    cvt_bf16_to_f16_kernel<<<2 * grid_pp, 256, 0, stream>>>(static_cast<const uint4*>(V),
-                                                       static_cast<uint4*>(ws), nk / 8);
+    const size_t sc_off = (nk * 2 + 255) / 256 * 256;
+    sc = reinterpret_cast<OperandScales*>(static_cast<char*>(ws) + sc_off);
+    uint32_t* part = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + sc_off + 256);
+    cvt_bf16_to_f16_kernel<<<n_cvt, 256, 0, stream>>>(static_cast<const uint4*>(V),
+                                                      static_cast<uint4*>(ws), nk / 8, part);
+    if (launch_programmatic(fwd_scales_kernel, dim3(host::sm_count()), dim3(1024), stream,
+                            (const uint32_t*)part, n_cvt, static_cast<const __nv_bfloat16*>(V),
+                            static_cast<__half*>(ws), nk / 8, sc) != cudaSuccess)
+      return FA_ERR_CUDA;
     enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, Dv, p.Sq, BHq, Dv, 64, 128);
     enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, Dv, p.Sk, BHk, Dv, 64, 128);
     enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, Dv, p.Sk, BHk, Dv, 64, 128);
@@ -1134,6 +1189,7 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
   a.lpt = p.causal ? 1 : 0;
   a.BH = (int)BHq;
   a.limit_ns = WAIT_LIMIT_NS;
+  a.sc = sc;
   const unsigned grid = (unsigned)std::min(a.n_items, host::sm_count());
   auto kern = fwd_kernel_for<D, F32>(hp);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -6,13 +6,19 @@
 #include <cstdint>
 #include <initializer_list>
 #include "ptx.cuh"
+#include "fa_scale.cuh"
 
 namespace fa {
 namespace {
 
-// bf16 -> fp16, exact for 2^-14 <= |x| <= 65504. 8 elements per 16-byte vector.
+// bf16 -> fp16 copy with exponent 0 (exact for 2^-14 <= |x| <= 65504), 8 elements per
+// 16-byte vector; block b also writes part[b], the largest |x| it read (fp32 bits),
+// from which the scale kernel decides whether the copy must be redone scaled.
 __global__ void cvt_bf16_to_f16_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
-                                       size_t n8) {
+                                       size_t n8, uint32_t* __restrict__ part) {
+  // the scale kernel launched after this one (a programmatic dependent) may be
+  // scheduled as soon as SMs free up; it waits for this grid before reading part[]
+  ptx::grid_launch_dependents();
   // four independent 16-byte loads in flight per thread, then the grid-stride tail
   auto cvt = [](uint4 v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -27,14 +33,24 @@ __global__ void cvt_bf16_to_f16_kernel(const uint4* __restrict__ in, uint4* __re
   };
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  uint32_t m = 0;
   for (; i + 3 * stride < n8; i += 4 * stride) {
     uint4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) v[u] = in[i + u * stride];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) out[i + u * stride] = cvt(v[u]);
+    for (int u = 0; u < 4; ++u) {
+      out[i + u * stride] = cvt(v[u]);
+      m = amax_acc(m, v[u]);
+    }
   }
-  for (; i < n8; i += stride) out[i] = cvt(in[i]);
+  for (; i < n8; i += stride) {
+    const uint4 v = in[i];
+    out[i] = cvt(v);
+    m = amax_acc(m, v);
+  }
+  uint32_t mv[1] = {amax_bits(m)};
+  block_max_store<1>(mv, part + blockIdx.x);
 }
 
 // x = hi + lo with hi = x with its low 13 mantissa bits cleared (a tf32 value)

@@ -14,7 +14,8 @@ non-causal single head. The pages use no public dataset; all values are drawn
 from the stated distributions.
 
 Draw order is fixed: Q, K, V, dO from one CPU ``torch.Generator`` seeded with
-``seed``, in fp32, then cast (round-to-nearest-even) to the workload dtype.
+``seed``, in fp32, each multiplied by its ``mag`` factor (1 unless stated), then
+cast (round-to-nearest-even) to the workload dtype.
 """
 from __future__ import annotations
 
@@ -40,6 +41,9 @@ class Workload:
     dist: str              # "normal" or "uniform"
     std_qk: float = 1.0    # std of Q and K for "normal"
     seed: int = 0
+    # multipliers of the Q, K, V, dO draws (applied in fp32 before the cast): inputs of
+    # very large or very small magnitude, as gradients dO often are
+    mag: tuple = (1.0, 1.0, 1.0, 1.0)
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -79,6 +83,8 @@ def make_inputs(w: Workload):
             t = torch.rand(shp, generator=g, dtype=torch.float32) * 2.0 - 1.0
         else:
             raise ValueError(f"unknown distribution {w.dist}")
+        if w.mag[idx] != 1.0:
+            t = t * w.mag[idx]
         out.append(t.to(w.torch_dtype).contiguous())
     return tuple(out)
 

@@ -24,8 +24,15 @@
  *
  * Precision. in_dtype FA_BF16: QK^T and dO V^T run on bf16/fp16 tensor cores
  * with fp32 accumulation; the probabilities P and dS enter the second GEMMs as
- * fp16 (their partner operands are converted bf16 -> fp16, exact for
- * 2^-14 <= |x| <= 65504; larger magnitudes are outside the supported range).
+ * fp16. Their partner operands (V in the forward; Q, K, V, dO in the backward) are
+ * copied to fp16 as x * 2^e, with one power of two e per tensor and call chosen from
+ * the tensor's largest magnitude, and dS likewise from a bound on |dS|; the scaling is
+ * undone in fp32. e = 0 when the largest magnitude is already in [0.25, 32768), else
+ * e moves it into [2^14, 2^15). A copied value is exact where x * 2^e is an fp16
+ * normal number; below that it rounds to fp16's subnormal spacing, an absolute error
+ * of at most 2^-23 (e = 0) or 2^-39 (e != 0) of the tensor's largest magnitude. So
+ * bf16 inputs of any magnitude whose scores and outputs fit in fp32 are supported
+ * (e.g. gradients dO of 1e-7, V of 1e5).
  * in_dtype FA_F32: every GEMM uses three tf32 tensor-core products (the
  * hi/lo split a = a_hi + a_lo; a_hi b_hi + a_hi b_lo + a_lo b_hi), giving close to
  * fp32 accuracy. Outputs are written in out_dtype (FA_F32 recommended; FA_BF16
@@ -96,10 +103,11 @@ typedef enum {
  * memory pool, the fa_fwd_noalloc scratch address, the status word): do not call it
  * again on a device after cudaDeviceReset() on that device, which invalidates that
  * state. The call validates its arguments synchronously, then enqueues
- * work on `stream` and returns without waiting. Temporary buffers (an fp16 copy
- * of V for bf16 inputs; hi/lo tf32 splits for fp32 inputs; for short query
- * sequences, whose work items are fewer than the SMs, fp32 partial O and LSE of up
- * to 16 key ranges, combined in range order, so results stay deterministic) are
+ * work on `stream` and returns without waiting. Temporary buffers (the scaled fp16
+ * copy of V and its scale factors for bf16 inputs; hi/lo tf32 splits for fp32
+ * inputs; for short query sequences, whose work items are fewer than the SMs, fp32
+ * partial O and LSE of up to 32 key ranges, combined in range order, so results stay
+ * deterministic) are
  * taken stream-ordered from a library-owned CUDA memory pool and released on the
  * same stream. Errors: FA_ERR_INVALID_ARG / _UNSUPPORTED / _ALIGNMENT before any work
  * is enqueued; FA_ERR_CUDA if a CUDA call or launch fails. Device-side barrier
@@ -124,8 +132,10 @@ FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, fl
  * file-scope device array of FA_NOALLOC_SCRATCH_BYTES inside libfa.so. Every GPU
  * on which the library is loaded holds that array until the process exits.
  *   - A problem whose scratch would not fit returns FA_ERR_SCRATCH_LIMIT before
- *     anything is enqueued: bf16 inputs need B*HKV*Sk*D*2 bytes; fp32 inputs
- *     need 4*(2*B*H*Sq*D + 2*B*HKV*Sk*D + 2*B*HKV*D*round_up(Sk,4)) bytes.
+ *     anything is enqueued: bf16 inputs need round_up(B*HKV*Sk*D*2, 256) + 256 +
+ *     32 * (the device's SM count) bytes (the fp16 copy of V, its scale factors and
+ *     the conversion's partial maxima); fp32 inputs need
+ *     4*(2*B*H*Sq*D + 2*B*HKV*Sk*D + 2*B*HKV*D*round_up(Sk,4)) bytes.
  *   - The first call on each device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture begins.
@@ -152,9 +162,11 @@ FA_API unsigned long long fa_noalloc_scratch_bytes(void);
  * P is rebuilt tile by tile from LSE (never stored); D_i = rowsum(dO_i * O_i) is
  * computed first by a preprocess kernel; dK/dV are accumulated per key tile over
  * the grouped query heads without atomics (deterministic: two calls on the same
- * inputs give bit-identical results). Workspace (D_i, fp16 / tf32-split operand
- * copies; for short query sequences with bf16 inputs, fp32 partial dQ of up to 16
- * key ranges, summed in range order) is stream-ordered from the library pool. Same ownership, alignment and
+ * inputs give bit-identical results). Workspace (D_i, the scaled fp16 / tf32-split
+ * operand copies and their scale factors; for short query sequences with bf16 inputs,
+ * fp32 partial dQ of up to 32 key ranges, summed in range order) is stream-ordered
+ * from the library pool. O must be the output of fa_fwd for the same inputs (the dS
+ * scaling bounds D_i by the largest |dO| and |V|). Same ownership, alignment and
  * error rules as fa_fwd. For bf16 inputs the dQ kernel is launched on `stream` as
  * a programmatic dependent of the dK/dV kernel: it starts on the SMs that dK/dV's
  * last wave leaves idle and completes only after dK/dV has, so work enqueued on

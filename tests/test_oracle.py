@@ -271,9 +271,39 @@ def pin_empty_rows(orc):
     np.testing.assert_allclose(dv, dv2, rtol=0, atol=1e-14)
 
 
+def pin_magnitude_homogeneity(orc):
+    # O is linear in V and LSE does not depend on it; the gradients are linear in dO;
+    # dQ and dK are linear in V while dV does not depend on it. With powers of two every
+    # product and sum scales exactly, so the results must match bit for bit, at the
+    # magnitudes the GPU parity cases use (V of 1e5, dO of 1e-7 and 1e4, V of 1e-6).
+    for causal, window in MODES[:3]:
+        q, k, v, do = _problem(61, B=1, H=4, HKV=2, Sq=10, Sk=9, D=4)
+        o, lse = orc.attention_fwd(q, k, v, 0.6, causal, window)
+        g = orc.attention_bwd(q, k, v, do, 0.6, causal, window)
+        for c in (2.0 ** 17, 2.0 ** -23, 2.0 ** 13, 2.0 ** -20):
+            o2, lse2 = orc.attention_fwd(q, k, v * c, 0.6, causal, window)
+            assert np.array_equal(o2, o * c) and np.array_equal(lse2, lse)
+            gd = orc.attention_bwd(q, k, v, do * c, 0.6, causal, window)
+            for x, y in zip(gd, g):
+                assert np.array_equal(x, y * c)
+            gv = orc.attention_bwd(q, k, v * c, do, 0.6, causal, window)
+            assert np.array_equal(gv[0], g[0] * c) and np.array_equal(gv[1], g[1] * c)
+            assert np.array_equal(gv[2], g[2])
+        # scores of 2^-40: the softmax is uniform over each row's visible keys to ~1e-12
+        c = 2.0 ** -20
+        o3, lse3 = orc.attention_fwd(q * c, k * c, v, 0.6, causal, window)
+        for i in range(q.shape[2]):
+            vis = [j for j in range(k.shape[2]) if _visible(i, j, causal, window)]
+            for h in range(4):
+                np.testing.assert_allclose(o3[0, h, i], v[0, h // 2, vis].mean(axis=0),
+                                           rtol=0, atol=1e-10)
+                assert abs(lse3[0, h, i] - math.log(len(vis))) < 1e-10
+
+
 PINS = [pin_hand_examples, pin_rows_sum_to_one, pin_lse_independent, pin_constant_v,
         pin_causal_row0_and_window1, pin_window_zero_is_full, pin_gqa_is_repeated_mha,
-        pin_invariants, pin_library_crosscheck, pin_finite_differences, pin_empty_rows]
+        pin_invariants, pin_library_crosscheck, pin_finite_differences, pin_empty_rows,
+        pin_magnitude_homogeneity]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])

@@ -74,6 +74,19 @@ SMALL = {
     # range but the first is empty
     "bf16-decode-sq1": C3.with_(B=1, H=8, HKV=2, Sq=1, Sk=5000, causal=False, seed=61),
     "bf16-decode-sq1-causal": C3.with_(B=1, H=8, HKV=2, Sq=1, Sk=5000, seed=62),
+    # bf16 inputs far outside fp16's range (largest finite 65504, normal from 2^-14):
+    # the fp16 operand copies must be scaled by powers of two (gradients dO of 1e-7,
+    # V of 1e5, Q and K of 2^-20, dO of 1e4 and V of 1e-6; alone and together)
+    "bf16-mag-tiny-dO": C3.with_(B=1, H=4, HKV=2, Sq=300, Sk=300, seed=71, mag=(1, 1, 1, 1e-7)),
+    "bf16-mag-huge-V": C3.with_(B=1, H=4, HKV=2, Sq=300, Sk=300, seed=72, mag=(1, 1, 1e5, 1)),
+    "bf16-mag-tiny-QK": C3.with_(B=1, H=4, HKV=2, Sq=300, Sk=300, seed=73,
+                                 mag=(2.0 ** -20, 2.0 ** -20, 1, 1)),
+    "bf16-mag-all": C4.with_(B=1, H=4, HKV=1, Sq=700, Sk=700, window=200, seed=74,
+                             mag=(2.0 ** -20, 2.0 ** -20, 1e5, 1e-7)),
+    "bf16-mag-huge-dO-tiny-V": C3.with_(B=1, H=2, HKV=1, Sq=400, Sk=500, causal=False, seed=75,
+                                        mag=(1, 1, 1e-6, 1e4)),
+    "bf16-mag-decode": C3.with_(B=1, H=8, HKV=2, Sq=64, Sk=3000, causal=False, seed=76,
+                                mag=(1, 1, 3e4, 1e-6)),
 }
 
 
