@@ -1211,6 +1211,14 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
 //              slot, so dP^T(c+1) may overwrite the slot right after dK(c) is issued.
 // P^T lives in shared memory so that the next score tile can enter the tensor pipe
 // while the softmax is still exponentiating.
+//
+// SPLIT (short query sequences, where a few keys can take almost all of a row's
+// weight and this kernel is bound by per-CTA set-up rather than by the tensor pipe):
+// P and dS enter the accumulating products as two fp16 terms each, x = hi + lo with
+// hi = fp16(x), lo = fp16(x - hi), i.e. about 22 significant bits instead of 11. P^T
+// hi / lo go into the S^T slot the softmax has just read (dV += P^T dO becomes two TS
+// MMAs, and the slot is freed by their commit instead of by the softmax's load), dS^T
+// lo into the half of its part's dP^T range that dS^T hi leaves free (two dK MMAs).
 template <int D>
 struct Dkv16Cfg {
   static constexpr int NCB = D / 64;
@@ -1280,11 +1288,22 @@ __device__ __forceinline__ void issue_acc128_ss(uint32_t acc, uint32_t a, uint32
   }
 }
 
-template <int D>
+// x = hi + lo for a pair of floats, both terms fp16 (packed as one 32-bit word each):
+// hi = fp16(x), lo = fp16(x - hi)
+__device__ __forceinline__ void split_half2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     fa_bwd_dkdv16_kernel(const __grid_constant__ KVMaps m, const BwdArgs a) {
   using C = Dkv16Cfg<D>;
   constexpr int NS = C::NS;
+  static_assert(!SPLIT || C::QC == 64, "two-term operands: 32 packed columns per term and part");
   // The dQ grid launched after this one reads nothing this grid writes: it may start
   // as soon as every block of this grid has started (see the launcher).
   grid_launch_dependents();
@@ -1327,7 +1346,9 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
       mbar_init(&bar_doempty[s], 2);  // dP^T(c) (B) and dV(c) (A) have read dO_c
     }
     mbar_init(&bar_s, 1);
-    mbar_init(&bar_sfree, C::SM_ARRIVALS);
+    // the S^T slot is freed by the softmax's load, or (SPLIT) by the dV MMAs that read
+    // P^T from it
+    mbar_init(&bar_sfree, SPLIT ? 1 : C::SM_ARRIVALS);
     mbar_init(&bar_p, C::SM_ARRIVALS);
     mbar_init(&bar_dvdone, 1);
     mbar_init(&bar_dp, 1);
@@ -1432,9 +1453,17 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         const int st = c % NS;
         if (!(ok = wait(&bar_p, c & 1))) break;
         tc_fence_after();
-        issue_acc128_ss<D>(tmem + C::DV, sbase + C::PT_OFF, sdO(st), c > 0);
-        tc_commit(&bar_doempty[st]);
-        tc_commit(&bar_dvdone);
+        if constexpr (SPLIT) {
+          // P^T hi and lo from the S^T slot, which S^T(c + 1) may take once both are read
+          issue_acc128<D>(tmem + C::DV, tmem + C::S_COL, sdO(st), c > 0);
+          issue_acc128<D>(tmem + C::DV, tmem + C::S_COL + C::QC / 2, sdO(st), true);
+          tc_commit(&bar_doempty[st]);
+          tc_commit(&bar_sfree);
+        } else {
+          issue_acc128_ss<D>(tmem + C::DV, sbase + C::PT_OFF, sdO(st), c > 0);
+          tc_commit(&bar_doempty[st]);
+          tc_commit(&bar_dvdone);
+        }
       }
       if (ok) tc_commit(&bar_done);
       tc_commit(&bar_drain[2]);
@@ -1454,6 +1483,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         if (!(ok = wait(&bar_ds, c & 1))) break;
         tc_fence_after();
         issue_acc128<D>(tmem + C::DK, tmem + C::DP_COL, sQ(st), c > 0);
+        if constexpr (SPLIT) issue_acc128<D>(tmem + C::DK, tmem + C::DP_COL + C::QC / 2, sQ(st), true);
         tc_commit(&bar_qempty[st]);
       }
       if (ok) tc_commit(&bar_done);
@@ -1506,7 +1536,8 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
       ld_cols(lane_addr + C::S_COL + part * QC, s);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_sfree);  // the S^T slot may take the next chunk
+      if constexpr (!SPLIT)
+        if (lane == 0) mbar_arrive(&bar_sfree);  // the S^T slot may take the next chunk
       // query i = q0 + k sees key j iff (!causal || j <= i) && (!window || j >= i-w+1)
       // && i < Sq && j < Sk
       if (tile_needs_mask(i0, i0 + BLOCK_M - 1, j0, j0 + BLOCK_N - 1, a.Sk, a.causal, a.window) ||
@@ -1530,17 +1561,29 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         s[4 * k4 + 2] = ex2(xb.x);
         s[4 * k4 + 3] = ex2(xb.y);
       }
-      // P^T into shared memory once dV has consumed the previous chunk's
-      if (c > 0) {
-        ok = __all_sync(0xffffffffu, wait(&bar_dvdone, (c - 1) & 1));
-        if (!ok) break;
-      }
+      if constexpr (SPLIT) {
+        // P^T hi / lo over the S^T columns this thread has just read: hi in the first
+        // QC / 2 packed columns of its part's range, lo in the other QC / 2
+        uint32_t ph[QC / 2], pl[QC / 2];
 #pragma unroll
-      for (int k8 = 0; k8 < QC / 8; ++k8)
-        st_shared_v4(pt_row + (((chunk0 + (uint32_t)k8) ^ sw) << 4), pack_half2(s[8 * k8], s[8 * k8 + 1]),
-                     pack_half2(s[8 * k8 + 2], s[8 * k8 + 3]), pack_half2(s[8 * k8 + 4], s[8 * k8 + 5]),
-                     pack_half2(s[8 * k8 + 6], s[8 * k8 + 7]));
-      fence_async_shared();
+        for (int k = 0; k < QC / 2; ++k) split_half2(s[2 * k], s[2 * k + 1], ph[k], pl[k]);
+        tmem_st32(lane_addr + C::S_COL + part * QC, ph);
+        tmem_st32(lane_addr + C::S_COL + part * QC + QC / 2, pl);
+        tmem_st_wait();
+        tc_fence_before();
+      } else {
+        // P^T into shared memory once dV has consumed the previous chunk's
+        if (c > 0) {
+          ok = __all_sync(0xffffffffu, wait(&bar_dvdone, (c - 1) & 1));
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int k8 = 0; k8 < QC / 8; ++k8)
+          st_shared_v4(pt_row + (((chunk0 + (uint32_t)k8) ^ sw) << 4), pack_half2(s[8 * k8], s[8 * k8 + 1]),
+                       pack_half2(s[8 * k8 + 2], s[8 * k8 + 3]), pack_half2(s[8 * k8 + 4], s[8 * k8 + 5]),
+                       pack_half2(s[8 * k8 + 6], s[8 * k8 + 7]));
+        fence_async_shared();
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_p);
       ok = __all_sync(0xffffffffu, wait(&bar_dp, c & 1));
@@ -1551,7 +1594,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         ld_cols(lane_addr + C::DP_COL + part * QC, g);
         const uint32_t dv = lv + 128 * 4;
         const float2 dpm = make_float2(dp_mul, dp_mul);
-        uint32_t pk[QC / 2];
+        uint32_t pk[QC / 2], pl[SPLIT ? QC / 2 : 1];
 #pragma unroll
         for (int k4 = 0; k4 < QC / 4; ++k4) {
           const float4 d4 = ld_shared_v4(dv + 16 * k4);
@@ -1561,12 +1604,19 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
                                  fma2(make_float2(g[k], g[k + 1]), dpm, make_float2(-d4.x, -d4.y)));
           const float2 ub = mul2(make_float2(s[k + 2], s[k + 3]),
                                  fma2(make_float2(g[k + 2], g[k + 3]), dpm, make_float2(-d4.z, -d4.w)));
-          pk[2 * k4] = pack_half2(ua.x, ua.y);
-          pk[2 * k4 + 1] = pack_half2(ub.x, ub.y);
+          if constexpr (SPLIT) {
+            split_half2(ua.x, ua.y, pk[2 * k4], pl[2 * k4]);
+            split_half2(ub.x, ub.y, pk[2 * k4 + 1], pl[2 * k4 + 1]);
+          } else {
+            pk[2 * k4] = pack_half2(ua.x, ua.y);
+            pk[2 * k4 + 1] = pack_half2(ub.x, ub.y);
+          }
         }
         // dS^T (fp16) into the first QC / 2 columns of this part's own dP^T range
+        // (SPLIT: dS^T lo into the other QC / 2)
         if constexpr (QC == 64) tmem_st32(lane_addr + C::DP_COL + part * QC, pk);
         else tmem_st16(lane_addr + C::DP_COL + part * QC, pk);
+        if constexpr (SPLIT) tmem_st32(lane_addr + C::DP_COL + part * QC + QC / 2, pl);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -2127,7 +2177,9 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       }
     } else {
       using C16 = Dkv16Cfg<D>;
-      auto kern = fa_bwd_dkdv16_kernel<D>;
+      // two-term P / dS for short query sequences (see the kernel)
+      const bool split = split_operands(p.H / p.HKV, n_qt);
+      auto kern = split ? fa_bwd_dkdv16_kernel<D, true> : fa_bwd_dkdv16_kernel<D, false>;
       // all the dynamic shared memory a block may have: the layout fills it after
       // aligning its base to 1 KB (the kernel checks the fit)
       int dyn = 0;

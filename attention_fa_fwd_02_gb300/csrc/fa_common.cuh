@@ -40,6 +40,15 @@ inline int key_range_tiles(int base, int n_kt, int sms) {
   return best_t;
 }
 
+// bf16 inputs: whether P (forward and backward) and dS (backward) enter the
+// accumulating products as two fp16 terms each. A dK / dV CTA walks rep * n_qt query
+// chunks (the grouped heads' query tiles); with at most 8 of them that kernel is bound
+// by its per-CTA set-up, not the tensor pipe, and short query sequences against long
+// key sequences are where one key can take almost all of a row's weight, which one
+// fp16 term of P / dS does not resolve to the 2e-2-of-RMS accuracy of the bf16 path.
+// The forward follows the same rule, as its O enters the backward's D_i = dO_i . O_i.
+inline bool split_operands(int rep, int n_qt) { return (long long)rep * n_qt <= 8; }
+
 // Launch shape of the key-range combine kernels (one thread per 4 of a row's Dv
 // columns): blockDim (Dv / 4, rows per block), about 64 threads; grid (row blocks,
 // heads, at most 65535: the kernels loop over the rest).

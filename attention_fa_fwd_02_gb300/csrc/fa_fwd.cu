@@ -130,16 +130,23 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t 
   }
 }
 
-template <class C>
+template <class C, bool PSPLIT = false>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t plo_tmem,
                                          uint32_t sv, uint32_t sv_lo, bool accumulate) {
   if constexpr (!C::F32) {
     // A = P (fp16, TMEM, 8 columns per 16 keys); B = V (fp16, MN-major in smem).
+    // PSPLIT: then A = P_lo, 64 columns further on.
     constexpr uint32_t id = make_idesc(128, C::D, FMT_F16, FMT_F16, false, true);
 #pragma unroll
     for (int kk = 0; kk < BLOCK_N / 16; ++kk)
       mma_f16_ts(o_tmem, p_tmem + kk * 8, make_sdesc(sv + kk * 16 * 128, C::CB_BYTES, SW128_ATOM),
                  id, (accumulate || kk > 0) ? 1u : 0u);
+    if constexpr (PSPLIT) {
+#pragma unroll
+      for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+        mma_f16_ts(o_tmem, p_tmem + 64 + kk * 8,
+                   make_sdesc(sv + kk * 16 * 128, C::CB_BYTES, SW128_ATOM), id, 1u);
+    }
   } else {
     // A = P_hi / P_lo (fp32, TMEM, one column per key); B = V^T (K-major: rows = d).
     constexpr uint32_t id = make_idesc(128, C::D, FMT_TF32, FMT_TF32, false, false);
@@ -204,7 +211,15 @@ __device__ __forceinline__ void issue_v_load(uint8_t* smem, int it, int t, int b
 // consecutive row tiles of one head. Both tiles then need exactly the item's key
 // tiles (two row tiles of a causal or windowed item need different ones, so one of
 // them computes a tile that is masked for it), and at Sq <= 128 no tile is padding.
-template <int D, bool F32, bool HP>
+//
+// PSPLIT (bf16 inputs, short query sequences): P enters O += P V as two fp16 terms,
+// P = hi + lo with hi = fp16(P), lo = fp16(P - hi): hi in the S slot's first 64
+// columns as usual, lo in the other 64 (free once the softmax has read S), and a
+// second PV MMA per tile. The next S MMA on the slot follows both in the issuer's
+// order. Where one key takes almost all of a row's weight, one fp16 term (11
+// significant bits) puts an error in O that the backward's D_i = dO_i . O_i then
+// passes on to dS at exactly the dominant keys.
+template <int D, bool F32, bool HP, bool PSPLIT>
 __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKlo,
@@ -455,7 +470,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
           named_bar_sync(1 + q, 128 + 32);  // P_q(g) is in TMEM
           tc_fence_after();
           if (leader) {
-            issue_pv<C>(tmem + C::o_col(q), tmem + C::s_col(q), tmem + C::PLO_COL, sV(vs, 0),
+            issue_pv<C, PSPLIT>(tmem + C::o_col(q), tmem + C::s_col(q), tmem + C::PLO_COL, sV(vs, 0),
                         sV(vs, C::NSPLIT - 1), t > 0);
             if (more) {
               issue_qk<C>(tmem + C::s_col(q), sQ(q, 0), sQ(q, C::NSPLIT - 1), sK(ks, 0),
@@ -623,15 +638,23 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
           float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            uint32_t pk[32];
+            uint32_t pk[32], pl[PSPLIT ? 32 : 1];
 #pragma unroll
             for (int kk = 0; kk < 32; ++kk) {
               const float2 x = fma2(make_float2(s[c * 64 + 2 * kk], s[c * 64 + 2 * kk + 1]), sl2x2, nmx2);
               const float2 pp = make_float2(ex2(x.x), ex2(x.y));
               ls[kk & 1] = add2(ls[kk & 1], pp);
-              pk[kk] = pack_half2(pp.x, pp.y);
+              if constexpr (PSPLIT) {
+                const __half2 h = __floats2half2_rn(pp.x, pp.y);
+                const float2 hf = __half22float2(h);
+                pk[kk] = *reinterpret_cast<const uint32_t*>(&h);
+                pl[kk] = pack_half2(pp.x - hf.x, pp.y - hf.y);
+              } else {
+                pk[kk] = pack_half2(pp.x, pp.y);
+              }
             }
             tmem_st32(s_addr + c * 32, pk);
+            if constexpr (PSPLIT) tmem_st32(s_addr + 64 + c * 32, pl);  // (S read in full above)
           }
           l0 = ls[0].x + ls[1].x;
           l1 = ls[0].y + ls[1].y;
@@ -830,12 +853,15 @@ bool encode_o_map(CUtensorMap* m, void* O, const fa_params& p) {
                                bf ? 2 : 4, O, p.D, p.Sq, (uint64_t)p.B * p.H, p.D, bf ? 64 : 32, 32);
 }
 
-// The forward kernel instantiation: head-pair items (two-tile kernels only) or not.
+// The forward kernel instantiation: head-pair items (two-tile kernels only) or not;
+// two-term P (bf16 inputs) or not.
 template <int D, bool F32>
-auto fwd_kernel_for(bool hp) {
-  auto kern = fa_fwd_kernel<D, F32, false>;
-  if constexpr (FwdCfg<D, F32>::NQ == 2)
-    if (hp) kern = fa_fwd_kernel<D, F32, true>;
+auto fwd_kernel_for(bool hp, bool psplit) {
+  auto kern = fa_fwd_kernel<D, F32, false, false>;
+  if constexpr (FwdCfg<D, F32>::NQ == 2) {
+    if (hp) kern = psplit ? fa_fwd_kernel<D, F32, true, true> : fa_fwd_kernel<D, F32, true, false>;
+    else if (psplit) kern = fa_fwd_kernel<D, F32, false, true>;
+  }
   return kern;
 }
 
@@ -956,7 +982,9 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
     }
   }
   const unsigned grid = (unsigned)std::min(a.n_items, sms);
-  auto kern = fwd_kernel_for<D, F32>(hp);
+  // two-term P for the shapes whose backward takes two-term P / dS (see split_operands)
+  const bool psplit = !F32 && split_operands(p.H / p.HKV, (p.Sq + BLOCK_M - 1) / BLOCK_M);
+  auto kern = fwd_kernel_for<D, F32>(hp, psplit);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_ALLOC);
   if (e == cudaSuccess) {
@@ -1191,7 +1219,9 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
   a.limit_ns = WAIT_LIMIT_NS;
   a.sc = sc;
   const unsigned grid = (unsigned)std::min(a.n_items, host::sm_count());
-  auto kern = fwd_kernel_for<D, F32>(hp);
+  // two-term P for the shapes whose backward takes two-term P / dS (see split_operands)
+  const bool psplit = !F32 && split_operands(p.H / p.HKV, (p.Sq + BLOCK_M - 1) / BLOCK_M);
+  auto kern = fwd_kernel_for<D, F32>(hp, psplit);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_ALLOC);
   if (e != cudaSuccess) return FA_ERR_CUDA;

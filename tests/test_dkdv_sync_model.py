@@ -16,6 +16,13 @@ fa_bwd_dkdv16_kernel (fa_bwd.cu) walks the 128-query chunks of one key tile:
     wait is what orders the dV MMA after the dO copy (P^T would otherwise be written
     as soon as S^T, i.e. Q_c, is in); dropping it is one of the planted faults.
 
+The variant with two-term P and dS (SPLIT, chosen for short query sequences): the
+softmax writes P^T = P_hi + P_lo into the S^T slot it has just read, instead of the
+shared P^T tile, and dV += P^T dO reads it from there (two MMAs); dS^T_lo goes into the
+half of the dP^T slot that dS^T_hi leaves free, and dK takes two MMAs. The S^T slot is
+then freed by the dV MMAs' commit, not by the softmax's load; keeping the early
+release is a planted fault.
+
 This test replays the roles in the kernel's order under random interleavings (copies
 land in any order, the tensor pipe runs in issue order) and checks every read of Q,
 dO, the TMEM slots and the P^T tile, and the accumulation order of dV and dK. Planted
@@ -31,7 +38,7 @@ NS = 2  # Q / dO ring depth at D = 128
 
 
 def run_protocol(nc, seed, q_release_count=2, wait_dv_done=True, wait_sfree=True,
-                 softmax_waits_do=True):
+                 softmax_waits_do=True, split=False, split_softmax_frees_s=False):
     """Play the chunks of one key tile; raises ProtocolError on a violation."""
     rnd = random.Random(seed)
     mb = {}
@@ -94,7 +101,8 @@ def run_protocol(nc, seed, q_release_count=2, wait_dv_done=True, wait_sfree=True
             def mma(c=c):
                 read("Q", smem_q, c)
                 if tmem["S"] is not None and not tmem["S"][2]:
-                    raise ProtocolError(f"S^T({c}) overwrote S^T({tmem['S'][1]}) before the softmax read it")
+                    raise ProtocolError(f"S^T({c}) overwrote {tmem['S'][0]}({tmem['S'][1]}) before "
+                                        "it was read")
                 tmem["S"] = ("S", c, False)
             pipe.append(mma)
             commit(M("s"))
@@ -106,16 +114,23 @@ def run_protocol(nc, seed, q_release_count=2, wait_dv_done=True, wait_sfree=True
             yield (lambda c=c: M("p").passed(c & 1))
 
             def mma(c=c):
-                if pt["tile"] != c:
+                if split:
+                    if tmem["S"] != ("P", c, False):
+                        raise ProtocolError(f"dV({c}) read {tmem['S']} from the S^T slot")
+                    tmem["S"] = ("P", c, True)
+                elif pt["tile"] != c:
                     raise ProtocolError(f"dV({c}) read the P^T tile of chunk {pt['tile']}")
                 read("dO", smem_do, c)
                 if acc["dV"] != c:
                     raise ProtocolError(f"dV accumulated chunk {c} after {acc['dV']} chunks")
                 acc["dV"] += 1
                 pt["read"] = True
-            pipe.append(mma)
+            pipe.append(mma)  # (split: the P_hi and P_lo MMAs, one after the other)
             commit(M(("doempty", st)))
-            commit(M("dvdone"))
+            if split:
+                commit(M("sfree"))  # P^T(c) has left the S^T slot: S^T(c + 1) may go in
+            else:
+                commit(M("dvdone"))
         commit(M("done", 2))
 
     def b_issuer():
@@ -153,13 +168,20 @@ def run_protocol(nc, seed, q_release_count=2, wait_dv_done=True, wait_sfree=True
             if tmem["S"] != ("S", c, False):
                 raise ProtocolError(f"softmax read S^T {tmem['S']}, wanted chunk {c}")
             tmem["S"] = ("S", c, True)
-            M("sfree").arrive()
+            if not split or split_softmax_frees_s:
+                M("sfree").arrive()
             yield None  # exponentials (lse2 of the chunk from the ring's vector slot)
-            if c > 0 and wait_dv_done:
-                yield (lambda c=c: M("dvdone").passed((c - 1) & 1))
-            if not pt["read"]:
-                raise ProtocolError(f"P^T({c}) written over P^T({pt['tile']}) before dV read it")
-            pt["tile"], pt["read"] = c, False
+            if split:
+                # P^T hi / lo over the S^T columns this thread has just read
+                if tmem["S"] != ("S", c, True):
+                    raise ProtocolError(f"P^T({c}) written over {tmem['S']}")
+                tmem["S"] = ("P", c, False)
+            else:
+                if c > 0 and wait_dv_done:
+                    yield (lambda c=c: M("dvdone").passed((c - 1) & 1))
+                if not pt["read"]:
+                    raise ProtocolError(f"P^T({c}) written over P^T({pt['tile']}) before dV read it")
+                pt["tile"], pt["read"] = c, False
             M("p").arrive()
             yield (lambda c=c: M("dp").passed(c & 1))
             if tmem["dP"] != ("dP", c):
@@ -200,6 +222,22 @@ def test_protocol_holds_under_random_interleavings():
     rnd = random.Random(20261206)
     for _ in range(2000):
         run_protocol(rnd.randint(1, 10), seed=rnd.randrange(10 ** 9))
+
+
+def test_split_protocol_holds_under_random_interleavings():
+    rnd = random.Random(20261207)
+    for _ in range(2000):
+        run_protocol(rnd.randint(1, 10), seed=rnd.randrange(10 ** 9), split=True)
+
+
+def test_planted_fault_split_st_slot_freed_by_the_softmax_is_caught():
+    # with P^T in the S^T slot, the softmax's early release lets S^T(c + 1) overwrite
+    # P^T(c) before dV has read it
+    assert _caught(3000, split=True, split_softmax_frees_s=True)
+
+
+def test_planted_fault_split_without_the_sfree_wait_is_caught():
+    assert _caught(3000, split=True, wait_sfree=False)
 
 
 def _caught(trials, **fault):

@@ -62,8 +62,12 @@ SMALL = {
     # sees only the last range, tile 11 no key at all (its dQ rows must come out 0)
     "bf16-decode-window-empty-tail": C4.with_(B=1, H=4, HKV=1, Sq=1500, Sk=1200, window=100,
                                               seed=55),
-    # the decode-shaped measurement line's launch: 128 queries against 16384 keys
+    # the decode-shaped measurement line's launch: 128 queries against 16384 keys, where
+    # a few keys take almost all of a row's weight (max|dV| ~ 80 RMS(dV)); and a second
+    # seed with Q, K ~ N(0, 2^2), more peaked still
     "bf16-decode-sq128-sk16384": C4.with_(Sq=128, causal=False, window=0, seed=56),
+    "bf16-decode-sq128-sk16384-std2": C4.with_(Sq=128, causal=False, window=0, seed=57,
+                                               std_qk=2.0),
     # forward items pair two query heads of a kv head when the group size is even
     # (three pairs per kv head here), else two row tiles of one head (group of 3)
     "bf16-gqa6-causal-ragged": C3.with_(B=1, H=12, HKV=2, Sq=300, Sk=300, seed=57),
