@@ -225,9 +225,10 @@ FA_API fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, voi
   return launch_fwd_noalloc(Q, K, V, O, LSE, normalized(*p), reinterpret_cast<cudaStream_t>(stream));
 }
 
-FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O,
-                        const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
-                        const fa_params* p, fa_stream_t stream) {
+namespace {
+fa_status bwd_entry(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                    const float* LSE, void* dQ, void* dK, void* dV, const fa_params* p,
+                    fa_stream_t stream, bool dsmat) {
   fa_status st = validate(p);
   if (st != FA_OK) return st;
   if (p->Sq > 0) {
@@ -239,8 +240,22 @@ FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void*
     if (st != FA_OK) return st;
   }
   if (p->Sq == 0 && p->Sk == 0) return FA_OK;
+  if (dsmat && p->in_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
   return launch_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, normalized(*p),
-                    reinterpret_cast<cudaStream_t>(stream));
+                    reinterpret_cast<cudaStream_t>(stream), dsmat);
+}
+}  // namespace
+
+FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O,
+                        const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                        const fa_params* p, fa_stream_t stream) {
+  return bwd_entry(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, false);
+}
+
+FA_API fa_status fa_bwd_dsmat(const void* Q, const void* K, const void* V, const void* O,
+                              const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                              const fa_params* p, fa_stream_t stream) {
+  return bwd_entry(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, true);
 }
 
 FA_API fa_status fa_device_status(fa_stream_t stream) {

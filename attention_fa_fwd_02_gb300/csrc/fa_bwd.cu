@@ -55,6 +55,10 @@ struct BwdArgs {
   // bf16 inputs: multipliers that undo the power-of-two scaling of the fp16 operand
   // copies (written by bwd_scales_kernel before these kernels start)
   const OperandScales* sc;
+  // materialised-dS backward: dS^T (scaled by 2^eD, fp16, hi and, with two-term
+  // operands, lo) as [B*H][Sk][ldq], query index fastest
+  __half* ds_hi;
+  __half* ds_lo;
 };
 
 // Tensor maps of one kernel launch; index [split] selects the hi (0) / lo (1) copy.
@@ -1298,12 +1302,17 @@ __device__ __forceinline__ void split_half2(float a, float b, uint32_t& hi, uint
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-template <int D, bool SPLIT>
+// MATDS (the materialised-dS backward): the softmax also stores every dS^T row it
+// forms (this thread's key j, its part's QC queries: 2 QC bytes per term) to a.ds_hi
+// (and a.ds_lo), from which dq_from_ds_kernel forms dQ = scale dS K as a GEMM instead
+// of recomputing S and dP.
+template <int D, bool SPLIT, bool MATDS>
 __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     fa_bwd_dkdv16_kernel(const __grid_constant__ KVMaps m, const BwdArgs a) {
   using C = Dkv16Cfg<D>;
   constexpr int NS = C::NS;
   static_assert(!SPLIT || C::QC == 64, "two-term operands: 32 packed columns per term and part");
+  static_assert(!MATDS || C::QC == 64, "dS^T rows stored as 128-byte pieces");
   // The dQ grid launched after this one reads nothing this grid writes: it may start
   // as soon as every block of this grid has started (see the launcher).
   grid_launch_dependents();
@@ -1617,6 +1626,23 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         if constexpr (QC == 64) tmem_st32(lane_addr + C::DP_COL + part * QC, pk);
         else tmem_st16(lane_addr + C::DP_COL + part * QC, pk);
         if constexpr (SPLIT) tmem_st32(lane_addr + C::DP_COL + part * QC + QC / 2, pl);
+        if constexpr (MATDS) {
+          // dS^T row j, queries q0 .. q0 + QC - 1 (padding queries carry P = 0, so 0)
+          if (!row_dead) {
+            const size_t off = ((size_t)bh * a.Sk + j) * a.ldq + q0;
+            // QC halves = QC / 8 vectors of 16 bytes (4 packed pairs each)
+            uint4* dh = reinterpret_cast<uint4*>(a.ds_hi + off);
+#pragma unroll
+            for (int v = 0; v < QC / 8; ++v)
+              dh[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            if constexpr (SPLIT) {
+              uint4* dl = reinterpret_cast<uint4*>(a.ds_lo + off);
+#pragma unroll
+              for (int v = 0; v < QC / 8; ++v)
+                dl[v] = make_uint4(pl[4 * v], pl[4 * v + 1], pl[4 * v + 2], pl[4 * v + 3]);
+            }
+          }
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -1656,6 +1682,175 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == C::A_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------- dQ from the materialised dS
+// The materialised-dS backward (metal-flash-attention README, backward pass: dS written
+// to memory, so that dQ is a plain GEMM instead of a second recomputation of S and
+// dP): dQ_i = scale sum_j dS_ij K_j over the key tiles query tile i can see, dS read
+// from the [B*H][Sk][ldq] buffer the MATDS dK / dV kernel wrote (hi and, two-term, lo).
+// One CTA per (head, 128-query tile) -- and key range: with fewer (head, query tile)
+// items than SMs the keys are split into ranges of a.tps tiles, each CTA writing a
+// partial dQ (fp32) that dq_range_sum_kernel adds up in range order, as for the
+// recompute dQ kernel -- heaviest causal tiles first. Roles: warp 0 the
+// TMA producer (a ring of NST stages, each the dS tile(s) and the K tile of one key
+// tile), warp 1 the MMA issuer and TMEM owner, warps 2-5 the epilogue (one TMEM lane
+// quarter each). The dS tile is stored key-major (queries fastest), which is the
+// MN-major layout of the A operand [128 queries x 128 keys].
+template <int D, bool SPLIT>
+struct DqGemmCfg {
+  static constexpr int NCB = D / 64;
+  static constexpr uint32_t CB = 128u * 128u;  // 128 rows x 128 bytes
+  static constexpr uint32_t A_TILE = 2 * CB;   // dS: 128 keys x 128 queries fp16
+  static constexpr uint32_t B_TILE = NCB * CB; // K: 128 keys x D fp16
+  static constexpr int NA = SPLIT ? 2 : 1;
+  static constexpr uint32_t STAGE = NA * A_TILE + B_TILE;
+  static constexpr int NST = (int)((200u * 1024u) / STAGE) < 4 ? (int)((200u * 1024u) / STAGE) : 4;
+  static constexpr uint32_t SMEM = NST * STAGE + 1024;
+  static constexpr int THREADS = 192;
+  static constexpr int TMA_WARP = 0, MMA_WARP = 1;
+  static constexpr uint32_t TMEM_COLS = D;  // the dQ accumulator
+  static_assert(NST >= 2 && SMEM <= 227u * 1024u, "shared memory budget");
+  static constexpr uint32_t EPI_WARP = epi_warp_bytes<D, false>();
+  static_assert(4 * EPI_WARP <= NST * STAGE, "epilogue staging");
+};
+
+struct DsMaps {
+  CUtensorMap ds_hi, ds_lo, K, dQ;
+};
+
+template <int D, bool SPLIT>
+__global__ void __launch_bounds__(DqGemmCfg<D, SPLIT>::THREADS, 1)
+    dq_from_ds_kernel(const __grid_constant__ DsMaps m, const BwdArgs a) {
+  using C = DqGemmCfg<D, SPLIT>;
+  constexpr int NST = C::NST;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bar_full[NST], bar_empty[NST], bar_done, bar_drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  const int warp = warp_id(), lane = lane_id();
+  volatile int* abort_flag = &abort_sh;
+
+  const int sp = blockIdx.x % a.n_splits, w = blockIdx.x / a.n_splits;
+  const int qt_lin = w / a.BHx, bh = w % a.BHx;
+  const int qt = a.lpt ? a.n_tiles - 1 - qt_lin : qt_lin;
+  const int i0 = qt * BLOCK_M;
+  const int b = bh / a.H, h = bh % a.H;
+  const int bg = b * a.HKV + h / (a.H / a.HKV);
+  int kt_lo, kt_hi;
+  kv_tile_range(i0, min(i0 + BLOCK_M - 1, a.Sq - 1), a.Sk, a.causal, a.window, &kt_lo, &kt_hi);
+  if (a.n_splits > 1) {
+    kt_lo = max(kt_lo, sp * a.tps);
+    kt_hi = min(kt_hi, (sp + 1) * a.tps);
+  }
+  const int n = kt_hi > kt_lo ? kt_hi - kt_lo : 0;
+  const int zo = sp * a.BHx + bh;  // output slab: dQ itself, or range sp's partial dQ
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(&bar_done, 1);
+    mbar_init(&bar_drain, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    __syncwarp();
+    tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t sbase = smem_u32(smem);
+  auto stage = [&](int st) { return sbase + st * C::STAGE; };
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    return mbar_wait(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
+  };
+
+  if (warp == C::TMA_WARP) {
+    if (lane == 0) {
+      int loads[NST];
+      for (int s = 0; s < NST; ++s) loads[s] = 0;
+      for (int t = 0; t < n; ++t) {
+        const int st = t % NST, k0 = (kt_lo + t) * BLOCK_N;
+        if (t >= NST && !wait(&bar_empty[st], ((t / NST) - 1) & 1)) break;
+        mbar_arrive_expect_tx(&bar_full[st], C::STAGE);
+        uint8_t* dst = smem + st * C::STAGE;
+        for (int blk = 0; blk < 2; ++blk) {  // the tile's two 64-query blocks
+          tma_load_3d(dst + blk * C::CB, &m.ds_hi, &bar_full[st], i0 + 64 * blk, k0, bh);
+          if constexpr (SPLIT)
+            tma_load_3d(dst + C::A_TILE + blk * C::CB, &m.ds_lo, &bar_full[st], i0 + 64 * blk, k0, bh);
+        }
+        for (int cb = 0; cb < C::NCB; ++cb)
+          tma_load_3d(dst + C::NA * C::A_TILE + cb * C::CB, &m.K, &bar_full[st], cb * 64, k0, bg);
+        ++loads[st];
+      }
+      // every issued copy must land before the CTA may exit
+      for (int s = 0; s < NST; ++s)
+        if (loads[s] > 0) drain_wait(&bar_full[s], (loads[s] - 1) & 1, a.limit_ns);
+    }
+  } else if (warp == C::MMA_WARP) {
+    if (lane == 0) {
+      // A = dS [128 queries x 128 keys], MN-major (queries fastest); B = K [128 keys x D],
+      // MN-major; 16 keys per MMA
+      constexpr uint32_t id = make_idesc(128, D, FMT_F16, FMT_F16, true, true);
+      bool ok = true;
+      for (int t = 0; t < n; ++t) {
+        const int st = t % NST;
+        if (!(ok = wait(&bar_full[st], (t / NST) & 1))) break;
+        tc_fence_after();
+        const uint32_t sb = stage(st) + C::NA * C::A_TILE;
+#pragma unroll
+        for (int term = 0; term < C::NA; ++term) {
+          const uint32_t sa = stage(st) + term * C::A_TILE;
+#pragma unroll
+          for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+            mma_f16_ss(tmem, make_sdesc(sa + kk * 16 * 128, C::CB, SW128_ATOM),
+                       make_sdesc(sb + kk * 16 * 128, C::CB, SW128_ATOM), id,
+                       (t > 0 || term > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&bar_empty[st]);
+      }
+      if (ok && n > 0) tc_commit(&bar_done);
+      tc_commit(&bar_drain);
+      drain_wait(&bar_drain, 0, a.limit_ns);
+    }
+  } else {
+    // epilogue: dQ * dq_mul (scale, and 2^-(eD + eK) for the scaled copies); rows of a
+    // tile that sees no key get 0. The ring is free once bar_done has completed (every
+    // MMA, hence every load, is done), and stages the stores.
+    const int wq = warp % 4;
+    bool ok = true;
+    if (n > 0) {
+      ok = __all_sync(0xffffffffu, wait(&bar_done, 0));
+      tc_fence_after();
+    }
+    if (ok) {
+      const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+      const int r_base = i0 + wq * 32;
+      const uint32_t st_w = sbase + wq * C::EPI_WARP;
+      const float mul = a.sc->dq_mul;
+      if (a.out_bf16)
+        store_rows_tma<D, true, D / 64>(&m.dQ, lane_addr, n > 0, mul, st_w, r_base, r_base < a.Sq, zo,
+                                        0, a.Dv);
+      else
+        store_rows_tma<D, false, D / 32>(&m.dQ, lane_addr, n > 0, mul, st_w, r_base, r_base < a.Sq, zo,
+                                         0, a.Dv);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -1959,11 +2154,14 @@ __global__ void zero_kernel(uint4* p, size_t n16) {
 // ------------------------------------------------------------------ launcher
 namespace {
 
+// dsmat (bf16 inputs): the materialised-dS variant -- the dK / dV kernel also stores
+// dS^T, and dQ is a GEMM over it (dq_from_ds_kernel) instead of the recompute kernel.
 template <int D, bool F32>
 fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                   const float* LSE, void* dQ, void* dK, void* dV, const fa_params& p,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, bool dsmat) {
   using C = BwdCfg<D, F32>;
+  if (F32 && dsmat) return FA_ERR_UNSUPPORTED;
   // Tensors have Dv = p.D <= D columns: loads past Dv read zeros, stores past it are
   // dropped, and the pre-passes work on Dv-element rows.
   const int Dv = p.D;
@@ -1992,6 +2190,12 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   const int dq_splits = (n_kt + dq_tps - 1) / dq_tps;
   const size_t part_off = (bytes + 255) / 256 * 256;  // partial dQ [splits][BH][Sq][Dv]
   if (dq_splits > 1) bytes = part_off + (size_t)dq_splits * nq * 4;
+  // two-term P / dS for short query sequences (see split_operands)
+  const bool split = !F32 && split_operands(p.H / p.HKV, n_qt);
+  // materialised dS^T: [B*H][Sk][ldq] fp16, one buffer per term
+  const size_t ds_elems = BH * (size_t)p.Sk * ldq;
+  const size_t ds_off = (bytes + 255) / 256 * 256;
+  if (dsmat) bytes = ds_off + (split ? 2 : 1) * ds_elems * 2;
   void* ws = nullptr;
   if (host::scratch_alloc(&ws, bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
   float* lse2 = static_cast<float*>(ws);
@@ -2000,6 +2204,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   OperandScales* sc = F32 ? nullptr : reinterpret_cast<OperandScales*>(static_cast<char*>(ws) + sc_off);
   uint32_t* part = F32 ? nullptr : reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + sc_off + 256);
   float* dq_part = dq_splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(ws) + part_off) : nullptr;
+  __half* ds_hi = dsmat ? reinterpret_cast<__half*>(static_cast<char*>(ws) + ds_off) : nullptr;
+  __half* ds_lo = dsmat && split ? ds_hi + ds_elems : nullptr;
   const int grid_pp = 4 * sms;
   const auto F32T = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   KVMaps mk;
@@ -2063,7 +2269,7 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     // of tiles) are skipped by the dQ kernel; their rows are zeroed here, before the
     // dK/dV launch (nothing may come between it and its dependent dQ launch). With
     // the keys split into ranges, the sum over the ranges writes them instead.
-    if (dq_splits == 1) {
+    if (dq_splits == 1 && !dsmat) {  // (the materialised-dS GEMM writes those rows itself)
       int t0 = n_qt;
       while (t0 > 0) {
         int lo, hi;
@@ -2162,6 +2368,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   a.tps = n_kt;
   a.limit_ns = WAIT_LIMIT_NS;
   a.sc = sc;
+  a.ds_hi = ds_hi;
+  a.ds_lo = ds_lo;
   cudaError_t e = cudaSuccess;
   {
     BwdArgs ak = a;
@@ -2177,9 +2385,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       }
     } else {
       using C16 = Dkv16Cfg<D>;
-      // two-term P / dS for short query sequences (see the kernel)
-      const bool split = split_operands(p.H / p.HKV, n_qt);
-      auto kern = split ? fa_bwd_dkdv16_kernel<D, true> : fa_bwd_dkdv16_kernel<D, false>;
+      auto kern = dsmat ? (split ? fa_bwd_dkdv16_kernel<D, true, true> : fa_bwd_dkdv16_kernel<D, false, true>)
+                        : (split ? fa_bwd_dkdv16_kernel<D, true, false> : fa_bwd_dkdv16_kernel<D, false, false>);
       // all the dynamic shared memory a block may have: the layout fills it after
       // aligning its base to 1 KB (the kernel checks the fit)
       int dyn = 0;
@@ -2207,6 +2414,36 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       if (e == cudaSuccess) {
         host::KernelTimer kt("fa_bwd_dq_kernel<64,f32>", stream);
         kern<<<(unsigned)(BH * aq.n_tiles), C::THREADS, C::Q_SMEM, stream>>>(mq, aq);
+        e = cudaGetLastError();
+      }
+    } else if (dsmat) {
+      // dQ = scale dS K over the stored dS^T (an ordinary launch: it reads what the
+      // dK / dV kernel wrote)
+      DsMaps md;
+      const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      bool enc2 = host::encode_tiled_3d(&md.ds_hi, F16, 2, ds_hi, ldq, p.Sk, BH, ldq, 64, 128);
+      md.ds_lo = md.ds_hi;
+      if (split) enc2 &= host::encode_tiled_3d(&md.ds_lo, F16, 2, ds_lo, ldq, p.Sk, BH, ldq, 64, 128);
+      md.K = mq.Kc[0];
+      md.dQ = mq.dQ;
+      if (!enc2) e = cudaErrorInvalidValue;
+      auto kern = split ? dq_from_ds_kernel<D, true> : dq_from_ds_kernel<D, false>;
+      const uint32_t smem_b = split ? DqGemmCfg<D, true>::SMEM : DqGemmCfg<D, false>::SMEM;
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_b);
+      if (e == cudaSuccess) {
+        host::KernelTimer kt(D == 128 ? "dq_from_ds_kernel<128,bf16>" : "dq_from_ds_kernel<64,bf16>",
+                             stream);
+        kern<<<(unsigned)(BH * (size_t)n_qt * dq_splits), DqGemmCfg<D, false>::THREADS, smem_b,
+               stream>>>(md, aq);
+        e = cudaGetLastError();
+      }
+      if (e == cudaSuccess && dq_splits > 1) {
+        host::KernelTimer kt("dq_range_sum", stream);
+        dim3 cg, cb;
+        combine_launch_shape((int)BH, p.Sq, Dv, &cg, &cb);
+        dq_range_sum_kernel<<<cg, cb, 0, stream>>>(dq_part, dQ, dq_tps, (int)BH, p.Sq, p.Sk,
+                                                   p.causal, p.window, Dv, p.out_dtype == FA_BF16);
         e = cudaGetLastError();
       }
     } else {
@@ -2255,7 +2492,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
 
 fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                      const float* LSE, void* dQ, void* dK, void* dV, const fa_params& p,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, bool dsmat) {
+  if (dsmat && p.in_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
   const int grid_pp = 4 * host::sm_count();
   const size_t osz = p.out_dtype == FA_BF16 ? 2 : 4;
   if (p.Sq == 0 || p.Sk == 0) {
@@ -2272,10 +2510,10 @@ fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O,
   }
   // head dims below a kernel's D run in it with the missing columns read as zeros
   if (p.in_dtype == FA_BF16) {
-    if (p.D <= 64) return run_bwd<64, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
-    if (p.D <= 128) return run_bwd<128, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
+    if (p.D <= 64) return run_bwd<64, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, dsmat);
+    if (p.D <= 128) return run_bwd<128, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, dsmat);
   } else {
-    if (p.D <= 64) return run_bwd<64, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
+    if (p.D <= 64) return run_bwd<64, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, false);
   }
   return FA_ERR_UNSUPPORTED;
 }

@@ -149,7 +149,7 @@ fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float
                      const fa_params& p, cudaStream_t stream);
 fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                      const float* LSE, void* dQ, void* dK, void* dV, const fa_params& p,
-                     cudaStream_t stream);
+                     cudaStream_t stream, bool dsmat);
 fa_status launch_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
                              const fa_params& p, cudaStream_t stream);
 fa_status launch_selftest_timeout(unsigned long long limit_ns, int* roles_done, cudaStream_t s);

@@ -21,7 +21,7 @@ STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_E
           4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_SCRATCH_LIMIT", 7: "FA_ERR_LAYOUT"}
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string", "fa_version",
            "fa_timing_enable", "fa_timing_read", "fa_fwd_noalloc", "fa_selftest_timeout",
-           "fa_noalloc_scratch_bytes")
+           "fa_noalloc_scratch_bytes", "fa_bwd_dsmat")
 
 
 class FAError(RuntimeError):
@@ -54,6 +54,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_fwd_noalloc.restype = st
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, P, vp]
     lib.fa_bwd.restype = st
+    lib.fa_bwd_dsmat.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, P, vp]
+    lib.fa_bwd_dsmat.restype = st
     lib.fa_device_status.argtypes = [vp]
     lib.fa_device_status.restype = st
     lib.fa_status_string.argtypes = [st]
@@ -112,6 +114,12 @@ def fa_bwd(Q: int, K: int, V: int, O: int, dO: int, LSE: int, dQ: int, dK: int, 
            params: fa_params, stream: int) -> int:
     """Direct call of the C ``fa_bwd``; returns the status."""
     return lib().fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, ctypes.byref(params), stream)
+
+
+def fa_bwd_dsmat(Q: int, K: int, V: int, O: int, dO: int, LSE: int, dQ: int, dK: int, dV: int,
+                 params: fa_params, stream: int) -> int:
+    """Direct call of the C ``fa_bwd_dsmat`` (the materialised-dS backward); returns the status."""
+    return lib().fa_bwd_dsmat(Q, K, V, O, dO, LSE, dQ, dK, dV, ctypes.byref(params), stream)
 
 
 def fa_device_status(stream: int) -> int:
@@ -177,8 +185,9 @@ def forward(q, k, v, scale=None, causal=False, window=0, out_dtype=None, stream=
 
 
 def backward(q, k, v, o, lse, do, scale=None, causal=False, window=0, out_dtype=None,
-             stream=None):
-    """dQ, dK, dV through ``fa_bwd`` (o / lse as returned by ``forward``)."""
+             stream=None, materialize_ds=False):
+    """dQ, dK, dV through ``fa_bwd`` (o / lse as returned by ``forward``), or through
+    ``fa_bwd_dsmat`` with ``materialize_ds``."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (do, "do")):
         _check(t, n)
@@ -187,11 +196,12 @@ def backward(q, k, v, o, lse, do, scale=None, causal=False, window=0, out_dtype=
     dq = torch.empty(q.shape, dtype=odt, device=q.device)
     dk = torch.empty(k.shape, dtype=odt, device=q.device)
     dv = torch.empty(v.shape, dtype=odt, device=q.device)
-    rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), p,
-                _stream_handle(stream))
+    entry = fa_bwd_dsmat if materialize_ds else fa_bwd
+    rc = entry(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+               lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), p,
+               _stream_handle(stream))
     if rc:
-        raise FAError(rc, "fa_bwd")
+        raise FAError(rc, "fa_bwd_dsmat" if materialize_ds else "fa_bwd")
     return dq, dk, dv
 
 

@@ -36,7 +36,9 @@ METRIC = "attention fwd/bwd TFLOP/s (H32/HKV8 S4096 D128 bf16 causal); % tensor 
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 # Algorithmic FLOPs per visible (query, key) pair per query head, per kernel:
 # forward 2 GEMMs (QK^T, PV); dK/dV kernel 4 (S^T, dP^T, dV, dK); dQ kernel 3 (S, dP, dQ).
-KERNEL_FLOPS_PER_PAIR_PER_D = {"fa_fwd_kernel": 4, "fa_bwd_dkdv_kernel": 8, "fa_bwd_dq_kernel": 6}
+# The materialised-dS backward's dQ GEMM: 1 (dS K).
+KERNEL_FLOPS_PER_PAIR_PER_D = {"fa_fwd_kernel": 4, "fa_bwd_dkdv_kernel": 8, "fa_bwd_dq_kernel": 6,
+                               "dq_from_ds_kernel": 2}
 # Source files whose change invalidates a committed DRAM-traffic figure.
 _COMMON_SOURCES = ["ptx.cuh", "fa_common.cuh", "fa_epilogue.cuh", "fa_prepass.cuh"]
 # head dim of each named workload (traffic figures in profiles/ are for these)
@@ -180,10 +182,10 @@ def oracle_sample(w, n_groups, batch=0):
     return (fwd + bwd) / dt / 1e12, dt, oracle.num_threads(), n_groups * rep
 
 
-def config_of(w, out_dtype="f32", extra=None):
+def config_of(w, out_dtype="f32", extra=None, bwd="recompute"):
     c = {"workload": w.name, "B": w.B, "H": w.H, "HKV": w.HKV, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
          "causal": bool(w.causal), "window": w.window, "scale": w.scale, "in_dtype": w.dtype,
-         "out_dtype": out_dtype,
+         "out_dtype": out_dtype, "backward": bwd,
          "l2": "256 MiB memset between timed steps; inputs also exceed L2"}
     if extra:
         c.update(extra)
@@ -225,7 +227,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_of(w, args.out_dtype),
+            "data": "synthetic", "config": config_of(w, args.out_dtype, bwd=args.bwd),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -286,12 +288,14 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     sh = int(stream.cuda_stream)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # the backward entry point: fa_bwd, or the materialised-dS variant
+    bwd_entry = fa.fa_bwd_dsmat if args.bwd == "dsmat" else fa.fa_bwd
 
     def step():
         rc = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(), p, sh)
         if rc:
             raise fa.FAError(rc, "fa_fwd")
-        rc = fa.fa_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), dod.data_ptr(),
+        rc = bwd_entry(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), dod.data_ptr(),
                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), p, sh)
         if rc:
             raise fa.FAError(rc, "fa_bwd")
@@ -385,7 +389,7 @@ def run_ours(args, rank, world, local_rank):
             stream.wait_event(done_out[j])
         ev_fwd = fwd_call(b)
         stream.wait_event(ev_do)
-        rc = fa.fa_bwd(b["q"].data_ptr(), b["k"].data_ptr(), b["v"].data_ptr(), b["o"].data_ptr(),
+        rc = bwd_entry(b["q"].data_ptr(), b["k"].data_ptr(), b["v"].data_ptr(), b["o"].data_ptr(),
                        b["do"].data_ptr(), b["lse"].data_ptr(), b["dq"].data_ptr(),
                        b["dk"].data_ptr(), b["dv"].data_ptr(), p, sh)
         if rc:
@@ -467,7 +471,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-        "data": "synthetic", "config": config_of(w, args.out_dtype),
+        "data": "synthetic", "config": config_of(w, args.out_dtype, bwd=args.bwd),
         "fwd_tflops": round(fwd_fl / (fwd_ms * 1e-3) / 1e12, 3) if fwd_ms else None,
         # the backward's share of the step: step time minus the forward kernels' time
         # (its dK / dV and dQ kernels overlap inside the step)
@@ -509,6 +513,9 @@ def main():
                     help="full attention over the keys (measurement lines)")
     ap.add_argument("--out-dtype", choices=["f32", "bf16"], default="f32",
                     help="dtype of O, dQ, dK, dV (measurement lines; the headline is f32)")
+    ap.add_argument("--bwd", choices=["recompute", "dsmat"], default="recompute",
+                    help="backward route: fa_bwd (recomputes S and dP for dQ) or fa_bwd_dsmat "
+                         "(materialised dS; measurement lines)")
     ap.add_argument("--head-dim", type=int, default=None,
                     help="run the workload with another head dim (measurement lines; the "
                          "headline is the workload's own)")

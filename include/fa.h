@@ -177,6 +177,23 @@ FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void*
                  fa_stream_t stream);
 
 /*
+ * Backward pass with dS materialised in device memory: the same contract, results and
+ * errors as fa_bwd (for in_dtype FA_BF16; FA_F32 returns FA_ERR_UNSUPPORTED), by the
+ * 5-product route of the metal-flash-attention README's backward-pass discussion
+ * instead of fa_bwd's 7: the dK / dV kernel forms S^T, dP^T, P^T, dS^T per key tile,
+ * accumulates dV and dK on chip and also writes dS^T (scaled fp16; two fp16 terms for
+ * short query sequences) to a workspace of B*H*Sk*round_up(Sq,128)*2 bytes per term;
+ * dQ = scale dS K is then a tensor-core GEMM over that buffer, with no second
+ * recomputation of S and dP. The buffer costs its write and read in memory traffic
+ * (about 2 GB at B=2, H=32, S=4096), which is more than the GEMM work it saves on
+ * this GPU at long sequences; fa_bwd never takes this route by itself. Deterministic,
+ * like fa_bwd. Workspace from the library pool, as for fa_bwd.
+ */
+FA_API fa_status fa_bwd_dsmat(const void* Q, const void* K, const void* V, const void* O,
+                              const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                              const fa_params* p, fa_stream_t stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the library's device status word
  * on the current device: FA_ERR_LAYOUT if a kernel since the last call found less
  * shared memory than its layout needs, FA_ERR_TIMEOUT if one gave up on a barrier

@@ -27,7 +27,7 @@ def test_header_declares_the_abi():
     assert _declared_symbols() == {"fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string",
                                    "fa_version", "fa_timing_enable", "fa_timing_read",
                                    "fa_fwd_noalloc", "fa_selftest_timeout",
-                                   "fa_noalloc_scratch_bytes"}
+                                   "fa_noalloc_scratch_bytes", "fa_bwd_dsmat"}
 
 
 def test_noalloc_scratch_size_matches_the_header(fa):
@@ -109,6 +109,12 @@ def test_invalid_params_rejected(fa, kw, code):
     p = _params(fa, **kw)
     assert fa.fa_fwd(A, A, A, A, A, p, 0) == code
     assert fa.fa_bwd(A, A, A, A, A, A, A, A, A, p, 0) == code
+    assert fa.fa_bwd_dsmat(A, A, A, A, A, A, A, A, A, p, 0) == code
+
+
+def test_materialised_ds_backward_is_bf16_only(fa):
+    p = _params(fa, D=64, in_dtype=fa.FA_F32)
+    assert fa.fa_bwd_dsmat(A, A, A, A, A, A, A, A, A, p, 0) == 2
 
 
 def test_noalloc_rejects_oversized_params_before_sizing_scratch(fa):
