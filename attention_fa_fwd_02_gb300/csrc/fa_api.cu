@@ -165,11 +165,11 @@ fa_status validate(const fa_params* p) {
   if ((double)p->B * p->H * p->Sq * p->D * 4.0 > lim ||
       (double)p->B * p->HKV * p->Sk * p->D * 4.0 > lim)
     return FA_ERR_INVALID_ARG;
-  // Head dims: multiples of 16 up to 128 (bf16) / 64 (fp32); each runs in the kernel
-  // built for the next of 64 / 128, with the missing columns read as zeros.
+  // Head dims: multiples of 16 up to 128; each runs in the kernel built for the next of
+  // 64 / 128, with the missing columns read as zeros.
   const bool d16 = p->D % 16 == 0 && p->D >= 16;
   const bool ok_bf16 = p->in_dtype == FA_BF16 && d16 && p->D <= 128;
-  const bool ok_f32 = p->in_dtype == FA_F32 && d16 && p->D <= 64;
+  const bool ok_f32 = p->in_dtype == FA_F32 && d16 && p->D <= 128;
   if (!ok_bf16 && !ok_f32) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }

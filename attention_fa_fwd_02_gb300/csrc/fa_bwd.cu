@@ -74,7 +74,12 @@ template <int D_, bool F32_>
 struct BwdCfg {
   static constexpr int D = D_;
   static constexpr bool F32 = F32_;
-  static constexpr int ESZ = F32 ? 4 : 2;
+  // fp32 inputs: 3xTF32 up to D = 64; above, two scaled fp16 terms per operand (X16,
+  // x 2^e = hi + lo, three kind::f16 products per GEMM; 16-bit B operands may be
+  // MN-major, so no transposed copies)
+  static constexpr bool X16 = F32 && D > 64;
+  static constexpr bool TF32 = F32 && !X16;
+  static constexpr int ESZ = TF32 ? 4 : 2;
   static constexpr int ROW = 128 / ESZ;                 // elements per 128-byte row
   static constexpr int NCB = D / ROW;                   // 128-byte column blocks per row
   static constexpr int CH = F32 ? 32 : 64;              // rows per streamed chunk
@@ -83,10 +88,10 @@ struct BwdCfg {
   static constexpr uint32_t SMALL_CB = CH * 128u;       // column block of a CH-row chunk
   static constexpr uint32_t BIG_TILE = NCB * BIG_CB;
   static constexpr uint32_t SMALL_TILE = NCB * SMALL_CB;
-  static constexpr uint32_t T_TILE = F32 ? D * 128u : 0u;  // transposed chunk: D rows x 32 fp32
+  static constexpr uint32_t T_TILE = TF32 ? D * 128u : 0u;  // transposed chunk: D rows x 32 fp32
   static constexpr uint32_t VEC_STAGE = 2 * CH * 4;        // lse2 + delta of one chunk
   // dkdv smem: K, V (hi[, lo]) | KV_NST x chunk (Q, dO [, Q^T, dO^T]) | KV_NST x vectors
-  static constexpr int KV_NST = F32 ? 1 : 4;
+  static constexpr int KV_NST = TF32 ? 1 : (X16 ? 2 : 4);
   static constexpr uint32_t KV_RES = 2 * NSPLIT * BIG_TILE;
   static constexpr uint32_t KV_STAGE = NSPLIT * (2 * SMALL_TILE + 2 * T_TILE);
   static constexpr uint32_t KV_VEC_OFF = KV_RES + KV_NST * KV_STAGE;
@@ -137,6 +142,19 @@ __device__ __forceinline__ void issue_rowdot(uint32_t d, uint32_t a, uint32_t a_
       mma_f16_ss(d, make_sdesc(a + cb * C::BIG_CB + in, 16, SW128_ATOM),
                  make_sdesc(b + cb * C::SMALL_CB + in, 16, SW128_ATOM), id, kk > 0);
     }
+  } else if constexpr (C::X16) {
+    constexpr uint32_t id = make_idesc(128, C::CH, FMT_F16, FMT_F16, false, false);
+#pragma unroll
+    for (int kk = 0; kk < C::D / 16; ++kk) {
+      const uint32_t cb = kk * 16 / 64, in = (kk * 16 % 64) * 2;
+      const uint64_t ah = make_sdesc(a + cb * C::BIG_CB + in, 16, SW128_ATOM);
+      const uint64_t al = make_sdesc(a_lo + cb * C::BIG_CB + in, 16, SW128_ATOM);
+      const uint64_t bh = make_sdesc(b + cb * C::SMALL_CB + in, 16, SW128_ATOM);
+      const uint64_t bl = make_sdesc(b_lo + cb * C::SMALL_CB + in, 16, SW128_ATOM);
+      mma_f16_ss(d, ah, bh, id, kk > 0);
+      mma_f16_ss(d, ah, bl, id, 1);
+      mma_f16_ss(d, al, bh, id, 1);
+    }
   } else {
     constexpr uint32_t id = make_idesc(128, C::CH, FMT_TF32, FMT_TF32, false, false);
 #pragma unroll
@@ -164,6 +182,17 @@ __device__ __forceinline__ void issue_acc(uint32_t acc, uint32_t a_tmem, uint32_
     for (int kk = 0; kk < C::CH / 16; ++kk)
       mma_f16_ts(acc, a_tmem + kk * 8, make_sdesc(b + kk * 16 * 128, C::SMALL_CB, SW128_ATOM), id,
                  (accumulate || kk > 0) ? 1u : 0u);
+  } else if constexpr (C::X16) {
+    // A hi / lo: packed fp16 in TMEM (8 columns per 16 rows); B hi / lo: the MN-major chunk
+    constexpr uint32_t id = make_idesc(128, C::D, FMT_F16, FMT_F16, false, true);
+#pragma unroll
+    for (int kk = 0; kk < C::CH / 16; ++kk) {
+      const uint64_t bh = make_sdesc(b + kk * 16 * 128, C::SMALL_CB, SW128_ATOM);
+      const uint64_t bl = make_sdesc(b_lo + kk * 16 * 128, C::SMALL_CB, SW128_ATOM);
+      mma_f16_ts(acc, a_tmem + kk * 8, bh, id, (accumulate || kk > 0) ? 1u : 0u);
+      mma_f16_ts(acc, a_tmem + kk * 8, bl, id, 1u);
+      mma_f16_ts(acc, alo_tmem + kk * 8, bh, id, 1u);
+    }
   } else {
     constexpr uint32_t id = make_idesc(128, C::D, FMT_TF32, FMT_TF32, false, false);
 #pragma unroll
@@ -218,7 +247,20 @@ __device__ __forceinline__ void tmem_ld_pair(uint32_t sa, uint32_t da, float (&x
 // hi (at `hi`) and lo (at `lo`) parts, one column each.
 template <class C>
 __device__ __forceinline__ void tmem_st_operand(uint32_t hi, uint32_t lo, const float (&x)[C::CH]) {
-  if constexpr (!C::F32) {
+  if constexpr (C::X16) {
+    // fp16 pairs: hi = fp16(x) into the first CH / 2 columns at `hi`, lo = fp16(x - hi) at `lo`
+    static_assert(C::CH == 32, "16 packed columns per term");
+    uint32_t ph[16], pl[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const __half2 h = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
+      const float2 hf = __half22float2(h);
+      ph[k] = *reinterpret_cast<const uint32_t*>(&h);
+      pl[k] = pack_half2(x[2 * k] - hf.x, x[2 * k + 1] - hf.y);
+    }
+    tmem_st16(hi, ph);
+    tmem_st16(lo, pl);
+  } else if constexpr (!C::F32) {
 #pragma unroll
     for (int c = 0; c < C::CH / 64; ++c) {
       uint32_t pk[32];
@@ -361,9 +403,11 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
         last_s[st] = c / NST;
         if (!wait(&bar_aempty[st], ((c / NST) & 1) ^ 1)) break;
         mbar_arrive_expect_tx(&bar_afull[st], 2 * C::NSPLIT * C::T_TILE + C::VEC_STAGE);
-        for (int sp = 0; sp < C::NSPLIT; ++sp) {
-          tma_load_3d(gen(sQt(st, sp)), &m.Qt[sp], &bar_afull[st], i0, 0, bh);
-          tma_load_3d(gen(sdOt(st, sp)), &m.dOt[sp], &bar_afull[st], i0, 0, bh);
+        if constexpr (C::TF32) {
+          for (int sp = 0; sp < C::NSPLIT; ++sp) {
+            tma_load_3d(gen(sQt(st, sp)), &m.Qt[sp], &bar_afull[st], i0, 0, bh);
+            tma_load_3d(gen(sdOt(st, sp)), &m.dOt[sp], &bar_afull[st], i0, 0, bh);
+          }
         }
         tma_load_3d(vecs + st * 2 * CH, &m.L, &bar_afull[st], i0, bh, 0);
         tma_load_3d(vecs + st * 2 * CH + CH, &m.Dl, &bar_afull[st], i0, bh, 0);
@@ -390,7 +434,9 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
         issue_rowdot<C>(tmem + C::dp_col(bb), sV(0), sV(C::NSPLIT - 1), sdOc(st, 0),
                         sdOc(st, C::NSPLIT - 1));
         tc_commit(&bar_sp[bb]);
-        tc_commit(&bar_sempty[st]);  // the score half of the stage may take the next chunk
+        // the score half of the stage may take the next chunk (X16: not yet -- the
+        // accumulating MMAs read the same Q / dO chunks; they release it)
+        if constexpr (!C::X16) tc_commit(&bar_sempty[st]);
       }
       tc_commit(&bar_drain[0]);
       drain_wait(&bar_drain[0], 0, a.limit_ns);
@@ -406,10 +452,18 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
         // the accumulate half (its phase of chunk c cannot be passed before aempty(c))
         if (!(ok = wait(&bar_afull[pst], (c / NST) & 1))) break;
         tc_fence_after();
-        issue_acc<C>(tmem + C::KV_ACC0, tmem + C::s_col(pb), tmem + C::plo_col(pb), sdOt(pst, 0),
-                     sdOt(pst, 1), c > 0);
-        issue_acc<C>(tmem + C::KV_ACC1, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sQt(pst, 0),
-                     sQt(pst, 1), c > 0);
+        if constexpr (C::X16) {  // B = the MN-major Q / dO chunks themselves
+          issue_acc<C>(tmem + C::KV_ACC0, tmem + C::s_col(pb), tmem + C::plo_col(pb), sdOc(pst, 0),
+                       sdOc(pst, 1), c > 0);
+          issue_acc<C>(tmem + C::KV_ACC1, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sQc(pst, 0),
+                       sQc(pst, 1), c > 0);
+          tc_commit(&bar_sempty[pst]);
+        } else {
+          issue_acc<C>(tmem + C::KV_ACC0, tmem + C::s_col(pb), tmem + C::plo_col(pb), sdOt(pst, 0),
+                       sdOt(pst, 1), c > 0);
+          issue_acc<C>(tmem + C::KV_ACC1, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sQt(pst, 0),
+                       sQt(pst, 1), c > 0);
+        }
         tc_commit(&bar_aempty[pst]);
         tc_commit(&bar_accdone[pb]);
       }
@@ -423,7 +477,9 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
     const int r_in = wq * 32 + lane;
     const int j = j0 + r_in;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-    const float sl2 = a.scale_log2;
+    // X16: scores and dP^T from the scaled copies (multipliers as in the bf16 kernels)
+    const float sl2 = C::X16 ? a.sc->sl2 : a.scale_log2;
+    const float dp_mul = C::X16 ? a.sc->dp_mul : 1.f;
     bool ok = true;
     for (int c = 0; c < nc; ++c) {
       const int bb = c & 1, st = c % NST;
@@ -450,7 +506,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
 #pragma unroll
       for (int k = 0; k < CH; ++k) {
         const float p = ex2(fmaf(s[k], sl2, -lv[k]));
-        dp[k] = p * (dp[k] - lv[CH + k]);
+        dp[k] = p * (C::X16 ? fmaf(dp[k], dp_mul, -lv[CH + k]) : dp[k] - lv[CH + k]);
         s[k] = p;
       }
       tmem_st_operand<C>(lane_addr + C::s_col(bb), lane_addr + C::plo_col(bb), s);
@@ -468,15 +524,16 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       const uint32_t st_v = sbase + wq * 2 * C::EPI_WARP, st_k = st_v + C::EPI_WARP;
       const int r_base = j0 + wq * 32;
       const bool any = r_base < a.Sk;
+      const float mul_v = C::X16 ? a.sc->dv_mul : 1.f, mul_k = C::X16 ? a.sc->dk_mul : a.scale;
       if (a.out_bf16) {
-        store_rows_tma<D, true, D / 64, false>(&m.dV, lane_addr + C::KV_ACC0, nc > 0, 1.f, st_v,
+        store_rows_tma<D, true, D / 64, false>(&m.dV, lane_addr + C::KV_ACC0, nc > 0, mul_v, st_v,
                                                r_base, any, bg, 0, a.Dv);
-        store_rows_tma<D, true, D / 64, false>(&m.dK, lane_addr + C::KV_ACC1, nc > 0, a.scale, st_k,
+        store_rows_tma<D, true, D / 64, false>(&m.dK, lane_addr + C::KV_ACC1, nc > 0, mul_k, st_k,
                                                r_base, any, bg, 0, a.Dv);
       } else {
-        store_rows_tma<D, false, D / 32, false>(&m.dV, lane_addr + C::KV_ACC0, nc > 0, 1.f, st_v,
+        store_rows_tma<D, false, D / 32, false>(&m.dV, lane_addr + C::KV_ACC0, nc > 0, mul_v, st_v,
                                                 r_base, any, bg, 0, a.Dv);
-        store_rows_tma<D, false, D / 32, false>(&m.dK, lane_addr + C::KV_ACC1, nc > 0, a.scale, st_k,
+        store_rows_tma<D, false, D / 32, false>(&m.dK, lane_addr + C::KV_ACC1, nc > 0, mul_k, st_k,
                                                 r_base, any, bg, 0, a.Dv);
       }
       if (lane == 0) bulk_wait_read_all();
@@ -582,7 +639,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
             tma_load_3d(gen(sKc(st, sp)) + cb * C::SMALL_CB, &m.Kc[sp], &bar_full[st], cb * C::ROW, k0, bg);
             tma_load_3d(gen(sVc(st, sp)) + cb * C::SMALL_CB, &m.Vc[sp], &bar_full[st], cb * C::ROW, k0, bg);
           }
-          if constexpr (C::F32) tma_load_3d(gen(sKt(st, sp)), &m.Kt[sp], &bar_full[st], k0, 0, bg);
+          if constexpr (C::TF32) tma_load_3d(gen(sKt(st, sp)), &m.Kt[sp], &bar_full[st], k0, 0, bg);
         }
         last[st] = c / NST;
       }
@@ -620,6 +677,9 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
         tc_fence_after();
         if constexpr (!C::F32)
           issue_acc<C>(tmem + C::Q_ACC, tmem + C::dp_col(pb), 0, sKc(pst, 0), 0, c > 0);
+        else if constexpr (C::X16)  // B = the MN-major K chunk itself
+          issue_acc<C>(tmem + C::Q_ACC, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sKc(pst, 0),
+                       sKc(pst, 1), c > 0);
         else
           issue_acc<C>(tmem + C::Q_ACC, tmem + C::dp_col(pb), tmem + C::dslo_col(pb), sKt(pst, 0),
                        sKt(pst, 1), c > 0);
@@ -635,7 +695,8 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
     const int r_in = wq * 32 + lane;
     const int i = i0 + r_in;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-    const float sl2 = a.scale_log2;
+    const float sl2 = C::X16 ? a.sc->sl2 : a.scale_log2;
+    const float dp_mul = C::X16 ? a.sc->dp_mul : 1.f;
     const bool row_valid = i < a.Sq;
     const size_t vrow = (size_t)bh * a.ldq + (size_t)(row_valid ? i : 0);
     const float lse2 = row_valid ? a.lse2[vrow] : INFINITY;
@@ -659,7 +720,8 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       }
       const float nl = -lse2;
 #pragma unroll
-      for (int k = 0; k < CH; ++k) dp[k] = ex2(fmaf(s[k], sl2, nl)) * (dp[k] - dl);
+      for (int k = 0; k < CH; ++k)
+        dp[k] = ex2(fmaf(s[k], sl2, nl)) * (C::X16 ? fmaf(dp[k], dp_mul, -dl) : dp[k] - dl);
       tmem_st_operand<C>(lane_addr + C::dp_col(bb), lane_addr + C::dslo_col(bb), dp);
       tmem_st_wait();
       tc_fence_before();
@@ -673,11 +735,12 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       // bar_done: every MMA has completed, so all operand buffers are free.
       const uint32_t st_q = sbase + wq * C::EPI_WARP;
       const int r_base = i0 + wq * 32;
+      const float mul_q = C::X16 ? a.sc->dq_mul : a.scale;
       if (a.out_bf16)
-        store_rows_tma<D, true, D / 64>(&m.dQ, lane_addr + C::Q_ACC, nc > 0, a.scale, st_q, r_base,
+        store_rows_tma<D, true, D / 64>(&m.dQ, lane_addr + C::Q_ACC, nc > 0, mul_q, st_q, r_base,
                                         r_base < a.Sq, bh, 0, a.Dv);
       else
-        store_rows_tma<D, false, D / 32>(&m.dQ, lane_addr + C::Q_ACC, nc > 0, a.scale, st_q,
+        store_rows_tma<D, false, D / 32>(&m.dQ, lane_addr + C::Q_ACC, nc > 0, mul_q, st_q,
                                          r_base, r_base < a.Sq, bh, 0, a.Dv);
     }
   }
@@ -2144,6 +2207,50 @@ __global__ void dq_range_sum_kernel(const float* __restrict__ part, void* __rest
   }
 }
 
+// fp32 inputs at D > 64 (X16): every block reduces the amax kernel's per-block maxima
+// of |Q|, |K|, |V|, |dO| and |delta|, picks the exponents (x16_exponent for the
+// copies, x16_ds_exponent for dS), and the grid writes x 2^e = hi + lo as fp16 pairs
+// and delta 2^eD; block 0 publishes the multipliers (as bwd_scales_kernel does).
+struct X16BwdArgs {
+  const uint32_t* part;
+  int n_part;
+  int dlog;
+  const float* src[4];  // Q, K, V, dO
+  __half* hi[4];
+  __half* lo[4];
+  size_t n4[4];
+  float* delta;
+  size_t n_delta;
+  float scale, scale_log2;
+  OperandScales* out;
+};
+__global__ void __launch_bounds__(256) x16_bwd_split_kernel(const __grid_constant__ X16BwdArgs a) {
+  uint32_t m[5];
+  reduce_partials<5>(a.part, a.n_part, m);
+  int e[5];
+  for (int k = 0; k < 4; ++k) e[k] = x16_exponent(m[k]);
+  e[SC_DS] = x16_ds_exponent(m[3], m[2], m[4], a.dlog);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    OperandScales sc;
+    sc.sl2 = ldexpf(a.scale_log2, -(e[SC_Q] + e[SC_K]));
+    sc.dp_mul = ldexpf(1.f, e[SC_DS] - e[SC_DO] - e[SC_V]);
+    sc.dq_mul = ldexpf(a.scale, -(e[SC_DS] + e[SC_K]));
+    sc.dk_mul = ldexpf(a.scale, -(e[SC_DS] + e[SC_Q]));
+    sc.dv_mul = ldexpf(1.f, -e[SC_DO]);
+    sc.o_mul = 1.f;
+    for (int k = 0; k < 5; ++k) sc.e[k] = e[k];
+    sc.pad = 0;
+    *a.out = sc;
+  }
+  for (int k = 0; k < 4; ++k) split_x16(a.src[k], a.hi[k], a.lo[k], a.n4[k], e[k]);
+  if (e[SC_DS] != 0) {
+    const float f = pow2i(e[SC_DS]);
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < a.n_delta; i += stride)
+      a.delta[i] *= f;
+  }
+}
+
 // Zero-fill outputs of an empty side (Sq == 0 or Sk == 0).
 __global__ void zero_kernel(uint4* p, size_t n16) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16;
@@ -2173,13 +2280,14 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   const size_t nqt = BH * Dv * ldqt, nkt = BHk * Dv * ldkt;
   size_t bytes = 2 * nvec * 4;
   if constexpr (!F32) bytes += (2 * nq + 2 * nk) * 2;
+  else if constexpr (C::X16) bytes += (4 * nq + 4 * nk) * 2;  // Q,dO,K,V fp16 hi/lo
   else bytes += (4 * nq + 4 * nk + 4 * nqt + 2 * nkt) * 4;  // Q,dO,K,V hi/lo + Q^T,dO^T,K^T hi/lo
   const size_t sched_off = (bytes + 15) / 16 * 16;  // the dQ kernel's work-item counter
   bytes = sched_off + 16;
   // bf16 inputs: the call's OperandScales and the pre-pass blocks' partial maxima
   const int n_pre = 8 * host::sm_count();  // pre-pass blocks
   const size_t sc_off = (bytes + 255) / 256 * 256;
-  if constexpr (!F32) bytes = sc_off + 256 + (size_t)n_pre * 5 * 4;
+  if constexpr (!C::TF32) bytes = sc_off + 256 + (size_t)n_pre * 5 * 4;
   // Fewer query tiles than SMs (short query sequences, bf16 inputs): the dQ work items
   // also split the keys into ranges of tps tiles (key_range_tiles picks tps), each
   // range writing a partial dQ (fp32) that a sum kernel adds up afterwards.
@@ -2201,8 +2309,9 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   float* lse2 = static_cast<float*>(ws);
   float* delta = lse2 + nvec;
   int* sched = reinterpret_cast<int*>(static_cast<char*>(ws) + sched_off);
-  OperandScales* sc = F32 ? nullptr : reinterpret_cast<OperandScales*>(static_cast<char*>(ws) + sc_off);
-  uint32_t* part = F32 ? nullptr : reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + sc_off + 256);
+  OperandScales* sc =
+      C::TF32 ? nullptr : reinterpret_cast<OperandScales*>(static_cast<char*>(ws) + sc_off);
+  uint32_t* part = C::TF32 ? nullptr : reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + sc_off + 256);
   float* dq_part = dq_splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(ws) + part_off) : nullptr;
   __half* ds_hi = dsmat ? reinterpret_cast<__half*>(static_cast<char*>(ws) + ds_off) : nullptr;
   __half* ds_lo = dsmat && split ? ds_hi + ds_elems : nullptr;
@@ -2301,6 +2410,76 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     mk.Qt[0] = mk.Qt[1] = mk.Qc[0]; mk.dOt[0] = mk.dOt[1] = mk.dOc[0];
     mq.Q[1] = mq.Q[0]; mq.dO[1] = mq.dO[0]; mq.Kc[1] = mq.Kc[0]; mq.Vc[1] = mq.Vc[0];
     mq.Kt[0] = mq.Kt[1] = mq.Kc[0];
+  } else if constexpr (C::X16) {
+    __half* qh = reinterpret_cast<__half*>(delta + nvec);
+    __half* ql = qh + nq;
+    __half* doh = ql + nq;
+    __half* dol = doh + nq;
+    __half* kh = dol + nq;
+    __half* kl = kh + nk;
+    __half* vh = kl + nk;
+    __half* vl = vh + nk;
+    {
+      host::KernelTimer kt("bwd_preprocess", stream);
+      bwd_preprocess_kernel<D><<<grid_pp, 256, 0, stream>>>(dO, O, LSE, Q, nullptr, nullptr, lse2,
+                                                           delta, p.Sq, ldq, nvec, 0,
+                                                           p.out_dtype == FA_BF16, Dv);
+    }
+    AmaxJobs aj = {};
+    aj.a[0] = static_cast<const float*>(Q);
+    aj.a[1] = static_cast<const float*>(K);
+    aj.a[2] = static_cast<const float*>(V);
+    aj.a[3] = static_cast<const float*>(dO);
+    aj.a[4] = delta;
+    aj.n4[0] = aj.n4[3] = nq / 4;
+    aj.n4[1] = aj.n4[2] = nk / 4;
+    aj.n4[4] = nvec / 4;
+    aj.n = 5;
+    {
+      host::KernelTimer kt("amax(Q,K,V,dO,delta)", stream);
+      amax_f32_kernel<5><<<n_pre, 256, 0, stream>>>(aj, part);
+    }
+    X16BwdArgs xa;
+    xa.part = part;
+    xa.n_part = n_pre;
+    int dlog = 0;
+    while ((1 << dlog) < Dv) ++dlog;
+    xa.dlog = dlog;
+    __half* his[4] = {qh, kh, vh, doh};
+    __half* los[4] = {ql, kl, vl, dol};
+    for (int k = 0; k < 4; ++k) {
+      xa.src[k] = aj.a[k];
+      xa.hi[k] = his[k];
+      xa.lo[k] = los[k];
+      xa.n4[k] = aj.n4[k];
+    }
+    xa.delta = delta;
+    xa.n_delta = nvec;
+    xa.scale = p.scale;
+    xa.scale_log2 = p.scale * LOG2E;
+    xa.out = sc;
+    {
+      host::KernelTimer kt("x16_split(Q,K,V,dO)", stream);
+      x16_bwd_split_kernel<<<n_pre, 256, 0, stream>>>(xa);
+    }
+    const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    __half* hl_q[2] = {qh, ql};
+    __half* hl_do[2] = {doh, dol};
+    __half* hl_k[2] = {kh, kl};
+    __half* hl_v[2] = {vh, vl};
+    for (int sp = 0; sp < 2; ++sp) {
+      enc &= host::encode_tiled_3d(&mk.K[sp], F16, 2, hl_k[sp], Dv, p.Sk, BHk, Dv, 64, 128);
+      enc &= host::encode_tiled_3d(&mk.V[sp], F16, 2, hl_v[sp], Dv, p.Sk, BHk, Dv, 64, 128);
+      enc &= host::encode_tiled_3d(&mk.Qc[sp], F16, 2, hl_q[sp], Dv, p.Sq, BH, Dv, 64, C::CH);
+      enc &= host::encode_tiled_3d(&mk.dOc[sp], F16, 2, hl_do[sp], Dv, p.Sq, BH, Dv, 64, C::CH);
+      enc &= host::encode_tiled_3d(&mq.Q[sp], F16, 2, hl_q[sp], Dv, p.Sq, BH, Dv, 64, 128);
+      enc &= host::encode_tiled_3d(&mq.dO[sp], F16, 2, hl_do[sp], Dv, p.Sq, BH, Dv, 64, 128);
+      enc &= host::encode_tiled_3d(&mq.Kc[sp], F16, 2, hl_k[sp], Dv, p.Sk, BHk, Dv, 64, C::CH);
+      enc &= host::encode_tiled_3d(&mq.Vc[sp], F16, 2, hl_v[sp], Dv, p.Sk, BHk, Dv, 64, C::CH);
+      mk.Qt[sp] = mk.Qc[sp];  // (no transposed copies: unused)
+      mk.dOt[sp] = mk.dOc[sp];
+      mq.Kt[sp] = mq.Kc[sp];
+    }
   } else {
     float* qh = delta + nvec;
     float* ql = qh + nq;
@@ -2379,7 +2558,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       auto kern = fa_bwd_dkdv_kernel<D, F32>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::KV_SMEM);
       if (e == cudaSuccess) {
-        host::KernelTimer kt("fa_bwd_dkdv_kernel<64,f32>", stream);
+        host::KernelTimer kt(D == 128 ? "fa_bwd_dkdv_kernel<128,f32>" : "fa_bwd_dkdv_kernel<64,f32>",
+                             stream);
         kern<<<(unsigned)(BHk * ak.n_tiles), C::THREADS, C::KV_SMEM, stream>>>(mk, ak);
         e = cudaGetLastError();
       }
@@ -2412,7 +2592,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       auto kern = fa_bwd_dq_kernel<D, F32>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::Q_SMEM);
       if (e == cudaSuccess) {
-        host::KernelTimer kt("fa_bwd_dq_kernel<64,f32>", stream);
+        host::KernelTimer kt(D == 128 ? "fa_bwd_dq_kernel<128,f32>" : "fa_bwd_dq_kernel<64,f32>",
+                             stream);
         kern<<<(unsigned)(BH * aq.n_tiles), C::THREADS, C::Q_SMEM, stream>>>(mq, aq);
         e = cudaGetLastError();
       }
@@ -2514,6 +2695,7 @@ fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O,
     if (p.D <= 128) return run_bwd<128, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, dsmat);
   } else {
     if (p.D <= 64) return run_bwd<64, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, false);
+    if (p.D <= 128) return run_bwd<128, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, false);
   }
   return FA_ERR_UNSUPPORTED;
 }

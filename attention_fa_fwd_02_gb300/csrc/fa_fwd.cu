@@ -59,8 +59,13 @@ template <int D_, bool F32_>
 struct FwdCfg {
   static constexpr int D = D_;
   static constexpr bool F32 = F32_;
+  // fp32 inputs: 3xTF32 (hi / lo tf32 splits) up to D = 64; above, whose tf32 tiles would
+  // not fit shared memory, two scaled fp16 terms per operand (X16: x 2^e = hi + lo,
+  // three kind::f16 products per GEMM)
+  static constexpr bool X16 = F32 && D > 64;
+  static constexpr bool TF32 = F32 && !X16;
   static constexpr int NQ = F32 ? 1 : 2;                   // query tiles per CTA
-  static constexpr int ESZ = F32 ? 4 : 2;                  // operand bytes in smem
+  static constexpr int ESZ = TF32 ? 4 : 2;                 // operand bytes in smem
   static constexpr int ROW_ELEMS = 128 / ESZ;              // elements per 128-byte row
   static constexpr int NCB = D / ROW_ELEMS;                // 128-byte column blocks per row-tile
   static constexpr uint32_t CB_BYTES = 128u * 128u;        // one column block of a 128-row tile
@@ -114,6 +119,20 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t 
       mma_f16_ss(d_tmem, make_sdesc(sq + off, 16, SW128_ATOM), make_sdesc(sk + off, 16, SW128_ATOM),
                  id, kk > 0);
     }
+  } else if constexpr (C::X16) {
+    // (Qh + Ql)(Kh + Kl)^T without the lo * lo term, fp16 terms
+    constexpr uint32_t id = make_idesc(128, 128, FMT_F16, FMT_F16, false, false);
+#pragma unroll
+    for (int kk = 0; kk < C::D / 16; ++kk) {
+      const uint32_t off = (kk * 16 / 64) * C::CB_BYTES + (kk * 16 % 64) * 2;
+      const uint64_t qh = make_sdesc(sq + off, 16, SW128_ATOM);
+      const uint64_t ql = make_sdesc(sq_lo + off, 16, SW128_ATOM);
+      const uint64_t kh = make_sdesc(sk + off, 16, SW128_ATOM);
+      const uint64_t kl = make_sdesc(sk_lo + off, 16, SW128_ATOM);
+      mma_f16_ss(d_tmem, qh, kh, id, kk > 0);
+      mma_f16_ss(d_tmem, qh, kl, id, 1);
+      mma_f16_ss(d_tmem, ql, kh, id, 1);
+    }
   } else {
     constexpr uint32_t id = make_idesc(128, 128, FMT_TF32, FMT_TF32, false, false);
 #pragma unroll
@@ -146,6 +165,18 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
       for (int kk = 0; kk < BLOCK_N / 16; ++kk)
         mma_f16_ts(o_tmem, p_tmem + 64 + kk * 8,
                    make_sdesc(sv + kk * 16 * 128, C::CB_BYTES, SW128_ATOM), id, 1u);
+    }
+  } else if constexpr (C::X16) {
+    // (Ph + Pl)(Vh + Vl) without the lo * lo term: P hi / lo in the S slot's two column
+    // halves, V hi / lo MN-major in smem
+    constexpr uint32_t id = make_idesc(128, C::D, FMT_F16, FMT_F16, false, true);
+#pragma unroll
+    for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
+      const uint64_t vh = make_sdesc(sv + kk * 16 * 128, C::CB_BYTES, SW128_ATOM);
+      const uint64_t vl = make_sdesc(sv_lo + kk * 16 * 128, C::CB_BYTES, SW128_ATOM);
+      mma_f16_ts(o_tmem, p_tmem + kk * 8, vh, id, (accumulate || kk > 0) ? 1u : 0u);
+      mma_f16_ts(o_tmem, p_tmem + kk * 8, vl, id, 1u);
+      mma_f16_ts(o_tmem, p_tmem + 64 + kk * 8, vh, id, 1u);
     }
   } else {
     // A = P_hi / P_lo (fp32, TMEM, one column per key); B = V^T (K-major: rows = d).
@@ -182,9 +213,10 @@ __device__ __forceinline__ void issue_v_load(uint8_t* smem, int it, int t, int b
   mbar_arrive_expect_tx(&bar_vfull[vs], C::NSPLIT * C::TILE_BYTES);
   for (int sp = 0; sp < C::NSPLIT; ++sp) {
     uint8_t* dst = smem + C::V_OFF + (vs * C::NSPLIT + sp) * C::TILE_BYTES;
-    if constexpr (!C::F32) {
+    if constexpr (!C::TF32) {
       for (int cb = 0; cb < C::NCB; ++cb)
-        tma_load_3d(dst + cb * C::CB_BYTES, tmV, &bar_vfull[vs], cb * C::ROW_ELEMS, t * BLOCK_N, bg);
+        tma_load_3d(dst + cb * C::CB_BYTES, sp ? tmVlo : tmV, &bar_vfull[vs], cb * C::ROW_ELEMS,
+                    t * BLOCK_N, bg);
     } else {  // V^T: 4 boxes of 32 keys x D rows
       for (int cb = 0; cb < 4; ++cb)
         tma_load_3d(dst + cb * C::VT_CB_BYTES, sp ? tmVlo : tmV, &bar_vfull[vs], t * BLOCK_N + cb * 32,
@@ -544,7 +576,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const uint32_t s_addr = lane_addr + C::s_col(q);
     const uint32_t o_addr = lane_addr + C::o_col(q);
-    const float sl2 = a.scale_log2;
+    // X16: the scores come from scaled copies of Q and K (sl2 carries 2^-(eQ + eK))
+    const float sl2 = C::X16 ? a.sc->sl2 : a.scale_log2;
     const float o_mul = a.sc ? a.sc->o_mul : 1.f;  // O from the scaled V copy, back to V's units
     bool ok = true;
     int g = 0, j = 0;
@@ -632,19 +665,20 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         }
         const float nm = -m;
         float l0 = 0.f, l1 = 0.f;
-        if constexpr (!C::F32) {
+        if constexpr (!C::TF32) {
+          constexpr bool TWO = PSPLIT || C::X16;  // P as fp16 hi + lo
           // exponent arguments and the row sum on packed pairs
           const float2 sl2x2 = make_float2(sl2, sl2), nmx2 = make_float2(nm, nm);
           float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            uint32_t pk[32], pl[PSPLIT ? 32 : 1];
+            uint32_t pk[32], pl[TWO ? 32 : 1];
 #pragma unroll
             for (int kk = 0; kk < 32; ++kk) {
               const float2 x = fma2(make_float2(s[c * 64 + 2 * kk], s[c * 64 + 2 * kk + 1]), sl2x2, nmx2);
               const float2 pp = make_float2(ex2(x.x), ex2(x.y));
               ls[kk & 1] = add2(ls[kk & 1], pp);
-              if constexpr (PSPLIT) {
+              if constexpr (TWO) {
                 const __half2 h = __floats2half2_rn(pp.x, pp.y);
                 const float2 hf = __half22float2(h);
                 pk[kk] = *reinterpret_cast<const uint32_t*>(&h);
@@ -654,7 +688,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
               }
             }
             tmem_st32(s_addr + c * 32, pk);
-            if constexpr (PSPLIT) tmem_st32(s_addr + 64 + c * 32, pl);  // (S read in full above)
+            if constexpr (TWO) tmem_st32(s_addr + 64 + c * 32, pl);  // (S read in full above)
           }
           l0 = ls[0].x + ls[1].x;
           l1 = ls[0].y + ls[1].y;
@@ -771,6 +805,38 @@ __global__ void __launch_bounds__(1024) fwd_scales_kernel(const uint32_t* __rest
   if (ev != 0) rescale_copy(V, V16, n8, ev);
 }
 
+// fp32 inputs at D > 64 (X16): every block reduces the amax kernel's per-block maxima
+// of |Q|, |K|, |V|, picks each tensor's exponent (x16_exponent), and the grid writes
+// x 2^e = hi + lo as fp16 pairs; block 0 publishes the multipliers (scores:
+// scale log2(e) 2^-(eQ + eK); O: 2^-eV).
+struct X16FwdArgs {
+  const uint32_t* part;
+  int n_part;
+  const float* src[3];  // Q, K, V
+  __half* hi[3];
+  __half* lo[3];
+  size_t n4[3];
+  float scale_log2;
+  OperandScales* out;
+};
+__global__ void __launch_bounds__(256) x16_fwd_split_kernel(const __grid_constant__ X16FwdArgs a) {
+  uint32_t m[3];
+  reduce_partials<3>(a.part, a.n_part, m);
+  int e[3];
+  for (int k = 0; k < 3; ++k) e[k] = x16_exponent(m[k]);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    OperandScales sc = {};
+    sc.sl2 = ldexpf(a.scale_log2, -(e[0] + e[1]));
+    sc.dp_mul = sc.dq_mul = sc.dk_mul = sc.dv_mul = 1.f;
+    sc.o_mul = pow2i(-e[2]);
+    sc.e[SC_Q] = e[0];
+    sc.e[SC_K] = e[1];
+    sc.e[SC_V] = e[2];
+    *a.out = sc;
+  }
+  for (int k = 0; k < 3; ++k) split_x16(a.src[k], a.hi[k], a.lo[k], a.n4[k], e[k]);
+}
+
 // Key ranges of one query row computed separately: partial outputs O_s
 // (each normalised by its own row sum) and natural-log LSE_s per range, slab
 // s * rows + r. The row's result is the softmax over all its keys:
@@ -853,6 +919,65 @@ bool encode_o_map(CUtensorMap* m, void* O, const fa_params& p) {
                                bf ? 2 : 4, O, p.D, p.Sq, (uint64_t)p.B * p.H, p.D, bf ? 64 : 32, 32);
 }
 
+// X16 (fp32 inputs, D > 64): scratch bytes for the fp16 hi / lo copies of Q, K, V, the
+// OperandScales and the amax kernel's n_amax x 3 partial maxima.
+size_t x16_fwd_bytes(const fa_params& p, int n_amax) {
+  const size_t nq = (size_t)p.B * p.H * p.Sq * p.D, nk = (size_t)p.B * p.HKV * p.Sk * p.D;
+  return (2 * nq + 4 * nk) * 2 + 256 + (size_t)n_amax * 3 * 4;
+}
+
+// X16: the copies and scales in `ws` (x16_fwd_bytes of it) and their tensor maps.
+bool prep_x16_fwd(void* ws, const void* Q, const void* K, const void* V, const fa_params& p,
+                  int n_amax, cudaStream_t stream, CUtensorMap* mQ, CUtensorMap* mQlo,
+                  CUtensorMap* mK, CUtensorMap* mKlo, CUtensorMap* mV, CUtensorMap* mVlo,
+                  OperandScales** sc_out) {
+  const int Dv = p.D;
+  const size_t nq = (size_t)p.B * p.H * p.Sq * Dv, nk = (size_t)p.B * p.HKV * p.Sk * Dv;
+  const uint64_t BHq = (uint64_t)p.B * p.H, BHk = (uint64_t)p.B * p.HKV;
+  __half* qh = static_cast<__half*>(ws);
+  __half* ql = qh + nq;
+  __half* kh = ql + nq;
+  __half* kl = kh + nk;
+  __half* vh = kl + nk;
+  __half* vl = vh + nk;
+  char* tail = reinterpret_cast<char*>(vl + nk);
+  OperandScales* sc = reinterpret_cast<OperandScales*>(tail);
+  uint32_t* part = reinterpret_cast<uint32_t*>(tail + 256);
+  AmaxJobs aj = {};
+  aj.a[0] = static_cast<const float*>(Q);
+  aj.a[1] = static_cast<const float*>(K);
+  aj.a[2] = static_cast<const float*>(V);
+  aj.n4[0] = nq / 4;
+  aj.n4[1] = aj.n4[2] = nk / 4;
+  aj.n = 3;
+  {
+    host::KernelTimer kt("amax(Q,K,V)", stream);
+    amax_f32_kernel<3><<<n_amax, 256, 0, stream>>>(aj, part);
+  }
+  X16FwdArgs xa;
+  xa.part = part;
+  xa.n_part = n_amax;
+  xa.src[0] = aj.a[0]; xa.src[1] = aj.a[1]; xa.src[2] = aj.a[2];
+  xa.hi[0] = qh; xa.hi[1] = kh; xa.hi[2] = vh;
+  xa.lo[0] = ql; xa.lo[1] = kl; xa.lo[2] = vl;
+  xa.n4[0] = nq / 4; xa.n4[1] = xa.n4[2] = nk / 4;
+  xa.scale_log2 = p.scale * LOG2E;
+  xa.out = sc;
+  {
+    host::KernelTimer kt("x16_split(Q,K,V)", stream);
+    x16_fwd_split_kernel<<<n_amax, 256, 0, stream>>>(xa);
+  }
+  const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  bool enc = host::encode_tiled_3d(mQ, F16, 2, qh, Dv, p.Sq, BHq, Dv, 64, 128);
+  enc &= host::encode_tiled_3d(mQlo, F16, 2, ql, Dv, p.Sq, BHq, Dv, 64, 128);
+  enc &= host::encode_tiled_3d(mK, F16, 2, kh, Dv, p.Sk, BHk, Dv, 64, 128);
+  enc &= host::encode_tiled_3d(mKlo, F16, 2, kl, Dv, p.Sk, BHk, Dv, 64, 128);
+  enc &= host::encode_tiled_3d(mV, F16, 2, vh, Dv, p.Sk, BHk, Dv, 64, 128);
+  enc &= host::encode_tiled_3d(mVlo, F16, 2, vl, Dv, p.Sk, BHk, Dv, 64, 128);
+  *sc_out = sc;
+  return enc && cudaGetLastError() == cudaSuccess;
+}
+
 // The forward kernel instantiation: head-pair items (two-tile kernels only) or not;
 // two-term P (bf16 inputs) or not.
 template <int D, bool F32>
@@ -904,6 +1029,10 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
     enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, Dv, p.Sk, BHk, Dv, 64, 128);
     enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, Dv, p.Sk, BHk, Dv, 64, 128);
     mQlo = mQ; mKlo = mK; mVlo = mV;
+  } else if constexpr (C::X16) {
+    const int n_amax = 8 * host::sm_count();
+    if (host::scratch_alloc(&ws, x16_fwd_bytes(p, n_amax), stream) != cudaSuccess) return FA_ERR_CUDA;
+    enc &= prep_x16_fwd(ws, Q, K, V, p, n_amax, stream, &mQ, &mQlo, &mK, &mKlo, &mV, &mVlo, &sc);
   } else {
     const int ldt = (p.Sk + 3) / 4 * 4;  // transposed V rows padded to 16 bytes
     const size_t nvt = (size_t)p.B * p.HKV * Dv * ldt;
@@ -988,7 +1117,7 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_ALLOC);
   if (e == cudaSuccess) {
-    host::KernelTimer kt(F32 ? "fa_fwd_kernel<64,f32>"
+    host::KernelTimer kt(F32 ? (D == 128 ? "fa_fwd_kernel<128,f32>" : "fa_fwd_kernel<64,f32>")
                              : (D == 128 ? "fa_fwd_kernel<128,bf16>" : "fa_fwd_kernel<64,bf16>"),
                          stream);
     kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, mO, a);
@@ -1025,6 +1154,7 @@ fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float
     if (p.D <= 128) return run_fwd<128, false>(Q, K, V, O, LSE, p, stream);
   } else {
     if (p.D <= 64) return run_fwd<64, true>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 128) return run_fwd<128, true>(Q, K, V, O, LSE, p, stream);
   }
   return FA_ERR_UNSUPPORTED;
 }
@@ -1127,12 +1257,14 @@ fa_status noalloc_scratch_addr(void** out) {
 // Scratch bytes the problem needs, in double so that no product can wrap around
 // (exact while it is anywhere near the array's size). bf16: the fp16 copy of V, padded
 // to 256 bytes, then the OperandScales and one partial maximum per conversion block.
-template <bool F32>
+template <bool F32, bool X16>
 double noalloc_bytes(const fa_params& p, int n_cvt) {
   const double nq = (double)p.B * p.H * p.Sq * p.D;
   const double nk = (double)p.B * p.HKV * p.Sk * p.D;
   if constexpr (!F32) {
     return std::ceil(nk * 2 / 256) * 256 + 256 + 4.0 * n_cvt;
+  } else if constexpr (X16) {  // fp16 hi / lo of Q, K, V, the scales, the amax partials
+    return (2 * nq + 4 * nk) * 2 + 256 + 12.0 * n_cvt;
   } else {
     const double ldt = (double)(((long long)p.Sk + 3) / 4 * 4);
     const double nvt = (double)p.B * p.HKV * p.D * ldt;
@@ -1145,7 +1277,8 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
                           const fa_params& p, cudaStream_t stream) {
   using C = FwdCfg<D, F32>;
   const int n_cvt = 8 * host::sm_count();  // conversion blocks (bf16 inputs)
-  if (noalloc_bytes<F32>(p, n_cvt) > (double)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+  if (noalloc_bytes<F32, C::X16>(p, n_cvt) > (double)FA_NOALLOC_SCRATCH_BYTES)
+    return FA_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;
   const fa_status st = noalloc_scratch_addr(&ws);
   if (st != FA_OK) return st;
@@ -1174,6 +1307,8 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
     enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, Dv, p.Sk, BHk, Dv, 64, 128);
     enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, Dv, p.Sk, BHk, Dv, 64, 128);
     mQlo = mQ; mKlo = mK; mVlo = mV;
+  } else if constexpr (C::X16) {
+    enc &= prep_x16_fwd(ws, Q, K, V, p, n_cvt, stream, &mQ, &mQlo, &mK, &mKlo, &mV, &mVlo, &sc);
   } else {
     const int ldt = (p.Sk + 3) / 4 * 4;
     const size_t nvt = (size_t)p.B * p.HKV * Dv * ldt;
@@ -1244,6 +1379,7 @@ fa_status launch_fwd_noalloc(const void* Q, const void* K, const void* V, void* 
     if (p.D <= 128) return run_fwd_noalloc<128, false>(Q, K, V, O, LSE, p, stream);
   } else {
     if (p.D <= 64) return run_fwd_noalloc<64, true>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 128) return run_fwd_noalloc<128, true>(Q, K, V, O, LSE, p, stream);
   }
   return FA_ERR_UNSUPPORTED;
 }

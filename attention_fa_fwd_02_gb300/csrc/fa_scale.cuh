@@ -69,6 +69,28 @@ __host__ __device__ inline int ds_exponent(uint32_t amax_do, uint32_t amax_v,
   return clamp_exp(DS_TOP - u);
 }
 
+// fp32 inputs carried as two scaled fp16 terms (x 2^e = hi + lo, the fp32 path at head
+// dims whose 3xTF32 tiles do not fit shared memory): the exponent always moves the
+// largest magnitude into [2^14, 2^15), so that the lo terms of the elements stay as far
+// above fp16's subnormal range as the tensor's range allows.
+__host__ __device__ inline int x16_exponent(uint32_t amax) {
+  if (amax == 0u) return 0;
+  const int fl = flog2_bits(amax);
+  if (fl >= 128) return 0;
+  return clamp_exp(COPY_TOP - fl);
+}
+// ... and dS: the bound's exponent U always moves to DS_TOP (see ds_exponent)
+__host__ __device__ inline int x16_ds_exponent(uint32_t amax_do, uint32_t amax_v,
+                                               uint32_t amax_delta, int dlog) {
+  if (amax_do == 0u || amax_v == 0u) return 0;
+  const int fg = flog2_bits(amax_do), fv = flog2_bits(amax_v);
+  const int fd = amax_delta == 0u ? -127 : flog2_bits(amax_delta);
+  if (fg >= 128 || fv >= 128 || fd >= 128) return 0;
+  int u = fg + fv + dlog + 2;
+  if (fd + 1 > u) u = fd + 1;
+  return clamp_exp(DS_TOP - (u + 1));
+}
+
 // Multipliers for the kernels, from the exponents of one call (written once per call
 // by the scale kernel, read by every CTA of the attention kernels).
 struct OperandScales {
@@ -144,6 +166,57 @@ __device__ __forceinline__ void reduce_partials(const uint32_t* part, int n_part
   __syncthreads();
 #pragma unroll
   for (int k = 0; k < N; ++k) m[k] = fin[k];
+}
+
+// Per-block largest |x| of up to 5 fp32 arrays (fp32 magnitudes order like their bits):
+// block b writes part[N b + k] for array k. Grid-stride over 4-element vectors.
+struct AmaxJobs {
+  const float* a[5];
+  size_t n4[5];  // 4-element vectors per array
+  int n;         // arrays
+};
+namespace {  // (each translation unit gets its own copy of the kernel)
+template <int N>
+__global__ void __launch_bounds__(256) amax_f32_kernel(const __grid_constant__ AmaxJobs js,
+                                                       uint32_t* __restrict__ part) {
+  uint32_t m[N];
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    m[k] = 0;
+    if (k >= js.n) continue;
+    const uint4* p = reinterpret_cast<const uint4*>(js.a[k]);
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < js.n4[k]; i += stride) {
+      const uint4 v = p[i];
+      m[k] = max(max(m[k], max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu)),
+                 max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu));
+    }
+  }
+  block_max_store<N>(m, part + (size_t)blockIdx.x * N);
+}
+}  // namespace
+
+// x 2^e = hi + lo, hi = fp16(x 2^e), lo = fp16(x 2^e - hi), for n4 vectors of 4 fp32
+// values; grid-stride.
+__device__ __forceinline__ void split_x16(const float* __restrict__ x, __half* __restrict__ hi,
+                                          __half* __restrict__ lo, size_t n4, int e) {
+  const float f = __uint_as_float((uint32_t)(127 + e) << 23);
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 v = reinterpret_cast<const float4*>(x)[i];
+    const float y[4] = {v.x * f, v.y * f, v.z * f, v.w * f};
+    uint32_t h[2], l[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const __half2 hh = __floats2half2_rn(y[2 * k], y[2 * k + 1]);
+      const float2 hf = __half22float2(hh);
+      const __half2 ll = __floats2half2_rn(y[2 * k] - hf.x, y[2 * k + 1] - hf.y);
+      h[k] = *reinterpret_cast<const uint32_t*>(&hh);
+      l[k] = *reinterpret_cast<const uint32_t*>(&ll);
+    }
+    reinterpret_cast<uint2*>(hi)[i] = make_uint2(h[0], h[1]);
+    reinterpret_cast<uint2*>(lo)[i] = make_uint2(l[0], l[1]);
+  }
 }
 
 // 2^e as a float, |e| <= EXP_LIMIT (exact: a normal power of two).

@@ -33,16 +33,17 @@
  * of at most 2^-23 (e = 0) or 2^-39 (e != 0) of the tensor's largest magnitude. So
  * bf16 inputs of any magnitude whose scores and outputs fit in fp32 are supported
  * (e.g. gradients dO of 1e-7, V of 1e5).
- * in_dtype FA_F32: every GEMM uses three tf32 tensor-core products (the
- * hi/lo split a = a_hi + a_lo; a_hi b_hi + a_hi b_lo + a_lo b_hi), giving close to
- * fp32 accuracy. Outputs are written in out_dtype (FA_F32 recommended; FA_BF16
+ * in_dtype FA_F32: every GEMM uses three tensor-core products of a hi/lo split of its
+ * operands, a = a_hi + a_lo, a_hi b_hi + a_hi b_lo + a_lo b_hi, giving close to fp32
+ * accuracy: tf32 terms for D <= 64; for D > 64, whose tf32 tiles would not fit shared
+ * memory, fp16 terms of x * 2^e (one power of two per tensor and call, chosen from its
+ * largest magnitude as for the bf16 path; about 22 significant bits, like the tf32 pair). Outputs are written in out_dtype (FA_F32 recommended; FA_BF16
  * rounds O / dQ / dK / dV to bf16 on store). LSE is always fp32, natural log.
  *
- * Supported in this build: head dims D that are multiples of 16, 16 <= D <= 128
- * for FA_BF16 inputs and 16 <= D <= 64 for FA_F32 inputs (the pages' set 16, 32, 48,
- * 64, 80, 96, 128 among them); other head dims return FA_ERR_UNSUPPORTED. A D below
- * 64 / 128 runs in the kernels built for 64 / 128, whose tensor-core work then
- * includes the zero columns up to that width.
+ * Supported in this build: head dims D that are multiples of 16, 16 <= D <= 128, for
+ * both input types (the pages' set 16, 32, 48, 64, 80, 96, 128 among them); other head
+ * dims return FA_ERR_UNSUPPORTED. A D below 64 / 128 runs in the kernels built for
+ * 64 / 128, whose tensor-core work then includes the zero columns up to that width.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -134,8 +135,9 @@ FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, fl
  *   - A problem whose scratch would not fit returns FA_ERR_SCRATCH_LIMIT before
  *     anything is enqueued: bf16 inputs need round_up(B*HKV*Sk*D*2, 256) + 256 +
  *     32 * (the device's SM count) bytes (the fp16 copy of V, its scale factors and
- *     the conversion's partial maxima); fp32 inputs need
- *     4*(2*B*H*Sq*D + 2*B*HKV*Sk*D + 2*B*HKV*D*round_up(Sk,4)) bytes.
+ *     the conversion's partial maxima); fp32 inputs with D <= 64 need
+ *     4*(2*B*H*Sq*D + 2*B*HKV*Sk*D + 2*B*HKV*D*round_up(Sk,4)) bytes, with D > 64
+ *     2*(2*B*H*Sq*D + 4*B*HKV*Sk*D) + 256 + 96 * (SM count) bytes.
  *   - The first call on each device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture begins.

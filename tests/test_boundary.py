@@ -100,8 +100,8 @@ MIS = 0x10008
     (dict(D=24), 2),                # head dim not a multiple of 16
     (dict(D=144), 2),               # above 128
     (dict(D=8), 2),
-    (dict(D=128, in_dtype=0), 2),   # fp32 inputs up to D=64
-    (dict(D=80, in_dtype=0), 2),
+    (dict(D=144, in_dtype=0), 2),   # fp32 inputs up to D=128 too
+    (dict(D=40, in_dtype=0), 2),
     # K and V of 2^59 bytes each: refused before any size is computed in size_t
     (dict(B=1024, H=1024, HKV=1024, Sq=1, Sk=1 << 30), 1),
 ])

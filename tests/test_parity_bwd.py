@@ -12,7 +12,7 @@ import torch
 import oracle
 from attention_fa_fwd_02_gb300.workloads import WORKLOADS, make_inputs
 from _parity import TOL, rms_err, to_np
-from test_parity_fwd import SMALL
+from test_parity_fwd import C2_D128, SMALL
 
 pytestmark = pytest.mark.gpu
 
@@ -93,9 +93,9 @@ def test_backward_bf16_outputs(fa, name):
         assert excess.max() <= 4e-2 * np.sqrt(np.mean(r ** 2))
 
 
-@pytest.mark.parametrize("cfg", ["c1", "c2", "c5"])
+@pytest.mark.parametrize("cfg", ["c1", "c2", "c5", "c2-d128"])
 def test_backward_full_config_fp32(fa, cfg):
-    w = WORKLOADS[cfg]
+    w = C2_D128 if cfg == "c2-d128" else WORKLOADS[cfg]
     q, k, v, do = make_inputs(w)
     got = _gpu_grads(fa, w, q, k, v, do)
     ref = oracle.attention_bwd(q, k, v, do, w.scale, w.causal, w.window)

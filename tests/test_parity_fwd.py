@@ -91,7 +91,24 @@ SMALL = {
                                         mag=(1, 1, 1e-6, 1e4)),
     "bf16-mag-decode": C3.with_(B=1, H=8, HKV=2, Sq=64, Sk=3000, causal=False, seed=76,
                                 mag=(1, 1, 3e4, 1e-6)),
+    # fp32 inputs at head dims above 64: two scaled fp16 terms per operand (3xTF32 tiles
+    # would not fit shared memory there); D = 80 / 96 run in the D = 128 kernels
+    "f32-d128-causal-ragged": C2.with_(B=1, H=2, HKV=2, Sq=300, Sk=300, D=128,
+                                       scale=128 ** -0.5, seed=81),
+    "f32-d128-gqa-window": C2.with_(B=1, H=4, HKV=2, Sq=450, Sk=450, D=128, window=100,
+                                    scale=128 ** -0.5, seed=82),
+    "f32-d96-noncausal-sq-ne-sk": C5.with_(Sq=257, Sk=390, D=96, scale=96 ** -0.5, seed=83),
+    "f32-d80-empty-rows": C2.with_(B=1, H=2, HKV=1, Sq=400, Sk=150, D=80, window=40,
+                                   scale=80 ** -0.5, seed=84),
+    "f32-d128-decode": C5.with_(Sq=100, Sk=3000, D=128, scale=128 ** -0.5, seed=85),
+    "f32-d128-many-items": C2.with_(B=1, H=64, HKV=16, Sq=300, Sk=300, D=128, scale=128 ** -0.5,
+                                    seed=86),
+    "f32-d128-mag": C2.with_(B=1, H=2, HKV=1, Sq=260, Sk=330, D=128, scale=128 ** -0.5, seed=87,
+                             mag=(2.0 ** -20, 3.0, 1e5, 1e-7)),
 }
+
+# fp32 inputs at D = 128 at the multi-head causal workload's full size (B4 H8 S1024)
+C2_D128 = C2.with_(D=128, scale=128 ** -0.5, name="causal-mha-b4-h8-s1024-d128-f32")
 
 
 @pytest.fixture(scope="module")
@@ -166,9 +183,9 @@ def test_forward_zero_keys(fa):
     assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
 
 
-@pytest.mark.parametrize("cfg", ["c1", "c2", "c5"])
+@pytest.mark.parametrize("cfg", ["c1", "c2", "c5", "c2-d128"])
 def test_forward_full_config_fp32(fa, cfg):
-    w = WORKLOADS[cfg]
+    w = C2_D128 if cfg == "c2-d128" else WORKLOADS[cfg]
     q, k, v, _ = make_inputs(w)
     o, lse = _run(fa, w, q, k, v)
     ro, rl = oracle.attention_fwd(q, k, v, w.scale, w.causal, w.window)

@@ -52,6 +52,10 @@ PAIRS = {
                                    seed=32)),
     "f32": (WORKLOADS["c2"].with_(B=1, H=2, HKV=2, Sq=500, Sk=500, seed=33),
             WORKLOADS["c5"].with_(Sq=300, Sk=450, seed=34)),
+    # fp32 at D = 128 (two scaled fp16 terms per operand)
+    "f32-d128": (WORKLOADS["c2"].with_(B=1, H=2, HKV=1, Sq=400, Sk=400, D=128, scale=128 ** -0.5,
+                                       seed=35),
+                 WORKLOADS["c5"].with_(Sq=200, Sk=350, D=96, scale=96 ** -0.5, seed=36)),
 }
 
 
