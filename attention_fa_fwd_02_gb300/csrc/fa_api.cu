@@ -24,7 +24,7 @@ int g_sms[MAX_DEVICES] = {};
 
 bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
                      uint64_t inner, uint64_t rows, uint64_t outer, uint64_t row_stride,
-                     uint32_t box_inner, uint32_t box_rows, bool swizzle) {
+                     uint32_t box_inner, uint32_t box_rows, int swizzle_bytes) {
   std::call_once(g_encode_once, [] {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -40,7 +40,9 @@ bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const 
   cuuint32_t estr[3] = {1, 1, 1};
   return g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                  : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                        : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

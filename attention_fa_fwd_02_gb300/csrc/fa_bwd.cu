@@ -120,13 +120,14 @@ struct BwdCfg {
   static constexpr uint32_t KV_ACC0 = 128 * KV_NSLOT;      // dV (dkdv)
   static constexpr uint32_t KV_ACC1 = 128 * KV_NSLOT + D;  // dK (dkdv)
   static constexpr uint32_t Q_ACC = 128 * Q_NSLOT;         // dQ (dq)
-  static_assert(KV_SMEM <= 227u * 1024u && Q_SMEM <= 227u * 1024u, "shared memory budget");
+  // (bf16 inputs use the Dkv16Cfg / Dq16Cfg kernels; these layouts are the fp32 kernels')
+  static_assert(!F32 || (KV_SMEM <= 227u * 1024u && Q_SMEM <= 227u * 1024u), "shared memory budget");
   static_assert((F32 ? 4 * CH : 2 * CH) <= 128, "TMEM slot width");
   static_assert(KV_ACC1 + D <= TMEM_COLS && Q_ACC + D <= TMEM_COLS, "TMEM budget");
   // Epilogues stage each warp's rows from the start of shared memory (every operand
   // buffer is spent by then): dV and dK side by side (dkdv), dQ (dq).
   static constexpr uint32_t EPI_WARP = epi_warp_bytes<D, false>();
-  static_assert(4 * 2 * EPI_WARP <= KV_VEC_OFF && 4 * EPI_WARP <= Q_RES + Q_NST * Q_STAGE,
+  static_assert(!F32 || (4 * 2 * EPI_WARP <= KV_VEC_OFF && 4 * EPI_WARP <= Q_RES + Q_NST * Q_STAGE),
                 "epilogue staging");
 };
 
@@ -765,8 +766,13 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
 // lanes 32*(w%4).., w < 4 taking keys [0, 64) of the chunk, w >= 4 keys [64, 128).
 template <int D>
 struct Dq16Cfg {
-  static constexpr int NCB = D / 64;                     // 128-byte column blocks per row
-  static constexpr uint32_t CB = 128u * 128u;            // column block of a 128-row tile
+  // smem rows of RB bytes with the swizzle of that width (64 bytes at D = 32)
+  static constexpr int RB = tile_row_bytes(D);
+  static constexpr uint32_t SWZ = RB == 128 ? SWZ_128B : SWZ_64B;
+  static constexpr uint32_t ATOM = 8u * RB;
+  static constexpr int ROW = RB / 2;                     // elements per row
+  static constexpr int NCB = D / ROW;                    // column blocks per row
+  static constexpr uint32_t CB = 128u * RB;              // column block of a 128-row tile
   static constexpr uint32_t TILE = NCB * CB;
   static constexpr int KST = 3, VST = 2;                 // K is held until dQ += dS K
   static constexpr uint32_t Q_OFF = 0, DO_OFF = TILE, K_OFF = 2 * TILE;
@@ -789,12 +795,13 @@ struct Dq16Cfg {
 
 template <int D>
 __device__ __forceinline__ void issue_rowdot128(uint32_t d, uint32_t a, uint32_t b) {
+  using L = Dq16Cfg<D>;  // (the tile layout of both backward kernels)
   constexpr uint32_t id = make_idesc(128, 128, FMT_F16, FMT_F16, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk * 16 / 64) * Dq16Cfg<D>::CB + (kk * 16 % 64) * 2;
-    mma_f16_ss(d, make_sdesc(a + off, 16, SW128_ATOM), make_sdesc(b + off, 16, SW128_ATOM), id,
-               kk > 0);
+    const uint32_t off = (kk * 16 / L::ROW) * L::CB + (kk * 16 % L::ROW) * 2;
+    mma_f16_ss(d, make_sdesc(a + off, 16, L::ATOM, L::SWZ), make_sdesc(b + off, 16, L::ATOM, L::SWZ),
+               id, kk > 0);
   }
 }
 
@@ -942,10 +949,10 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
       mbar_arrive_expect_tx(&bar_kfull[0], C::TILE);
       mbar_arrive_expect_tx(&bar_vfull[0], C::TILE);
       for (int cb = 0; cb < C::NCB; ++cb) {
-        tma_load_3d(smem + C::Q_OFF + cb * C::CB, &m.Q[0], &bar_q, cb * 64, it.i0, it.bh);
-        tma_load_3d(smem + C::DO_OFF + cb * C::CB, &m.dO[0], &bar_do, cb * 64, it.i0, it.bh);
-        tma_load_3d(smem + C::K_OFF + cb * C::CB, &m.Kc[0], &bar_kfull[0], cb * 64, k0, it.bg);
-        tma_load_3d(smem + C::V_OFF + cb * C::CB, &m.Vc[0], &bar_vfull[0], cb * 64, k0, it.bg);
+        tma_load_3d(smem + C::Q_OFF + cb * C::CB, &m.Q[0], &bar_q, cb * C::ROW, it.i0, it.bh);
+        tma_load_3d(smem + C::DO_OFF + cb * C::CB, &m.dO[0], &bar_do, cb * C::ROW, it.i0, it.bh);
+        tma_load_3d(smem + C::K_OFF + cb * C::CB, &m.Kc[0], &bar_kfull[0], cb * C::ROW, k0, it.bg);
+        tma_load_3d(smem + C::V_OFF + cb * C::CB, &m.Vc[0], &bar_vfull[0], cb * C::ROW, k0, it.bg);
       }
     }
   }
@@ -997,7 +1004,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         if (!wait(&bar_kempty[ks], ((g_ / KST) & 1) ^ 1)) return false;
         mbar_arrive_expect_tx(&bar_kfull[ks], C::TILE);
         for (int cb = 0; cb < C::NCB; ++cb)
-          tma_load_3d(gen(sK(ks)) + cb * C::CB, &m.Kc[0], &bar_kfull[ks], cb * 64, k0, bg);
+          tma_load_3d(gen(sK(ks)) + cb * C::CB, &m.Kc[0], &bar_kfull[ks], cb * C::ROW, k0, bg);
         last_k[ks] = g_ / KST;
         return true;
       };
@@ -1006,7 +1013,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         if (!wait(&bar_vempty[vs], ((g_ / VST) & 1) ^ 1)) return false;
         mbar_arrive_expect_tx(&bar_vfull[vs], C::TILE);
         for (int cb = 0; cb < C::NCB; ++cb)
-          tma_load_3d(gen(sV(vs)) + cb * C::CB, &m.Vc[0], &bar_vfull[vs], cb * 64, k0, bg);
+          tma_load_3d(gen(sV(vs)) + cb * C::CB, &m.Vc[0], &bar_vfull[vs], cb * C::ROW, k0, bg);
         last_v[vs] = g_ / VST;
         return true;
       };
@@ -1017,7 +1024,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(full, C::TILE);
         for (int cb = 0; cb < C::NCB; ++cb)
           tma_load_3d(gen(sbase + (is_q ? C::Q_OFF : C::DO_OFF)) + cb * C::CB, is_q ? &m.Q[0] : &m.dO[0],
-                      full, cb * 64, it.i0, it.bh);
+                      full, cb * C::ROW, it.i0, it.bh);
         last_qd = j;
         return true;
       };
@@ -1118,7 +1125,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BLOCK_N / 16; ++kk)
             mma_f16_ts(tmem + C::ACC, tmem + C::DS_COL + 64 * pb + kk * 8,
-                       make_sdesc(sK(ks) + kk * 16 * 128, C::CB, SW128_ATOM), id,
+                       make_sdesc(sK(ks) + kk * 16 * C::RB, C::CB, C::ATOM, C::SWZ), id,
                        (c > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&bar_kempty[ks]);
           tc_commit(&bar_accdone[pb]);
@@ -1228,7 +1235,9 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
       const bool any = r_base < a.Sq;
       auto epilogue = [&](auto out_bf16_tag) {
         constexpr bool BF = decltype(out_bf16_tag)::value;
-        constexpr bool ONE_HALF = BF && D == 64;  // a bf16 box is a whole 64-column row
+        // a bf16 box is a whole 64-column row, an fp32 one 32 columns: then the first half
+        // of the warps stores everything
+        constexpr bool ONE_HALF = (BF && D == 64) || (!BF && D == 32);
         constexpr int NCOL = ONE_HALF ? D : D / 2;
         const bool mine = !ONE_HALF || half == 0;
         const int x0 = ONE_HALF ? 0 : half * (D / 2);
@@ -1241,13 +1250,22 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         }
         tc_fence_before();
         mbar_arrive(&bar_dqfree);  // dQ has left TMEM: the next item may accumulate
+        // staging: the V ring, one warp's boxes after another
+        constexpr uint32_t STG = (uint32_t)(NCOL * (BF ? 2 : 4) / 128) * EPI_BOX_BYTES;
+        static_assert(8 * STG <= C::VST * C::TILE || (ONE_HALF && 4 * STG <= C::VST * C::TILE),
+                      "epilogue staging");
         if (mine)
-          stage_store_rows<NCOL, BF>(r, dq_mul, sbase + C::V_OFF + warp * (C::EPI_WARP / 2),
+          stage_store_rows<NCOL, BF>(r, dq_mul, sbase + C::V_OFF + warp * STG,
                                      &m.dQ, x0, r_base, any,
                                      SPLIT ? (w % a.n_splits) * a.BHx + it.bh : it.bh, a.Dv);
       };
-      if (a.out_bf16) epilogue(std::true_type{});
-      else epilogue(std::false_type{});
+      // (bf16 outputs only in the D >= 64 kernels: the host routes smaller head dims there)
+      if constexpr (D >= 64) {
+        if (a.out_bf16) epilogue(std::true_type{});
+        else epilogue(std::false_type{});
+      } else {
+        epilogue(std::false_type{});
+      }
       if (lane == 0) bulk_wait_read_all();
       __syncwarp();
       mbar_arrive(&bar_vfree);  // the staging area (the V ring) may be refilled
@@ -1288,15 +1306,19 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
 // lo into the half of its part's dP^T range that dS^T hi leaves free (two dK MMAs).
 template <int D>
 struct Dkv16Cfg {
-  static constexpr int NCB = D / 64;
-  static constexpr uint32_t CB = 128u * 128u;
+  static constexpr int RB = Dq16Cfg<D>::RB;             // (the same tile layout as dQ's)
+  static constexpr uint32_t SWZ = Dq16Cfg<D>::SWZ, ATOM = Dq16Cfg<D>::ATOM;
+  static constexpr int ROW = Dq16Cfg<D>::ROW;
+  static constexpr int NCB = D / ROW;
+  static constexpr uint32_t CB = 128u * RB;
+  static constexpr uint32_t PT_CB = 128u * 128u;        // column block of the P^T tile
   static constexpr uint32_t TILE = NCB * CB;            // 128 rows x D fp16
   static constexpr int NS = D == 128 ? 2 : 3;           // Q and dO ring depth
   static constexpr uint32_t K_OFF = 0, V_OFF = TILE, Q_OFF = 2 * TILE;
   static constexpr uint32_t DO_OFF = Q_OFF + NS * TILE;
   static constexpr uint32_t PT_OFF = DO_OFF + NS * TILE;  // P^T: 128 keys x 128 queries fp16
   static constexpr uint32_t VEC = 2 * 128 * 4;            // lse2 | delta of a chunk
-  static constexpr uint32_t VEC_OFF = PT_OFF + 2 * CB;
+  static constexpr uint32_t VEC_OFF = PT_OFF + 2 * PT_CB;
   static constexpr uint32_t LAYOUT = VEC_OFF + NS * VEC;  // bytes from the 1 KB-aligned base
   // NPART softmax warps share each TMEM lane quarter, each taking QC = 128 / NPART
   // of the chunk's queries: more warps per SM sub-partition hide more latency.
@@ -1333,24 +1355,26 @@ struct Dkv16Cfg {
 template <int D>
 __device__ __forceinline__ void issue_acc128(uint32_t acc, uint32_t a_tmem, uint32_t b,
                                              bool accumulate) {
+  using L = Dkv16Cfg<D>;
   constexpr uint32_t id = make_idesc(128, D, FMT_F16, FMT_F16, false, true);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    mma_f16_ts(acc, a_tmem + Dkv16Cfg<D>::op_col(kk),
-               make_sdesc(b + kk * 16 * 128, Dkv16Cfg<D>::CB, SW128_ATOM), id,
-               (accumulate || kk > 0) ? 1u : 0u);
+    mma_f16_ts(acc, a_tmem + L::op_col(kk), make_sdesc(b + kk * 16 * L::RB, L::CB, L::ATOM, L::SWZ),
+               id, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // ACC[128 x D] (+)= A[128 x 128] (K-major fp16 tile in smem) * B[128 x D] (MN-major).
 template <int D>
 __device__ __forceinline__ void issue_acc128_ss(uint32_t acc, uint32_t a, uint32_t b,
                                                 bool accumulate) {
+  using L = Dkv16Cfg<D>;
   constexpr uint32_t id = make_idesc(128, D, FMT_F16, FMT_F16, false, true);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t off = (kk * 16 / 64) * Dkv16Cfg<D>::CB + (kk * 16 % 64) * 2;
+    // A: the P^T tile (128-byte rows whatever D); B: the MN-major dO chunk
+    const uint32_t off = (kk * 16 / 64) * L::PT_CB + (kk * 16 % 64) * 2;
     mma_f16_ss(acc, make_sdesc(a + off, 16, SW128_ATOM),
-               make_sdesc(b + kk * 16 * 128, Dkv16Cfg<D>::CB, SW128_ATOM), id,
+               make_sdesc(b + kk * 16 * L::RB, L::CB, L::ATOM, L::SWZ), id,
                (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -1437,10 +1461,10 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
       mbar_arrive_expect_tx(&bar_dofull[0], C::TILE);
       mbar_arrive_expect_tx(&bar_qfull[0], C::TILE + C::VEC);
       for (int cb = 0; cb < C::NCB; ++cb) {
-        tma_load_3d(smem + C::K_OFF + cb * C::CB, &m.K[0], &bar_kv, cb * 64, j0, bg);
-        tma_load_3d(smem + C::V_OFF + cb * C::CB, &m.V[0], &bar_kv, cb * 64, j0, bg);
-        tma_load_3d(smem + C::DO_OFF + cb * C::CB, &m.dOc[0], &bar_dofull[0], cb * 64, i00, bh0);
-        tma_load_3d(smem + C::Q_OFF + cb * C::CB, &m.Qc[0], &bar_qfull[0], cb * 64, i00, bh0);
+        tma_load_3d(smem + C::K_OFF + cb * C::CB, &m.K[0], &bar_kv, cb * C::ROW, j0, bg);
+        tma_load_3d(smem + C::V_OFF + cb * C::CB, &m.V[0], &bar_kv, cb * C::ROW, j0, bg);
+        tma_load_3d(smem + C::DO_OFF + cb * C::CB, &m.dOc[0], &bar_dofull[0], cb * C::ROW, i00, bh0);
+        tma_load_3d(smem + C::Q_OFF + cb * C::CB, &m.Qc[0], &bar_qfull[0], cb * C::ROW, i00, bh0);
       }
       float* vec = reinterpret_cast<float*>(smem + C::VEC_OFF);
       tma_load_3d(vec, &m.L, &bar_qfull[0], i00, bh0, 0);
@@ -1482,12 +1506,12 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         if (!wait(&bar_doempty[st], ((c / NS) & 1) ^ 1)) break;
         mbar_arrive_expect_tx(&bar_dofull[st], C::TILE);
         for (int cb = 0; cb < C::NCB; ++cb)
-          tma_load_3d(gen(sdO(st)) + cb * C::CB, &m.dOc[0], &bar_dofull[st], cb * 64, i0, bh);
+          tma_load_3d(gen(sdO(st)) + cb * C::CB, &m.dOc[0], &bar_dofull[st], cb * C::ROW, i0, bh);
         last_do[st] = c / NS;
         if (!wait(&bar_qempty[st], ((c / NS) & 1) ^ 1)) break;
         mbar_arrive_expect_tx(&bar_qfull[st], C::TILE + C::VEC);
         for (int cb = 0; cb < C::NCB; ++cb)
-          tma_load_3d(gen(sQ(st)) + cb * C::CB, &m.Qc[0], &bar_qfull[st], cb * 64, i0, bh);
+          tma_load_3d(gen(sQ(st)) + cb * C::CB, &m.Qc[0], &bar_qfull[st], cb * C::ROW, i0, bh);
         float* vec = reinterpret_cast<float*>(smem + C::VEC_OFF + st * C::VEC);
         tma_load_3d(vec, &m.L, &bar_qfull[st], i0, bh, 0);
         tma_load_3d(vec + 128, &m.Dl, &bar_qfull[st], i0, bh, 0);
@@ -1573,7 +1597,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     // this thread's QC queries of row r_in of the swizzled P^T tile: column block
     // (QC p) / 64, 16-byte chunks from (QC p % 64) / 8
-    const uint32_t pt_row = sbase + C::PT_OFF + (QC * part / 64) * C::CB + r_in * 128;
+    const uint32_t pt_row = sbase + C::PT_OFF + (QC * part / 64) * C::PT_CB + r_in * 128;
     const uint32_t chunk0 = (uint32_t)((QC * part % 64) / 8);
     const uint32_t sw = (uint32_t)(r_in & 7);
     // scores and dP^T come from the scaled fp16 copies (see the dQ kernel)
@@ -1729,13 +1753,15 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
       const CUtensorMap* tm = which ? &m.dK : &m.dV;
       const float mul = which ? a.sc->dk_mul : a.sc->dv_mul;  // scale 2^-(eD+eQ) / 2^-eO
       const uint32_t stage = sbase + warp * (C::EPI_WARP / HP);
-      if (a.out_bf16) {
-        if constexpr (DW % 64 == 0)
-          store_rows_tma<DW, true, DW / 64>(tm, acc, nc > 0, mul, stage, r_base, any, bg, cpart * DW,
-                                            a.Dv);
-        else if (cpart == 0)  // a bf16 box is a 64-column row: one warp per output does it
-          store_rows_tma<D, true, D / 64>(tm, lane_addr + (which ? C::DK : C::DV), nc > 0, mul,
-                                          sbase + warp * C::EPI_WARP, r_base, any, bg, 0, a.Dv);
+      if (D >= 64 && a.out_bf16) {  // (bf16 outputs: D >= 64 kernels only)
+        if constexpr (D >= 64) {
+          if constexpr (DW % 64 == 0)
+            store_rows_tma<DW, true, DW / 64>(tm, acc, nc > 0, mul, stage, r_base, any, bg,
+                                              cpart * DW, a.Dv);
+          else if (cpart == 0)  // a bf16 box is a 64-column row: one warp per output does it
+            store_rows_tma<D, true, D / 64>(tm, lane_addr + (which ? C::DK : C::DV), nc > 0, mul,
+                                            sbase + warp * C::EPI_WARP, r_base, any, bg, 0, a.Dv);
+        }
       } else {
         store_rows_tma<DW, false, DW / 32>(tm, acc, nc > 0, mul, stage, r_base, any, bg, cpart * DW,
                                            a.Dv);
@@ -2321,7 +2347,7 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   QMaps mq;
   bool enc = true;
   const uint32_t qchunk = F32 ? C::CH : 128;  // query rows per dkdv chunk
-  enc &= host::encode_tiled_3d(&mk.L, F32T, 4, lse2, ldq, BH, 1, ldq, qchunk, 1, false);
+  enc &= host::encode_tiled_3d(&mk.L, F32T, 4, lse2, ldq, BH, 1, ldq, qchunk, 1, 0);
   {
     const bool bf = p.out_dtype == FA_BF16;
     const auto odt = bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : F32T;
@@ -2334,7 +2360,7 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     else
       enc &= host::encode_tiled_3d(&mq.dQ, odt, oes, dQ, Dv, p.Sq, BH, Dv, 128 / oes, 32);
   }
-  enc &= host::encode_tiled_3d(&mk.Dl, F32T, 4, delta, ldq, BH, 1, ldq, qchunk, 1, false);
+  enc &= host::encode_tiled_3d(&mk.Dl, F32T, 4, delta, ldq, BH, 1, ldq, qchunk, 1, 0);
   if constexpr (!F32) {
     __half* q16 = reinterpret_cast<__half*>(delta + nvec);
     __half* do16 = q16 + nq;
@@ -2398,14 +2424,16 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       }
     }
     const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    enc &= host::encode_tiled_3d(&mk.K[0], F16, 2, k16, Dv, p.Sk, BHk, Dv, 64, 128);
-    enc &= host::encode_tiled_3d(&mk.V[0], F16, 2, v16, Dv, p.Sk, BHk, Dv, 64, 128);
-    enc &= host::encode_tiled_3d(&mk.Qc[0], F16, 2, q16, Dv, p.Sq, BH, Dv, 64, 128);
-    enc &= host::encode_tiled_3d(&mk.dOc[0], F16, 2, do16, Dv, p.Sq, BH, Dv, 64, 128);
-    enc &= host::encode_tiled_3d(&mq.Q[0], F16, 2, q16, Dv, p.Sq, BH, Dv, 64, 128);
-    enc &= host::encode_tiled_3d(&mq.dO[0], F16, 2, do16, Dv, p.Sq, BH, Dv, 64, 128);
-    enc &= host::encode_tiled_3d(&mq.Kc[0], F16, 2, k16, Dv, p.Sk, BHk, Dv, 64, 128);
-    enc &= host::encode_tiled_3d(&mq.Vc[0], F16, 2, v16, Dv, p.Sk, BHk, Dv, 64, 128);
+    // boxes of one tile row block: 64 elements (128-byte swizzle), 32 at D = 32 (64-byte)
+    constexpr int ROWE = Dq16Cfg<D>::ROW, RBY = Dq16Cfg<D>::RB;
+    enc &= host::encode_tiled_3d(&mk.K[0], F16, 2, k16, Dv, p.Sk, BHk, Dv, ROWE, 128, RBY);
+    enc &= host::encode_tiled_3d(&mk.V[0], F16, 2, v16, Dv, p.Sk, BHk, Dv, ROWE, 128, RBY);
+    enc &= host::encode_tiled_3d(&mk.Qc[0], F16, 2, q16, Dv, p.Sq, BH, Dv, ROWE, 128, RBY);
+    enc &= host::encode_tiled_3d(&mk.dOc[0], F16, 2, do16, Dv, p.Sq, BH, Dv, ROWE, 128, RBY);
+    enc &= host::encode_tiled_3d(&mq.Q[0], F16, 2, q16, Dv, p.Sq, BH, Dv, ROWE, 128, RBY);
+    enc &= host::encode_tiled_3d(&mq.dO[0], F16, 2, do16, Dv, p.Sq, BH, Dv, ROWE, 128, RBY);
+    enc &= host::encode_tiled_3d(&mq.Kc[0], F16, 2, k16, Dv, p.Sk, BHk, Dv, ROWE, 128, RBY);
+    enc &= host::encode_tiled_3d(&mq.Vc[0], F16, 2, v16, Dv, p.Sk, BHk, Dv, ROWE, 128, RBY);
     mk.K[1] = mk.K[0]; mk.V[1] = mk.V[0]; mk.Qc[1] = mk.Qc[0]; mk.dOc[1] = mk.dOc[0];
     mk.Qt[0] = mk.Qt[1] = mk.Qc[0]; mk.dOt[0] = mk.dOt[1] = mk.dOc[0];
     mq.Q[1] = mq.Q[0]; mq.dO[1] = mq.dO[0]; mq.Kc[1] = mq.Kc[0]; mq.Vc[1] = mq.Vc[0];
@@ -2565,8 +2593,9 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       }
     } else {
       using C16 = Dkv16Cfg<D>;
-      auto kern = dsmat ? (split ? fa_bwd_dkdv16_kernel<D, true, true> : fa_bwd_dkdv16_kernel<D, false, true>)
-                        : (split ? fa_bwd_dkdv16_kernel<D, true, false> : fa_bwd_dkdv16_kernel<D, false, false>);
+      auto kern = split ? fa_bwd_dkdv16_kernel<D, true, false> : fa_bwd_dkdv16_kernel<D, false, false>;
+      if constexpr (D >= 64)  // (the materialised-dS route runs in the D >= 64 kernels)
+        if (dsmat) kern = split ? fa_bwd_dkdv16_kernel<D, true, true> : fa_bwd_dkdv16_kernel<D, false, true>;
       // all the dynamic shared memory a block may have: the layout fills it after
       // aligning its base to 1 KB (the kernel checks the fit)
       int dyn = 0;
@@ -2574,7 +2603,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
       if (e == cudaSuccess) {
-        host::KernelTimer kt(D == 128 ? "fa_bwd_dkdv_kernel<128,bf16>" : "fa_bwd_dkdv_kernel<64,bf16>",
+        host::KernelTimer kt(D == 128 ? "fa_bwd_dkdv_kernel<128,bf16>"
+                                      : (D == 64 ? "fa_bwd_dkdv_kernel<64,bf16>" : "fa_bwd_dkdv_kernel<32,bf16>"),
                              stream);
         kern<<<(unsigned)(BHk * ak.n_tiles), C16::THREADS, dyn, stream>>>(mk, ak);
         e = cudaGetLastError();
@@ -2597,9 +2627,10 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
         kern<<<(unsigned)(BH * aq.n_tiles), C::THREADS, C::Q_SMEM, stream>>>(mq, aq);
         e = cudaGetLastError();
       }
-    } else if (dsmat) {
+    } else if (D >= 64 && dsmat) {
       // dQ = scale dS K over the stored dS^T (an ordinary launch: it reads what the
       // dK / dV kernel wrote)
+      if constexpr (D >= 64) {
       DsMaps md;
       const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
       bool enc2 = host::encode_tiled_3d(&md.ds_hi, F16, 2, ds_hi, ldq, p.Sk, BH, ldq, 64, 128);
@@ -2627,12 +2658,14 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
                                                    p.causal, p.window, Dv, p.out_dtype == FA_BF16);
         e = cudaGetLastError();
       }
+      }
     } else {
       using C16 = Dq16Cfg<D>;
       auto kern = dq_splits > 1 ? fa_bwd_dq16_kernel<D, true> : fa_bwd_dq16_kernel<D, false>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C16::SMEM);
       if (e == cudaSuccess) {
-        host::KernelTimer kt(D == 128 ? "fa_bwd_dq_kernel<128,bf16>" : "fa_bwd_dq_kernel<64,bf16>",
+        host::KernelTimer kt(D == 128 ? "fa_bwd_dq_kernel<128,bf16>"
+                                      : (D == 64 ? "fa_bwd_dq_kernel<64,bf16>" : "fa_bwd_dq_kernel<32,bf16>"),
                              stream);
         // Persistent: one CTA per SM (at most), work items handed out dynamically.
         // Launched as a programmatic dependent of the dK / dV kernel (which does not
@@ -2691,6 +2724,9 @@ fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O,
   }
   // head dims below a kernel's D run in it with the missing columns read as zeros
   if (p.in_dtype == FA_BF16) {
+    // (the D = 32 kernels write fp32 outputs and recompute dS for dQ)
+    if (p.D <= 32 && p.out_dtype == FA_F32 && !dsmat)
+      return run_bwd<32, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, false);
     if (p.D <= 64) return run_bwd<64, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, dsmat);
     if (p.D <= 128) return run_bwd<128, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, dsmat);
   } else {

@@ -58,6 +58,11 @@ inline void combine_launch_shape(int BH, int Sq, int Dv, dim3* grid, dim3* block
   *grid = dim3((Sq + rpb - 1) / rpb, BH < 65535 ? BH : 65535);
 }
 
+// Operand tiles of 16-bit elements for head dim D: rows of min(2 D, 128) bytes, with
+// the swizzle of that width (D = 32: 64-byte rows, so that the tensor cores do not
+// work on padding columns).
+constexpr int tile_row_bytes(int D) { return 2 * D < 128 ? 2 * D : 128; }
+
 // Status bits a kernel may set in its device status word.
 enum : unsigned int {
   DEV_TIMEOUT = 1u,  // a barrier wait gave up
@@ -112,10 +117,10 @@ namespace host {
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 // A [outer][rows][inner] tensor whose rows are `row_stride` elements apart and whose
 // outer slabs are rows * row_stride elements apart; box {box_inner, box_rows, 1},
-// zero fill out of bounds; 128-byte swizzle unless `swizzle` is false.
+// zero fill out of bounds; `swizzle_bytes` 128 (the default), 64 or 0 (none).
 bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
                      uint64_t inner, uint64_t rows, uint64_t outer, uint64_t row_stride,
-                     uint32_t box_inner, uint32_t box_rows, bool swizzle = true);
+                     uint32_t box_inner, uint32_t box_rows, int swizzle_bytes = 128);
 
 // Stream-ordered scratch from a library-owned pool on the current device.
 cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);

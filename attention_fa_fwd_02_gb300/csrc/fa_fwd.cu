@@ -66,18 +66,25 @@ struct FwdCfg {
   static constexpr bool TF32 = F32 && !X16;
   static constexpr int NQ = F32 ? 1 : 2;                   // query tiles per CTA
   static constexpr int ESZ = TF32 ? 4 : 2;                 // operand bytes in smem
-  static constexpr int ROW_ELEMS = 128 / ESZ;              // elements per 128-byte row
-  static constexpr int NCB = D / ROW_ELEMS;                // 128-byte column blocks per row-tile
-  static constexpr uint32_t CB_BYTES = 128u * 128u;        // one column block of a 128-row tile
+  // smem rows of RB bytes with the swizzle of that width: 128, or 64 for bf16 at D = 32
+  static constexpr int RB = F32 ? 128 : tile_row_bytes(D);
+  static constexpr uint32_t SWZ = RB == 128 ? SWZ_128B : SWZ_64B;
+  static constexpr uint32_t ATOM = 8u * RB;                // 8-row swizzle atom
+  static constexpr int ROW_ELEMS = RB / ESZ;               // elements per row
+  static constexpr int NCB = D / ROW_ELEMS;                // column blocks per row-tile
+  static constexpr uint32_t CB_BYTES = 128u * RB;          // one column block of a 128-row tile
   static constexpr uint32_t TILE_BYTES = NCB * CB_BYTES;   // a 128 x D operand tile
   static constexpr uint32_t VT_CB_BYTES = D * 128u;        // fp32 V^T: 32 keys x D rows
   static constexpr int NSPLIT = F32 ? 2 : 1;               // hi / lo copies
   static constexpr int KST = F32 ? 1 : (D == 128 ? 2 : 3); // K ring depth
   static constexpr int VST = F32 ? 1 : 3;                  // V ring depth
+  // a V ring stage also stages an epilogue: at least one 32 x 128-byte box per warp
+  static constexpr uint32_t V_STAGE =
+      NSPLIT * TILE_BYTES > 4 * EPI_BOX_BYTES ? NSPLIT * TILE_BYTES : 4 * EPI_BOX_BYTES;
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t K_OFF = Q_OFF + NQ * NSPLIT * TILE_BYTES;
   static constexpr uint32_t V_OFF = K_OFF + KST * NSPLIT * TILE_BYTES;
-  static constexpr uint32_t SMEM_BYTES = V_OFF + VST * NSPLIT * TILE_BYTES;
+  static constexpr uint32_t SMEM_BYTES = V_OFF + VST * V_STAGE;
   static constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
   static constexpr int SOFTMAX_WARPS = 4 * NQ;
   // The last warpgroup holds the control warps: the MMA issuer (which also owns
@@ -103,7 +110,7 @@ struct FwdCfg {
   static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory budget");
   static_assert(F32 ? (256 + D <= 512) : (256 + 2 * D <= 512), "TMEM budget");
   // Epilogue: each softmax warp stages its 32 O rows in its quarter of a V ring stage.
-  static constexpr uint32_t STAGE_PER_WARP = NSPLIT * TILE_BYTES / 4;
+  static constexpr uint32_t STAGE_PER_WARP = V_STAGE / 4;
   static constexpr int STAGE_BOXES = (int)(STAGE_PER_WARP / EPI_BOX_BYTES);
   static_assert(STAGE_BOXES >= 1 && STAGE_PER_WARP % 1024 == 0, "O staging layout");
 };
@@ -115,9 +122,9 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t 
     constexpr uint32_t id = make_idesc(128, 128, FMT_BF16, FMT_BF16, false, false);
 #pragma unroll
     for (int kk = 0; kk < C::D / 16; ++kk) {
-      const uint32_t off = (kk * 16 / 64) * C::CB_BYTES + (kk * 16 % 64) * 2;
-      mma_f16_ss(d_tmem, make_sdesc(sq + off, 16, SW128_ATOM), make_sdesc(sk + off, 16, SW128_ATOM),
-                 id, kk > 0);
+      const uint32_t off = (kk * 16 / C::ROW_ELEMS) * C::CB_BYTES + (kk * 16 % C::ROW_ELEMS) * 2;
+      mma_f16_ss(d_tmem, make_sdesc(sq + off, 16, C::ATOM, C::SWZ),
+                 make_sdesc(sk + off, 16, C::ATOM, C::SWZ), id, kk > 0);
     }
   } else if constexpr (C::X16) {
     // (Qh + Ql)(Kh + Kl)^T without the lo * lo term, fp16 terms
@@ -158,13 +165,13 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
     constexpr uint32_t id = make_idesc(128, C::D, FMT_F16, FMT_F16, false, true);
 #pragma unroll
     for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-      mma_f16_ts(o_tmem, p_tmem + kk * 8, make_sdesc(sv + kk * 16 * 128, C::CB_BYTES, SW128_ATOM),
+      mma_f16_ts(o_tmem, p_tmem + kk * 8, make_sdesc(sv + kk * 16 * C::RB, C::CB_BYTES, C::ATOM, C::SWZ),
                  id, (accumulate || kk > 0) ? 1u : 0u);
     if constexpr (PSPLIT) {
 #pragma unroll
       for (int kk = 0; kk < BLOCK_N / 16; ++kk)
         mma_f16_ts(o_tmem, p_tmem + 64 + kk * 8,
-                   make_sdesc(sv + kk * 16 * 128, C::CB_BYTES, SW128_ATOM), id, 1u);
+                   make_sdesc(sv + kk * 16 * C::RB, C::CB_BYTES, C::ATOM, C::SWZ), id, 1u);
     }
   } else if constexpr (C::X16) {
     // (Ph + Pl)(Vh + Vl) without the lo * lo term: P hi / lo in the S slot's two column
@@ -212,7 +219,7 @@ __device__ __forceinline__ void issue_v_load(uint8_t* smem, int it, int t, int b
   const int vs = it % C::VST;
   mbar_arrive_expect_tx(&bar_vfull[vs], C::NSPLIT * C::TILE_BYTES);
   for (int sp = 0; sp < C::NSPLIT; ++sp) {
-    uint8_t* dst = smem + C::V_OFF + (vs * C::NSPLIT + sp) * C::TILE_BYTES;
+    uint8_t* dst = smem + C::V_OFF + vs * C::V_STAGE + sp * C::TILE_BYTES;
     if constexpr (!C::TF32) {
       for (int cb = 0; cb < C::NCB; ++cb)
         tma_load_3d(dst + cb * C::CB_BYTES, sp ? tmVlo : tmV, &bar_vfull[vs], cb * C::ROW_ELEMS,
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
   const uint32_t sbase = smem_u32(smem);
   auto sQ = [&](int q, int sp) { return sbase + C::Q_OFF + (q * C::NSPLIT + sp) * C::TILE_BYTES; };
   auto sK = [&](int st, int sp) { return sbase + C::K_OFF + (st * C::NSPLIT + sp) * C::TILE_BYTES; };
-  auto sV = [&](int st, int sp) { return sbase + C::V_OFF + (st * C::NSPLIT + sp) * C::TILE_BYTES; };
+  auto sV = [&](int st, int sp) { return sbase + C::V_OFF + st * C::V_STAGE + sp * C::TILE_BYTES; };
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait(bar, parity, abort_flag, &g_fwd_status, DEV_TIMEOUT, a.limit_ns);
   };
@@ -731,11 +738,14 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         a.LSE[(size_t)zo * a.Sq + i] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
       const int r_base = r0 + wq * 32;
       const uint32_t stage = sV(slot, 0) + wq * C::STAGE_PER_WARP;
+      // (bf16 outputs: 64-column boxes, so D >= 64 kernels only; the host routes
+      // bf16 outputs at smaller head dims to the D = 64 kernels)
+      constexpr bool BF_OUT = D >= 64;
       if (q < NQ - 1) {
         if (ok) {
-          if (a.out_bf16)
-            store_rows_tma<D, true, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                     r_base < a.Sq, zo, 0, a.Dv);
+          if (BF_OUT && a.out_bf16)
+            store_rows_tma<D, BF_OUT, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
+                                                       r_base < a.Sq, zo, 0, a.Dv);
           else
             store_rows_tma<D, false, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
                                                       r_base < a.Sq, zo, 0, a.Dv);
@@ -744,9 +754,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
         if (wq == 0 && lane == 0) mbar_arrive(&bar_grant[q + 1]);
       } else {
         if (ok) {
-          if (a.out_bf16)
-            store_rows_tma<D, true, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                            r_base < a.Sq, zo, 0, a.Dv);
+          if (BF_OUT && a.out_bf16)
+            store_rows_tma<D, BF_OUT, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage, r_base,
+                                                              r_base < a.Sq, zo, 0, a.Dv);
           else
             store_rows_tma<D, false, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage,
                                                              r_base, r_base < a.Sq, zo, 0, a.Dv);
@@ -1025,9 +1035,12 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
         return FA_ERR_CUDA;
       }
     }
-    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, Dv, p.Sq, BHq, Dv, 64, 128);
-    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, Dv, p.Sk, BHk, Dv, 64, 128);
-    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, Dv, p.Sk, BHk, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, Dv, p.Sq, BHq, Dv,
+                                 C::ROW_ELEMS, 128, C::RB);
+    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, Dv, p.Sk, BHk, Dv,
+                                 C::ROW_ELEMS, 128, C::RB);
+    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, Dv, p.Sk, BHk, Dv,
+                                 C::ROW_ELEMS, 128, C::RB);
     mQlo = mQ; mKlo = mK; mVlo = mV;
   } else if constexpr (C::X16) {
     const int n_amax = 8 * host::sm_count();
@@ -1118,7 +1131,8 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
                                        (int)C::SMEM_ALLOC);
   if (e == cudaSuccess) {
     host::KernelTimer kt(F32 ? (D == 128 ? "fa_fwd_kernel<128,f32>" : "fa_fwd_kernel<64,f32>")
-                             : (D == 128 ? "fa_fwd_kernel<128,bf16>" : "fa_fwd_kernel<64,bf16>"),
+                             : (D == 128 ? "fa_fwd_kernel<128,bf16>"
+                                         : (D == 64 ? "fa_fwd_kernel<64,bf16>" : "fa_fwd_kernel<32,bf16>")),
                          stream);
     kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, mO, a);
     e = cudaGetLastError();
@@ -1150,6 +1164,8 @@ fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float
   }
   // head dims below a kernel's D run in it with the missing columns read as zeros
   if (p.in_dtype == FA_BF16) {
+    // (the D = 32 kernel writes fp32 outputs only)
+    if (p.D <= 32 && p.out_dtype == FA_F32) return run_fwd<32, false>(Q, K, V, O, LSE, p, stream);
     if (p.D <= 64) return run_fwd<64, false>(Q, K, V, O, LSE, p, stream);
     if (p.D <= 128) return run_fwd<128, false>(Q, K, V, O, LSE, p, stream);
   } else {
@@ -1303,9 +1319,12 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
                             (const uint32_t*)part, n_cvt, static_cast<const __nv_bfloat16*>(V),
                             static_cast<__half*>(ws), nk / 8, sc) != cudaSuccess)
       return FA_ERR_CUDA;
-    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, Dv, p.Sq, BHq, Dv, 64, 128);
-    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, Dv, p.Sk, BHk, Dv, 64, 128);
-    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, Dv, p.Sk, BHk, Dv, 64, 128);
+    enc &= host::encode_tiled_3d(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, Dv, p.Sq, BHq, Dv,
+                                 C::ROW_ELEMS, 128, C::RB);
+    enc &= host::encode_tiled_3d(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, Dv, p.Sk, BHk, Dv,
+                                 C::ROW_ELEMS, 128, C::RB);
+    enc &= host::encode_tiled_3d(&mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws, Dv, p.Sk, BHk, Dv,
+                                 C::ROW_ELEMS, 128, C::RB);
     mQlo = mQ; mKlo = mK; mVlo = mV;
   } else if constexpr (C::X16) {
     enc &= prep_x16_fwd(ws, Q, K, V, p, n_cvt, stream, &mQ, &mQlo, &mK, &mKlo, &mV, &mVlo, &sc);

@@ -240,17 +240,21 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t M, uint32_t N, uint32
          ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
-// Shared-memory matrix descriptor (64 bit), 128-byte swizzle:
+// Shared-memory matrix descriptor (64 bit):
 //   [0,14) start address >> 4; [16,30) leading byte offset >> 4;
 //   [32,46) stride byte offset >> 4; [46,48) = 1 (descriptor version);
-//   [49,52) base offset (0: atoms are 1024-byte aligned); [61,64) = 2 (128B swizzle).
-// K-major operand: rows of 128 bytes, 8-row atoms at `sbo` = 1024; lbo unused (16).
-// MN-major operand: 128-byte rows run along M/N; `lbo` = byte distance between
-// 64-element (16-bit) / 32-element (32-bit) column blocks, `sbo` = 1024 between
-// groups of 8 rows along K.
-__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+//   [49,52) base offset (0: atoms are aligned to their size); [61,64) swizzle mode
+//   (2 = 128-byte, 4 = 64-byte).
+// 128-byte swizzle (the default): K-major operand: rows of 128 bytes, 8-row atoms at
+// `sbo` = 1024; lbo unused (16). MN-major operand: 128-byte rows run along M/N; `lbo`
+// = byte distance between 64-element (16-bit) / 32-element (32-bit) column blocks,
+// `sbo` = 1024 between groups of 8 rows along K. 64-byte swizzle: the same with rows
+// of 64 bytes and 512-byte atoms (`sbo` = 512).
+enum : uint32_t { SWZ_128B = 2, SWZ_64B = 4 };
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                               uint32_t swz = SWZ_128B) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swz << 61);
 }
 
 // ---- TMEM <-> registers. Warp w may touch lanes [32*(w%4), 32*(w%4)+32).

@@ -12,7 +12,7 @@ import torch
 import oracle
 from attention_fa_fwd_02_gb300.workloads import WORKLOADS, make_inputs
 from _parity import TOL, rms_err, to_np
-from test_parity_fwd import C2_D128, SMALL
+from test_parity_fwd import C2_D128, C3_D32, SMALL
 
 pytestmark = pytest.mark.gpu
 
@@ -75,7 +75,8 @@ def test_backward_unseen_keys_get_zero_grad(fa):
     assert torch.all(dk[:, :, w.Sq:] == 0) and torch.all(dv[:, :, w.Sq:] == 0)
 
 
-@pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa"])
+@pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa",
+                                  "bf16-d32-causal-gqa-ragged"])
 def test_backward_bf16_outputs(fa, name):
     # bf16 outputs: each gradient element is rounded on store (2^-9 relative, the
     # 2^-8 |r| term), and the forward's bf16-rounded O enters D_i = rowsum(dO * O),
@@ -102,11 +103,12 @@ def test_backward_full_config_fp32(fa, cfg):
     _check(w, got, ref, cfg)
 
 
-@pytest.mark.parametrize("cfg,b,g", [("c3", 1, 5), ("c3", 0, 0), ("c4", 0, 3), ("c4", 0, 0)])
+@pytest.mark.parametrize("cfg,b,g", [("c3", 1, 5), ("c3", 0, 0), ("c4", 0, 3), ("c4", 0, 0),
+                                     ("c3-d32", 1, 2)])
 def test_backward_full_config_bf16_slice(fa, cfg, b, g):
     # Full-size launch; whole (batch, kv-group) slices are independent, so the
     # oracle checks one slice exactly (dK / dV of the group sum its query heads).
-    w = WORKLOADS[cfg]
+    w = C3_D32 if cfg == "c3-d32" else WORKLOADS[cfg]
     q, k, v, do = make_inputs(w)
     dq, dk, dv = _gpu_grads(fa, w, q, k, v, do)
     rep = w.H // w.HKV

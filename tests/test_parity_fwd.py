@@ -91,6 +91,15 @@ SMALL = {
                                         mag=(1, 1, 1e-6, 1e4)),
     "bf16-mag-decode": C3.with_(B=1, H=8, HKV=2, Sq=64, Sk=3000, causal=False, seed=76,
                                 mag=(1, 1, 3e4, 1e-6)),
+    # bf16 at D <= 32 runs in kernels built for D = 32 (64-byte rows and swizzle)
+    "bf16-d32-causal-gqa-ragged": C3.with_(B=1, H=4, HKV=2, Sq=333, Sk=333, D=32,
+                                           scale=32 ** -0.5, seed=91),
+    "bf16-d32-window-sq-ne-sk": C4.with_(B=1, H=4, HKV=1, Sq=500, Sk=700, D=32, window=150,
+                                         scale=32 ** -0.5, seed=92),
+    "bf16-d32-decode": C4.with_(H=8, HKV=2, Sq=100, Sk=5000, D=32, causal=False, window=0,
+                                scale=32 ** -0.5, seed=93),
+    "bf16-d16-gqa3-noncausal": C3.with_(B=1, H=6, HKV=2, Sq=260, Sk=300, D=16, causal=False,
+                                        scale=0.25, seed=94),
     # fp32 inputs at head dims above 64: two scaled fp16 terms per operand (3xTF32 tiles
     # would not fit shared memory there); D = 80 / 96 run in the D = 128 kernels
     "f32-d128-causal-ragged": C2.with_(B=1, H=2, HKV=2, Sq=300, Sk=300, D=128,
@@ -109,6 +118,8 @@ SMALL = {
 
 # fp32 inputs at D = 128 at the multi-head causal workload's full size (B4 H8 S1024)
 C2_D128 = C2.with_(D=128, scale=128 ** -0.5, name="causal-mha-b4-h8-s1024-d128-f32")
+# bf16 at D = 32 at the GQA causal workload's full size (B2 H32/8 S4096)
+C3_D32 = C3.with_(D=32, scale=32 ** -0.5, name="causal-gqa-b2-h32-hkv8-s4096-d32-bf16")
 
 
 @pytest.fixture(scope="module")
@@ -157,7 +168,8 @@ def test_forward_deterministic(fa, name):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-@pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa"])
+@pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa",
+                                  "bf16-d32-causal-gqa-ragged"])
 def test_forward_bf16_output(fa, name):
     # bf16 outputs: rounding O to bf16 moves each element by at most half an ulp,
     # 2^-9 |O| (round to nearest, 8 significant bits). Allow that per element on top
@@ -192,11 +204,12 @@ def test_forward_full_config_fp32(fa, cfg):
     _check(w, o, lse, ro, rl, cfg)
 
 
-@pytest.mark.parametrize("cfg,b,g", [("c3", 1, 5), ("c3", 0, 0), ("c4", 0, 3), ("c4", 0, 0)])
+@pytest.mark.parametrize("cfg,b,g", [("c3", 1, 5), ("c3", 0, 0), ("c4", 0, 3), ("c4", 0, 0),
+                                     ("c3-d32", 1, 2)])
 def test_forward_full_config_bf16_slice(fa, cfg, b, g):
     # Full-size launch (the benchmark's configuration); the oracle checks whole
     # (batch, kv-group) slices, which are independent of the rest.
-    w = WORKLOADS[cfg]
+    w = C3_D32 if cfg == "c3-d32" else WORKLOADS[cfg]
     q, k, v, _ = make_inputs(w)
     o, lse = _run(fa, w, q, k, v)
     rep = w.H // w.HKV
