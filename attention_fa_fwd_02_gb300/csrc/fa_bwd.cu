@@ -24,6 +24,7 @@
 #include <cfloat>
 #include <climits>
 #include <algorithm>
+#include <vector>
 #include <type_traits>
 #include "fa_common.cuh"
 #include "ptx.cuh"
@@ -1406,7 +1407,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_kv, bar_qfull[NS], bar_qempty[NS], bar_dofull[NS],
+  __shared__ __align__(8) uint64_t bar_kv, bar_kvfree, bar_qfull[NS], bar_qempty[NS], bar_dofull[NS],
       bar_doempty[NS], bar_s, bar_sfree, bar_p, bar_dvdone, bar_dp, bar_ds, bar_done, bar_drain[3];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -1422,19 +1423,41 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
   }
   const int warp = warp_id(), lane = lane_id();
   volatile int* abort_flag = &abort_sh;
-
-  const int jt = blockIdx.x / a.BHx;
-  const int bg = blockIdx.x % a.BHx;
-  const int b = bg / a.HKV, g = bg % a.HKV;
   const int rep = a.H / a.HKV;
-  const int j0 = jt * BLOCK_N;
-  int qt_lo, qt_hi;
-  q_tile_range(j0, min(j0 + BLOCK_N - 1, a.Sk - 1), a.Sq, a.causal, a.window, &qt_lo, &qt_hi);
-  const int ncq = qt_hi - qt_lo;
-  const int nc = rep * ncq;
+
+  // ---- work items: key tile jt of (batch, kv head) bg, w = jt * BHx + bg, so key
+  // tile 0 -- which, under a causal mask, the most queries see -- comes first. Each
+  // CTA walks items in rounds of gridDim.x, item c of even rounds and G - 1 - c of odd
+  // ones (one round when the grid has a CTA per item). (A host-side longest-first
+  // assignment to the least loaded CTA measured 1-3% slower than these rounds.)
+  const int n_items = a.n_tiles * a.BHx;
+  struct Item { int bg, b, g, j0, qt_lo, ncq, nc; };
+  auto item = [&](int w) {
+    Item it;
+    const int jt = w / a.BHx;
+    it.bg = w % a.BHx;
+    it.b = it.bg / a.HKV;
+    it.g = it.bg % a.HKV;
+    it.j0 = jt * BLOCK_N;
+    int qt_hi;
+    q_tile_range(it.j0, min(it.j0 + BLOCK_N - 1, a.Sk - 1), a.Sq, a.causal, a.window, &it.qt_lo, &qt_hi);
+    it.ncq = qt_hi - it.qt_lo;
+    it.nc = rep * it.ncq;
+    return it;
+  };
+  auto item_w = [&](int k) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return k * G + ((k & 1) ? G - 1 - c : c);
+  };
+  auto chunk_rows = [&](const Item& it, int c, int* bh, int* i0) {
+    const int r = c / it.ncq, qt = it.qt_lo + c % it.ncq;
+    *bh = it.b * a.H + it.g * rep + r;
+    *i0 = qt * BLOCK_M;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_kv, 1);
+    mbar_init(&bar_kvfree, 2);  // the S and the B issuer: an item's last S^T / dP^T read K / V
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bar_qfull[s], 1);
       mbar_init(&bar_qempty[s], 2);   // S^T(c) (A) and dK(c) (B) have read Q_c
@@ -1449,27 +1472,10 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     mbar_init(&bar_dvdone, 1);
     mbar_init(&bar_dp, 1);
     mbar_init(&bar_ds, C::SM_ARRIVALS);
-    mbar_init(&bar_done, 2);  // dV issuer and B issuer
+    mbar_init(&bar_done, 2);  // dV issuer and B issuer, one phase per item with chunks
     for (int s = 0; s < 3; ++s) mbar_init(&bar_drain[s], 1);
     abort_sh = 0;
     fence_mbar_init();
-    if (nc > 0) {
-      // The resident K / V tiles and the first (Q, dO) chunk are issued here, before
-      // the TMEM allocation and the CTA-wide sync, so their latency overlaps the setup.
-      const int bh0 = b * a.H + g * rep, i00 = qt_lo * BLOCK_M;  // chunk 0
-      mbar_arrive_expect_tx(&bar_kv, 2 * C::TILE);
-      mbar_arrive_expect_tx(&bar_dofull[0], C::TILE);
-      mbar_arrive_expect_tx(&bar_qfull[0], C::TILE + C::VEC);
-      for (int cb = 0; cb < C::NCB; ++cb) {
-        tma_load_3d(smem + C::K_OFF + cb * C::CB, &m.K[0], &bar_kv, cb * C::ROW, j0, bg);
-        tma_load_3d(smem + C::V_OFF + cb * C::CB, &m.V[0], &bar_kv, cb * C::ROW, j0, bg);
-        tma_load_3d(smem + C::DO_OFF + cb * C::CB, &m.dOc[0], &bar_dofull[0], cb * C::ROW, i00, bh0);
-        tma_load_3d(smem + C::Q_OFF + cb * C::CB, &m.Qc[0], &bar_qfull[0], cb * C::ROW, i00, bh0);
-      }
-      float* vec = reinterpret_cast<float*>(smem + C::VEC_OFF);
-      tma_load_3d(vec, &m.L, &bar_qfull[0], i00, bh0, 0);
-      tma_load_3d(vec + 128, &m.Dl, &bar_qfull[0], i00, bh0, 0);
-    }
   }
   if (warp == C::A_WARP) {
     __syncwarp();
@@ -1487,37 +1493,56 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
   };
-  auto chunk_rows = [&](int c, int* bh, int* i0) {
-    const int r = c / ncq, qt = qt_lo + c % ncq;
-    *bh = b * a.H + g * rep + r;
-    *i0 = qt * BLOCK_M;
-  };
+  // Chunk barriers count chunks across items (g); bar_kv, bar_kvfree and bar_done
+  // count items with chunks (j). Every phase of a per-item barrier needs the previous
+  // one observed first (K / V of item j load after kv_free(j - 1), whose commits follow
+  // waits on bar_kv(j - 1); done(j) needs this item's P^T / dS^T, written after the
+  // epilogue waited on done(j - 1)), so no parity wait can miss a phase. The first dV
+  // and dK MMAs of an item overwrite the accumulators only after the softmax wrote that
+  // item's first P^T / dS^T, i.e. after its epilogue read the previous item's out of
+  // TMEM.
 
   if (warp >= C::SOFTMAX_WARPS) {
   regs_decrease<C::REGS_CONTROL>();
   if (warp == C::TMA_WARP) {
-    if (lane == 0 && nc > 0) {
-      int last_q[NS], last_do[NS];  // chunk 0 was issued with the resident tiles
-      for (int s = 0; s < NS; ++s) last_q[s] = last_do[s] = s == 0 ? 0 : -1;
-      for (int c = 1; c < nc; ++c) {
-        const int st = c % NS;
-        int bh, i0;
-        chunk_rows(c, &bh, &i0);
-        if (!wait(&bar_doempty[st], ((c / NS) & 1) ^ 1)) break;
-        mbar_arrive_expect_tx(&bar_dofull[st], C::TILE);
-        for (int cb = 0; cb < C::NCB; ++cb)
-          tma_load_3d(gen(sdO(st)) + cb * C::CB, &m.dOc[0], &bar_dofull[st], cb * C::ROW, i0, bh);
-        last_do[st] = c / NS;
-        if (!wait(&bar_qempty[st], ((c / NS) & 1) ^ 1)) break;
-        mbar_arrive_expect_tx(&bar_qfull[st], C::TILE + C::VEC);
-        for (int cb = 0; cb < C::NCB; ++cb)
-          tma_load_3d(gen(sQ(st)) + cb * C::CB, &m.Qc[0], &bar_qfull[st], cb * C::ROW, i0, bh);
-        float* vec = reinterpret_cast<float*>(smem + C::VEC_OFF + st * C::VEC);
-        tma_load_3d(vec, &m.L, &bar_qfull[st], i0, bh, 0);
-        tma_load_3d(vec + 128, &m.Dl, &bar_qfull[st], i0, bh, 0);
-        last_q[st] = c / NS;
+    if (lane == 0) {
+      int last_q[NS], last_do[NS], last_kv = -1;
+      for (int s = 0; s < NS; ++s) last_q[s] = last_do[s] = -1;
+      bool ok = true;
+      int g = 0, j = 0;
+      for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
+        const Item it = item(w);
+        if (it.nc == 0) continue;
+        // K / V of this item once the previous item's last S^T and dP^T have read them
+        if (j > 0 && !(ok = wait(&bar_kvfree, (j - 1) & 1))) break;
+        mbar_arrive_expect_tx(&bar_kv, 2 * C::TILE);
+        for (int cb = 0; cb < C::NCB; ++cb) {
+          tma_load_3d(smem + C::K_OFF + cb * C::CB, &m.K[0], &bar_kv, cb * C::ROW, it.j0, it.bg);
+          tma_load_3d(smem + C::V_OFF + cb * C::CB, &m.V[0], &bar_kv, cb * C::ROW, it.j0, it.bg);
+        }
+        last_kv = j;
+        for (int c = 0; c < it.nc; ++c, ++g) {
+          const int st = g % NS;
+          int bh, i0;
+          chunk_rows(it, c, &bh, &i0);
+          if (!(ok = wait(&bar_doempty[st], ((g / NS) & 1) ^ 1))) break;
+          mbar_arrive_expect_tx(&bar_dofull[st], C::TILE);
+          for (int cb = 0; cb < C::NCB; ++cb)
+            tma_load_3d(gen(sdO(st)) + cb * C::CB, &m.dOc[0], &bar_dofull[st], cb * C::ROW, i0, bh);
+          last_do[st] = g / NS;
+          if (!(ok = wait(&bar_qempty[st], ((g / NS) & 1) ^ 1))) break;
+          mbar_arrive_expect_tx(&bar_qfull[st], C::TILE + C::VEC);
+          for (int cb = 0; cb < C::NCB; ++cb)
+            tma_load_3d(gen(sQ(st)) + cb * C::CB, &m.Qc[0], &bar_qfull[st], cb * C::ROW, i0, bh);
+          float* vec = reinterpret_cast<float*>(smem + C::VEC_OFF + st * C::VEC);
+          tma_load_3d(vec, &m.L, &bar_qfull[st], i0, bh, 0);
+          tma_load_3d(vec + 128, &m.Dl, &bar_qfull[st], i0, bh, 0);
+          last_q[st] = g / NS;
+        }
+        ++j;
       }
-      drain_wait(&bar_kv, 0, a.limit_ns);
+      // Drain: every issued copy must land before the CTA may exit.
+      if (last_kv >= 0) drain_wait(&bar_kv, last_kv & 1, a.limit_ns);
       for (int s = 0; s < NS; ++s) {
         if (last_q[s] >= 0) drain_wait(&bar_qfull[s], last_q[s] & 1, a.limit_ns);
         if (last_do[s] >= 0) drain_wait(&bar_dofull[s], last_do[s] & 1, a.limit_ns);
@@ -1525,16 +1550,24 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     }
   } else if (warp == C::A_WARP) {
     // S issuer: S^T(c) once Q_c is in and the softmax has loaded S^T(c-1).
-    if (lane == 0 && nc > 0) {
-      bool ok = wait(&bar_kv, 0);
-      for (int c = 0; ok && c < nc; ++c) {
-        const int st = c % NS;
-        if (!(ok = wait(&bar_qfull[st], (c / NS) & 1))) break;
-        if (c > 0 && !(ok = wait(&bar_sfree, (c - 1) & 1))) break;
-        tc_fence_after();
-        issue_rowdot128<D>(tmem + C::S_COL, sbase + C::K_OFF, sQ(st));
-        tc_commit(&bar_s);
-        tc_commit(&bar_qempty[st]);
+    if (lane == 0) {
+      bool ok = true;
+      int g = 0, j = 0;
+      for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
+        const Item it = item(w);
+        if (it.nc == 0) continue;
+        if (!(ok = wait(&bar_kv, j & 1))) break;
+        for (int c = 0; c < it.nc; ++c, ++g) {
+          const int st = g % NS;
+          if (!(ok = wait(&bar_qfull[st], (g / NS) & 1))) break;
+          if (g > 0 && !(ok = wait(&bar_sfree, (g - 1) & 1))) break;
+          tc_fence_after();
+          issue_rowdot128<D>(tmem + C::S_COL, sbase + C::K_OFF, sQ(st));
+          tc_commit(&bar_s);
+          tc_commit(&bar_qempty[st]);
+        }
+        tc_commit(&bar_kvfree);  // this item's S^T MMAs are done with K
+        ++j;
       }
       tc_commit(&bar_drain[0]);
       drain_wait(&bar_drain[0], 0, a.limit_ns);
@@ -1543,46 +1576,59 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     // dV issuer: dV += P^T(c) dO_c once the softmax has written P^T(c); the softmax
     // observed dO_c land before that (an mbarrier wait here, right after this warp's
     // previous MMAs, would wait for them to drain: +4% kernel time).
-    if (lane == 0 && nc > 0) {
+    if (lane == 0) {
       bool ok = true;
-      for (int c = 0; ok && c < nc; ++c) {
-        const int st = c % NS;
-        if (!(ok = wait(&bar_p, c & 1))) break;
-        tc_fence_after();
-        if constexpr (SPLIT) {
-          // P^T hi and lo from the S^T slot, which S^T(c + 1) may take once both are read
-          issue_acc128<D>(tmem + C::DV, tmem + C::S_COL, sdO(st), c > 0);
-          issue_acc128<D>(tmem + C::DV, tmem + C::S_COL + C::QC / 2, sdO(st), true);
-          tc_commit(&bar_doempty[st]);
-          tc_commit(&bar_sfree);
-        } else {
-          issue_acc128_ss<D>(tmem + C::DV, sbase + C::PT_OFF, sdO(st), c > 0);
-          tc_commit(&bar_doempty[st]);
-          tc_commit(&bar_dvdone);
+      int g = 0;
+      for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
+        const Item it = item(w);
+        if (it.nc == 0) continue;
+        for (int c = 0; c < it.nc; ++c, ++g) {
+          const int st = g % NS;
+          if (!(ok = wait(&bar_p, g & 1))) break;
+          tc_fence_after();
+          if constexpr (SPLIT) {
+            // P^T hi and lo from the S^T slot, which S^T(c + 1) may take once both are read
+            issue_acc128<D>(tmem + C::DV, tmem + C::S_COL, sdO(st), c > 0);
+            issue_acc128<D>(tmem + C::DV, tmem + C::S_COL + C::QC / 2, sdO(st), true);
+            tc_commit(&bar_doempty[st]);
+            tc_commit(&bar_sfree);
+          } else {
+            issue_acc128_ss<D>(tmem + C::DV, sbase + C::PT_OFF, sdO(st), c > 0);
+            tc_commit(&bar_doempty[st]);
+            tc_commit(&bar_dvdone);
+          }
         }
+        if (ok) tc_commit(&bar_done);
       }
-      if (ok) tc_commit(&bar_done);
       tc_commit(&bar_drain[2]);
       drain_wait(&bar_drain[2], 0, a.limit_ns);
     }
   } else if (warp == C::B_WARP) {
     // Chunk c: dP^T(c) = V dO^T, then dK += dS^T(c) Q once the softmax wrote dS^T(c).
-    if (lane == 0 && nc > 0) {
-      bool ok = wait(&bar_kv, 0);
-      for (int c = 0; ok && c < nc; ++c) {
-        const int st = c % NS;
-        if (!(ok = wait(&bar_dofull[st], (c / NS) & 1))) break;
-        tc_fence_after();
-        issue_rowdot128<D>(tmem + C::DP_COL, sbase + C::V_OFF, sdO(st));
-        tc_commit(&bar_dp);
-        tc_commit(&bar_doempty[st]);
-        if (!(ok = wait(&bar_ds, c & 1))) break;
-        tc_fence_after();
-        issue_acc128<D>(tmem + C::DK, tmem + C::DP_COL, sQ(st), c > 0);
-        if constexpr (SPLIT) issue_acc128<D>(tmem + C::DK, tmem + C::DP_COL + C::QC / 2, sQ(st), true);
-        tc_commit(&bar_qempty[st]);
+    if (lane == 0) {
+      bool ok = true;
+      int g = 0, j = 0;
+      for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
+        const Item it = item(w);
+        if (it.nc == 0) continue;
+        if (!(ok = wait(&bar_kv, j & 1))) break;
+        for (int c = 0; c < it.nc; ++c, ++g) {
+          const int st = g % NS;
+          if (!(ok = wait(&bar_dofull[st], (g / NS) & 1))) break;
+          tc_fence_after();
+          issue_rowdot128<D>(tmem + C::DP_COL, sbase + C::V_OFF, sdO(st));
+          tc_commit(&bar_dp);
+          tc_commit(&bar_doempty[st]);
+          if (c + 1 == it.nc) tc_commit(&bar_kvfree);  // the item's last dP^T read V
+          if (!(ok = wait(&bar_ds, g & 1))) break;
+          tc_fence_after();
+          issue_acc128<D>(tmem + C::DK, tmem + C::DP_COL, sQ(st), c > 0);
+          if constexpr (SPLIT) issue_acc128<D>(tmem + C::DK, tmem + C::DP_COL + C::QC / 2, sQ(st), true);
+          tc_commit(&bar_qempty[st]);
+        }
+        if (ok) tc_commit(&bar_done);
+        ++j;
       }
-      if (ok) tc_commit(&bar_done);
       tc_commit(&bar_drain[1]);
       drain_wait(&bar_drain[1], 0, a.limit_ns);
     }
@@ -1593,7 +1639,6 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     constexpr int QC = C::QC;
     const int wq = warp % 4, part = warp / 4;
     const int r_in = wq * 32 + lane;
-    const int j = j0 + r_in;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     // this thread's QC queries of row r_in of the swizzled P^T tile: column block
     // (QC p) / 64, 16-byte chunks from (QC p % 64) / 8
@@ -1602,7 +1647,6 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     const uint32_t sw = (uint32_t)(r_in & 7);
     // scores and dP^T come from the scaled fp16 copies (see the dQ kernel)
     const float sl2 = a.sc->sl2, dp_mul = a.sc->dp_mul;
-    const bool row_dead = j >= a.Sk;
     auto ld_cols = [&](uint32_t addr, float (&x)[QC]) {
       if constexpr (QC == 64) {
         uint32_t r0[32], r1[32];
@@ -1617,133 +1661,144 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
       }
     };
     bool ok = true;
-    for (int c = 0; c < nc; ++c) {
-      const int st = c % NS;
-      int bh, i0;
-      chunk_rows(c, &bh, &i0);
-      const int q0 = i0 + part * QC;  // first query of this thread's part
-      float s[QC];
-      // S^T(c) and chunk c's vectors; and dO_c, so that the dV MMA issued once P^T(c)
-      // is written reads a landed tile (nothing else orders it after that copy)
-      ok = __all_sync(0xffffffffu, wait(&bar_s, c & 1) && wait(&bar_qfull[st], (c / NS) & 1) &&
-                                       wait(&bar_dofull[st], (c / NS) & 1));
-      if (!ok) break;
-      tc_fence_after();
-      ld_cols(lane_addr + C::S_COL + part * QC, s);
-      tc_fence_before();
-      __syncwarp();
-      if constexpr (!SPLIT)
-        if (lane == 0) mbar_arrive(&bar_sfree);  // the S^T slot may take the next chunk
-      // query i = q0 + k sees key j iff (!causal || j <= i) && (!window || j >= i-w+1)
-      // && i < Sq && j < Sk
-      if (tile_needs_mask(i0, i0 + BLOCK_M - 1, j0, j0 + BLOCK_N - 1, a.Sk, a.causal, a.window) ||
-          i0 + BLOCK_M > a.Sq) {
-        const int k_lo = a.causal ? j - q0 : INT_MIN / 2;
-        const int k_hi = min(a.window > 0 ? j + a.window - 1 - q0 : INT_MAX / 2, a.Sq - 1 - q0);
-#pragma unroll
-        for (int k = 0; k < QC; ++k)
-          if (row_dead || k < k_lo || k > k_hi) s[k] = -INFINITY;
-      }
-      // lse2 / delta of the chunk's queries, read with explicit shared-space loads
-      const uint32_t lv = sbase + C::VEC_OFF + st * C::VEC + part * QC * 4;
-      const float2 sl2x2 = make_float2(sl2, sl2);
-#pragma unroll
-      for (int k4 = 0; k4 < QC / 4; ++k4) {  // exponent arguments on packed pairs
-        const float4 l4 = ld_shared_v4(lv + 16 * k4);
-        const float2 xa = fma2(make_float2(s[4 * k4], s[4 * k4 + 1]), sl2x2, make_float2(-l4.x, -l4.y));
-        const float2 xb = fma2(make_float2(s[4 * k4 + 2], s[4 * k4 + 3]), sl2x2, make_float2(-l4.z, -l4.w));
-        s[4 * k4] = ex2(xa.x);
-        s[4 * k4 + 1] = ex2(xa.y);
-        s[4 * k4 + 2] = ex2(xb.x);
-        s[4 * k4 + 3] = ex2(xb.y);
-      }
-      if constexpr (SPLIT) {
-        // P^T hi / lo over the S^T columns this thread has just read: hi in the first
-        // QC / 2 packed columns of its part's range, lo in the other QC / 2
-        uint32_t ph[QC / 2], pl[QC / 2];
-#pragma unroll
-        for (int k = 0; k < QC / 2; ++k) split_half2(s[2 * k], s[2 * k + 1], ph[k], pl[k]);
-        tmem_st32(lane_addr + C::S_COL + part * QC, ph);
-        tmem_st32(lane_addr + C::S_COL + part * QC + QC / 2, pl);
-        tmem_st_wait();
+    int g = 0, jj = 0;  // chunks and items with chunks so far
+    for (int k = 0, w = item_w(0); ok && w < n_items; w = item_w(++k)) {
+      const Item it = item(w);
+      const int j0 = it.j0;
+      const int j = j0 + r_in;  // this thread's key row
+      const bool row_dead = j >= a.Sk;
+      for (int c = 0; c < it.nc; ++c, ++g) {
+        const int st = g % NS;
+        int bh, i0;
+        chunk_rows(it, c, &bh, &i0);
+        const int q0 = i0 + part * QC;  // first query of this thread's part
+        float s[QC];
+        // S^T(c) and chunk c's vectors; and dO_c, so that the dV MMA issued once P^T(c)
+        // is written reads a landed tile (nothing else orders it after that copy)
+        ok = __all_sync(0xffffffffu, wait(&bar_s, g & 1) && wait(&bar_qfull[st], (g / NS) & 1) &&
+                                         wait(&bar_dofull[st], (g / NS) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        ld_cols(lane_addr + C::S_COL + part * QC, s);
         tc_fence_before();
-      } else {
-        // P^T into shared memory once dV has consumed the previous chunk's
-        if (c > 0) {
-          ok = __all_sync(0xffffffffu, wait(&bar_dvdone, (c - 1) & 1));
-          if (!ok) break;
+        __syncwarp();
+        if constexpr (!SPLIT)
+          if (lane == 0) mbar_arrive(&bar_sfree);  // the S^T slot may take the next chunk
+        // query i = q0 + k sees key j iff (!causal || j <= i) && (!window || j >= i-w+1)
+        // && i < Sq && j < Sk
+        if (tile_needs_mask(i0, i0 + BLOCK_M - 1, j0, j0 + BLOCK_N - 1, a.Sk, a.causal, a.window) ||
+            i0 + BLOCK_M > a.Sq) {
+          const int k_lo = a.causal ? j - q0 : INT_MIN / 2;
+          const int k_hi = min(a.window > 0 ? j + a.window - 1 - q0 : INT_MAX / 2, a.Sq - 1 - q0);
+#pragma unroll
+          for (int kq = 0; kq < QC; ++kq)
+            if (row_dead || kq < k_lo || kq > k_hi) s[kq] = -INFINITY;
         }
+        // lse2 / delta of the chunk's queries, read with explicit shared-space loads
+        const uint32_t lv = sbase + C::VEC_OFF + st * C::VEC + part * QC * 4;
+        const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
-        for (int k8 = 0; k8 < QC / 8; ++k8)
-          st_shared_v4(pt_row + (((chunk0 + (uint32_t)k8) ^ sw) << 4), pack_half2(s[8 * k8], s[8 * k8 + 1]),
-                       pack_half2(s[8 * k8 + 2], s[8 * k8 + 3]), pack_half2(s[8 * k8 + 4], s[8 * k8 + 5]),
-                       pack_half2(s[8 * k8 + 6], s[8 * k8 + 7]));
-        fence_async_shared();
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_p);
-      ok = __all_sync(0xffffffffu, wait(&bar_dp, c & 1));
-      if (!ok) break;
-      tc_fence_after();
-      {
-        float g[QC];
-        ld_cols(lane_addr + C::DP_COL + part * QC, g);
-        const uint32_t dv = lv + 128 * 4;
-        const float2 dpm = make_float2(dp_mul, dp_mul);
-        uint32_t pk[QC / 2], pl[SPLIT ? QC / 2 : 1];
+        for (int k4 = 0; k4 < QC / 4; ++k4) {  // exponent arguments on packed pairs
+          const float4 l4 = ld_shared_v4(lv + 16 * k4);
+          const float2 xa = fma2(make_float2(s[4 * k4], s[4 * k4 + 1]), sl2x2, make_float2(-l4.x, -l4.y));
+          const float2 xb = fma2(make_float2(s[4 * k4 + 2], s[4 * k4 + 3]), sl2x2, make_float2(-l4.z, -l4.w));
+          s[4 * k4] = ex2(xa.x);
+          s[4 * k4 + 1] = ex2(xa.y);
+          s[4 * k4 + 2] = ex2(xb.x);
+          s[4 * k4 + 3] = ex2(xb.y);
+        }
+        if constexpr (SPLIT) {
+          // P^T hi / lo over the S^T columns this thread has just read: hi in the first
+          // QC / 2 packed columns of its part's range, lo in the other QC / 2
+          uint32_t ph[QC / 2], pl[QC / 2];
 #pragma unroll
-        for (int k4 = 0; k4 < QC / 4; ++k4) {
-          const float4 d4 = ld_shared_v4(dv + 16 * k4);
-          const int k = 4 * k4;
-          // dS = P (dP - delta) on packed pairs
-          const float2 ua = mul2(make_float2(s[k], s[k + 1]),
-                                 fma2(make_float2(g[k], g[k + 1]), dpm, make_float2(-d4.x, -d4.y)));
-          const float2 ub = mul2(make_float2(s[k + 2], s[k + 3]),
-                                 fma2(make_float2(g[k + 2], g[k + 3]), dpm, make_float2(-d4.z, -d4.w)));
-          if constexpr (SPLIT) {
-            split_half2(ua.x, ua.y, pk[2 * k4], pl[2 * k4]);
-            split_half2(ub.x, ub.y, pk[2 * k4 + 1], pl[2 * k4 + 1]);
-          } else {
-            pk[2 * k4] = pack_half2(ua.x, ua.y);
-            pk[2 * k4 + 1] = pack_half2(ub.x, ub.y);
+          for (int kq = 0; kq < QC / 2; ++kq) split_half2(s[2 * kq], s[2 * kq + 1], ph[kq], pl[kq]);
+          tmem_st32(lane_addr + C::S_COL + part * QC, ph);
+          tmem_st32(lane_addr + C::S_COL + part * QC + QC / 2, pl);
+          tmem_st_wait();
+          tc_fence_before();
+        } else {
+          // P^T into shared memory once dV has consumed the previous chunk's
+          if (g > 0) {
+            ok = __all_sync(0xffffffffu, wait(&bar_dvdone, (g - 1) & 1));
+            if (!ok) break;
           }
-        }
-        // dS^T (fp16) into the first QC / 2 columns of this part's own dP^T range
-        // (SPLIT: dS^T lo into the other QC / 2)
-        if constexpr (QC == 64) tmem_st32(lane_addr + C::DP_COL + part * QC, pk);
-        else tmem_st16(lane_addr + C::DP_COL + part * QC, pk);
-        if constexpr (SPLIT) tmem_st32(lane_addr + C::DP_COL + part * QC + QC / 2, pl);
-        if constexpr (MATDS) {
-          // dS^T row j, queries q0 .. q0 + QC - 1 (padding queries carry P = 0, so 0)
-          if (!row_dead) {
-            const size_t off = ((size_t)bh * a.Sk + j) * a.ldq + q0;
-            // QC halves = QC / 8 vectors of 16 bytes (4 packed pairs each)
-            uint4* dh = reinterpret_cast<uint4*>(a.ds_hi + off);
 #pragma unroll
-            for (int v = 0; v < QC / 8; ++v)
-              dh[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int k8 = 0; k8 < QC / 8; ++k8)
+            st_shared_v4(pt_row + (((chunk0 + (uint32_t)k8) ^ sw) << 4), pack_half2(s[8 * k8], s[8 * k8 + 1]),
+                         pack_half2(s[8 * k8 + 2], s[8 * k8 + 3]), pack_half2(s[8 * k8 + 4], s[8 * k8 + 5]),
+                         pack_half2(s[8 * k8 + 6], s[8 * k8 + 7]));
+          fence_async_shared();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_p);
+        ok = __all_sync(0xffffffffu, wait(&bar_dp, g & 1));
+        if (!ok) break;
+        tc_fence_after();
+        {
+          float gd[QC];
+          ld_cols(lane_addr + C::DP_COL + part * QC, gd);
+          const uint32_t dv = lv + 128 * 4;
+          const float2 dpm = make_float2(dp_mul, dp_mul);
+          uint32_t pk[QC / 2], pl[SPLIT ? QC / 2 : 1];
+#pragma unroll
+          for (int k4 = 0; k4 < QC / 4; ++k4) {
+            const float4 d4 = ld_shared_v4(dv + 16 * k4);
+            const int kq = 4 * k4;
+            // dS = P (dP - delta) on packed pairs
+            const float2 ua = mul2(make_float2(s[kq], s[kq + 1]),
+                                   fma2(make_float2(gd[kq], gd[kq + 1]), dpm, make_float2(-d4.x, -d4.y)));
+            const float2 ub = mul2(make_float2(s[kq + 2], s[kq + 3]),
+                                   fma2(make_float2(gd[kq + 2], gd[kq + 3]), dpm, make_float2(-d4.z, -d4.w)));
             if constexpr (SPLIT) {
-              uint4* dl = reinterpret_cast<uint4*>(a.ds_lo + off);
+              split_half2(ua.x, ua.y, pk[2 * k4], pl[2 * k4]);
+              split_half2(ub.x, ub.y, pk[2 * k4 + 1], pl[2 * k4 + 1]);
+            } else {
+              pk[2 * k4] = pack_half2(ua.x, ua.y);
+              pk[2 * k4 + 1] = pack_half2(ub.x, ub.y);
+            }
+          }
+          // dS^T (fp16) into the first QC / 2 columns of this part's own dP^T range
+          // (SPLIT: dS^T lo into the other QC / 2)
+          if constexpr (QC == 64) tmem_st32(lane_addr + C::DP_COL + part * QC, pk);
+          else tmem_st16(lane_addr + C::DP_COL + part * QC, pk);
+          if constexpr (SPLIT) tmem_st32(lane_addr + C::DP_COL + part * QC + QC / 2, pl);
+          if constexpr (MATDS) {
+            // dS^T row j, queries q0 .. q0 + QC - 1 (padding queries carry P = 0, so 0)
+            if (!row_dead) {
+              const size_t off = ((size_t)bh * a.Sk + j) * a.ldq + q0;
+              // QC halves = QC / 8 vectors of 16 bytes (4 packed pairs each)
+              uint4* dh = reinterpret_cast<uint4*>(a.ds_hi + off);
 #pragma unroll
               for (int v = 0; v < QC / 8; ++v)
-                dl[v] = make_uint4(pl[4 * v], pl[4 * v + 1], pl[4 * v + 2], pl[4 * v + 3]);
+                dh[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+              if constexpr (SPLIT) {
+                uint4* dl = reinterpret_cast<uint4*>(a.ds_lo + off);
+#pragma unroll
+                for (int v = 0; v < QC / 8; ++v)
+                  dl[v] = make_uint4(pl[4 * v], pl[4 * v + 1], pl[4 * v + 2], pl[4 * v + 3]);
+              }
             }
           }
         }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_ds);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_ds);
-    }
-    if (ok && nc > 0) {
-      ok = __all_sync(0xffffffffu, wait(&bar_done, 0));
-      tc_fence_after();
-    }
-    if (ok) {
-      // bar_done: every MMA has completed, so all operand buffers are free. Parts
-      // 0 .. NPART/2-1 write dV, the others dK; each part D / (NPART / 2) columns of
-      // rows j0 + 32 (w % 4) ...
+      if (!ok) break;
+      if (it.nc > 0) {
+        ok = __all_sync(0xffffffffu, wait(&bar_done, jj & 1));
+        if (!ok) break;
+        tc_fence_after();
+        ++jj;
+      }
+      // ---- epilogue of the item: every MMA of it has completed (an item without
+      // chunks writes zeros). Parts 0 .. NPART/2-1 write dV, the others dK; each part D /
+      // (NPART / 2) columns of rows j0 + 32 (w % 4) ... The stores are staged in the P^T
+      // tile, one 32 x 128-byte box per warp at a time (the other buffers may already
+      // hold the next item's tiles); it is free here (the item's dV MMAs are done) and
+      // this thread writes the next P^T only after its stores have read it.
       constexpr int HP = C::NPART / 2;     // parts per output
       constexpr int DW = D / HP;           // columns per warp
       const int which = part / HP, cpart = part % HP;
@@ -1752,20 +1807,24 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
       const uint32_t acc = lane_addr + (which ? C::DK : C::DV) + cpart * DW;
       const CUtensorMap* tm = which ? &m.dK : &m.dV;
       const float mul = which ? a.sc->dk_mul : a.sc->dv_mul;  // scale 2^-(eD+eQ) / 2^-eO
-      const uint32_t stage = sbase + warp * (C::EPI_WARP / HP);
+      const uint32_t stage = sbase + C::PT_OFF + warp * EPI_BOX_BYTES;
+      static_assert(C::SOFTMAX_WARPS * EPI_BOX_BYTES <= 2 * C::PT_CB, "epilogue staging");
       if (D >= 64 && a.out_bf16) {  // (bf16 outputs: D >= 64 kernels only)
         if constexpr (D >= 64) {
-          if constexpr (DW % 64 == 0)
-            store_rows_tma<DW, true, DW / 64>(tm, acc, nc > 0, mul, stage, r_base, any, bg,
-                                              cpart * DW, a.Dv);
-          else if (cpart == 0)  // a bf16 box is a 64-column row: one warp per output does it
-            store_rows_tma<D, true, D / 64>(tm, lane_addr + (which ? C::DK : C::DV), nc > 0, mul,
-                                            sbase + warp * C::EPI_WARP, r_base, any, bg, 0, a.Dv);
+          if constexpr (DW % 64 == 0) {
+            store_rows_tma<DW, true, 1>(tm, acc, it.nc > 0, mul, stage, r_base, any, it.bg, cpart * DW,
+                                        a.Dv);
+          } else {
+            // a bf16 box is a 64-column row: one warp per output does it
+            if (cpart == 0)
+              store_rows_tma<D, true, 1>(tm, lane_addr + (which ? C::DK : C::DV), it.nc > 0, mul, stage,
+                                         r_base, any, it.bg, 0, a.Dv);
+          }
         }
       } else {
-        store_rows_tma<DW, false, DW / 32>(tm, acc, nc > 0, mul, stage, r_base, any, bg, cpart * DW,
-                                           a.Dv);
+        store_rows_tma<DW, false, 1>(tm, acc, it.nc > 0, mul, stage, r_base, any, it.bg, cpart * DW, a.Dv);
       }
+      tc_fence_before();  // (the accumulator loads precede every later hand-off)
     }
   }
   tc_fence_before();
@@ -2606,7 +2665,9 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
         host::KernelTimer kt(D == 128 ? "fa_bwd_dkdv_kernel<128,bf16>"
                                       : (D == 64 ? "fa_bwd_dkdv_kernel<64,bf16>" : "fa_bwd_dkdv_kernel<32,bf16>"),
                              stream);
-        kern<<<(unsigned)(BHk * ak.n_tiles), C16::THREADS, dyn, stream>>>(mk, ak);
+        // persistent: one CTA per SM (at most), walking the (key tile, kv head) items
+        const unsigned grid = (unsigned)std::min<size_t>(BHk * ak.n_tiles, (size_t)sms);
+        kern<<<grid, C16::THREADS, dyn, stream>>>(mk, ak);
         e = cudaGetLastError();
       }
     }
