@@ -155,7 +155,8 @@ fa_status validate(const fa_params* p) {
   if (!(std::isfinite(p->scale) && p->scale > 0.f)) return FA_ERR_INVALID_ARG;
   if ((p->causal != 0 && p->causal != 1) || p->window < 0) return FA_ERR_INVALID_ARG;
   if ((p->in_dtype != FA_F32 && p->in_dtype != FA_BF16) ||
-      (p->out_dtype != FA_F32 && p->out_dtype != FA_BF16))
+      (p->out_dtype != FA_F32 && p->out_dtype != FA_BF16) ||
+      (p->f32_mma != FA_F32_MMA_F16X2 && p->f32_mma != FA_F32_MMA_TF32X3))
     return FA_ERR_INVALID_ARG;
   // Index arithmetic inside the kernels uses 32-bit row / head / grid counters.
   const long long bh = (long long)p->B * p->H;
@@ -167,11 +168,13 @@ fa_status validate(const fa_params* p) {
   if ((double)p->B * p->H * p->Sq * p->D * 4.0 > lim ||
       (double)p->B * p->HKV * p->Sk * p->D * 4.0 > lim)
     return FA_ERR_INVALID_ARG;
-  // Head dims: multiples of 16 up to 128; each runs in the kernel built for the next of
-  // 64 / 128, with the missing columns read as zeros.
+  // Head dims: multiples of 16 up to 128 (3xTF32: up to 64); each runs in the kernel
+  // built for the next of 32 (bf16 in, fp32 out), 64 and 128, with the missing columns
+  // read as zeros.
   const bool d16 = p->D % 16 == 0 && p->D >= 16;
   const bool ok_bf16 = p->in_dtype == FA_BF16 && d16 && p->D <= 128;
-  const bool ok_f32 = p->in_dtype == FA_F32 && d16 && p->D <= 128;
+  const bool ok_f32 = p->in_dtype == FA_F32 && d16 &&
+                      p->D <= (p->f32_mma == FA_F32_MMA_TF32X3 ? 64 : 128);
   if (!ok_bf16 && !ok_f32) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }

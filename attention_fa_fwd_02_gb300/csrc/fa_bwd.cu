@@ -10,9 +10,11 @@
 // Kernels:
 //   preprocess   D_i, the log2-domain LSE (+inf for rows that saw no key, so their
 //                P is exactly 0) and the tensor-core operand copies: fp16 for bf16
-//                inputs; tf32 hi / lo splits (plus transposed copies of Q, K, dO,
-//                since tf32 operands must be K-major) for fp32 inputs.
-//   dkdv         one CTA per (batch, kv head, 128-key tile). It walks CH-query
+//                inputs; for fp32 inputs two scaled fp16 terms, or tf32 hi / lo
+//                splits (plus transposed copies of Q, K, dO, since tf32 operands
+//                must be K-major).
+//   dkdv         per (batch, kv head, 128-key tile) -- for bf16 inputs a work item
+//                of a persistent CTA, for fp32 inputs one CTA. It walks CH-query
 //                chunks of every grouped query head that can see the tile:
 //                S^T = K Q^T and dP^T = V dO^T into a double-buffered TMEM slot,
 //                softmax warps turn them into P^T and dS^T (back into TMEM),
@@ -20,7 +22,8 @@
 //   dq           one CTA per (batch, head, 128-query tile), CH-key chunks:
 //                S = Q K^T, dP = dO V^T, dS = P (dP - D), dQ += dS K.
 // While the softmax warps work on chunk c, the tensor core computes chunk c+1.
-// For fp32 inputs every product is the 3xTF32 sum a_hi b_hi + a_hi b_lo + a_lo b_hi.
+// For fp32 inputs every product is the three-term sum a_hi b_hi + a_hi b_lo + a_lo b_hi,
+// of fp16 terms (x 2^e = hi + lo) or of tf32 terms (3xTF32).
 #include <cfloat>
 #include <climits>
 #include <algorithm>
@@ -71,15 +74,16 @@ struct QMaps {  // dq
   CUtensorMap Q[2], dO[2], Kc[2], Vc[2], Kt[2], dQ;
 };
 
-template <int D_, bool F32_>
+template <int D_, int PREC>
 struct BwdCfg {
   static constexpr int D = D_;
-  static constexpr bool F32 = F32_;
-  // fp32 inputs: 3xTF32 up to D = 64; above, two scaled fp16 terms per operand (X16,
-  // x 2^e = hi + lo, three kind::f16 products per GEMM; 16-bit B operands may be
-  // MN-major, so no transposed copies)
-  static constexpr bool X16 = F32 && D > 64;
-  static constexpr bool TF32 = F32 && !X16;
+  static constexpr bool F32 = PREC != IN_BF16;
+  // fp32 inputs: two scaled fp16 terms per operand (X16, x 2^e = hi + lo, three
+  // kind::f16 products per GEMM; 16-bit B operands may be MN-major, so no transposed
+  // copies), or 3xTF32 up to D = 64
+  static constexpr bool X16 = PREC == IN_F32_X16;
+  static constexpr bool TF32 = PREC == IN_F32_TF32;
+  static_assert(!TF32 || D <= 64, "3xTF32 tiles up to D = 64");
   static constexpr int ESZ = TF32 ? 4 : 2;
   static constexpr int ROW = 128 / ESZ;                 // elements per 128-byte row
   static constexpr int NCB = D / ROW;                   // 128-byte column blocks per row
@@ -288,7 +292,7 @@ __device__ __forceinline__ void tmem_st_operand(uint32_t hi, uint32_t lo, const 
 }
 
 // ------------------------------------------------------------------ dK / dV
-template <int D, bool F32>
+template <int D, int F32>
 __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ KVMaps m, const BwdArgs a) {
   using C = BwdCfg<D, F32>;
@@ -552,7 +556,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
 }
 
 // ----------------------------------------------------------------------- dQ
-template <int D, bool F32>
+template <int D, int F32>
 __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
     fa_bwd_dq_kernel(const __grid_constant__ QMaps m, const BwdArgs a) {
   using C = BwdCfg<D, F32>;
@@ -2292,7 +2296,7 @@ __global__ void dq_range_sum_kernel(const float* __restrict__ part, void* __rest
   }
 }
 
-// fp32 inputs at D > 64 (X16): every block reduces the amax kernel's per-block maxima
+// fp32 inputs as two fp16 terms (X16): every block reduces the amax kernel's per-block maxima
 // of |Q|, |K|, |V|, |dO| and |delta|, picks the exponents (x16_exponent for the
 // copies, x16_ds_exponent for dS), and the grid writes x 2^e = hi + lo as fp16 pairs
 // and delta 2^eD; block 0 publishes the multipliers (as bwd_scales_kernel does).
@@ -2348,7 +2352,7 @@ namespace {
 
 // dsmat (bf16 inputs): the materialised-dS variant -- the dK / dV kernel also stores
 // dS^T, and dQ is a GEMM over it (dq_from_ds_kernel) instead of the recompute kernel.
-template <int D, bool F32>
+template <int D, int F32>
 fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                   const float* LSE, void* dQ, void* dK, void* dV, const fa_params& p,
                   cudaStream_t stream, bool dsmat) {
@@ -2645,7 +2649,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       auto kern = fa_bwd_dkdv_kernel<D, F32>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::KV_SMEM);
       if (e == cudaSuccess) {
-        host::KernelTimer kt(D == 128 ? "fa_bwd_dkdv_kernel<128,f32>" : "fa_bwd_dkdv_kernel<64,f32>",
+        host::KernelTimer kt(C::TF32 ? "fa_bwd_dkdv_kernel<64,tf32>"
+                             : (D == 128 ? "fa_bwd_dkdv_kernel<128,f32>" : "fa_bwd_dkdv_kernel<64,f32>"),
                              stream);
         kern<<<(unsigned)(BHk * ak.n_tiles), C::THREADS, C::KV_SMEM, stream>>>(mk, ak);
         e = cudaGetLastError();
@@ -2683,7 +2688,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       auto kern = fa_bwd_dq_kernel<D, F32>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::Q_SMEM);
       if (e == cudaSuccess) {
-        host::KernelTimer kt(D == 128 ? "fa_bwd_dq_kernel<128,f32>" : "fa_bwd_dq_kernel<64,f32>",
+        host::KernelTimer kt(C::TF32 ? "fa_bwd_dq_kernel<64,tf32>"
+                             : (D == 128 ? "fa_bwd_dq_kernel<128,f32>" : "fa_bwd_dq_kernel<64,f32>"),
                              stream);
         kern<<<(unsigned)(BH * aq.n_tiles), C::THREADS, C::Q_SMEM, stream>>>(mq, aq);
         e = cudaGetLastError();
@@ -2787,12 +2793,14 @@ fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O,
   if (p.in_dtype == FA_BF16) {
     // (the D = 32 kernels write fp32 outputs and recompute dS for dQ)
     if (p.D <= 32 && p.out_dtype == FA_F32 && !dsmat)
-      return run_bwd<32, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, false);
-    if (p.D <= 64) return run_bwd<64, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, dsmat);
-    if (p.D <= 128) return run_bwd<128, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, dsmat);
+      return run_bwd<32, IN_BF16>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, false);
+    if (p.D <= 64) return run_bwd<64, IN_BF16>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, dsmat);
+    if (p.D <= 128) return run_bwd<128, IN_BF16>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, dsmat);
+  } else if (p.f32_mma == FA_F32_MMA_TF32X3) {
+    if (p.D <= 64) return run_bwd<64, IN_F32_TF32>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, false);
   } else {
-    if (p.D <= 64) return run_bwd<64, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, false);
-    if (p.D <= 128) return run_bwd<128, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, false);
+    if (p.D <= 64) return run_bwd<64, IN_F32_X16>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, false);
+    if (p.D <= 128) return run_bwd<128, IN_F32_X16>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream, false);
   }
   return FA_ERR_UNSUPPORTED;
 }

@@ -63,6 +63,12 @@ inline void combine_launch_shape(int BH, int Sq, int Dv, dim3* grid, dim3* block
 // work on padding columns).
 constexpr int tile_row_bytes(int D) { return 2 * D < 128 ? 2 * D : 128; }
 
+// Input precision of a kernel instantiation (the integer F32 template argument of the
+// forward and backward kernels and their launchers): bf16 inputs; fp32 inputs as two
+// scaled fp16 terms per operand (three kind::f16 products per GEMM); fp32 inputs as
+// hi / lo tf32 splits (three kind::tf32 products per GEMM, head dims up to 64).
+enum : int { IN_BF16 = 0, IN_F32_X16 = 1, IN_F32_TF32 = 2 };
+
 // Status bits a kernel may set in its device status word.
 enum : unsigned int {
   DEV_TIMEOUT = 1u,  // a barrier wait gave up

@@ -9,7 +9,7 @@
 //   warps [0, 4*NQ)   softmax: thread = one query row = one TMEM lane. Reads the
 //                     S row from TMEM, masks boundary tiles, keeps the running max
 //                     m (log2 units) and sum l, writes P back into TMEM (fp16 for
-//                     bf16 inputs; tf32 hi + lo for fp32 inputs), rescales its O
+//                     bf16 inputs; fp16 or tf32 hi + lo for fp32 inputs), rescales its O
 //                     row in TMEM when m grows by more than RESCALE_THRESHOLD, and
 //                     in the epilogue writes LSE = (m + log2 l) ln 2 and O = acc / l
 //                     (staged in a V ring stage, written by TMA stores).
@@ -55,15 +55,16 @@ struct FwdArgs {
   const OperandScales* sc;  // bf16 inputs: o_mul = 2^-eV undoes the scaled fp16 copy of V
 };
 
-template <int D_, bool F32_>
+template <int D_, int PREC>
 struct FwdCfg {
   static constexpr int D = D_;
-  static constexpr bool F32 = F32_;
-  // fp32 inputs: 3xTF32 (hi / lo tf32 splits) up to D = 64; above, whose tf32 tiles would
-  // not fit shared memory, two scaled fp16 terms per operand (X16: x 2^e = hi + lo,
-  // three kind::f16 products per GEMM)
-  static constexpr bool X16 = F32 && D > 64;
-  static constexpr bool TF32 = F32 && !X16;
+  static constexpr bool F32 = PREC != IN_BF16;
+  // fp32 inputs: two scaled fp16 terms per operand (X16: x 2^e = hi + lo, three
+  // kind::f16 products per GEMM), or 3xTF32 (hi / lo tf32 splits) up to D = 64, above
+  // which the tf32 tiles would not fit shared memory
+  static constexpr bool X16 = PREC == IN_F32_X16;
+  static constexpr bool TF32 = PREC == IN_F32_TF32;
+  static_assert(!TF32 || D <= 64, "3xTF32 tiles up to D = 64");
   static constexpr int NQ = F32 ? 1 : 2;                   // query tiles per CTA
   static constexpr int ESZ = TF32 ? 4 : 2;                 // operand bytes in smem
   // smem rows of RB bytes with the swizzle of that width: 128, or 64 for bf16 at D = 32
@@ -258,7 +259,7 @@ __device__ __forceinline__ void issue_v_load(uint8_t* smem, int it, int t, int b
 // order. Where one key takes almost all of a row's weight, one fp16 term (11
 // significant bits) puts an error in O that the backward's D_i = dO_i . O_i then
 // passes on to dS at exactly the dominant keys.
-template <int D, bool F32, bool HP, bool PSPLIT>
+template <int D, int F32, bool HP, bool PSPLIT>
 __global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKlo,
@@ -815,7 +816,7 @@ __global__ void __launch_bounds__(1024) fwd_scales_kernel(const uint32_t* __rest
   if (ev != 0) rescale_copy(V, V16, n8, ev);
 }
 
-// fp32 inputs at D > 64 (X16): every block reduces the amax kernel's per-block maxima
+// fp32 inputs as two fp16 terms (X16): every block reduces the amax kernel's per-block maxima
 // of |Q|, |K|, |V|, picks each tensor's exponent (x16_exponent), and the grid writes
 // x 2^e = hi + lo as fp16 pairs; block 0 publishes the multipliers (scores:
 // scale log2(e) 2^-(eQ + eK); O: 2^-eV).
@@ -929,7 +930,7 @@ bool encode_o_map(CUtensorMap* m, void* O, const fa_params& p) {
                                bf ? 2 : 4, O, p.D, p.Sq, (uint64_t)p.B * p.H, p.D, bf ? 64 : 32, 32);
 }
 
-// X16 (fp32 inputs, D > 64): scratch bytes for the fp16 hi / lo copies of Q, K, V, the
+// X16 (fp32 inputs as two fp16 terms): scratch bytes for the fp16 hi / lo copies of Q, K, V, the
 // OperandScales and the amax kernel's n_amax x 3 partial maxima.
 size_t x16_fwd_bytes(const fa_params& p, int n_amax) {
   const size_t nq = (size_t)p.B * p.H * p.Sq * p.D, nk = (size_t)p.B * p.HKV * p.Sk * p.D;
@@ -990,7 +991,7 @@ bool prep_x16_fwd(void* ws, const void* Q, const void* K, const void* V, const f
 
 // The forward kernel instantiation: head-pair items (two-tile kernels only) or not;
 // two-term P (bf16 inputs) or not.
-template <int D, bool F32>
+template <int D, int F32>
 auto fwd_kernel_for(bool hp, bool psplit) {
   auto kern = fa_fwd_kernel<D, F32, false, false>;
   if constexpr (FwdCfg<D, F32>::NQ == 2) {
@@ -1000,7 +1001,7 @@ auto fwd_kernel_for(bool hp, bool psplit) {
   return kern;
 }
 
-template <int D, bool F32>
+template <int D, int F32>
 fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                   const fa_params& p, cudaStream_t stream) {
   using C = FwdCfg<D, F32>;
@@ -1130,7 +1131,8 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_ALLOC);
   if (e == cudaSuccess) {
-    host::KernelTimer kt(F32 ? (D == 128 ? "fa_fwd_kernel<128,f32>" : "fa_fwd_kernel<64,f32>")
+    host::KernelTimer kt(C::TF32 ? "fa_fwd_kernel<64,tf32>"
+                         : F32 ? (D == 128 ? "fa_fwd_kernel<128,f32>" : "fa_fwd_kernel<64,f32>")
                              : (D == 128 ? "fa_fwd_kernel<128,bf16>"
                                          : (D == 64 ? "fa_fwd_kernel<64,bf16>" : "fa_fwd_kernel<32,bf16>")),
                          stream);
@@ -1165,12 +1167,14 @@ fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float
   // head dims below a kernel's D run in it with the missing columns read as zeros
   if (p.in_dtype == FA_BF16) {
     // (the D = 32 kernel writes fp32 outputs only)
-    if (p.D <= 32 && p.out_dtype == FA_F32) return run_fwd<32, false>(Q, K, V, O, LSE, p, stream);
-    if (p.D <= 64) return run_fwd<64, false>(Q, K, V, O, LSE, p, stream);
-    if (p.D <= 128) return run_fwd<128, false>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 32 && p.out_dtype == FA_F32) return run_fwd<32, IN_BF16>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 64) return run_fwd<64, IN_BF16>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 128) return run_fwd<128, IN_BF16>(Q, K, V, O, LSE, p, stream);
+  } else if (p.f32_mma == FA_F32_MMA_TF32X3) {
+    if (p.D <= 64) return run_fwd<64, IN_F32_TF32>(Q, K, V, O, LSE, p, stream);
   } else {
-    if (p.D <= 64) return run_fwd<64, true>(Q, K, V, O, LSE, p, stream);
-    if (p.D <= 128) return run_fwd<128, true>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 64) return run_fwd<64, IN_F32_X16>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 128) return run_fwd<128, IN_F32_X16>(Q, K, V, O, LSE, p, stream);
   }
   return FA_ERR_UNSUPPORTED;
 }
@@ -1288,12 +1292,12 @@ double noalloc_bytes(const fa_params& p, int n_cvt) {
   }
 }
 
-template <int D, bool F32>
+template <int D, int F32>
 fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
                           const fa_params& p, cudaStream_t stream) {
   using C = FwdCfg<D, F32>;
   const int n_cvt = 8 * host::sm_count();  // conversion blocks (bf16 inputs)
-  if (noalloc_bytes<F32, C::X16>(p, n_cvt) > (double)FA_NOALLOC_SCRATCH_BYTES)
+  if (noalloc_bytes<C::F32, C::X16>(p, n_cvt) > (double)FA_NOALLOC_SCRATCH_BYTES)
     return FA_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;
   const fa_status st = noalloc_scratch_addr(&ws);
@@ -1394,11 +1398,13 @@ fa_status launch_fwd_noalloc(const void* Q, const void* K, const void* V, void* 
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
   if (p.in_dtype == FA_BF16) {
-    if (p.D <= 64) return run_fwd_noalloc<64, false>(Q, K, V, O, LSE, p, stream);
-    if (p.D <= 128) return run_fwd_noalloc<128, false>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 64) return run_fwd_noalloc<64, IN_BF16>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 128) return run_fwd_noalloc<128, IN_BF16>(Q, K, V, O, LSE, p, stream);
+  } else if (p.f32_mma == FA_F32_MMA_TF32X3) {
+    if (p.D <= 64) return run_fwd_noalloc<64, IN_F32_TF32>(Q, K, V, O, LSE, p, stream);
   } else {
-    if (p.D <= 64) return run_fwd_noalloc<64, true>(Q, K, V, O, LSE, p, stream);
-    if (p.D <= 128) return run_fwd_noalloc<128, true>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 64) return run_fwd_noalloc<64, IN_F32_X16>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 128) return run_fwd_noalloc<128, IN_F32_X16>(Q, K, V, O, LSE, p, stream);
   }
   return FA_ERR_UNSUPPORTED;
 }

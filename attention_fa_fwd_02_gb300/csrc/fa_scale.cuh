@@ -69,8 +69,8 @@ __host__ __device__ inline int ds_exponent(uint32_t amax_do, uint32_t amax_v,
   return clamp_exp(DS_TOP - u);
 }
 
-// fp32 inputs carried as two scaled fp16 terms (x 2^e = hi + lo, the fp32 path at head
-// dims whose 3xTF32 tiles do not fit shared memory): the exponent always moves the
+// fp32 inputs carried as two scaled fp16 terms (x 2^e = hi + lo; the default fp32 path,
+// the other being 3xTF32): the exponent always moves the
 // largest magnitude into [2^14, 2^15), so that the lo terms of the elements stay as far
 // above fp16's subnormal range as the tensor's range allows.
 __host__ __device__ inline int x16_exponent(uint32_t amax) {

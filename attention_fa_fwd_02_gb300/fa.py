@@ -17,6 +17,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfa.so")
 
 FA_F32, FA_BF16 = 0, 1
+FA_F32_MMA_F16X2, FA_F32_MMA_TF32X3 = 0, 1
+F32_MMA = {"f16x2": FA_F32_MMA_F16X2, "tf32x3": FA_F32_MMA_TF32X3}
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
           4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_SCRATCH_LIMIT", 7: "FA_ERR_LAYOUT"}
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_device_status", "fa_status_string", "fa_version",
@@ -34,7 +36,7 @@ class fa_params(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("HKV", ctypes.c_int),
                 ("Sq", ctypes.c_int), ("Sk", ctypes.c_int), ("D", ctypes.c_int),
                 ("scale", ctypes.c_float), ("causal", ctypes.c_int), ("window", ctypes.c_int),
-                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int)]
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("f32_mma", ctypes.c_int)]
 
 
 class fa_kernel_time(ctypes.Structure):
@@ -145,7 +147,8 @@ def fa_timing_read() -> dict:
 
 
 # ------------------------------------------------------------ torch helpers
-def make_params(q, k, scale=None, causal=False, window=0, out_dtype=None) -> fa_params:
+def make_params(q, k, scale=None, causal=False, window=0, out_dtype=None,
+                f32_mma="f16x2") -> fa_params:
     import torch
     B, H, Sq, D = q.shape
     HKV, Sk = k.shape[1], k.shape[2]
@@ -153,8 +156,10 @@ def make_params(q, k, scale=None, causal=False, window=0, out_dtype=None) -> fa_
     if in_dt is None:
         raise TypeError(f"unsupported input dtype {q.dtype}")
     out_dt = FA_F32 if out_dtype in (None, torch.float32) else FA_BF16
+    if f32_mma not in F32_MMA:
+        raise ValueError(f"f32_mma must be one of {sorted(F32_MMA)}")
     return fa_params(B, H, HKV, Sq, Sk, D, float(1.0 / math.sqrt(D) if scale is None else scale),
-                     int(bool(causal)), int(window), in_dt, out_dt)
+                     int(bool(causal)), int(window), in_dt, out_dt, F32_MMA[f32_mma])
 
 
 def _check(t, name):
@@ -168,12 +173,14 @@ def _stream_handle(stream) -> int:
     return int(s.cuda_stream)
 
 
-def forward(q, k, v, scale=None, causal=False, window=0, out_dtype=None, stream=None):
-    """O, LSE = attention(q, k, v) on the GPU through ``fa_fwd``."""
+def forward(q, k, v, scale=None, causal=False, window=0, out_dtype=None, stream=None,
+            f32_mma="f16x2"):
+    """O, LSE = attention(q, k, v) on the GPU through ``fa_fwd``. ``f32_mma`` (fp32
+    inputs): "f16x2" (two scaled fp16 terms per operand) or "tf32x3" (D <= 64)."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check(t, n)
-    p = make_params(q, k, scale, causal, window, out_dtype)
+    p = make_params(q, k, scale, causal, window, out_dtype, f32_mma)
     o = torch.empty(q.shape, dtype=torch.float32 if p.out_dtype == FA_F32 else torch.bfloat16,
                     device=q.device)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
@@ -185,13 +192,13 @@ def forward(q, k, v, scale=None, causal=False, window=0, out_dtype=None, stream=
 
 
 def backward(q, k, v, o, lse, do, scale=None, causal=False, window=0, out_dtype=None,
-             stream=None, materialize_ds=False):
+             stream=None, materialize_ds=False, f32_mma="f16x2"):
     """dQ, dK, dV through ``fa_bwd`` (o / lse as returned by ``forward``), or through
     ``fa_bwd_dsmat`` with ``materialize_ds``."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (do, "do")):
         _check(t, n)
-    p = make_params(q, k, scale, causal, window, out_dtype)
+    p = make_params(q, k, scale, causal, window, out_dtype, f32_mma)
     odt = torch.float32 if p.out_dtype == FA_F32 else torch.bfloat16
     dq = torch.empty(q.shape, dtype=odt, device=q.device)
     dk = torch.empty(k.shape, dtype=odt, device=q.device)

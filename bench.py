@@ -68,13 +68,14 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def tensor_peaks(peaks, dtype):
-    """(burst, sustained) dense tensor peak in TFLOP/s for the path's arithmetic type:
-    the measured bf16 figures, or half of them for the tf32 products of the fp32 path
-    (the nominal tf32 / bf16 rate ratio). The burst figure is the roofline denominator
-    for kernels of well under a second timed at full clocks; the sustained one (a
-    seconds-long loop under the power cap) is reported beside it."""
-    div = 1.0 if dtype == "bf16" else 2.0
+def tensor_peaks(peaks, dtype, f32_mma="f16x2"):
+    """(burst, sustained) dense tensor peak in TFLOP/s of the tensor-core kind the path
+    runs on: the measured bf16 figures for kind::f16 (bf16 inputs, and fp32 inputs as
+    two fp16 terms), half of them for the tf32 products of the 3xTF32 path (the nominal
+    tf32 / bf16 rate ratio). The burst figure is the roofline denominator for kernels of
+    well under a second timed at full clocks; the sustained one (a seconds-long loop
+    under the power cap) is reported beside it."""
+    div = 2.0 if (dtype == "f32" and f32_mma == "tf32x3") else 1.0
     return peaks["bf16_tflops"] / div, peaks["bf16_tflops_sustained"] / div
 
 
@@ -182,11 +183,13 @@ def oracle_sample(w, n_groups, batch=0):
     return (fwd + bwd) / dt / 1e12, dt, oracle.num_threads(), n_groups * rep
 
 
-def config_of(w, out_dtype="f32", extra=None, bwd="recompute"):
+def config_of(w, out_dtype="f32", extra=None, bwd="recompute", f32_mma="f16x2"):
     c = {"workload": w.name, "B": w.B, "H": w.H, "HKV": w.HKV, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
          "causal": bool(w.causal), "window": w.window, "scale": w.scale, "in_dtype": w.dtype,
          "out_dtype": out_dtype, "backward": bwd,
          "l2": "256 MiB memset between timed steps; inputs also exceed L2"}
+    if w.dtype == "f32":
+        c["f32_mma"] = f32_mma
     if extra:
         c.update(extra)
     return c
@@ -227,7 +230,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_of(w, args.out_dtype, bwd=args.bwd),
+            "data": "synthetic", "config": config_of(w, args.out_dtype, bwd=args.bwd, f32_mma=args.f32_mma),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -279,7 +282,7 @@ def run_ours(args, rank, world, local_rank):
     q, k, v, do = make_inputs(wr)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     odt = torch.bfloat16 if args.out_dtype == "bf16" else torch.float32
-    p = fa.make_params(qd, kd, w.scale, w.causal, w.window, out_dtype=odt)
+    p = fa.make_params(qd, kd, w.scale, w.causal, w.window, out_dtype=odt, f32_mma=args.f32_mma)
     o = torch.empty(q.shape, dtype=odt, device=dev)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
     dq = torch.empty(q.shape, dtype=odt, device=dev)
@@ -438,7 +441,7 @@ def run_ours(args, rank, world, local_rank):
     fwd_fl, bwd_fl, vis = flops_for(w)
     value = whole_job_tflops(fwd_fl + bwd_fl, world, ms_max)
     peaks, peak_src = load_peaks()
-    peak, peak_sus = tensor_peaks(peaks, w.dtype)
+    peak, peak_sus = tensor_peaks(peaks, w.dtype, args.f32_mma)
     per_kernel = {}
     fwd_ms = 0.0
     launches = 0
@@ -471,7 +474,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-        "data": "synthetic", "config": config_of(w, args.out_dtype, bwd=args.bwd),
+        "data": "synthetic", "config": config_of(w, args.out_dtype, bwd=args.bwd, f32_mma=args.f32_mma),
         "fwd_tflops": round(fwd_fl / (fwd_ms * 1e-3) / 1e12, 3) if fwd_ms else None,
         # the backward's share of the step: step time minus the forward kernels' time
         # (its dK / dV and dQ kernels overlap inside the step)
@@ -483,7 +486,9 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": traffic,
                      "peak_source": (f"{peak_src} bf16 burst (MEASURED_PEAKS.json)"
                                      if peak_src == "measured" else "fallback 1.9 PFLOP/s burst")
-                     + ("" if w.dtype == "bf16" else " x 1/2, the nominal tf32 / bf16 rate ratio"),
+                     + ("" if w.dtype == "bf16" else
+                        " x 1/2, the nominal tf32 / bf16 rate ratio; 3 products per GEMM"
+                        if args.f32_mma == "tf32x3" else " (kind::f16); 3 products per GEMM"),
                      "peak_sustained": peak_sus, "frac_sustained": round(achieved / peak_sus, 4)},
         "kernels": {k_: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
                          for kk, vv in e.items()} for k_, e in per_kernel.items()},
@@ -516,6 +521,9 @@ def main():
     ap.add_argument("--bwd", choices=["recompute", "dsmat"], default="recompute",
                     help="backward route: fa_bwd (recomputes S and dP for dQ) or fa_bwd_dsmat "
                          "(materialised dS; measurement lines)")
+    ap.add_argument("--f32-mma", choices=["f16x2", "tf32x3"], default="f16x2",
+                    help="fp32 workloads: tensor-core terms (two scaled fp16 terms per operand, "
+                         "or 3xTF32 for head dims up to 64)")
     ap.add_argument("--head-dim", type=int, default=None,
                     help="run the workload with another head dim (measurement lines; the "
                          "headline is the workload's own)")

@@ -35,15 +35,20 @@
  * (e.g. gradients dO of 1e-7, V of 1e5).
  * in_dtype FA_F32: every GEMM uses three tensor-core products of a hi/lo split of its
  * operands, a = a_hi + a_lo, a_hi b_hi + a_hi b_lo + a_lo b_hi, giving close to fp32
- * accuracy: tf32 terms for D <= 64; for D > 64, whose tf32 tiles would not fit shared
- * memory, fp16 terms of x * 2^e (one power of two per tensor and call, chosen from its
- * largest magnitude as for the bf16 path; about 22 significant bits, like the tf32 pair). Outputs are written in out_dtype (FA_F32 recommended; FA_BF16
- * rounds O / dQ / dK / dV to bf16 on store). LSE is always fp32, natural log.
+ * accuracy (about 22 significant bits per operand). fa_params.f32_mma picks the terms:
+ * FA_F32_MMA_F16X2 (0, the default) uses fp16 terms of x * 2^e (one power of two per
+ * tensor and call, chosen from its largest magnitude as for the bf16 path) on the
+ * fp16 tensor-core rate, at every supported head dim; FA_F32_MMA_TF32X3 uses tf32
+ * terms (fp32's exponent range, no scaling) at half that rate, for D <= 64 only.
+ * P and dS enter the second GEMMs as the same kind of pair. Outputs are written in
+ * out_dtype (FA_F32 recommended; FA_BF16 rounds O / dQ / dK / dV to bf16 on store).
+ * LSE is always fp32, natural log.
  *
  * Supported in this build: head dims D that are multiples of 16, 16 <= D <= 128, for
  * both input types (the pages' set 16, 32, 48, 64, 80, 96, 128 among them); other head
- * dims return FA_ERR_UNSUPPORTED. A D below 64 / 128 runs in the kernels built for
- * 64 / 128, whose tensor-core work then includes the zero columns up to that width.
+ * dims return FA_ERR_UNSUPPORTED. Each D runs in the kernels built for the next of 32
+ * (bf16 inputs with fp32 outputs), 64 and 128, whose tensor-core work then includes
+ * the zero columns up to that width.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -65,6 +70,9 @@ typedef struct CUstream_st* fa_stream_t;
 
 typedef enum { FA_F32 = 0, FA_BF16 = 1 } fa_dtype;
 
+/* Tensor-core terms of the fp32-input path (see Precision above). */
+typedef enum { FA_F32_MMA_F16X2 = 0, FA_F32_MMA_TF32X3 = 1 } fa_f32_mma;
+
 typedef struct {
   int B;            /* batch size, >= 1 */
   int H;            /* query heads, >= 1 */
@@ -77,6 +85,9 @@ typedef struct {
   int window;       /* >= 0; 0 = no window, else key j visible only if j >= i - window + 1 */
   fa_dtype in_dtype;  /* dtype of Q, K, V, dO */
   fa_dtype out_dtype; /* dtype of O, dQ, dK, dV */
+  fa_f32_mma f32_mma; /* in_dtype FA_F32 only (a valid value is still required for bf16):
+                         FA_F32_MMA_F16X2 (0) or FA_F32_MMA_TF32X3 (D <= 64, else
+                         FA_ERR_UNSUPPORTED); a zero-initialised struct gets the first */
 } fa_params;
 
 typedef enum {
@@ -105,8 +116,8 @@ typedef enum {
  * again on a device after cudaDeviceReset() on that device, which invalidates that
  * state. The call validates its arguments synchronously, then enqueues
  * work on `stream` and returns without waiting. Temporary buffers (the scaled fp16
- * copy of V and its scale factors for bf16 inputs; hi/lo tf32 splits for fp32
- * inputs; for short query sequences, whose work items are fewer than the SMs, fp32
+ * copy of V and its scale factors for bf16 inputs; the hi/lo splits of Q, K, V for
+ * fp32 inputs; for short query sequences, whose work items are fewer than the SMs, fp32
  * partial O and LSE of up to 32 key ranges, combined in range order, so results stay
  * deterministic) are
  * taken stream-ordered from a library-owned CUDA memory pool and released on the
@@ -129,15 +140,16 @@ FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, fl
  * that runs where a cudaMalloc is not allowed or would block on a lock. For them
  * this entry point computes exactly what fa_fwd computes, with the same
  * arguments, rules and errors, but its scratch (the fp16 copy of V for bf16
- * inputs; the tf32 hi/lo splits of Q, K, V for fp32 inputs) lives in a
+ * inputs; the hi/lo splits of Q, K, V for fp32 inputs) lives in a
  * file-scope device array of FA_NOALLOC_SCRATCH_BYTES inside libfa.so. Every GPU
  * on which the library is loaded holds that array until the process exits.
  *   - A problem whose scratch would not fit returns FA_ERR_SCRATCH_LIMIT before
  *     anything is enqueued: bf16 inputs need round_up(B*HKV*Sk*D*2, 256) + 256 +
  *     32 * (the device's SM count) bytes (the fp16 copy of V, its scale factors and
- *     the conversion's partial maxima); fp32 inputs with D <= 64 need
- *     4*(2*B*H*Sq*D + 2*B*HKV*Sk*D + 2*B*HKV*D*round_up(Sk,4)) bytes, with D > 64
- *     2*(2*B*H*Sq*D + 4*B*HKV*Sk*D) + 256 + 96 * (SM count) bytes.
+ *     the conversion's partial maxima); fp32 inputs need
+ *     2*(2*B*H*Sq*D + 4*B*HKV*Sk*D) + 256 + 96 * (SM count) bytes with
+ *     FA_F32_MMA_F16X2 and 4*(2*B*H*Sq*D + 2*B*HKV*Sk*D + 2*B*HKV*D*round_up(Sk,4))
+ *     bytes with FA_F32_MMA_TF32X3.
  *   - The first call on each device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture begins.
@@ -164,7 +176,7 @@ FA_API unsigned long long fa_noalloc_scratch_bytes(void);
  * P is rebuilt tile by tile from LSE (never stored); D_i = rowsum(dO_i * O_i) is
  * computed first by a preprocess kernel; dK/dV are accumulated per key tile over
  * the grouped query heads without atomics (deterministic: two calls on the same
- * inputs give bit-identical results). Workspace (D_i, the scaled fp16 / tf32-split
+ * inputs give bit-identical results). Workspace (D_i, the scaled fp16 or hi/lo-split
  * operand copies and their scale factors; for short query sequences with bf16 inputs,
  * fp32 partial dQ of up to 32 key ranges, summed in range order) is stream-ordered
  * from the library pool. O must be the output of fa_fwd for the same inputs (the dS

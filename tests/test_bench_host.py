@@ -96,4 +96,6 @@ def test_roofline_denominator_is_the_burst_peak():
     # figure is their denominator, the power-capped sustained one is reported beside it
     peaks = {"bf16_tflops": 1965.9, "bf16_tflops_sustained": 1727.6, "hbm_gbs": 6795.1}
     assert bench.tensor_peaks(peaks, "bf16") == (1965.9, 1727.6)
-    assert bench.tensor_peaks(peaks, "f32") == (1965.9 / 2, 1727.6 / 2)
+    # fp32 inputs: two fp16 terms run at the kind::f16 rate, 3xTF32 at the tf32 rate
+    assert bench.tensor_peaks(peaks, "f32") == (1965.9, 1727.6)
+    assert bench.tensor_peaks(peaks, "f32", "tf32x3") == (1965.9 / 2, 1727.6 / 2)

@@ -102,6 +102,10 @@ MIS = 0x10008
     (dict(D=8), 2),
     (dict(D=144, in_dtype=0), 2),   # fp32 inputs up to D=128 too
     (dict(D=40, in_dtype=0), 2),
+    (dict(f32_mma=2), 1),           # not an fa_f32_mma value (checked for bf16 inputs too)
+    (dict(f32_mma=-1, in_dtype=0), 1),
+    (dict(D=80, in_dtype=0, f32_mma=1), 2),    # 3xTF32 up to D = 64 only
+    (dict(D=128, in_dtype=0, f32_mma=1), 2),
     # K and V of 2^59 bytes each: refused before any size is computed in size_t
     (dict(B=1024, H=1024, HKV=1024, Sq=1, Sk=1 << 30), 1),
 ])
@@ -160,3 +164,26 @@ def test_binding_fails_loudly_without_library(tmp_path):
     from attention_fa_fwd_02_gb300 import fa as fa_mod
     with pytest.raises(ImportError):
         fa_mod._load(str(tmp_path / "missing.so"))
+
+
+def test_params_struct_layout_matches_the_header(fa, tmp_path):
+    # the ctypes mirror of fa_params must have the C struct's size and field offsets
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc")
+    if cc is None:
+        pytest.skip("needs gcc")
+    names = [n for n, _ in fa.fa_params._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stddef.h>\n#include <stdio.h>\n#include \"fa.h\"\nint main(void) {\n"
+                   + f'  printf("%zu", sizeof(fa_params));\n'
+                   + "".join(f'  printf(" %zu", offsetof(fa_params, {n}));\n' for n in names)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([cc, "-I", os.path.join(root, "include"), str(src), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
+    want = [ctypes.sizeof(fa.fa_params)] + [getattr(fa.fa_params, n).offset for n in names]
+    assert got == want

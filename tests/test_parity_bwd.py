@@ -3,7 +3,7 @@
 The GPU path takes O and LSE from its own forward pass, exactly as a caller
 would; the oracle derives dQ / dK / dV from Q, K, V, dO alone through the softmax
 Jacobian. Tolerances (max-abs error / RMS of the oracle tensor): 5e-3 for fp32
-inputs (3xTF32 path), 2e-2 for bf16 inputs.
+inputs (either f32_mma), 2e-2 for bf16 inputs.
 """
 import numpy as np
 import pytest

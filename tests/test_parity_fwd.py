@@ -1,6 +1,6 @@
 """GPU parity of the forward pass (fa_fwd through the C ABI) against the fp64 oracle.
 
-Tolerances (from the problem statement): fp32 inputs (3xTF32 path) O <= 2e-3
+Tolerances (from the problem statement): fp32 inputs (either f32_mma) O <= 2e-3
 max-abs / RMS, LSE <= 1e-3 absolute; bf16 inputs O <= 2e-2, LSE <= 1e-2. The
 oracle runs on the same (bf16-rounded) inputs.
 """

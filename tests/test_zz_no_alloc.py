@@ -35,9 +35,9 @@ def fa():
     return m
 
 
-def _call(fa, entry, w, tensors):
+def _call(fa, entry, w, tensors, f32_mma="f16x2"):
     qd, kd, vd = tensors
-    p = fa.make_params(qd, kd, w.scale, w.causal, w.window)
+    p = fa.make_params(qd, kd, w.scale, w.causal, w.window, f32_mma=f32_mma)
     o = torch.empty(qd.shape, dtype=torch.float32, device=qd.device)
     lse = torch.empty(qd.shape[:3], dtype=torch.float32, device=qd.device)
     rc = entry(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(), p,
@@ -52,6 +52,9 @@ PAIRS = {
                                    seed=32)),
     "f32": (WORKLOADS["c2"].with_(B=1, H=2, HKV=2, Sq=500, Sk=500, seed=33),
             WORKLOADS["c5"].with_(Sq=300, Sk=450, seed=34)),
+    # the same pair through the 3xTF32 kernels (fa_params.f32_mma)
+    "f32-tf32x3": (WORKLOADS["c2"].with_(B=1, H=2, HKV=2, Sq=500, Sk=500, seed=33),
+                   WORKLOADS["c5"].with_(Sq=300, Sk=450, seed=34)),
     # fp32 at D = 128 (two scaled fp16 terms per operand)
     "f32-d128": (WORKLOADS["c2"].with_(B=1, H=2, HKV=1, Sq=400, Sk=400, D=128, scale=128 ** -0.5,
                                        seed=35),
@@ -62,12 +65,13 @@ PAIRS = {
 @pytest.mark.parametrize("kind", list(PAIRS))
 def test_noalloc_matches_oracle_and_fa_fwd_on_two_calls_in_a_row(fa, kind):
     ws = PAIRS[kind]
+    mode = "tf32x3" if kind.endswith("tf32x3") else "f16x2"
     cpu = [make_inputs(w)[:3] for w in ws]
     ins = [tuple(t.cuda() for t in c) for c in cpu]
     # two no-allocation calls back to back, the second on different data
-    got = [_call(fa, fa.fa_fwd_noalloc, w, t) for w, t in zip(ws, ins)]
+    got = [_call(fa, fa.fa_fwd_noalloc, w, t, mode) for w, t in zip(ws, ins)]
     fa.check_device_status()
-    ref = [_call(fa, fa.fa_fwd, w, t) for w, t in zip(ws, ins)]
+    ref = [_call(fa, fa.fa_fwd, w, t, mode) for w, t in zip(ws, ins)]
     fa.check_device_status()
     for w, c, (o, lse), (ro, rl) in zip(ws, cpu, got, ref):
         tol = TOL[w.dtype]
