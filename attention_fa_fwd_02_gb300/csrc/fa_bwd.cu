@@ -87,7 +87,8 @@ struct BwdCfg {
   static constexpr int ESZ = TF32 ? 4 : 2;
   static constexpr int ROW = 128 / ESZ;                 // elements per 128-byte row
   static constexpr int NCB = D / ROW;                   // 128-byte column blocks per row
-  static constexpr int CH = F32 ? 32 : 64;              // rows per streamed chunk
+  // rows per streamed chunk: 32 where K and V hi / lo (resident) leave room for no more
+  static constexpr int CH = (TF32 || (X16 && D > 64)) ? 32 : 64;
   static constexpr int NSPLIT = F32 ? 2 : 1;
   static constexpr uint32_t BIG_CB = 128u * 128u;       // column block of a 128-row tile
   static constexpr uint32_t SMALL_CB = CH * 128u;       // column block of a CH-row chunk
@@ -96,13 +97,13 @@ struct BwdCfg {
   static constexpr uint32_t T_TILE = TF32 ? D * 128u : 0u;  // transposed chunk: D rows x 32 fp32
   static constexpr uint32_t VEC_STAGE = 2 * CH * 4;        // lse2 + delta of one chunk
   // dkdv smem: K, V (hi[, lo]) | KV_NST x chunk (Q, dO [, Q^T, dO^T]) | KV_NST x vectors
-  static constexpr int KV_NST = TF32 ? 1 : (X16 ? 2 : 4);
+  static constexpr int KV_NST = TF32 ? 1 : ((X16 && D > 64) ? 2 : 4);
   static constexpr uint32_t KV_RES = 2 * NSPLIT * BIG_TILE;
   static constexpr uint32_t KV_STAGE = NSPLIT * (2 * SMALL_TILE + 2 * T_TILE);
   static constexpr uint32_t KV_VEC_OFF = KV_RES + KV_NST * KV_STAGE;
   static constexpr uint32_t KV_SMEM = KV_VEC_OFF + KV_NST * VEC_STAGE + 1024;
   // dq smem: Q, dO (hi[, lo]) | Q_NST x chunk (K, V [, K^T])
-  static constexpr int Q_NST = F32 ? 2 : 4;
+  static constexpr int Q_NST = (TF32 || (X16 && D > 64)) ? 2 : 4;
   static constexpr uint32_t Q_RES = 2 * NSPLIT * BIG_TILE;
   static constexpr uint32_t Q_STAGE = NSPLIT * (2 * SMALL_TILE + T_TILE);
   static constexpr uint32_t Q_SMEM = Q_RES + Q_NST * Q_STAGE + 1024;
@@ -113,21 +114,26 @@ struct BwdCfg {
   static constexpr int THREADS = 256;
   static constexpr int MMA_WARP = 4, ACC_WARP = 5, TMA_WARP = 6;
   static constexpr uint32_t TMEM_COLS = 512;
-  // TMEM slots: S | dP | P_lo | dS_lo, CH columns each (fp32 P / dS hi overwrite
-  // S / dP; fp16 P / dS take the first CH/2 columns of S / dP). A ring of slots
+  // TMEM slots: S | dP | P_lo | dS_lo, CH columns each (3xTF32: fp32 P / dS hi
+  // overwrite S / dP), or S | dP (X16: fp16 P / dS hi in the first CH/2 columns of
+  // S / dP, lo in the other CH/2), CH columns each. A ring of slots
   // lets the tensor core score chunk c+1.. while the softmax works on chunk c:
   // dkdv has room for two slots next to its dV and dK accumulators, dq for three.
   static constexpr int KV_NSLOT = 2, Q_NSLOT = 3;
   __host__ __device__ static constexpr uint32_t s_col(int b) { return 128u * b; }
   __host__ __device__ static constexpr uint32_t dp_col(int b) { return 128u * b + CH; }
-  __host__ __device__ static constexpr uint32_t plo_col(int b) { return 128u * b + 2 * CH; }
-  __host__ __device__ static constexpr uint32_t dslo_col(int b) { return 128u * b + 3 * CH; }
+  __host__ __device__ static constexpr uint32_t plo_col(int b) {
+    return X16 ? 128u * b + CH / 2 : 128u * b + 2 * CH;
+  }
+  __host__ __device__ static constexpr uint32_t dslo_col(int b) {
+    return X16 ? 128u * b + CH + CH / 2 : 128u * b + 3 * CH;
+  }
   static constexpr uint32_t KV_ACC0 = 128 * KV_NSLOT;      // dV (dkdv)
   static constexpr uint32_t KV_ACC1 = 128 * KV_NSLOT + D;  // dK (dkdv)
   static constexpr uint32_t Q_ACC = 128 * Q_NSLOT;         // dQ (dq)
   // (bf16 inputs use the Dkv16Cfg / Dq16Cfg kernels; these layouts are the fp32 kernels')
   static_assert(!F32 || (KV_SMEM <= 227u * 1024u && Q_SMEM <= 227u * 1024u), "shared memory budget");
-  static_assert((F32 ? 4 * CH : 2 * CH) <= 128, "TMEM slot width");
+  static_assert((TF32 ? 4 * CH : 2 * CH) <= 128, "TMEM slot width");
   static_assert(KV_ACC1 + D <= TMEM_COLS && Q_ACC + D <= TMEM_COLS, "TMEM budget");
   // Epilogues stage each warp's rows from the start of shared memory (every operand
   // buffer is spent by then): dV and dK side by side (dkdv), dQ (dq).
@@ -254,18 +260,22 @@ __device__ __forceinline__ void tmem_ld_pair(uint32_t sa, uint32_t da, float (&x
 template <class C>
 __device__ __forceinline__ void tmem_st_operand(uint32_t hi, uint32_t lo, const float (&x)[C::CH]) {
   if constexpr (C::X16) {
-    // fp16 pairs: hi = fp16(x) into the first CH / 2 columns at `hi`, lo = fp16(x - hi) at `lo`
-    static_assert(C::CH == 32, "16 packed columns per term");
-    uint32_t ph[16], pl[16];
+    // fp16 pairs: hi = fp16(x) into CH / 2 columns at `hi`, lo = fp16(x - hi) at `lo`
+    static_assert(C::CH % 32 == 0, "16 packed columns per store");
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const __half2 h = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
-      const float2 hf = __half22float2(h);
-      ph[k] = *reinterpret_cast<const uint32_t*>(&h);
-      pl[k] = pack_half2(x[2 * k] - hf.x, x[2 * k + 1] - hf.y);
+    for (int c = 0; c < C::CH / 32; ++c) {
+      uint32_t ph[16], pl[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float x0 = x[c * 32 + 2 * k], x1 = x[c * 32 + 2 * k + 1];
+        const __half2 h = __floats2half2_rn(x0, x1);
+        const float2 hf = __half22float2(h);
+        ph[k] = *reinterpret_cast<const uint32_t*>(&h);
+        pl[k] = pack_half2(x0 - hf.x, x1 - hf.y);
+      }
+      tmem_st16(hi + c * 16, ph);
+      tmem_st16(lo + c * 16, pl);
     }
-    tmem_st16(hi, ph);
-    tmem_st16(lo, pl);
   } else if constexpr (!C::F32) {
 #pragma unroll
     for (int c = 0; c < C::CH / 64; ++c) {
