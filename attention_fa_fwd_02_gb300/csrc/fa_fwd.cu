@@ -55,7 +55,7 @@ struct FwdArgs {
   const OperandScales* sc;  // bf16 inputs: o_mul = 2^-eV undoes the scaled fp16 copy of V
 };
 
-template <int D_, int PREC>
+template <int D_, int PREC, int NQ_ = 0>
 struct FwdCfg {
   static constexpr int D = D_;
   static constexpr bool F32 = PREC != IN_BF16;
@@ -65,7 +65,10 @@ struct FwdCfg {
   static constexpr bool X16 = PREC == IN_F32_X16;
   static constexpr bool TF32 = PREC == IN_F32_TF32;
   static_assert(!TF32 || D <= 64, "3xTF32 tiles up to D = 64");
-  static constexpr int NQ = F32 ? 1 : 2;                   // query tiles per CTA
+  // query tiles per item: two (their softmaxes alternate with each other's MMAs) where
+  // the operand tiles leave room for them, unless NQ_ asks for one
+  static constexpr int NQ = (TF32 || (X16 && D > 64) || NQ_ == 1) ? 1 : 2;
+  static_assert(F32 || NQ == 2, "bf16 items hold two query tiles");
   static constexpr int ESZ = TF32 ? 4 : 2;                 // operand bytes in smem
   // smem rows of RB bytes with the swizzle of that width: 128, or 64 for bf16 at D = 32
   static constexpr int RB = F32 ? 128 : tile_row_bytes(D);
@@ -77,8 +80,8 @@ struct FwdCfg {
   static constexpr uint32_t TILE_BYTES = NCB * CB_BYTES;   // a 128 x D operand tile
   static constexpr uint32_t VT_CB_BYTES = D * 128u;        // fp32 V^T: 32 keys x D rows
   static constexpr int NSPLIT = F32 ? 2 : 1;               // hi / lo copies
-  static constexpr int KST = F32 ? 1 : (D == 128 ? 2 : 3); // K ring depth
-  static constexpr int VST = F32 ? 1 : 3;                  // V ring depth
+  static constexpr int KST = NQ == 1 ? 1 : ((D == 128 || X16) ? 2 : 3);  // K ring depth
+  static constexpr int VST = NQ == 1 ? 1 : 3;                             // V ring depth
   // a V ring stage also stages an epilogue: at least one 32 x 128-byte box per warp
   static constexpr uint32_t V_STAGE =
       NSPLIT * TILE_BYTES > 4 * EPI_BOX_BYTES ? NSPLIT * TILE_BYTES : 4 * EPI_BOX_BYTES;
@@ -259,13 +262,13 @@ __device__ __forceinline__ void issue_v_load(uint8_t* smem, int it, int t, int b
 // order. Where one key takes almost all of a row's weight, one fp16 term (11
 // significant bits) puts an error in O that the backward's D_i = dO_i . O_i then
 // passes on to dS at exactly the dominant keys.
-template <int D, int F32, bool HP, bool PSPLIT>
-__global__ void __launch_bounds__(FwdCfg<D, F32>::THREADS, 1)
+template <int D, int F32, bool HP, bool PSPLIT, int NQ_ = 0>
+__global__ void __launch_bounds__(FwdCfg<D, F32, NQ_>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKlo,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmVlo,
                   const __grid_constant__ CUtensorMap tmO, const FwdArgs a) {
-  using C = FwdCfg<D, F32>;
+  using C = FwdCfg<D, F32, NQ_>;
   constexpr int NQ = C::NQ, KST = C::KST, VST = C::VST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -990,21 +993,23 @@ bool prep_x16_fwd(void* ws, const void* Q, const void* K, const void* V, const f
 }
 
 // The forward kernel instantiation: head-pair items (two-tile kernels only) or not;
-// two-term P (bf16 inputs) or not.
-template <int D, int F32>
+// two-term P (bf16 inputs; fp32 inputs always carry P as two terms) or not.
+template <int D, int F32, int NQ_ = 0>
 auto fwd_kernel_for(bool hp, bool psplit) {
-  auto kern = fa_fwd_kernel<D, F32, false, false>;
-  if constexpr (FwdCfg<D, F32>::NQ == 2) {
-    if (hp) kern = psplit ? fa_fwd_kernel<D, F32, true, true> : fa_fwd_kernel<D, F32, true, false>;
-    else if (psplit) kern = fa_fwd_kernel<D, F32, false, true>;
+  auto kern = fa_fwd_kernel<D, F32, false, false, NQ_>;
+  if constexpr (FwdCfg<D, F32, NQ_>::NQ == 2) {
+    if (hp) kern = fa_fwd_kernel<D, F32, true, false, NQ_>;
+    if constexpr (F32 == IN_BF16) {
+      if (psplit) kern = hp ? fa_fwd_kernel<D, F32, true, true, NQ_> : fa_fwd_kernel<D, F32, false, true, NQ_>;
+    }
   }
   return kern;
 }
 
-template <int D, int F32>
+template <int D, int F32, int NQ_ = 0>
 fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                   const fa_params& p, cudaStream_t stream) {
-  using C = FwdCfg<D, F32>;
+  using C = FwdCfg<D, F32, NQ_>;
   const int Dv = p.D;
   const size_t nq = (size_t)p.B * p.H * p.Sq * Dv;
   const size_t nk = (size_t)p.B * p.HKV * p.Sk * Dv;
@@ -1127,7 +1132,7 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   const unsigned grid = (unsigned)std::min(a.n_items, sms);
   // two-term P for the shapes whose backward takes two-term P / dS (see split_operands)
   const bool psplit = !F32 && split_operands(p.H / p.HKV, (p.Sq + BLOCK_M - 1) / BLOCK_M);
-  auto kern = fwd_kernel_for<D, F32>(hp, psplit);
+  auto kern = fwd_kernel_for<D, F32, NQ_>(hp, psplit);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_ALLOC);
   if (e == cudaSuccess) {
@@ -1173,7 +1178,16 @@ fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float
   } else if (p.f32_mma == FA_F32_MMA_TF32X3) {
     if (p.D <= 64) return run_fwd<64, IN_F32_TF32>(Q, K, V, O, LSE, p, stream);
   } else {
-    if (p.D <= 64) return run_fwd<64, IN_F32_X16>(Q, K, V, O, LSE, p, stream);
+    if (p.D <= 64) {
+      // two query tiles per item, unless that leaves SMs idle which one tile per item
+      // would fill: key ranges split items only where the keys are long
+      const int sms = host::sm_count(), n_qt = (p.Sq + BLOCK_M - 1) / BLOCK_M;
+      const int n_kt = (p.Sk + BLOCK_N - 1) / BLOCK_N;
+      const long long bh = (long long)p.B * p.H, items1 = bh * n_qt, items2 = bh * ((n_qt + 1) / 2);
+      const bool one = items2 < sms && (items1 >= sms || key_range_tiles((int)items2, n_kt, sms) == n_kt);
+      return one ? run_fwd<64, IN_F32_X16, 1>(Q, K, V, O, LSE, p, stream)
+                 : run_fwd<64, IN_F32_X16>(Q, K, V, O, LSE, p, stream);
+    }
     if (p.D <= 128) return run_fwd<128, IN_F32_X16>(Q, K, V, O, LSE, p, stream);
   }
   return FA_ERR_UNSUPPORTED;

@@ -58,6 +58,11 @@ SMALL = {
     "bf16-decode-d96": C3.with_(B=1, H=4, HKV=1, Sq=32, Sk=4000, D=96, causal=False,
                                 scale=96 ** -0.5, seed=53),
     "f32-decode": C5.with_(Sq=100, Sk=4000, seed=54),
+    # fp32 at D <= 64 with few items and long keys: two query tiles per item (two row
+    # tiles of one head; two heads of one kv head), keys split into ranges
+    "f32-two-tile-causal-ragged": C2.with_(B=1, H=2, HKV=1, Sq=700, Sk=2100, seed=91),
+    "f32-two-tile-head-pairs-window": C2.with_(B=1, H=4, HKV=2, Sq=300, Sk=2500, window=700,
+                                               causal=False, seed=92),
     # window ending before the keys do, with the dQ keys split into ranges: tile 10
     # sees only the last range, tile 11 no key at all (its dQ rows must come out 0)
     "bf16-decode-window-empty-tail": C4.with_(B=1, H=4, HKV=1, Sq=1500, Sk=1200, window=100,
