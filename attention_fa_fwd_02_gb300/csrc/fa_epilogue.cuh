@@ -26,8 +26,11 @@ constexpr uint32_t epi_warp_bytes() {
 // Rows r_base .. r_base + 31 of slab z: columns [0, D) of the fp32 accumulator at
 // TMEM address t_addr (this warp's lane base), times mul, in the output type of
 // the tensor map `tm` (fp32, or bf16 when OUT_BF16). `stage` (1024-byte aligned)
-// holds BOXES boxes; with fewer boxes than the row needs, the warp waits for the
-// previous stores to have read the staging area before refilling it. have == false
+// holds BOXES boxes, used as a ring: each box is stored (its own bulk group) as soon
+// as it is written, and a slot is refilled once the store that last used it has read
+// it, so staging the next box overlaps the copy engine reading the previous ones (the
+// reads complete in commit order; waiting until at most BOXES - 1 groups are unread
+// frees the oldest slot, counting this thread's earlier groups too). have == false
 // writes zeros (no accumulator). any_row == false skips the stores (all rows are
 // past the tensor's end). With WAIT, the stores have read their shared-memory
 // sources on return (the global writes complete on their own, before the kernel
@@ -50,8 +53,8 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tm, uint32_t t
 #pragma unroll
   for (int b = 0; b < NBOX; ++b) {
     const int slot = b % BOXES;
-    if (slot == 0 && b > 0) {
-      if (lane == 0) bulk_wait_read_all();
+    if (b >= BOXES) {
+      if (lane == 0) bulk_wait_read<BOXES - 1>();
       __syncwarp();
     }
     const uint32_t row = stage + slot * EPI_BOX_BYTES + lane * 128u;
@@ -91,15 +94,12 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tm, uint32_t t
         st_shared_v4(row + ((c ^ sw) << 4), w[0], w[1], w[2], w[3]);
       }
     }
-    if (slot == BOXES - 1 || b == NBOX - 1) {
-      fence_async_shared();
-      __syncwarp();
-      if (lane == 0 && any_row) {
-        for (int j = b - slot; j <= b; ++j)
-          if (x0 + j * COLS < x_end)
-            tma_store_3d(tm, stage + (j % BOXES) * EPI_BOX_BYTES, x0 + j * COLS, r_base, z);
-        bulk_commit_group();
-      }
+    fence_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      if (any_row && x0 + b * COLS < x_end)
+        tma_store_3d(tm, stage + slot * EPI_BOX_BYTES, x0 + b * COLS, r_base, z);
+      bulk_commit_group();  // (an empty group where nothing was stored keeps the count)
     }
   }
   if constexpr (WAIT) {
