@@ -461,7 +461,8 @@ def run_ours(args, rank, world, local_rank):
     achieved = per_kernel[dom]["tflops"]
     traffic = (committed_traffic(dom_base, args.workload)
                if w.D == WORKLOADS_D[args.workload] and args.out_dtype == "f32" and not args.sq
-               and not args.non_causal else None)
+               and not args.non_causal and args.f32_mma == "f16x2" and args.bwd == "recompute"
+               else None)
     cpu = None
     if not args.no_cpu_baseline:
         # every kv group of batch element 0: ~10 s of oracle work on the 16 host cores at C3
