@@ -19,7 +19,8 @@
 //                S^T = K Q^T and dP^T = V dO^T into a double-buffered TMEM slot,
 //                softmax warps turn them into P^T and dS^T (back into TMEM),
 //                then dV += P^T dO and dK += dS^T Q accumulate in TMEM.
-//   dq           one CTA per (batch, head, 128-query tile), CH-key chunks:
+//   dq           per (batch, head, 128-query tile) -- for bf16 inputs a work item of
+//                a persistent CTA, for fp32 inputs one CTA -- CH-key chunks:
 //                S = Q K^T, dP = dO V^T, dS = P (dP - D), dQ += dS K.
 // While the softmax warps work on chunk c, the tensor core computes chunk c+1.
 // For fp32 inputs every product is the three-term sum a_hi b_hi + a_hi b_lo + a_lo b_hi,
@@ -770,7 +771,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
 }
 
 // --------------------------------------------------------- dQ, fp16 operands
-// bf16 inputs: one CTA per (batch, head, 128-query tile), 128-key chunks, so the
+// bf16 inputs: work item = (batch, head, 128-query tile), 128-key chunks, so the
 // score MMAs are 128 x 128 (a 128 x 64 MMA reads 3/4 of the shared-memory bytes of a
 // 128 x 128 one for half the work, and the dq kernel is bound by those reads).
 // TMEM: S slot [0, 128), dP slot [128, 256), two fp16 dS operand slots of 64
@@ -1299,8 +1300,9 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
 }
 
 // ------------------------------------------------------ dK / dV, fp16 operands
-// bf16 inputs: one CTA per (batch, kv head, 128-key tile), 128-query chunks of every
-// grouped query head that can see the tile, so the score MMAs are 128 x 128.
+// bf16 inputs: work item = (batch, kv head, 128-key tile), walked by persistent CTAs
+// (one per SM); an item takes the 128-query chunks of every grouped query head that can
+// see the tile, so the score MMAs are 128 x 128.
 // TMEM: S^T slot [0, 128), dP^T slot [128, 256), dV, dK accumulators after them.
 // Three issuers (a thread's MMAs run in issue order; an issuer stalls while the
 // tensor pipe is full, so independent streams get their own thread):
@@ -1310,7 +1312,8 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
 //              by the softmax into the first half of each 64-column half of its
 //              slot, so dP^T(c+1) may overwrite the slot right after dK(c) is issued.
 // P^T lives in shared memory so that the next score tile can enter the tensor pipe
-// while the softmax is still exponentiating.
+// while the softmax is still exponentiating (in the S^T slot, which would make dV a TS
+// product, S^T(c + 1) had to wait for dV(c): 11% slower at C3).
 //
 // SPLIT (short query sequences, where a few keys can take almost all of a row's
 // weight and this kernel is bound by per-CTA set-up rather than by the tensor pipe):
