@@ -108,4 +108,80 @@ __device__ __forceinline__ void store_rows_tma(const CUtensorMap* tm, uint32_t t
   }
 }
 
+// The same rows written by the warp itself instead of by tensor stores: each 32 x
+// 128-byte box is staged in `stage` (one box, 1024-byte aligned, this warp's alone) in
+// the swizzled layout, read back four rows per instruction (thread t: row t / 8, 16-byte
+// chunk t % 8) and written with coalesced 16-byte global stores, four whole 128-byte
+// lines per instruction. Nothing waits on the copy engine: the box is free again once
+// the warp's own shared loads returned. `out` is the [z][rows][x_end] tensor of the
+// output type; rows at or past `rows` and columns at or past x_end are not written.
+template <int D, bool OUT_BF16>
+__device__ __forceinline__ void store_rows_direct(void* out, uint32_t t_addr, bool have, float mul,
+                                                  uint32_t stage, int r_base, int rows, int z,
+                                                  int x_end) {
+  using namespace ptx;
+  constexpr int COLS = OUT_BF16 ? 64 : 32;  // output columns per 128-byte box row
+  constexpr int NBOX = D / COLS;
+  constexpr int ESZ = OUT_BF16 ? 2 : 4;
+  const uint32_t lane = lane_id();
+  const uint32_t sw = lane & 7u;
+  const uint32_t row = stage + lane * 128u;
+  const int rr = (int)(lane >> 3), ch = (int)(lane & 7u);  // read-back: row rr + 4 i, chunk ch
+#pragma unroll
+  for (int b = 0; b < NBOX; ++b) {
+    if (b * COLS >= x_end) break;
+    if constexpr (!OUT_BF16) {
+      uint32_t r[32];
+      if (have) {
+        tmem_ld32(t_addr + b * 32, r);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = 0u;
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(row + ((c ^ sw) << 4), __float_as_uint(__uint_as_float(r[4 * c]) * mul),
+                     __float_as_uint(__uint_as_float(r[4 * c + 1]) * mul),
+                     __float_as_uint(__uint_as_float(r[4 * c + 2]) * mul),
+                     __float_as_uint(__uint_as_float(r[4 * c + 3]) * mul));
+    } else {
+      uint32_t r0[32], r1[32];
+      if (have) {
+        tmem_ld32x2(t_addr + b * 64, t_addr + b * 64 + 32, r0, r1);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r0[k] = r1[k] = 0u;
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = (c % 4) * 8 + 2 * e;
+          const float x0 = __uint_as_float(c < 4 ? r0[k] : r1[k]) * mul;
+          const float x1 = __uint_as_float(c < 4 ? r0[k + 1] : r1[k + 1]) * mul;
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(x0, x1);
+          w[e] = *reinterpret_cast<uint32_t*>(&v2);
+        }
+        st_shared_v4(row + ((c ^ sw) << 4), w[0], w[1], w[2], w[3]);
+      }
+    }
+    __syncwarp();
+    const int col = b * COLS + ch * (16 / ESZ);  // first output column of this thread's chunk
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rl = rr + 4 * i;  // row of the box this thread reads
+      const float4 v = ld_shared_v4(stage + (uint32_t)rl * 128u + (((uint32_t)ch ^ ((uint32_t)rl & 7u)) << 4));
+      const int grow = r_base + rl;
+      if (grow < rows && col < x_end) {
+        char* dst = static_cast<char*>(out) + (((size_t)z * rows + grow) * x_end + col) * ESZ;
+        *reinterpret_cast<float4*>(dst) = v;
+      }
+    }
+    __syncwarp();  // the box is read back: the next one may overwrite it
+  }
+  // the staging writes ordered before later copy-engine writes into the same stage
+  fence_async_shared();
+}
+
 }  // namespace fa

@@ -82,9 +82,11 @@ struct FwdCfg {
   static constexpr int NSPLIT = F32 ? 2 : 1;               // hi / lo copies
   static constexpr int KST = NQ == 1 ? 1 : ((D == 128 || X16) ? 2 : 3);  // K ring depth
   static constexpr int VST = NQ == 1 ? 1 : 3;                             // V ring depth
-  // a V ring stage also stages an epilogue: at least one 32 x 128-byte box per warp
-  static constexpr uint32_t V_STAGE =
-      NSPLIT * TILE_BYTES > 4 * EPI_BOX_BYTES ? NSPLIT * TILE_BYTES : 4 * EPI_BOX_BYTES;
+  // a V ring stage also stages an item's epilogue, the NQ tiles side by side: at least
+  // one 32 x 128-byte box per warp of each tile
+  static constexpr uint32_t V_STAGE = NSPLIT * TILE_BYTES > 4 * NQ * EPI_BOX_BYTES
+                                          ? NSPLIT * TILE_BYTES
+                                          : 4 * NQ * EPI_BOX_BYTES;
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t K_OFF = Q_OFF + NQ * NSPLIT * TILE_BYTES;
   static constexpr uint32_t V_OFF = K_OFF + KST * NSPLIT * TILE_BYTES;
@@ -98,9 +100,11 @@ struct FwdCfg {
   static constexpr int V_WARP = SOFTMAX_WARPS + 2;
   static constexpr int RELAY_WARP = SOFTMAX_WARPS + 3;  // relays load completions to the issuer
   // named barriers: 1 + q = P_q written (softmax -> issuer), RELAY_BAR = operands
-  // loaded (relay -> issuer), EPI_BAR0 + q = the four warps of tile q (epilogue)
+  // loaded (relay -> issuer), EPI_BAR0 + q = the four warps of tile q (epilogue),
+  // EPI_JOIN = every tile's epilogue stores have read their part of the stage
   static constexpr uint32_t RELAY_BAR = 3;
   static constexpr uint32_t EPI_BAR0 = 4;
+  static constexpr uint32_t EPI_JOIN = 6;
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 4);
   // Register split for NQ = 2 (launched at 168 per thread for 384 threads): the
   // softmax warpgroups hold a whole 128-column S row in registers.
@@ -113,8 +117,9 @@ struct FwdCfg {
   __host__ __device__ static constexpr uint32_t o_col(int q) { return 256u + (uint32_t)D * q; }
   static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory budget");
   static_assert(F32 ? (256 + D <= 512) : (256 + 2 * D <= 512), "TMEM budget");
-  // Epilogue: each softmax warp stages its 32 O rows in its quarter of a V ring stage.
-  static constexpr uint32_t STAGE_PER_WARP = V_STAGE / 4;
+  // Epilogue: each softmax warp stages its 32 O rows in its share of the tile's part
+  // (1 / NQ) of a V ring stage.
+  static constexpr uint32_t STAGE_PER_WARP = V_STAGE / (4 * NQ);
   static constexpr int STAGE_BOXES = (int)(STAGE_PER_WARP / EPI_BOX_BYTES);
   static_assert(STAGE_BOXES >= 1 && STAGE_PER_WARP % 1024 == 0, "O staging layout");
 };
@@ -421,9 +426,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F32, NQ_>::THREADS, 1)
     // every use in position order and is the only waiter on the empty barriers, so
     // it sees every release of a stage in order (seen[] counts them) and no parity
     // wait can skip a phase. Key tiles complete on the full barriers (only loads
-    // count there); the epilogue stage goes to query tile 0 on its grant barrier (one
-    // phase per item, only after the previous epilogue stage was released), and tile
-    // q hands it to tile q + 1 on the next grant barrier once its stores have read it.
+    // count there); the epilogue stage goes to every query tile at once on the tiles'
+    // grant barriers (one phase per item, only after the previous epilogue stage was
+    // released), each tile staging through its own 1 / NQ of it, and the last tile
+    // releases it once every tile's stores have read their part (EPI_JOIN).
     if (lane == 0) {
       uint32_t pos = 0;
       int seen[VST], loads[VST];  // releases seen, copies issued, per stage
@@ -449,7 +455,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32, NQ_>::THREADS, 1)
         if (!ok) break;
         if (pos >= (uint32_t)VST && !(ok = wait_release(pos - VST))) break;
         if (prev_stage >= 0 && !(ok = wait_release((uint32_t)prev_stage))) break;
-        mbar_arrive(&bar_grant[0]);
+        for (int q = 0; q < NQ; ++q) mbar_arrive(&bar_grant[q]);
         prev_stage = (int)pos;
         ++pos;
       }
@@ -594,14 +600,15 @@ __global__ void __launch_bounds__(FwdCfg<D, F32, NQ_>::THREADS, 1)
     int g = 0, j = 0;
     uint32_t pos = 0;
     // The last tile's epilogue gives the stage back to the V ring once its TMA stores
-    // have read it: checked after this warpgroup's next hand-off, so the wait for the
-    // stores does not delay the next P.
+    // and those of the other tiles (EPI_JOIN) have read it: checked after this
+    // warpgroup's next hand-off, so the wait for the stores does not delay the next P.
     bool pending = false;
     int pend_slot = 0;
     auto release = [&]() {
       if (lane == 0) bulk_wait_read_all();
       __syncwarp();
-      named_bar_sync(C::EPI_BAR0 + q, 128);
+      if constexpr (NQ == 1) named_bar_sync(C::EPI_BAR0 + q, 128);
+      else named_bar_sync(C::EPI_JOIN, 128 * NQ);
       if (wq == 0 && lane == 0) mbar_arrive(&bar_vempty[pend_slot]);
       pending = false;
     };
@@ -732,39 +739,34 @@ __global__ void __launch_bounds__(FwdCfg<D, F32, NQ_>::THREADS, 1)
         ++j;
       }
       if (pending) release();
-      // ---- epilogue: LSE, and O = acc / l staged in the item's V ring stage (tile 0
-      // gets it from the V producer, tile q + 1 from tile q once q's stores have read
-      // it), TMA stores.
+      // ---- epilogue: LSE, and O = acc / l staged in this tile's part of the item's V
+      // ring stage (granted to every tile by the V producer), TMA stores.
       const int slot = pos % VST;
       if (ok) ok = __all_sync(0xffffffffu, wait(&bar_grant[q], k & 1));
       const float inv = (l > 0.f) ? (o_mul / l) : 0.f;
       if (ok && i < a.Sq)
         a.LSE[(size_t)zo * a.Sq + i] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
       const int r_base = r0 + wq * 32;
-      const uint32_t stage = sV(slot, 0) + wq * C::STAGE_PER_WARP;
+      const uint32_t stage = sV(slot, 0) + (uint32_t)q * (C::V_STAGE / NQ) + wq * C::STAGE_PER_WARP;
       // (bf16 outputs: 64-column boxes, so D >= 64 kernels only; the host routes
       // bf16 outputs at smaller head dims to the D = 64 kernels)
       constexpr bool BF_OUT = D >= 64;
+      // O rows staged box by box in this warp's share of the stage and written by the
+      // warp itself (coalesced 16-byte stores): the share is free again when the call
+      // returns, no copy-engine read to wait for
+      if (ok) {
+        if (BF_OUT && a.out_bf16)
+          store_rows_direct<D, BF_OUT>(a.O, o_addr, n > 0, inv, stage, r_base, a.Sq, zo, a.Dv);
+        else
+          store_rows_direct<D, false>(a.O, o_addr, n > 0, inv, stage, r_base, a.Sq, zo, a.Dv);
+      }
       if (q < NQ - 1) {
-        if (ok) {
-          if (BF_OUT && a.out_bf16)
-            store_rows_tma<D, BF_OUT, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                       r_base < a.Sq, zo, 0, a.Dv);
-          else
-            store_rows_tma<D, false, C::STAGE_BOXES>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                      r_base < a.Sq, zo, 0, a.Dv);
-        }
-        named_bar_sync(C::EPI_BAR0 + q, 128);
-        if (wq == 0 && lane == 0) mbar_arrive(&bar_grant[q + 1]);
+        // this tile is done with its part: the last tile may release the stage. (After
+        // an abort a sync, so that this tile cannot arrive for the next item before the
+        // last tile's release has taken this generation.)
+        if (ok) named_bar_arrive(C::EPI_JOIN, 128 * NQ);
+        else named_bar_sync(C::EPI_JOIN, 128 * NQ);
       } else {
-        if (ok) {
-          if (BF_OUT && a.out_bf16)
-            store_rows_tma<D, BF_OUT, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage, r_base,
-                                                              r_base < a.Sq, zo, 0, a.Dv);
-          else
-            store_rows_tma<D, false, C::STAGE_BOXES, false>(&tmO, o_addr, n > 0, inv, stage,
-                                                             r_base, r_base < a.Sq, zo, 0, a.Dv);
-        }
         pending = true;
         pend_slot = slot;
       }

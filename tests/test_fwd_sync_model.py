@@ -17,9 +17,12 @@ kernel's order -- under random interleavings and checks that
     has to read, and the epilogue reads each O accumulator before it is reused.
 
 Item lists mix items with no key, one key tile and several, as the causal /
-windowed schedules do. The model must follow fa_fwd_kernel: a change to the
-kernel's hand-offs has to be made here too. Two planted faults (the races above,
-put back into the model) must be caught.
+windowed schedules do. An item's epilogue stage goes to all its query tiles at once,
+each staging through its own part; the last tile releases it after the others have
+announced (EPI_JOIN) that their stores read their parts. The model must follow
+fa_fwd_kernel: a change to the kernel's hand-offs has to be made here too. Three
+planted faults (the races above, put back into the model, and a tile announcing its
+part before its stores read it) must be caught.
 """
 import random
 
@@ -82,7 +85,7 @@ class NamedBarrier:
 
 
 def run_protocol(items, NQ, KST, VST, seed, relay_observes_first_k=True,
-                 release_after_reads=True):
+                 release_after_reads=True, join_after_reads=True):
     """Play one CTA's item list; raises ProtocolError on any violation."""
     rnd = random.Random(seed)
     mb = {}
@@ -121,8 +124,8 @@ def run_protocol(items, NQ, KST, VST, seed, relay_observes_first_k=True,
             return True
         if c[0] == "V":
             return consumed.get(c[1], 0) == NQ
-        if c[0] == "STAGING":
-            return ("st", c[1], c[2]) not in stores
+        if c[0] == "STAGING":  # an item's epilogue: every tile's stores must have read it
+            return all(("st", c[1], q) not in stores for q in range(NQ))
         return False
 
     def load_q(q, item):
@@ -221,7 +224,8 @@ def run_protocol(items, NQ, KST, VST, seed, relay_observes_first_k=True,
                 yield from wait_release(prev_stage)
             if not v_stage_free(pos % VST):
                 raise ProtocolError(f"epilogue stage granted while busy: {smem_v[pos % VST]}")
-            M(("grant", 0)).arrive()
+            for q in range(NQ):  # every tile at once, each staging through its own part
+                M(("grant", q)).arrive()
             prev_stage = pos
             pos += 1
 
@@ -313,7 +317,8 @@ def run_protocol(items, NQ, KST, VST, seed, relay_observes_first_k=True,
             tag = pending["tag"]
             if release_after_reads:
                 yield (lambda tag=tag: tag not in stores)
-            yield from nsync(("epi", q), f"softmax{q}", 128, 128)
+            # every tile's stores have read their part (the other tiles arrive on the join)
+            yield from nsync(("join",), f"softmax{q}", 128, 128 * NQ)
             M(("vempty", pending["slot"])).arrive()
             pending["on"] = False
 
@@ -339,23 +344,22 @@ def run_protocol(items, NQ, KST, VST, seed, relay_observes_first_k=True,
                 yield from release()
             slot = pos % VST
             yield (lambda k=k: M(("grant", q)).passed(k & 1))
-            if q == 0 and not v_stage_free(slot):
-                raise ProtocolError(f"staging into a busy stage: {smem_v[slot]}")
-            if q > 0 and (smem_v[slot] != ("STAGING", k, q - 1) or ("st", k, q - 1) in stores):
-                raise ProtocolError("stage handed over before the previous tile's stores read it")
-            smem_v[slot] = ("STAGING", k, q)
+            if smem_v[slot] != ("STAGING", k):  # the first tile to start its stores
+                if not v_stage_free(slot):
+                    raise ProtocolError(f"staging into a busy stage: {smem_v[slot]}")
+                smem_v[slot] = ("STAGING", k)
             tag = ("st", k, q)
             stores.add(tag)
 
-            def store_read(slot=slot, k=k, q=q, tag=tag):
-                if smem_v[slot] != ("STAGING", k, q):
+            def store_read(slot=slot, k=k, tag=tag):
+                if smem_v[slot] != ("STAGING", k):
                     raise ProtocolError(f"TMA store read an overwritten stage: {smem_v[slot]}")
                 stores.discard(tag)
             tma(store_read)
-            if q < NQ - 1:  # hand the stage on once the stores have read it
-                yield (lambda tag=tag: tag not in stores)
-                yield from nsync(("epi", q), f"softmax{q}", 128, 128)
-                M(("grant", q + 1)).arrive()
+            if q < NQ - 1:  # its part has been read: the last tile may release the stage
+                if join_after_reads:
+                    yield (lambda tag=tag: tag not in stores)
+                N(("join",)).arrive(f"softmax{q}", 128, 128 * NQ)
             else:
                 pending.update(on=True, slot=slot, tag=tag)
             yield None
@@ -424,3 +428,9 @@ def test_planted_fault_relay_skips_first_k_is_caught():
 def test_planted_fault_early_stage_release_is_caught():
     # giving the epilogue stage back before its TMA stores read it
     assert _caught((2, 2, 3), 3000, release_after_reads=False)
+
+
+def test_planted_fault_join_before_the_stores_read_is_caught():
+    # a tile that announces its part as read before its stores have read it lets the
+    # last tile release the stage while those stores may still read it
+    assert _caught((2, 2, 3), 400, join_after_reads=False)
