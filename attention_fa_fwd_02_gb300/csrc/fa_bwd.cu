@@ -515,9 +515,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
         const int k_hi = min(a.window > 0 ? j + a.window - 1 - i0 : INT_MAX / 2,   // i <= j+w-1
                              a.Sq - 1 - i0);
         const bool row_dead = j >= a.Sk;
-#pragma unroll
-        for (int k = 0; k < CH; ++k)
-          if (row_dead || k < k_lo || k > k_hi) s[k] = -INFINITY;
+        mask_outside<CH>(s, row_dead ? INT_MAX / 2 : k_lo, k_hi);
       }
       const float* lv = vecs + st * 2 * CH;
 #pragma unroll
@@ -730,10 +728,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       float s[CH], dp[CH];
       tmem_ld_pair<CH>(lane_addr + C::s_col(bb), lane_addr + C::dp_col(bb), s, dp);
       if (tile_needs_mask(i0, i0 + BLOCK_M - 1, k0, k0 + CH - 1, a.Sk, a.causal, a.window)) {
-        const int rel_hi = hi_i - k0, rel_lo = lo_i - k0;
-#pragma unroll
-        for (int k = 0; k < CH; ++k)
-          if (k > rel_hi || k < rel_lo) s[k] = -INFINITY;
+        mask_outside<CH>(s, lo_i - k0, hi_i - k0);
       }
       const float nl = -lse2;
 #pragma unroll
@@ -1193,10 +1188,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         }
         if (tile_needs_mask(it.i0, it.i0 + BLOCK_M - 1, kc0, kc0 + BLOCK_N - 1, a.Sk, a.causal,
                             a.window)) {
-          const int rel_hi = hi_i - k0, rel_lo = lo_i - k0;
-#pragma unroll
-          for (int kk = 0; kk < 64; ++kk)
-            if (kk > rel_hi || kk < rel_lo) s[kk] = -INFINITY;
+          mask_outside<64>(s, lo_i - k0, hi_i - k0);
         }
         {
           const float2 sl2x2 = make_float2(sl2, sl2), nlx2 = make_float2(nl, nl);
@@ -1707,9 +1699,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
             i0 + BLOCK_M > a.Sq) {
           const int k_lo = a.causal ? j - q0 : INT_MIN / 2;
           const int k_hi = min(a.window > 0 ? j + a.window - 1 - q0 : INT_MAX / 2, a.Sq - 1 - q0);
-#pragma unroll
-          for (int kq = 0; kq < QC; ++kq)
-            if (row_dead || kq < k_lo || kq > k_hi) s[kq] = -INFINITY;
+          mask_outside<QC>(s, row_dead ? INT_MAX / 2 : k_lo, k_hi);
         }
         // lse2 / delta of the chunk's queries, read with explicit shared-space loads
         const uint32_t lv = sbase + C::VEC_OFF + st * C::VEC + part * QC * 4;

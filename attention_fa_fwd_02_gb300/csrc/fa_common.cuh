@@ -117,6 +117,26 @@ __host__ __device__ inline bool tile_needs_mask(int r0, int r1, int c0, int c1, 
   return false;
 }
 
+// x[c] = -inf for the columns c in [0, N) outside [lo, hi] (N a multiple of 32; an
+// empty range when hi < lo). The kept columns become one bit mask per 32 columns and
+// each element one bit test and select: about a third of the issue time of two
+// comparisons per element.
+template <int N>
+__device__ __forceinline__ void mask_outside(float (&x)[N], int lo, int hi) {
+  static_assert(N % 32 == 0, "32 columns per mask word");
+#pragma unroll
+  for (int w = 0; w < N / 32; ++w) {
+    // (64-bit: lo and hi may sit near the ends of the int range)
+    const int l = (int)min(max((long long)lo - 32 * w, 0ll), 32ll);
+    const int h = (int)min(max((long long)hi - 32 * w + 1, 0ll), 32ll);
+    const uint32_t below_h = h >= 32 ? 0xffffffffu : ((1u << h) - 1u);
+    const uint32_t below_l = l >= 32 ? 0xffffffffu : ((1u << l) - 1u);
+    const uint32_t keep = below_h & ~below_l;
+#pragma unroll
+    for (int b = 0; b < 32; ++b) x[32 * w + b] = ((keep >> b) & 1u) ? x[32 * w + b] : -INFINITY;
+  }
+}
+
 // ---------------------------------------------------------------- host side
 namespace host {
 

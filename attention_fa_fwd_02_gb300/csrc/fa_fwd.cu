@@ -647,10 +647,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32, NQ_>::THREADS, 1)
         }
         const int c0 = (itm.t_lo + t) * BLOCK_N;
         if (tile_needs_mask(r0, r0 + BLOCK_M - 1, c0, c0 + BLOCK_N - 1, a.Sk, a.causal, a.window)) {
-          const int rel_hi = hi_i - c0, rel_lo = lo_i - c0;
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c > rel_hi || c < rel_lo) s[c] = -INFINITY;
+          mask_outside<128>(s, lo_i - c0, hi_i - c0);
         }
         // row max: eight chains of three-input maxima
         float mx[8];
