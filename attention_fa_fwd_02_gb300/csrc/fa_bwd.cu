@@ -1502,6 +1502,11 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
   };
+  // (the issuers' waits for the softmax's hand-offs poll instead of suspending: they sit
+  // on the per-chunk critical path)
+  auto poll = [&](uint64_t* bar, uint32_t parity) {
+    return mbar_wait_poll(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
+  };
   // Chunk barriers count chunks across items (g); bar_kv, bar_kvfree and bar_done
   // count items with chunks (j). Every phase of a per-item barrier needs the previous
   // one observed first (K / V of item j load after kv_free(j - 1), whose commits follow
@@ -1593,7 +1598,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         if (it.nc == 0) continue;
         for (int c = 0; c < it.nc; ++c, ++g) {
           const int st = g % NS;
-          if (!(ok = wait(&bar_p, g & 1))) break;
+          if (!(ok = poll(&bar_p, g & 1))) break;
           tc_fence_after();
           if constexpr (SPLIT) {
             // P^T hi and lo from the S^T slot, which S^T(c + 1) may take once both are read
@@ -1629,7 +1634,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
           tc_commit(&bar_dp);
           tc_commit(&bar_doempty[st]);
           if (c + 1 == it.nc) tc_commit(&bar_kvfree);  // the item's last dP^T read V
-          if (!(ok = wait(&bar_ds, g & 1))) break;
+          if (!(ok = poll(&bar_ds, g & 1))) break;
           tc_fence_after();
           issue_acc128<D>(tmem + C::DK, tmem + C::DP_COL, sQ(st), c > 0);
           if constexpr (SPLIT) issue_acc128<D>(tmem + C::DK, tmem + C::DP_COL + C::QC / 2, sQ(st), true);

@@ -70,6 +70,41 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// A polling wait for a thread on the critical path of a hand-off: it tests the phase
+// without suspending (a suspended try_wait can take a few hundred cycles to resume),
+// with the same limits as mbar_wait: it gives up after `limit_ns`, or once another
+// thread of the CTA raised `*abort`, raising `*abort` and recording `code`.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               unsigned int* status, uint32_t code,
+                                               uint64_t limit_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        *abort = 1;
+        atomicOr(status, code);
+        return false;
+      }
+    }
+  }
+}
+
 // A wait that cannot hang: it gives up after `limit_ns` of wall time, or as soon as
 // another thread of the CTA has raised `*abort`. On giving up it raises `*abort`,
 // records `code` in the device status word and returns false. Between checks the
