@@ -983,6 +983,9 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
   };
+  auto poll = [&](uint64_t* bar, uint32_t parity) {  // (issuer waits on the softmax: no suspend)
+    return mbar_wait_poll(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
+  };
   // Reader side of the item ring: entry k, then release the entry (one arrival per
   // reading thread / warp). A failed wait reads as "no further item".
   auto take_thread = [&](int k) {
@@ -1098,14 +1101,14 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
           if (is_s) {
             const int ks = g % KST;
             if (!(ok = wait(&bar_kfull[ks], (g / KST) & 1))) break;
-            if (g > 0 && !(ok = wait(&bar_sfree, (g - 1) & 1))) break;
+            if (g > 0 && !(ok = poll(&bar_sfree, (g - 1) & 1))) break;
             tc_fence_after();
             issue_rowdot128<D>(tmem + C::S_COL, sbase + C::Q_OFF, sK(ks));
             tc_commit(&bar_s);
           } else {
             const int vs = g % VST;
             if (!(ok = wait(&bar_vfull[vs], (g / VST) & 1))) break;
-            if (g > 0 && !(ok = wait(&bar_dpfree, (g - 1) & 1))) break;
+            if (g > 0 && !(ok = poll(&bar_dpfree, (g - 1) & 1))) break;
             tc_fence_after();
             issue_rowdot128<D>(tmem + C::DP_COL, sbase + C::DO_OFF, sV(vs));
             tc_commit(&bar_dp);
@@ -1130,7 +1133,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         if (it.nc == 0) continue;
         for (int c = 0; c < it.nc; ++c, ++g) {
           const int pb = g & 1, ks = g % KST;
-          if (!(ok = wait(&bar_ds[pb], (g >> 1) & 1))) break;
+          if (!(ok = poll(&bar_ds[pb], (g >> 1) & 1))) break;
           if (c == 0 && j > 0 && !(ok = wait(&bar_dqfree, (j - 1) & 1))) break;
           tc_fence_after();
 #pragma unroll
@@ -1574,7 +1577,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         for (int c = 0; c < it.nc; ++c, ++g) {
           const int st = g % NS;
           if (!(ok = wait(&bar_qfull[st], (g / NS) & 1))) break;
-          if (g > 0 && !(ok = wait(&bar_sfree, (g - 1) & 1))) break;
+          if (g > 0 && !(ok = poll(&bar_sfree, (g - 1) & 1))) break;
           tc_fence_after();
           issue_rowdot128<D>(tmem + C::S_COL, sbase + C::K_OFF, sQ(st));
           tc_commit(&bar_s);
