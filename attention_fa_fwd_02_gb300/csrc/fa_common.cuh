@@ -117,6 +117,7 @@ __host__ __device__ inline bool tile_needs_mask(int r0, int r1, int c0, int c1, 
   return false;
 }
 
+#if defined(__CUDACC__)
 // x[c] = -inf for the columns c in [0, N) outside [lo, hi] (N a multiple of 32; an
 // empty range when hi < lo). The kept columns become one bit mask per 32 columns and
 // each element one bit test and select: about a third of the issue time of two
@@ -136,6 +137,7 @@ __device__ __forceinline__ void mask_outside(float (&x)[N], int lo, int hi) {
     for (int b = 0; b < 32; ++b) x[32 * w + b] = ((keep >> b) & 1u) ? x[32 * w + b] : -INFINITY;
   }
 }
+#endif  // __CUDACC__
 
 // ---------------------------------------------------------------- host side
 namespace host {
