@@ -1100,14 +1100,14 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         for (int c = 0; c < it.nc; ++c, ++g) {
           if (is_s) {
             const int ks = g % KST;
-            if (!(ok = wait(&bar_kfull[ks], (g / KST) & 1))) break;
+            if (!(ok = poll(&bar_kfull[ks], (g / KST) & 1))) break;
             if (g > 0 && !(ok = poll(&bar_sfree, (g - 1) & 1))) break;
             tc_fence_after();
             issue_rowdot128<D>(tmem + C::S_COL, sbase + C::Q_OFF, sK(ks));
             tc_commit(&bar_s);
           } else {
             const int vs = g % VST;
-            if (!(ok = wait(&bar_vfull[vs], (g / VST) & 1))) break;
+            if (!(ok = poll(&bar_vfull[vs], (g / VST) & 1))) break;
             if (g > 0 && !(ok = poll(&bar_dpfree, (g - 1) & 1))) break;
             tc_fence_after();
             issue_rowdot128<D>(tmem + C::DP_COL, sbase + C::DO_OFF, sV(vs));
@@ -1576,7 +1576,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         if (!(ok = wait(&bar_kv, j & 1))) break;
         for (int c = 0; c < it.nc; ++c, ++g) {
           const int st = g % NS;
-          if (!(ok = wait(&bar_qfull[st], (g / NS) & 1))) break;
+          if (!(ok = poll(&bar_qfull[st], (g / NS) & 1))) break;
           if (g > 0 && !(ok = poll(&bar_sfree, (g - 1) & 1))) break;
           tc_fence_after();
           issue_rowdot128<D>(tmem + C::S_COL, sbase + C::K_OFF, sQ(st));
@@ -1631,7 +1631,7 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
         if (!(ok = wait(&bar_kv, j & 1))) break;
         for (int c = 0; c < it.nc; ++c, ++g) {
           const int st = g % NS;
-          if (!(ok = wait(&bar_dofull[st], (g / NS) & 1))) break;
+          if (!(ok = poll(&bar_dofull[st], (g / NS) & 1))) break;
           tc_fence_after();
           issue_rowdot128<D>(tmem + C::DP_COL, sbase + C::V_OFF, sdO(st));
           tc_commit(&bar_dp);
