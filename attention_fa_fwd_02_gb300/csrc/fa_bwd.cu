@@ -388,6 +388,11 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
   };
+  // (the issuers poll: a suspending wait right after their own MMA burst returns only
+  // once the burst has drained)
+  auto poll = [&](uint64_t* bar, uint32_t parity) {
+    return mbar_wait_poll(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
+  };
   auto chunk_rows = [&](int c, int* bh, int* i0) {
     const int r = c / ncq, qc = qc_lo + c % ncq;
     *bh = b * a.H + g * rep + r;
@@ -443,8 +448,8 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       bool ok = wait(&bar_kv, 0);
       for (int c = 0; ok && c < nc; ++c) {
         const int st = c % NST, bb = c & 1;
-        if (!(ok = wait(&bar_sfull[st], (c / NST) & 1))) break;
-        if (c >= 2 && !(ok = wait(&bar_accdone[bb], ((c - 2) >> 1) & 1))) break;
+        if (!(ok = poll(&bar_sfull[st], (c / NST) & 1))) break;
+        if (c >= 2 && !(ok = poll(&bar_accdone[bb], ((c - 2) >> 1) & 1))) break;
         tc_fence_after();
         issue_rowdot<C>(tmem + C::s_col(bb), sK(0), sK(C::NSPLIT - 1), sQc(st, 0),
                         sQc(st, C::NSPLIT - 1));
@@ -465,9 +470,9 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       bool ok = true;
       for (int c = 0; ok && c < nc; ++c) {
         const int pb = c & 1, pst = c % NST;
-        if (!(ok = wait(&bar_ds[pb], (c >> 1) & 1))) break;
+        if (!(ok = poll(&bar_ds[pb], (c >> 1) & 1))) break;
         // the accumulate half (its phase of chunk c cannot be passed before aempty(c))
-        if (!(ok = wait(&bar_afull[pst], (c / NST) & 1))) break;
+        if (!(ok = poll(&bar_afull[pst], (c / NST) & 1))) break;
         tc_fence_after();
         if constexpr (C::X16) {  // B = the MN-major Q / dO chunks themselves
           issue_acc<C>(tmem + C::KV_ACC0, tmem + C::s_col(pb), tmem + C::plo_col(pb), sdOc(pst, 0),
@@ -632,6 +637,11 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
   };
+  // (the issuers poll: a suspending wait right after their own MMA burst returns only
+  // once the burst has drained)
+  auto poll = [&](uint64_t* bar, uint32_t parity) {
+    return mbar_wait_poll(bar, parity, abort_flag, &g_bwd_status, DEV_TIMEOUT, a.limit_ns);
+  };
 
   if (warp == C::TMA_WARP) {
     if (lane == 0 && nc > 0) {
@@ -669,8 +679,8 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       bool ok = wait(&bar_q, 0);
       for (int c = 0; ok && c < nc; ++c) {
         const int st = c % NST, bb = c % NSL;
-        if (!(ok = wait(&bar_full[st], (c / NST) & 1))) break;
-        if (c >= NSL && !(ok = wait(&bar_accdone[bb], ((c / NSL) - 1) & 1))) break;
+        if (!(ok = poll(&bar_full[st], (c / NST) & 1))) break;
+        if (c >= NSL && !(ok = poll(&bar_accdone[bb], ((c / NSL) - 1) & 1))) break;
         tc_fence_after();
         issue_rowdot<C>(tmem + C::s_col(bb), sQ(0), sQ(C::NSPLIT - 1), sKc(st, 0),
                         sKc(st, C::NSPLIT - 1));
@@ -688,7 +698,7 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       bool ok = true;
       for (int c = 0; ok && c < nc; ++c) {
         const int pb = c % NSL, pst = c % NST;
-        if (!(ok = wait(&bar_ds[pb], (c / NSL) & 1))) break;
+        if (!(ok = poll(&bar_ds[pb], (c / NSL) & 1))) break;
         tc_fence_after();
         if constexpr (!C::F32)
           issue_acc<C>(tmem + C::Q_ACC, tmem + C::dp_col(pb), 0, sKc(pst, 0), 0, c > 0);
@@ -1095,7 +1105,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
       for (int k = 0, w = take_thread(0); ok && w < n_items; w = take_thread(++k)) {
         const Item it = item(w);
         if (it.nc == 0) continue;
-        if (!(ok = wait(is_s ? &bar_q : &bar_do, j & 1))) break;  // S needs Q, dP needs dO
+        if (!(ok = poll(is_s ? &bar_q : &bar_do, j & 1))) break;  // S needs Q, dP needs dO
         ++j;
         for (int c = 0; c < it.nc; ++c, ++g) {
           if (is_s) {
@@ -1134,7 +1144,7 @@ __global__ void __launch_bounds__(Dq16Cfg<D>::THREADS, 1)
         for (int c = 0; c < it.nc; ++c, ++g) {
           const int pb = g & 1, ks = g % KST;
           if (!(ok = poll(&bar_ds[pb], (g >> 1) & 1))) break;
-          if (c == 0 && j > 0 && !(ok = wait(&bar_dqfree, (j - 1) & 1))) break;
+          if (c == 0 && j > 0 && !(ok = poll(&bar_dqfree, (j - 1) & 1))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BLOCK_N / 16; ++kk)
