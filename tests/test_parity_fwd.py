@@ -177,7 +177,7 @@ def test_forward_deterministic(fa, name):
                                   "bf16-d32-causal-gqa-ragged"])
 def test_forward_bf16_output(fa, name):
     # bf16 outputs: rounding O to bf16 moves each element by at most half an ulp,
-    # 2^-9 |O| (round to nearest, 8 significant bits). Allow that per element on top
+    # 2^-8 |O| (round to nearest, 8 significant bits). Allow that per element on top
     # of the fp32-output tolerance: |o - ref| <= 2^-8 |ref| + 2e-2 * RMS(ref). (The
     # decode case combines fp32 partial outputs of 6 key ranges and rounds once.)
     w = SMALL[name]
