@@ -58,11 +58,47 @@ def _draw_cases(n=64, seed=2024):
 CASES = _draw_cases()
 
 
+def _draw_wide_cases(n=24, seed=2025):
+    # longer sequences (more tiles, key ranges, several items per persistent CTA) and
+    # per-tensor magnitudes far outside fp16's range (the operand copies' power-of-two
+    # scaling), with sharper softmax rows (Q, K std up to 3)
+    rng = np.random.default_rng(seed)
+    cases = []
+    for idx in range(n):
+        dtype = "bf16" if rng.random() < 0.6 else "f32"
+        D = int(rng.choice([32, 64, 96, 128]))
+        HKV = int(rng.integers(1, 3))
+        group = int(rng.integers(1, 5))
+        Sq = int(rng.integers(1, 2501))
+        Sk = int(rng.integers(1, 2501))
+        causal = bool(rng.random() < 0.5)
+        window = 0 if rng.random() < 0.5 else int(rng.integers(1, max(Sq, Sk) + 50))
+        std_qk = float(rng.choice([1.0, 2.0, 3.0]))
+        # Q and K by reciprocal powers of two (the scores, and so the softmax, unchanged:
+        # scores of thousands would test fp32 itself), V and dO independently
+        a_qk = int(rng.integers(-20, 21)) if rng.random() < 0.5 else 0
+        mag = (2.0 ** a_qk, 2.0 ** -a_qk) + tuple(
+            float(2.0 ** rng.integers(-24, 21)) if rng.random() < 0.5 else 1.0 for _ in range(2))
+        mode = "f16x2"
+        if dtype == "f32" and D <= 64 and rng.random() < 0.4:
+            mode = "tf32x3"
+        if dtype == "bf16":
+            mode = str(rng.choice(["f32out", "f32out", "dsmat"]))
+        w = Workload(f"wide{idx}", 1, HKV * group, HKV, Sq, Sk, D, D ** -0.5, causal, window,
+                     dtype, "normal", std_qk, 4000 + idx, mag)
+        cases.append((w, mode))
+    return cases
+
+
+WIDE = _draw_wide_cases()
+
+
 def _label(case):
     w, mma = case
+    mag = "" if w.mag == (1.0, 1.0, 1.0, 1.0) else "-mag" + "/".join(f"{m:.0e}" for m in w.mag)
     return (f"{w.name}-{w.dtype}-{mma}-B{w.B}H{w.H}/{w.HKV}"
             f"-Sq{w.Sq}-Sk{w.Sk}-D{w.D}{'-causal' if w.causal else ''}"
-            f"{'-w' + str(w.window) if w.window else ''}")
+            f"{'-w' + str(w.window) if w.window else ''}{mag}")
 
 
 @pytest.fixture(scope="module")
@@ -87,10 +123,14 @@ def test_draws_cover_the_features():
     assert any(w.D % 64 for w in ws)
     assert any(min(w.Sq, w.Sk) < 130 for w in ws)
     assert any(w.Sq % 128 and w.Sk % 128 for w in ws)
+    wide = [w for w, _ in WIDE]
+    assert any(max(w.Sq, w.Sk) > 2000 for w in wide)
+    assert any(min(w.mag) < 2.0 ** -14 for w in wide) and any(max(w.mag) > 2.0 ** 15 for w in wide)
+    assert {w.dtype for w in wide} == {"bf16", "f32"} and any(m == "dsmat" for _, m in WIDE)
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("case", CASES, ids=[_label(c) for c in CASES])
+@pytest.mark.parametrize("case", CASES + WIDE, ids=[_label(c) for c in CASES + WIDE])
 def test_fuzz_forward_backward(fa, case):
     w, mode = case
     q, k, v, do = make_inputs(w)
