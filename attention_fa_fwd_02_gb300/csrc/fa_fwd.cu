@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F32, NQ_>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKlo,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmVlo,
-                  const __grid_constant__ CUtensorMap tmO, const FwdArgs a) {
+                  const FwdArgs a) {
   using C = FwdCfg<D, F32, NQ_>;
   constexpr int NQ = C::NQ, KST = C::KST, VST = C::VST;
   extern __shared__ uint8_t smem_raw[];
@@ -599,13 +599,12 @@ __global__ void __launch_bounds__(FwdCfg<D, F32, NQ_>::THREADS, 1)
     bool ok = true;
     int g = 0, j = 0;
     uint32_t pos = 0;
-    // The last tile's epilogue gives the stage back to the V ring once its TMA stores
-    // and those of the other tiles (EPI_JOIN) have read it: checked after this
-    // warpgroup's next hand-off, so the wait for the stores does not delay the next P.
+    // The last tile's epilogue gives the stage back to the V ring once every tile's
+    // warps have read their parts of it back (EPI_JOIN): done after this warpgroup's
+    // next hand-off, so that the join does not delay the next P.
     bool pending = false;
     int pend_slot = 0;
     auto release = [&]() {
-      if (lane == 0) bulk_wait_read_all();
       __syncwarp();
       if constexpr (NQ == 1) named_bar_sync(C::EPI_BAR0 + q, 128);
       else named_bar_sync(C::EPI_JOIN, 128 * NQ);
@@ -923,15 +922,6 @@ __global__ void combine_splits_kernel(const float* __restrict__ Op, const float*
 // ------------------------------------------------------------------ launcher
 namespace {
 
-// O as [B*H][Sq][D] in the output type; boxes of 32 rows x 128 bytes, 128-byte swizzle.
-// Tensors have p.D columns (the kernel's D or fewer: loads past p.D read zeros, stores
-// past it are dropped).
-bool encode_o_map(CUtensorMap* m, void* O, const fa_params& p) {
-  const bool bf = p.out_dtype == FA_BF16;
-  return host::encode_tiled_3d(m, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                               bf ? 2 : 4, O, p.D, p.Sq, (uint64_t)p.B * p.H, p.D, bf ? 64 : 32, 32);
-}
-
 // X16 (fp32 inputs as two fp16 terms): scratch bytes for the fp16 hi / lo copies of Q, K, V, the
 // OperandScales and the amax kernel's n_amax x 3 partial maxima.
 size_t x16_fwd_bytes(const fa_params& p, int n_amax) {
@@ -1014,9 +1004,9 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   const size_t nk = (size_t)p.B * p.HKV * p.Sk * Dv;
   const int grid_pp = 4 * host::sm_count();
   void* ws = nullptr;
-  CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo, mO;
+  CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo;
   const uint64_t BHq = (uint64_t)p.B * p.H, BHk = (uint64_t)p.B * p.HKV;
-  bool enc = encode_o_map(&mO, O, p);
+  bool enc = true;
   OperandScales* sc = nullptr;
   if constexpr (!F32) {
     // fp16 copy of V | the call's OperandScales | the conversion blocks' partial maxima
@@ -1121,12 +1111,6 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
     a.O = pws;
     a.LSE = static_cast<float*>(pws) + o_floats;
     a.out_bf16 = 0;
-    if (!host::encode_tiled_3d(&mO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pws, Dv, p.Sq,
-                               (uint64_t)a.n_splits * BHq, Dv, 32, 32)) {
-      host::scratch_free(pws, stream);
-      host::scratch_free(ws, stream);
-      return FA_ERR_CUDA;
-    }
   }
   const unsigned grid = (unsigned)std::min(a.n_items, sms);
   // two-term P for the shapes whose backward takes two-term P / dS (see split_operands)
@@ -1140,7 +1124,7 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
                              : (D == 128 ? "fa_fwd_kernel<128,bf16>"
                                          : (D == 64 ? "fa_fwd_kernel<64,bf16>" : "fa_fwd_kernel<32,bf16>")),
                          stream);
-    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, mO, a);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, a);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess && a.n_splits > 1) {
@@ -1319,9 +1303,9 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
   const size_t nq = (size_t)p.B * p.H * p.Sq * Dv;
   const size_t nk = (size_t)p.B * p.HKV * p.Sk * Dv;
   const int grid_pp = 4 * host::sm_count();
-  CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo, mO;
+  CUtensorMap mQ, mQlo, mK, mKlo, mV, mVlo;
   const uint64_t BHq = (uint64_t)p.B * p.H, BHk = (uint64_t)p.B * p.HKV;
-  bool enc = encode_o_map(&mO, O, p);
+  bool enc = true;
   // The whole scratch region used below is rewritten by the pre-pass kernels on
   // every call (the V copy, every conversion block's partial maximum, the scales),
   // so nothing left over from an earlier call is ever read.
@@ -1396,7 +1380,7 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_ALLOC);
   if (e != cudaSuccess) return FA_ERR_CUDA;
-  kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, mO, a);
+  kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, a);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
