@@ -308,6 +308,11 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ KVMaps m, const BwdArgs a) {
   using C = BwdCfg<D, F32>;
   constexpr int CH = C::CH, NST = C::KV_NST;
+  // A programmatic dependent of the kernel that wrote the operand copies: wait for it,
+  // and only then let the dQ grid launched after this one start (it reads those copies
+  // without a wait of its own, on the SMs this grid leaves free).
+  grid_dependency_wait();
+  grid_launch_dependents();
   // (fp32 inputs only: bf16 inputs use fa_bwd_dkdv16_kernel, whose accumulating MMAs
   // would read the score half of a stage, which this kernel releases early)
   static_assert(F32, "the 3xTF32 dK / dV kernel");
@@ -773,6 +778,9 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // Launched as a programmatic dependent of the dK / dV grid (it reads nothing that grid
+  // writes): this grid completes only after that one has.
+  grid_dependency_wait();
 }
 
 // --------------------------------------------------------- dQ, fp16 operands
@@ -2344,6 +2352,9 @@ struct X16BwdArgs {
   OperandScales* out;
 };
 __global__ void __launch_bounds__(256) x16_bwd_split_kernel(const __grid_constant__ X16BwdArgs a) {
+  // a programmatic dependent of the amax pass: its partial maxima once it has completed
+  grid_launch_dependents();
+  grid_dependency_wait();
   uint32_t m[5];
   reduce_partials<5>(a.part, a.n_part, m);
   int e[5];
@@ -2558,7 +2569,12 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     aj.n = 5;
     {
       host::KernelTimer kt("amax(Q,K,V,dO,delta)", stream);
-      amax_f32_kernel<5><<<n_pre, 256, 0, stream>>>(aj, part);
+      // programmatic dependents from here to dQ, each waiting for the grid before it
+      if (launch_programmatic(amax_f32_kernel<5>, dim3(n_pre), dim3(256), stream, aj, part) !=
+          cudaSuccess) {
+        host::scratch_free(ws, stream);
+        return FA_ERR_CUDA;
+      }
     }
     X16BwdArgs xa;
     xa.part = part;
@@ -2581,7 +2597,10 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     xa.out = sc;
     {
       host::KernelTimer kt("x16_split(Q,K,V,dO)", stream);
-      x16_bwd_split_kernel<<<n_pre, 256, 0, stream>>>(xa);
+      if (launch_programmatic(x16_bwd_split_kernel, dim3(n_pre), dim3(256), stream, xa) != cudaSuccess) {
+        host::scratch_free(ws, stream);
+        return FA_ERR_CUDA;
+      }
     }
     const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     __half* hl_q[2] = {qh, ql};
@@ -2682,8 +2701,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
         host::KernelTimer kt(C::TF32 ? "fa_bwd_dkdv_kernel<64,tf32>"
                              : (D == 128 ? "fa_bwd_dkdv_kernel<128,f32>" : "fa_bwd_dkdv_kernel<64,f32>"),
                              stream);
-        kern<<<(unsigned)(BHk * ak.n_tiles), C::THREADS, C::KV_SMEM, stream>>>(mk, ak);
-        e = cudaGetLastError();
+        e = launch_programmatic_smem(kern, dim3((unsigned)(BHk * ak.n_tiles)), dim3(C::THREADS),
+                                     C::KV_SMEM, stream, mk, ak);
       }
     } else {
       using C16 = Dkv16Cfg<D>;
@@ -2721,8 +2740,10 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
         host::KernelTimer kt(C::TF32 ? "fa_bwd_dq_kernel<64,tf32>"
                              : (D == 128 ? "fa_bwd_dq_kernel<128,f32>" : "fa_bwd_dq_kernel<64,f32>"),
                              stream);
-        kern<<<(unsigned)(BH * aq.n_tiles), C::THREADS, C::Q_SMEM, stream>>>(mq, aq);
-        e = cudaGetLastError();
+        // starts once every dK / dV block has, on the SMs that grid leaves free (it reads
+        // nothing that grid writes; it waits for it before exiting)
+        e = launch_programmatic_smem(kern, dim3((unsigned)(BH * aq.n_tiles)), dim3(C::THREADS),
+                                     C::Q_SMEM, stream, mq, aq);
       }
     } else if (D >= 64 && dsmat) {
       // dQ = scale dS K over the stored dS^T (an ordinary launch: it reads what the

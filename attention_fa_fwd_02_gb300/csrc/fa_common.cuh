@@ -189,17 +189,19 @@ fa_status launch_selftest_timeout(unsigned long long limit_ns, int* roles_done, 
 unsigned int read_and_clear_fwd_status(cudaError_t* err);
 unsigned int read_and_clear_bwd_status(cudaError_t* err);
 
-// Launches `kernel` on `stream` as a programmatic dependent of the grid launched before
-// it there: its blocks may be scheduled once every block of that grid has signalled
-// (griddepcontrol.launch_dependents) or exited, and the kernel must execute
-// griddepcontrol.wait before it reads anything that grid writes.
+// Launches `kernel` on `stream` (with `smem` bytes of dynamic shared memory) as a
+// programmatic dependent of the grid launched before it there: its blocks may be
+// scheduled once every block of that grid has signalled (griddepcontrol.launch_dependents)
+// or exited, and the kernel must execute griddepcontrol.wait before it reads anything that
+// grid writes -- and before it exits, so that it cannot complete before that grid (the
+// kernels after it rely on the order).
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3 block,
-                                      cudaStream_t stream, Args... args) {
+inline cudaError_t launch_programmatic_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                           size_t smem, cudaStream_t stream, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -207,6 +209,13 @@ inline cudaError_t launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// The same without dynamic shared memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                      cudaStream_t stream, Args... args) {
+  return launch_programmatic_smem(kernel, grid, block, 0, stream, args...);
 }
 
 // Default barrier-wait limit (ns) for the kernels.

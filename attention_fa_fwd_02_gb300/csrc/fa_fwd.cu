@@ -275,6 +275,12 @@ __global__ void __launch_bounds__(FwdCfg<D, F32, NQ_>::THREADS, 1)
                   const FwdArgs a) {
   using C = FwdCfg<D, F32, NQ_>;
   constexpr int NQ = C::NQ, KST = C::KST, VST = C::VST;
+  if constexpr (C::F32) {
+    // fp32 inputs: a programmatic dependent of the kernel that wrote the operand copies
+    // and their scales (every thread reads one or the other)
+    grid_launch_dependents();
+    grid_dependency_wait();
+  }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -832,6 +838,9 @@ struct X16FwdArgs {
   OperandScales* out;
 };
 __global__ void __launch_bounds__(256) x16_fwd_split_kernel(const __grid_constant__ X16FwdArgs a) {
+  // a programmatic dependent of the amax pass: its partial maxima once it has completed
+  grid_launch_dependents();
+  grid_dependency_wait();
   uint32_t m[3];
   reduce_partials<3>(a.part, a.n_part, m);
   int e[3];
@@ -864,6 +873,9 @@ __global__ void combine_splits_kernel(const float* __restrict__ Op, const float*
                                       void* __restrict__ O, float* __restrict__ LSE, int n_splits,
                                       int BH, int Sq, int Dv, int out_bf16) {
   constexpr int G = KEY_RANGE_GROUP;
+  // a programmatic dependent of the forward kernel: its partial results once it has
+  // completed (every thread waits, so this grid cannot complete before that one)
+  grid_dependency_wait();
   const int i = blockIdx.x * blockDim.y + threadIdx.y;
   const int c = threadIdx.x * 4;
   if (i >= Sq || c >= Dv) return;
@@ -968,7 +980,9 @@ bool prep_x16_fwd(void* ws, const void* Q, const void* K, const void* V, const f
   xa.out = sc;
   {
     host::KernelTimer kt("x16_split(Q,K,V)", stream);
-    x16_fwd_split_kernel<<<n_amax, 256, 0, stream>>>(xa);
+    // a programmatic dependent of the amax pass (it waits for it before reading)
+    if (launch_programmatic(x16_fwd_split_kernel, dim3(n_amax), dim3(256), stream, xa) != cudaSuccess)
+      return false;
   }
   const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   bool enc = host::encode_tiled_3d(mQ, F16, 2, qh, Dv, p.Sq, BHq, Dv, 64, 128);
@@ -1124,18 +1138,24 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
                              : (D == 128 ? "fa_fwd_kernel<128,bf16>"
                                          : (D == 64 ? "fa_fwd_kernel<64,bf16>" : "fa_fwd_kernel<32,bf16>")),
                          stream);
-    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, a);
-    e = cudaGetLastError();
+    if constexpr (F32 != IN_BF16) {
+      // fp32: a programmatic dependent of the kernel that split the operands
+      e = launch_programmatic_smem(kern, dim3(grid), dim3(C::THREADS), C::SMEM_ALLOC, stream, mQ,
+                                   mQlo, mK, mKlo, mV, mVlo, a);
+    } else {
+      kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, a);
+      e = cudaGetLastError();
+    }
   }
   if (e == cudaSuccess && a.n_splits > 1) {
     host::KernelTimer kt("combine_splits", stream);
     const float* op = static_cast<const float*>(pws);
     dim3 cg, cb;
     combine_launch_shape((int)BHq, p.Sq, Dv, &cg, &cb);
-    combine_splits_kernel<<<cg, cb, 0, stream>>>(op, op + (size_t)a.n_splits * rows * Dv, O, LSE,
-                                                 a.n_splits, (int)BHq, p.Sq, Dv,
-                                                 p.out_dtype == FA_BF16);
-    e = cudaGetLastError();
+    // a programmatic dependent of the forward kernel (it waits for it before reading)
+    e = launch_programmatic(combine_splits_kernel, cg, cb, stream, op,
+                            op + (size_t)a.n_splits * rows * Dv, O, LSE, a.n_splits, (int)BHq,
+                            p.Sq, Dv, (int)(p.out_dtype == FA_BF16));
   }
   cudaError_t e2 = host::scratch_free(ws, stream);
   const cudaError_t e3 = host::scratch_free(pws, stream);
@@ -1380,8 +1400,15 @@ fa_status run_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_ALLOC);
   if (e != cudaSuccess) return FA_ERR_CUDA;
-  kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, a);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  if constexpr (F32 != IN_BF16) {
+    // fp32: a programmatic dependent of the kernel that split the operands
+    e = launch_programmatic_smem(kern, dim3(grid), dim3(C::THREADS), C::SMEM_ALLOC, stream, mQ, mQlo,
+                                 mK, mKlo, mV, mVlo, a);
+  } else {
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(mQ, mQlo, mK, mKlo, mV, mVlo, a);
+    e = cudaGetLastError();
+  }
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace

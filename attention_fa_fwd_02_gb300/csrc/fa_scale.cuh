@@ -179,6 +179,10 @@ namespace {  // (each translation unit gets its own copy of the kernel)
 template <int N>
 __global__ void __launch_bounds__(256) amax_f32_kernel(const __grid_constant__ AmaxJobs js,
                                                        uint32_t* __restrict__ part) {
+  // (launched as a programmatic dependent after the delta pass: its arrays are read only
+  // once that grid has completed; a plain launch returns from the wait at once)
+  ptx::grid_launch_dependents();
+  ptx::grid_dependency_wait();
   uint32_t m[N];
   const size_t stride = (size_t)gridDim.x * blockDim.x;
 #pragma unroll
