@@ -1431,8 +1431,11 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
   constexpr int NS = C::NS;
   static_assert(!SPLIT || C::QC == 64, "two-term operands: 32 packed columns per term and part");
   static_assert(!MATDS || C::QC == 64, "dS^T rows stored as 128-byte pieces");
-  // The dQ grid launched after this one reads nothing this grid writes: it may start
-  // as soon as every block of this grid has started (see the launcher).
+  // A programmatic dependent of the kernel that fixed the operand copies' scales (and may
+  // have rewritten the copies): wait for it first. The dQ grid launched after this one
+  // reads those copies and nothing this grid writes: it may start once every block of
+  // this grid has passed that wait (see the launcher).
+  grid_dependency_wait();
   grid_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -2292,6 +2295,9 @@ __global__ void __launch_bounds__(1024) bwd_scales_kernel(const __grid_constant_
 __global__ void dq_range_sum_kernel(const float* __restrict__ part, void* __restrict__ dQ,
                                     int tps, int BH, int Sq, int Sk, int causal, int window, int Dv,
                                     int out_bf16) {
+  // a programmatic dependent of the kernel that wrote the partial dQ (every thread waits,
+  // so this grid cannot complete before that one)
+  grid_dependency_wait();
   const int i = blockIdx.x * blockDim.y + threadIdx.y;
   const int c = threadIdx.x * 4;
   if (i >= Sq || c >= Dv) return;
@@ -2721,8 +2727,8 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
                              stream);
         // persistent: one CTA per SM (at most), walking the (key tile, kv head) items
         const unsigned grid = (unsigned)std::min<size_t>(BHk * ak.n_tiles, (size_t)sms);
-        kern<<<grid, C16::THREADS, dyn, stream>>>(mk, ak);
-        e = cudaGetLastError();
+        // a programmatic dependent of the scales kernel (it waits for it first)
+        e = launch_programmatic_smem(kern, dim3(grid), dim3(C16::THREADS), (size_t)dyn, stream, mk, ak);
       }
     }
   }
@@ -2772,9 +2778,9 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
         host::KernelTimer kt("dq_range_sum", stream);
         dim3 cg, cb;
         combine_launch_shape((int)BH, p.Sq, Dv, &cg, &cb);
-        dq_range_sum_kernel<<<cg, cb, 0, stream>>>(dq_part, dQ, dq_tps, (int)BH, p.Sq, p.Sk,
-                                                   p.causal, p.window, Dv, p.out_dtype == FA_BF16);
-        e = cudaGetLastError();
+        e = launch_programmatic(dq_range_sum_kernel, cg, cb, stream, (const float*)dq_part, dQ,
+                                dq_tps, (int)BH, p.Sq, p.Sk, (int)p.causal, p.window, Dv,
+                                (int)(p.out_dtype == FA_BF16));
       }
       }
     } else {
@@ -2810,9 +2816,9 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
         host::KernelTimer kt("dq_range_sum", stream);
         dim3 cg, cb;
         combine_launch_shape((int)BH, p.Sq, Dv, &cg, &cb);
-        dq_range_sum_kernel<<<cg, cb, 0, stream>>>(dq_part, dQ, dq_tps, (int)BH, p.Sq, p.Sk,
-                                                   p.causal, p.window, Dv, p.out_dtype == FA_BF16);
-        e = cudaGetLastError();
+        e = launch_programmatic(dq_range_sum_kernel, cg, cb, stream, (const float*)dq_part, dQ,
+                                dq_tps, (int)BH, p.Sq, p.Sk, (int)p.causal, p.window, Dv,
+                                (int)(p.out_dtype == FA_BF16));
       }
     }
   }
