@@ -160,6 +160,20 @@ def flops_for(w):
     return fwd, 2.5 * fwd, vis
 
 
+def step_hbm_bytes(w, out_bytes):
+    """Algorithmic HBM bytes of one fwd + bwd step: every tensor the step takes in read
+    once, every tensor it hands out written once. Forward: Q, K, V in; O, LSE out.
+    Backward: Q, K, V, O, dO, LSE in; dQ, dK, dV out. (in_bytes / out_bytes: element
+    sizes of the inputs and of O, dQ, dK, dV; LSE is fp32.)"""
+    in_bytes = 2 if w.dtype == "bf16" else 4
+    nq = w.B * w.H * w.Sq * w.D
+    nk = w.B * w.HKV * w.Sk * w.D
+    rows = w.B * w.H * w.Sq
+    fwd = in_bytes * (nq + 2 * nk) + out_bytes * nq + 4 * rows
+    bwd = in_bytes * (2 * nq + 2 * nk) + out_bytes * nq + 4 * rows + out_bytes * (nq + 2 * nk)
+    return fwd + bwd
+
+
 _INPUT_CACHE = {}
 
 
@@ -499,6 +513,12 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
+    # the step's algorithmic HBM traffic over its time: what a latency-bound case (small
+    # shapes) reaches against the copy bandwidth
+    hbm_b = step_hbm_bytes(w, 2 if args.out_dtype == "bf16" else 4)
+    gbs = hbm_b * world / (ms_max * 1e-3) / 1e9
+    line["hbm"] = {"bytes_per_step": hbm_b, "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"],
+                   "unit": "GB/s", "frac": round(gbs / world / peaks["hbm_gbs"], 4)}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

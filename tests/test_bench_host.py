@@ -91,6 +91,20 @@ def test_source_hash_covers_the_kernel_sources():
     assert bench.source_sha("fa_fwd_kernel") != bench.source_sha("fa_bwd_dkdv_kernel")
 
 
+def test_step_hbm_bytes_counts_each_tensor_once():
+    from attention_fa_fwd_02_gb300.workloads import WORKLOADS
+    w = WORKLOADS["c1"]  # fp32 B1 H1 S128 D64: every tensor 128 x 64 x 4 bytes, LSE 512
+    t = 128 * 64 * 4
+    # fwd: Q, K, V in, O out, LSE out; bwd: Q, K, V, O, dO in, LSE in, dQ, dK, dV out
+    assert bench.step_hbm_bytes(w, 4) == (4 * t + 512) + (8 * t + 512)
+    c3 = WORKLOADS["c3"]  # bf16 inputs, fp32 or bf16 outputs
+    nq, nk, rows = 2 * 32 * 4096 * 128, 2 * 8 * 4096 * 128, 2 * 32 * 4096
+    f32 = bench.step_hbm_bytes(c3, 4)
+    assert f32 == 2 * (nq + 2 * nk) + 4 * nq + 4 * rows + 2 * (2 * nq + 2 * nk) + 4 * nq + 4 * rows \
+        + 4 * (nq + 2 * nk)
+    assert bench.step_hbm_bytes(c3, 2) == f32 - 2 * (2 * nq + nq + 2 * nk)
+
+
 def test_roofline_denominator_is_the_burst_peak():
     # the kernels are timed for well under a second at full clocks: the burst cuBLAS
     # figure is their denominator, the power-capped sustained one is reported beside it
