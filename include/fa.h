@@ -181,10 +181,13 @@ FA_API unsigned long long fa_noalloc_scratch_bytes(void);
  * fp32 partial dQ of up to 32 key ranges, summed in range order) is stream-ordered
  * from the library pool. O must be the output of fa_fwd for the same inputs (the dS
  * scaling bounds D_i by the largest |dO| and |V|). Same ownership, alignment and
- * error rules as fa_fwd. For bf16 inputs the dQ kernel is launched on `stream` as
- * a programmatic dependent of the dK/dV kernel: it starts on the SMs that dK/dV's
- * last wave leaves idle and completes only after dK/dV has, so work enqueued on
- * `stream` afterwards sees all three gradients.
+ * error rules as fa_fwd. For both input types the dQ kernel is launched on `stream`
+ * as a programmatic dependent of the dK/dV kernel: it starts on the SMs that dK/dV
+ * leaves idle and completes only after dK/dV has, so work enqueued on `stream`
+ * afterwards sees all three gradients. (Inside both calls, every kernel after the
+ * first is a programmatic dependent of the one before and waits for it before it
+ * reads that kernel's results and before it exits; the first is an ordinary launch.
+ * Stream order as the caller sees it is unchanged.)
  */
 FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                  const float* LSE, void* dQ, void* dK, void* dV, const fa_params* p,
