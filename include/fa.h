@@ -184,10 +184,11 @@ FA_API unsigned long long fa_noalloc_scratch_bytes(void);
  * error rules as fa_fwd. For both input types the dQ kernel is launched on `stream`
  * as a programmatic dependent of the dK/dV kernel: it starts on the SMs that dK/dV
  * leaves idle and completes only after dK/dV has, so work enqueued on `stream`
- * afterwards sees all three gradients. (Inside both calls, every kernel after the
- * first is a programmatic dependent of the one before and waits for it before it
- * reads that kernel's results and before it exits; the first is an ordinary launch.
- * Stream order as the caller sees it is unchanged.)
+ * afterwards sees all three gradients. (Inside both calls, most kernels after the
+ * first are launched as programmatic dependents of the kernel before them; each such
+ * kernel waits for that one before it reads its results and before it exits, and the
+ * first kernel of a call is an ordinary launch, so stream order as the caller sees it
+ * is unchanged.)
  */
 FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                  const float* LSE, void* dQ, void* dK, void* dV, const fa_params* p,
