@@ -2,8 +2,8 @@
 
 A caller that runs the same attention shapes over and over captures the calls once
 and replays the graph. The library's stream-ordered scratch (pool allocations) and
-the backward's programmatic dependent launch of the dQ kernel must both survive
-capture; every replay must recompute all outputs (they are overwritten with NaN
+the kernels' programmatic dependent launches (the dQ kernel after dK/dV; the fp32
+path's chains) must both survive capture; every replay must recompute all outputs (they are overwritten with NaN
 before each replay) and match eager calls bit for bit -- the kernels are
 deterministic (dK/dV without atomics; the dQ items each computed by one CTA).
 """
@@ -21,7 +21,12 @@ CASES = {
     # short queries: forward and dQ split the keys into ranges (scratch for the partial
     # results allocated and freed inside the graph)
     "bf16-decode": WORKLOADS["c3"].with_(B=1, H=4, HKV=2, Sq=100, Sk=2500, causal=False, seed=34),
+    # fp32 through the 3xTF32 kernels, and at D = 128 with keys split into ranges (the
+    # fp32 kernels run as chains of programmatic dependent launches)
+    "f32-tf32x3": WORKLOADS["c2"].with_(B=1, H=4, HKV=2, Sq=300, Sk=300, seed=35),
+    "f32-d128-decode": WORKLOADS["c5"].with_(Sq=100, Sk=3000, D=128, scale=128 ** -0.5, seed=36),
 }
+MMA = {"f32-tf32x3": "tf32x3"}
 
 
 @pytest.fixture(scope="module")
@@ -36,9 +41,10 @@ def fa():
 @pytest.mark.parametrize("name", list(CASES))
 def test_graph_replay_matches_eager(fa, name):
     w = CASES[name]
+    mma = MMA.get(name, "f16x2")
     q, k, v, do = (t.cuda() for t in make_inputs(w))
-    o, lse = fa.forward(q, k, v, w.scale, w.causal, w.window)
-    dq, dk, dv = fa.backward(q, k, v, o, lse, do, w.scale, w.causal, w.window)
+    o, lse = fa.forward(q, k, v, w.scale, w.causal, w.window, f32_mma=mma)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, w.scale, w.causal, w.window, f32_mma=mma)
     torch.cuda.synchronize()
     fa.check_device_status()
 
@@ -46,8 +52,8 @@ def test_graph_replay_matches_eager(fa, name):
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.graph(graph, stream=side):
-        go, glse = fa.forward(q, k, v, w.scale, w.causal, w.window)
-        gdq, gdk, gdv = fa.backward(q, k, v, go, glse, do, w.scale, w.causal, w.window)
+        go, glse = fa.forward(q, k, v, w.scale, w.causal, w.window, f32_mma=mma)
+        gdq, gdk, gdv = fa.backward(q, k, v, go, glse, do, w.scale, w.causal, w.window, f32_mma=mma)
     torch.cuda.synchronize()
     for _ in range(3):
         for t in (go, glse, gdq, gdk, gdv):
