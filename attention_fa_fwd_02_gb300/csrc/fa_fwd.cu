@@ -30,6 +30,7 @@
 #include "ptx.cuh"
 #include "fa_prepass.cuh"
 #include "fa_epilogue.cuh"
+#include "fa_decode.cuh"
 
 namespace fa {
 using namespace ptx;
@@ -931,6 +932,97 @@ __global__ void combine_splits_kernel(const float* __restrict__ Op, const float*
   }
 }
 
+// The same merge for few rows with many ranges (the decode kernel's partial results):
+// block (Dv / 4, SG) per row (rows blockIdx.x + multiples of gridDim.x), its SG thread
+// groups dealt the ranges -- group g takes ranges g, g + SG, .. in order, with the
+// running maximum above -- and the groups' (m, sum, O) merged in group order through
+// shared memory: a row's loads go out from SG times as many threads, the order is fixed
+// (deterministic). Dv <= 128, SG <= COMBINE_GROUPS.
+constexpr int COMBINE_GROUPS = 16;
+__global__ void combine_splits_grouped_kernel(const float* __restrict__ Op, const float* __restrict__ Lp,
+                                              void* __restrict__ O, float* __restrict__ LSE,
+                                              int n_splits, int rows, int Dv, int out_bf16) {
+  constexpr int G = KEY_RANGE_GROUP;
+  __shared__ float m_s[COMBINE_GROUPS], sum_s[COMBINE_GROUPS];
+  __shared__ __align__(16) float acc_s[COMBINE_GROUPS][128];
+  // a programmatic dependent of the decode kernel, as combine_splits_kernel
+  grid_dependency_wait();
+  const int c = threadIdx.x * 4, grp = threadIdx.y, SG = blockDim.y;
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    float m = -INFINITY, sum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = grp; s0 < n_splits; s0 += SG * G) {
+      float ls[G];
+      float4 ov[G];
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        const int sp = s0 + k * SG;
+        if (sp < n_splits) {
+          ls[k] = Lp[(size_t)sp * rows + r];
+          ov[k] = *reinterpret_cast<const float4*>(Op + ((size_t)sp * rows + r) * Dv + c);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        if (s0 + k * SG < n_splits && ls[k] != -INFINITY) {
+          if (ls[k] > m) {  // new maximum: rescale what was summed (exp(-inf) = 0 at first)
+            const float sc = expf(m - ls[k]);
+            sum *= sc;
+            acc.x *= sc;
+            acc.y *= sc;
+            acc.z *= sc;
+            acc.w *= sc;
+            m = ls[k];
+          }
+          const float wgt = expf(ls[k] - m);
+          sum += wgt;
+          acc.x += wgt * ov[k].x;
+          acc.y += wgt * ov[k].y;
+          acc.z += wgt * ov[k].z;
+          acc.w += wgt * ov[k].w;
+        }
+      }
+    }
+    if (threadIdx.x == 0) {
+      m_s[grp] = m;
+      sum_s[grp] = sum;
+    }
+    *reinterpret_cast<float4*>(&acc_s[grp][c]) = acc;
+    __syncthreads();
+    if (grp == 0) {
+      float M = -INFINITY;
+      for (int h = 0; h < SG; ++h) M = fmaxf(M, m_s[h]);
+      float S = 0.f;
+      float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -INFINITY) {
+        for (int h = 0; h < SG; ++h) {
+          const float w = expf(m_s[h] - M);  // (a group that saw no key: exp(-inf) = 0)
+          const float4 a4 = *reinterpret_cast<const float4*>(&acc_s[h][c]);
+          S += sum_s[h] * w;
+          A.x += a4.x * w;
+          A.y += a4.y * w;
+          A.z += a4.z * w;
+          A.w += a4.w * w;
+        }
+      }
+      const float inv = S > 0.f ? 1.f / S : 0.f;
+      if (c == 0) LSE[r] = S > 0.f ? M + logf(S) : -INFINITY;
+      if (out_bf16) {
+        __nv_bfloat162 lo2 = __floats2bfloat162_rn(A.x * inv, A.y * inv);
+        __nv_bfloat162 hi2 = __floats2bfloat162_rn(A.z * inv, A.w * inv);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&lo2);
+        u.y = *reinterpret_cast<uint32_t*>(&hi2);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(O) + (size_t)r * Dv + c) = u;
+      } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(O) + (size_t)r * Dv + c) =
+            make_float4(A.x * inv, A.y * inv, A.z * inv, A.w * inv);
+      }
+    }
+    __syncthreads();  // (the next row's groups overwrite the merge area)
+  }
+}
+
 // ------------------------------------------------------------------ launcher
 namespace {
 
@@ -1162,7 +1254,96 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
   return (e == cudaSuccess && e2 == cudaSuccess && e3 == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
 }
 
+// The decode forward (fa_decode.cuh): the keys of each (batch, kv head) split into ranges
+// so that one wave of CTAs (as many per SM as fit) streams K and V, each range at least
+// one chunk per warp; with more than one range, partial O / LSE in scratch and the
+// range-order combine.
+template <int DK, int ROWS, bool F32IN>
+fa_status run_decode(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                     const fa_params& p, cudaStream_t stream) {
+  DecodeArgs a;
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.B = p.B;
+  a.H = p.H;
+  a.HKV = p.HKV;
+  a.Sq = p.Sq;
+  a.Sk = p.Sk;
+  a.Dv = p.D;
+  a.rep = p.H / p.HKV;
+  a.rows = a.rep * p.Sq;
+  a.causal = p.causal;
+  a.window = p.window;
+  a.scale_log2 = p.scale * LOG2E;
+  a.out_bf16 = p.out_dtype == FA_BF16;
+  a.k_wide = reinterpret_cast<uintptr_t>(K) % 32 == 0;
+  constexpr size_t smem = decode_smem_bytes<DK, ROWS, F32IN>();
+  auto kern = fa_decode_kernel<DK, ROWS, F32IN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  // CTAs resident per SM (registers and shared memory), asked once per kernel
+  static const int per_sm = [&] {
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, DEC_WARPS * 32, smem) != cudaSuccess)
+      o = 1;
+    return std::max(o, 1);
+  }();
+  const long long groups = (long long)p.B * p.HKV;
+  const int sms = host::sm_count();
+  const int min_keys = DEC_WARPS * DEC_KEYS;
+  long long n = ((long long)per_sm * sms + groups - 1) / groups;
+  n = std::max(1ll, std::min(n, ((long long)p.Sk + min_keys - 1) / min_keys));
+  int kps = (int)(((long long)p.Sk + n - 1) / n);
+  kps = (kps + DEC_KEYS - 1) / DEC_KEYS * DEC_KEYS;
+  a.keys_per_split = kps;
+  a.n_splits = (p.Sk + kps - 1) / kps;
+  const size_t rows_all = (size_t)p.B * p.H * p.Sq;
+  void* pws = nullptr;
+  if (a.n_splits > 1) {
+    if (host::scratch_alloc(&pws, ((size_t)a.n_splits * rows_all * p.D + (size_t)a.n_splits * rows_all) * 4,
+                            stream) != cudaSuccess)
+      return FA_ERR_CUDA;
+    a.O = pws;
+    a.LSE = static_cast<float*>(pws) + (size_t)a.n_splits * rows_all * p.D;
+  } else {
+    a.O = O;
+    a.LSE = LSE;
+  }
+  {
+    host::KernelTimer kt("fa_decode_kernel", stream);
+    kern<<<dim3((unsigned)groups, (unsigned)a.n_splits), DEC_WARPS * 32, smem, stream>>>(a);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess && a.n_splits > 1) {
+    host::KernelTimer kt("combine_splits", stream);
+    const int q4 = p.D / 4;
+    const int sg = std::max(1, std::min({256 / q4, a.n_splits, COMBINE_GROUPS}));
+    const dim3 cg((unsigned)std::min<size_t>(rows_all, 65535)), cb(q4, sg);
+    const float* op = static_cast<const float*>(pws);
+    e = launch_programmatic(combine_splits_grouped_kernel, cg, cb, stream, op,
+                            op + (size_t)a.n_splits * rows_all * p.D, O, LSE, a.n_splits, (int)rows_all,
+                            p.D, (int)(p.out_dtype == FA_BF16));
+  }
+  const cudaError_t e2 = host::scratch_free(pws, stream);
+  return (e == cudaSuccess && e2 == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int DK, bool F32IN>
+fa_status run_decode_rows(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                          const fa_params& p, cudaStream_t stream) {
+  const int rows = p.H / p.HKV * p.Sq;
+  if (rows <= 4) return run_decode<DK, 4, F32IN>(Q, K, V, O, LSE, p, stream);
+  return run_decode<DK, DEC_ROWS, F32IN>(Q, K, V, O, LSE, p, stream);
+}
+
 }  // namespace
+
+// Whether fa_fwd takes the decode kernel: every kv head's query rows (the grouped heads'
+// Sq rows each) fit one CTA's DEC_ROWS.
+bool decode_shaped(const fa_params& p) {
+  return p.Sk > 0 && (long long)(p.H / p.HKV) * p.Sq <= DEC_ROWS;
+}
 
 fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                      const fa_params& p, cudaStream_t stream) {
@@ -1171,6 +1352,13 @@ fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float
     fill_empty_kernel<<<4 * host::sm_count(), 256, 0, stream>>>(O, LSE, rows, p.D,
                                                                 p.out_dtype == FA_BF16);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+  if (decode_shaped(p)) {
+    const bool f32 = p.in_dtype != FA_BF16;
+    if (p.D <= 64) return f32 ? run_decode_rows<64, true>(Q, K, V, O, LSE, p, stream)
+                              : run_decode_rows<64, false>(Q, K, V, O, LSE, p, stream);
+    return f32 ? run_decode_rows<128, true>(Q, K, V, O, LSE, p, stream)
+               : run_decode_rows<128, false>(Q, K, V, O, LSE, p, stream);
   }
   // head dims below a kernel's D run in it with the missing columns read as zeros
   if (p.in_dtype == FA_BF16) {

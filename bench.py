@@ -38,12 +38,13 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # forward 2 GEMMs (QK^T, PV); dK/dV kernel 4 (S^T, dP^T, dV, dK); dQ kernel 3 (S, dP, dQ).
 # The materialised-dS backward's dQ GEMM: 1 (dS K).
 KERNEL_FLOPS_PER_PAIR_PER_D = {"fa_fwd_kernel": 4, "fa_bwd_dkdv_kernel": 8, "fa_bwd_dq_kernel": 6,
-                               "dq_from_ds_kernel": 2}
+                               "dq_from_ds_kernel": 2, "fa_decode_kernel": 4}
 # Source files whose change invalidates a committed DRAM-traffic figure.
 _COMMON_SOURCES = ["ptx.cuh", "fa_common.cuh", "fa_epilogue.cuh", "fa_prepass.cuh"]
 # head dim of each named workload (traffic figures in profiles/ are for these)
-# fa_fwd's launches besides its kernel (operand conversion, the key-range combine)
-FWD_AUX_KERNELS = ("cvt_bf16_to_f16(V)", "split_tf32(Q,K,V)", "combine_splits")
+# fa_fwd's launches besides its kernel (operand conversion and scaling, the key-range combine)
+FWD_AUX_KERNELS = ("cvt_bf16_to_f16(V)", "fwd_scales", "amax(Q,K,V)", "x16_split(Q,K,V)",
+                   "split_tf32(Q,K,V)", "combine_splits")
 WORKLOADS_D = {"c1": 64, "c2": 64, "c3": 128, "c4": 128, "c5": 64}
 KERNEL_SOURCES = {"fa_fwd_kernel": ["fa_fwd.cu"] + _COMMON_SOURCES,
                   "fa_bwd_dkdv_kernel": ["fa_bwd.cu"] + _COMMON_SOURCES,
@@ -467,7 +468,7 @@ def run_ours(args, rank, world, local_rank):
             fl = KERNEL_FLOPS_PER_PAIR_PER_D[base] * w.B * w.H * vis * w.D
             entry["tflops"] = fl / (tot / n * 1e-3) / 1e12
         per_kernel[name] = entry
-        if base.startswith("fa_fwd") or name in FWD_AUX_KERNELS:
+        if base.startswith("fa_fwd") or base == "fa_decode_kernel" or name in FWD_AUX_KERNELS:
             fwd_ms += tot / n
     dom = max((k_ for k_ in per_kernel if "tflops" in per_kernel[k_]),
               key=lambda k_: per_kernel[k_]["launches"] * per_kernel[k_]["ms_per_launch"])

@@ -191,6 +191,33 @@ def test_forward_bf16_output(fa, name):
     assert lse_err(to_np(lse), rl) <= 1e-2
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_forward_decode_16_byte_aligned_inputs(fa, dtype, D):
+    # the C ABI promises 16-byte alignment only: Q, K and V here start 16 bytes into
+    # their allocations (torch's are 256-byte aligned), so the decode kernel's K rows
+    # must be read 16 bytes per load instead of 32
+    base = C3 if dtype == "bf16" else C5
+    w = base.with_(B=2, H=8, HKV=2, Sq=1, Sk=3001, D=D, scale=D ** -0.5, causal=False,
+                   window=700, seed=120 + D)
+    q, k, v, _ = make_inputs(w)
+    dev = torch.device("cuda:0")
+    pad = 16 // q.element_size()
+
+    def offset_copy(t):
+        buf = torch.empty(t.numel() + pad, dtype=t.dtype, device=dev)
+        view = buf[pad:].view(t.shape)
+        view.copy_(t.to(dev))
+        assert view.data_ptr() % 32 == 16 and view.is_contiguous()
+        return view
+
+    o, lse = fa.forward(offset_copy(q), offset_copy(k), offset_copy(v), w.scale, w.causal,
+                        w.window)
+    fa.check_device_status()
+    ro, rl = oracle.attention_fwd(q, k, v, w.scale, w.causal, w.window)
+    _check(w, o, lse, ro, rl, f"decode-16B-aligned-{dtype}-d{D}")
+
+
 def test_forward_zero_keys(fa):
     w = C3.with_(B=1, H=2, HKV=1, Sq=130, Sk=0, seed=5)
     q = torch.randn(1, 2, 130, 128).to(torch.bfloat16).cuda()
