@@ -115,13 +115,16 @@ typedef enum {
  * memory pool, the fa_fwd_noalloc scratch address, the status word): do not call it
  * again on a device after cudaDeviceReset() on that device, which invalidates that
  * state. The call validates its arguments synchronously, then enqueues
- * work on `stream` and returns without waiting. Temporary buffers (the scaled fp16
- * copy of V and its scale factors for bf16 inputs; the hi/lo splits of Q, K, V for
- * fp32 inputs; for short query sequences, whose work items are fewer than the SMs, fp32
- * partial O and LSE of up to 32 key ranges, combined in range order, so results stay
- * deterministic) are
- * taken stream-ordered from a library-owned CUDA memory pool and released on the
- * same stream. Errors: FA_ERR_INVALID_ARG / _UNSUPPORTED / _ALIGNMENT before any work
+ * work on `stream` and returns without waiting. Decode shapes -- at most 8 query rows
+ * per kv head, (H / HKV) * Sq <= 8 -- run in a CUDA-core kernel that reads K and V once
+ * and computes in fp32 for either input type (f32_mma does not apply there); every
+ * other shape runs on the tensor cores. Temporary buffers (the scaled fp16 copy of V
+ * and its scale factors for bf16 inputs; the hi/lo splits of Q, K, V for fp32 inputs;
+ * for short query sequences, whose work items are fewer than the SMs, fp32 partial O
+ * and LSE of up to 32 key ranges, combined in range order; for decode shapes, partial
+ * O and LSE of as many key ranges as fill the GPU once, combined in a fixed order: so
+ * results stay deterministic) are taken stream-ordered from a library-owned CUDA
+ * memory pool and released on the same stream. Errors: FA_ERR_INVALID_ARG / _UNSUPPORTED / _ALIGNMENT before any work
  * is enqueued; FA_ERR_CUDA if a CUDA call or launch fails. Device-side barrier
  * timeouts are reported later by fa_device_status().
  */
@@ -138,10 +141,11 @@ FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, fl
  * (real-time or safety-certified inference), hosts whose own allocator owns the
  * whole device and would be starved or fragmented by a second pool, and code
  * that runs where a cudaMalloc is not allowed or would block on a lock. For them
- * this entry point computes exactly what fa_fwd computes, with the same
- * arguments, rules and errors, but its scratch (the fp16 copy of V for bf16
- * inputs; the hi/lo splits of Q, K, V for fp32 inputs) lives in a
- * file-scope device array of FA_NOALLOC_SCRATCH_BYTES inside libfa.so. Every GPU
+ * this entry point computes what fa_fwd computes, with the same arguments, rules
+ * and errors (at decode shapes through the tensor-core kernels, so there its outputs
+ * may differ from fa_fwd's by rounding, within the same bounds), but its scratch
+ * (the fp16 copy of V for bf16 inputs; the hi/lo splits of Q, K, V for fp32 inputs)
+ * lives in a file-scope device array of FA_NOALLOC_SCRATCH_BYTES inside libfa.so. Every GPU
  * on which the library is loaded holds that array until the process exits.
  *   - A problem whose scratch would not fit returns FA_ERR_SCRATCH_LIMIT before
  *     anything is enqueued: bf16 inputs need round_up(B*HKV*Sk*D*2, 256) + 256 +

@@ -83,6 +83,16 @@ SMALL = {
     # range but the first is empty
     "bf16-decode-sq1": C3.with_(B=1, H=8, HKV=2, Sq=1, Sk=5000, causal=False, seed=61),
     "bf16-decode-sq1-causal": C3.with_(B=1, H=8, HKV=2, Sq=1, Sk=5000, seed=62),
+    # at most 8 query rows per kv head (grouped heads x Sq) take the CUDA-core decode
+    # kernel: 8 rows over 20000 keys; fp32 with Dv = 80 in the kernel built for 128
+    # (8 rows), D = 32 causal (3 rows, key 0 only), a window narrower than Sq (8 rows)
+    "bf16-decode-rows8-s20000": C3.with_(B=1, H=8, HKV=1, Sq=1, Sk=20000, causal=False,
+                                         seed=63),
+    "f32-decode-sq2-gqa4-d80": C5.with_(B=2, H=8, HKV=2, Sq=2, Sk=2500, D=80, scale=80 ** -0.5,
+                                        seed=64),
+    "f32-decode-sq1-d32-causal": C5.with_(H=3, Sq=1, Sk=777, D=32, scale=32 ** -0.5,
+                                          causal=True, seed=65),
+    "f32-decode-sq8-window3": C5.with_(Sq=8, Sk=3000, window=3, seed=66),
     # bf16 inputs far outside fp16's range (largest finite 65504, normal from 2^-14):
     # the fp16 operand copies must be scaled by powers of two (gradients dO of 1e-7,
     # V of 1e5, Q and K of 2^-20, dO of 1e4 and V of 1e-6; alone and together)
