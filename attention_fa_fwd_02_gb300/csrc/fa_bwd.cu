@@ -34,6 +34,7 @@
 #include "ptx.cuh"
 #include "fa_prepass.cuh"
 #include "fa_epilogue.cuh"
+#include "fa_decode_bwd.cuh"
 
 namespace fa {
 using namespace ptx;
@@ -2828,6 +2829,96 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
 
 }  // namespace
 
+namespace {
+
+// The decode backward (fa_decode_bwd.cuh): the keys of each (batch, kv head) split into
+// ranges as for the decode forward, one wave of CTAs; with more than one range, partial
+// dQ in scratch and the fixed-order range sum.
+template <int DK, int ROWS, bool F32IN>
+fa_status run_decode_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                         const float* LSE, void* dQ, void* dK, void* dV, const fa_params& p,
+                         cudaStream_t stream) {
+  DecodeBwdArgs a;
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.O = O;
+  a.dO = dO;
+  a.LSE = LSE;
+  a.dK = dK;
+  a.dV = dV;
+  a.B = p.B;
+  a.H = p.H;
+  a.HKV = p.HKV;
+  a.Sq = p.Sq;
+  a.Sk = p.Sk;
+  a.Dv = p.D;
+  a.rep = p.H / p.HKV;
+  a.rows = a.rep * p.Sq;
+  a.causal = p.causal;
+  a.window = p.window;
+  a.out_bf16 = p.out_dtype == FA_BF16;
+  a.k_wide = reinterpret_cast<uintptr_t>(K) % 32 == 0;
+  a.v_wide = reinterpret_cast<uintptr_t>(V) % 32 == 0;
+  a.scale = p.scale;
+  a.scale_log2 = p.scale * LOG2E;
+  constexpr size_t smem = decode_bwd_smem_bytes<DK, ROWS, F32IN>();
+  auto kern = fa_decode_bwd_kernel<DK, ROWS, F32IN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  // CTAs resident per SM (registers and shared memory), asked once per kernel
+  static const int per_sm = [&] {
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, DEC_WARPS * 32, smem) != cudaSuccess)
+      o = 1;
+    return std::max(o, 1);
+  }();
+  const long long groups = (long long)p.B * p.HKV;
+  const int sms = host::sm_count();
+  const int min_keys = DEC_WARPS * DEC_KEYS;
+  long long n = ((long long)per_sm * sms + groups - 1) / groups;
+  n = std::max(1ll, std::min(n, ((long long)p.Sk + min_keys - 1) / min_keys));
+  int kps = (int)(((long long)p.Sk + n - 1) / n);
+  kps = (kps + DEC_KEYS - 1) / DEC_KEYS * DEC_KEYS;
+  a.keys_per_split = kps;
+  a.n_splits = (p.Sk + kps - 1) / kps;
+  const size_t rows_all = (size_t)p.B * p.H * p.Sq;
+  void* pws = nullptr;
+  if (a.n_splits > 1) {
+    if (host::scratch_alloc(&pws, (size_t)a.n_splits * rows_all * p.D * 4, stream) != cudaSuccess)
+      return FA_ERR_CUDA;
+    a.dQ = pws;
+  } else {
+    a.dQ = dQ;
+  }
+  {
+    host::KernelTimer kt("fa_decode_bwd_kernel", stream);
+    kern<<<dim3((unsigned)groups, (unsigned)a.n_splits), DEC_WARPS * 32, smem, stream>>>(a);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess && a.n_splits > 1) {
+    host::KernelTimer kt("dq_range_sum", stream);
+    const int q4 = p.D / 4;
+    const int sg = std::max(1, std::min({256 / q4, a.n_splits, DEC_SUM_GROUPS}));
+    const dim3 cg((unsigned)std::min<size_t>(rows_all, 65535)), cb(q4, sg);
+    e = launch_programmatic(dq_splits_sum_kernel, cg, cb, stream, (const float*)pws, dQ, a.n_splits,
+                            (int)rows_all, p.D, (int)(p.out_dtype == FA_BF16));
+  }
+  const cudaError_t e2 = host::scratch_free(pws, stream);
+  return (e == cudaSuccess && e2 == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int DK, bool F32IN>
+fa_status run_decode_bwd_rows(const void* Q, const void* K, const void* V, const void* O,
+                              const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                              const fa_params& p, cudaStream_t stream) {
+  if (p.H / p.HKV * p.Sq <= 4)
+    return run_decode_bwd<DK, 4, F32IN>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
+  return run_decode_bwd<DK, DEC_ROWS, F32IN>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
+}
+
+}  // namespace
+
 fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                      const float* LSE, void* dQ, void* dK, void* dV, const fa_params& p,
                      cudaStream_t stream, bool dsmat) {
@@ -2845,6 +2936,16 @@ fa_status launch_bwd(const void* Q, const void* K, const void* V, const void* O,
       zero_kernel<<<grid_pp, 256, 0, stream>>>(static_cast<uint4*>(dV), n16);
     }
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+  // decode shapes (a few query rows per kv head): the CUDA-core backward, for both input
+  // types (the materialised-dS route keeps its own kernels)
+  if (!dsmat && decode_shaped(p)) {
+    const bool f32 = p.in_dtype != FA_BF16;
+    if (p.D <= 64)
+      return f32 ? run_decode_bwd_rows<64, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream)
+                 : run_decode_bwd_rows<64, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
+    return f32 ? run_decode_bwd_rows<128, true>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream)
+               : run_decode_bwd_rows<128, false>(Q, K, V, O, dO, LSE, dQ, dK, dV, p, stream);
   }
   // head dims below a kernel's D run in it with the missing columns read as zeros
   if (p.in_dtype == FA_BF16) {

@@ -360,6 +360,12 @@ fa_decode_kernel(const DecodeArgs a) {
   ptx::grid_launch_dependents();
 }
 
+// Whether fa_fwd and fa_bwd take the decode kernels: every kv head's query rows (the
+// grouped heads' Sq rows each) fit one CTA's DEC_ROWS.
+inline bool decode_shaped(const fa_params& p) {
+  return p.Sk > 0 && (long long)(p.H / p.HKV) * p.Sq <= DEC_ROWS;
+}
+
 template <int DK, int ROWS, bool F32IN>
 constexpr size_t decode_smem_bytes() {
   return decode_v_bytes<DK, F32IN>() +

@@ -1339,12 +1339,6 @@ fa_status run_decode_rows(const void* Q, const void* K, const void* V, void* O, 
 
 }  // namespace
 
-// Whether fa_fwd takes the decode kernel: every kv head's query rows (the grouped heads'
-// Sq rows each) fit one CTA's DEC_ROWS.
-bool decode_shaped(const fa_params& p) {
-  return p.Sk > 0 && (long long)(p.H / p.HKV) * p.Sq <= DEC_ROWS;
-}
-
 fa_status launch_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                      const fa_params& p, cudaStream_t stream) {
   if (p.Sk == 0) {

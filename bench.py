@@ -38,7 +38,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # forward 2 GEMMs (QK^T, PV); dK/dV kernel 4 (S^T, dP^T, dV, dK); dQ kernel 3 (S, dP, dQ).
 # The materialised-dS backward's dQ GEMM: 1 (dS K).
 KERNEL_FLOPS_PER_PAIR_PER_D = {"fa_fwd_kernel": 4, "fa_bwd_dkdv_kernel": 8, "fa_bwd_dq_kernel": 6,
-                               "dq_from_ds_kernel": 2, "fa_decode_kernel": 4}
+                               "dq_from_ds_kernel": 2, "fa_decode_kernel": 4,
+                               "fa_decode_bwd_kernel": 10}
 # Source files whose change invalidates a committed DRAM-traffic figure.
 _COMMON_SOURCES = ["ptx.cuh", "fa_common.cuh", "fa_epilogue.cuh", "fa_prepass.cuh"]
 # head dim of each named workload (traffic figures in profiles/ are for these)
@@ -161,18 +162,40 @@ def flops_for(w):
     return fwd, 2.5 * fwd, vis
 
 
-def step_hbm_bytes(w, out_bytes):
-    """Algorithmic HBM bytes of one fwd + bwd step: every tensor the step takes in read
-    once, every tensor it hands out written once. Forward: Q, K, V in; O, LSE out.
-    Backward: Q, K, V, O, dO, LSE in; dQ, dK, dV out. (in_bytes / out_bytes: element
-    sizes of the inputs and of O, dQ, dK, dV; LSE is fp32.)"""
+def pass_hbm_bytes(w, out_bytes):
+    """Algorithmic HBM bytes of the forward and of the backward pass: every tensor a
+    pass takes in read once, every tensor it hands out written once. Forward: Q, K, V
+    in; O, LSE out. Backward: Q, K, V, O, dO, LSE in; dQ, dK, dV out. (in_bytes /
+    out_bytes: element sizes of the inputs and of O, dQ, dK, dV; LSE is fp32.)"""
     in_bytes = 2 if w.dtype == "bf16" else 4
     nq = w.B * w.H * w.Sq * w.D
     nk = w.B * w.HKV * w.Sk * w.D
     rows = w.B * w.H * w.Sq
     fwd = in_bytes * (nq + 2 * nk) + out_bytes * nq + 4 * rows
     bwd = in_bytes * (2 * nq + 2 * nk) + out_bytes * nq + 4 * rows + out_bytes * (nq + 2 * nk)
-    return fwd + bwd
+    return fwd, bwd
+
+
+def step_hbm_bytes(w, out_bytes):
+    """Algorithmic HBM bytes of one fwd + bwd step (both passes of pass_hbm_bytes)."""
+    return sum(pass_hbm_bytes(w, out_bytes))
+
+
+# Kernels that do a whole pass in one launch and are bound by HBM (the decode shapes'
+# CUDA-core kernels): their roofline is the pass's algorithmic bytes over the launch's
+# time, against the copy bandwidth. Value: the pass (0 forward, 1 backward).
+HBM_PASS_KERNELS = {"fa_decode_kernel": 0, "fa_decode_bwd_kernel": 1}
+
+
+def hbm_roofline(kernel, nbytes, ms_per_launch, peaks, peak_src, traffic):
+    """The roofline entry of an HBM-bound kernel: nbytes algorithmic bytes per launch over
+    its average launch time, against the measured copy bandwidth."""
+    gbs = nbytes / (ms_per_launch * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+            "bytes_per_launch": nbytes,
+            "peak_source": ("measured HBM copy (MEASURED_PEAKS.json)" if peak_src == "measured"
+                            else "fallback 6.8 TB/s copy")}
 
 
 _INPUT_CACHE = {}
@@ -505,7 +528,10 @@ def run_ours(args, rank, world, local_rank):
                      + ("" if w.dtype == "bf16" else
                         " x 1/2, the nominal tf32 / bf16 rate ratio; 3 products per GEMM"
                         if args.f32_mma == "tf32x3" else " (kind::f16); 3 products per GEMM"),
-                     "peak_sustained": peak_sus, "frac_sustained": round(achieved / peak_sus, 4)},
+                     "peak_sustained": peak_sus, "frac_sustained": round(achieved / peak_sus, 4)}
+        if dom_base not in HBM_PASS_KERNELS else
+        hbm_roofline(dom, pass_hbm_bytes(w, 2 if args.out_dtype == "bf16" else 4)[HBM_PASS_KERNELS[dom_base]],
+                     per_kernel[dom]["ms_per_launch"], peaks, peak_src, traffic),
         "kernels": {k_: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
                          for kk, vv in e.items()} for k_, e in per_kernel.items()},
         "e2e": {"value": round(whole_job_tflops(fwd_fl + bwd_fl, world, ms_e2e), 3),

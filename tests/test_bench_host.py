@@ -105,6 +105,24 @@ def test_step_hbm_bytes_counts_each_tensor_once():
     assert bench.step_hbm_bytes(c3, 2) == f32 - 2 * (2 * nq + nq + 2 * nk)
 
 
+def test_decode_kernels_take_the_hbm_roofline_of_their_pass():
+    # the decode shapes' kernels each do a whole pass in one launch: forward = Q, K, V in,
+    # O, LSE out; backward = Q, K, V, O, dO, LSE in, dQ, dK, dV out
+    from attention_fa_fwd_02_gb300.workloads import WORKLOADS
+    w = WORKLOADS["c4"].with_(Sq=1, causal=False, window=0)  # bf16 B1 H16/HKV4 Sk 16384 D128
+    nq, nk, rows = 16 * 128, 4 * 16384 * 128, 16
+    fwd, bwd = bench.pass_hbm_bytes(w, 4)
+    assert fwd == 2 * (nq + 2 * nk) + 4 * nq + 4 * rows
+    assert bwd == 2 * (2 * nq + 2 * nk) + 4 * nq + 4 * rows + 4 * (nq + 2 * nk)
+    assert fwd + bwd == bench.step_hbm_bytes(w, 4)
+    assert set(bench.HBM_PASS_KERNELS) == {"fa_decode_kernel", "fa_decode_bwd_kernel"}
+    peaks = {"bf16_tflops": 1965.9, "bf16_tflops_sustained": 1727.6, "hbm_gbs": 6795.1}
+    r = bench.hbm_roofline("fa_decode_kernel", fwd, 0.02, peaks, "measured", None)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6795.1
+    assert abs(r["achieved"] - fwd / 20e-6 / 1e9) < 0.01
+    assert abs(r["frac"] - r["achieved"] / 6795.1) < 1e-4
+
+
 def test_roofline_denominator_is_the_burst_peak():
     # the kernels are timed for well under a second at full clocks: the burst cuBLAS
     # figure is their denominator, the power-capped sustained one is reported beside it

@@ -55,10 +55,13 @@ def test_backward_small(fa, name):
     _check(w, got, ref, name)
 
 
-@pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa"])
+@pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa", "bf16-decode-sq1",
+                                  "f32-decode-sq2-gqa4-d80"])
 def test_backward_deterministic(fa, name):
     # dK / dV are accumulated per key tile without atomics, dQ per query tile (or per
-    # key range, the ranges then summed in order): bit-identical reruns.
+    # key range, the ranges then summed in a fixed order): bit-identical reruns. (The
+    # decode shapes' backward: every key's dK, dV formed by one lane pair, dQ summed
+    # over the warps and the key ranges in fixed orders.)
     w = SMALL[name]
     q, k, v, do = make_inputs(w)
     a = _gpu_grads(fa, w, q, k, v, do)
@@ -76,7 +79,7 @@ def test_backward_unseen_keys_get_zero_grad(fa):
 
 
 @pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa",
-                                  "bf16-d32-causal-gqa-ragged"])
+                                  "bf16-d32-causal-gqa-ragged", "bf16-decode-rows8-s20000"])
 def test_backward_bf16_outputs(fa, name):
     # bf16 outputs: each gradient element is rounded on store (at most 2^-8 |r|), and
     # the backward forms Delta_i = rowsum(dO * O) from the bf16 O the forward stored,
@@ -93,6 +96,32 @@ def test_backward_bf16_outputs(fa, name):
         assert g.dtype == torch.bfloat16
         ex = bf16_output_excess(to_np(g), r, extra)
         assert ex <= TOL["bf16"]["grad"], f"{name}: {n} excess {ex:.3e}"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_backward_decode_16_byte_aligned_inputs(fa, dtype):
+    # the C ABI promises 16-byte alignment only: Q, K, V and dO here start 16 bytes into
+    # their allocations, so the decode backward reads K and V rows 16 bytes per load
+    base = WORKLOADS["c3"] if dtype == "bf16" else WORKLOADS["c5"]
+    w = base.with_(B=2, H=8, HKV=2, Sq=1, Sk=3001, D=128, scale=128 ** -0.5, causal=False,
+                   window=0, seed=130)
+    q, k, v, do = make_inputs(w)
+    dev = torch.device("cuda:0")
+    pad = 16 // q.element_size()
+
+    def offset_copy(t):
+        buf = torch.empty(t.numel() + pad, dtype=t.dtype, device=dev)
+        view = buf[pad:].view(t.shape)
+        view.copy_(t.to(dev))
+        assert view.data_ptr() % 32 == 16 and view.is_contiguous()
+        return view
+
+    qd, kd, vd, dod = (offset_copy(t) for t in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, w.scale, w.causal, w.window)
+    got = fa.backward(qd, kd, vd, o, lse, dod, w.scale, w.causal, w.window)
+    fa.check_device_status()
+    ref = oracle.attention_bwd(q, k, v, do, w.scale, w.causal, w.window)
+    _check(w, got, ref, f"decode-16B-aligned-{dtype}")
 
 
 @pytest.mark.parametrize("cfg", ["c1", "c2", "c5", "c2-d128"])
