@@ -13,13 +13,14 @@
 //     S_rj  = q_r . k_j and dP_rj = dO_r . v_j, each lane over its half of the dims, one
 //             shuffle adding the halves;
 //     P_rj  = exp(scale S_rj - LSE_r) (visible keys, else 0), dS_rj = P_rj (dP_rj - D_r)
-//             with D_r = dO_r . O_r formed by the CTA for its rows;
-//     dV_j  = sum_r P_rj dO_r and dK_j = scale sum_r dS_rj q_r over the lane's half of the
-//             columns, stored at once: every key belongs to exactly one lane pair of one
-//             CTA, so no sum crosses CTAs and nothing is atomic;
-//     dQ_r += sum_j dS_rj k_j with lane = DK / 32 columns, k_j from a per-warp shared
-//             copy of the chunk's K rows (cp.async), dS through a per-warp [key][row]
-//             buffer -- the forward's PV loop with dS for P and K for V.
+//             with D_r = dO_r . O_r formed by the CTA for its rows; P and dS of the
+//             chunk go to per-warp [key][row] buffers.
+//   Then, key by key, lane = DK / 32 columns (q_r and dO_r of those columns held in
+//   registers, k_j from a per-warp shared copy of the chunk's K rows, cp.async):
+//     dV_j  = sum_r P_rj dO_r and dK_j = scale sum_r dS_rj q_r, stored as whole rows
+//             (coalesced): every key belongs to one warp of one CTA, so no sum crosses
+//             CTAs and nothing is atomic;
+//     dQ_r += dS_rj k_j, rows in pairs.
 //   The 8 warps' dQ sum in warp order in shared memory; the CTA writes its range's
 //   scale * dQ, which dq_splits_sum_kernel adds up in a fixed order -- or, with one
 //   range, dQ itself.
@@ -49,17 +50,18 @@ struct DecodeBwdArgs {
 
 // shared-memory layout: the K buffers [warps][DEC_KEYS][DK] of the input type (after the
 // key loop the dQ merge area [warps][ROWS][DK] fp32 over them), q and dO [ROWS][DK] fp32,
-// dS [warps][DEC_KEYS][ROWS] fp32, then LSE (log2 domain) and D [ROWS]
+// dS and P [warps][DEC_KEYS][ROWS] fp32, then LSE (log2 domain) and D [ROWS]
 template <int DK, int ROWS, bool F32IN>
 constexpr size_t decode_bwd_smem_bytes() {
-  return decode_v_bytes<DK, F32IN>() + 4ull * (2 * ROWS * DK + DEC_WARPS * DEC_KEYS * ROWS + 2 * ROWS);
+  return decode_v_bytes<DK, F32IN>() + 4ull * (2 * ROWS * DK + 2 * DEC_WARPS * DEC_KEYS * ROWS + 2 * ROWS);
 }
 
-// CTAs per SM the kernel is built for, as for the forward (two for 4 rows), except fp32
-// at D = 128, whose K and V half rows alone take 128 registers per thread
+// CTAs per SM the kernel is built for: two at D <= 64 with 4 rows; else one (the K and V
+// halves of the next chunk, q and dO at the lane's columns, and the dQ sums do not fit
+// 128 registers per thread without spilling)
 template <int DK, int ROWS, bool F32IN>
 __host__ __device__ constexpr int decode_bwd_min_ctas() {
-  return ROWS == 4 && !(F32IN && DK == 128) ? 2 : 1;
+  return ROWS == 4 && DK == 64 ? 2 : 1;
 }
 
 template <int DK, int ROWS, bool F32IN>
@@ -80,7 +82,8 @@ fa_decode_bwd_kernel(const DecodeBwdArgs a) {
   float* q_s = reinterpret_cast<float*>(dsm_raw + decode_v_bytes<DK, F32IN>());
   float* do_s = q_s + ROWS * DK;
   float* ds_s = do_s + ROWS * DK;
-  float* lse_s = ds_s + DEC_WARPS * DEC_KEYS * ROWS;
+  float* p_s = ds_s + DEC_WARPS * DEC_KEYS * ROWS;
+  float* lse_s = p_s + DEC_WARPS * DEC_KEYS * ROWS;
   float* dd_s = lse_s + ROWS;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -97,6 +100,7 @@ fa_decode_bwd_kernel(const DecodeBwdArgs a) {
   };
 
   float* dsw = ds_s + warp * DEC_KEYS * ROWS;
+  float* psw = p_s + warp * DEC_KEYS * ROWS;
   T* kw = k_st + warp * DEC_KEYS * DK;
   const uint32_t kw_s = (uint32_t)__cvta_generic_to_shared(kw);
   const int piece = lane % CPR;
@@ -213,6 +217,15 @@ fa_decode_bwd_kernel(const DecodeBwdArgs a) {
     }
   };
 
+  // q_r and dO_r at this lane's columns lane * CPL .., in column pairs
+  float2 q_reg[ROWS][CPL / 2], do_reg[ROWS][CPL / 2];
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+    for (int c2 = 0; c2 < CPL / 2; ++c2) {
+      q_reg[r][c2] = *reinterpret_cast<const float2*>(q_s + r * DK + lane * CPL + 2 * c2);
+      do_reg[r][c2] = *reinterpret_cast<const float2*>(do_s + r * DK + lane * CPL + 2 * c2);
+    }
   float2 dq2[ROWS / 2][CPL];  // (dQ[2 rp][c], dQ[2 rp + 1][c]) at this lane's columns
 #pragma unroll
   for (int rp = 0; rp < ROWS / 2; ++rp)
@@ -244,59 +257,24 @@ fa_decode_bwd_kernel(const DecodeBwdArgs a) {
       P[r] = vis ? exp2f(fmaf(s, a.scale_log2, -lse_s[r])) : 0.f;
       dS[r] = P[r] * (dp - dd_s[r]);
     }
-    // dV_j and dK_j over this lane's half of the columns, 4 at a time
-    if (j < k1) {
-      const size_t orow = kv_base + (size_t)j * a.Dv;
-#pragma unroll 2  // (a full unroll hoists every group's shared loads and spills)
-      for (int d4 = v0 * EPV; d4 < (v0 + NH) * EPV; d4 += 4) {
-        if (d4 < a.Dv) {  // (Dv a multiple of 16: groups of 4 all in or out)
-          float2 av0 = make_float2(0.f, 0.f), av1 = av0, ak0 = av0, ak1 = av0;
-#pragma unroll
-          for (int r = 0; r < ROWS; ++r) {
-            const float4 o4 = *reinterpret_cast<const float4*>(do_s + r * DK + d4);
-            const float4 q4 = *reinterpret_cast<const float4*>(q_s + r * DK + d4);
-            const float2 pp = make_float2(P[r], P[r]), ss = make_float2(dS[r], dS[r]);
-            av0 = __ffma2_rn(pp, make_float2(o4.x, o4.y), av0);
-            av1 = __ffma2_rn(pp, make_float2(o4.z, o4.w), av1);
-            ak0 = __ffma2_rn(ss, make_float2(q4.x, q4.y), ak0);
-            ak1 = __ffma2_rn(ss, make_float2(q4.z, q4.w), ak1);
-          }
-          const float2 sc = make_float2(a.scale, a.scale);
-          ak0 = __fmul2_rn(ak0, sc);
-          ak1 = __fmul2_rn(ak1, sc);
-          if (a.out_bf16) {
-            uint2 uv, uk;
-            __nv_bfloat162 h = __floats2bfloat162_rn(av0.x, av0.y);
-            uv.x = *reinterpret_cast<uint32_t*>(&h);
-            h = __floats2bfloat162_rn(av1.x, av1.y);
-            uv.y = *reinterpret_cast<uint32_t*>(&h);
-            h = __floats2bfloat162_rn(ak0.x, ak0.y);
-            uk.x = *reinterpret_cast<uint32_t*>(&h);
-            h = __floats2bfloat162_rn(ak1.x, ak1.y);
-            uk.y = *reinterpret_cast<uint32_t*>(&h);
-            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.dV) + orow + d4) = uv;
-            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.dK) + orow + d4) = uk;
-          } else {
-            *reinterpret_cast<float4*>(static_cast<float*>(a.dV) + orow + d4) =
-                make_float4(av0.x, av0.y, av1.x, av1.y);
-            *reinterpret_cast<float4*>(static_cast<float*>(a.dK) + orow + d4) =
-                make_float4(ak0.x, ak0.y, ak1.x, ak1.y);
-          }
-        }
-      }
-    }
-    // dS of the chunk's keys into the warp's [key][row] buffer
+    // P and dS of the chunk's keys into the warp's [key][row] buffers
     if (half == 0) {
 #pragma unroll
-      for (int r4 = 0; r4 < ROWS; r4 += 4)
+      for (int r4 = 0; r4 < ROWS; r4 += 4) {
+        *reinterpret_cast<float4*>(psw + kl * ROWS + r4) =
+            make_float4(P[r4], P[r4 + 1], P[r4 + 2], P[r4 + 3]);
         *reinterpret_cast<float4*>(dsw + kl * ROWS + r4) =
             make_float4(dS[r4], dS[r4 + 1], dS[r4 + 2], dS[r4 + 3]);
+      }
     }
     dec_cp_wait_all();
     __syncwarp();
-    // ---- dQ_r += sum_j dS_rj k_j, lane = columns lane * CPL .., rows in pairs
-    if (lane * CPL < a.Dv) {
-#pragma unroll 4
+    // ---- per key of the chunk, lane = columns lane * CPL ..:
+    //   dV_j = sum_r P_rj dO_r and dK_j = scale sum_r dS_rj q_r (q, dO of the lane's
+    //   columns in registers), stored as whole rows; dQ_r += dS_rj k_j (k_j from the
+    //   chunk's shared copy, rows in pairs)
+    if (lane * CPL < a.Dv) {  // (Dv a multiple of 16: a lane's columns are all in or all out)
+#pragma unroll 1
       for (int jj = 0; jj < DEC_KEYS; ++jj) {
         float kv[CPL];
         const T* kp = kw + jj * DK + lane * CPL;
@@ -319,15 +297,65 @@ fa_decode_bwd_kernel(const DecodeBwdArgs a) {
             kv[0] = x.x; kv[1] = x.y;
           }
         }
+        const float* pj = psw + jj * ROWS;
         const float* dj = dsw + jj * ROWS;
+        float2 av[CPL / 2], ak[CPL / 2];  // dV_j, dK_j at the lane's columns, in pairs
+#pragma unroll
+        for (int c2 = 0; c2 < CPL / 2; ++c2) av[c2] = ak[c2] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int r4 = 0; r4 < ROWS; r4 += 4) {
+          const float4 p4 = *reinterpret_cast<const float4*>(pj + r4);
           const float4 d4v = *reinterpret_cast<const float4*>(dj + r4);
+          const float pr[4] = {p4.x, p4.y, p4.z, p4.w}, dr[4] = {d4v.x, d4v.y, d4v.z, d4v.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 pp = make_float2(pr[u], pr[u]), dd = make_float2(dr[u], dr[u]);
+#pragma unroll
+            for (int c2 = 0; c2 < CPL / 2; ++c2) {
+              av[c2] = __ffma2_rn(pp, do_reg[r4 + u][c2], av[c2]);
+              ak[c2] = __ffma2_rn(dd, q_reg[r4 + u][c2], ak[c2]);
+            }
+          }
 #pragma unroll
           for (int c = 0; c < CPL; ++c) {
             const float2 kk = make_float2(kv[c], kv[c]);
             dq2[r4 / 2][c] = __ffma2_rn(make_float2(d4v.x, d4v.y), kk, dq2[r4 / 2][c]);
             dq2[r4 / 2 + 1][c] = __ffma2_rn(make_float2(d4v.z, d4v.w), kk, dq2[r4 / 2 + 1][c]);
+          }
+        }
+        if (j0 + jj < k1) {
+          const size_t o = kv_base + (size_t)(j0 + jj) * a.Dv + lane * CPL;
+          const float2 sc = make_float2(a.scale, a.scale);
+#pragma unroll
+          for (int c2 = 0; c2 < CPL / 2; ++c2) ak[c2] = __fmul2_rn(ak[c2], sc);
+          if (a.out_bf16) {
+            uint32_t uv[CPL / 2], uk[CPL / 2];
+#pragma unroll
+            for (int c2 = 0; c2 < CPL / 2; ++c2) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(av[c2].x, av[c2].y);
+              uv[c2] = *reinterpret_cast<uint32_t*>(&h);
+              h = __floats2bfloat162_rn(ak[c2].x, ak[c2].y);
+              uk[c2] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            __nv_bfloat16* dVo = static_cast<__nv_bfloat16*>(a.dV) + o;
+            __nv_bfloat16* dKo = static_cast<__nv_bfloat16*>(a.dK) + o;
+            if constexpr (CPL == 4) {
+              *reinterpret_cast<uint2*>(dVo) = make_uint2(uv[0], uv[1]);
+              *reinterpret_cast<uint2*>(dKo) = make_uint2(uk[0], uk[1]);
+            } else {
+              *reinterpret_cast<uint32_t*>(dVo) = uv[0];
+              *reinterpret_cast<uint32_t*>(dKo) = uk[0];
+            }
+          } else {
+            float* dVo = static_cast<float*>(a.dV) + o;
+            float* dKo = static_cast<float*>(a.dK) + o;
+            if constexpr (CPL == 4) {
+              *reinterpret_cast<float4*>(dVo) = make_float4(av[0].x, av[0].y, av[1].x, av[1].y);
+              *reinterpret_cast<float4*>(dKo) = make_float4(ak[0].x, ak[0].y, ak[1].x, ak[1].y);
+            } else {
+              *reinterpret_cast<float2*>(dVo) = av[0];
+              *reinterpret_cast<float2*>(dKo) = ak[0];
+            }
           }
         }
       }
