@@ -180,15 +180,19 @@ FA_API unsigned long long fa_noalloc_scratch_bytes(void);
  * P is rebuilt tile by tile from LSE (never stored); D_i = rowsum(dO_i * O_i) is
  * computed first by a preprocess kernel; dK/dV are accumulated per key tile over
  * the grouped query heads without atomics (deterministic: two calls on the same
- * inputs give bit-identical results). Workspace (D_i, the scaled fp16 or hi/lo-split
- * operand copies and their scale factors; for short query sequences with bf16 inputs,
- * fp32 partial dQ of up to 32 key ranges, summed in range order) is stream-ordered
- * from the library pool. O must be the output of fa_fwd for the same inputs (the dS
+ * inputs give bit-identical results). Decode shapes ((H / HKV) * Sq <= 8, as for
+ * fa_fwd) run in one CUDA-core kernel in fp32 for either input type: one pass over K
+ * and V, D_i formed by that kernel, each key's dK / dV formed once, dQ summed over
+ * key ranges in a fixed order. Workspace (D_i, the scaled fp16 or hi/lo-split operand
+ * copies and their scale factors; for short query sequences with bf16 inputs, fp32
+ * partial dQ of up to 32 key ranges, summed in range order; for decode shapes, fp32
+ * partial dQ of as many key ranges as fill the GPU once) is stream-ordered from the
+ * library pool. O must be the output of fa_fwd for the same inputs (the dS
  * scaling bounds D_i by the largest |dO| and |V|). Same ownership, alignment and
- * error rules as fa_fwd. For both input types the dQ kernel is launched on `stream`
- * as a programmatic dependent of the dK/dV kernel: it starts on the SMs that dK/dV
- * leaves idle and completes only after dK/dV has, so work enqueued on `stream`
- * afterwards sees all three gradients. (Inside both calls, most kernels after the
+ * error rules as fa_fwd. Outside decode shapes, for both input types the dQ kernel is
+ * launched on `stream` as a programmatic dependent of the dK/dV kernel: it starts on
+ * the SMs that dK/dV leaves idle and completes only after dK/dV has, so work enqueued
+ * on `stream` afterwards sees all three gradients. (Inside both calls, most kernels after the
  * first are launched as programmatic dependents of the kernel before them; each such
  * kernel waits for that one before it reads its results and before it exits, and the
  * first kernel of a call is an ordinary launch, so stream order as the caller sees it
