@@ -592,8 +592,12 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
   const int warp = warp_id(), lane = lane_id();
   volatile int* abort_flag = &abort_sh;
 
-  const int qt_lin = blockIdx.x / a.BHx;
-  const int bh = blockIdx.x % a.BHx;
+  // work item: (query tile, head) and, with the keys split into ranges (few query
+  // tiles), key range kr of a.tps key tiles, whose partial dQ goes to slab kr
+  const int kr = a.n_splits > 1 ? (int)(blockIdx.x % a.n_splits) : 0;
+  const int w_item = a.n_splits > 1 ? (int)(blockIdx.x / a.n_splits) : (int)blockIdx.x;
+  const int qt_lin = w_item / a.BHx;
+  const int bh = w_item % a.BHx;
   const int qt = a.lpt ? (a.n_tiles - 1 - qt_lin) : qt_lin;
   const int b = bh / a.H, h = bh % a.H;
   const int bg = b * a.HKV + h / (a.H / a.HKV);
@@ -607,8 +611,15 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
     if (a.window > 0 && i0 - a.window + 1 > 0) jmin = i0 - a.window + 1;
     if (jmax < jmin) { kc_lo = 0; kc_hi = 0; }
     else { kc_lo = jmin / CH; kc_hi = jmax / CH + 1; }
+    if (a.n_splits > 1) {  // the range's chunks: key tiles [kr tps, (kr + 1) tps)
+      constexpr int CPT = BLOCK_N / CH;
+      kc_lo = max(kc_lo, kr * a.tps * CPT);
+      kc_hi = min(kc_hi, (kr + 1) * a.tps * CPT);
+      if (kc_hi < kc_lo) kc_hi = kc_lo;
+    }
   }
   const int nc = kc_hi - kc_lo;
+  const int zq = a.n_splits > 1 ? kr * a.BHx + bh : bh;  // dQ slab row block
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
@@ -766,10 +777,10 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       const float mul_q = C::X16 ? a.sc->dq_mul : a.scale;
       if (a.out_bf16)
         store_rows_tma<D, true, D / 64>(&m.dQ, lane_addr + C::Q_ACC, nc > 0, mul_q, st_q, r_base,
-                                        r_base < a.Sq, bh, 0, a.Dv);
+                                        r_base < a.Sq, zq, 0, a.Dv);
       else
         store_rows_tma<D, false, D / 32>(&m.dQ, lane_addr + C::Q_ACC, nc > 0, mul_q, st_q,
-                                         r_base, r_base < a.Sq, bh, 0, a.Dv);
+                                         r_base, r_base < a.Sq, zq, 0, a.Dv);
     }
   }
   tc_fence_before();
@@ -2425,13 +2436,16 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   const int n_pre = 8 * host::sm_count();  // pre-pass blocks
   const size_t sc_off = (bytes + 255) / 256 * 256;
   if constexpr (!C::TF32) bytes = sc_off + 256 + (size_t)n_pre * 5 * 4;
-  // Fewer query tiles than SMs (short query sequences, bf16 inputs): the dQ work items
-  // also split the keys into ranges of tps tiles (key_range_tiles picks tps), each
-  // range writing a partial dQ (fp32) that a sum kernel adds up afterwards.
+  // Fewer query tiles than SMs (short query sequences): the dQ work items also split the
+  // keys into ranges of tps tiles (key_range_tiles picks tps), each range writing a
+  // partial dQ (fp32) that a sum kernel adds up afterwards. The fp32 dQ kernel is not
+  // persistent (one CTA per item): it splits only below half the SMs, so that a grid
+  // which nearly fills the GPU in one wave keeps that wave.
   const int sms = host::sm_count();
   const int n_qt = (p.Sq + BLOCK_M - 1) / BLOCK_M, n_kt = (p.Sk + BLOCK_N - 1) / BLOCK_N;
   int dq_tps = n_kt;
-  if (!F32 && BH * n_qt < (size_t)sms) dq_tps = key_range_tiles((int)BH * n_qt, n_kt, sms);
+  if (F32 ? 2 * BH * n_qt <= (size_t)sms : BH * n_qt < (size_t)sms)
+    dq_tps = key_range_tiles((int)BH * n_qt, n_kt, sms);
   const int dq_splits = (n_kt + dq_tps - 1) / dq_tps;
   const size_t part_off = (bytes + 255) / 256 * 256;  // partial dQ [splits][BH][Sq][Dv]
   if (dq_splits > 1) bytes = part_off + (size_t)dq_splits * nq * 4;
@@ -2749,8 +2763,16 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
                              stream);
         // starts once every dK / dV block has, on the SMs that grid leaves free (it reads
         // nothing that grid writes; it waits for it before exiting)
-        e = launch_programmatic_smem(kern, dim3((unsigned)(BH * aq.n_tiles)), dim3(C::THREADS),
-                                     C::Q_SMEM, stream, mq, aq);
+        e = launch_programmatic_smem(kern, dim3((unsigned)(BH * aq.n_tiles * dq_splits)),
+                                     dim3(C::THREADS), C::Q_SMEM, stream, mq, aq);
+      }
+      if (e == cudaSuccess && dq_splits > 1) {
+        host::KernelTimer kt("dq_range_sum", stream);
+        dim3 cg, cb;
+        combine_launch_shape((int)BH, p.Sq, Dv, &cg, &cb);
+        e = launch_programmatic(dq_range_sum_kernel, cg, cb, stream, (const float*)dq_part, dQ,
+                                dq_tps, (int)BH, p.Sq, p.Sk, (int)p.causal, p.window, Dv,
+                                (int)(p.out_dtype == FA_BF16));
       }
     } else if (D >= 64 && dsmat) {
       // dQ = scale dS K over the stored dS^T (an ordinary launch: it reads what the

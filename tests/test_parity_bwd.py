@@ -56,7 +56,7 @@ def test_backward_small(fa, name):
 
 
 @pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa", "bf16-decode-sq1",
-                                  "f32-decode-sq2-gqa4-d80"])
+                                  "f32-decode-sq2-gqa4-d80", "f32-decode"])
 def test_backward_deterministic(fa, name):
     # dK / dV are accumulated per key tile without atomics, dQ per query tile (or per
     # key range, the ranges then summed in a fixed order): bit-identical reruns. (The
