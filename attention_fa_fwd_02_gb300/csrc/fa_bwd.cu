@@ -1436,7 +1436,7 @@ __device__ __forceinline__ void split_half2(float a, float b, uint32_t& hi, uint
 // forms (this thread's key j, its part's QC queries: 2 QC bytes per term) to a.ds_hi
 // (and a.ds_lo), from which dq_from_ds_kernel forms dQ = scale dS K as a GEMM instead
 // of recomputing S and dP.
-template <int D, bool SPLIT, bool MATDS>
+template <int D, bool SPLIT, bool MATDS, bool QSPLIT = false>
 __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
     fa_bwd_dkdv16_kernel(const __grid_constant__ KVMaps m, const BwdArgs a) {
   using C = Dkv16Cfg<D>;
@@ -1475,19 +1475,36 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
   // CTA walks items in rounds of gridDim.x, item c of even rounds and G - 1 - c of odd
   // ones (one round when the grid has a CTA per item). (A host-side longest-first
   // assignment to the least loaded CTA measured 1-3% slower than these rounds.)
-  const int n_items = a.n_tiles * a.BHx;
-  struct Item { int bg, b, g, j0, qt_lo, ncq, nc; };
+  // QSPLIT (fewer (kv head, key tile) items than SMs: short key sequences): the queries
+  // are also split into a.n_splits ranges of a.tps query tiles, item w = (jt * BHx + bg)
+  // * n_splits + range, each writing partial dK, dV to slab range * BHx + bg (z). (A
+  // template flag: the unsplit kernel stays exactly as it was, which a runtime flag did
+  // not -- it cost the C3 dK / dV kernel 2%.)
+  const int n_qs = QSPLIT ? a.n_splits : 1;
+  const int n_items = a.n_tiles * a.BHx * n_qs;
+  struct Item { int bg, b, g, j0, qt_lo, ncq, nc, z; };
   auto item = [&](int w) {
     Item it;
-    const int jt = w / a.BHx;
-    it.bg = w % a.BHx;
+    int qs = 0, wk = w;
+    if constexpr (QSPLIT) {
+      qs = w % n_qs;
+      wk = w / n_qs;
+    }
+    const int jt = wk / a.BHx;
+    it.bg = wk % a.BHx;
     it.b = it.bg / a.HKV;
     it.g = it.bg % a.HKV;
     it.j0 = jt * BLOCK_N;
     int qt_hi;
     q_tile_range(it.j0, min(it.j0 + BLOCK_N - 1, a.Sk - 1), a.Sq, a.causal, a.window, &it.qt_lo, &qt_hi);
+    if constexpr (QSPLIT) {
+      it.qt_lo = max(it.qt_lo, qs * a.tps);
+      qt_hi = min(qt_hi, (qs + 1) * a.tps);
+      if (qt_hi < it.qt_lo) qt_hi = it.qt_lo;
+    }
     it.ncq = qt_hi - it.qt_lo;
     it.nc = rep * it.ncq;
+    it.z = QSPLIT ? qs * a.BHx + it.bg : it.bg;
     return it;
   };
   auto item_w = [&](int k) {
@@ -1869,17 +1886,17 @@ __global__ void __launch_bounds__(Dkv16Cfg<D>::THREADS, 1)
       if (D >= 64 && a.out_bf16) {  // (bf16 outputs: D >= 64 kernels only)
         if constexpr (D >= 64) {
           if constexpr (DW % 64 == 0) {
-            store_rows_tma<DW, true, 1>(tm, acc, it.nc > 0, mul, stage, r_base, any, it.bg, cpart * DW,
+            store_rows_tma<DW, true, 1>(tm, acc, it.nc > 0, mul, stage, r_base, any, it.z, cpart * DW,
                                         a.Dv);
           } else {
             // a bf16 box is a 64-column row: one warp per output does it
             if (cpart == 0)
               store_rows_tma<D, true, 1>(tm, lane_addr + (which ? C::DK : C::DV), it.nc > 0, mul, stage,
-                                         r_base, any, it.bg, 0, a.Dv);
+                                         r_base, any, it.z, 0, a.Dv);
           }
         }
       } else {
-        store_rows_tma<DW, false, 1>(tm, acc, it.nc > 0, mul, stage, r_base, any, it.bg, cpart * DW, a.Dv);
+        store_rows_tma<DW, false, 1>(tm, acc, it.nc > 0, mul, stage, r_base, any, it.z, cpart * DW, a.Dv);
       }
       tc_fence_before();  // (the accumulator loads precede every later hand-off)
     }
@@ -2449,6 +2466,15 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   const int dq_splits = (n_kt + dq_tps - 1) / dq_tps;
   const size_t part_off = (bytes + 255) / 256 * 256;  // partial dQ [splits][BH][Sq][Dv]
   if (dq_splits > 1) bytes = part_off + (size_t)dq_splits * nq * 4;
+  // Fewer (kv head, key tile) items than SMs (short key sequences; bf16 inputs, the
+  // recompute route): the dK / dV items also split the queries into ranges of kv_qtps
+  // tiles, each range writing partial dK and dV (fp32) that a sum kernel adds up.
+  int kv_qtps = n_qt;
+  if (!F32 && !dsmat && !split_operands(p.H / p.HKV, n_qt) && BHk * n_kt < (size_t)sms)
+    kv_qtps = key_range_tiles((int)BHk * n_kt, n_qt, sms);
+  const int kv_splits = (n_qt + kv_qtps - 1) / kv_qtps;
+  const size_t kvp_off = (bytes + 255) / 256 * 256;  // partial dK then dV [splits][BHk][Sk][Dv]
+  if (kv_splits > 1) bytes = kvp_off + 2 * (size_t)kv_splits * nk * 4;
   // two-term P / dS for short query sequences (see split_operands)
   const bool split = !F32 && split_operands(p.H / p.HKV, n_qt);
   // materialised dS^T: [B*H][Sk][ldq] fp16, one buffer per term
@@ -2464,6 +2490,7 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
       C::TF32 ? nullptr : reinterpret_cast<OperandScales*>(static_cast<char*>(ws) + sc_off);
   uint32_t* part = C::TF32 ? nullptr : reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + sc_off + 256);
   float* dq_part = dq_splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(ws) + part_off) : nullptr;
+  float* kv_part = kv_splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(ws) + kvp_off) : nullptr;
   __half* ds_hi = dsmat ? reinterpret_cast<__half*>(static_cast<char*>(ws) + ds_off) : nullptr;
   __half* ds_lo = dsmat && split ? ds_hi + ds_elems : nullptr;
   const int grid_pp = 4 * sms;
@@ -2477,8 +2504,15 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     const bool bf = p.out_dtype == FA_BF16;
     const auto odt = bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : F32T;
     const int oes = bf ? 2 : 4;
-    enc &= host::encode_tiled_3d(&mk.dK, odt, oes, dK, Dv, p.Sk, BHk, Dv, 128 / oes, 32);
-    enc &= host::encode_tiled_3d(&mk.dV, odt, oes, dV, Dv, p.Sk, BHk, Dv, 128 / oes, 32);
+    if (kv_splits > 1) {
+      const uint64_t zs = (uint64_t)kv_splits * BHk;
+      enc &= host::encode_tiled_3d(&mk.dK, F32T, 4, kv_part, Dv, p.Sk, zs, Dv, 32, 32);
+      enc &= host::encode_tiled_3d(&mk.dV, F32T, 4, kv_part + (size_t)kv_splits * nk, Dv, p.Sk, zs, Dv,
+                                   32, 32);
+    } else {
+      enc &= host::encode_tiled_3d(&mk.dK, odt, oes, dK, Dv, p.Sk, BHk, Dv, 128 / oes, 32);
+      enc &= host::encode_tiled_3d(&mk.dV, odt, oes, dV, Dv, p.Sk, BHk, Dv, 128 / oes, 32);
+    }
     if (dq_splits > 1)
       enc &= host::encode_tiled_3d(&mq.dQ, F32T, 4, dq_part, Dv, p.Sq, (uint64_t)dq_splits * BH, Dv,
                                    32, 32);
@@ -2715,6 +2749,9 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     BwdArgs ak = a;
     ak.n_tiles = (p.Sk + BLOCK_N - 1) / BLOCK_N;
     ak.BHx = (int)BHk;
+    ak.n_splits = kv_splits;  // query ranges of the dK / dV items
+    ak.tps = kv_qtps;
+    if (kv_splits > 1) ak.out_bf16 = 0;  // the partial sums are fp32
     if constexpr (F32) {
       auto kern = fa_bwd_dkdv_kernel<D, F32>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::KV_SMEM);
@@ -2728,6 +2765,7 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     } else {
       using C16 = Dkv16Cfg<D>;
       auto kern = split ? fa_bwd_dkdv16_kernel<D, true, false> : fa_bwd_dkdv16_kernel<D, false, false>;
+      if (kv_splits > 1) kern = fa_bwd_dkdv16_kernel<D, false, false, true>;  // (never with split)
       if constexpr (D >= 64)  // (the materialised-dS route runs in the D >= 64 kernels)
         if (dsmat) kern = split ? fa_bwd_dkdv16_kernel<D, true, true> : fa_bwd_dkdv16_kernel<D, false, true>;
       // all the dynamic shared memory a block may have: the layout fills it after
@@ -2740,8 +2778,9 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
         host::KernelTimer kt(D == 128 ? "fa_bwd_dkdv_kernel<128,bf16>"
                                       : (D == 64 ? "fa_bwd_dkdv_kernel<64,bf16>" : "fa_bwd_dkdv_kernel<32,bf16>"),
                              stream);
-        // persistent: one CTA per SM (at most), walking the (key tile, kv head) items
-        const unsigned grid = (unsigned)std::min<size_t>(BHk * ak.n_tiles, (size_t)sms);
+        // persistent: one CTA per SM (at most), walking the (key tile, kv head, query
+        // range) items
+        const unsigned grid = (unsigned)std::min<size_t>(BHk * ak.n_tiles * kv_splits, (size_t)sms);
         // a programmatic dependent of the scales kernel (it waits for it first)
         e = launch_programmatic_smem(kern, dim3(grid), dim3(C16::THREADS), (size_t)dyn, stream, mk, ak);
       }
@@ -2844,6 +2883,22 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
                                 (int)(p.out_dtype == FA_BF16));
       }
     }
+  }
+  if (e == cudaSuccess && kv_splits > 1) {
+    // dK, dV = the sums of the query ranges' partial slabs, in a fixed order
+    // (programmatic dependents of the launch before them, which completes after dK / dV)
+    host::KernelTimer kt("dkv_range_sum", stream);
+    const int q4 = Dv / 4;
+    const int sg = std::max(1, std::min({256 / q4, kv_splits, DEC_SUM_GROUPS}));
+    const size_t rows = BHk * (size_t)p.Sk;
+    const dim3 cg((unsigned)std::min<size_t>(rows, 65535)), cb(q4, sg);
+    const int obf = (int)(p.out_dtype == FA_BF16);
+    e = launch_programmatic(dq_splits_sum_kernel, cg, cb, stream, (const float*)kv_part, dK, kv_splits,
+                            (int)rows, Dv, obf);
+    if (e == cudaSuccess)
+      e = launch_programmatic(dq_splits_sum_kernel, cg, cb, stream,
+                              (const float*)(kv_part + (size_t)kv_splits * nk), dV, kv_splits, (int)rows,
+                              Dv, obf);
   }
   const cudaError_t e2 = host::scratch_free(ws, stream);
   return (e == cudaSuccess && e2 == cudaSuccess) ? FA_OK : FA_ERR_CUDA;

@@ -242,6 +242,8 @@ def workload_of(args):
                     name=w.name.replace(f"-d{w.D}-", f"-d{args.head_dim}-"))
     if args.sq and args.sq != w.Sq:  # short query sequence against the same keys
         w = w.with_(Sq=args.sq, name=f"{w.name}-sq{args.sq}")
+    if args.sk and args.sk != w.Sk:  # short key sequence for the same queries
+        w = w.with_(Sk=args.sk, name=f"{w.name}-sk{args.sk}")
     if args.non_causal and w.causal:
         w = w.with_(causal=False, window=0, name=f"{w.name}-noncausal")
     return w
@@ -499,6 +501,7 @@ def run_ours(args, rank, world, local_rank):
     achieved = per_kernel[dom]["tflops"]
     traffic = (committed_traffic(dom_base, args.workload)
                if w.D == WORKLOADS_D[args.workload] and args.out_dtype == "f32" and not args.sq
+               and not args.sk
                and not args.non_causal and args.f32_mma == "f16x2" and args.bwd == "recompute"
                else None)
     cpu = None
@@ -562,6 +565,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sq", type=int, default=None,
                     help="query rows per head (measurement lines, e.g. decode-shaped)")
+    ap.add_argument("--sk", type=int, default=None,
+                    help="key rows per kv head (measurement lines, e.g. short key sequences)")
     ap.add_argument("--non-causal", action="store_true",
                     help="full attention over the keys (measurement lines)")
     ap.add_argument("--out-dtype", choices=["f32", "bf16"], default="f32",

@@ -56,8 +56,9 @@ def test_visible_fractions_and_flops_of_the_five_workloads():
 
 
 class _Args:
-    def __init__(self, workload="c3", head_dim=None, sq=None, non_causal=False):
+    def __init__(self, workload="c3", head_dim=None, sq=None, non_causal=False, sk=None):
         self.workload, self.head_dim, self.sq, self.non_causal = workload, head_dim, sq, non_causal
+        self.sk = sk
 
 
 def test_workload_options():
@@ -67,6 +68,8 @@ def test_workload_options():
     w = bench.workload_of(_Args(workload="c4", sq=128, non_causal=True))
     assert (w.Sq, w.Sk, w.causal, w.window) == (128, 16384, False, 0)
     assert "sq128" in w.name and "noncausal" in w.name
+    w = bench.workload_of(_Args(workload="c4", sk=256))
+    assert (w.Sq, w.Sk) == (16384, 256) and "sk256" in w.name
 
 
 def test_traffic_is_reported_only_for_the_sources_it_was_measured_on(monkeypatch):

@@ -56,7 +56,8 @@ def test_backward_small(fa, name):
 
 
 @pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa", "bf16-decode-sq1",
-                                  "f32-decode-sq2-gqa4-d80", "f32-decode"])
+                                  "f32-decode-sq2-gqa4-d80", "f32-decode",
+                                  "bf16-short-keys-causal-window"])
 def test_backward_deterministic(fa, name):
     # dK / dV are accumulated per key tile without atomics, dQ per query tile (or per
     # key range, the ranges then summed in a fixed order): bit-identical reruns. (The
@@ -79,7 +80,8 @@ def test_backward_unseen_keys_get_zero_grad(fa):
 
 
 @pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa",
-                                  "bf16-d32-causal-gqa-ragged", "bf16-decode-rows8-s20000"])
+                                  "bf16-d32-causal-gqa-ragged", "bf16-decode-rows8-s20000",
+                                  "bf16-short-keys"])
 def test_backward_bf16_outputs(fa, name):
     # bf16 outputs: each gradient element is rounded on store (at most 2^-8 |r|), and
     # the backward forms Delta_i = rowsum(dO * O) from the bf16 O the forward stored,

@@ -93,6 +93,13 @@ SMALL = {
     "f32-decode-sq1-d32-causal": C5.with_(H=3, Sq=1, Sk=777, D=32, scale=32 ** -0.5,
                                           causal=True, seed=65),
     "f32-decode-sq8-window3": C5.with_(Sq=8, Sk=3000, window=3, seed=66),
+    # short key sequences: fewer (kv head, key tile) dK / dV items than SMs, so the bf16
+    # backward splits the queries into ranges (partial dK, dV summed afterwards)
+    "bf16-short-keys": C3.with_(B=1, H=4, HKV=1, Sq=3000, Sk=200, causal=False, seed=67),
+    "bf16-short-keys-causal-window": C4.with_(B=1, H=4, HKV=2, Sq=2500, Sk=300, window=700,
+                                              seed=68),
+    "bf16-short-keys-d64-gqa": C3.with_(B=2, H=6, HKV=3, Sq=2048, Sk=64, D=64, scale=0.125,
+                                        seed=69),
     # bf16 inputs far outside fp16's range (largest finite 65504, normal from 2^-14):
     # the fp16 operand copies must be scaled by powers of two (gradients dO of 1e-7,
     # V of 1e5, Q and K of 2^-20, dO of 1e4 and V of 1e-6; alone and together)
