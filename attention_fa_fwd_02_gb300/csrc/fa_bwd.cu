@@ -304,7 +304,7 @@ __device__ __forceinline__ void tmem_st_operand(uint32_t hi, uint32_t lo, const 
 }
 
 // ------------------------------------------------------------------ dK / dV
-template <int D, int F32>
+template <int D, int F32, bool QSPLIT = false>
 __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ KVMaps m, const BwdArgs a) {
   using C = BwdCfg<D, F32>;
@@ -333,8 +333,13 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
   volatile int* abort_flag = &abort_sh;
 
   // Key tile 0 is seen by the most queries under a causal mask: schedule it first.
-  const int jt = blockIdx.x / a.BHx;
-  const int bg = blockIdx.x % a.BHx;
+  // QSPLIT (few items: short key sequences): each also takes query range kr of a.tps
+  // query tiles, writing partial dK, dV to slab kr. (A template flag: as a runtime one it
+  // cost the unsplit C5 kernel 2%.)
+  const int kr = QSPLIT ? (int)(blockIdx.x % a.n_splits) : 0;
+  const unsigned w_item = QSPLIT ? blockIdx.x / a.n_splits : blockIdx.x;  // (unsigned, as before)
+  const int jt = w_item / a.BHx;
+  const int bg = w_item % a.BHx;
   const int b = bg / a.HKV, g = bg % a.HKV;
   const int rep = a.H / a.HKV;
   const int j0 = jt * BLOCK_N;
@@ -348,9 +353,16 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
     }
     if (imax < imin) { qc_lo = 0; qc_hi = 0; }
     else { qc_lo = imin / CH; qc_hi = imax / CH + 1; }
+    if constexpr (QSPLIT) {  // the range's chunks: query tiles [kr tps, (kr + 1) tps)
+      constexpr int CPT = BLOCK_M / CH;
+      qc_lo = max(qc_lo, kr * a.tps * CPT);
+      qc_hi = min(qc_hi, (kr + 1) * a.tps * CPT);
+      if (qc_hi < qc_lo) qc_hi = qc_lo;
+    }
   }
   const int ncq = qc_hi - qc_lo;
   const int nc = rep * ncq;
+  const int zkv = QSPLIT ? kr * a.BHx + bg : bg;  // dK / dV slab row block
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_kv, 1);
@@ -553,14 +565,14 @@ __global__ void __launch_bounds__(BwdCfg<D, F32>::THREADS, 1)
       const float mul_v = C::X16 ? a.sc->dv_mul : 1.f, mul_k = C::X16 ? a.sc->dk_mul : a.scale;
       if (a.out_bf16) {
         store_rows_tma<D, true, D / 64, false>(&m.dV, lane_addr + C::KV_ACC0, nc > 0, mul_v, st_v,
-                                               r_base, any, bg, 0, a.Dv);
+                                               r_base, any, zkv, 0, a.Dv);
         store_rows_tma<D, true, D / 64, false>(&m.dK, lane_addr + C::KV_ACC1, nc > 0, mul_k, st_k,
-                                               r_base, any, bg, 0, a.Dv);
+                                               r_base, any, zkv, 0, a.Dv);
       } else {
         store_rows_tma<D, false, D / 32, false>(&m.dV, lane_addr + C::KV_ACC0, nc > 0, mul_v, st_v,
-                                                r_base, any, bg, 0, a.Dv);
+                                                r_base, any, zkv, 0, a.Dv);
         store_rows_tma<D, false, D / 32, false>(&m.dK, lane_addr + C::KV_ACC1, nc > 0, mul_k, st_k,
-                                                r_base, any, bg, 0, a.Dv);
+                                                r_base, any, zkv, 0, a.Dv);
       }
       if (lane == 0) bulk_wait_read_all();
       __syncwarp();
@@ -2466,11 +2478,13 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
   const int dq_splits = (n_kt + dq_tps - 1) / dq_tps;
   const size_t part_off = (bytes + 255) / 256 * 256;  // partial dQ [splits][BH][Sq][Dv]
   if (dq_splits > 1) bytes = part_off + (size_t)dq_splits * nq * 4;
-  // Fewer (kv head, key tile) items than SMs (short key sequences; bf16 inputs, the
-  // recompute route): the dK / dV items also split the queries into ranges of kv_qtps
+  // Fewer (kv head, key tile) items than SMs (short key sequences; for bf16 inputs the
+  // plain recompute route, for fp32 -- whose kernel runs one CTA per item -- at most
+  // half the SMs): the dK / dV items also split the queries into ranges of kv_qtps
   // tiles, each range writing partial dK and dV (fp32) that a sum kernel adds up.
   int kv_qtps = n_qt;
-  if (!F32 && !dsmat && !split_operands(p.H / p.HKV, n_qt) && BHk * n_kt < (size_t)sms)
+  if (F32 ? 2 * BHk * n_kt <= (size_t)sms
+          : !dsmat && !split_operands(p.H / p.HKV, n_qt) && BHk * n_kt < (size_t)sms)
     kv_qtps = key_range_tiles((int)BHk * n_kt, n_qt, sms);
   const int kv_splits = (n_qt + kv_qtps - 1) / kv_qtps;
   const size_t kvp_off = (bytes + 255) / 256 * 256;  // partial dK then dV [splits][BHk][Sk][Dv]
@@ -2753,14 +2767,14 @@ fa_status run_bwd(const void* Q, const void* K, const void* V, const void* O, co
     ak.tps = kv_qtps;
     if (kv_splits > 1) ak.out_bf16 = 0;  // the partial sums are fp32
     if constexpr (F32) {
-      auto kern = fa_bwd_dkdv_kernel<D, F32>;
+      auto kern = kv_splits > 1 ? fa_bwd_dkdv_kernel<D, F32, true> : fa_bwd_dkdv_kernel<D, F32>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::KV_SMEM);
       if (e == cudaSuccess) {
         host::KernelTimer kt(C::TF32 ? "fa_bwd_dkdv_kernel<64,tf32>"
                              : (D == 128 ? "fa_bwd_dkdv_kernel<128,f32>" : "fa_bwd_dkdv_kernel<64,f32>"),
                              stream);
-        e = launch_programmatic_smem(kern, dim3((unsigned)(BHk * ak.n_tiles)), dim3(C::THREADS),
-                                     C::KV_SMEM, stream, mk, ak);
+        e = launch_programmatic_smem(kern, dim3((unsigned)(BHk * ak.n_tiles * kv_splits)),
+                                     dim3(C::THREADS), C::KV_SMEM, stream, mk, ak);
       }
     } else {
       using C16 = Dkv16Cfg<D>;

@@ -57,7 +57,7 @@ def test_backward_small(fa, name):
 
 @pytest.mark.parametrize("name", ["bf16-gqa-causal-ragged", "bf16-decode-gqa", "bf16-decode-sq1",
                                   "f32-decode-sq2-gqa4-d80", "f32-decode",
-                                  "bf16-short-keys-causal-window"])
+                                  "bf16-short-keys-causal-window", "f32-short-keys-gqa-window"])
 def test_backward_deterministic(fa, name):
     # dK / dV are accumulated per key tile without atomics, dQ per query tile (or per
     # key range, the ranges then summed in a fixed order): bit-identical reruns. (The
@@ -124,6 +124,20 @@ def test_backward_decode_16_byte_aligned_inputs(fa, dtype):
     fa.check_device_status()
     ref = oracle.attention_bwd(q, k, v, do, w.scale, w.causal, w.window)
     _check(w, got, ref, f"decode-16B-aligned-{dtype}")
+
+
+def test_backward_short_keys_tf32x3(fa):
+    # fp32 through the 3xTF32 kernels with few key tiles: the dK / dV items split the
+    # queries into ranges there too
+    w = SMALL["f32-short-keys"]
+    q, k, v, do = make_inputs(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, w.scale, w.causal, w.window, f32_mma="tf32x3")
+    got = fa.backward(qd, kd, vd, o, lse, dod, w.scale, w.causal, w.window, f32_mma="tf32x3")
+    fa.check_device_status()
+    ref = oracle.attention_bwd(q, k, v, do, w.scale, w.causal, w.window)
+    _check(w, got, ref, "f32-short-keys-tf32x3")
 
 
 @pytest.mark.parametrize("cfg", ["c1", "c2", "c5", "c2-d128"])

@@ -100,6 +100,10 @@ SMALL = {
                                               seed=68),
     "bf16-short-keys-d64-gqa": C3.with_(B=2, H=6, HKV=3, Sq=2048, Sk=64, D=64, scale=0.125,
                                         seed=69),
+    # (fp32: the one-CTA-per-item dK / dV kernel splits below half the SMs)
+    "f32-short-keys": C5.with_(Sq=3000, Sk=200, seed=70),
+    "f32-short-keys-gqa-window": C2.with_(B=1, H=4, HKV=2, Sq=2000, Sk=256, window=500, seed=75),
+    "f32-short-keys-d128": C5.with_(Sq=1500, Sk=130, D=128, scale=128 ** -0.5, seed=76),
     # bf16 inputs far outside fp16's range (largest finite 65504, normal from 2^-14):
     # the fp16 operand copies must be scaled by powers of two (gradients dO of 1e-7,
     # V of 1e5, Q and K of 2^-20, dO of 1e4 and V of 1e-6; alone and together)
