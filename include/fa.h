@@ -185,9 +185,9 @@ FA_API unsigned long long fa_noalloc_scratch_bytes(void);
  * and V, D_i formed by that kernel, each key's dK / dV formed once, dQ summed over
  * key ranges in a fixed order. Workspace (D_i, the scaled fp16 or hi/lo-split operand
  * copies and their scale factors; for short query sequences with bf16 inputs, fp32
- * partial dQ of up to 32 key ranges, summed in range order; for short key sequences
- * with bf16 inputs, fp32 partial dK and dV of up to 32 query ranges, summed in range
- * order; for decode shapes, fp32 partial dQ of as many key ranges as fill the GPU
+ * partial dQ of up to 32 key ranges, summed in range order; for short key
+ * sequences, fp32 partial dK and dV of up to 32 query ranges, summed in range order;
+ * for decode shapes, fp32 partial dQ of as many key ranges as fill the GPU
  * once) is stream-ordered from the library pool. O must be the output of fa_fwd for the same inputs (the dS
  * scaling bounds D_i by the largest |dO| and |V|). Same ownership, alignment and
  * error rules as fa_fwd. Outside decode shapes, for both input types the dQ kernel is
