@@ -3,7 +3,7 @@
 A caller that runs the same attention shapes over and over captures the calls once
 and replays the graph. The library's stream-ordered scratch (pool allocations) and
 the kernels' programmatic dependent launches (the dQ kernel after dK/dV; the fp32
-path's chains) must both survive capture; every replay must recompute all outputs (they are overwritten with NaN
+path's chains; the key- and query-range sums) must both survive capture; every replay must recompute all outputs (they are overwritten with NaN
 before each replay) and match eager calls bit for bit -- the kernels are
 deterministic (dK/dV without atomics; the dQ items each computed by one CTA).
 """
@@ -25,6 +25,14 @@ CASES = {
     # fp32 kernels run as chains of programmatic dependent launches)
     "f32-tf32x3": WORKLOADS["c2"].with_(B=1, H=4, HKV=2, Sq=300, Sk=300, seed=35),
     "f32-d128-decode": WORKLOADS["c5"].with_(Sq=100, Sk=3000, D=128, scale=128 ** -0.5, seed=36),
+    # decode shapes (at most 8 query rows per kv head): the CUDA-core kernels, their
+    # key-range partials and the fixed-order merges launched as programmatic dependents
+    "bf16-decode-sq1": WORKLOADS["c3"].with_(B=1, H=8, HKV=2, Sq=1, Sk=5000, causal=False,
+                                             seed=37),
+    "f32-decode-sq2": WORKLOADS["c5"].with_(Sq=2, Sk=3000, seed=38),
+    # short key sequences: the dK / dV items split the queries into ranges, summed after dQ
+    "bf16-short-keys": WORKLOADS["c3"].with_(B=1, H=4, HKV=1, Sq=3000, Sk=200, causal=False,
+                                             seed=39),
 }
 MMA = {"f32-tf32x3": "tf32x3"}
 
