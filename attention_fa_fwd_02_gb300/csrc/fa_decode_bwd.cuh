@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, (decode_bwd_min_ctas<DK, ROWS,
 fa_decode_bwd_kernel(const DecodeBwdArgs a) {
   static_assert(DK == 64 || DK == 128, "head dims up to 64 or 128: 2 or 4 columns per lane");
   static_assert(ROWS % 4 == 0 && ROWS <= DEC_ROWS, "rows per kv head: 4 or 8");
+  static_assert(ROWS <= DEC_WARPS, "warp r forms row r's D_r");
   static_assert((size_t)DEC_WARPS * ROWS * DK * 4 <= decode_v_bytes<DK, F32IN>(),
                 "the dQ merge area fits over the K buffers");
   constexpr int CPL = DK / 32;
