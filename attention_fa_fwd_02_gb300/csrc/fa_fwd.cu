@@ -1258,9 +1258,11 @@ fa_status run_fwd(const void* Q, const void* K, const void* V, void* O, float* L
 // so that one wave of CTAs (as many per SM as fit) streams K and V, each range at least
 // one chunk per warp; with more than one range, partial O / LSE in scratch and the
 // range-order combine.
+// (fixed_ws: the no-allocation entry point's array, FA_NOALLOC_SCRATCH_BYTES, for the
+// partial results instead of the memory pool)
 template <int DK, int ROWS, bool F32IN>
 fa_status run_decode(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                     const fa_params& p, cudaStream_t stream) {
+                     const fa_params& p, cudaStream_t stream, void* fixed_ws = nullptr) {
   DecodeArgs a;
   a.Q = Q;
   a.K = K;
@@ -1301,9 +1303,13 @@ fa_status run_decode(const void* Q, const void* K, const void* V, void* O, float
   const size_t rows_all = (size_t)p.B * p.H * p.Sq;
   void* pws = nullptr;
   if (a.n_splits > 1) {
-    if (host::scratch_alloc(&pws, ((size_t)a.n_splits * rows_all * p.D + (size_t)a.n_splits * rows_all) * 4,
-                            stream) != cudaSuccess)
+    const size_t need = ((size_t)a.n_splits * rows_all * p.D + (size_t)a.n_splits * rows_all) * 4;
+    if (fixed_ws) {
+      if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;  // (nothing enqueued yet)
+      pws = fixed_ws;
+    } else if (host::scratch_alloc(&pws, need, stream) != cudaSuccess) {
       return FA_ERR_CUDA;
+    }
     a.O = pws;
     a.LSE = static_cast<float*>(pws) + (size_t)a.n_splits * rows_all * p.D;
   } else {
@@ -1325,16 +1331,16 @@ fa_status run_decode(const void* Q, const void* K, const void* V, void* O, float
                             op + (size_t)a.n_splits * rows_all * p.D, O, LSE, a.n_splits, (int)rows_all,
                             p.D, (int)(p.out_dtype == FA_BF16));
   }
-  const cudaError_t e2 = host::scratch_free(pws, stream);
+  const cudaError_t e2 = fixed_ws ? cudaSuccess : host::scratch_free(pws, stream);
   return (e == cudaSuccess && e2 == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
 }
 
 template <int DK, bool F32IN>
 fa_status run_decode_rows(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                          const fa_params& p, cudaStream_t stream) {
+                          const fa_params& p, cudaStream_t stream, void* fixed_ws = nullptr) {
   const int rows = p.H / p.HKV * p.Sq;
-  if (rows <= 4) return run_decode<DK, 4, F32IN>(Q, K, V, O, LSE, p, stream);
-  return run_decode<DK, DEC_ROWS, F32IN>(Q, K, V, O, LSE, p, stream);
+  if (rows <= 4) return run_decode<DK, 4, F32IN>(Q, K, V, O, LSE, p, stream, fixed_ws);
+  return run_decode<DK, DEC_ROWS, F32IN>(Q, K, V, O, LSE, p, stream, fixed_ws);
 }
 
 }  // namespace
@@ -1602,6 +1608,16 @@ fa_status launch_fwd_noalloc(const void* Q, const void* K, const void* V, void* 
     fill_empty_kernel<<<4 * host::sm_count(), 256, 0, stream>>>(O, LSE, rows, p.D,
                                                                 p.out_dtype == FA_BF16);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+  if (decode_shaped(p)) {  // fa_fwd's decode kernel, its partial results in the array
+    void* ws = nullptr;
+    const fa_status st = noalloc_scratch_addr(&ws);
+    if (st != FA_OK) return st;
+    const bool f32 = p.in_dtype != FA_BF16;
+    if (p.D <= 64) return f32 ? run_decode_rows<64, true>(Q, K, V, O, LSE, p, stream, ws)
+                              : run_decode_rows<64, false>(Q, K, V, O, LSE, p, stream, ws);
+    return f32 ? run_decode_rows<128, true>(Q, K, V, O, LSE, p, stream, ws)
+               : run_decode_rows<128, false>(Q, K, V, O, LSE, p, stream, ws);
   }
   if (p.in_dtype == FA_BF16) {
     if (p.D <= 64) return run_fwd_noalloc<64, IN_BF16>(Q, K, V, O, LSE, p, stream);

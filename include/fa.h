@@ -141,14 +141,17 @@ FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, fl
  * (real-time or safety-certified inference), hosts whose own allocator owns the
  * whole device and would be starved or fragmented by a second pool, and code
  * that runs where a cudaMalloc is not allowed or would block on a lock. For them
- * this entry point computes what fa_fwd computes, with the same arguments, rules
- * and errors (at decode shapes through the tensor-core kernels, so there its outputs
- * may differ from fa_fwd's by rounding, within the same bounds), but its scratch
- * (the fp16 copy of V for bf16 inputs; the hi/lo splits of Q, K, V for fp32 inputs)
- * lives in a file-scope device array of FA_NOALLOC_SCRATCH_BYTES inside libfa.so. Every GPU
- * on which the library is loaded holds that array until the process exits.
+ * this entry point computes exactly what fa_fwd computes, with the same arguments,
+ * rules and errors, but its scratch (the fp16 copy of V for bf16 inputs; the hi/lo
+ * splits of Q, K, V for fp32 inputs; at decode shapes the decode kernel's partial
+ * results) lives in a file-scope device array of FA_NOALLOC_SCRATCH_BYTES inside
+ * libfa.so. Every GPU on which the library is loaded holds that array until the
+ * process exits.
  *   - A problem whose scratch would not fit returns FA_ERR_SCRATCH_LIMIT before
- *     anything is enqueued: bf16 inputs need round_up(B*HKV*Sk*D*2, 256) + 256 +
+ *     anything is enqueued. Decode shapes ((H / HKV) * Sq <= 8) need 4*(D+1)*B*H*Sq*n
+ *     bytes for n key ranges (n = 1, no scratch, once B*HKV reaches twice the SM
+ *     count; at most about 3 MB). Other shapes: bf16 inputs need
+ *     round_up(B*HKV*Sk*D*2, 256) + 256 +
  *     32 * (the device's SM count) bytes (the fp16 copy of V, its scale factors and
  *     the conversion's partial maxima); fp32 inputs need
  *     2*(2*B*H*Sq*D + 4*B*HKV*Sk*D) + 256 + 96 * (SM count) bytes with

@@ -85,16 +85,35 @@ def test_noalloc_matches_oracle_and_fa_fwd_on_two_calls_in_a_row(fa, kind):
 
 
 def test_noalloc_refuses_problems_larger_than_its_scratch(fa):
-    # bf16 inputs need B*HKV*Sk*D*2 bytes of scratch: Sk = 2^17 + 1 keys at D = 128 is
-    # just over the 32 MiB array. The tensors are real, so even a wrong answer here
-    # would stay inside allocated memory.
+    # bf16 inputs on the tensor-core path need B*HKV*Sk*D*2 bytes of scratch: Sk = 2^17
+    # + 1 keys at D = 128 is just over the 32 MiB array. (9 query rows: above the decode
+    # shapes, whose kernel needs only its small partial results.) The tensors are real,
+    # so even a wrong answer here would stay inside allocated memory.
     sk = (fa.noalloc_scratch_bytes() // (128 * 2)) + 1
-    q = torch.zeros(1, 1, 1, 128, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(1, 1, 9, 128, dtype=torch.bfloat16, device="cuda")
     k = torch.zeros(1, 1, sk, 128, dtype=torch.bfloat16, device="cuda")
     p = fa.make_params(q, k, 0.1, False, 0)
-    o = torch.empty(1, 1, 1, 128, dtype=torch.float32, device="cuda")
-    lse = torch.empty(1, 1, 1, dtype=torch.float32, device="cuda")
+    o = torch.empty(1, 1, 9, 128, dtype=torch.float32, device="cuda")
+    lse = torch.empty(1, 1, 9, dtype=torch.float32, device="cuda")
     rc = fa.fa_fwd_noalloc(q.data_ptr(), k.data_ptr(), k.data_ptr(), o.data_ptr(), lse.data_ptr(),
                            p, int(torch.cuda.current_stream().cuda_stream))
     assert rc == FA_ERR_SCRATCH_LIMIT
     assert "static scratch" in fa.status_string(rc)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_noalloc_decode_shapes_match_fa_fwd_bit_for_bit(fa, dtype):
+    # decode shapes (at most 8 query rows per kv head) run fa_fwd's decode kernel, with
+    # its key-range partial results in the array: the same outputs, bit for bit, and
+    # within the parity bounds of the oracle
+    base = WORKLOADS["c3"] if dtype == "bf16" else WORKLOADS["c5"]
+    w = base.with_(B=2, H=8, HKV=2, Sq=2, Sk=7000, causal=False, window=0, seed=37)
+    c = make_inputs(w)[:3]
+    t = tuple(x.cuda() for x in c)
+    got = _call(fa, fa.fa_fwd_noalloc, w, t)
+    ref = _call(fa, fa.fa_fwd, w, t)
+    fa.check_device_status()
+    assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
+    xo, xl = oracle.attention_fwd(*c, w.scale, w.causal, w.window)
+    assert rms_err(to_np(got[0]), xo) <= TOL[w.dtype]["O"]
+    assert lse_err(to_np(got[1]), xl) <= TOL[w.dtype]["LSE"]
